@@ -1,0 +1,151 @@
+/*
+ * kime_attn.h -- C ABI of libkime_attn: packed variable-length multi-head
+ * attention (head_dim 64) over a fused qkv row buffer, with RoPE applied to q
+ * and k on load, for one NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the semantics (docs.rs pages):
+ *   kime-cpu 0.0.17, src/kime_cpu/plan.rs   -- Step::Rope, Step::Attention, CpuPlan::run
+ *   kime-cuda 0.0.3, src/plan.rs            -- Op::Attention lowering, fn rope_tables
+ *   ffai-argus 0.7.3, src/text.rs           -- CausalSoftmax, KvAppend, TextTower::block
+ *
+ * Conventions shared by every entry point:
+ *  - All tensors are caller-owned and row-major.  Device pointers must be
+ *    16-byte aligned.  The library allocates nothing and never synchronises;
+ *    all work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) on the current device.
+ *  - A host-detectable error returns KIME_EINVAL or KIME_ERANGE and enqueues
+ *    nothing.  A failed launch returns KIME_ECUDA.
+ *  - Errors found on the device (malformed cu_seqlens, an out-of-range
+ *    position, a timed-out wait) OR a KIME_DEV_* bit into *dev_status when
+ *    dev_status is non-NULL (device int32, never cleared by the library) and
+ *    skip the offending sequence; they never trap.
+ *  - head_dim must be 64.  qkv rows are [q heads | k heads | v heads], 64
+ *    columns per head, width W = 64*(heads + 2*kv_heads).  q head h reads kv
+ *    head h / (heads / kv_heads) (grouped-query attention, ffai-argus
+ *    TextTower::block GQA fold).
+ *  - RoPE is rotate-half: element t pairs with t+32,
+ *      y[t]    = x[t]*cos[p][t]    - x[t+32]*sin[p][t]
+ *      y[t+32] = x[t+32]*cos[p][t] + x[t]*sin[p][t],
+ *    at the token's position p inside its own sequence (kime-cpu Step::Rope:
+ *    the row index minus the start of its sequence).  Tables are float32
+ *    [rope_len, 32] device arrays, e.g. from kime_rope_tables().
+ */
+#ifndef KIME_ATTN_H
+#define KIME_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KIME_OK = 0,
+  KIME_EINVAL = -1,  /* malformed argument (null pointer, head_dim != 64, heads % kv_heads, ...) */
+  KIME_ERANGE = -2,  /* a size out of range (workspace too small, max_seqlen > rope_len, ...) */
+  KIME_ECUDA = -3,   /* a CUDA call failed; see kime_attn_last_cuda_error() */
+  KIME_ETIMEOUT = -4 /* reserved for callers mapping KIME_DEV_TIMEOUT to a status */
+} kime_status;
+
+typedef enum { KIME_F32 = 0, KIME_BF16 = 1 } kime_dtype;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define KIME_DEV_BAD_CU 1       /* cu_seqlens not monotone, outside [0,total], cu[0]!=0 or cu[n]!=total */
+#define KIME_DEV_SEQ_TOO_LONG 2 /* a sequence longer than max_seqlen: it is skipped */
+#define KIME_DEV_BAD_POS 4      /* a decode/append position outside [0, min(cap, rope_len)): skipped */
+#define KIME_DEV_TIMEOUT 8      /* a pipeline wait ran past its time limit; the work item is abandoned */
+
+/* kime_attn_varlen -- attention over a packed batch of variable-length
+ * sequences (kime-cuda Op::Attention / kime-cpu Step::Attention, with the RoPE
+ * step fused into the load).
+ *
+ * For sequence s with rows cu_seqlens[s] .. cu_seqlens[s+1]-1 (length L), head
+ * h, local query i:
+ *   out[cu[s]+i, 64h:64h+64] = sum_{j in A(i)} softmax_j(scale * <rope(q_i,i), rope(k_j,j)>) v_j
+ * with A(i) = { j < L : (!causal || j <= i) && (window < 0 || |i-j| <= window) }.
+ * window = -1 means none (kime-cuda encodes window None as -1); causal with
+ * offset 0 is ffai-argus CausalSoftmax.  Masked keys are skipped, never
+ * materialised.
+ *
+ *  qkv          device, [total_tokens, W], dtype (KIME_F32 or KIME_BF16)
+ *  cu_seqlens   device int32 [n_seqs+1], cu[0]=0, non-decreasing, cu[n]=total_tokens
+ *  max_seqlen   host upper bound on every sequence length; must be <= rope_len
+ *  window       -1 or >= 0; causal 0/1; scale > 0 (0.125, or 1 if q is pre-scaled)
+ *  rope_cos/sin device float32 [rope_len, 32]
+ *  out          device, [total_tokens, heads*64], same dtype as qkv; rows of
+ *               skipped sequences are left untouched
+ *  workspace    device scratch of kime_attn_workspace_bytes(0, ...) bytes;
+ *               contents need no initialisation; calls that share it must be
+ *               ordered on one stream
+ * BF16 runs on the tensor cores (tcgen05, FP32 accumulate); FP32 runs on FP32
+ * FMA.  Two launches: the device scheduler, then the attention kernel. */
+int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int n_seqs, int total_tokens,
+                     int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal, float scale,
+                     const float* rope_cos, const float* rope_sin, int rope_len, void* out, void* workspace,
+                     size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* kime_kv_append -- in-place KV-cache append of one new token per sequence
+ * (ffai-argus KvAppend: rows written at pos, pos checked against cap before
+ * any write).
+ *
+ *  qkv_new      device bf16 [n_seqs, W]: the new token's fused row per sequence
+ *  pos          device int32 [n_seqs]: positions already used = the row written
+ *  k_cache/v_cache  device bf16 [n_seqs, kv_heads, cap, 64]
+ * Writes k_cache[s,g,pos[s]] = bf16(rope(k, pos[s])) (float32 rotation, one
+ * rounding per operation, then round to nearest even) and v_cache[s,g,pos[s]] =
+ * v.  Nothing else is written.  pos is not advanced (the caller does that).
+ * pos[s] outside [0, min(cap, rope_len)) sets KIME_DEV_BAD_POS and skips s. */
+int kime_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
+                   int cap, const float* rope_cos, const float* rope_sin, int rope_len, void* k_cache, void* v_cache,
+                   int32_t* dev_status, void* stream);
+
+/* kime_attn_decode -- single-token attention against the KV cache
+ * (ffai-argus CausalSoftmax with q_len 1 and offset k_len-1: the new token
+ * attends to the entire cache, rows 0..=pos[s], its own appended row included;
+ * call kime_kv_append first).
+ *
+ *  qkv_new, pos, caches as for kime_kv_append (caches are read only)
+ *  out          device bf16 [n_seqs, heads*64]
+ *  workspace    device scratch of kime_attn_workspace_bytes(1, ...) bytes
+ * Split-KV over chunks of 256 keys with a merge by the last chunk to finish;
+ * heads/kv_heads must be 1..8.  One memset of the per-(sequence, kv head)
+ * tickets and one kernel launch. */
+int kime_attn_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
+                     int cap, float scale, const float* rope_cos, const float* rope_sin, int rope_len,
+                     const void* k_cache, const void* v_cache, void* out, void* workspace, size_t workspace_bytes,
+                     int32_t* dev_status, void* stream);
+
+/* Scratch bytes for op 0 (varlen: uses n_seqs, total_tokens) or op 1 (decode:
+ * uses n_seqs, heads, kv_heads, cap).  Returns 0 for an unknown op or
+ * malformed sizes. */
+size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads, int kv_heads, int cap);
+
+/* Host helper: float32 cos/sin tables [len, 32] for heads of 64 by kime-cuda's
+ * fn rope_tables: inv_i = 1/(float)(theta^(float)(2i/64)) in float32, angle =
+ * (float)p * inv_i in float32, cos and sin taken in double and narrowed.
+ * cos_out / sin_out are HOST arrays of len*32 floats.  Returns KIME_EINVAL for
+ * theta <= 0, len < 0 or null outputs. */
+int kime_rope_tables(double theta, int len, float* cos_out, float* sin_out);
+
+/* Test aid: run only the device scheduler of kime_attn_varlen and copy its
+ * work list out.  tiles_out (device int32 [max_pairs, 8]) receives, per
+ * (sequence, 128-row query tile) pair, {s, qt, kt_begin, kt_end, full_begin,
+ * full_end, row0, L}: key tiles [kt_begin, kt_end) are visited and
+ * [full_begin, full_end) need no per-key mask.  *n_pairs_out (device int32)
+ * receives the count.  max_pairs must be >= total_tokens/128 + n_seqs + 1. */
+int kime_attn_debug_tiles(const int32_t* cu_seqlens, int n_seqs, int total_tokens, int max_seqlen, int window,
+                          int causal, void* workspace, size_t workspace_bytes, int32_t* tiles_out, int max_pairs,
+                          int32_t* n_pairs_out, int32_t* dev_status, void* stream);
+
+/* The cudaError_t of the last failing CUDA call in this thread (0 if none). */
+int kime_attn_last_cuda_error(void);
+
+/* A static string naming a kime_status value. */
+const char* kime_attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KIME_ATTN_H */

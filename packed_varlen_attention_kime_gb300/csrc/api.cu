@@ -1,0 +1,198 @@
+// api.cu -- the C ABI of libkime_attn (declared in include/kime_attn.h):
+// argument checks, workspace carving, TMA tensor-map encoding and launches.
+// No allocation and no synchronisation happen here.
+#include <math.h>
+#include <string.h>
+
+#include "../../include/kime_attn.h"
+#include "kime_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return KIME_OK;
+  g_last_cuda_error = static_cast<int>(e);
+  return KIME_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D map over the bf16 qkv buffer [total, W]: boxes of 128 rows x 64 columns
+// (one head of 128 tokens), 128-byte swizzle, rows past `total` read as zero.
+int encode_qkv_map(CUtensorMap* map, const void* qkv, int total, int W) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return KIME_ECUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(total)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(W) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kime::kHead), static_cast<cuuint32_t>(kime::kBM)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qkv), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_cuda_error = static_cast<int>(r);
+    return KIME_ECUDA;
+  }
+  return KIME_OK;
+}
+
+size_t varlen_ws_bytes(int n_seqs, int total) {
+  return sizeof(kime::WsHeader) + static_cast<size_t>(kime::max_pairs_for(n_seqs, total)) * sizeof(kime::Pair);
+}
+
+bool heads_ok(int heads, int kv_heads, int head_dim) {
+  return head_dim == kime::kHead && heads > 0 && kv_heads > 0 && heads % kv_heads == 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads, int kv_heads, int cap) {
+  if (n_seqs < 0) return 0;
+  if (op == 0) {
+    if (total_tokens < 0) return 0;
+    return varlen_ws_bytes(n_seqs, total_tokens);
+  }
+  if (op == 1) {
+    if (!heads_ok(heads, kv_heads, kime::kHead) || cap <= 0) return 0;
+    return kime::decode_workspace_bytes(n_seqs, heads, kv_heads, cap);
+  }
+  return 0;
+}
+
+int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int n_seqs, int total_tokens,
+                     int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal, float scale,
+                     const float* rope_cos, const float* rope_sin, int rope_len, void* out, void* workspace,
+                     size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (dtype != KIME_F32 && dtype != KIME_BF16) return KIME_EINVAL;
+  if (!heads_ok(heads, kv_heads, head_dim)) return KIME_EINVAL;
+  if (n_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || rope_len < 0 || window < -1) return KIME_EINVAL;
+  if (!(scale > 0.f) || !isfinite(scale)) return KIME_EINVAL;
+  if (causal != 0 && causal != 1) return KIME_EINVAL;
+  if (n_seqs == 0 || total_tokens == 0) return KIME_OK;
+  if (!qkv || !cu_seqlens || !rope_cos || !rope_sin || !out || !workspace) return KIME_EINVAL;
+  if (!aligned16(qkv) || !aligned16(out) || !aligned16(rope_cos) || !aligned16(rope_sin) || !aligned16(workspace))
+    return KIME_EINVAL;
+  if (max_seqlen > rope_len) return KIME_ERANGE;
+  if (workspace_bytes < varlen_ws_bytes(n_seqs, total_tokens)) return KIME_ERANGE;
+  const long long W = 64LL * (heads + 2LL * kv_heads);
+  if (W > (1LL << 30) || static_cast<long long>(total_tokens) * W > (1LL << 46)) return KIME_ERANGE;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int max_pairs = kime::max_pairs_for(n_seqs, total_tokens);
+  int rc = cuda_status(
+      kime::launch_schedule(cu_seqlens, n_seqs, total_tokens, max_seqlen, causal, window, workspace, max_pairs,
+                            dev_status, st));
+  if (rc) return rc;
+  if (dtype == KIME_F32) {
+    return cuda_status(kime::launch_varlen_f32(static_cast<const float*>(qkv), cu_seqlens, n_seqs, total_tokens,
+                                               heads, kv_heads, window, causal, scale, rope_cos, rope_sin,
+                                               static_cast<float*>(out), workspace, max_pairs, dev_status, st));
+  }
+  CUtensorMap map;
+  rc = encode_qkv_map(&map, qkv, total_tokens, static_cast<int>(W));
+  if (rc) return rc;
+  return cuda_status(kime::launch_prefill_bf16(&map, cu_seqlens, n_seqs, total_tokens, heads, kv_heads, window,
+                                               causal, scale, rope_cos, rope_sin, out, workspace, max_pairs,
+                                               dev_status, st));
+}
+
+int kime_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
+                   int cap, const float* rope_cos, const float* rope_sin, int rope_len, void* k_cache, void* v_cache,
+                   int32_t* dev_status, void* stream) {
+  if (!heads_ok(heads, kv_heads, head_dim) || n_seqs < 0 || cap <= 0 || rope_len < 0) return KIME_EINVAL;
+  if (n_seqs == 0) return KIME_OK;
+  if (!qkv_new || !pos || !rope_cos || !rope_sin || !k_cache || !v_cache) return KIME_EINVAL;
+  if (n_seqs > (1 << 30)) return KIME_ERANGE;
+  return cuda_status(kime::launch_kv_append(qkv_new, pos, n_seqs, heads, kv_heads, cap, rope_cos, rope_sin,
+                                            rope_len, k_cache, v_cache, dev_status,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int kime_attn_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
+                     int cap, float scale, const float* rope_cos, const float* rope_sin, int rope_len,
+                     const void* k_cache, const void* v_cache, void* out, void* workspace, size_t workspace_bytes,
+                     int32_t* dev_status, void* stream) {
+  if (!heads_ok(heads, kv_heads, head_dim) || n_seqs < 0 || cap <= 0 || rope_len < 0) return KIME_EINVAL;
+  if (heads / kv_heads > kime::kMaxGroup) return KIME_EINVAL;
+  if (!(scale > 0.f) || !isfinite(scale)) return KIME_EINVAL;
+  if (n_seqs == 0) return KIME_OK;
+  if (!qkv_new || !pos || !rope_cos || !rope_sin || !k_cache || !v_cache || !out || !workspace) return KIME_EINVAL;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace) || !aligned16(out)) return KIME_EINVAL;
+  if (n_seqs > 65535) return KIME_ERANGE;
+  if (workspace_bytes < kime::decode_workspace_bytes(n_seqs, heads, kv_heads, cap)) return KIME_ERANGE;
+  return cuda_status(kime::launch_decode(qkv_new, pos, n_seqs, heads, kv_heads, cap, scale, rope_cos, rope_sin,
+                                         rope_len, k_cache, v_cache, out, workspace, dev_status,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int kime_rope_tables(double theta, int len, float* cos_out, float* sin_out) {
+  if (!(theta > 0.0) || len < 0 || (len > 0 && (!cos_out || !sin_out))) return KIME_EINVAL;
+  float inv[kime::kHalf];
+  for (int i = 0; i < kime::kHalf; ++i) {
+    const float expo = static_cast<float>(2 * i) / static_cast<float>(kime::kHead);
+    inv[i] = 1.0f / static_cast<float>(pow(theta, static_cast<double>(expo)));
+  }
+  for (int p = 0; p < len; ++p) {
+    for (int i = 0; i < kime::kHalf; ++i) {
+      const double a = static_cast<double>(static_cast<float>(p) * inv[i]);
+      cos_out[static_cast<size_t>(p) * kime::kHalf + i] = static_cast<float>(cos(a));
+      sin_out[static_cast<size_t>(p) * kime::kHalf + i] = static_cast<float>(sin(a));
+    }
+  }
+  return KIME_OK;
+}
+
+int kime_attn_debug_tiles(const int32_t* cu_seqlens, int n_seqs, int total_tokens, int max_seqlen, int window,
+                          int causal, void* workspace, size_t workspace_bytes, int32_t* tiles_out, int max_pairs,
+                          int32_t* n_pairs_out, int32_t* dev_status, void* stream) {
+  if (n_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || window < -1) return KIME_EINVAL;
+  if (!cu_seqlens || !workspace || !tiles_out || !n_pairs_out) return KIME_EINVAL;
+  const int need = kime::max_pairs_for(n_seqs, total_tokens);
+  if (max_pairs < need || workspace_bytes < varlen_ws_bytes(n_seqs, total_tokens)) return KIME_ERANGE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = cuda_status(kime::launch_schedule(cu_seqlens, n_seqs, total_tokens, max_seqlen, causal ? 1 : 0, window,
+                                             workspace, need, dev_status, st));
+  if (rc) return rc;
+  const char* ws = static_cast<const char*>(workspace);
+  rc = cuda_status(cudaMemcpyAsync(n_pairs_out, ws + offsetof(kime::WsHeader, n_pairs), 4,
+                                   cudaMemcpyDeviceToDevice, st));
+  if (rc) return rc;
+  return cuda_status(cudaMemcpyAsync(tiles_out, ws + sizeof(kime::WsHeader), static_cast<size_t>(need) * 32,
+                                     cudaMemcpyDeviceToDevice, st));
+}
+
+int kime_attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* kime_attn_status_string(int status) {
+  switch (status) {
+    case KIME_OK: return "ok";
+    case KIME_EINVAL: return "invalid argument";
+    case KIME_ERANGE: return "size out of range";
+    case KIME_ECUDA: return "CUDA error";
+    case KIME_ETIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// kime_internal.h -- host-visible internals shared by the translation units of
+// libkime_attn (workspace layout, launcher entry points).  Not installed.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kime {
+
+constexpr int kHead = 64;       // head_dim; the library supports exactly this
+constexpr int kHalf = 32;       // RoPE pairs per head
+constexpr int kBM = 128;        // query rows per tile
+constexpr int kBN = 128;        // keys per tile
+constexpr int kDecChunk = 256;  // keys per split-KV decode work item
+constexpr int kMaxGroup = 8;    // largest heads/kv_heads the decode path takes
+
+// One (sequence, query tile) of the schedule with its key-tile ranges:
+// tiles [kt_begin, kt_end) are visited; [full_begin, full_end) among them need
+// no per-column test.  row0 = cu_seqlens[s], L = sequence length.
+struct Pair {
+  int32_t s, qt, kt_begin, kt_end, full_begin, full_end, row0, L;
+};
+static_assert(sizeof(Pair) == 32, "Pair is 32 bytes");
+
+// Head of the prefill workspace.  next_unit is the persistent kernels' work
+// counter; a unit is (pair, head) = (u / heads, u % heads).
+struct WsHeader {
+  int32_t next_unit;
+  int32_t n_pairs;
+  int32_t pad[14];
+};
+static_assert(sizeof(WsHeader) == 64, "WsHeader is 64 bytes");
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int max_pairs_for(int n_seqs, int total_tokens) { return total_tokens / kBM + n_seqs + 1; }
+inline int dec_chunks_for(int cap) { return (cap + kDecChunk - 1) / kDecChunk; }
+
+size_t decode_workspace_bytes(int n_seqs, int heads, int kv_heads, int cap);
+
+// Launchers (each returns a cudaError_t of the launch).
+cudaError_t launch_schedule(const int32_t* cu, int n_seqs, int total, int max_seqlen, int causal, int window,
+                            void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
+cudaError_t launch_varlen_f32(const float* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
+                              int window, int causal, float scale, const float* cos_t, const float* sin_t,
+                              float* out, void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
+cudaError_t launch_prefill_bf16(const CUtensorMap* qkv_map, const int32_t* cu, int n_seqs, int total, int heads,
+                                int kv_heads, int window, int causal, float scale, const float* cos_t,
+                                const float* sin_t, void* out, void* ws, int max_pairs, int32_t* dev_status,
+                                cudaStream_t st);
+cudaError_t launch_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int cap,
+                             const float* cos_t, const float* sin_t, int rope_len, void* k_cache, void* v_cache,
+                             int32_t* dev_status, cudaStream_t st);
+cudaError_t launch_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int cap,
+                          float scale, const float* cos_t, const float* sin_t, int rope_len, const void* k_cache,
+                          const void* v_cache, void* out, void* ws, int32_t* dev_status, cudaStream_t st);
+
+}  // namespace kime
