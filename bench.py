@@ -1,0 +1,441 @@
+"""Benchmark of the packed-varlen attention hot path on GB300.
+
+One step = the attention of one ModernBERT-base-shaped encoder layer pair over
+one packed batch (64 sequences, lengths U[32,512], 12 heads x 64, BF16 qkv
+N(0, 1.5^2)): the local layer (window 64, RoPE theta 1e4) then the global
+layer (full, theta 1.6e5), each one kime_attn_varlen call (device scheduler +
+tcgen05 attention kernel).  Inputs are resident in HBM before the timed region
+and L2 is flushed (a 512 MB write) before every timed step.
+
+The same run also times, outside the headline number: ModernBERT-large-shaped
+layers (8 x U[1024,8192]), SmolLM2-shaped causal GQA prefill (16 x 1142) and
+the SmolLM2-shaped decode step (KV append + split-KV decode, 128 sequences,
+cache 8192) -- the "extra" object -- and the FP64 CPU oracle on a bounded
+sample of the headline workload (cpu_baseline).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extra]
+
+Under torchrun every rank runs the same workload on its own GPU with no
+exchange between ranks (weak scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("packed-varlen attention tokens/s & TFLOP/s (% BF16 peak); decode GB/s (% HBM) at 1 GB300")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---- helpers ---------------------------------------------------------------------
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        out = {}
+        for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            v = d.get(k)
+            if isinstance(v, dict):
+                v = v.get("value")
+            if v is not None:
+                out[k] = float(v)
+        if "hbm_gbs" in out and "bf16_tflops" in out:
+            return out, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def visible_pairs(lengths, window, causal):
+    """Exact number of (query, key) pairs attended, summed over sequences."""
+    tot = 0
+    for L in lengths:
+        i = np.arange(L)
+        if window < 0:
+            hi = i if causal else np.full(L, L - 1)
+            lo = np.zeros(L, np.int64)
+        else:
+            hi = np.minimum(i if causal else i + window, L - 1)
+            lo = np.maximum(i - window, 0)
+        tot += int((hi - lo + 1).sum())
+    return tot
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.text = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.text, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.text, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(getattr(self, "text", ""))) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if "Active" in v and "Not" not in v})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def l2_flush_buffer(dev):
+    return torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+
+# ---- workloads on the GPU ------------------------------------------------------------
+
+class VarlenRun:
+    """Device-resident inputs, tables, outputs and workspace for one varlen workload."""
+
+    def __init__(self, name, dev, seed_offset=0):
+        import packed_varlen_attention_kime_gb300 as kime
+        from packed_varlen_attention_kime_gb300.inputs import varlen_case
+        self.kime = kime
+        self.case = varlen_case(name, device=str(dev))
+        c = self.case
+        self.dev = dev
+        self.cu = c.cu_seqlens.to(dev)
+        self.tables = {}
+        for lay in c.layers:
+            if lay.theta not in self.tables:
+                cs, sn = kime.kime_rope_tables(lay.theta, c.max_seqlen)
+                self.tables[lay.theta] = (cs.to(dev), sn.to(dev))
+        self.outs = [torch.empty((c.total, c.heads * 64), dtype=c.qkv.dtype, device=dev) for _ in c.layers]
+        self.ws = torch.empty(kime.kime_attn_workspace_bytes(0, len(c.lengths), c.total), dtype=torch.uint8,
+                              device=dev)
+        self.flops = [4 * 64 * c.heads * visible_pairs(c.lengths, l.window, l.causal) for l in c.layers]
+        W = c.qkv.shape[1]
+        self.bytes_per_layer = c.total * W * 2 + c.total * c.heads * 64 * 2  # qkv read + out written
+
+    def layer(self, k, qkv=None, out=None):
+        c, lay = self.case, self.case.layers[k]
+        cs, sn = self.tables[lay.theta]
+        self.kime.kime_attn_varlen(self.case.qkv if qkv is None else qkv, self.cu, c.max_seqlen, c.heads,
+                                   c.kv_heads, lay.window, lay.causal, lay.scale, cs, sn,
+                                   out=self.outs[k] if out is None else out, workspace=self.ws)
+
+
+class DecodeRun:
+    def __init__(self, dev):
+        import packed_varlen_attention_kime_gb300 as kime
+        from packed_varlen_attention_kime_gb300.inputs import decode_case
+        self.kime = kime
+        c = self.case = decode_case(device=str(dev))
+        self.dev = dev
+        self.pos = c.pos.to(dev)
+        cs, sn = kime.kime_rope_tables(c.theta, c.cap)
+        self.cs, self.sn = cs.to(dev), sn.to(dev)
+        self.out = torch.empty((len(c.pos), c.heads * 64), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(kime.kime_attn_workspace_bytes(1, len(c.pos), 0, c.heads, c.kv_heads, c.cap),
+                              dtype=torch.uint8, device=dev)
+        keys = (c.pos.long() + 1).sum().item()
+        # K and V prefixes read + new rows read + appended rows written + out written
+        W = c.qkv_new.shape[1]
+        self.bytes = int(keys * c.kv_heads * 64 * 2 * 2 + len(c.pos) * (W * 2 + c.kv_heads * 2 * 128 +
+                                                                        c.heads * 64 * 2))
+        self.flops = int(4 * 64 * c.heads * keys)
+
+    def step(self):
+        c = self.case
+        self.kime.kime_kv_append(c.qkv_new, self.pos, c.heads, c.kv_heads, c.k_cache, c.v_cache, self.cs, self.sn)
+        self.kime.kime_attn_decode(c.qkv_new, self.pos, c.heads, c.kv_heads, c.k_cache, c.v_cache, c.scale,
+                                   self.cs, self.sn, out=self.out, workspace=self.ws)
+
+
+def time_fn(fn, n, warmup, flush, stream, events=1):
+    """Median and mean ms of fn over n calls, L2 flushed before each; fn gets
+    the list of events to record its sub-steps (len events+1)."""
+    for _ in range(warmup):
+        fn(None)
+    torch.cuda.synchronize()
+    per = []
+    subs = []
+    for _ in range(n):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(events + 1)]
+        ev[0].record(stream)
+        fn(ev)
+        ev[-1].record(stream)
+        torch.cuda.synchronize()
+        per.append(ev[0].elapsed_time(ev[-1]))
+        subs.append([ev[i].elapsed_time(ev[i + 1]) for i in range(events)])
+    return per, subs
+
+
+def extra_measurements(dev, flush, stream, pk, reps=10):
+    out = {}
+    for name in ("modernbert_large", "smollm2_prefill"):
+        r = VarlenRun(name, dev)
+        nl = len(r.case.layers)
+
+        def f(ev, r=r, nl=nl):
+            for k in range(nl):
+                r.layer(k)
+                if ev is not None and k + 1 < nl:
+                    ev[k + 1].record(stream)
+        per, subs = time_fn(f, reps, 3, flush, stream, events=nl)
+        layers = {}
+        for k, lay in enumerate(r.case.layers):
+            ms = statistics.median([s[k] for s in subs])
+            tf = r.flops[k] / (ms * 1e-3) / 1e12
+            gbs = r.bytes_per_layer / (ms * 1e-3) / 1e9
+            layers[lay.name] = {"ms": round(ms, 4), "tflops": round(tf, 2), "gbs": round(gbs, 1),
+                                "tc_frac": round(tf / pk["bf16_tflops"], 4), "hbm_frac": round(gbs / pk["hbm_gbs"], 4),
+                                "roof_frac": round(max(r.flops[k] / (pk["bf16_tflops"] * 1e12),
+                                                       r.bytes_per_layer / (pk["hbm_gbs"] * 1e9)) / (ms * 1e-3), 4)}
+        out[name] = {"tokens": r.case.total, "tokens_per_s": round(r.case.total / (statistics.median(per) * 1e-3)),
+                     "layers": layers}
+        del r
+        torch.cuda.empty_cache()
+    d = DecodeRun(dev)
+    per, _ = time_fn(lambda ev: d.step(), reps, 3, flush, stream)
+    ms = statistics.median(per)
+    gbs = d.bytes / (ms * 1e-3) / 1e9
+    out["smollm2_decode"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm_gbs"], 4),
+                             "tokens_per_s": round(len(d.case.pos) / (ms * 1e-3)), "bytes": d.bytes}
+    del d
+    torch.cuda.empty_cache()
+    return out
+
+
+# ---- CPU oracle leg ----------------------------------------------------------------
+
+def oracle_sample_rate(case, budget_s=15.0):
+    """Oracle throughput (tokens/s over the layer pair) on whole sequences of the
+    workload, taken in order until about budget_s of CPU work is done."""
+    import oracle
+    from packed_varlen_attention_kime_gb300.inputs import bf16_bits, cu_from_lengths
+    oracle.build()
+    x = bf16_bits(case.qkv)
+    tabs = {}
+    for lay in case.layers:
+        c, s = oracle.rope_tables_f32(lay.theta, case.max_seqlen)
+        tabs[lay.theta] = (c.astype(np.float64), s.astype(np.float64))
+    cores = os.cpu_count() or 1
+    tokens, spent, nseq = 0, 0.0, 0
+    cu = case.cu_seqlens.numpy()
+    while nseq < len(case.lengths) and spent < budget_s:
+        a, b = int(cu[nseq]), int(cu[nseq + 1])
+        sub_cu = cu_from_lengths([b - a]).numpy()
+        t0 = time.perf_counter()
+        for lay in case.layers:
+            c, s = tabs[lay.theta]
+            oracle.attn_varlen(x[a:b], sub_cu, case.heads, case.kv_heads, lay.window, lay.causal, lay.scale, c, s,
+                               nthreads=cores)
+        spent += time.perf_counter() - t0
+        tokens += b - a
+        nseq += 1
+    return tokens / spent, cores, f"first {nseq} of {len(case.lengths)} sequences ({tokens} tokens), both layers"
+
+
+# ---- main ----------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    from __graft_entry__ import build
+    build()
+    pk, pk_src = peaks()
+    stream = torch.cuda.current_stream(dev)
+    flush = l2_flush_buffer(dev)
+    run = VarlenRun("modernbert_base", dev)
+    c = run.case
+
+    def step(ev):
+        run.layer(0)
+        if ev is not None:
+            ev[1].record(stream)
+        run.layer(1)
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        per, subs = time_fn(step, args.steps, args.warmup, flush, stream, events=2)
+    clocks = clk.summary()
+    total_ms = sum(per)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * c.total * args.steps / (total_ms * 1e-3)
+
+    # roofline of the dominant call (the global layer: scheduler + attention kernel)
+    g_ms = statistics.mean(s[1] for s in subs)
+    l_ms = statistics.mean(s[0] for s in subs)
+    g_bytes = run.bytes_per_layer
+    achieved = g_bytes / (g_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": None,
+            "kernel": "kime_attn_varlen global layer (schedule + prefill_bf16_kernel)",
+            "algorithmic_bytes": g_bytes, "avg_ms": round(g_ms, 5), "peak_source": pk_src}
+    flops_step = sum(run.flops)
+    tflops = flops_step / (ms_step * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host qkv -> device, both layers,
+    # both outputs -> pinned host, every step.
+    h_qkv = c.qkv.cpu().pin_memory()
+    h_cu = c.cu_seqlens.pin_memory()
+    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in run.outs]
+    d_qkv = torch.empty_like(c.qkv)
+
+    def e2e_step(ev):
+        d_qkv.copy_(h_qkv, non_blocking=True)
+        run.cu.copy_(h_cu, non_blocking=True)
+        run.layer(0, qkv=d_qkv)
+        run.layer(1, qkv=d_qkv)
+        for h, o in zip(h_out, run.outs):
+            h.copy_(o, non_blocking=True)
+    e_per, _ = time_fn(e2e_step, max(5, args.steps // 5), 3, flush, stream)
+    e_ms = statistics.mean(e_per)
+    e2e = {"value": round(world * c.total / (e_ms * 1e-3)), "unit": "tokens/s",
+           "h2d_bytes_per_step": h_qkv.numel() * 2 + h_cu.numel() * 4,
+           "d2h_bytes_per_step": sum(o.numel() * 2 for o in run.outs), "ms_per_step": round(e_ms, 4)}
+
+    extra = {}
+    if not args.no_extra and rank == 0:
+        del h_qkv, h_out, d_qkv
+        extra = extra_measurements(dev, flush, stream, pk)
+
+    cpu = None
+    if rank == 0 and world == 1:
+        rate, cores, sample = oracle_sample_rate(VarlenRunCPU(c), args.cpu_budget)
+        cpu = {"value": round(rate, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "modernbert_base local+global layer pair", "seqs": len(c.lengths),
+                       "tokens": c.total, "heads": c.heads, "head_dim": 64,
+                       "layers": ["local window 64 theta 1e4", "global full theta 1.6e5"],
+                       "l2": "flushed (512 MB write) before every timed step", "parallelism": f"dp{world}"},
+            "useful_tflops": round(tflops, 3), "tc_frac": round(tflops / pk["bf16_tflops"], 4),
+            "layer_ms": {"local": round(l_ms, 5), "global": round(g_ms, 5)},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": 4 * args.steps, "extra": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+class VarlenRunCPU:
+    """The CPU view of a varlen case for the oracle leg."""
+
+    def __init__(self, case):
+        self.qkv = case.qkv.cpu()
+        self.cu_seqlens = case.cu_seqlens.cpu()
+        self.lengths, self.heads, self.kv_heads = case.lengths, case.heads, case.kv_heads
+        self.layers, self.max_seqlen = case.layers, case.max_seqlen
+
+
+def reference_arm(args, rank, world):
+    """The oracle, as it stands, on the host cores: each step is a bounded sample
+    of the headline workload.  Under torchrun only rank 0 runs."""
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    import oracle
+    from packed_varlen_attention_kime_gb300.inputs import bf16_bits, cu_from_lengths, varlen_case
+    oracle.build()
+    case = varlen_case("modernbert_base")
+    x = bf16_bits(case.qkv)
+    cores = os.cpu_count() or 1
+    tabs = {}
+    for lay in case.layers:
+        cs, sn = oracle.rope_tables_f32(lay.theta, case.max_seqlen)
+        tabs[lay.theta] = (cs.astype(np.float64), sn.astype(np.float64))
+    cu = case.cu_seqlens.numpy()
+    # one step: the two shortest-index sequences' worth of rows, both layers
+    a, b = int(cu[0]), int(cu[2])
+    sub_cu = cu_from_lengths(case.lengths[:2]).numpy()
+
+    def step():
+        for lay in case.layers:
+            cs, sn = tabs[lay.theta]
+            oracle.attn_varlen(x[a:b], sub_cu, case.heads, case.kv_heads, lay.window, lay.causal, lay.scale, cs,
+                               sn, nthreads=cores)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = (b - a) * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "modernbert_base local+global layer pair",
+                       "sample": f"sequences 0-1 ({b - a} tokens) of 64, both layers, per step"},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"sequences 0-1 ({b - a} tokens), both layers, per step"},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -2,6 +2,7 @@
 // argument checks, workspace carving, TMA tensor-map encoding and launches.
 // No allocation and no synchronisation happen here.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "../../include/kime_attn.h"
@@ -55,9 +56,7 @@ int encode_qkv_map(CUtensorMap* map, const void* qkv, int total, int W) {
   return KIME_OK;
 }
 
-size_t varlen_ws_bytes(int n_seqs, int total) {
-  return sizeof(kime::WsHeader) + static_cast<size_t>(kime::max_pairs_for(n_seqs, total)) * sizeof(kime::Pair);
-}
+size_t varlen_ws_bytes(int n_seqs, int total) { return kime::varlen_workspace_bytes(n_seqs, total); }
 
 bool heads_ok(int heads, int kv_heads, int head_dim) {
   return head_dim == kime::kHead && heads > 0 && kv_heads > 0 && heads % kv_heads == 0;
@@ -112,9 +111,13 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
   CUtensorMap map;
   rc = encode_qkv_map(&map, qkv, total_tokens, static_cast<int>(W));
   if (rc) return rc;
-  return cuda_status(kime::launch_prefill_bf16(&map, cu_seqlens, n_seqs, total_tokens, heads, kv_heads, window,
-                                               causal, scale, rope_cos, rope_sin, out, workspace, max_pairs,
-                                               dev_status, st));
+  static const bool v1 = getenv("KIME_PREFILL_V1") != nullptr;
+  if (v1)
+    return cuda_status(kime::launch_prefill_bf16(&map, cu_seqlens, n_seqs, total_tokens, heads, kv_heads, window,
+                                                 causal, scale, rope_cos, rope_sin, out, workspace, max_pairs,
+                                                 dev_status, st));
+  return cuda_status(kime::launch_prefill_tc(&map, n_seqs, total_tokens, heads, kv_heads, window, causal, scale,
+                                             rope_cos, rope_sin, out, workspace, max_pairs, dev_status, st));
 }
 
 int kime_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,

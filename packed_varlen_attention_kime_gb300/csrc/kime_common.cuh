@@ -27,6 +27,39 @@ __device__ __forceinline__ void report(int32_t* dev_status, int32_t bits) {
   if (dev_status) atomicOr(dev_status, bits);
 }
 
+// ---- key-tile ranges of a query tile -------------------------------------------
+// ceil(a / b) for a > 0, else 0.
+__device__ __forceinline__ int ceil_pos(int a, int b) { return a <= 0 ? 0 : (a + b - 1) / b; }
+// Number of key tiles kt >= 0 whose last key kt*128 + 127 is <= x.
+__device__ __forceinline__ int tiles_ending_by(int x) { return x < kBN - 1 ? 0 : (x - (kBN - 1)) / kBN + 1; }
+
+// Key-tile ranges of query tile qt (rows q0 = 128 qt .. q1-1, q1 = min(q0+128, L))
+// of a length-L sequence.  Tiles [kb, ke) hold at least one visible key:
+//   k0 < L; causal: k0 <= q1-1; window w: k0 <= q1-1+w and k0+127 >= q0-w.
+// Tiles [fb, fe) inside them are full -- every row sees every key:
+//   k0+128 <= L; causal: k0+127 <= q0; window: k0 >= q1-1-w and k0+127 <= q0+w.
+__device__ __forceinline__ void tile_ranges(int L, int qt, int causal, int window, int& kb, int& ke, int& fb,
+                                            int& fe) {
+  const int q0 = qt * kBM, q1 = min(q0 + kBM, L);
+  kb = 0;
+  ke = (L + kBN - 1) / kBN;
+  if (causal) ke = min(ke, (q1 - 1) / kBN + 1);
+  if (window >= 0) {
+    ke = min(ke, (q1 - 1 + window) / kBN + 1);
+    kb = max(kb, ceil_pos(q0 - window - (kBN - 1), kBN));
+  }
+  fb = 0;
+  fe = L / kBN;
+  if (causal) fe = min(fe, tiles_ending_by(q0));
+  if (window >= 0) {
+    fe = min(fe, tiles_ending_by(q0 + window));
+    fb = max(fb, ceil_pos(q1 - 1 - window, kBN));
+  }
+  fb = max(fb, kb);
+  fe = min(fe, ke);
+  if (fe <= fb) fb = fe = kb;
+}
+
 // ---- small numeric helpers ---------------------------------------------------
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

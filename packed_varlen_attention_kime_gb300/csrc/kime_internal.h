@@ -23,18 +23,40 @@ struct Pair {
 };
 static_assert(sizeof(Pair) == 32, "Pair is 32 bytes");
 
-// Head of the prefill workspace.  next_unit is the persistent kernels' work
-// counter; a unit is (pair, head) = (u / heads, u % heads).
+// Two consecutive query tiles (2*qp, 2*qp+1) of one sequence: the unit of the
+// tensor-core kernel, whose two softmax warpgroups share each K/V tile.  nt is
+// 1 when the sequence's last tile has no partner; [kb, ke) is the union of the
+// two tiles' visited key-tile ranges.
+struct Duo {
+  int32_t s, qt0, nt, kb, ke, row0, L, cost;
+};
+static_assert(sizeof(Duo) == 32, "Duo is 32 bytes");
+
+// Head of the prefill workspace.  next_unit / next_duo are the persistent
+// kernels' work counters; a unit is (entry, head) = (u / heads, u % heads).
 struct WsHeader {
   int32_t next_unit;
   int32_t n_pairs;
-  int32_t pad[14];
+  int32_t next_duo;
+  int32_t n_duos;
+  int32_t pad[12];
 };
 static_assert(sizeof(WsHeader) == 64, "WsHeader is 64 bytes");
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int max_pairs_for(int n_seqs, int total_tokens) { return total_tokens / kBM + n_seqs + 1; }
+inline int max_duos_for(int n_seqs, int total_tokens) { return total_tokens / (2 * kBM) + n_seqs + 1; }
 inline int dec_chunks_for(int cap) { return (cap + kDecChunk - 1) / kDecChunk; }
+
+// Prefill workspace: header | pairs[max_pairs] | duos[max_duos].
+inline size_t varlen_workspace_bytes(int n_seqs, int total_tokens) {
+  return sizeof(WsHeader) + static_cast<size_t>(max_pairs_for(n_seqs, total_tokens)) * sizeof(Pair) +
+         static_cast<size_t>(max_duos_for(n_seqs, total_tokens)) * sizeof(Duo);
+}
+inline Pair* ws_pairs(void* ws) { return reinterpret_cast<Pair*>(static_cast<char*>(ws) + sizeof(WsHeader)); }
+inline Duo* ws_duos(void* ws, int max_pairs) {
+  return reinterpret_cast<Duo*>(static_cast<char*>(ws) + sizeof(WsHeader) + static_cast<size_t>(max_pairs) * sizeof(Pair));
+}
 
 size_t decode_workspace_bytes(int n_seqs, int heads, int kv_heads, int cap);
 
@@ -48,6 +70,9 @@ cudaError_t launch_prefill_bf16(const CUtensorMap* qkv_map, const int32_t* cu, i
                                 int kv_heads, int window, int causal, float scale, const float* cos_t,
                                 const float* sin_t, void* out, void* ws, int max_pairs, int32_t* dev_status,
                                 cudaStream_t st);
+cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, int n_seqs, int total, int heads, int kv_heads,
+                              int window, int causal, float scale, const float* cos_t, const float* sin_t, void* out,
+                              void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int cap,
                              const float* cos_t, const float* sin_t, int rope_len, void* k_cache, void* v_cache,
                              int32_t* dev_status, cudaStream_t st);

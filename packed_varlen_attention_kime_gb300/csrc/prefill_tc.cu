@@ -1,0 +1,485 @@
+// prefill_tc.cu -- packed variable-length attention over a BF16 fused qkv
+// buffer on the sm_103a tensor cores: warp-specialised, two query tiles per
+// CTA sharing every K/V tile, ping-pong between two softmax warpgroups.
+//
+// Semantics (per sequence s, head h, local query i of a length-L sequence):
+// out = softmax over visible keys j of scale * <rope(q_i, i), rope(k_j, j)>,
+// times v_j.  q is head h of the row; k, v are kv head h / (heads/kv_heads)
+// (ffai-argus 0.7.3 src/text.rs, TextTower::block GQA fold).  RoPE is
+// rotate-half with the float32 tables of kime-cuda 0.0.3 src/plan.rs
+// (fn rope_tables); positions restart at every sequence (kime-cpu 0.0.17
+// src/kime_cpu/plan.rs, Step::Rope).  Key j is visible when j < L, j <= i if
+// causal, |i - j| <= window if window >= 0 (kime-cuda Op::Attention: window
+// None = -1).  Masked keys are skipped, never written as -inf (ffai-argus
+// src/text.rs, module doc and CausalSoftmax).
+//
+// CTA = 384 threads, one unit = (two consecutive 128-row query tiles A, B of
+// one sequence, head h), taken from the device schedule:
+//   warps 0-3   softmax warpgroup A (query tile A = TMEM lanes 0..127)
+//   warps 4-7   softmax warpgroup B (query tile B)
+//   warp 8      TMA producer: Q tiles, then a 3-stage K/V ring
+//   warp 9      MMA issuer (one thread): S = Q K^T and PV = P V, tcgen05.mma
+//   warps 10-11 RoPE of every K tile in shared memory (shared by A and B)
+// TMEM (512 columns): S_A 0..127, S_B 128..255, PV_A 256..319, PV_B 320..383.
+// Per key tile t the MMA thread issues PV_A(t), S_A(t+1), PV_B(t), S_B(t+1),
+// so one warpgroup's softmax overlaps the other's MMAs.  A softmax warpgroup
+// consumes PV(t-1) -- O = O * alpha(t-1) + PV(t-1), O in registers -- after it
+// has the row maxima of tile t, then writes P(t) (bf16, swizzled K-major) to
+// shared memory.  Every wait is bounded; on a timeout every role winds down.
+#include "kime_common.cuh"
+
+namespace kime {
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kStages = 3;
+constexpr uint32_t kTile = kBM * kHead * 2;  // 16 KB: 128 rows x 128 B
+constexpr uint32_t kOffQ = 0;                // 2 tiles
+constexpr uint32_t kOffK = kOffQ + 2 * kTile;
+constexpr uint32_t kOffV = kOffK + kStages * kTile;
+constexpr uint32_t kOffP = kOffV + kStages * kTile;  // 2 x 32 KB
+constexpr uint32_t kOffBar = kOffP + 4 * kTile;
+constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, 0, 1);
+
+struct UnitInfo {
+  int32_t u, s, qt0, nt, kb, ke, row0, L;
+};
+
+struct Shared {
+  uint64_t unit_full[2], unit_empty[2];
+  uint64_t q_full, q_empty;
+  uint64_t qrot[2];
+  uint64_t kv_full[kStages], krot[kStages], kv_empty[kStages];
+  uint64_t s_full[2], p_full[2], pv_full[2];
+  UnitInfo info[2];
+  uint32_t tmem_base;
+  int32_t abort;
+};
+static_assert(sizeof(Shared) <= 512, "barrier block");
+
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// RoPE (rotate-half) of row r of a 128-byte-swizzled [128 x 64] bf16 tile, in
+// place, with table row (c, s).  16-byte chunk k of row r sits at k ^ (r & 7).
+__device__ __forceinline__ void rope_row_sw128(uint8_t* tile, int r, const float* __restrict__ c,
+                                               const float* __restrict__ s) {
+  uint8_t* row = tile + r * 128;
+  const int sw = r & 7;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint4* plo = reinterpret_cast<uint4*>(row + ((k ^ sw) << 4));
+    uint4* phi = reinterpret_cast<uint4*>(row + (((k + 4) ^ sw) << 4));
+    const uint4 a = *plo, b = *phi;
+    const float4 c0 = __ldg(reinterpret_cast<const float4*>(c + 8 * k));
+    const float4 c1 = __ldg(reinterpret_cast<const float4*>(c + 8 * k + 4));
+    const float4 s0 = __ldg(reinterpret_cast<const float4*>(s + 8 * k));
+    const float4 s1 = __ldg(reinterpret_cast<const float4*>(s + 8 * k + 4));
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+    const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    uint32_t ya[4], yb[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float a0, a1, b0, b1;
+      rope_pair(bf16lo(aw[e]), bf16lo(bw[e]), cc[2 * e], ss[2 * e], a0, b0);
+      rope_pair(bf16hi(aw[e]), bf16hi(bw[e]), cc[2 * e + 1], ss[2 * e + 1], a1, b1);
+      ya[e] = pack_bf16x2(a0, a1);
+      yb[e] = pack_bf16x2(b0, b1);
+    }
+    *plo = make_uint4(ya[0], ya[1], ya[2], ya[3]);
+    *phi = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+  }
+}
+
+struct Params {
+  int heads, kv_heads, window, causal;
+  float scale_log2;
+  const float* cos_t;
+  const float* sin_t;
+  __nv_bfloat16* out;
+  WsHeader* hdr;
+  const Duo* duos;
+  int32_t* dev_status;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap qkv_map, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Shared* sh = reinterpret_cast<Shared*>(smem + kOffBar);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.heads / p.kv_heads;
+  const int n_units = p.hdr->n_duos * p.heads;
+
+  if (tid == 0) {
+    tma_prefetch_map(&qkv_map);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh->unit_full[i], 1);
+      mbar_init(&sh->unit_empty[i], 4);  // softmax A, softmax B, MMA, RoPE
+      mbar_init(&sh->qrot[i], 1);
+      mbar_init(&sh->s_full[i], 1);
+      mbar_init(&sh->p_full[i], 1);
+      mbar_init(&sh->pv_full[i], 1);
+    }
+    mbar_init(&sh->q_full, 1);
+    mbar_init(&sh->q_empty, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sh->kv_full[i], 1);
+      mbar_init(&sh->krot[i], 1);
+      mbar_init(&sh->kv_empty[i], 1);
+    }
+    sh->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&sh->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+  volatile int32_t* abort_flag = &sh->abort;
+
+  // Bounded wait; a timeout anywhere raises the CTA's abort flag, after which
+  // every wait returns false at once and every role leaves its loop.
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity)) return true;
+    *abort_flag = 1;
+    report(p.dev_status, ST_TIMEOUT);
+    return false;
+  };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t n = 0, c = 0;
+      for (;; ++n) {
+        const int slot = n & 1;
+        const int u = atomicAdd(&p.hdr->next_duo, 1);
+        if (!wait(&sh->unit_empty[slot], ((n >> 1) & 1) ^ 1)) break;
+        UnitInfo inf;
+        inf.u = u < n_units ? u : -1;
+        if (inf.u >= 0) {
+          const Duo d = p.duos[u / p.heads];
+          inf.s = d.s; inf.qt0 = d.qt0; inf.nt = d.nt; inf.kb = d.kb; inf.ke = d.ke; inf.row0 = d.row0; inf.L = d.L;
+        }
+        sh->info[slot] = inf;
+        mbar_arrive(&sh->unit_full[slot]);
+        if (inf.u < 0) break;
+        const int h = inf.u % p.heads, g = h / G;
+        if (!wait(&sh->q_empty, (n & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(&sh->q_full, inf.nt * kTile);
+        tma_load_2d(smem + kOffQ, &qkv_map, &sh->q_full, h * kHead, inf.row0 + inf.qt0 * kBM);
+        if (inf.nt == 2)
+          tma_load_2d(smem + kOffQ + kTile, &qkv_map, &sh->q_full, h * kHead, inf.row0 + (inf.qt0 + 1) * kBM);
+        const int kx = (p.heads + g) * kHead, vx = (p.heads + p.kv_heads + g) * kHead;
+        bool ok = true;
+        for (int t = inf.kb; t < inf.ke; ++t, ++c) {
+          const int st = c % kStages;
+          if (!wait(&sh->kv_empty[st], ((c / kStages) & 1) ^ 1)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sh->kv_full[st], 2 * kTile);
+          tma_load_2d(smem + kOffK + st * kTile, &qkv_map, &sh->kv_full[st], kx, inf.row0 + t * kBN);
+          tma_load_2d(smem + kOffV + st * kTile, &qkv_map, &sh->kv_full[st], vx, inf.row0 + t * kBN);
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t n = 0, c = 0, pc[2] = {0, 0}, qr[2] = {0, 0};
+      const uint32_t aq[2] = {smem_u32(smem + kOffQ), smem_u32(smem + kOffQ + kTile)};
+      const uint32_t ap[2] = {smem_u32(smem + kOffP), smem_u32(smem + kOffP + 2 * kTile)};
+      for (;; ++n) {
+        const int slot = n & 1;
+        if (!wait(&sh->unit_full[slot], (n >> 1) & 1)) break;
+        const UnitInfo inf = sh->info[slot];
+        if (inf.u < 0) break;
+        int kb[2], ke[2], fb, fe;
+        tile_ranges(inf.L, inf.qt0, p.causal, p.window, kb[0], ke[0], fb, fe);
+        kb[1] = ke[1] = 0;
+        if (inf.nt == 2) tile_ranges(inf.L, inf.qt0 + 1, p.causal, p.window, kb[1], ke[1], fb, fe);
+        bool ok = true;
+        for (int w = 0; w < inf.nt && ok; ++w) ok = wait(&sh->qrot[w], (qr[w]++) & 1);
+        auto issue_s = [&](int w, int stage) {
+          tc_fence_after();
+          const uint32_t bk = smem_u32(smem + kOffK + stage * kTile);
+#pragma unroll
+          for (int ks = 0; ks < kHead / 16; ++ks)
+            tc_mma_ss(tmem + w * 128, sdesc_sw128(aq[w] + ks * 32, 16, 1024), sdesc_sw128(bk + ks * 32, 16, 1024),
+                      kIdescS, ks > 0);
+          tc_commit(&sh->s_full[w]);
+        };
+        // S for the first key tile
+        if (ok) {
+          const int st = c % kStages;
+          ok = wait(&sh->kv_full[st], (c / kStages) & 1) && wait(&sh->krot[st], (c / kStages) & 1);
+          for (int w = 0; ok && w < inf.nt; ++w)
+            if (inf.kb >= kb[w] && inf.kb < ke[w]) issue_s(w, st);
+        }
+        for (int t = inf.kb; ok && t < inf.ke; ++t, ++c) {
+          const int st = c % kStages, st1 = (c + 1) % kStages;
+          bool next_ready = false;
+          for (int w = 0; ok && w < inf.nt; ++w) {
+            if (t >= kb[w] && t < ke[w]) {
+              if (!(ok = wait(&sh->p_full[w], (pc[w]++) & 1))) break;
+              tc_fence_after();
+              const uint32_t bv = smem_u32(smem + kOffV + st * kTile);
+#pragma unroll
+              for (int ks = 0; ks < kBN / 16; ++ks)
+                tc_mma_ss(tmem + 256 + w * 64, sdesc_sw128(ap[w] + (ks >> 2) * kTile + (ks & 3) * 32, 16, 1024),
+                          sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, ks > 0);
+              tc_commit(&sh->pv_full[w]);
+            }
+            if (t + 1 < inf.ke && t + 1 >= kb[w] && t + 1 < ke[w]) {
+              if (!next_ready) {
+                const uint32_t ph1 = ((c + 1) / kStages) & 1;
+                if (!(ok = wait(&sh->kv_full[st1], ph1) && wait(&sh->krot[st1], ph1))) break;
+                next_ready = true;
+              }
+              issue_s(w, st1);
+            }
+          }
+          tc_commit(&sh->kv_empty[st]);  // every MMA reading stage st is issued
+        }
+        tc_commit(&sh->q_empty);
+        if (!ok) break;
+        mbar_arrive(&sh->unit_empty[slot]);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ K RoPE
+    const int r0 = tid - 320;  // 0..63: rows r0 and r0 + 64
+    uint32_t n = 0, c = 0;
+    for (;; ++n) {
+      const int slot = n & 1;
+      bool ok = wait(&sh->unit_full[slot], (n >> 1) & 1);
+      if (named_bar_or(3, 64, !ok)) break;
+      const UnitInfo inf = sh->info[slot];
+      if (inf.u < 0) break;
+      for (int t = inf.kb; t < inf.ke; ++t, ++c) {
+        const int st = c % kStages;
+        ok = wait(&sh->kv_full[st], (c / kStages) & 1);
+        if (ok) {
+          uint8_t* kt = smem + kOffK + st * kTile;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int r = r0 + 64 * half, j = t * kBN + r;
+            if (j < inf.L) rope_row_sw128(kt, r, p.cos_t + static_cast<size_t>(j) * kHalf,
+                                          p.sin_t + static_cast<size_t>(j) * kHalf);
+          }
+          fence_proxy_async_smem();
+        }
+        if (named_bar_or(3, 64, !ok)) { ok = false; break; }
+        if (r0 == 0) mbar_arrive(&sh->krot[st]);
+      }
+      if (!ok) break;
+      if (r0 == 0) mbar_arrive(&sh->unit_empty[slot]);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int w = warp >> 2;           // 0: tile A, 1: tile B
+    const int r = tid & 127;           // row in the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + w * 128 + lane_off, tPV = tmem + 256 + w * 64 + lane_off;
+    uint8_t* sQ = smem + kOffQ + w * kTile;
+    uint8_t* sP = smem + kOffP + w * 2 * kTile;
+    uint32_t n = 0, sc = 0, pvc = 0;
+    for (;; ++n) {
+      const int slot = n & 1;
+      bool ok = wait(&sh->unit_full[slot], (n >> 1) & 1);
+      if (named_bar_or(1 + w, 128, !ok)) break;
+      const UnitInfo inf = sh->info[slot];
+      if (inf.u < 0) break;
+      if (w >= inf.nt) {  // no partner tile in this unit
+        named_bar_or(1 + w, 128, false);
+        if (r == 0) mbar_arrive(&sh->unit_empty[slot]);
+        continue;
+      }
+      const int h = inf.u % p.heads;
+      const int qt = inf.qt0 + w, q0 = qt * kBM, i = q0 + r;
+      const bool row_ok = i < inf.L;
+      int kb, ke, fb, fe;
+      tile_ranges(inf.L, qt, p.causal, p.window, kb, ke, fb, fe);
+
+      ok = wait(&sh->q_full, n & 1);
+      if (ok && row_ok)
+        rope_row_sw128(sQ, r, p.cos_t + static_cast<size_t>(i) * kHalf, p.sin_t + static_cast<size_t>(i) * kHalf);
+      fence_proxy_async_smem();
+      if (named_bar_or(1 + w, 128, !ok)) break;
+      if (r == 0) {
+        mbar_arrive(&sh->qrot[w]);
+        mbar_arrive(&sh->unit_empty[slot]);  // every thread has its copy of the unit
+      }
+
+      float o[kHead];
+#pragma unroll
+      for (int d = 0; d < kHead; ++d) o[d] = 0.f;
+      float m = -INFINITY, l = 0.f, alpha_prev = 0.f;
+      const float cl = p.scale_log2;
+      for (int t = kb; t < ke; ++t) {
+        const int k0 = t * kBN;
+        ok = wait(&sh->s_full[w], (sc++) & 1);
+        tc_fence_after();
+        const bool full = t >= fb && t < fe;
+        auto raw = [&](int j, uint32_t bits) -> float {  // raw score or -inf if masked
+          const float x = __uint_as_float(bits);
+          if (full) return row_ok ? x : -INFINITY;
+          const int jj = k0 + j;
+          bool vis = row_ok && jj < inf.L;
+          if (p.causal) vis = vis && jj <= i;
+          if (p.window >= 0) vis = vis && abs(i - jj) <= p.window;
+          return vis ? x : -INFINITY;
+        };
+        float mx = -INFINITY;
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32_wait(tS + cc * 32, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, raw(cc * 32 + e, v[e]));
+        }
+        const float m_new = fmaxf(m, mx * cl);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = fast_exp2(m - m_use);
+        // Consume PV of the previous tile (its MMA also read the P buffer).
+        if (t > kb) {
+          ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
+          tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < kHead / 32; ++cc) {
+            uint32_t v[32];
+            tmem_ld32_wait(tPV + cc * 32, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[cc * 32 + e] = fmaf(o[cc * 32 + e], alpha_prev, __uint_as_float(v[e]));
+          }
+        }
+        float rowsum = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < kBN / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32_wait(tS + cc * 32, v);
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint32_t pw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = cc * 32 + q8 * 8 + 2 * e;
+              const float p0 = fast_exp2(fmaf(raw(j, v[q8 * 8 + 2 * e]), cl, -m_use));
+              const float p1 = fast_exp2(fmaf(raw(j + 1, v[q8 * 8 + 2 * e + 1]), cl, -m_use));
+              rowsum += p0 + p1;
+              pw[e] = pack_bf16x2(p0, p1);
+            }
+            const int ch = cc * 4 + q8;  // 16-byte chunk of the P row
+            *reinterpret_cast<uint4*>(sP + (ch >> 3) * kTile + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
+                make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          }
+        }
+        l = l * alpha + rowsum;
+        m = m_new;
+        alpha_prev = alpha;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        if (named_bar_or(1 + w, 128, !ok)) { ok = false; break; }
+        if (r == 0) mbar_arrive(&sh->p_full[w]);
+      }
+      if (!ok) break;
+      ok = wait(&sh->pv_full[w], (pvc++) & 1);
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < kHead / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld32_wait(tPV + cc * 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[cc * 32 + e] = fmaf(o[cc * 32 + e], alpha_prev, __uint_as_float(v[e]));
+      }
+      tc_fence_before();
+      if (named_bar_or(1 + w, 128, !ok)) break;
+      if (row_ok) {
+        const float inv = 1.f / l;
+        __nv_bfloat16* dst = p.out + static_cast<size_t>(inf.row0 + i) * p.heads * kHead + h * kHead;
+#pragma unroll
+        for (int d = 0; d < kHead; d += 8) {
+          uint4 wv;
+          wv.x = pack_bf16x2(o[d] * inv, o[d + 1] * inv);
+          wv.y = pack_bf16x2(o[d + 2] * inv, o[d + 3] * inv);
+          wv.z = pack_bf16x2(o[d + 4] * inv, o[d + 5] * inv);
+          wv.w = pack_bf16x2(o[d + 6] * inv, o[d + 7] * inv);
+          *reinterpret_cast<uint4*>(dst + d) = wv;
+        }
+      }
+    }
+  }
+
+  // Wind down: after an abort, give copies and MMAs still in flight a bounded
+  // chance to land before shared memory and TMEM are released.
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    auto settle = [&](uint64_t* bar) {  // whichever phase is pending, let it finish
+      mbar_wait(bar, 0);
+      mbar_wait(bar, 1);
+    };
+    for (int i = 0; i < kStages; ++i) settle(&sh->kv_full[i]);
+    settle(&sh->q_full);
+    for (int i = 0; i < 2; ++i) {
+      settle(&sh->s_full[i]);
+      settle(&sh->pv_full[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, int n_seqs, int total, int heads, int kv_heads,
+                              int window, int causal, float scale, const float* cos_t, const float* sin_t, void* out,
+                              void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st) {
+  (void)n_seqs; (void)total;
+  static int configured[64] = {0};
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  Params prm;
+  prm.heads = heads;
+  prm.kv_heads = kv_heads;
+  prm.window = window;
+  prm.causal = causal;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.cos_t = cos_t;
+  prm.sin_t = sin_t;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.hdr = static_cast<WsHeader*>(ws);
+  prm.duos = ws_duos(ws, max_pairs);
+  prm.dev_status = dev_status;
+  prefill_tc_kernel<<<sms, kThreads, kSmemBytes, st>>>(*qkv_map, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace kime
