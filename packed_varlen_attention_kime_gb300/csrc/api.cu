@@ -2,7 +2,6 @@
 // argument checks, workspace carving, TMA tensor-map encoding and launches.
 // No allocation and no synchronisation happen here.
 #include <math.h>
-#include <stdlib.h>
 #include <string.h>
 
 #include "../../include/kime_attn.h"
@@ -111,11 +110,6 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
   CUtensorMap map;
   rc = encode_qkv_map(&map, qkv, total_tokens, static_cast<int>(W));
   if (rc) return rc;
-  static const bool v1 = getenv("KIME_PREFILL_V1") != nullptr;
-  if (v1)
-    return cuda_status(kime::launch_prefill_bf16(&map, cu_seqlens, n_seqs, total_tokens, heads, kv_heads, window,
-                                                 causal, scale, rope_cos, rope_sin, out, workspace, max_pairs,
-                                                 dev_status, st));
   return cuda_status(kime::launch_prefill_tc(&map, n_seqs, total_tokens, heads, kv_heads, window, causal, scale,
                                              rope_cos, rope_sin, out, workspace, max_pairs, dev_status, st));
 }

@@ -66,10 +66,6 @@ cudaError_t launch_schedule(const int32_t* cu, int n_seqs, int total, int max_se
 cudaError_t launch_varlen_f32(const float* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
                               int window, int causal, float scale, const float* cos_t, const float* sin_t,
                               float* out, void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
-cudaError_t launch_prefill_bf16(const CUtensorMap* qkv_map, const int32_t* cu, int n_seqs, int total, int heads,
-                                int kv_heads, int window, int causal, float scale, const float* cos_t,
-                                const float* sin_t, void* out, void* ws, int max_pairs, int32_t* dev_status,
-                                cudaStream_t st);
 cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, int n_seqs, int total, int heads, int kv_heads,
                               int window, int causal, float scale, const float* cos_t, const float* sin_t, void* out,
                               void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);

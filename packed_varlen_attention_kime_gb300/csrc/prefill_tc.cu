@@ -19,7 +19,12 @@
 //   warps 4-7   softmax warpgroup B (query tile B)
 //   warp 8      TMA producer: Q tiles, then a 3-stage K/V ring
 //   warp 9      MMA issuer (one thread): S = Q K^T and PV = P V, tcgen05.mma
-//   warps 10-11 RoPE of every K tile in shared memory (shared by A and B)
+//   warps 10-11 RoPE of every K tile in shared memory (shared by A and B), and
+//               the V tile's conversion to f16
+// MMA operands are f16 (11-bit significand): q and k are rotated in float32 and
+// rounded once to f16 (q times scale*log2(e) first, so S arrives in log2
+// units), V is widened from bf16 exactly, P is rounded to f16.  Inputs must
+// stay inside the f16 range (|value| < 65504; conversions saturate).
 // TMEM (512 columns): S_A 0..127, S_B 128..255, PV_A 256..319, PV_B 320..383.
 // Per key tile t the MMA thread issues PV_A(t), S_A(t+1), PV_B(t), S_B(t+1),
 // so one warpgroup's softmax overlaps the other's MMAs.  A softmax warpgroup
@@ -42,8 +47,8 @@ constexpr uint32_t kOffP = kOffV + kStages * kTile;  // 2 x 32 KB
 constexpr uint32_t kOffBar = kOffP + 4 * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, 0, 0);
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, 0, 1);
+constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
+constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
 
 struct UnitInfo {
   int32_t u, s, qt0, nt, kb, ke, row0, L;
@@ -72,10 +77,13 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
-// RoPE (rotate-half) of row r of a 128-byte-swizzled [128 x 64] bf16 tile, in
-// place, with table row (c, s).  16-byte chunk k of row r sits at k ^ (r & 7).
-__device__ __forceinline__ void rope_row_sw128(uint8_t* tile, int r, const float* __restrict__ c,
-                                               const float* __restrict__ s) {
+// Row r of a 128-byte-swizzled [128 x 64] tile (16-byte chunk k of row r sits
+// at chunk k ^ (r & 7)), bf16 on entry, converted in place to the f16 operand
+// the MMAs read.  rope_row: rotate-half RoPE with table row (c, s) in float32
+// (one rounding per operation), times `mul`, rounded once to f16.
+// convert_row: the bf16 values widened and rounded to f16.
+__device__ __forceinline__ void rope_row(uint8_t* tile, int r, const float* __restrict__ c,
+                                         const float* __restrict__ s, float mul) {
   uint8_t* row = tile + r * 128;
   const int sw = r & 7;
 #pragma unroll
@@ -96,17 +104,27 @@ __device__ __forceinline__ void rope_row_sw128(uint8_t* tile, int r, const float
       float a0, a1, b0, b1;
       rope_pair(bf16lo(aw[e]), bf16lo(bw[e]), cc[2 * e], ss[2 * e], a0, b0);
       rope_pair(bf16hi(aw[e]), bf16hi(bw[e]), cc[2 * e + 1], ss[2 * e + 1], a1, b1);
-      ya[e] = pack_bf16x2(a0, a1);
-      yb[e] = pack_bf16x2(b0, b1);
+      ya[e] = pack_f16x2(a0 * mul, a1 * mul);
+      yb[e] = pack_f16x2(b0 * mul, b1 * mul);
     }
     *plo = make_uint4(ya[0], ya[1], ya[2], ya[3]);
     *phi = make_uint4(yb[0], yb[1], yb[2], yb[3]);
   }
 }
 
+__device__ __forceinline__ void convert_row(uint8_t* tile, int r) {
+  uint4* row = reinterpret_cast<uint4*>(tile + r * 128);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint4 a = row[k];
+    row[k] = make_uint4(pack_f16x2(bf16lo(a.x), bf16hi(a.x)), pack_f16x2(bf16lo(a.y), bf16hi(a.y)),
+                        pack_f16x2(bf16lo(a.z), bf16hi(a.z)), pack_f16x2(bf16lo(a.w), bf16hi(a.w)));
+  }
+}
+
 struct Params {
   int heads, kv_heads, window, causal;
-  float scale_log2;
+  float qmul;  // scale * log2(e), folded into q before its f16 rounding
   const float* cos_t;
   const float* sin_t;
   __nv_bfloat16* out;
@@ -279,11 +297,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait(&sh->kv_full[st], (c / kStages) & 1);
         if (ok) {
           uint8_t* kt = smem + kOffK + st * kTile;
+          uint8_t* vt = smem + kOffV + st * kTile;
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const int r = r0 + 64 * half, j = t * kBN + r;
-            if (j < inf.L) rope_row_sw128(kt, r, p.cos_t + static_cast<size_t>(j) * kHalf,
-                                          p.sin_t + static_cast<size_t>(j) * kHalf);
+            if (j < inf.L)
+              rope_row(kt, r, p.cos_t + static_cast<size_t>(j) * kHalf, p.sin_t + static_cast<size_t>(j) * kHalf,
+                       1.f);
+            else
+              convert_row(kt, r);
+            convert_row(vt, r);
           }
           fence_proxy_async_smem();
         }
@@ -320,8 +343,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_ranges(inf.L, qt, p.causal, p.window, kb, ke, fb, fe);
 
       ok = wait(&sh->q_full, n & 1);
-      if (ok && row_ok)
-        rope_row_sw128(sQ, r, p.cos_t + static_cast<size_t>(i) * kHalf, p.sin_t + static_cast<size_t>(i) * kHalf);
+      if (ok) {
+        if (row_ok)
+          rope_row(sQ, r, p.cos_t + static_cast<size_t>(i) * kHalf, p.sin_t + static_cast<size_t>(i) * kHalf,
+                   p.qmul);
+        else
+          convert_row(sQ, r);
+      }
       fence_proxy_async_smem();
       if (named_bar_or(1 + w, 128, !ok)) break;
       if (r == 0) {
@@ -333,13 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int d = 0; d < kHead; ++d) o[d] = 0.f;
       float m = -INFINITY, l = 0.f, alpha_prev = 0.f;
-      const float cl = p.scale_log2;
       for (int t = kb; t < ke; ++t) {
         const int k0 = t * kBN;
         ok = wait(&sh->s_full[w], (sc++) & 1);
         tc_fence_after();
         const bool full = t >= fb && t < fe;
-        auto raw = [&](int j, uint32_t bits) -> float {  // raw score or -inf if masked
+        auto raw = [&](int j, uint32_t bits) -> float {  // logit (log2 units) or -inf if masked
           const float x = __uint_as_float(bits);
           if (full) return row_ok ? x : -INFINITY;
           const int jj = k0 + j;
@@ -356,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) mx = fmaxf(mx, raw(cc * 32 + e, v[e]));
         }
-        const float m_new = fmaxf(m, mx * cl);
+        const float m_new = fmaxf(m, mx);
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = fast_exp2(m - m_use);
         // Consume PV of the previous tile (its MMA also read the P buffer).
@@ -382,10 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int j = cc * 32 + q8 * 8 + 2 * e;
-              const float p0 = fast_exp2(fmaf(raw(j, v[q8 * 8 + 2 * e]), cl, -m_use));
-              const float p1 = fast_exp2(fmaf(raw(j + 1, v[q8 * 8 + 2 * e + 1]), cl, -m_use));
+              const float p0 = fast_exp2(raw(j, v[q8 * 8 + 2 * e]) - m_use);
+              const float p1 = fast_exp2(raw(j + 1, v[q8 * 8 + 2 * e + 1]) - m_use);
               rowsum += p0 + p1;
-              pw[e] = pack_bf16x2(p0, p1);
+              pw[e] = pack_f16x2(p0, p1);
             }
             const int ch = cc * 4 + q8;  // 16-byte chunk of the P row
             *reinterpret_cast<uint4*>(sP + (ch >> 3) * kTile + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
@@ -471,7 +498,7 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, int n_seqs, int total,
   prm.kv_heads = kv_heads;
   prm.window = window;
   prm.causal = causal;
-  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.qmul = scale * 1.4426950408889634f;
   prm.cos_t = cos_t;
   prm.sin_t = sin_t;
   prm.out = static_cast<__nv_bfloat16*>(out);
