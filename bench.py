@@ -275,6 +275,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-soak", action="store_true", help="skip the 1 s load before the timed steps")
+    ap.add_argument("--only", default=None,
+                    help="profiling aid: run only WORKLOAD[:LAYER] (modernbert_base, modernbert_large, "
+                         "smollm2_prefill, smollm2_decode) for --steps steps and print its timings")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -287,6 +291,8 @@ def main():
 
     if args.impl == "reference":
         return reference_arm(args, rank, world)
+    if args.only:
+        return only_arm(args, local)
 
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
@@ -310,7 +316,7 @@ def main():
     with ClockSampler(local) as clk:
         # keep the GPU under the same load for about a second first, so the
         # 100 ms clock samples cover the timed steps and the state they run in
-        t_end = time.perf_counter() + 1.0
+        t_end = time.perf_counter() + (0.0 if args.no_soak else 1.0)
         while time.perf_counter() < t_end:
             for _ in range(20):
                 step(None)
@@ -363,7 +369,7 @@ def main():
         extra = extra_measurements(dev, flush, stream, pk)
 
     cpu = None
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
         rate, cores, sample = oracle_sample_rate(VarlenRunCPU(c), args.cpu_budget)
         cpu = {"value": round(rate, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
 
@@ -384,6 +390,31 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def only_arm(args, local):
+    """One workload (and optionally one layer) alone: the command ncu captures."""
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    from __graft_entry__ import build
+    build()
+    stream = torch.cuda.current_stream(dev)
+    flush = l2_flush_buffer(dev)
+    name, _, layer = args.only.partition(":")
+    if name == "smollm2_decode":
+        d = DecodeRun(dev)
+        per, _ = time_fn(lambda ev: d.step(), args.steps, args.warmup, flush, stream)
+        print(json.dumps({"only": name, "ms": [round(x, 4) for x in per]}))
+        return
+    r = VarlenRun(name, dev)
+    ks = [k for k, l in enumerate(r.case.layers) if not layer or l.name == layer]
+
+    def f(ev):
+        for k in ks:
+            r.layer(k)
+    per, _ = time_fn(f, args.steps, args.warmup, flush, stream)
+    print(json.dumps({"only": args.only, "layers": [r.case.layers[k].name for k in ks],
+                      "ms": [round(x, 4) for x in per]}))
 
 
 class VarlenRunCPU:
