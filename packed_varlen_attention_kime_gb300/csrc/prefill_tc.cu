@@ -25,11 +25,12 @@
 // rounded once to f16 (q times scale*log2(e) first, so S arrives in log2
 // units), V is widened from bf16 exactly, P is rounded to f16.  Inputs must
 // stay inside the f16 range (|value| < 65504; conversions saturate).
-// TMEM (512 columns): S_A 0..127, S_B 128..255, PV_A 256..319, PV_B 320..383.
+// TMEM (512 columns): S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383.
 // Per key tile t the MMA thread issues PV_A(t), S_A(t+1), PV_B(t), S_B(t+1),
-// so one warpgroup's softmax overlaps the other's MMAs.  A softmax warpgroup
-// consumes PV(t-1) -- O = O * alpha(t-1) + PV(t-1), O in registers -- after it
-// has the row maxima of tile t, then writes P(t) (bf16, swizzled K-major) to
+// so one warpgroup's softmax overlaps the other's MMAs.  The PV MMAs accumulate
+// O in TMEM.  A softmax warpgroup reads S(t) once, takes P(t) = 2^(S - m_ref)
+// against a reference max that moves only when exceeded by more than 2^8
+// (then O is rescaled in TMEM), and writes P(t) (f16, swizzled K-major) to
 // shared memory.  Every wait is bounded; on a timeout every role winds down.
 #include "kime_common.cuh"
 
@@ -115,7 +116,8 @@ __device__ __forceinline__ void rope_row(uint8_t* tile, int r, const float* __re
 __device__ __forceinline__ void convert_row(uint8_t* tile, int r) {
   uint4* row = reinterpret_cast<uint4*>(tile + r * 128);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int kk = 0; kk < 8; ++kk) {
+    const int k = kk ^ (r & 7);  // neighbouring rows touch different banks
     const uint4 a = row[k];
     row[k] = make_uint4(pack_f16x2(bf16lo(a.x), bf16hi(a.x)), pack_f16x2(bf16lo(a.y), bf16hi(a.y)),
                         pack_f16x2(bf16lo(a.z), bf16hi(a.z)), pack_f16x2(bf16lo(a.w), bf16hi(a.w)));
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int ks = 0; ks < kBN / 16; ++ks)
                 tc_mma_ss(tmem + 256 + w * 64, sdesc_sw128(ap[w] + (ks >> 2) * kTile + (ks & 3) * 32, 16, 1024),
-                          sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, ks > 0);
+                          sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, (ks > 0 || t > kb[w]) ? 1u : 0u);
               tc_commit(&sh->pv_full[w]);
             }
             if (t + 1 < inf.ke && t + 1 >= kb[w] && t + 1 < ke[w]) {
@@ -321,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int w = warp >> 2;           // 0: tile A, 1: tile B
     const int r = tid & 127;           // row in the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + w * 128 + lane_off, tPV = tmem + 256 + w * 64 + lane_off;
+    const uint32_t tS = tmem + w * 128 + lane_off, tO = tmem + 256 + w * 64 + lane_off;
     uint8_t* sQ = smem + kOffQ + w * kTile;
     uint8_t* sP = smem + kOffP + w * 2 * kTile;
     uint32_t n = 0, sc = 0, pvc = 0;
@@ -357,71 +359,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sh->unit_empty[slot]);  // every thread has its copy of the unit
       }
 
-      float o[kHead];
-#pragma unroll
-      for (int d = 0; d < kHead; ++d) o[d] = 0.f;
-      float m = -INFINITY, l = 0.f, alpha_prev = 0.f;
+      // Online softmax with a lazily moved reference max: P = 2^(S - m_ref) and
+      // O (in TMEM, accumulated by the PV MMAs) stay relative to m_ref, which
+      // only moves -- rescaling O and l -- when a row's max exceeds it by more
+      // than 2^8.  Logits arrive in log2 units (scale*log2(e) is folded into q).
+      float m_ref = -INFINITY, l = 0.f;
       for (int t = kb; t < ke; ++t) {
         const int k0 = t * kBN;
         ok = wait(&sh->s_full[w], (sc++) & 1);
         tc_fence_after();
-        const bool full = t >= fb && t < fe;
-        auto raw = [&](int j, uint32_t bits) -> float {  // logit (log2 units) or -inf if masked
-          const float x = __uint_as_float(bits);
-          if (full) return row_ok ? x : -INFINITY;
-          const int jj = k0 + j;
-          bool vis = row_ok && jj < inf.L;
-          if (p.causal) vis = vis && jj <= i;
-          if (p.window >= 0) vis = vis && abs(i - jj) <= p.window;
-          return vis ? x : -INFINITY;
-        };
-        float mx = -INFINITY;
+        uint32_t v[128];
+        tmem_ld128_wait(tS, v);
+        float x[128];
 #pragma unroll
-        for (int cc = 0; cc < kBN / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld32_wait(tS + cc * 32, v);
+        for (int j = 0; j < kBN; ++j) x[j] = __uint_as_float(v[j]);
+        if (!(t >= fb && t < fe)) {
+          // visible keys of this row in this tile form one interval [lo, hi]
+          int lo = 0, hi = min(kBN - 1, inf.L - 1 - k0);
+          if (p.causal) hi = min(hi, i - k0);
+          if (p.window >= 0) {
+            lo = max(lo, i - p.window - k0);
+            hi = min(hi, i + p.window - k0);
+          }
+          if (!row_ok) hi = -1;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, raw(cc * 32 + e, v[e]));
+          for (int j = 0; j < kBN; ++j)
+            if (j < lo || j > hi) x[j] = -INFINITY;
         }
-        const float m_new = fmaxf(m, mx);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = fast_exp2(m - m_use);
-        // Consume PV of the previous tile (its MMA also read the P buffer).
+        float mx = x[0];
+#pragma unroll
+        for (int j = 1; j < kBN; ++j) mx = fmaxf(mx, x[j]);
+        // move the reference max on the first visible keys, or when it is
+        // exceeded by more than 8 (a factor 256)
+        float alpha = 1.f;
+        if (mx > m_ref + 8.f) {
+          if (m_ref != -INFINITY) alpha = fast_exp2(m_ref - mx);
+          m_ref = mx;
+        }
+        // PV of the previous tile must be done before P is overwritten (it read
+        // the P buffer) and before O is rescaled (it accumulated into O).
         if (t > kb) {
           ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
           tc_fence_after();
-#pragma unroll
-          for (int cc = 0; cc < kHead / 32; ++cc) {
-            uint32_t v[32];
-            tmem_ld32_wait(tPV + cc * 32, v);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[cc * 32 + e] = fmaf(o[cc * 32 + e], alpha_prev, __uint_as_float(v[e]));
-          }
         }
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         float rowsum = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < kBN / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld32_wait(tS + cc * 32, v);
+        for (int ch = 0; ch < kBN / 8; ++ch) {  // P row, keys 0..63 in half 0, 64..127 in half 1
+          uint32_t pw[4];
 #pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint32_t pw[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = cc * 32 + q8 * 8 + 2 * e;
-              const float p0 = fast_exp2(raw(j, v[q8 * 8 + 2 * e]) - m_use);
-              const float p1 = fast_exp2(raw(j + 1, v[q8 * 8 + 2 * e + 1]) - m_use);
-              rowsum += p0 + p1;
-              pw[e] = pack_f16x2(p0, p1);
-            }
-            const int ch = cc * 4 + q8;  // 16-byte chunk of the P row
-            *reinterpret_cast<uint4*>(sP + (ch >> 3) * kTile + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
-                make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = fast_exp2(x[8 * ch + 2 * e] - m_use), p1 = fast_exp2(x[8 * ch + 2 * e + 1] - m_use);
+            rowsum += p0 + p1;
+            pw[e] = pack_f16x2(p0, p1);
           }
+          *reinterpret_cast<uint4*>(sP + (ch >> 3) * kTile + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
+              make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
         l = l * alpha + rowsum;
-        m = m_new;
-        alpha_prev = alpha;
+        if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {
+          uint32_t ov[64];
+          tmem_ld64_wait(tO, ov);
+#pragma unroll
+          for (int d = 0; d < kHead; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
+          tmem_st64_wait(tO, ov);
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         if (named_bar_or(1 + w, 128, !ok)) { ok = false; break; }
@@ -430,13 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ok = wait(&sh->pv_full[w], (pvc++) & 1);
       tc_fence_after();
-#pragma unroll
-      for (int cc = 0; cc < kHead / 32; ++cc) {
-        uint32_t v[32];
-        tmem_ld32_wait(tPV + cc * 32, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[cc * 32 + e] = fmaf(o[cc * 32 + e], alpha_prev, __uint_as_float(v[e]));
-      }
+      uint32_t ov[64];
+      tmem_ld64_wait(tO, ov);
       tc_fence_before();
       if (named_bar_or(1 + w, 128, !ok)) break;
       if (row_ok) {
@@ -445,10 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int d = 0; d < kHead; d += 8) {
           uint4 wv;
-          wv.x = pack_bf16x2(o[d] * inv, o[d + 1] * inv);
-          wv.y = pack_bf16x2(o[d + 2] * inv, o[d + 3] * inv);
-          wv.z = pack_bf16x2(o[d + 4] * inv, o[d + 5] * inv);
-          wv.w = pack_bf16x2(o[d + 6] * inv, o[d + 7] * inv);
+          wv.x = pack_bf16x2(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv);
+          wv.y = pack_bf16x2(__uint_as_float(ov[d + 2]) * inv, __uint_as_float(ov[d + 3]) * inv);
+          wv.z = pack_bf16x2(__uint_as_float(ov[d + 4]) * inv, __uint_as_float(ov[d + 5]) * inv);
+          wv.w = pack_bf16x2(__uint_as_float(ov[d + 6]) * inv, __uint_as_float(ov[d + 7]) * inv);
           *reinterpret_cast<uint4*>(dst + d) = wv;
         }
       }
