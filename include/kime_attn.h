@@ -138,6 +138,29 @@ int kime_attn_debug_tiles(const int32_t* cu_seqlens, int n_seqs, int total_token
                           int causal, void* workspace, size_t workspace_bytes, int32_t* tiles_out, int max_pairs,
                           int32_t* n_pairs_out, int32_t* dev_status, void* stream);
 
+/* Bytes of the scratch array built into the library for kime_attn_varlen_noalloc. */
+#define KIME_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* kime_attn_varlen_noalloc -- the same attention as kime_attn_varlen, for
+ * callers that cannot allocate device memory when they call it (for instance a
+ * host program whose own pool owns every device allocation, or a loop in which
+ * an allocation, which may synchronise the device, is not allowed).  The source
+ * pages have no counterpart of this entry point.
+ *
+ * Arguments are those of kime_attn_varlen without workspace / workspace_bytes:
+ * the scheduler's scratch is a KIME_NOALLOC_SCRATCH_BYTES array inside the
+ * library, held by every GPU that loads the library until the process exits.
+ * Returns KIME_ERANGE, launching nothing, when the batch needs more scratch than
+ * that (kime_attn_workspace_bytes(0, n_seqs, total_tokens, ...) is the need:
+ * about 48 bytes per 128 tokens plus 64 per sequence).  The first call on a
+ * device looks up the array's device address with that device current; make
+ * it before any stream capture.  All calls share the array, so calls that
+ * overlap on the GPU race; order them on one stream.  Allocates nothing. */
+int kime_attn_varlen_noalloc(const void* qkv, int dtype, const int32_t* cu_seqlens, int n_seqs, int total_tokens,
+                             int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal,
+                             float scale, const float* rope_cos, const float* rope_sin, int rope_len, void* out,
+                             int32_t* dev_status, void* stream);
+
 /* The cudaError_t of the last failing CUDA call in this thread (0 if none). */
 int kime_attn_last_cuda_error(void);
 

@@ -17,8 +17,8 @@ import torch
 
 __all__ = [
     "KimeError", "load_library", "kime_attn_varlen", "kime_kv_append", "kime_attn_decode",
-    "kime_attn_workspace_bytes", "kime_rope_tables", "kime_attn_debug_tiles", "KIME_F32", "KIME_BF16",
-    "EXPORTED_SYMBOLS",
+    "kime_attn_workspace_bytes", "kime_rope_tables", "kime_attn_debug_tiles", "kime_attn_varlen_noalloc",
+    "KIME_F32", "KIME_BF16", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +30,9 @@ DEV_BAD_CU, DEV_SEQ_TOO_LONG, DEV_BAD_POS, DEV_TIMEOUT = 1, 2, 4, 8
 EXPORTED_SYMBOLS = (
     "kime_attn_varlen", "kime_kv_append", "kime_attn_decode", "kime_attn_workspace_bytes",
     "kime_rope_tables", "kime_attn_debug_tiles", "kime_attn_last_cuda_error", "kime_attn_status_string",
+    "kime_attn_varlen_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 1 << 20
 
 _lib = None
 
@@ -64,6 +66,8 @@ def load_library(path: str = LIB_PATH):
     lib.kime_rope_tables.restype = I
     lib.kime_attn_debug_tiles.argtypes = [P, I, I, I, I, I, P, S, P, I, P, P, P]
     lib.kime_attn_debug_tiles.restype = I
+    lib.kime_attn_varlen_noalloc.argtypes = [P, I, P, I, I, I, I, I, I, I, I, F, P, P, I, P, P, P]
+    lib.kime_attn_varlen_noalloc.restype = I
     lib.kime_attn_last_cuda_error.argtypes = []
     lib.kime_attn_last_cuda_error.restype = I
     lib.kime_attn_status_string.argtypes = [I]
@@ -127,6 +131,26 @@ def kime_attn_varlen(qkv, cu_seqlens, max_seqlen, heads, kv_heads, window, causa
                               workspace.numel() * workspace.element_size(), _p(dev_status),
                               _stream(stream, qkv.device))
     _check("kime_attn_varlen", rc)
+    return out
+
+
+def kime_attn_varlen_noalloc(qkv, cu_seqlens, max_seqlen, heads, kv_heads, window, causal, scale,
+                             rope_cos, rope_sin, out=None, dev_status=None, stream=None):
+    """kime_attn_varlen without a caller-provided scratch buffer: for callers
+    that cannot allocate device memory at call time.  The C entry point uses a
+    fixed scratch array built into the library (NOALLOC_SCRATCH_BYTES), shared
+    by all calls -- calls that overlap on the GPU race.  Only `out`, if not
+    given, is allocated here by torch."""
+    lib = load_library()
+    T = qkv.shape[0]
+    n_seqs = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty((T, heads * 64), dtype=qkv.dtype, device=qkv.device)
+    rc = lib.kime_attn_varlen_noalloc(_p(qkv), _dtype_code(qkv), _p(cu_seqlens), n_seqs, T, int(max_seqlen),
+                                      heads, kv_heads, 64, int(window), int(bool(causal)), float(scale),
+                                      _p(rope_cos), _p(rope_sin), rope_cos.shape[0], _p(out), _p(dev_status),
+                                      _stream(stream, qkv.device))
+    _check("kime_attn_varlen_noalloc", rc)
     return out
 
 
