@@ -13,16 +13,19 @@
 // None = -1).  Masked keys are skipped, never written as -inf (ffai-argus
 // src/text.rs, module doc and CausalSoftmax).
 //
-// CTA = 384 threads, one unit = (two consecutive 128-row query tiles A, B of
+// CTA = 512 threads, one unit = (two consecutive 128-row query tiles A, B of
 // one sequence, head h), taken from the device schedule:
-//   warps 0-3   softmax warpgroup A (query tile A = TMEM lanes 0..127)
-//   warps 4-7   softmax warpgroup B (query tile B)
-//   warp 8      TMA producer: Q tiles, then a 3-stage K/V ring
-//   warp 9      MMA issuer (one thread): S = Q K^T and PV = P V, tcgen05.mma
-//   warps 10-11 RoPE of every K tile in shared memory (shared by A and B), and
-//               the V tile's conversion to f16
-// MMA operands are f16 (11-bit significand): q and k are rotated in float32 and
-// rounded once to f16 (q times scale*log2(e) first, so S arrives in log2
+//   warpgroup 0  softmax for query tile A (TMEM lanes 0..127)
+//   warpgroup 1  softmax for query tile B
+//   warpgroup 2  RoPE: rotates the unit's Q tiles (double-buffered per unit)
+//                and every K tile in shared memory, converts each V tile;
+//                thread r owns row r of a tile
+//   warpgroup 3  warp 12: TMA producer (Q tiles, 3-stage K/V ring);
+//                warp 13: MMA issuer (one thread, tcgen05.mma)
+// Registers are rebalanced with setmaxnreg: 168 for the softmax warpgroups,
+// 128 for RoPE, 48 for the producer / MMA warpgroup (sum 512 x 128).
+// MMA operands are f16 (11-bit significand): q and k are rotated in float32
+// and rounded once to f16 (q times scale*log2(e) first, so S arrives in log2
 // units), V is widened from bf16 exactly, P is rounded to f16.  Inputs must
 // stay inside the f16 range (|value| < 65504; conversions saturate).
 // TMEM (512 columns): S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383.
@@ -38,11 +41,11 @@ namespace kime {
 
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kStages = 3;
 constexpr uint32_t kTile = kBM * kHead * 2;  // 16 KB: 128 rows x 128 B
-constexpr uint32_t kOffQ = 0;                // 2 tiles
-constexpr uint32_t kOffK = kOffQ + 2 * kTile;
+constexpr uint32_t kOffQ = 0;                // 2 unit slots x 2 tiles
+constexpr uint32_t kOffK = kOffQ + 4 * kTile;
 constexpr uint32_t kOffV = kOffK + kStages * kTile;
 constexpr uint32_t kOffP = kOffV + kStages * kTile;  // 2 x 32 KB
 constexpr uint32_t kOffBar = kOffP + 4 * kTile;
@@ -50,6 +53,7 @@ constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct UnitInfo {
   int32_t u, s, qt0, nt, kb, ke, row0, L;
@@ -57,8 +61,7 @@ struct UnitInfo {
 
 struct Shared {
   uint64_t unit_full[2], unit_empty[2];
-  uint64_t q_full, q_empty;
-  uint64_t qrot[2];
+  uint64_t q_full[2], q_empty[2], qrot[2];
   uint64_t kv_full[kStages], krot[kStages], kv_empty[kStages];
   uint64_t s_full[2], p_full[2], pv_full[2];
   UnitInfo info[2];
@@ -78,13 +81,33 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// One row's cos/sin table entries (32 + 32 floats), loaded ahead of use.
+struct TableRow {
+  float4 c[8], s[8];
+};
+__device__ __forceinline__ void load_table_row(TableRow& t, const float* __restrict__ c, const float* __restrict__ s) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    t.c[k] = __ldg(reinterpret_cast<const float4*>(c) + k);
+    t.s[k] = __ldg(reinterpret_cast<const float4*>(s) + k);
+  }
+}
+
 // Row r of a 128-byte-swizzled [128 x 64] tile (16-byte chunk k of row r sits
 // at chunk k ^ (r & 7)), bf16 on entry, converted in place to the f16 operand
-// the MMAs read.  rope_row: rotate-half RoPE with table row (c, s) in float32
-// (one rounding per operation), times `mul`, rounded once to f16.
+// the MMAs read.  rope_row: rotate-half RoPE with the row's table entries in
+// float32 (one rounding per operation), times `mul`, rounded once to f16.
 // convert_row: the bf16 values widened and rounded to f16.
-__device__ __forceinline__ void rope_row(uint8_t* tile, int r, const float* __restrict__ c,
-                                         const float* __restrict__ s, float mul) {
+__device__ __forceinline__ void rope_row(uint8_t* tile, int r, const TableRow& tb, float mul) {
   uint8_t* row = tile + r * 128;
   const int sw = r & 7;
 #pragma unroll
@@ -92,10 +115,7 @@ __device__ __forceinline__ void rope_row(uint8_t* tile, int r, const float* __re
     uint4* plo = reinterpret_cast<uint4*>(row + ((k ^ sw) << 4));
     uint4* phi = reinterpret_cast<uint4*>(row + (((k + 4) ^ sw) << 4));
     const uint4 a = *plo, b = *phi;
-    const float4 c0 = __ldg(reinterpret_cast<const float4*>(c + 8 * k));
-    const float4 c1 = __ldg(reinterpret_cast<const float4*>(c + 8 * k + 4));
-    const float4 s0 = __ldg(reinterpret_cast<const float4*>(s + 8 * k));
-    const float4 s1 = __ldg(reinterpret_cast<const float4*>(s + 8 * k + 4));
+    const float4 c0 = tb.c[2 * k], c1 = tb.c[2 * k + 1], s0 = tb.s[2 * k], s1 = tb.s[2 * k + 1];
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
     const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
@@ -140,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Shared* sh = reinterpret_cast<Shared*>(smem + kOffBar);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
   const int G = p.heads / p.kv_heads;
   const int n_units = p.hdr->n_duos * p.heads;
 
@@ -149,13 +169,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh->unit_full[i], 1);
       mbar_init(&sh->unit_empty[i], 4);  // softmax A, softmax B, MMA, RoPE
+      mbar_init(&sh->q_full[i], 1);
+      mbar_init(&sh->q_empty[i], 1);
       mbar_init(&sh->qrot[i], 1);
       mbar_init(&sh->s_full[i], 1);
       mbar_init(&sh->p_full[i], 1);
       mbar_init(&sh->pv_full[i], 1);
     }
-    mbar_init(&sh->q_full, 1);
-    mbar_init(&sh->q_empty, 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sh->kv_full[i], 1);
       mbar_init(&sh->krot[i], 1);
@@ -184,9 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return false;
   };
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+  if (wg == 3) {
+    regs_dec<48>();
+    if (warp == 12 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
       uint32_t n = 0, c = 0;
       for (;; ++n) {
         const int slot = n & 1;
@@ -202,11 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sh->unit_full[slot]);
         if (inf.u < 0) break;
         const int h = inf.u % p.heads, g = h / G;
-        if (!wait(&sh->q_empty, (n & 1) ^ 1)) break;
-        mbar_arrive_expect_tx(&sh->q_full, inf.nt * kTile);
-        tma_load_2d(smem + kOffQ, &qkv_map, &sh->q_full, h * kHead, inf.row0 + inf.qt0 * kBM);
+        if (!wait(&sh->q_empty[slot], ((n >> 1) & 1) ^ 1)) break;
+        uint8_t* q = smem + kOffQ + slot * 2 * kTile;
+        mbar_arrive_expect_tx(&sh->q_full[slot], inf.nt * kTile);
+        tma_load_2d(q, &qkv_map, &sh->q_full[slot], h * kHead, inf.row0 + inf.qt0 * kBM);
         if (inf.nt == 2)
-          tma_load_2d(smem + kOffQ + kTile, &qkv_map, &sh->q_full, h * kHead, inf.row0 + (inf.qt0 + 1) * kBM);
+          tma_load_2d(q + kTile, &qkv_map, &sh->q_full[slot], h * kHead, inf.row0 + (inf.qt0 + 1) * kBM);
         const int kx = (p.heads + g) * kHead, vx = (p.heads + p.kv_heads + g) * kHead;
         bool ok = true;
         for (int t = inf.kb; t < inf.ke; ++t, ++c) {
@@ -218,31 +240,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
       }
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t n = 0, c = 0, pc[2] = {0, 0}, qr[2] = {0, 0};
-      const uint32_t aq[2] = {smem_u32(smem + kOffQ), smem_u32(smem + kOffQ + kTile)};
+    } else if (warp == 13 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      uint32_t n = 0, c = 0, pc[2] = {0, 0};
       const uint32_t ap[2] = {smem_u32(smem + kOffP), smem_u32(smem + kOffP + 2 * kTile)};
       for (;; ++n) {
         const int slot = n & 1;
         if (!wait(&sh->unit_full[slot], (n >> 1) & 1)) break;
         const UnitInfo inf = sh->info[slot];
         if (inf.u < 0) break;
-        int kb[2], ke[2], fb, fe;
-        tile_ranges(inf.L, inf.qt0, p.causal, p.window, kb[0], ke[0], fb, fe);
-        kb[1] = ke[1] = 0;
-        if (inf.nt == 2) tile_ranges(inf.L, inf.qt0 + 1, p.causal, p.window, kb[1], ke[1], fb, fe);
-        bool ok = true;
-        for (int w = 0; w < inf.nt && ok; ++w) ok = wait(&sh->qrot[w], (qr[w]++) & 1);
+        int kb0, ke0, kb1 = 0, ke1 = 0, fb, fe;
+        tile_ranges(inf.L, inf.qt0, p.causal, p.window, kb0, ke0, fb, fe);
+        if (inf.nt == 2) tile_ranges(inf.L, inf.qt0 + 1, p.causal, p.window, kb1, ke1, fb, fe);
+        const uint32_t aq = smem_u32(smem + kOffQ + slot * 2 * kTile);
+        bool ok = wait(&sh->qrot[slot], (n >> 1) & 1);
+        auto in_range = [&](int w, int t) { return w == 0 ? (t >= kb0 && t < ke0) : (t >= kb1 && t < ke1); };
         auto issue_s = [&](int w, int stage) {
           tc_fence_after();
           const uint32_t bk = smem_u32(smem + kOffK + stage * kTile);
+          const uint32_t aqw = aq + w * kTile;
 #pragma unroll
           for (int ks = 0; ks < kHead / 16; ++ks)
-            tc_mma_ss(tmem + w * 128, sdesc_sw128(aq[w] + ks * 32, 16, 1024), sdesc_sw128(bk + ks * 32, 16, 1024),
+            tc_mma_ss(tmem + w * 128, sdesc_sw128(aqw + ks * 32, 16, 1024), sdesc_sw128(bk + ks * 32, 16, 1024),
                       kIdescS, ks > 0);
           tc_commit(&sh->s_full[w]);
         };
@@ -251,23 +270,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = c % kStages;
           ok = wait(&sh->kv_full[st], (c / kStages) & 1) && wait(&sh->krot[st], (c / kStages) & 1);
           for (int w = 0; ok && w < inf.nt; ++w)
-            if (inf.kb >= kb[w] && inf.kb < ke[w]) issue_s(w, st);
+            if (in_range(w, inf.kb)) issue_s(w, st);
         }
         for (int t = inf.kb; ok && t < inf.ke; ++t, ++c) {
           const int st = c % kStages, st1 = (c + 1) % kStages;
           bool next_ready = false;
           for (int w = 0; ok && w < inf.nt; ++w) {
-            if (t >= kb[w] && t < ke[w]) {
+            if (in_range(w, t)) {
               if (!(ok = wait(&sh->p_full[w], (pc[w]++) & 1))) break;
               tc_fence_after();
               const uint32_t bv = smem_u32(smem + kOffV + st * kTile);
+              const uint32_t acc0 = (w == 0 ? t > kb0 : t > kb1) ? 1u : 0u;
 #pragma unroll
               for (int ks = 0; ks < kBN / 16; ++ks)
                 tc_mma_ss(tmem + 256 + w * 64, sdesc_sw128(ap[w] + (ks >> 2) * kTile + (ks & 3) * 32, 16, 1024),
-                          sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, (ks > 0 || t > kb[w]) ? 1u : 0u);
+                          sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, ks > 0 ? 1u : acc0);
               tc_commit(&sh->pv_full[w]);
             }
-            if (t + 1 < inf.ke && t + 1 >= kb[w] && t + 1 < ke[w]) {
+            if (t + 1 < inf.ke && in_range(w, t + 1)) {
               if (!next_ready) {
                 const uint32_t ph1 = ((c + 1) / kStages) & 1;
                 if (!(ok = wait(&sh->kv_full[st1], ph1) && wait(&sh->krot[st1], ph1))) break;
@@ -277,54 +297,70 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tc_commit(&sh->kv_empty[st]);  // every MMA reading stage st is issued
+          if (t + 1 == inf.ke) tc_commit(&sh->q_empty[slot]);  // the unit's last S is issued
         }
-        tc_commit(&sh->q_empty);
         if (!ok) break;
         mbar_arrive(&sh->unit_empty[slot]);
       }
     }
     __syncwarp();
-  } else if (warp >= 10) {
-    // ------------------------------------------------------------ K RoPE
-    const int r0 = tid - 320;  // 0..63: rows r0 and r0 + 64
+  } else if (wg == 2) {
+    // keeps the 128 registers per thread it was launched with
+    // ------------------------------------------------------------ RoPE
+    const int r = tid - 256;  // row of every tile this thread converts
     uint32_t n = 0, c = 0;
     for (;; ++n) {
       const int slot = n & 1;
       bool ok = wait(&sh->unit_full[slot], (n >> 1) & 1);
-      if (named_bar_or(3, 64, !ok)) break;
+      if (named_bar_or(3, 128, !ok)) break;
       const UnitInfo inf = sh->info[slot];
       if (inf.u < 0) break;
+      // the unit's query tiles: row r of each, at positions q0 + r
+      uint8_t* q = smem + kOffQ + slot * 2 * kTile;
+      TableRow tb;
+      for (int w = 0; w < inf.nt; ++w) {
+        const int i = (inf.qt0 + w) * kBM + r;
+        if (i < inf.L)
+          load_table_row(tb, p.cos_t + static_cast<size_t>(i) * kHalf, p.sin_t + static_cast<size_t>(i) * kHalf);
+        if (w == 0) ok = wait(&sh->q_full[slot], (n >> 1) & 1);
+        if (ok) {
+          if (i < inf.L)
+            rope_row(q + w * kTile, r, tb, p.qmul);
+          else
+            convert_row(q + w * kTile, r);
+        }
+      }
+      fence_proxy_async_smem();
+      if (named_bar_or(3, 128, !ok)) break;
+      if (r == 0) {
+        mbar_arrive(&sh->qrot[slot]);
+        mbar_arrive(&sh->unit_empty[slot]);  // every thread has its copy of the unit
+      }
       for (int t = inf.kb; t < inf.ke; ++t, ++c) {
-        const int st = c % kStages;
+        const int st = c % kStages, j = t * kBN + r;
+        if (j < inf.L)
+          load_table_row(tb, p.cos_t + static_cast<size_t>(j) * kHalf, p.sin_t + static_cast<size_t>(j) * kHalf);
         ok = wait(&sh->kv_full[st], (c / kStages) & 1);
         if (ok) {
-          uint8_t* kt = smem + kOffK + st * kTile;
-          uint8_t* vt = smem + kOffV + st * kTile;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int r = r0 + 64 * half, j = t * kBN + r;
-            if (j < inf.L)
-              rope_row(kt, r, p.cos_t + static_cast<size_t>(j) * kHalf, p.sin_t + static_cast<size_t>(j) * kHalf,
-                       1.f);
-            else
-              convert_row(kt, r);
-            convert_row(vt, r);
-          }
+          if (j < inf.L)
+            rope_row(smem + kOffK + st * kTile, r, tb, 1.f);
+          else
+            convert_row(smem + kOffK + st * kTile, r);
+          convert_row(smem + kOffV + st * kTile, r);
           fence_proxy_async_smem();
         }
-        if (named_bar_or(3, 64, !ok)) { ok = false; break; }
-        if (r0 == 0) mbar_arrive(&sh->krot[st]);
+        if (named_bar_or(3, 128, !ok)) { ok = false; break; }
+        if (r == 0) mbar_arrive(&sh->krot[st]);
       }
       if (!ok) break;
-      if (r0 == 0) mbar_arrive(&sh->unit_empty[slot]);
     }
-  } else if (warp < 8) {
+  } else {
+    regs_inc<168>();
     // ------------------------------------------------------------ softmax warpgroups
-    const int w = warp >> 2;           // 0: tile A, 1: tile B
+    const int w = wg;                  // 0: tile A, 1: tile B
     const int r = tid & 127;           // row in the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + w * 128 + lane_off, tO = tmem + 256 + w * 64 + lane_off;
-    uint8_t* sQ = smem + kOffQ + w * kTile;
     uint8_t* sP = smem + kOffP + w * 2 * kTile;
     uint32_t n = 0, sc = 0, pvc = 0;
     for (;; ++n) {
@@ -332,32 +368,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = wait(&sh->unit_full[slot], (n >> 1) & 1);
       if (named_bar_or(1 + w, 128, !ok)) break;
       const UnitInfo inf = sh->info[slot];
+      named_bar_or(1 + w, 128, false);  // every thread has its copy of the unit
+      if (r == 0 && inf.u >= 0) mbar_arrive(&sh->unit_empty[slot]);
       if (inf.u < 0) break;
-      if (w >= inf.nt) {  // no partner tile in this unit
-        named_bar_or(1 + w, 128, false);
-        if (r == 0) mbar_arrive(&sh->unit_empty[slot]);
-        continue;
-      }
+      if (w >= inf.nt) continue;  // no partner tile in this unit
       const int h = inf.u % p.heads;
       const int qt = inf.qt0 + w, q0 = qt * kBM, i = q0 + r;
       const bool row_ok = i < inf.L;
       int kb, ke, fb, fe;
       tile_ranges(inf.L, qt, p.causal, p.window, kb, ke, fb, fe);
-
-      ok = wait(&sh->q_full, n & 1);
-      if (ok) {
-        if (row_ok)
-          rope_row(sQ, r, p.cos_t + static_cast<size_t>(i) * kHalf, p.sin_t + static_cast<size_t>(i) * kHalf,
-                   p.qmul);
-        else
-          convert_row(sQ, r);
-      }
-      fence_proxy_async_smem();
-      if (named_bar_or(1 + w, 128, !ok)) break;
-      if (r == 0) {
-        mbar_arrive(&sh->qrot[w]);
-        mbar_arrive(&sh->unit_empty[slot]);  // every thread has its copy of the unit
-      }
 
       // Online softmax with a lazily moved reference max: P = 2^(S - m_ref) and
       // O (in TMEM, accumulated by the PV MMAs) stay relative to m_ref, which
@@ -461,8 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar, 1);
     };
     for (int i = 0; i < kStages; ++i) settle(&sh->kv_full[i]);
-    settle(&sh->q_full);
     for (int i = 0; i < 2; ++i) {
+      settle(&sh->q_full[i]);
       settle(&sh->s_full[i]);
       settle(&sh->pv_full[i]);
     }
