@@ -37,6 +37,27 @@
 // shared memory.  Every wait is bounded; on a timeout every role winds down.
 #include "kime_common.cuh"
 
+// Phase profiler, compiled in only with -DKIME_PHASE_PROFILE: each role's
+// first thread charges clock64() time to numbered phases and adds its totals
+// to g_kime_phase at the end.  Normal builds expand every PHASE_* to nothing.
+#ifdef KIME_PHASE_PROFILE
+__device__ unsigned long long g_kime_phase[64];
+#define PHASE_DECL unsigned long long ph_t0 = clock64(), ph_acc[12] = {0}
+#define PHASE(k)                              \
+  {                                           \
+    const unsigned long long now_ = clock64(); \
+    ph_acc[k] += now_ - ph_t0;                 \
+    ph_t0 = now_;                              \
+  }
+#define PHASE_FLUSH(base, cond) \
+  if (cond)                     \
+    for (int q_ = 0; q_ < 12; ++q_) atomicAdd(&g_kime_phase[(base) + q_], ph_acc[q_])
+#else
+#define PHASE_DECL
+#define PHASE(k)
+#define PHASE_FLUSH(base, cond)
+#endif
+
 namespace kime {
 
 namespace {
@@ -209,10 +230,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       uint32_t n = 0, c = 0;
+      PHASE_DECL;
       for (;; ++n) {
         const int slot = n & 1;
         const int u = atomicAdd(&p.hdr->next_duo, 1);
+        PHASE(3);
         if (!wait(&sh->unit_empty[slot], ((n >> 1) & 1) ^ 1)) break;
+        PHASE(0);
         UnitInfo inf;
         inf.u = u < n_units ? u : -1;
         if (inf.u >= 0) {
@@ -223,7 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sh->unit_full[slot]);
         if (inf.u < 0) break;
         const int h = inf.u % p.heads, g = h / G;
+        PHASE(3);
         if (!wait(&sh->q_empty[slot], ((n >> 1) & 1) ^ 1)) break;
+        PHASE(1);
         uint8_t* q = smem + kOffQ + slot * 2 * kTile;
         mbar_arrive_expect_tx(&sh->q_full[slot], inf.nt * kTile);
         tma_load_2d(q, &qkv_map, &sh->q_full[slot], h * kHead, inf.row0 + inf.qt0 * kBM);
@@ -233,27 +259,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int t = inf.kb; t < inf.ke; ++t, ++c) {
           const int st = c % kStages;
+          PHASE(3);
           if (!wait(&sh->kv_empty[st], ((c / kStages) & 1) ^ 1)) { ok = false; break; }
+          PHASE(2);
           mbar_arrive_expect_tx(&sh->kv_full[st], 2 * kTile);
           tma_load_2d(smem + kOffK + st * kTile, &qkv_map, &sh->kv_full[st], kx, inf.row0 + t * kBN);
           tma_load_2d(smem + kOffV + st * kTile, &qkv_map, &sh->kv_full[st], vx, inf.row0 + t * kBN);
         }
         if (!ok) break;
       }
+      PHASE_FLUSH(48, true);
     } else if (warp == 13 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       uint32_t n = 0, c = 0, pc[2] = {0, 0};
       const uint32_t ap[2] = {smem_u32(smem + kOffP), smem_u32(smem + kOffP + 2 * kTile)};
+      PHASE_DECL;
       for (;; ++n) {
         const int slot = n & 1;
+        PHASE(4);
         if (!wait(&sh->unit_full[slot], (n >> 1) & 1)) break;
+        PHASE(0);
         const UnitInfo inf = sh->info[slot];
         if (inf.u < 0) break;
         int kb0, ke0, kb1 = 0, ke1 = 0, fb, fe;
         tile_ranges(inf.L, inf.qt0, p.causal, p.window, kb0, ke0, fb, fe);
         if (inf.nt == 2) tile_ranges(inf.L, inf.qt0 + 1, p.causal, p.window, kb1, ke1, fb, fe);
         const uint32_t aq = smem_u32(smem + kOffQ + slot * 2 * kTile);
+        PHASE(4);
         bool ok = wait(&sh->qrot[slot], (n >> 1) & 1);
+        PHASE(1);
         auto in_range = [&](int w, int t) { return w == 0 ? (t >= kb0 && t < ke0) : (t >= kb1 && t < ke1); };
         auto issue_s = [&](int w, int stage) {
           tc_fence_after();
@@ -269,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           const int st = c % kStages;
           ok = wait(&sh->kv_full[st], (c / kStages) & 1) && wait(&sh->krot[st], (c / kStages) & 1);
+          PHASE(2);
           for (int w = 0; ok && w < inf.nt; ++w)
             if (in_range(w, inf.kb)) issue_s(w, st);
         }
@@ -277,7 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool next_ready = false;
           for (int w = 0; ok && w < inf.nt; ++w) {
             if (in_range(w, t)) {
+              PHASE(4);
               if (!(ok = wait(&sh->p_full[w], (pc[w]++) & 1))) break;
+              PHASE(3);
               tc_fence_after();
               const uint32_t bv = smem_u32(smem + kOffV + st * kTile);
               const uint32_t acc0 = (w == 0 ? t > kb0 : t > kb1) ? 1u : 0u;
@@ -290,7 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t + 1 < inf.ke && in_range(w, t + 1)) {
               if (!next_ready) {
                 const uint32_t ph1 = ((c + 1) / kStages) & 1;
+                PHASE(4);
                 if (!(ok = wait(&sh->kv_full[st1], ph1) && wait(&sh->krot[st1], ph1))) break;
+                PHASE(2);
                 next_ready = true;
               }
               issue_s(w, st1);
@@ -302,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         mbar_arrive(&sh->unit_empty[slot]);
       }
+      PHASE_FLUSH(40, true);
     }
     __syncwarp();
   } else if (wg == 2) {
@@ -309,10 +349,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ RoPE
     const int r = tid - 256;  // row of every tile this thread converts
     uint32_t n = 0, c = 0;
+    PHASE_DECL;
     for (;; ++n) {
       const int slot = n & 1;
       bool ok = wait(&sh->unit_full[slot], (n >> 1) & 1);
       if (named_bar_or(3, 128, !ok)) break;
+      PHASE(0);
       const UnitInfo inf = sh->info[slot];
       if (inf.u < 0) break;
       // the unit's query tiles: row r of each, at positions q0 + r
@@ -332,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       if (named_bar_or(3, 128, !ok)) break;
+      PHASE(1);
       if (r == 0) {
         mbar_arrive(&sh->qrot[slot]);
         mbar_arrive(&sh->unit_empty[slot]);  // every thread has its copy of the unit
@@ -340,7 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = c % kStages, j = t * kBN + r;
         if (j < inf.L)
           load_table_row(tb, p.cos_t + static_cast<size_t>(j) * kHalf, p.sin_t + static_cast<size_t>(j) * kHalf);
+        PHASE(2);
         ok = wait(&sh->kv_full[st], (c / kStages) & 1);
+        PHASE(3);
         if (ok) {
           if (j < inf.L)
             rope_row(smem + kOffK + st * kTile, r, tb, 1.f);
@@ -349,11 +394,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           convert_row(smem + kOffV + st * kTile, r);
           fence_proxy_async_smem();
         }
+        PHASE(4);
         if (named_bar_or(3, 128, !ok)) { ok = false; break; }
         if (r == 0) mbar_arrive(&sh->krot[st]);
+        PHASE(5);
       }
       if (!ok) break;
     }
+    PHASE_FLUSH(32, r == 0);
   } else {
     regs_inc<168>();
     // ------------------------------------------------------------ softmax warpgroups
@@ -363,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + w * 128 + lane_off, tO = tmem + 256 + w * 64 + lane_off;
     uint8_t* sP = smem + kOffP + w * 2 * kTile;
     uint32_t n = 0, sc = 0, pvc = 0;
+    PHASE_DECL;
     for (;; ++n) {
       const int slot = n & 1;
       bool ok = wait(&sh->unit_full[slot], (n >> 1) & 1);
@@ -385,10 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref = -INFINITY, l = 0.f;
       for (int t = kb; t < ke; ++t) {
         const int k0 = t * kBN;
+        PHASE(7);
         ok = wait(&sh->s_full[w], (sc++) & 1);
         tc_fence_after();
+        PHASE(0);
         uint32_t v[128];
         tmem_ld128_wait(tS, v);
+        PHASE(1);
         float x[128];
 #pragma unroll
         for (int j = 0; j < kBN; ++j) x[j] = __uint_as_float(v[j]);
@@ -415,12 +467,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (m_ref != -INFINITY) alpha = fast_exp2(m_ref - mx);
           m_ref = mx;
         }
+        PHASE(2);
         // PV of the previous tile must be done before P is overwritten (it read
         // the P buffer) and before O is rescaled (it accumulated into O).
         if (t > kb) {
           ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
           tc_fence_after();
         }
+        PHASE(3);
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         float rowsum = 0.f;
 #pragma unroll
@@ -436,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(pw[0], pw[1], pw[2], pw[3]);
         }
         l = l * alpha + rowsum;
+        PHASE(4);
         if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {
           uint32_t ov[64];
           tmem_ld64_wait(tO, ov);
@@ -443,10 +498,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int d = 0; d < kHead; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
           tmem_st64_wait(tO, ov);
         }
+        PHASE(5);
         fence_proxy_async_smem();
         tc_fence_before();
         if (named_bar_or(1 + w, 128, !ok)) { ok = false; break; }
         if (r == 0) mbar_arrive(&sh->p_full[w]);
+        PHASE(6);
       }
       if (!ok) break;
       ok = wait(&sh->pv_full[w], (pvc++) & 1);
@@ -468,7 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(dst + d) = wv;
         }
       }
+      PHASE(8);
     }
+    PHASE_FLUSH(16 * w, r == 0);
   }
 
   // Wind down: after an abort, give copies and MMAs still in flight a bounded
@@ -495,6 +554,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
+
+#ifdef KIME_PHASE_PROFILE
+extern "C" int kime_debug_phase_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_kime_phase, sizeof(g_kime_phase));
+}
+extern "C" int kime_debug_phase_clear() {
+  unsigned long long z[64] = {0};
+  return cudaMemcpyToSymbol(g_kime_phase, z, sizeof(z));
+}
+#endif
 
 cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, int n_seqs, int total, int heads, int kv_heads,
                               int window, int causal, float scale, const float* cos_t, const float* sin_t, void* out,
