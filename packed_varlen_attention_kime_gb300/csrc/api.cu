@@ -135,7 +135,9 @@ int kime_attn_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int he
   if (!(scale > 0.f) || !isfinite(scale)) return KIME_EINVAL;
   if (n_seqs == 0) return KIME_OK;
   if (!qkv_new || !pos || !rope_cos || !rope_sin || !k_cache || !v_cache || !out || !workspace) return KIME_EINVAL;
-  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace) || !aligned16(out)) return KIME_EINVAL;
+  if (!aligned16(qkv_new) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(workspace) || !aligned16(out) ||
+      !aligned16(rope_cos) || !aligned16(rope_sin))
+    return KIME_EINVAL;
   if (n_seqs > 65535) return KIME_ERANGE;
   if (workspace_bytes < kime::decode_workspace_bytes(n_seqs, heads, kv_heads, cap)) return KIME_ERANGE;
   return cuda_status(kime::launch_decode(qkv_new, pos, n_seqs, heads, kv_heads, cap, scale, rope_cos, rope_sin,

@@ -11,12 +11,14 @@
 // head h / (heads/kv_heads), all heads of one kv group together (the GQA fold
 // of TextTower::block: the cache is never expanded per q head).
 //
-// Split-KV: one CTA per (key chunk of 256, kv head, sequence).  The chunk's K
-// and V rows arrive by two 1-D bulk copies into shared memory; 8 threads share
-// a key (8 dims each), so scores need a 3-step shuffle reduction.  Each CTA
-// reduces its chunk to (m, l, o[64]) per q head (base-2 logits); the last CTA
-// of a (sequence, kv head) to finish -- found with an atomic ticket, no waiting
-// -- merges the chunks: m = max m_c, l = sum l_c 2^(m_c-m), o = sum o_c 2^(m_c-m) / l.
+// Split-KV: one CTA per (chunk of 128 keys, kv head, sequence); CTAs of
+// chunks past pos[s] exit at once.  A chunk's K and V rows arrive by two 1-D
+// bulk copies into shared memory while the CTA rotates its q.  8 threads share
+// a key (8 dims each), so scores need a 3-step shuffle reduction; all G q heads
+// of the kv group are done together.  Each CTA reduces its chunk to
+// (m, l, o[64]) per q head (base-2 logits); the last CTA of a (sequence, kv
+// head) to finish -- found with an atomic ticket, no waiting -- merges the
+// chunks: m = max m_c, l = sum l_c 2^(m_c-m), o = sum o_c 2^(m_c-m) / l.
 #include "kime_common.cuh"
 
 namespace kime {
@@ -25,10 +27,16 @@ namespace {
 
 constexpr int kAppendThreads = 128;
 constexpr int kDecThreads = 128;
-constexpr int kGroups = kDecThreads / 8;        // keys processed at once
+constexpr int kGroups = kDecThreads / 8;        // keys processed at once (8 threads per key)
+constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kKeysPerThread = kDecChunk / kGroups;
+constexpr uint32_t kStageBytes = 2 * kDecChunk * kHead * 2;  // K and V of one chunk
 constexpr int kPartialFloats = 68;               // m, l, o[64], 2 pad
-constexpr uint32_t kDecSmem = 2 * kDecChunk * kHead * 2 + 64;
+
+template <int G>
+constexpr uint32_t dec_smem_bytes() {
+  return kStageBytes + ((kDecWarps * G * kHead + 2 * kDecWarps * G) * 4 + 15) / 16 * 16 + 8;
+}
 
 __global__ void __launch_bounds__(kAppendThreads)
     kv_append_kernel(const uint16_t* __restrict__ qkv_new, const int32_t* __restrict__ pos, int heads,
@@ -64,189 +72,256 @@ __global__ void __launch_bounds__(kAppendThreads)
 
 template <int G>
 __global__ void __launch_bounds__(kDecThreads)
-    decode_kernel(const uint16_t* __restrict__ qkv_new, const int32_t* __restrict__ pos, int heads, int kv_heads,
-                  int cap, float scale_log2, const float* __restrict__ cos_t, const float* __restrict__ sin_t,
-                  int rope_len, const uint16_t* __restrict__ k_cache, const uint16_t* __restrict__ v_cache,
-                  __nv_bfloat16* __restrict__ out, float* __restrict__ partials, int32_t* __restrict__ tickets,
-                  int max_chunks, int32_t* dev_status) {
+    decode_kernel(const uint16_t* __restrict__ qkv_new, const int32_t* __restrict__ pos, int n_seqs, int heads,
+                  int kv_heads, int cap, float scale_log2, const float* __restrict__ cos_t,
+                  const float* __restrict__ sin_t, int rope_len, const uint16_t* __restrict__ k_cache,
+                  const uint16_t* __restrict__ v_cache, __nv_bfloat16* __restrict__ out,
+                  float* __restrict__ partials, int32_t* __restrict__ tickets, int max_chunks, int32_t* dev_status) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint16_t* Ks = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* Vs = Ks + kDecChunk * kHead;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + 2 * kDecChunk * kHead * 2);
+  // [K | V of the chunk][merge buffers][mbarrier]
+  float* red_o = reinterpret_cast<float*>(smem + kStageBytes);  // [warps][G][64]
+  float* red_m = red_o + kDecWarps * G * kHead;                  // [warps][G]
+  float* red_l = red_m + kDecWarps * G;                          // [warps][G]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kStageBytes +
+                                              ((kDecWarps * G * kHead + 2 * kDecWarps * G) * 4 + 15) / 16 * 16);
   __shared__ int s_last;
+  (void)n_seqs;
 
   const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
-  const int tid = threadIdx.x;
-  const int P = pos[s];
+  const int tid = threadIdx.x, lane8 = tid & 7, grp = tid >> 3, d0 = lane8 * 8;
+  const size_t W = static_cast<size_t>(kHead) * (heads + 2 * kv_heads);
+  const int P = __ldg(pos + s);
   if (P < 0 || P >= cap || P >= rope_len) {
     if (c == 0 && g == 0 && tid == 0) report(dev_status, ST_BAD_POS);
     return;
   }
-  const int n_keys = P + 1;
-  const int n_c = (n_keys + kDecChunk - 1) / kDecChunk;
+  const int n_c = (P + 1 + kDecChunk - 1) / kDecChunk;
   if (c >= n_c) return;
-  const int j0 = c * kDecChunk;
-  const int nk = min(kDecChunk, n_keys - j0);
-  const size_t base = ((static_cast<size_t>(s) * kv_heads + g) * cap + j0) * kHead;
-
+  const int nk = min(kDecChunk, P + 1 - c * kDecChunk);
+  const int st = 0;
   if (tid == 0) {
+    const size_t base = ((static_cast<size_t>(s) * kv_heads + g) * cap + static_cast<size_t>(c) * kDecChunk) * kHead;
     mbar_init(bar, 1);
     fence_mbar_init();
     mbar_arrive_expect_tx(bar, 2u * nk * kHead * 2);
-    bulk_load(Ks, k_cache + base, nk * kHead * 2, bar);
-    bulk_load(Vs, v_cache + base, nk * kHead * 2, bar);
+    bulk_load(smem, k_cache + base, nk * kHead * 2, bar);
+    bulk_load(smem + kStageBytes / 2, v_cache + base, nk * kHead * 2, bar);
   }
-
-  // q heads of this kv group, RoPE'd at P, this thread's 8 dims, pre-multiplied
-  // by scale * log2(e).
-  const int lane8 = tid & 7, grp = tid >> 3;
-  const int d0 = lane8 * 8;
-  const size_t W = static_cast<size_t>(kHead) * (heads + 2 * kv_heads);
-  float q[G][8];
   {
-    const int tb = d0 & (kHalf - 1);
-    const float* cp = cos_t + static_cast<size_t>(P) * kHalf + tb;
-    const float* sp = sin_t + static_cast<size_t>(P) * kHalf + tb;
+    // q heads of this kv group, RoPE'd at P, this thread's 8 dims, times
+    // scale * log2(e).
+    float q[G][8];
+    {
+      const int tb = d0 & (kHalf - 1);
+      const float4* cp = reinterpret_cast<const float4*>(cos_t + static_cast<size_t>(P) * kHalf + tb);
+      const float4* sp = reinterpret_cast<const float4*>(sin_t + static_cast<size_t>(P) * kHalf + tb);
+      const float4 c0 = __ldg(cp), c1 = __ldg(cp + 1), s0 = __ldg(sp), s1 = __ldg(sp + 1);
+      const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const uint16_t* xq = qkv_new + static_cast<size_t>(s) * W + (g * G + hh) * kHead;
+        const uint4 xa = __ldg(reinterpret_cast<const uint4*>(xq + tb));
+        const uint4 xb = __ldg(reinterpret_cast<const uint4*>(xq + tb + kHalf));
+        const float fa[8] = {bf16lo(xa.x), bf16hi(xa.x), bf16lo(xa.y), bf16hi(xa.y),
+                             bf16lo(xa.z), bf16hi(xa.z), bf16lo(xa.w), bf16hi(xa.w)};
+        const float fb[8] = {bf16lo(xb.x), bf16hi(xb.x), bf16lo(xb.y), bf16hi(xb.y),
+                             bf16lo(xb.z), bf16hi(xb.z), bf16lo(xb.w), bf16hi(xb.w)};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float ya, yb;
+          rope_pair(fa[e], fb[e], cc[e], ss[e], ya, yb);
+          q[hh][e] = (d0 < kHalf ? ya : yb) * scale_log2;
+        }
+      }
+    }
+    __syncthreads();  // the barrier is initialised before anyone waits on it
+    const bool ok = mbar_wait(bar, 0);
+    if (__syncthreads_or(!ok)) {
+      // the copies did not land in time: report, give them one more bounded
+      // wait so the shared memory outlives them, and leave the chunk undone
+      if (tid == 0) {
+        report(dev_status, ST_TIMEOUT);
+        mbar_wait(bar, 0);
+      }
+      return;
+    }
+    const uint16_t* Ks = reinterpret_cast<const uint16_t*>(smem + st * kStageBytes);
+    const uint16_t* Vs = Ks + kDecChunk * kHead;
+
+    // scores of this thread's keys grp, grp + 16, ...
+    float sc[G][kKeysPerThread];
+#pragma unroll
+    for (int k = 0; k < kKeysPerThread; ++k) {
+      const int kk = grp + k * kGroups;
+      float part[G];
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) part[hh] = 0.f;
+      if (kk < nk) {
+        const uint4 kw = *reinterpret_cast<const uint4*>(Ks + kk * kHead + d0);
+        const float kf[8] = {bf16lo(kw.x), bf16hi(kw.x), bf16lo(kw.y), bf16hi(kw.y),
+                             bf16lo(kw.z), bf16hi(kw.z), bf16lo(kw.w), bf16hi(kw.w)};
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) part[hh] = fmaf(q[hh][e], kf[e], part[hh]);
+      }
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        float v = part[hh];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        sc[hh][k] = kk < nk ? v : -INFINITY;
+      }
+    }
+    float m[G], l[G], o[G][8];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
-      const uint16_t* xq = qkv_new + static_cast<size_t>(s) * W + (g * G + hh) * kHead;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kKeysPerThread; ++k) mx = fmaxf(mx, sc[hh][k]);
+      m[hh] = mx;
+      l[hh] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[hh][e] = 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kKeysPerThread; ++k) {
+      const int kk = grp + k * kGroups;
+      if (kk >= nk) continue;
+      const uint4 vw = *reinterpret_cast<const uint4*>(Vs + kk * kHead + d0);
+      const float vf[8] = {bf16lo(vw.x), bf16hi(vw.x), bf16lo(vw.y), bf16hi(vw.y),
+                           bf16lo(vw.z), bf16hi(vw.z), bf16lo(vw.w), bf16hi(vw.w)};
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const float pr = fast_exp2(sc[hh][k] - m[hh]);
+        l[hh] += pr;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[hh][e] = fmaf(pr, vf[e], o[hh][e]);
+      }
+    }
+    // merge the 16 key groups of this chunk: the 4 groups of a warp by
+    // shuffles, then the 4 warps through shared memory
+    const int wid = tid >> 5;
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      float mw = fmaxf(m[hh], __shfl_xor_sync(0xffffffffu, m[hh], 8));
+      mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 16));
+      const float wgt = m[hh] == -INFINITY ? 0.f : fast_exp2(m[hh] - mw);
+      float lw = l[hh] * wgt;
+      lw += __shfl_xor_sync(0xffffffffu, lw, 8);
+      lw += __shfl_xor_sync(0xffffffffu, lw, 16);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const int t = tb + e;
-        const float a = __uint_as_float(static_cast<uint32_t>(xq[t]) << 16);
-        const float b = __uint_as_float(static_cast<uint32_t>(xq[t + kHalf]) << 16);
-        float ya, yb;
-        rope_pair(a, b, cp[e], sp[e], ya, yb);
-        q[hh][e] = (d0 < kHalf ? ya : yb) * scale_log2;
+        float ov = o[hh][e] * wgt;
+        ov += __shfl_xor_sync(0xffffffffu, ov, 8);
+        ov += __shfl_xor_sync(0xffffffffu, ov, 16);
+        o[hh][e] = ov;
+      }
+      if ((tid & 31) < 8) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) red_o[(wid * G + hh) * kHead + d0 + e] = o[hh][e];
+        if (lane8 == 0) {
+          red_m[wid * G + hh] = mw;
+          red_l[wid * G + hh] = lw;
+        }
       }
     }
-  }
-  __syncthreads();  // barrier initialised before anyone waits on it
-  const bool ok = mbar_wait(bar, 0);
-  if (__syncthreads_or(!ok)) {
-    // The copies did not land in time: report, give them one more bounded
-    // wait so the shared memory outlives them, and leave the chunk undone.
-    if (tid == 0) {
-      report(dev_status, ST_TIMEOUT);
-      mbar_wait(bar, 0);
-    }
-    return;
-  }
-
-  // Scores of this thread's keys (grp, grp + 16, ...).
-  float sc[G][kKeysPerThread];
+    __syncthreads();
+    const bool single = n_c == 1;
+    float* part = partials + ((static_cast<size_t>(s) * kv_heads + g) * max_chunks + c) * G * kPartialFloats;
+    for (int e = tid; e < G * kHead; e += kDecThreads) {
+      const int hh = e / kHead, d = e % kHead;
+      float M = -INFINITY;
 #pragma unroll
-  for (int it = 0; it < kKeysPerThread; ++it) {
-    const int kk = grp + it * kGroups;
-    float part[G];
+      for (int wv = 0; wv < kDecWarps; ++wv) M = fmaxf(M, red_m[wv * G + hh]);
+      float Lsum = 0.f, O = 0.f;
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) part[hh] = 0.f;
-    if (kk < nk) {
-      const uint4 kw = *reinterpret_cast<const uint4*>(Ks + kk * kHead + d0);
-      const float kf[8] = {bf16lo(kw.x), bf16hi(kw.x), bf16lo(kw.y), bf16hi(kw.y),
-                           bf16lo(kw.z), bf16hi(kw.z), bf16lo(kw.w), bf16hi(kw.w)};
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) part[hh] = fmaf(q[hh][e], kf[e], part[hh]);
-    }
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      float v = part[hh];
-      v += __shfl_xor_sync(0xffffffffu, v, 1);
-      v += __shfl_xor_sync(0xffffffffu, v, 2);
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      sc[hh][it] = kk < nk ? v : -INFINITY;
-    }
-  }
-  float m[G], l[G], o[G][8];
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh) {
-    float mx = -INFINITY;
-#pragma unroll
-    for (int it = 0; it < kKeysPerThread; ++it) mx = fmaxf(mx, sc[hh][it]);
-    m[hh] = mx;
-    l[hh] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) o[hh][e] = 0.f;
-  }
-#pragma unroll
-  for (int it = 0; it < kKeysPerThread; ++it) {
-    const int kk = grp + it * kGroups;
-    if (kk >= nk) continue;
-    const uint4 vw = *reinterpret_cast<const uint4*>(Vs + kk * kHead + d0);
-    const float vf[8] = {bf16lo(vw.x), bf16hi(vw.x), bf16lo(vw.y), bf16hi(vw.y),
-                         bf16lo(vw.z), bf16hi(vw.z), bf16lo(vw.w), bf16hi(vw.w)};
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      const float p = fast_exp2(sc[hh][it] - m[hh]);
-      l[hh] += p;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[hh][e] = fmaf(p, vf[e], o[hh][e]);
-    }
-  }
-  __syncthreads();  // K/V consumed; reuse the K area for the cross-group merge
-
-  float* red_o = reinterpret_cast<float*>(smem);          // [kGroups][G][64]
-  float* red_m = red_o + kGroups * G * kHead;             // [kGroups][G]
-  float* red_l = red_m + kGroups * G;                     // [kGroups][G]
-#pragma unroll
-  for (int hh = 0; hh < G; ++hh) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) red_o[(grp * G + hh) * kHead + d0 + e] = o[hh][e];
-    if (lane8 == 0) {
-      red_m[grp * G + hh] = m[hh];
-      red_l[grp * G + hh] = l[hh];
-    }
-  }
-  __syncthreads();
-
-  const bool single = n_c == 1;
-  float* part = partials + ((static_cast<size_t>(s) * kv_heads + g) * max_chunks + c) * G * kPartialFloats;
-  for (int e = tid; e < G * kHead; e += kDecThreads) {
-    const int hh = e / kHead, d = e % kHead;
-    float M = -INFINITY;
-#pragma unroll
-    for (int gr = 0; gr < kGroups; ++gr) M = fmaxf(M, red_m[gr * G + hh]);
-    float Lsum = 0.f, O = 0.f;
-#pragma unroll
-    for (int gr = 0; gr < kGroups; ++gr) {
-      const float w = fast_exp2(red_m[gr * G + hh] - M);
-      Lsum = fmaf(red_l[gr * G + hh], w, Lsum);
-      O = fmaf(red_o[(gr * G + hh) * kHead + d], w, O);
-    }
-    if (single) {
-      out[static_cast<size_t>(s) * heads * kHead + (g * G + hh) * kHead + d] = __float2bfloat16_rn(O / Lsum);
-    } else {
-      part[hh * kPartialFloats + 2 + d] = O;
-      if (d == 0) {
-        part[hh * kPartialFloats] = M;
-        part[hh * kPartialFloats + 1] = Lsum;
+      for (int wv = 0; wv < kDecWarps; ++wv) {
+        const float wgt = red_m[wv * G + hh] == -INFINITY ? 0.f : fast_exp2(red_m[wv * G + hh] - M);
+        Lsum = fmaf(red_l[wv * G + hh], wgt, Lsum);
+        O = fmaf(red_o[(wv * G + hh) * kHead + d], wgt, O);
+      }
+      if (single) {
+        out[static_cast<size_t>(s) * heads * kHead + (g * G + hh) * kHead + d] = __float2bfloat16_rn(O / Lsum);
+      } else {
+        part[hh * kPartialFloats + 2 + d] = O;
+        if (d == 0) {
+          part[hh * kPartialFloats] = M;
+          part[hh * kPartialFloats + 1] = Lsum;
+        }
       }
     }
-  }
-  if (single) return;
-
-  // Publish this chunk; the last CTA of (s, g) to arrive merges all chunks.
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&tickets[s * kv_heads + g], 1) == n_c - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const float* all = partials + (static_cast<size_t>(s) * kv_heads + g) * max_chunks * G * kPartialFloats;
-  for (int e = tid; e < G * kHead; e += kDecThreads) {
-    const int hh = e / kHead, d = e % kHead;
-    float M = -INFINITY;
-    for (int cc = 0; cc < n_c; ++cc) M = fmaxf(M, __ldcg(all + (cc * G + hh) * kPartialFloats));
-    float Lsum = 0.f, O = 0.f;
-    for (int cc = 0; cc < n_c; ++cc) {
-      const float* pc = all + (cc * G + hh) * kPartialFloats;
-      const float w = fast_exp2(__ldcg(pc) - M);
-      Lsum = fmaf(__ldcg(pc + 1), w, Lsum);
-      O = fmaf(__ldcg(pc + 2 + d), w, O);
+    if (!single) {
+      // publish this chunk; the last CTA of (s, g) to arrive merges all chunks
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) s_last = atomicAdd(&tickets[s * kv_heads + g], 1) == n_c - 1;
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        // Merge in the consumed stage buffer: per-head max of m over the
+        // chunks (strided over threads, then reduced), then blocks of chunk
+        // weights 2^(m_c - M) in shared memory; every output sums its column
+        // over the chunks with independent loads.
+        const float* all = partials + (static_cast<size_t>(s) * kv_heads + g) * max_chunks * G * kPartialFloats;
+        float* red = reinterpret_cast<float*>(smem + st * kStageBytes);  // [G][threads]
+        float* hdr = red + G * kDecThreads;                               // [G] M, [G] L
+        float* wts = hdr + 2 * G;                                         // [block][G]
+        constexpr int kBlock = (kStageBytes / 4 - (kDecThreads + 2) * G) / G;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          float M = -INFINITY;
+          for (int cc = tid; cc < n_c; cc += kDecThreads) M = fmaxf(M, __ldcg(all + (cc * G + hh) * kPartialFloats));
+          red[hh * kDecThreads + tid] = M;
+        }
+        __syncthreads();
+        if (tid < G) {
+          float M = -INFINITY;
+          for (int k = 0; k < kDecThreads; ++k) M = fmaxf(M, red[tid * kDecThreads + k]);
+          hdr[tid] = M;
+          hdr[G + tid] = 0.f;
+        }
+        float O[(G * kHead + kDecThreads - 1) / kDecThreads];
+#pragma unroll
+        for (int k = 0; k < (G * kHead + kDecThreads - 1) / kDecThreads; ++k) O[k] = 0.f;
+        for (int c0 = 0; c0 < n_c; c0 += kBlock) {
+          const int nb = min(kBlock, n_c - c0);
+          __syncthreads();
+          for (int e = tid; e < nb * G; e += kDecThreads)
+            wts[e] = fast_exp2(__ldcg(all + (c0 * G + e) * kPartialFloats) - hdr[e % G]);
+          __syncthreads();
+          if (tid < G) {
+            float Lsum = hdr[G + tid];
+            for (int cc = 0; cc < nb; ++cc)
+              Lsum = fmaf(__ldcg(all + ((c0 + cc) * G + tid) * kPartialFloats + 1), wts[cc * G + tid], Lsum);
+            hdr[G + tid] = Lsum;
+          }
+#pragma unroll
+          for (int k = 0; k < (G * kHead + kDecThreads - 1) / kDecThreads; ++k) {
+            const int e = tid + k * kDecThreads;
+            if (e < G * kHead) {
+              const int hh = e / kHead, d = e % kHead;
+              float acc = O[k];
+#pragma unroll 8
+              for (int cc = 0; cc < nb; ++cc)
+                acc = fmaf(__ldcg(all + ((c0 + cc) * G + hh) * kPartialFloats + 2 + d), wts[cc * G + hh], acc);
+              O[k] = acc;
+            }
+          }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < (G * kHead + kDecThreads - 1) / kDecThreads; ++k) {
+          const int e = tid + k * kDecThreads;
+          if (e < G * kHead) {
+            const int hh = e / kHead, d = e % kHead;
+            out[static_cast<size_t>(s) * heads * kHead + (g * G + hh) * kHead + d] = __float2bfloat16_rn(O[k] / hdr[G + hh]);
+          }
+        }
+      }
     }
-    out[static_cast<size_t>(s) * heads * kHead + (g * G + hh) * kHead + d] = __float2bfloat16_rn(O / Lsum);
   }
 }
 
@@ -257,8 +332,9 @@ cudaError_t launch_decode_g(const void* qkv_new, const int32_t* pos, int n_seqs,
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
+  constexpr uint32_t smem = dec_smem_bytes<G>();
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
@@ -269,9 +345,9 @@ cudaError_t launch_decode_g(const void* qkv_new, const int32_t* pos, int n_seqs,
   cudaError_t e = cudaMemsetAsync(tickets, 0, static_cast<size_t>(n_seqs) * kv_heads * 4, st);
   if (e != cudaSuccess) return e;
   dim3 grid(max_chunks, kv_heads, n_seqs);
-  decode_kernel<G><<<grid, kDecThreads, kDecSmem, st>>>(
-      static_cast<const uint16_t*>(qkv_new), pos, heads, kv_heads, cap, scale * 1.4426950408889634f, cos_t, sin_t,
-      rope_len, static_cast<const uint16_t*>(k_cache), static_cast<const uint16_t*>(v_cache),
+  decode_kernel<G><<<grid, kDecThreads, smem, st>>>(
+      static_cast<const uint16_t*>(qkv_new), pos, n_seqs, heads, kv_heads, cap, scale * 1.4426950408889634f, cos_t,
+      sin_t, rope_len, static_cast<const uint16_t*>(k_cache), static_cast<const uint16_t*>(v_cache),
       static_cast<__nv_bfloat16*>(out), partials, tickets, max_chunks, dev_status);
   return cudaGetLastError();
 }

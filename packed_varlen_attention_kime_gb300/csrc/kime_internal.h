@@ -12,7 +12,7 @@ constexpr int kHead = 64;       // head_dim; the library supports exactly this
 constexpr int kHalf = 32;       // RoPE pairs per head
 constexpr int kBM = 128;        // query rows per tile
 constexpr int kBN = 128;        // keys per tile
-constexpr int kDecChunk = 256;  // keys per split-KV decode work item
+constexpr int kDecChunk = 128;  // keys per split-KV decode work item
 constexpr int kMaxGroup = 8;    // largest heads/kv_heads the decode path takes
 
 // One (sequence, query tile) of the schedule with its key-tile ranges:

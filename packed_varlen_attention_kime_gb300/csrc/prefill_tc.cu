@@ -20,7 +20,7 @@
 //   warpgroup 2  RoPE: rotates the unit's Q tiles (double-buffered per unit)
 //                and every K tile in shared memory, converts each V tile;
 //                thread r owns row r of a tile
-//   warpgroup 3  warp 12: TMA producer (Q tiles, 3-stage K/V ring);
+//   warpgroup 3  warp 12: TMA producer (Q tiles, 4-stage K/V ring);
 //                warp 13: MMA issuer (one thread, tcgen05.mma)
 // Registers are rebalanced with setmaxnreg: 168 for the softmax warpgroups,
 // 128 for RoPE, 48 for the producer / MMA warpgroup (sum 512 x 128).
@@ -28,13 +28,16 @@
 // and rounded once to f16 (q times scale*log2(e) first, so S arrives in log2
 // units), V is widened from bf16 exactly, P is rounded to f16.  Inputs must
 // stay inside the f16 range (|value| < 65504; conversions saturate).
-// TMEM (512 columns): S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383.
+// TMEM (512 columns): S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383,
+// P_A 384..447, P_B 448..511 (f16 P, two per 32-bit column).
 // Per key tile t the MMA thread issues PV_A(t), S_A(t+1), PV_B(t), S_B(t+1),
-// so one warpgroup's softmax overlaps the other's MMAs.  The PV MMAs accumulate
-// O in TMEM.  A softmax warpgroup reads S(t) once, takes P(t) = 2^(S - m_ref)
-// against a reference max that moves only when exceeded by more than 2^8
-// (then O is rescaled in TMEM), and writes P(t) (f16, swizzled K-major) to
-// shared memory.  Every wait is bounded; on a timeout every role winds down.
+// so one warpgroup's softmax overlaps the other's MMAs.  The PV MMAs take P
+// from TMEM (A operand) and V from shared memory, and accumulate O in TMEM.  A
+// softmax warpgroup reads S(t) once, takes P(t) = 2^(S - m_ref) against a
+// reference max that moves only when exceeded by more than 2^8 (then O is
+// rescaled in TMEM), and stores P(t) into TMEM.  Keeping P out of shared
+// memory leaves its bandwidth to the MMA operands Q, K, V.  Every wait is
+// bounded; on a timeout every role winds down.
 #include "kime_common.cuh"
 
 // Phase profiler, compiled in only with -DKIME_PHASE_PROFILE: each role's
@@ -63,13 +66,12 @@ namespace kime {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr uint32_t kTile = kBM * kHead * 2;  // 16 KB: 128 rows x 128 B
 constexpr uint32_t kOffQ = 0;                // 2 unit slots x 2 tiles
 constexpr uint32_t kOffK = kOffQ + 4 * kTile;
 constexpr uint32_t kOffV = kOffK + kStages * kTile;
-constexpr uint32_t kOffP = kOffV + kStages * kTile;  // 2 x 32 KB
-constexpr uint32_t kOffBar = kOffP + 4 * kTile;
+constexpr uint32_t kOffBar = kOffV + kStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
@@ -272,7 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 13 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       uint32_t n = 0, c = 0, pc[2] = {0, 0};
-      const uint32_t ap[2] = {smem_u32(smem + kOffP), smem_u32(smem + kOffP + 2 * kTile)};
       PHASE_DECL;
       for (;; ++n) {
         const int slot = n & 1;
@@ -320,9 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t acc0 = (w == 0 ? t > kb0 : t > kb1) ? 1u : 0u;
 #pragma unroll
               for (int ks = 0; ks < kBN / 16; ++ks)
-                tc_mma_ss(tmem + 256 + w * 64, sdesc_sw128(ap[w] + (ks >> 2) * kTile + (ks & 3) * 32, 16, 1024),
-                          sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, ks > 0 ? 1u : acc0);
+                tc_mma_ts(tmem + 256 + w * 64, tmem + 384 + w * 64 + ks * 8, sdesc_sw128(bv + ks * 2048, 0, 1024),
+                          kIdescPV, ks > 0 ? 1u : acc0);
               tc_commit(&sh->pv_full[w]);
+              PHASE(5);
             }
             if (t + 1 < inf.ke && in_range(w, t + 1)) {
               if (!next_ready) {
@@ -333,10 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 next_ready = true;
               }
               issue_s(w, st1);
+              PHASE(6);
             }
           }
           tc_commit(&sh->kv_empty[st]);  // every MMA reading stage st is issued
           if (t + 1 == inf.ke) tc_commit(&sh->q_empty[slot]);  // the unit's last S is issued
+          PHASE(7);
         }
         if (!ok) break;
         mbar_arrive(&sh->unit_empty[slot]);
@@ -409,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = tid & 127;           // row in the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + w * 128 + lane_off, tO = tmem + 256 + w * 64 + lane_off;
-    uint8_t* sP = smem + kOffP + w * 2 * kTile;
+    const uint32_t tP = tmem + 384 + w * 64 + lane_off;
     uint32_t n = 0, sc = 0, pvc = 0;
     PHASE_DECL;
     for (;; ++n) {
@@ -469,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         PHASE(2);
         // PV of the previous tile must be done before P is overwritten (it read
-        // the P buffer) and before O is rescaled (it accumulated into O).
+        // P) and before O is rescaled (it accumulated into O).
         if (t > kb) {
           ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
           tc_fence_after();
@@ -477,18 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         PHASE(3);
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         float rowsum = 0.f;
+        uint32_t pw[kBN / 2];
 #pragma unroll
-        for (int ch = 0; ch < kBN / 8; ++ch) {  // P row, keys 0..63 in half 0, 64..127 in half 1
-          uint32_t pw[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = fast_exp2(x[8 * ch + 2 * e] - m_use), p1 = fast_exp2(x[8 * ch + 2 * e + 1] - m_use);
-            rowsum += p0 + p1;
-            pw[e] = pack_f16x2(p0, p1);
-          }
-          *reinterpret_cast<uint4*>(sP + (ch >> 3) * kTile + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
-              make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        for (int j = 0; j < kBN; j += 2) {
+          const float p0 = fast_exp2(x[j] - m_use), p1 = fast_exp2(x[j + 1] - m_use);
+          rowsum += p0 + p1;
+          pw[j / 2] = pack_f16x2(p0, p1);
         }
+        tmem_st64(tP, pw);  // this row's P: keys 2c, 2c+1 in column c
         l = l * alpha + rowsum;
         PHASE(4);
         if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -496,10 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld64_wait(tO, ov);
 #pragma unroll
           for (int d = 0; d < kHead; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
-          tmem_st64_wait(tO, ov);
+          tmem_st64(tO, ov);
         }
+        tmem_wait_st();
         PHASE(5);
-        fence_proxy_async_smem();
         tc_fence_before();
         if (named_bar_or(1 + w, 128, !ok)) { ok = false; break; }
         if (r == 0) mbar_arrive(&sh->p_full[w]);

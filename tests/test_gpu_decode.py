@@ -41,8 +41,8 @@ def oracle_step(case, seqs):
 
 def test_append_and_decode_small_all_outputs(cuda_lib):
     case = decode_case(n_seqs=12, cap=700, seed=21)
-    case.pos[:4] = torch.tensor([0, 1, 255, 256], dtype=torch.int32)  # chunk edges, empty history
-    case.pos[4] = 699                                                # last row of the cache
+    # empty history, 128-key chunk edges, the last row of the cache
+    case.pos[:7] = torch.tensor([0, 1, 127, 128, 255, 256, 699], dtype=torch.int32)
     out, kc, vc = gpu_step(case)
     ref, kb, vb = oracle_step(case, np.arange(12))
     # the caches after append are bit-identical, canaries (every other row) untouched
