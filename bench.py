@@ -115,6 +115,17 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` over the ranks of the default process group (the
+    value itself when there is none): the job's time is its slowest rank's."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def l2_flush_buffer(dev):
     return torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
@@ -323,11 +334,7 @@ def main():
             torch.cuda.synchronize()
         per, subs = time_fn(step, args.steps, args.warmup, flush, stream, events=2)
     clocks = clk.summary()
-    total_ms = sum(per)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(per), dev if world > 1 else None)
     ms_step = total_ms / args.steps
     value = world * c.total * args.steps / (total_ms * 1e-3)
 

@@ -74,6 +74,7 @@ constexpr uint32_t kOffV = kOffK + kStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kPolyOf8 = 2;  // exponentials per 8 keys taken on the FMA pipe
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -461,9 +462,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kBN; ++j)
             if (j < lo || j > hi) x[j] = -INFINITY;
         }
-        float mx = x[0];
+        float mx8[8];  // eight independent chains, then a tree
 #pragma unroll
-        for (int j = 1; j < kBN; ++j) mx = fmaxf(mx, x[j]);
+        for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+#pragma unroll
+        for (int j = 8; j < kBN; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], x[j]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         // move the reference max on the first visible keys, or when it is
         // exceeded by more than 8 (a factor 256)
         float alpha = 1.f;
@@ -480,15 +485,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         PHASE(3);
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        float rowsum = 0.f;
-        uint32_t pw[kBN / 2];
+        // kPolyOf8 of every 8 exponentials run on the FMA pipe (exp2_poly), the
+        // rest on the MUFU, so the two pipes share the load.  A masked key
+        // (-inf) gives 0 on the MUFU and 2^-125 from exp2_poly: both round to
+        // an f16 zero in P, and 2^-125 cannot change l (l >= 1: the row max
+        // contributes 2^(max - m_ref) >= 1).
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < kBN; j += 2) {
-          const float p0 = fast_exp2(x[j] - m_use), p1 = fast_exp2(x[j + 1] - m_use);
-          rowsum += p0 + p1;
-          pw[j / 2] = pack_f16x2(p0, p1);
+        for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P at a time
+          uint32_t pw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = q4 * 32 + 2 * e;
+            const float a0 = x[j] - m_use, a1 = x[j + 1] - m_use;
+            const float p0 = (j & 7) < kPolyOf8 ? exp2_poly(a0) : fast_exp2(a0);
+            const float p1 = ((j + 1) & 7) < kPolyOf8 ? exp2_poly(a1) : fast_exp2(a1);
+            rs[e & 3] += p0 + p1;
+            pw[e] = pack_f16x2(p0, p1);
+          }
+          tmem_st16(tP + q4 * 16, pw);  // this row's P: keys 2c, 2c+1 in column c
         }
-        tmem_st64(tP, pw);  // this row's P: keys 2c, 2c+1 in column c
+        const float rowsum = (rs[0] + rs[1]) + (rs[2] + rs[3]);
         l = l * alpha + rowsum;
         PHASE(4);
         if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {
