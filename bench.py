@@ -185,8 +185,7 @@ class DecodeRun:
 
     def step(self):
         c = self.case
-        self.kime.kime_kv_append(c.qkv_new, self.pos, c.heads, c.kv_heads, c.k_cache, c.v_cache, self.cs, self.sn)
-        self.kime.kime_attn_decode(c.qkv_new, self.pos, c.heads, c.kv_heads, c.k_cache, c.v_cache, c.scale,
+        self.kime.kime_decode_step(c.qkv_new, self.pos, c.heads, c.kv_heads, c.k_cache, c.v_cache, c.scale,
                                    self.cs, self.sn, out=self.out, workspace=self.ws)
 
 

@@ -116,6 +116,17 @@ int kime_attn_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int he
                      const void* k_cache, const void* v_cache, void* out, void* workspace, size_t workspace_bytes,
                      int32_t* dev_status, void* stream);
 
+/* kime_decode_step -- kime_kv_append followed by kime_attn_decode in one
+ * launch (plus the ticket memset): the CTA whose 128-key chunk holds row pos[s]
+ * of a kv head writes the appended row (same rotation and rounding as
+ * kime_kv_append) to the caches and uses it directly; no other CTA reads that
+ * row.  Arguments as kime_attn_decode, with writable caches; workspace from
+ * kime_attn_workspace_bytes(1, ...). */
+int kime_decode_step(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
+                     int cap, float scale, const float* rope_cos, const float* rope_sin, int rope_len, void* k_cache,
+                     void* v_cache, void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                     void* stream);
+
 /* Scratch bytes for op 0 (varlen: uses n_seqs, total_tokens) or op 1 (decode:
  * uses n_seqs, heads, kv_heads, cap).  Returns 0 for an unknown op or
  * malformed sizes. */

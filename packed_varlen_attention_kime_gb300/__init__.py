@@ -18,7 +18,7 @@ import torch
 __all__ = [
     "KimeError", "load_library", "kime_attn_varlen", "kime_kv_append", "kime_attn_decode",
     "kime_attn_workspace_bytes", "kime_rope_tables", "kime_attn_debug_tiles", "kime_attn_varlen_noalloc",
-    "KIME_F32", "KIME_BF16", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
+    "kime_decode_step", "KIME_F32", "KIME_BF16", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +30,7 @@ DEV_BAD_CU, DEV_SEQ_TOO_LONG, DEV_BAD_POS, DEV_TIMEOUT = 1, 2, 4, 8
 EXPORTED_SYMBOLS = (
     "kime_attn_varlen", "kime_kv_append", "kime_attn_decode", "kime_attn_workspace_bytes",
     "kime_rope_tables", "kime_attn_debug_tiles", "kime_attn_last_cuda_error", "kime_attn_status_string",
-    "kime_attn_varlen_noalloc",
+    "kime_attn_varlen_noalloc", "kime_decode_step",
 )
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -66,6 +66,8 @@ def load_library(path: str = LIB_PATH):
     lib.kime_rope_tables.restype = I
     lib.kime_attn_debug_tiles.argtypes = [P, I, I, I, I, I, P, S, P, I, P, P, P]
     lib.kime_attn_debug_tiles.restype = I
+    lib.kime_decode_step.argtypes = [P, P, I, I, I, I, I, F, P, P, I, P, P, P, P, S, P, P]
+    lib.kime_decode_step.restype = I
     lib.kime_attn_varlen_noalloc.argtypes = [P, I, P, I, I, I, I, I, I, I, I, F, P, P, I, P, P, P]
     lib.kime_attn_varlen_noalloc.restype = I
     lib.kime_attn_last_cuda_error.argtypes = []
@@ -181,6 +183,25 @@ def kime_attn_decode(qkv_new, pos, heads, kv_heads, k_cache, v_cache, scale, rop
                               _p(out), _p(workspace), workspace.numel() * workspace.element_size(),
                               _p(dev_status), _stream(stream, qkv_new.device))
     _check("kime_attn_decode", rc)
+    return out
+
+
+def kime_decode_step(qkv_new, pos, heads, kv_heads, k_cache, v_cache, scale, rope_cos, rope_sin,
+                     out=None, workspace=None, dev_status=None, stream=None):
+    """KV append and single-token decode in one launch; returns ``out``."""
+    lib = load_library()
+    n = pos.numel()
+    cap = k_cache.shape[2]
+    if out is None:
+        out = torch.empty((n, heads * 64), dtype=torch.bfloat16, device=qkv_new.device)
+    need = kime_attn_workspace_bytes(1, n, 0, heads, kv_heads, cap)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=qkv_new.device)
+    rc = lib.kime_decode_step(_p(qkv_new), _p(pos), n, heads, kv_heads, 64, cap, float(scale),
+                              _p(rope_cos), _p(rope_sin), rope_cos.shape[0], _p(k_cache), _p(v_cache),
+                              _p(out), _p(workspace), workspace.numel() * workspace.element_size(),
+                              _p(dev_status), _stream(stream, qkv_new.device))
+    _check("kime_decode_step", rc)
     return out
 
 

@@ -126,10 +126,14 @@ int kime_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int head
                                             static_cast<cudaStream_t>(stream)));
 }
 
-int kime_attn_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
-                     int cap, float scale, const float* rope_cos, const float* rope_sin, int rope_len,
-                     const void* k_cache, const void* v_cache, void* out, void* workspace, size_t workspace_bytes,
-                     int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int decode_common(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim, int cap,
+                  float scale, const float* rope_cos, const float* rope_sin, int rope_len, const void* k_cache,
+                  const void* v_cache, void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                  void* stream, bool append) {
   if (!heads_ok(heads, kv_heads, head_dim) || n_seqs < 0 || cap <= 0 || rope_len < 0) return KIME_EINVAL;
   if (heads / kv_heads > kime::kMaxGroup) return KIME_EINVAL;
   if (!(scale > 0.f) || !isfinite(scale)) return KIME_EINVAL;
@@ -142,7 +146,27 @@ int kime_attn_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int he
   if (workspace_bytes < kime::decode_workspace_bytes(n_seqs, heads, kv_heads, cap)) return KIME_ERANGE;
   return cuda_status(kime::launch_decode(qkv_new, pos, n_seqs, heads, kv_heads, cap, scale, rope_cos, rope_sin,
                                          rope_len, k_cache, v_cache, out, workspace, dev_status,
-                                         static_cast<cudaStream_t>(stream)));
+                                         static_cast<cudaStream_t>(stream), append));
+}
+
+}  // namespace
+
+extern "C" {
+
+int kime_attn_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
+                     int cap, float scale, const float* rope_cos, const float* rope_sin, int rope_len,
+                     const void* k_cache, const void* v_cache, void* out, void* workspace, size_t workspace_bytes,
+                     int32_t* dev_status, void* stream) {
+  return decode_common(qkv_new, pos, n_seqs, heads, kv_heads, head_dim, cap, scale, rope_cos, rope_sin, rope_len,
+                       k_cache, v_cache, out, workspace, workspace_bytes, dev_status, stream, false);
+}
+
+int kime_decode_step(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
+                     int cap, float scale, const float* rope_cos, const float* rope_sin, int rope_len, void* k_cache,
+                     void* v_cache, void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                     void* stream) {
+  return decode_common(qkv_new, pos, n_seqs, heads, kv_heads, head_dim, cap, scale, rope_cos, rope_sin, rope_len,
+                       k_cache, v_cache, out, workspace, workspace_bytes, dev_status, stream, true);
 }
 
 int kime_rope_tables(double theta, int len, float* cos_out, float* sin_out) {

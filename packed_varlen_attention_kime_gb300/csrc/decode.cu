@@ -70,12 +70,16 @@ __global__ void __launch_bounds__(kAppendThreads)
   }
 }
 
-template <int G>
+// kAppend: the CTA whose chunk holds row pos[s] also performs the KV append of
+// kv_append_kernel for its kv head (the same float32 rotation and rounding),
+// writes the row to the caches and patches its shared-memory copy, so append
+// and attention take one launch.  No other CTA reads that row.
+template <int G, bool kAppend>
 __global__ void __launch_bounds__(kDecThreads)
     decode_kernel(const uint16_t* __restrict__ qkv_new, const int32_t* __restrict__ pos, int n_seqs, int heads,
                   int kv_heads, int cap, float scale_log2, const float* __restrict__ cos_t,
-                  const float* __restrict__ sin_t, int rope_len, const uint16_t* __restrict__ k_cache,
-                  const uint16_t* __restrict__ v_cache, __nv_bfloat16* __restrict__ out,
+                  const float* __restrict__ sin_t, int rope_len, uint16_t* __restrict__ k_cache,
+                  uint16_t* __restrict__ v_cache, __nv_bfloat16* __restrict__ out,
                   float* __restrict__ partials, int32_t* __restrict__ tickets, int max_chunks, int32_t* dev_status) {
   extern __shared__ __align__(128) uint8_t smem[];
   // [K | V of the chunk][merge buffers][mbarrier]
@@ -145,6 +149,35 @@ __global__ void __launch_bounds__(kDecThreads)
         mbar_wait(bar, 0);
       }
       return;
+    }
+    if (kAppend && c == n_c - 1) {
+      // this chunk holds row P: write the appended k (rotated at P) and v of
+      // kv head g to the caches and over the stale copy in shared memory
+      const int rp = P - c * kDecChunk;
+      uint16_t* ks = reinterpret_cast<uint16_t*>(smem) + rp * kHead;
+      uint16_t* vs = reinterpret_cast<uint16_t*>(smem + kStageBytes / 2) + rp * kHead;
+      const uint16_t* row = qkv_new + static_cast<size_t>(s) * W;
+      const size_t dst = ((static_cast<size_t>(s) * kv_heads + g) * cap + P) * kHead;
+      if (tid < kHalf) {
+        const uint16_t* xk = row + (heads + g) * kHead;
+        const float a = __uint_as_float(static_cast<uint32_t>(xk[tid]) << 16);
+        const float b = __uint_as_float(static_cast<uint32_t>(xk[tid + kHalf]) << 16);
+        float ya, yb;
+        rope_pair(a, b, cos_t[static_cast<size_t>(P) * kHalf + tid], sin_t[static_cast<size_t>(P) * kHalf + tid], ya,
+                  yb);
+        const uint32_t w2 = pack_bf16x2(ya, yb);
+        const uint16_t lo = static_cast<uint16_t>(w2 & 0xffffu), hi = static_cast<uint16_t>(w2 >> 16);
+        k_cache[dst + tid] = lo;
+        k_cache[dst + tid + kHalf] = hi;
+        ks[tid] = lo;
+        ks[tid + kHalf] = hi;
+      } else if (tid < kHalf + kHead) {
+        const int t = tid - kHalf;
+        const uint16_t v = row[(heads + kv_heads + g) * kHead + t];
+        v_cache[dst + t] = v;
+        vs[t] = v;
+      }
+      __syncthreads();
     }
     const uint16_t* Ks = reinterpret_cast<const uint16_t*>(smem + st * kStageBytes);
     const uint16_t* Vs = Ks + kDecChunk * kHead;
@@ -325,16 +358,17 @@ __global__ void __launch_bounds__(kDecThreads)
   }
 }
 
-template <int G>
+template <int G, bool kAppend>
 cudaError_t launch_decode_g(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int cap,
-                            float scale, const float* cos_t, const float* sin_t, int rope_len, const void* k_cache,
-                            const void* v_cache, void* out, void* ws, int32_t* dev_status, cudaStream_t st) {
+                            float scale, const float* cos_t, const float* sin_t, int rope_len, void* k_cache,
+                            void* v_cache, void* out, void* ws, int32_t* dev_status, cudaStream_t st) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   constexpr uint32_t smem = dec_smem_bytes<G>();
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_kernel<G, kAppend>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
@@ -345,9 +379,9 @@ cudaError_t launch_decode_g(const void* qkv_new, const int32_t* pos, int n_seqs,
   cudaError_t e = cudaMemsetAsync(tickets, 0, static_cast<size_t>(n_seqs) * kv_heads * 4, st);
   if (e != cudaSuccess) return e;
   dim3 grid(max_chunks, kv_heads, n_seqs);
-  decode_kernel<G><<<grid, kDecThreads, smem, st>>>(
+  decode_kernel<G, kAppend><<<grid, kDecThreads, smem, st>>>(
       static_cast<const uint16_t*>(qkv_new), pos, n_seqs, heads, kv_heads, cap, scale * 1.4426950408889634f, cos_t,
-      sin_t, rope_len, static_cast<const uint16_t*>(k_cache), static_cast<const uint16_t*>(v_cache),
+      sin_t, rope_len, static_cast<uint16_t*>(k_cache), static_cast<uint16_t*>(v_cache),
       static_cast<__nv_bfloat16*>(out), partials, tickets, max_chunks, dev_status);
   return cudaGetLastError();
 }
@@ -372,11 +406,17 @@ cudaError_t launch_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs
 
 cudaError_t launch_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int cap,
                           float scale, const float* cos_t, const float* sin_t, int rope_len, const void* k_cache,
-                          const void* v_cache, void* out, void* ws, int32_t* dev_status, cudaStream_t st) {
+                          const void* v_cache, void* out, void* ws, int32_t* dev_status, cudaStream_t st,
+                          bool append) {
+  void* kc = const_cast<void*>(k_cache);
+  void* vc = const_cast<void*>(v_cache);
   switch (heads / kv_heads) {
-#define KIME_G(N) \
-  case N:         \
-    return launch_decode_g<N>(qkv_new, pos, n_seqs, heads, kv_heads, cap, scale, cos_t, sin_t, rope_len, k_cache, v_cache, out, ws, dev_status, st);
+#define KIME_G(N)                                                                                                    \
+  case N:                                                                                                            \
+    return append ? launch_decode_g<N, true>(qkv_new, pos, n_seqs, heads, kv_heads, cap, scale, cos_t, sin_t,        \
+                                             rope_len, kc, vc, out, ws, dev_status, st)                              \
+                  : launch_decode_g<N, false>(qkv_new, pos, n_seqs, heads, kv_heads, cap, scale, cos_t, sin_t,       \
+                                              rope_len, kc, vc, out, ws, dev_status, st);
     KIME_G(1) KIME_G(2) KIME_G(3) KIME_G(4) KIME_G(5) KIME_G(6) KIME_G(7) KIME_G(8)
 #undef KIME_G
     default:

@@ -74,6 +74,7 @@ cudaError_t launch_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs
                              int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int cap,
                           float scale, const float* cos_t, const float* sin_t, int rope_len, const void* k_cache,
-                          const void* v_cache, void* out, void* ws, int32_t* dev_status, cudaStream_t st);
+                          const void* v_cache, void* out, void* ws, int32_t* dev_status, cudaStream_t st,
+                          bool append);
 
 }  // namespace kime

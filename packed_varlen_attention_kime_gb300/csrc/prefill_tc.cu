@@ -186,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   Shared* sh = reinterpret_cast<Shared*>(smem + kOffBar);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
   const int G = p.heads / p.kv_heads;
-  const int n_units = p.hdr->n_duos * p.heads;
 
   if (tid == 0) {
     tma_prefetch_map(&qkv_map);
@@ -232,6 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<48>();
     if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
+      griddep_wait();  // the schedule written by the kernel before this one
+      const int n_units = p.hdr->n_duos * p.heads;
       uint32_t n = 0, c = 0;
       PHASE_DECL;
       for (;; ++n) {
@@ -607,8 +608,19 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, int n_seqs, int total,
   prm.hdr = static_cast<WsHeader*>(ws);
   prm.duos = ws_duos(ws, max_pairs);
   prm.dev_status = dev_status;
-  prefill_tc_kernel<<<sms, kThreads, kSmemBytes, st>>>(*qkv_map, prm);
-  return cudaGetLastError();
+  // launched with programmatic stream serialization: its prologue overlaps the
+  // scheduler, whose lists it waits for (griddep_wait) before reading them
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, *qkv_map, prm);
 }
 
 }  // namespace kime

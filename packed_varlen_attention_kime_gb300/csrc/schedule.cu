@@ -51,6 +51,9 @@ __global__ void __launch_bounds__(kSchedThreads)
   __shared__ int hist[2][kBuckets];
   __shared__ int cursor[2][kBuckets];
   __shared__ int s_bad;
+  // The attention kernel may start now: it sets itself up (barriers, TMEM,
+  // tensor map) and waits for this kernel's lists before reading them.
+  griddep_launch_dependents();
   for (int i = threadIdx.x; i < 2 * kBuckets; i += blockDim.x) hist[i / kBuckets][i % kBuckets] = 0;
   if (threadIdx.x == 0) {
     s_bad = 0;

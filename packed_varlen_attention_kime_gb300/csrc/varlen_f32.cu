@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(kThreads)
   const int tid = threadIdx.x;
   const size_t W = static_cast<size_t>(kHead) * (heads + 2 * kv_heads);
   const int G = heads / kv_heads;
+  griddep_wait();  // the schedule written by the kernel before this one
   const int n_units = hdr->n_pairs * heads;
 
   for (;;) {
@@ -156,9 +157,18 @@ cudaError_t launch_varlen_f32(const float* qkv, const int32_t* cu, int n_seqs, i
   }
   WsHeader* hdr = static_cast<WsHeader*>(ws);
   const Pair* pairs = reinterpret_cast<const Pair*>(static_cast<char*>(ws) + sizeof(WsHeader));
-  varlen_f32_kernel<<<sms * 2, kThreads, smem, st>>>(qkv, heads, kv_heads, window, causal, scale, cos_t, sin_t, out,
-                                                     hdr, pairs);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms * 2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, varlen_f32_kernel, qkv, heads, kv_heads, window, causal, scale, cos_t, sin_t, out,
+                            hdr, pairs);
 }
 
 }  // namespace kime

@@ -13,14 +13,20 @@ from parity_util import check_bf16, gpu_tables, oracle_tables
 pytestmark = pytest.mark.gpu
 
 
-def gpu_step(case, dev_status=None):
+def gpu_step(case, dev_status=None, fused=False):
+    """Append then decode through the C ABI: two entry points, or the fused
+    kime_decode_step."""
     dev = torch.device("cuda")
     c, s = gpu_tables(case.theta, case.cap)
     qn, pos = case.qkv_new.to(dev), case.pos.to(dev)
     kc, vc = case.k_cache.to(dev, copy=True), case.v_cache.to(dev, copy=True)
-    kime.kime_kv_append(qn, pos, case.heads, case.kv_heads, kc, vc, c, s, dev_status=dev_status)
-    out = kime.kime_attn_decode(qn, pos, case.heads, case.kv_heads, kc, vc, case.scale, c, s,
-                                dev_status=dev_status)
+    if fused:
+        out = kime.kime_decode_step(qn, pos, case.heads, case.kv_heads, kc, vc, case.scale, c, s,
+                                    dev_status=dev_status)
+    else:
+        kime.kime_kv_append(qn, pos, case.heads, case.kv_heads, kc, vc, c, s, dev_status=dev_status)
+        out = kime.kime_attn_decode(qn, pos, case.heads, case.kv_heads, kc, vc, case.scale, c, s,
+                                    dev_status=dev_status)
     torch.cuda.synchronize()
     return out, kc, vc
 
@@ -39,11 +45,12 @@ def oracle_step(case, seqs):
     return out, kb, vb
 
 
-def test_append_and_decode_small_all_outputs(cuda_lib):
+@pytest.mark.parametrize("fused", [False, True])
+def test_append_and_decode_small_all_outputs(cuda_lib, fused):
     case = decode_case(n_seqs=12, cap=700, seed=21)
     # empty history, 128-key chunk edges, the last row of the cache
     case.pos[:7] = torch.tensor([0, 1, 127, 128, 255, 256, 699], dtype=torch.int32)
-    out, kc, vc = gpu_step(case)
+    out, kc, vc = gpu_step(case, fused=fused)
     ref, kb, vb = oracle_step(case, np.arange(12))
     # the caches after append are bit-identical, canaries (every other row) untouched
     assert np.array_equal(bf16_bits(kc), kb)
@@ -59,9 +66,10 @@ def test_decode_group_sizes(cuda_lib, heads, kv_heads):
     check_bf16(out.float().cpu().numpy(), ref, f"decode H{heads}/{kv_heads}")
 
 
-def test_decode_full_size_sampled(cuda_lib):
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_full_size_sampled(cuda_lib, fused):
     case = decode_case(device="cuda")
-    out, kc, _ = gpu_step(case)
+    out, kc, _ = gpu_step(case, fused=fused)
     assert torch.isfinite(out.float()).all()
     rng = np.random.default_rng(5)
     pos = case.pos.numpy()
@@ -90,7 +98,7 @@ def test_bad_positions_are_flagged_and_skipped(cuda_lib):
     case.pos[2] = -5
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     k_before = case.k_cache.clone()
-    out, kc, vc = gpu_step(case, dev_status=st)
+    out, kc, vc = gpu_step(case, dev_status=st, fused=True)
     assert int(st.item()) & kime.DEV_BAD_POS
     kc = kc.cpu()
     assert torch.equal(kc[1], k_before[1]) and torch.equal(kc[2], k_before[2])
