@@ -11,14 +11,16 @@
 // head h / (heads/kv_heads), all heads of one kv group together (the GQA fold
 // of TextTower::block: the cache is never expanded per q head).
 //
-// Split-KV: one CTA per (chunk of 128 keys, kv head, sequence); CTAs of
-// chunks past pos[s] exit at once.  A chunk's K and V rows arrive by two 1-D
-// bulk copies into shared memory while the CTA rotates its q.  8 threads share
+// Split-KV: one CTA per (two chunks of 128 keys, kv head, sequence); CTAs
+// past pos[s] exit at once.  Each chunk's K and V rows arrive by two 1-D bulk
+// copies into their own shared-memory stage -- all issued at the start, so the
+// second chunk lands while the first is computed and q is rotated.  8 threads share
 // a key (8 dims each), so scores need a 3-step shuffle reduction; all G q heads
-// of the kv group are done together.  Each CTA reduces its chunk to
-// (m, l, o[64]) per q head (base-2 logits); the last CTA of a (sequence, kv
-// head) to finish -- found with an atomic ticket, no waiting -- merges the
-// chunks: m = max m_c, l = sum l_c 2^(m_c-m), o = sum o_c 2^(m_c-m) / l.
+// of the kv group are done together, with an online softmax across the two
+// chunks.  Each CTA reduces its keys to (m, l, o[64]) per q head (base-2
+// logits); the last CTA of a (sequence, kv head) to finish -- found with an
+// atomic ticket, no waiting -- merges the parts:
+// m = max m_c, l = sum l_c 2^(m_c-m), o = sum o_c 2^(m_c-m) / l.
 #include "kime_common.cuh"
 
 namespace kime {
@@ -33,9 +35,11 @@ constexpr int kKeysPerThread = kDecChunk / kGroups;
 constexpr uint32_t kStageBytes = 2 * kDecChunk * kHead * 2;  // K and V of one chunk
 constexpr int kPartialFloats = 68;               // m, l, o[64], 2 pad
 
+constexpr int kDecPer = 2;  // chunks per CTA: the second one's copies land while the first is computed
+
 template <int G>
 constexpr uint32_t dec_smem_bytes() {
-  return kStageBytes + ((kDecWarps * G * kHead + 2 * kDecWarps * G) * 4 + 15) / 16 * 16 + 8;
+  return kDecPer * kStageBytes + ((kDecWarps * G * kHead + 2 * kDecWarps * G) * 4 + 15) / 16 * 16 + 8 * kDecPer;
 }
 
 __global__ void __launch_bounds__(kAppendThreads)
@@ -75,41 +79,45 @@ __global__ void __launch_bounds__(kAppendThreads)
 // writes the row to the caches and patches its shared-memory copy, so append
 // and attention take one launch.  No other CTA reads that row.
 template <int G, bool kAppend>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, G > 4 ? 2 : 3)
     decode_kernel(const uint16_t* __restrict__ qkv_new, const int32_t* __restrict__ pos, int n_seqs, int heads,
                   int kv_heads, int cap, float scale_log2, const float* __restrict__ cos_t,
                   const float* __restrict__ sin_t, int rope_len, uint16_t* __restrict__ k_cache,
                   uint16_t* __restrict__ v_cache, __nv_bfloat16* __restrict__ out,
                   float* __restrict__ partials, int32_t* __restrict__ tickets, int max_chunks, int32_t* dev_status) {
   extern __shared__ __align__(128) uint8_t smem[];
-  // [K | V of the chunk][merge buffers][mbarrier]
-  float* red_o = reinterpret_cast<float*>(smem + kStageBytes);  // [warps][G][64]
-  float* red_m = red_o + kDecWarps * G * kHead;                  // [warps][G]
-  float* red_l = red_m + kDecWarps * G;                          // [warps][G]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kStageBytes +
+  // [K | V of chunk A][K | V of chunk B][merge buffers][2 mbarriers]
+  float* red_o = reinterpret_cast<float*>(smem + kDecPer * kStageBytes);  // [warps][G][64]
+  float* red_m = red_o + kDecWarps * G * kHead;                            // [warps][G]
+  float* red_l = red_m + kDecWarps * G;                                    // [warps][G]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kDecPer * kStageBytes +
                                               ((kDecWarps * G * kHead + 2 * kDecWarps * G) * 4 + 15) / 16 * 16);
   __shared__ int s_last;
   (void)n_seqs;
 
-  const int c = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
+  const int pc = blockIdx.x, g = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, lane8 = tid & 7, grp = tid >> 3, d0 = lane8 * 8;
   const size_t W = static_cast<size_t>(kHead) * (heads + 2 * kv_heads);
   const int P = __ldg(pos + s);
   if (P < 0 || P >= cap || P >= rope_len) {
-    if (c == 0 && g == 0 && tid == 0) report(dev_status, ST_BAD_POS);
+    if (pc == 0 && g == 0 && tid == 0) report(dev_status, ST_BAD_POS);
     return;
   }
-  const int n_c = (P + 1 + kDecChunk - 1) / kDecChunk;
-  if (c >= n_c) return;
-  const int nk = min(kDecChunk, P + 1 - c * kDecChunk);
-  const int st = 0;
+  const int n_c = (P + 1 + kDecChunk - 1) / kDecChunk;  // chunks of keys 0..=P
+  const int n_parts = (n_c + kDecPer - 1) / kDecPer;      // CTAs for this (s, g)
+  if (pc >= n_parts) return;
+  const int c_first = pc * kDecPer, n_here = min(kDecPer, n_c - c_first);
   if (tid == 0) {
-    const size_t base = ((static_cast<size_t>(s) * kv_heads + g) * cap + static_cast<size_t>(c) * kDecChunk) * kHead;
-    mbar_init(bar, 1);
+    for (int i = 0; i < kDecPer; ++i) mbar_init(&bar[i], 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar, 2u * nk * kHead * 2);
-    bulk_load(smem, k_cache + base, nk * kHead * 2, bar);
-    bulk_load(smem + kStageBytes / 2, v_cache + base, nk * kHead * 2, bar);
+    for (int i = 0; i < n_here; ++i) {
+      const int c = c_first + i, nk = min(kDecChunk, P + 1 - c * kDecChunk);
+      const size_t base =
+          ((static_cast<size_t>(s) * kv_heads + g) * cap + static_cast<size_t>(c) * kDecChunk) * kHead;
+      mbar_arrive_expect_tx(&bar[i], 2u * nk * kHead * 2);
+      bulk_load(smem + i * kStageBytes, k_cache + base, nk * kHead * 2, &bar[i]);
+      bulk_load(smem + i * kStageBytes + kStageBytes / 2, v_cache + base, nk * kHead * 2, &bar[i]);
+    }
   }
   {
     // q heads of this kv group, RoPE'd at P, this thread's 8 dims, times
@@ -139,102 +147,116 @@ __global__ void __launch_bounds__(kDecThreads)
         }
       }
     }
-    __syncthreads();  // the barrier is initialised before anyone waits on it
-    const bool ok = mbar_wait(bar, 0);
-    if (__syncthreads_or(!ok)) {
-      // the copies did not land in time: report, give them one more bounded
-      // wait so the shared memory outlives them, and leave the chunk undone
-      if (tid == 0) {
-        report(dev_status, ST_TIMEOUT);
-        mbar_wait(bar, 0);
-      }
-      return;
-    }
-    if (kAppend && c == n_c - 1) {
-      // this chunk holds row P: write the appended k (rotated at P) and v of
-      // kv head g to the caches and over the stale copy in shared memory
-      const int rp = P - c * kDecChunk;
-      uint16_t* ks = reinterpret_cast<uint16_t*>(smem) + rp * kHead;
-      uint16_t* vs = reinterpret_cast<uint16_t*>(smem + kStageBytes / 2) + rp * kHead;
-      const uint16_t* row = qkv_new + static_cast<size_t>(s) * W;
-      const size_t dst = ((static_cast<size_t>(s) * kv_heads + g) * cap + P) * kHead;
-      if (tid < kHalf) {
-        const uint16_t* xk = row + (heads + g) * kHead;
-        const float a = __uint_as_float(static_cast<uint32_t>(xk[tid]) << 16);
-        const float b = __uint_as_float(static_cast<uint32_t>(xk[tid + kHalf]) << 16);
-        float ya, yb;
-        rope_pair(a, b, cos_t[static_cast<size_t>(P) * kHalf + tid], sin_t[static_cast<size_t>(P) * kHalf + tid], ya,
-                  yb);
-        const uint32_t w2 = pack_bf16x2(ya, yb);
-        const uint16_t lo = static_cast<uint16_t>(w2 & 0xffffu), hi = static_cast<uint16_t>(w2 >> 16);
-        k_cache[dst + tid] = lo;
-        k_cache[dst + tid + kHalf] = hi;
-        ks[tid] = lo;
-        ks[tid + kHalf] = hi;
-      } else if (tid < kHalf + kHead) {
-        const int t = tid - kHalf;
-        const uint16_t v = row[(heads + kv_heads + g) * kHead + t];
-        v_cache[dst + t] = v;
-        vs[t] = v;
-      }
-      __syncthreads();
-    }
-    const uint16_t* Ks = reinterpret_cast<const uint16_t*>(smem + st * kStageBytes);
-    const uint16_t* Vs = Ks + kDecChunk * kHead;
-
-    // scores of this thread's keys grp, grp + 16, ...
-    float sc[G][kKeysPerThread];
-#pragma unroll
-    for (int k = 0; k < kKeysPerThread; ++k) {
-      const int kk = grp + k * kGroups;
-      float part[G];
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) part[hh] = 0.f;
-      if (kk < nk) {
-        const uint4 kw = *reinterpret_cast<const uint4*>(Ks + kk * kHead + d0);
-        const float kf[8] = {bf16lo(kw.x), bf16hi(kw.x), bf16lo(kw.y), bf16hi(kw.y),
-                             bf16lo(kw.z), bf16hi(kw.z), bf16lo(kw.w), bf16hi(kw.w)};
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) part[hh] = fmaf(q[hh][e], kf[e], part[hh]);
-      }
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        float v = part[hh];
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        sc[hh][k] = kk < nk ? v : -INFINITY;
-      }
-    }
+    __syncthreads();  // the barriers are initialised before anyone waits on them
     float m[G], l[G], o[G][8];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
-      float mx = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < kKeysPerThread; ++k) mx = fmaxf(mx, sc[hh][k]);
-      m[hh] = mx;
+      m[hh] = -INFINITY;
       l[hh] = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[hh][e] = 0.f;
     }
+#pragma unroll 1
+    for (int ci = 0; ci < n_here; ++ci) {
+      const int c = c_first + ci, nk = min(kDecChunk, P + 1 - c * kDecChunk);
+      uint8_t* stage = smem + ci * kStageBytes;
+      const bool ok = mbar_wait(&bar[ci], 0);
+      if (__syncthreads_or(!ok)) {
+        // the copies did not land in time: report, give the ones in flight one
+        // more bounded wait so the shared memory outlives them, leave the work
+        if (tid == 0) {
+          report(dev_status, ST_TIMEOUT);
+          for (int i = ci; i < n_here; ++i) mbar_wait(&bar[i], 0);
+        }
+        return;
+      }
+      if (kAppend && c == n_c - 1) {
+        // this chunk holds row P: write the appended k (rotated at P) and v of
+        // kv head g to the caches and over the stale copy in shared memory
+        const int rp = P - c * kDecChunk;
+        uint16_t* ks = reinterpret_cast<uint16_t*>(stage) + rp * kHead;
+        uint16_t* vs = reinterpret_cast<uint16_t*>(stage + kStageBytes / 2) + rp * kHead;
+        const uint16_t* row = qkv_new + static_cast<size_t>(s) * W;
+        const size_t dst = ((static_cast<size_t>(s) * kv_heads + g) * cap + P) * kHead;
+        if (tid < kHalf) {
+          const uint16_t* xk = row + (heads + g) * kHead;
+          const float a = __uint_as_float(static_cast<uint32_t>(xk[tid]) << 16);
+          const float b = __uint_as_float(static_cast<uint32_t>(xk[tid + kHalf]) << 16);
+          float ya, yb;
+          rope_pair(a, b, cos_t[static_cast<size_t>(P) * kHalf + tid], sin_t[static_cast<size_t>(P) * kHalf + tid],
+                    ya, yb);
+          const uint32_t w2 = pack_bf16x2(ya, yb);
+          const uint16_t lo = static_cast<uint16_t>(w2 & 0xffffu), hi = static_cast<uint16_t>(w2 >> 16);
+          k_cache[dst + tid] = lo;
+          k_cache[dst + tid + kHalf] = hi;
+          ks[tid] = lo;
+          ks[tid + kHalf] = hi;
+        } else if (tid < kHalf + kHead) {
+          const int t = tid - kHalf;
+          const uint16_t v = row[(heads + kv_heads + g) * kHead + t];
+          v_cache[dst + t] = v;
+          vs[t] = v;
+        }
+        __syncthreads();
+      }
+      const uint16_t* Ks = reinterpret_cast<const uint16_t*>(stage);
+      const uint16_t* Vs = Ks + kDecChunk * kHead;
+
+      // scores of this thread's keys grp, grp + 16, ...
+      float sc[G][kKeysPerThread];
 #pragma unroll
-    for (int k = 0; k < kKeysPerThread; ++k) {
-      const int kk = grp + k * kGroups;
-      if (kk >= nk) continue;
-      const uint4 vw = *reinterpret_cast<const uint4*>(Vs + kk * kHead + d0);
-      const float vf[8] = {bf16lo(vw.x), bf16hi(vw.x), bf16lo(vw.y), bf16hi(vw.y),
-                           bf16lo(vw.z), bf16hi(vw.z), bf16lo(vw.w), bf16hi(vw.w)};
+      for (int k = 0; k < kKeysPerThread; ++k) {
+        const int kk = grp + k * kGroups;
+        float part[G];
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) part[hh] = 0.f;
+        if (kk < nk) {
+          const uint4 kw = *reinterpret_cast<const uint4*>(Ks + kk * kHead + d0);
+          const float kf[8] = {bf16lo(kw.x), bf16hi(kw.x), bf16lo(kw.y), bf16hi(kw.y),
+                               bf16lo(kw.z), bf16hi(kw.z), bf16lo(kw.w), bf16hi(kw.w)};
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) part[hh] = fmaf(q[hh][e], kf[e], part[hh]);
+        }
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          float v = part[hh];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          sc[hh][k] = kk < nk ? v : -INFINITY;
+        }
+      }
+      // online update of this thread's (m, l, o) with the chunk
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        const float pr = fast_exp2(sc[hh][k] - m[hh]);
-        l[hh] += pr;
+        float mx = m[hh];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[hh][e] = fmaf(pr, vf[e], o[hh][e]);
+        for (int k = 0; k < kKeysPerThread; ++k) mx = fmaxf(mx, sc[hh][k]);
+        const float alpha = mx == -INFINITY ? 1.f : fast_exp2(m[hh] - mx);
+        m[hh] = mx;
+        l[hh] *= alpha;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[hh][e] *= alpha;
+      }
+#pragma unroll
+      for (int k = 0; k < kKeysPerThread; ++k) {
+        const int kk = grp + k * kGroups;
+        if (kk >= nk) continue;
+        const uint4 vw = *reinterpret_cast<const uint4*>(Vs + kk * kHead + d0);
+        const float vf[8] = {bf16lo(vw.x), bf16hi(vw.x), bf16lo(vw.y), bf16hi(vw.y),
+                             bf16lo(vw.z), bf16hi(vw.z), bf16lo(vw.w), bf16hi(vw.w)};
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          const float pr = fast_exp2(sc[hh][k] - m[hh]);
+          l[hh] += pr;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[hh][e] = fmaf(pr, vf[e], o[hh][e]);
+        }
       }
     }
-    // merge the 16 key groups of this chunk: the 4 groups of a warp by
+    // merge the 16 key groups of this CTA: the 4 groups of a warp by
     // shuffles, then the 4 warps through shared memory
     const int wid = tid >> 5;
 #pragma unroll
@@ -262,8 +284,8 @@ __global__ void __launch_bounds__(kDecThreads)
       }
     }
     __syncthreads();
-    const bool single = n_c == 1;
-    float* part = partials + ((static_cast<size_t>(s) * kv_heads + g) * max_chunks + c) * G * kPartialFloats;
+    const bool single = n_parts == 1;
+    float* part = partials + ((static_cast<size_t>(s) * kv_heads + g) * max_chunks + pc) * G * kPartialFloats;
     for (int e = tid; e < G * kHead; e += kDecThreads) {
       const int hh = e / kHead, d = e % kHead;
       float M = -INFINITY;
@@ -290,7 +312,7 @@ __global__ void __launch_bounds__(kDecThreads)
       // publish this chunk; the last CTA of (s, g) to arrive merges all chunks
       __threadfence();
       __syncthreads();
-      if (tid == 0) s_last = atomicAdd(&tickets[s * kv_heads + g], 1) == n_c - 1;
+      if (tid == 0) s_last = atomicAdd(&tickets[s * kv_heads + g], 1) == n_parts - 1;
       __syncthreads();
       if (s_last) {
         __threadfence();
@@ -299,14 +321,14 @@ __global__ void __launch_bounds__(kDecThreads)
         // weights 2^(m_c - M) in shared memory; every output sums its column
         // over the chunks with independent loads.
         const float* all = partials + (static_cast<size_t>(s) * kv_heads + g) * max_chunks * G * kPartialFloats;
-        float* red = reinterpret_cast<float*>(smem + st * kStageBytes);  // [G][threads]
+        float* red = reinterpret_cast<float*>(smem);  // [G][threads], in the consumed stage 0
         float* hdr = red + G * kDecThreads;                               // [G] M, [G] L
         float* wts = hdr + 2 * G;                                         // [block][G]
         constexpr int kBlock = (kStageBytes / 4 - (kDecThreads + 2) * G) / G;
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
           float M = -INFINITY;
-          for (int cc = tid; cc < n_c; cc += kDecThreads) M = fmaxf(M, __ldcg(all + (cc * G + hh) * kPartialFloats));
+          for (int cc = tid; cc < n_parts; cc += kDecThreads) M = fmaxf(M, __ldcg(all + (cc * G + hh) * kPartialFloats));
           red[hh * kDecThreads + tid] = M;
         }
         __syncthreads();
@@ -319,8 +341,8 @@ __global__ void __launch_bounds__(kDecThreads)
         float O[(G * kHead + kDecThreads - 1) / kDecThreads];
 #pragma unroll
         for (int k = 0; k < (G * kHead + kDecThreads - 1) / kDecThreads; ++k) O[k] = 0.f;
-        for (int c0 = 0; c0 < n_c; c0 += kBlock) {
-          const int nb = min(kBlock, n_c - c0);
+        for (int c0 = 0; c0 < n_parts; c0 += kBlock) {
+          const int nb = min(kBlock, n_parts - c0);
           __syncthreads();
           for (int e = tid; e < nb * G; e += kDecThreads)
             wts[e] = fast_exp2(__ldcg(all + (c0 * G + e) * kPartialFloats) - hdr[e % G]);
@@ -378,7 +400,7 @@ cudaError_t launch_decode_g(const void* qkv_new, const int32_t* pos, int n_seqs,
                                              align_up(static_cast<size_t>(n_seqs) * kv_heads * 4, 256));
   cudaError_t e = cudaMemsetAsync(tickets, 0, static_cast<size_t>(n_seqs) * kv_heads * 4, st);
   if (e != cudaSuccess) return e;
-  dim3 grid(max_chunks, kv_heads, n_seqs);
+  dim3 grid((max_chunks + kDecPer - 1) / kDecPer, kv_heads, n_seqs);
   decode_kernel<G, kAppend><<<grid, kDecThreads, smem, st>>>(
       static_cast<const uint16_t*>(qkv_new), pos, n_seqs, heads, kv_heads, cap, scale * 1.4426950408889634f, cos_t,
       sin_t, rope_len, static_cast<uint16_t*>(k_cache), static_cast<uint16_t*>(v_cache),

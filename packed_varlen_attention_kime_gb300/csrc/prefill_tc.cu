@@ -74,7 +74,7 @@ constexpr uint32_t kOffV = kOffK + kStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kPolyOf8 = 2;  // exponentials per 8 keys taken on the FMA pipe
+constexpr int kPolyOf8 = 0;  // exponentials per 8 keys taken on the FMA pipe
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -463,13 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < kBN; ++j)
             if (j < lo || j > hi) x[j] = -INFINITY;
         }
-        float mx8[8];  // eight independent chains, then a tree
+        // row max: eight running maxima, each taking two keys per three-input
+        // max (64 instructions for 128 keys, short dependency chains)
+        float m8[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(x[2 * k], x[2 * k + 1]);
 #pragma unroll
-        for (int j = 8; j < kBN; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], x[j]);
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int j = 16; j < kBN; j += 2) m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], x[j], x[j + 1]);
+        const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         // move the reference max on the first visible keys, or when it is
         // exceeded by more than 8 (a factor 256)
         float alpha = 1.f;
@@ -491,7 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (-inf) gives 0 on the MUFU and 2^-125 from exp2_poly: both round to
         // an f16 zero in P, and 2^-125 cannot change l (l >= 1: the row max
         // contributes 2^(max - m_ref) >= 1).
-        float rs[4] = {0.f, 0.f, 0.f, 0.f};
+        // P = 2^(x - m_use), row sums in four chains; kPolyOf8 of every 8
+        // exponentials on the FMA pipe (exp2_poly), the rest
+        // on the MUFU.  A masked key (-inf) gives 0 on the MUFU and 2^-125 from
+        // exp2_poly: both round to an f16 zero in P, and 2^-125 cannot change l
+        // (l >= 1: the row max contributes 2^(max - m_ref) >= 1).
+        float rs2f[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P at a time
           uint32_t pw[16];
@@ -501,12 +507,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float a0 = x[j] - m_use, a1 = x[j + 1] - m_use;
             const float p0 = (j & 7) < kPolyOf8 ? exp2_poly(a0) : fast_exp2(a0);
             const float p1 = ((j + 1) & 7) < kPolyOf8 ? exp2_poly(a1) : fast_exp2(a1);
-            rs[e & 3] += p0 + p1;
+            rs2f[e & 3] += p0 + p1;
             pw[e] = pack_f16x2(p0, p1);
           }
           tmem_st16(tP + q4 * 16, pw);  // this row's P: keys 2c, 2c+1 in column c
         }
-        const float rowsum = (rs[0] + rs[1]) + (rs[2] + rs[3]);
+        const float rowsum = (rs2f[0] + rs2f[1]) + (rs2f[2] + rs2f[3]);
         l = l * alpha + rowsum;
         PHASE(4);
         if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {
