@@ -21,17 +21,19 @@
 //                and every K tile in shared memory, converts each V tile;
 //                thread r owns row r of a tile
 //   warpgroup 3  warp 12: TMA producer (Q tiles, 4-stage K/V ring);
-//                warp 13: MMA issuer (one thread, tcgen05.mma)
-// Registers are rebalanced with setmaxnreg: 168 for the softmax warpgroups,
-// 128 for RoPE, 48 for the producer / MMA warpgroup (sum 512 x 128).
+//                warps 13, 14: MMA issuers (one thread each, tcgen05.mma), one
+//                per query tile, so the two tiles' MMAs never wait on each other
+// Registers are rebalanced with setmaxnreg: 160 for the softmax warpgroups,
+// 136 for RoPE, 56 for the producer / MMA warpgroup (sum 512 x 128).
 // MMA operands are f16 (11-bit significand): q and k are rotated in float32
 // and rounded once to f16 (q times scale*log2(e) first, so S arrives in log2
 // units), V is widened from bf16 exactly, P is rounded to f16.  Inputs must
 // stay inside the f16 range (|value| < 65504; conversions saturate).
 // TMEM (512 columns): S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383,
 // P_A 384..447, P_B 448..511 (f16 P, two per 32-bit column).
-// Per key tile t the MMA thread issues PV_A(t), S_A(t+1), PV_B(t), S_B(t+1),
-// so one warpgroup's softmax overlaps the other's MMAs.  The PV MMAs take P
+// Per key tile t each tile's issuer issues PV(t) then S(t+1) as soon as its
+// softmax warpgroup has stored P(t), so one warpgroup's softmax overlaps the
+// other's MMAs.  The PV MMAs take P
 // from TMEM (A operand) and V from shared memory, and accumulate O in TMEM.  A
 // softmax warpgroup reads S(t) once, takes P(t) = 2^(S - m_ref) against a
 // reference max that moves only when exceeded by more than 2^8 (then O is
@@ -191,9 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&qkv_map);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh->unit_full[i], 1);
-      mbar_init(&sh->unit_empty[i], 4);  // softmax A, softmax B, MMA, RoPE
+      mbar_init(&sh->unit_empty[i], 5);  // softmax A, softmax B, two MMA issuers, RoPE
       mbar_init(&sh->q_full[i], 1);
-      mbar_init(&sh->q_empty[i], 1);
+      mbar_init(&sh->q_empty[i], 2);     // both MMA issuers
       mbar_init(&sh->qrot[i], 1);
       mbar_init(&sh->s_full[i], 1);
       mbar_init(&sh->p_full[i], 1);
@@ -202,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sh->kv_full[i], 1);
       mbar_init(&sh->krot[i], 1);
-      mbar_init(&sh->kv_empty[i], 1);
+      mbar_init(&sh->kv_empty[i], 2);  // both MMA issuers
     }
     sh->abort = 0;
     fence_mbar_init();
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (wg == 3) {
-    regs_dec<48>();
+    regs_dec<56>();
     if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       griddep_wait();  // the schedule written by the kernel before this one
@@ -273,9 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
       PHASE_FLUSH(48, true);
-    } else if (warp == 13 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
-      uint32_t n = 0, c = 0, pc[2] = {0, 0};
+    } else if ((warp == 13 || warp == 14) && lane == 0) {
+      // ---------------------------------------------------------- MMA issuers
+      // one per query tile (warp 13: tile A, warp 14: tile B), so neither
+      // softmax warpgroup's MMAs queue behind the other's
+      const int w = warp - 13;
+      uint32_t n = 0, c = 0, pc = 0;
+      const uint32_t tS = tmem + w * 128, tO = tmem + 256 + w * 64, tP = tmem + 384 + w * 64;
       PHASE_DECL;
       for (;; ++n) {
         const int slot = n & 1;
@@ -284,74 +290,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         PHASE(0);
         const UnitInfo inf = sh->info[slot];
         if (inf.u < 0) break;
-        int kb0, ke0, kb1 = 0, ke1 = 0, fb, fe;
-        tile_ranges(inf.L, inf.qt0, p.causal, p.window, kb0, ke0, fb, fe);
-        if (inf.nt == 2) tile_ranges(inf.L, inf.qt0 + 1, p.causal, p.window, kb1, ke1, fb, fe);
-        const uint32_t aq = smem_u32(smem + kOffQ + slot * 2 * kTile);
+        int kb = 0, ke = 0, fb, fe;  // this tile's range; empty when the unit has no tile B
+        if (w < inf.nt) tile_ranges(inf.L, inf.qt0 + w, p.causal, p.window, kb, ke, fb, fe);
+        const uint32_t aq = smem_u32(smem + kOffQ + slot * 2 * kTile) + w * kTile;
         PHASE(4);
         bool ok = wait(&sh->qrot[slot], (n >> 1) & 1);
         PHASE(1);
-        auto in_range = [&](int w, int t) { return w == 0 ? (t >= kb0 && t < ke0) : (t >= kb1 && t < ke1); };
-        auto issue_s = [&](int w, int stage) {
+        auto issue_s = [&](int stage) {
           tc_fence_after();
           const uint32_t bk = smem_u32(smem + kOffK + stage * kTile);
-          const uint32_t aqw = aq + w * kTile;
 #pragma unroll
           for (int ks = 0; ks < kHead / 16; ++ks)
-            tc_mma_ss(tmem + w * 128, sdesc_sw128(aqw + ks * 32, 16, 1024), sdesc_sw128(bk + ks * 32, 16, 1024),
-                      kIdescS, ks > 0);
+            tc_mma_ss(tS, sdesc_sw128(aq + ks * 32, 16, 1024), sdesc_sw128(bk + ks * 32, 16, 1024), kIdescS, ks > 0);
           tc_commit(&sh->s_full[w]);
         };
-        // S for the first key tile
-        if (ok) {
-          const int st = c % kStages;
-          ok = wait(&sh->kv_full[st], (c / kStages) & 1) && wait(&sh->krot[st], (c / kStages) & 1);
+        auto wait_k = [&](uint32_t cc) {  // K tile number cc of the ring landed and rotated
+          const uint32_t ph = (cc / kStages) & 1;
+          return wait(&sh->kv_full[cc % kStages], ph) && wait(&sh->krot[cc % kStages], ph);
+        };
+        // the first S of this tile's range (it may start after the unit's first key tile)
+        if (ok && ke > kb) {
+          PHASE(4);
+          ok = wait_k(c + (kb - inf.kb));
           PHASE(2);
-          for (int w = 0; ok && w < inf.nt; ++w)
-            if (in_range(w, inf.kb)) issue_s(w, st);
+          if (ok) issue_s((c + (kb - inf.kb)) % kStages);
+          PHASE(6);
         }
         for (int t = inf.kb; ok && t < inf.ke; ++t, ++c) {
-          const int st = c % kStages, st1 = (c + 1) % kStages;
-          bool next_ready = false;
-          for (int w = 0; ok && w < inf.nt; ++w) {
-            if (in_range(w, t)) {
-              PHASE(4);
-              if (!(ok = wait(&sh->p_full[w], (pc[w]++) & 1))) break;
-              PHASE(3);
-              tc_fence_after();
-              const uint32_t bv = smem_u32(smem + kOffV + st * kTile);
-              const uint32_t acc0 = (w == 0 ? t > kb0 : t > kb1) ? 1u : 0u;
+          const int st = c % kStages;
+          if (t >= kb && t < ke) {
+            PHASE(4);
+            if (!(ok = wait(&sh->p_full[w], (pc++) & 1))) break;
+            PHASE(3);
+            tc_fence_after();
+            const uint32_t bv = smem_u32(smem + kOffV + st * kTile);
+            const uint32_t acc0 = t > kb ? 1u : 0u;
 #pragma unroll
-              for (int ks = 0; ks < kBN / 16; ++ks)
-                tc_mma_ts(tmem + 256 + w * 64, tmem + 384 + w * 64 + ks * 8, sdesc_sw128(bv + ks * 2048, 0, 1024),
-                          kIdescPV, ks > 0 ? 1u : acc0);
-              tc_commit(&sh->pv_full[w]);
-              PHASE(5);
-            }
-            if (t + 1 < inf.ke && in_range(w, t + 1)) {
-              if (!next_ready) {
-                const uint32_t ph1 = ((c + 1) / kStages) & 1;
-                PHASE(4);
-                if (!(ok = wait(&sh->kv_full[st1], ph1) && wait(&sh->krot[st1], ph1))) break;
-                PHASE(2);
-                next_ready = true;
-              }
-              issue_s(w, st1);
+            for (int ks = 0; ks < kBN / 16; ++ks)
+              tc_mma_ts(tO, tP + ks * 8, sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, ks > 0 ? 1u : acc0);
+            tc_commit(&sh->pv_full[w]);
+            PHASE(5);
+            if (t + 1 < ke) {
+              PHASE(4);
+              if (!(ok = wait_k(c + 1))) break;
+              PHASE(2);
+              issue_s((c + 1) % kStages);
               PHASE(6);
             }
           }
-          tc_commit(&sh->kv_empty[st]);  // every MMA reading stage st is issued
-          if (t + 1 == inf.ke) tc_commit(&sh->q_empty[slot]);  // the unit's last S is issued
+          tc_commit(&sh->kv_empty[st]);  // this issuer's MMAs reading stage st are issued
+          if (t + 1 == inf.ke) tc_commit(&sh->q_empty[slot]);  // and its last S of the unit
           PHASE(7);
         }
         if (!ok) break;
         mbar_arrive(&sh->unit_empty[slot]);
       }
-      PHASE_FLUSH(40, true);
+      PHASE_FLUSH(w == 0 ? 40 : 56, true);
     }
     __syncwarp();
   } else if (wg == 2) {
-    // keeps the 128 registers per thread it was launched with
+    regs_inc<136>();
     // ------------------------------------------------------------ RoPE
     const int r = tid - 256;  // row of every tile this thread converts
     uint32_t n = 0, c = 0;
@@ -409,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     PHASE_FLUSH(32, r == 0);
   } else {
-    regs_inc<168>();
+    regs_inc<160>();
     // ------------------------------------------------------------ softmax warpgroups
     const int w = wg;                  // 0: tile A, 1: tile B
     const int r = tid & 127;           // row in the tile = TMEM lane
