@@ -56,6 +56,10 @@ def _load():
         lib.kime_oracle_kv_append.restype = I
         lib.kime_oracle_attn_decode.argtypes = [P, P, I, I, I, I, D, P, P, I, P, P, P, L, P, I]
         lib.kime_oracle_attn_decode.restype = I
+        lib.kime_oracle_kv_append_varlen.argtypes = [P, P, P, I, I, I, I, P, P, I, P, P]
+        lib.kime_oracle_kv_append_varlen.restype = I
+        lib.kime_oracle_attn_chunk.argtypes = [P, P, P, I, I, I, I, D, P, P, I, P, P, P, P, L, P, I]
+        lib.kime_oracle_attn_chunk.restype = I
         _lib = lib
     return _lib
 
@@ -206,6 +210,56 @@ def attn_decode(qkv_new_bits, pos, heads, kv_heads, cap, scale, cos, sin, k_cach
                                      _ptr(cos), _ptr(sin), cos.shape[0], _ptr(k_cache_bits),
                                      _ptr(v_cache_bits), _ptr(ip), n_items, _ptr(out),
                                      _threads(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out
+
+
+def kv_append_varlen(qkv_bits, cu, pos, heads, kv_heads, cap, cos32, sin32, k_cache_bits, v_cache_bits):
+    """Multi-token in-place append: row i of sequence s goes to cache row
+    pos[s] + i of uint16 (bfloat16 bits) caches [n, kv_heads, cap, 64].
+    Returns the number of sequences skipped for out-of-range positions."""
+    lib = _load()
+    q = np.ascontiguousarray(qkv_bits, np.uint16)
+    cu = np.ascontiguousarray(cu, np.int32)
+    pos = np.ascontiguousarray(pos, np.int32)
+    assert len(cu) == len(pos) + 1
+    c = np.ascontiguousarray(cos32, np.float32)
+    s = np.ascontiguousarray(sin32, np.float32)
+    assert k_cache_bits.dtype == np.uint16 and k_cache_bits.flags.c_contiguous
+    assert v_cache_bits.dtype == np.uint16 and v_cache_bits.flags.c_contiguous
+    return lib.kime_oracle_kv_append_varlen(_ptr(q), _ptr(cu), _ptr(pos), len(pos), heads, kv_heads, cap,
+                                            _ptr(c), _ptr(s), c.shape[0], _ptr(k_cache_bits),
+                                            _ptr(v_cache_bits))
+
+
+def attn_chunk(qkv_bits, cu, pos, heads, kv_heads, cap, scale, cos, sin, k_cache_bits, v_cache_bits,
+               rows=None, row_heads=None, nthreads=None):
+    """Chunked-prefill outputs in float64: row i of sequence s (position
+    pos[s] + i) attends cache rows 0..pos[s]+i.  The caches must already hold
+    the chunk (``kv_append_varlen``).  rows=None: [T, heads*64]; else the
+    (row, head) items, [n, 64]."""
+    lib = _load()
+    q = np.ascontiguousarray(qkv_bits, np.uint16)
+    cu = np.ascontiguousarray(cu, np.int32)
+    pos = np.ascontiguousarray(pos, np.int32)
+    n = len(pos)
+    assert len(cu) == n + 1
+    cos = np.ascontiguousarray(cos, np.float64)
+    sin = np.ascontiguousarray(sin, np.float64)
+    if rows is None:
+        T = int(cu[-1]) if n > 0 else 0
+        out = np.zeros((T, heads * 64), np.float64)
+        n_items, rp, hp = T * heads, None, None
+    else:
+        rp = np.ascontiguousarray(rows, np.int32)
+        hp = np.ascontiguousarray(row_heads, np.int32)
+        n_items = len(rp)
+        out = np.zeros((n_items, 64), np.float64)
+    rc = lib.kime_oracle_attn_chunk(_ptr(q), _ptr(cu), _ptr(pos), n, heads, kv_heads, cap, float(scale),
+                                    _ptr(cos), _ptr(sin), cos.shape[0], _ptr(k_cache_bits),
+                                    _ptr(v_cache_bits), _ptr(rp), _ptr(hp), n_items, _ptr(out),
+                                    _threads(nthreads))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return out

@@ -1,7 +1,7 @@
 /*
  * kime_oracle.c -- plain FP64 CPU oracle for packed variable-length attention
- * with RoPE applied to q and k, the in-place KV-cache append and single-token
- * decode.
+ * with RoPE applied to q and k, the in-place KV-cache append, single-token
+ * decode and chunked prefill against the cache.
  *
  * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
  * cpu_baseline / reference legs of bench.py may load this library.  It shares
@@ -29,6 +29,10 @@
  *                    h / (heads/kv_heads).
  *                  - KvAppend: write rows at pos, checking pos+seq <= cap
  *                    before anything is written.
+ *                  - TextTower::block, KV cache: a block of seq new tokens at
+ *                    index_pos is written into the preallocated cache, then
+ *                    attends cache rows 0..index_pos+seq with CausalSoftmax
+ *                    offset index_pos (chunked prefill; decode is seq = 1).
  *
  * Everything is computed in double precision.  Inputs are widened exactly
  * (float64, float32, or bfloat16 bit patterns).  The one place the oracle
@@ -413,6 +417,146 @@ int kime_oracle_attn_decode(const uint16_t *qkv_new, const int32_t *pos, int n_s
                                k_cache, v_cache, items, n_items, out, t, nthreads};
         if (nthreads == 1) decode_worker(&jobs[t]);
         else pthread_create(&th[t], NULL, decode_worker, &jobs[t]);
+    }
+    if (nthreads > 1)
+        for (int t = 0; t < nthreads; t++) pthread_join(th[t], NULL);
+    return 0;
+}
+
+/* ---- chunked prefill against the cache ([argus] TextTower::block) -------- */
+
+/* Multi-token append: sequence s owns rows cu[s]..cu[s+1]-1 of qkv
+ * [T, 64*(heads+2*kv_heads)] (bfloat16 bits); its row i is the token at
+ * position pos[s] + i, whose k heads (rotated there) and v heads go to cache
+ * row pos[s] + i.  [argus] KvAppend refuses a block with pos + seq > cap before
+ * writing anything: a sequence with pos[s] < 0 or pos[s] + L above cap or
+ * rope_len is not written at all, and the return value counts those.  The
+ * rotation and rounding are the single-token append's. */
+int kime_oracle_kv_append_varlen(const uint16_t *qkv, const int32_t *cu, const int32_t *pos, int n_seqs,
+                                 int heads, int kv_heads, int cap, const float *cos_t, const float *sin_t,
+                                 int rope_len, uint16_t *k_cache, uint16_t *v_cache) {
+    size_t W = (size_t)HEAD * (heads + 2 * kv_heads);
+    int bad = 0;
+    for (int s = 0; s < n_seqs; s++) {
+        int L = cu[s + 1] - cu[s], P0 = pos[s];
+        if (P0 < 0 || (long)P0 + L > cap || (long)P0 + L > rope_len) {
+            bad++;
+            continue;
+        }
+        for (int i = 0; i < L; i++) {
+            int P = P0 + i;
+            const uint16_t *row = qkv + (size_t)(cu[s] + i) * W;
+            const float *c = cos_t + (size_t)P * HALF, *sn = sin_t + (size_t)P * HALF;
+            for (int g = 0; g < kv_heads; g++) {
+                const uint16_t *xk = row + (size_t)(heads + g) * HEAD;
+                const uint16_t *xv = row + (size_t)(heads + kv_heads + g) * HEAD;
+                size_t dst = (((size_t)s * kv_heads + g) * cap + P) * HEAD;
+                for (int t = 0; t < HALF; t++) {
+                    float a = (float)bf16_bits_to_double(xk[t]);
+                    float b = (float)bf16_bits_to_double(xk[t + HALF]);
+                    float ac = a * c[t], bs = b * sn[t], bc = b * c[t], as = a * sn[t];
+                    k_cache[dst + t] = kime_oracle_f32_to_bf16(ac - bs);
+                    k_cache[dst + t + HALF] = kime_oracle_f32_to_bf16(bc + as);
+                }
+                for (int t = 0; t < HEAD; t++) v_cache[dst + t] = xv[t];
+            }
+        }
+    }
+    return bad;
+}
+
+typedef struct {
+    const uint16_t *qkv;
+    const int32_t *cu, *pos;
+    int n_seqs, heads, kv_heads, cap;
+    double scale;
+    const double *cos, *sin;
+    const uint16_t *k_cache, *v_cache;
+    const int32_t *rows, *row_heads;
+    long n_items;
+    double *out;
+    int tid, nthreads;
+} chunk_job;
+
+/* Query row r (row i of its sequence s), head h: q is rotated at position
+ * P = pos[s] + i and attends cache rows 0..=P of kv head h/(heads/kv_heads),
+ * the cache already holding the chunk's own keys ([argus] CausalSoftmax: row i
+ * of a block at offset index_pos sees keys 0..=i+offset).  Only visible keys
+ * are visited. */
+static void chunk_one(const chunk_job *d, int r, int h, double *out) {
+    int s = seq_of_row(d->cu, d->n_seqs, r);
+    int P = d->pos[s] + (r - d->cu[s]);
+    int g = h / (d->heads / d->kv_heads);
+    size_t W = (size_t)HEAD * (d->heads + 2 * d->kv_heads);
+    double xq[HEAD], yq[HEAD];
+    for (int t = 0; t < HEAD; t++) xq[t] = bf16_bits_to_double(d->qkv[(size_t)r * W + (size_t)h * HEAD + t]);
+    kime_oracle_rope(xq, d->cos + (size_t)P * HALF, d->sin + (size_t)P * HALF, yq);
+    const uint16_t *K = d->k_cache + ((size_t)s * d->kv_heads + g) * d->cap * HEAD;
+    const uint16_t *V = d->v_cache + ((size_t)s * d->kv_heads + g) * d->cap * HEAD;
+    double *sc = (double *)malloc(sizeof(double) * (size_t)(P + 1));
+    double m = -INFINITY;
+    for (int j = 0; j <= P; j++) {
+        double dot = 0.0;
+        for (int t = 0; t < HEAD; t++) dot += yq[t] * bf16_bits_to_double(K[(size_t)j * HEAD + t]);
+        sc[j] = d->scale * dot;
+        if (sc[j] > m) m = sc[j];
+    }
+    double den = 0.0, num[HEAD];
+    for (int t = 0; t < HEAD; t++) num[t] = 0.0;
+    for (int j = 0; j <= P; j++) {
+        double p = exp(sc[j] - m);
+        den += p;
+        for (int t = 0; t < HEAD; t++) num[t] += p * bf16_bits_to_double(V[(size_t)j * HEAD + t]);
+    }
+    for (int t = 0; t < HEAD; t++) out[t] = num[t] / den;
+    free(sc);
+}
+
+static void *chunk_worker(void *p) {
+    chunk_job *d = (chunk_job *)p;
+    for (long k = d->tid; k < d->n_items; k += d->nthreads) {
+        int r, h;
+        if (d->rows) {
+            r = d->rows[k];
+            h = d->row_heads[k];
+        } else {
+            r = (int)(k / d->heads);
+            h = (int)(k % d->heads);
+        }
+        chunk_one(d, r, h, d->out + (size_t)k * HEAD);
+    }
+    return NULL;
+}
+
+/* Chunked-prefill attention outputs for n_items (token row, head) pairs, or
+ * for every row and head when rows is NULL (then out is [T, heads*64]).  The
+ * caches must already hold every sequence's chunk (kime_oracle_kv_append_varlen).
+ * Returns 0, or a negative code when an argument is malformed or a sequence's
+ * positions leave [0, min(cap, rope_len)). */
+int kime_oracle_attn_chunk(const uint16_t *qkv, const int32_t *cu, const int32_t *pos, int n_seqs, int heads,
+                           int kv_heads, int cap, double scale, const double *cos_t, const double *sin_t,
+                           int rope_len, const uint16_t *k_cache, const uint16_t *v_cache,
+                           const int32_t *rows, const int32_t *row_heads, long n_items, double *out,
+                           int nthreads) {
+    if (heads <= 0 || kv_heads <= 0 || heads % kv_heads || n_seqs < 0) return -1;
+    if (n_seqs > 0 && cu[0] != 0) return -1;
+    for (int s = 0; s < n_seqs; s++) {
+        if (cu[s + 1] < cu[s]) return -1;
+        if (pos[s] < 0 || (long)pos[s] + (cu[s + 1] - cu[s]) > cap ||
+            (long)pos[s] + (cu[s + 1] - cu[s]) > rope_len)
+            return -2;
+    }
+    if (n_seqs == 0) return 0;
+    if (!rows) n_items = (long)cu[n_seqs] * heads;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    chunk_job jobs[256];
+    for (int t = 0; t < nthreads; t++) {
+        jobs[t] = (chunk_job){qkv, cu, pos, n_seqs, heads, kv_heads, cap, scale, cos_t, sin_t,
+                              k_cache, v_cache, rows, row_heads, n_items, out, t, nthreads};
+        if (nthreads == 1) chunk_worker(&jobs[t]);
+        else pthread_create(&th[t], NULL, chunk_worker, &jobs[t]);
     }
     if (nthreads > 1)
         for (int t = 0; t < nthreads; t++) pthread_join(th[t], NULL);

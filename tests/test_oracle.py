@@ -8,7 +8,9 @@ bfloat16 rounding), a closed form, or an invariant stated on the source pages:
       materialising -inf then softmax, bit for bit; the 1/8 scale fold is exact.
   ffai-argus tests: causal rows sum to one with an exactly-zero tail; a decode
       step (offset k_len-1) attends to the whole cache.
-  ffai-argus TextTower::block: GQA fold = MHA with kv heads repeated.
+  ffai-argus TextTower::block: GQA fold = MHA with kv heads repeated; a block
+      of new tokens at index_pos is appended to the cache, then attends it
+      with CausalSoftmax offset index_pos.
   kime-cuda 0.0.3 src/plan.rs, fn rope_tables: the table recipe.
 """
 import json
@@ -369,7 +371,7 @@ def test_tile_classification_golden():
     with open(os.path.join(GOLDEN, "tiles_small.json")) as f:
         cases = json.load(f)["cases"]
     for case in cases:
-        got = otiles.classify(cu_of(case["lengths"]), case["causal"], case["window"])
+        got = otiles.classify(cu_of(case["lengths"]), case["causal"], case["window"], pos=case.get("pos"))
         want = {(int(k.split(",")[0]), int(k.split(",")[1])): v for k, v in case["codes"].items()}
         assert set(got) == set(want), case["name"]
         for key, codes in want.items():
@@ -388,3 +390,173 @@ def test_tile_classification_is_two_nested_intervals():
                 assert len(vis) > 0 and np.all(np.diff(vis) == 1)
                 if len(full):
                     assert np.all(np.diff(full) == 1)
+    for pos in ([0] * 8, [5, 0, 127, 128, 129, 1000, 3, 255]):
+        for (s, qt), codes in otiles.classify(cu_of(lengths), True, -1, pos=pos).items():
+            vis = np.flatnonzero(codes > 0)
+            full = np.flatnonzero(codes == 2)
+            assert len(vis) > 0 and np.all(np.diff(vis) == 1)
+            if len(full):
+                assert np.all(np.diff(full) == 1)
+
+
+# ---- chunked prefill against the cache ------------------------------------------
+
+def bf16_from_bits(b):
+    return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def chunk_setup(lengths, pos, H, Hkv, cap, theta=1e5, seed=0):
+    """Random bf16 chunk rows, caches holding random already-rotated keys and
+    values below each sequence's pos (garbage above), float32 tables."""
+    g = torch.Generator().manual_seed(seed)
+    T = int(sum(lengths))
+    x = torch.randn(T, 64 * (H + 2 * Hkv), generator=g).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16).copy()
+    n = len(lengths)
+    kb = torch.randn(n, Hkv, cap, 64, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    vb = torch.randn(n, Hkv, cap, 64, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    c32, s32 = oracle.rope_tables_f32(theta, cap)
+    return bits, kb, vb, c32, s32
+
+
+def test_kv_append_varlen_rotates_rounds_and_touches_only_its_rows():
+    lengths, pos = [3, 0, 5, 1], np.array([0, 7, 10, 19], np.int32)
+    H, Hkv, cap = 6, 2, 20
+    bits, kb, vb, c, s = chunk_setup(lengths, pos, H, Hkv, cap)
+    k0, v0 = kb.copy(), vb.copy()
+    cu = cu_of(lengths)
+    assert oracle.kv_append_varlen(bits, cu, pos, H, Hkv, cap, c, s, kb, vb) == 0
+    x = bf16_from_bits(bits).astype(np.float32)
+    touched = np.zeros(kb.shape, bool)
+    for si, L in enumerate(lengths):
+        for i in range(L):
+            r, P = cu[si] + i, pos[si] + i
+            for g in range(Hkv):
+                xk = x[r, (H + g) * 64:(H + g + 1) * 64]
+                a, b = xk[:32], xk[32:]
+                y = np.concatenate([a * c[P] - b * s[P], b * c[P] + a * s[P]]).astype(np.float32)
+                assert np.array_equal(kb[si, g, P], bf16_round_np(y))
+                assert np.array_equal(vb[si, g, P], bits[r, (H + Hkv + g) * 64:(H + Hkv + g + 1) * 64])
+            touched[si, :, P] = True
+    assert np.array_equal(kb[~touched], k0[~touched]) and np.array_equal(vb[~touched], v0[~touched])
+    # a sequence whose block would leave [0, cap) (or the tables) writes nothing
+    kb2, vb2 = k0.copy(), v0.copy()
+    bad = np.array([-1, 7, 16, 19], np.int32)  # seq 0 negative, seq 2: 16 + 5 > 20
+    assert oracle.kv_append_varlen(bits, cu, bad, H, Hkv, cap, c, s, kb2, vb2) == 2
+    assert np.array_equal(kb2[[0, 2]], k0[[0, 2]]) and np.array_equal(vb2[[0, 2]], v0[[0, 2]])
+    assert not np.array_equal(kb2[3], k0[3])
+    short_c, short_s = c[:20], s[:20]
+    kb3, vb3 = k0.copy(), v0.copy()
+    assert oracle.kv_append_varlen(bits, cu, pos, H, Hkv, cap, short_c[:19], short_s[:19], kb3, vb3) == 1
+
+
+def test_chunk_matches_dense_brute_force():
+    lengths, pos = [4, 1, 0, 7], np.array([0, 9, 3, 25], np.int32)
+    H, Hkv, cap = 6, 2, 40
+    G = H // Hkv
+    bits, kb, vb, c32, s32 = chunk_setup(lengths, pos, H, Hkv, cap, seed=3)
+    cu = cu_of(lengths)
+    oracle.kv_append_varlen(bits, cu, pos, H, Hkv, cap, c32, s32, kb, vb)
+    c, s = c32.astype(np.float64), s32.astype(np.float64)
+    got = oracle.attn_chunk(bits, cu, pos, H, Hkv, cap, 0.125, c, s, kb, vb)
+    kf, vf, x = bf16_from_bits(kb), bf16_from_bits(vb), bf16_from_bits(bits)
+    for si, L in enumerate(lengths):
+        if L == 0:
+            continue
+        P = pos[si] + np.arange(L)
+        Lk = pos[si] + L
+        vis = np.arange(Lk)[None, :] <= P[:, None]
+        for h in range(H):
+            g = h // G
+            q = rotate_complex(x[cu[si]:cu[si + 1], h * 64:(h + 1) * 64], c[P], s[P])
+            S = np.where(vis, 0.125 * (q @ kf[si, g, :Lk].T), -np.inf)
+            Pm = np.exp(S - S.max(axis=1, keepdims=True))
+            ref = (Pm / Pm.sum(axis=1, keepdims=True)) @ vf[si, g, :Lk]
+            np.testing.assert_allclose(got[cu[si]:cu[si + 1], h * 64:(h + 1) * 64], ref, rtol=0, atol=1e-12)
+
+
+def test_chunk_equals_trailing_rows_of_causal_prefill_bitwise():
+    # Identity tables (cos 1, sin 0): a cache holding the raw keys of tokens
+    # 0..pos-1 plus a chunk of the next L tokens is causal prefill over pos+L
+    # tokens, whose last L rows the chunk must reproduce bit for bit.
+    H, Hkv = 6, 2
+    seqs = [(0, 5), (17, 1), (40, 9)]  # (pos, L)
+    cap = 64
+    g = torch.Generator().manual_seed(11)
+    W = 64 * (H + 2 * Hkv)
+    full = [torch.randn(p + L, W, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            for p, L in seqs]
+    ones, zeros = np.ones((cap, 32), np.float32), np.zeros((cap, 32), np.float32)
+    kb = np.zeros((len(seqs), Hkv, cap, 64), np.uint16)
+    vb = np.zeros((len(seqs), Hkv, cap, 64), np.uint16)
+    for si, (p, L) in enumerate(seqs):
+        for gg in range(Hkv):
+            kb[si, gg, :p] = full[si][:p, (H + gg) * 64:(H + gg + 1) * 64]
+            vb[si, gg, :p] = full[si][:p, (H + Hkv + gg) * 64:(H + Hkv + gg + 1) * 64]
+    chunk = np.concatenate([f[p:] for f, (p, L) in zip(full, seqs)])
+    cu = cu_of([L for p, L in seqs])
+    pos = np.array([p for p, L in seqs], np.int32)
+    assert oracle.kv_append_varlen(chunk, cu, pos, H, Hkv, cap, ones, zeros, kb, vb) == 0
+    got = oracle.attn_chunk(chunk, cu, pos, H, Hkv, cap, 0.125, ones.astype(np.float64),
+                            zeros.astype(np.float64), kb, vb)
+    for si, (p, L) in enumerate(seqs):
+        pre = oracle.attn_varlen(full[si], np.array([0, p + L], np.int32), H, Hkv, -1, True, 0.125,
+                                 ones.astype(np.float64), zeros.astype(np.float64))
+        assert np.array_equal(got[cu[si]:cu[si + 1]], pre[p:])
+
+
+def test_chunk_split_in_two_is_bitwise_equal():
+    # Prefilling a block in one chunk or in two consecutive chunks (the second
+    # at pos + L1) leaves the same cache and gives the same rows, bit for bit.
+    lengths, pos = [9, 6], np.array([3, 0], np.int32)
+    H, Hkv, cap = 4, 2, 32
+    bits, kb, vb, c32, s32 = chunk_setup(lengths, pos, H, Hkv, cap, seed=5)
+    c, s = c32.astype(np.float64), s32.astype(np.float64)
+    cu = cu_of(lengths)
+    k1, v1 = kb.copy(), vb.copy()
+    oracle.kv_append_varlen(bits, cu, pos, H, Hkv, cap, c32, s32, k1, v1)
+    one = oracle.attn_chunk(bits, cu, pos, H, Hkv, cap, 0.125, c, s, k1, v1)
+    split = [4, 2]
+    first = np.concatenate([bits[cu[i]:cu[i] + split[i]] for i in range(2)])
+    second = np.concatenate([bits[cu[i] + split[i]:cu[i + 1]] for i in range(2)])
+    cu1, cu2 = cu_of(split), cu_of([lengths[i] - split[i] for i in range(2)])
+    pos2 = pos + np.array(split, np.int32)
+    k2, v2 = kb.copy(), vb.copy()
+    oracle.kv_append_varlen(first, cu1, pos, H, Hkv, cap, c32, s32, k2, v2)
+    a = oracle.attn_chunk(first, cu1, pos, H, Hkv, cap, 0.125, c, s, k2, v2)
+    oracle.kv_append_varlen(second, cu2, pos2, H, Hkv, cap, c32, s32, k2, v2)
+    b = oracle.attn_chunk(second, cu2, pos2, H, Hkv, cap, 0.125, c, s, k2, v2)
+    assert np.array_equal(k1, k2) and np.array_equal(v1, v2)
+    for i in range(2):
+        assert np.array_equal(one[cu[i]:cu[i] + split[i]], a[cu1[i]:cu1[i + 1]])
+        assert np.array_equal(one[cu[i] + split[i]:cu[i + 1]], b[cu2[i]:cu2[i + 1]])
+
+
+def test_chunk_of_one_token_equals_decode_bitwise():
+    lengths, pos = [1, 1, 1], np.array([0, 13, 30], np.int32)
+    H, Hkv, cap = 6, 3, 31
+    bits, kb, vb, c32, s32 = chunk_setup(lengths, pos, H, Hkv, cap, seed=8)
+    c, s = c32.astype(np.float64), s32.astype(np.float64)
+    k1, v1, k2, v2 = kb.copy(), vb.copy(), kb.copy(), vb.copy()
+    oracle.kv_append_varlen(bits, cu_of(lengths), pos, H, Hkv, cap, c32, s32, k1, v1)
+    oracle.kv_append(bits, pos, H, Hkv, cap, c32, s32, k2, v2)
+    assert np.array_equal(k1, k2) and np.array_equal(v1, v2)
+    ch = oracle.attn_chunk(bits, cu_of(lengths), pos, H, Hkv, cap, 0.125, c, s, k1, v1)
+    dec = oracle.attn_decode(bits, pos, H, Hkv, cap, 0.125, c, s, k2, v2)
+    assert np.array_equal(ch, dec)
+
+
+def test_chunk_sampled_rows_equal_full_computation():
+    lengths, pos = [5, 3], np.array([2, 11], np.int32)
+    H, Hkv, cap = 4, 1, 16
+    bits, kb, vb, c32, s32 = chunk_setup(lengths, pos, H, Hkv, cap, seed=9)
+    c, s = c32.astype(np.float64), s32.astype(np.float64)
+    cu = cu_of(lengths)
+    oracle.kv_append_varlen(bits, cu, pos, H, Hkv, cap, c32, s32, kb, vb)
+    full = oracle.attn_chunk(bits, cu, pos, H, Hkv, cap, 0.125, c, s, kb, vb)
+    rows, heads = np.array([0, 4, 5, 7], np.int32), np.array([3, 0, 2, 1], np.int32)
+    part = oracle.attn_chunk(bits, cu, pos, H, Hkv, cap, 0.125, c, s, kb, vb, rows=rows, row_heads=heads)
+    for k, (r, h) in enumerate(zip(rows, heads)):
+        assert np.array_equal(part[k], full[r, h * 64:(h + 1) * 64])
+    with pytest.raises(ValueError):
+        oracle.attn_chunk(bits, cu, np.array([2, 14], np.int32), H, Hkv, cap, 0.125, c, s, kb, vb)
