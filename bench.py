@@ -189,6 +189,37 @@ class DecodeRun:
                                    self.cs, self.sn, out=self.out, workspace=self.ws)
 
 
+class ChunkRun:
+    """Chunked prefill against the KV cache (SmolLM2 shapes): append the chunks
+    and attend, one kime_chunk_step per step (the same positions every step)."""
+
+    def __init__(self, dev):
+        import packed_varlen_attention_kime_gb300 as kime
+        from packed_varlen_attention_kime_gb300.inputs import chunk_case
+        self.kime = kime
+        c = self.case = chunk_case(device=str(dev))
+        self.cu, self.pos = c.cu_seqlens.to(dev), c.pos.to(dev)
+        cs, sn = kime.kime_rope_tables(c.theta, c.cap)
+        self.cs, self.sn = cs.to(dev), sn.to(dev)
+        self.out = torch.empty((c.total, c.heads * 64), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(kime.kime_attn_workspace_bytes(2, len(c.lengths), c.total), dtype=torch.uint8,
+                              device=dev)
+        L = np.array(c.lengths, np.int64)
+        P = c.pos.numpy().astype(np.int64)
+        keys = int((P + L).sum())                       # cache rows each kv head's prefix spans
+        pairs = int((L * P + L * (L + 1) // 2).sum())   # visible (query, key) pairs per head
+        W = c.qkv.shape[1]
+        # qkv rows read + K/V prefixes read + appended K/V rows written + out written
+        self.bytes = int(c.total * W * 2 + keys * c.kv_heads * 256 + c.total * c.kv_heads * 256 +
+                         c.total * c.heads * 128)
+        self.flops = int(4 * 64 * c.heads * pairs)
+
+    def step(self):
+        c = self.case
+        self.kime.kime_chunk_step(c.qkv, self.cu, self.pos, c.max_seqlen, c.heads, c.kv_heads, c.k_cache,
+                                  c.v_cache, c.scale, self.cs, self.sn, out=self.out, workspace=self.ws)
+
+
 def time_fn(fn, n, warmup, flush, stream, events=1):
     """Median and mean ms of fn over n calls, L2 flushed before each; fn gets
     the list of events to record its sub-steps (len events+1)."""
@@ -242,6 +273,16 @@ def extra_measurements(dev, flush, stream, pk, reps=10):
                              "tokens_per_s": round(len(d.case.pos) / (ms * 1e-3)), "bytes": d.bytes}
     del d
     torch.cuda.empty_cache()
+    ch = ChunkRun(dev)
+    per, _ = time_fn(lambda ev: ch.step(), reps, 3, flush, stream)
+    ms = statistics.median(per)
+    tf = ch.flops / (ms * 1e-3) / 1e12
+    out["smollm2_chunk"] = {"ms": round(ms, 4), "tflops": round(tf, 2), "tc_frac": round(tf / pk["bf16_tflops"], 4),
+                            "gbs": round(ch.bytes / (ms * 1e-3) / 1e9, 1),
+                            "tokens_per_s": round(ch.case.total / (ms * 1e-3)), "flops": ch.flops,
+                            "bytes": ch.bytes}
+    del ch
+    torch.cuda.empty_cache()
     return out
 
 
@@ -288,7 +329,7 @@ def main():
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s load before the timed steps")
     ap.add_argument("--only", default=None,
                     help="profiling aid: run only WORKLOAD[:LAYER] (modernbert_base, modernbert_large, "
-                         "smollm2_prefill, smollm2_decode) for --steps steps and print its timings")
+                         "smollm2_prefill, smollm2_decode, smollm2_chunk) for --steps steps and print its timings")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -407,8 +448,8 @@ def only_arm(args, local):
     stream = torch.cuda.current_stream(dev)
     flush = l2_flush_buffer(dev)
     name, _, layer = args.only.partition(":")
-    if name == "smollm2_decode":
-        d = DecodeRun(dev)
+    if name in ("smollm2_decode", "smollm2_chunk"):
+        d = DecodeRun(dev) if name == "smollm2_decode" else ChunkRun(dev)
         per, _ = time_fn(lambda ev: d.step(), args.steps, args.warmup, flush, stream)
         print(json.dumps({"only": name, "ms": [round(x, 4) for x in per]}))
         return

@@ -108,7 +108,7 @@ int kime_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int head
  *  qkv_new, pos, caches as for kime_kv_append (caches are read only)
  *  out          device bf16 [n_seqs, heads*64]
  *  workspace    device scratch of kime_attn_workspace_bytes(1, ...) bytes
- * Split-KV over chunks of 256 keys with a merge by the last chunk to finish;
+ * Split-KV, 256 keys per CTA, with a merge by the last CTA to finish;
  * heads/kv_heads must be 1..8.  One memset of the per-(sequence, kv head)
  * tickets and one kernel launch. */
 int kime_attn_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
@@ -127,9 +127,62 @@ int kime_decode_step(const void* qkv_new, const int32_t* pos, int n_seqs, int he
                      void* v_cache, void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                      void* stream);
 
-/* Scratch bytes for op 0 (varlen: uses n_seqs, total_tokens) or op 1 (decode:
- * uses n_seqs, heads, kv_heads, cap).  Returns 0 for an unknown op or
- * malformed sizes. */
+/* kime_kv_append_varlen -- multi-token in-place KV-cache append, the first
+ * half of chunked prefill (ffai-argus 0.7.3 src/text.rs, TextTower::block: a
+ * block of seq new tokens at index_pos is written into the preallocated cache,
+ * KvAppend refusing pos + seq > cap before anything is written).
+ *
+ *  qkv          device bf16 [total_tokens, W], W = 64*(heads + 2*kv_heads):
+ *               the new tokens, sequence s owning rows cu[s]..cu[s+1]-1
+ *  cu_seqlens   device int32 [n_seqs+1], cu[0] = 0, cu[n_seqs] = total_tokens
+ *  pos          device int32 [n_seqs]: cache rows already used; row i of
+ *               sequence s is the token at position pos[s] + i
+ *  k_cache/v_cache  device bf16 [n_seqs, kv_heads, cap, 64], 16-byte aligned
+ * Writes k_cache[s,g,pos[s]+i] = bf16(rope(k, pos[s]+i)) (float32 rotation,
+ * one rounding per operation, round to nearest even) and v_cache[s,g,pos[s]+i]
+ * = v for every row; nothing else.  A sequence with pos[s] < 0 or
+ * pos[s] + L > min(cap, rope_len) sets KIME_DEV_BAD_POS and none of its rows
+ * is written; rows outside a valid cu set KIME_DEV_BAD_CU.  pos is not
+ * advanced.  One launch. */
+int kime_kv_append_varlen(const void* qkv, const int32_t* cu_seqlens, const int32_t* pos, int n_seqs,
+                          int total_tokens, int heads, int kv_heads, int head_dim, int cap, const float* rope_cos,
+                          const float* rope_sin, int rope_len, void* k_cache, void* v_cache, int32_t* dev_status,
+                          void* stream);
+
+/* kime_attn_chunk -- the attention half of chunked prefill: row i of sequence
+ * s, at position P = pos[s] + i, attends cache rows 0..=P of its kv head
+ * (ffai-argus CausalSoftmax: row i of a block at offset index_pos sees keys
+ * 0..=i+offset).  The caches must already hold the chunk
+ * (kime_kv_append_varlen on the same stream, or kime_chunk_step).  q is
+ * rotated at P with the tables; cached keys are used as stored.
+ *
+ *  qkv, cu_seqlens, pos, caches  as for kime_kv_append_varlen (caches read only)
+ *  max_seqlen   host upper bound on any chunk length (longer: KIME_DEV_SEQ_TOO_LONG)
+ *  scale        softmax scale (> 0, finite)
+ *  out          device bf16 [total_tokens, heads*64]
+ *  workspace    device scratch of kime_attn_workspace_bytes(2, n_seqs,
+ *               total_tokens, ...) bytes
+ * BF16 inputs on the tensor cores, FP32 accumulation: the prefill kernel of
+ * kime_attn_varlen with K/V tiles taken from the cache.  A sequence whose
+ * positions leave [0, min(cap, rope_len)) sets KIME_DEV_BAD_POS and its rows
+ * of out are not written.  n_seqs*kv_heads*cap must stay below 2^31.  Two
+ * launches (scheduler, attention). */
+int kime_attn_chunk(const void* qkv, const int32_t* cu_seqlens, const int32_t* pos, int n_seqs, int total_tokens,
+                    int max_seqlen, int heads, int kv_heads, int head_dim, int cap, float scale,
+                    const float* rope_cos, const float* rope_sin, int rope_len, const void* k_cache,
+                    const void* v_cache, void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                    void* stream);
+
+/* kime_chunk_step -- kime_kv_append_varlen then kime_attn_chunk on one stream
+ * (three launches).  Arguments as kime_attn_chunk, with writable caches. */
+int kime_chunk_step(const void* qkv, const int32_t* cu_seqlens, const int32_t* pos, int n_seqs, int total_tokens,
+                    int max_seqlen, int heads, int kv_heads, int head_dim, int cap, float scale,
+                    const float* rope_cos, const float* rope_sin, int rope_len, void* k_cache, void* v_cache,
+                    void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* Scratch bytes for op 0 (varlen: uses n_seqs, total_tokens), op 1 (decode:
+ * uses n_seqs, heads, kv_heads, cap) or op 2 (chunked prefill: uses n_seqs,
+ * total_tokens).  Returns 0 for an unknown op or malformed sizes. */
 size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads, int kv_heads, int cap);
 
 /* Host helper: float32 cos/sin tables [len, 32] for heads of 64 by kime-cuda's
@@ -148,6 +201,14 @@ int kime_rope_tables(double theta, int len, float* cos_out, float* sin_out);
 int kime_attn_debug_tiles(const int32_t* cu_seqlens, int n_seqs, int total_tokens, int max_seqlen, int window,
                           int causal, void* workspace, size_t workspace_bytes, int32_t* tiles_out, int max_pairs,
                           int32_t* n_pairs_out, int32_t* dev_status, void* stream);
+
+/* Test aid: kime_attn_debug_tiles for chunks at offsets pos (device int32
+ * [n_seqs]) against a cache of cap rows: key tiles count cache rows from 0,
+ * row i of sequence s sits at position pos[s] + i (causal). */
+int kime_attn_debug_tiles_chunk(const int32_t* cu_seqlens, const int32_t* pos, int n_seqs, int total_tokens,
+                                int max_seqlen, int cap, int rope_len, void* workspace, size_t workspace_bytes,
+                                int32_t* tiles_out, int max_pairs, int32_t* n_pairs_out, int32_t* dev_status,
+                                void* stream);
 
 /* Bytes of the scratch array built into the library for kime_attn_varlen_noalloc. */
 #define KIME_NOALLOC_SCRATCH_BYTES (1u << 20)

@@ -18,7 +18,8 @@ import torch
 __all__ = [
     "KimeError", "load_library", "kime_attn_varlen", "kime_kv_append", "kime_attn_decode",
     "kime_attn_workspace_bytes", "kime_rope_tables", "kime_attn_debug_tiles", "kime_attn_varlen_noalloc",
-    "kime_decode_step", "KIME_F32", "KIME_BF16", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
+    "kime_decode_step", "kime_kv_append_varlen", "kime_attn_chunk", "kime_chunk_step",
+    "kime_attn_debug_tiles_chunk", "KIME_F32", "KIME_BF16", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,7 +31,8 @@ DEV_BAD_CU, DEV_SEQ_TOO_LONG, DEV_BAD_POS, DEV_TIMEOUT = 1, 2, 4, 8
 EXPORTED_SYMBOLS = (
     "kime_attn_varlen", "kime_kv_append", "kime_attn_decode", "kime_attn_workspace_bytes",
     "kime_rope_tables", "kime_attn_debug_tiles", "kime_attn_last_cuda_error", "kime_attn_status_string",
-    "kime_attn_varlen_noalloc", "kime_decode_step",
+    "kime_attn_varlen_noalloc", "kime_decode_step", "kime_kv_append_varlen", "kime_attn_chunk",
+    "kime_chunk_step", "kime_attn_debug_tiles_chunk",
 )
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -70,6 +72,14 @@ def load_library(path: str = LIB_PATH):
     lib.kime_decode_step.restype = I
     lib.kime_attn_varlen_noalloc.argtypes = [P, I, P, I, I, I, I, I, I, I, I, F, P, P, I, P, P, P]
     lib.kime_attn_varlen_noalloc.restype = I
+    lib.kime_kv_append_varlen.argtypes = [P, P, P, I, I, I, I, I, I, P, P, I, P, P, P, P]
+    lib.kime_kv_append_varlen.restype = I
+    lib.kime_attn_chunk.argtypes = [P, P, P, I, I, I, I, I, I, I, F, P, P, I, P, P, P, P, S, P, P]
+    lib.kime_attn_chunk.restype = I
+    lib.kime_chunk_step.argtypes = [P, P, P, I, I, I, I, I, I, I, F, P, P, I, P, P, P, P, S, P, P]
+    lib.kime_chunk_step.restype = I
+    lib.kime_attn_debug_tiles_chunk.argtypes = [P, P, I, I, I, I, I, P, S, P, I, P, P, P]
+    lib.kime_attn_debug_tiles_chunk.restype = I
     lib.kime_attn_last_cuda_error.argtypes = []
     lib.kime_attn_last_cuda_error.restype = I
     lib.kime_attn_status_string.argtypes = [I]
@@ -221,5 +231,70 @@ def kime_attn_debug_tiles(cu_seqlens, total_tokens, max_seqlen, window, causal, 
                                    int(bool(causal)), _p(ws), need, _p(tiles), max_pairs, _p(count),
                                    _p(dev_status), _stream(stream, dev))
     _check("kime_attn_debug_tiles", rc)
+    n = int(count.item())
+    return tiles[:n]
+
+
+def kime_kv_append_varlen(qkv, cu_seqlens, pos, heads, kv_heads, k_cache, v_cache, rope_cos, rope_sin,
+                          dev_status=None, stream=None):
+    """Writes row i of each sequence's block (RoPE'd k, v) at cache row pos[s] + i."""
+    lib = load_library()
+    cap = k_cache.shape[2]
+    rc = lib.kime_kv_append_varlen(_p(qkv), _p(cu_seqlens), _p(pos), pos.numel(), qkv.shape[0], heads, kv_heads,
+                                   64, cap, _p(rope_cos), _p(rope_sin), rope_cos.shape[0], _p(k_cache),
+                                   _p(v_cache), _p(dev_status), _stream(stream, qkv.device))
+    _check("kime_kv_append_varlen", rc)
+
+
+def _chunk(fn, qkv, cu_seqlens, pos, max_seqlen, heads, kv_heads, k_cache, v_cache, scale, rope_cos, rope_sin,
+           out, workspace, dev_status, stream):
+    lib = load_library()
+    T = qkv.shape[0]
+    n = pos.numel()
+    cap = k_cache.shape[2]
+    if out is None:
+        out = torch.empty((T, heads * 64), dtype=torch.bfloat16, device=qkv.device)
+    need = kime_attn_workspace_bytes(2, n, T)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=qkv.device)
+    rc = getattr(lib, fn)(_p(qkv), _p(cu_seqlens), _p(pos), n, T, int(max_seqlen), heads, kv_heads, 64, cap,
+                          float(scale), _p(rope_cos), _p(rope_sin), rope_cos.shape[0], _p(k_cache), _p(v_cache),
+                          _p(out), _p(workspace), workspace.numel() * workspace.element_size(), _p(dev_status),
+                          _stream(stream, qkv.device))
+    _check(fn, rc)
+    return out
+
+
+def kime_attn_chunk(qkv, cu_seqlens, pos, max_seqlen, heads, kv_heads, k_cache, v_cache, scale, rope_cos,
+                    rope_sin, out=None, workspace=None, dev_status=None, stream=None):
+    """Chunked-prefill attention: row i of sequence s attends cache rows
+    0..pos[s]+i (the caches already hold the chunk); returns ``out``."""
+    return _chunk("kime_attn_chunk", qkv, cu_seqlens, pos, max_seqlen, heads, kv_heads, k_cache, v_cache, scale,
+                  rope_cos, rope_sin, out, workspace, dev_status, stream)
+
+
+def kime_chunk_step(qkv, cu_seqlens, pos, max_seqlen, heads, kv_heads, k_cache, v_cache, scale, rope_cos,
+                    rope_sin, out=None, workspace=None, dev_status=None, stream=None):
+    """kime_kv_append_varlen then kime_attn_chunk; returns ``out``."""
+    return _chunk("kime_chunk_step", qkv, cu_seqlens, pos, max_seqlen, heads, kv_heads, k_cache, v_cache, scale,
+                  rope_cos, rope_sin, out, workspace, dev_status, stream)
+
+
+def kime_attn_debug_tiles_chunk(cu_seqlens, pos, total_tokens, max_seqlen, cap, rope_len, dev_status=None,
+                                stream=None):
+    """The scheduler's work list for chunks at offsets pos (causal): int32
+    [n_pairs, 8] rows of (s, qt, kt_begin, kt_end, full_begin, full_end, row0, L)."""
+    lib = load_library()
+    n_seqs = cu_seqlens.numel() - 1
+    dev = cu_seqlens.device
+    max_pairs = total_tokens // 128 + n_seqs + 1
+    need = kime_attn_workspace_bytes(2, n_seqs, total_tokens)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    tiles = torch.zeros((max_pairs, 8), dtype=torch.int32, device=dev)
+    count = torch.zeros(1, dtype=torch.int32, device=dev)
+    rc = lib.kime_attn_debug_tiles_chunk(_p(cu_seqlens), _p(pos), n_seqs, int(total_tokens), int(max_seqlen),
+                                         int(cap), int(rope_len), _p(ws), need, _p(tiles), max_pairs, _p(count),
+                                         _p(dev_status), _stream(stream, dev))
+    _check("kime_attn_debug_tiles_chunk", rc)
     n = int(count.item())
     return tiles[:n]

@@ -36,8 +36,9 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D map over the bf16 qkv buffer [total, W]: boxes of 128 rows x 64 columns
-// (one head of 128 tokens), 128-byte swizzle, rows past `total` read as zero.
+// 2-D map over a bf16 row buffer [total, W] (the qkv rows, or a KV cache seen
+// as [n_seqs*kv_heads*cap, 64]): boxes of 128 rows x 64 columns (one head of
+// 128 tokens), 128-byte swizzle, rows past `total` read as zero.
 int encode_qkv_map(CUtensorMap* map, const void* qkv, int total, int W) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return KIME_ECUDA;
@@ -75,6 +76,10 @@ size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads
     if (!heads_ok(heads, kv_heads, kime::kHead) || cap <= 0) return 0;
     return kime::decode_workspace_bytes(n_seqs, heads, kv_heads, cap);
   }
+  if (op == 2) {
+    if (total_tokens < 0) return 0;
+    return varlen_ws_bytes(n_seqs, total_tokens);
+  }
   return 0;
 }
 
@@ -98,9 +103,8 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int max_pairs = kime::max_pairs_for(n_seqs, total_tokens);
-  int rc = cuda_status(
-      kime::launch_schedule(cu_seqlens, n_seqs, total_tokens, max_seqlen, causal, window, workspace, max_pairs,
-                            dev_status, st));
+  int rc = cuda_status(kime::launch_schedule(cu_seqlens, nullptr, n_seqs, total_tokens, max_seqlen, causal, window,
+                                             0, 0, workspace, max_pairs, dev_status, st));
   if (rc) return rc;
   if (dtype == KIME_F32) {
     return cuda_status(kime::launch_varlen_f32(static_cast<const float*>(qkv), cu_seqlens, n_seqs, total_tokens,
@@ -110,8 +114,9 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
   CUtensorMap map;
   rc = encode_qkv_map(&map, qkv, total_tokens, static_cast<int>(W));
   if (rc) return rc;
-  return cuda_status(kime::launch_prefill_tc(&map, n_seqs, total_tokens, heads, kv_heads, window, causal, scale,
-                                             rope_cos, rope_sin, out, workspace, max_pairs, dev_status, st));
+  return cuda_status(kime::launch_prefill_tc(&map, nullptr, nullptr, n_seqs, total_tokens, heads, kv_heads, 0, window,
+                                             causal, scale, rope_cos, rope_sin, out, workspace, max_pairs,
+                                             dev_status, st));
 }
 
 int kime_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
@@ -129,6 +134,62 @@ int kime_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int head
 }  // extern "C"
 
 namespace {
+
+// Host checks shared by the chunked-prefill entry points (append: out and
+// workspace unused).
+int chunk_args_ok(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total, int heads,
+                  int kv_heads, int head_dim, int cap, const float* rope_cos, const float* rope_sin, int rope_len,
+                  const void* k_cache, const void* v_cache) {
+  if (!heads_ok(heads, kv_heads, head_dim) || n_seqs < 0 || total < 0 || cap <= 0 || rope_len < 0)
+    return KIME_EINVAL;
+  if (n_seqs == 0 || total == 0) return KIME_OK;
+  if (!qkv || !cu || !pos || !rope_cos || !rope_sin || !k_cache || !v_cache) return KIME_EINVAL;
+  if (!aligned16(qkv) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(rope_cos) || !aligned16(rope_sin))
+    return KIME_EINVAL;
+  const long long W = 64LL * (heads + 2LL * kv_heads);
+  if (W > (1LL << 30) || static_cast<long long>(total) * W > (1LL << 46)) return KIME_ERANGE;
+  if (static_cast<long long>(n_seqs) * kv_heads * cap >= (1LL << 31)) return KIME_ERANGE;
+  return KIME_OK;
+}
+
+int chunk_attend(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total, int max_seqlen,
+                 int heads, int kv_heads, int cap, float scale, const float* rope_cos, const float* rope_sin,
+                 int rope_len, const void* k_cache, const void* v_cache, void* out, void* workspace,
+                 int32_t* dev_status, cudaStream_t st) {
+  const int max_pairs = kime::max_pairs_for(n_seqs, total);
+  int rc = cuda_status(kime::launch_schedule(cu, pos, n_seqs, total, max_seqlen, 1, -1, cap, rope_len, workspace,
+                                             max_pairs, dev_status, st));
+  if (rc) return rc;
+  const int W = 64 * (heads + 2 * kv_heads), rows = n_seqs * kv_heads * cap;
+  CUtensorMap qmap, kmap, vmap;
+  if ((rc = encode_qkv_map(&qmap, qkv, total, W))) return rc;
+  if ((rc = encode_qkv_map(&kmap, k_cache, rows, kime::kHead))) return rc;
+  if ((rc = encode_qkv_map(&vmap, v_cache, rows, kime::kHead))) return rc;
+  return cuda_status(kime::launch_prefill_tc(&qmap, &kmap, &vmap, n_seqs, total, heads, kv_heads, cap, -1, 1, scale,
+                                             rope_cos, rope_sin, out, workspace, max_pairs, dev_status, st));
+}
+
+int chunk_common(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total, int max_seqlen,
+                 int heads, int kv_heads, int head_dim, int cap, float scale, const float* rope_cos,
+                 const float* rope_sin, int rope_len, const void* k_cache, const void* v_cache, void* out,
+                 void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream, bool append) {
+  int rc = chunk_args_ok(qkv, cu, pos, n_seqs, total, heads, kv_heads, head_dim, cap, rope_cos, rope_sin, rope_len,
+                         k_cache, v_cache);
+  if (rc) return rc;
+  if (!(scale > 0.f) || !isfinite(scale) || max_seqlen < 0) return KIME_EINVAL;
+  if (n_seqs == 0 || total == 0) return KIME_OK;
+  if (!out || !workspace || !aligned16(out) || !aligned16(workspace)) return KIME_EINVAL;
+  if (workspace_bytes < varlen_ws_bytes(n_seqs, total)) return KIME_ERANGE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (append) {
+    rc = cuda_status(kime::launch_kv_append_varlen(qkv, cu, pos, n_seqs, total, heads, kv_heads, cap, rope_cos,
+                                                   rope_sin, rope_len, const_cast<void*>(k_cache),
+                                                   const_cast<void*>(v_cache), dev_status, st));
+    if (rc) return rc;
+  }
+  return chunk_attend(qkv, cu, pos, n_seqs, total, max_seqlen, heads, kv_heads, cap, scale, rope_cos, rope_sin,
+                      rope_len, k_cache, v_cache, out, workspace, dev_status, st);
+}
 
 int decode_common(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim, int cap,
                   float scale, const float* rope_cos, const float* rope_sin, int rope_len, const void* k_cache,
@@ -169,6 +230,37 @@ int kime_decode_step(const void* qkv_new, const int32_t* pos, int n_seqs, int he
                        k_cache, v_cache, out, workspace, workspace_bytes, dev_status, stream, true);
 }
 
+int kime_kv_append_varlen(const void* qkv, const int32_t* cu_seqlens, const int32_t* pos, int n_seqs,
+                          int total_tokens, int heads, int kv_heads, int head_dim, int cap, const float* rope_cos,
+                          const float* rope_sin, int rope_len, void* k_cache, void* v_cache, int32_t* dev_status,
+                          void* stream) {
+  int rc = chunk_args_ok(qkv, cu_seqlens, pos, n_seqs, total_tokens, heads, kv_heads, head_dim, cap, rope_cos,
+                         rope_sin, rope_len, k_cache, v_cache);
+  if (rc || n_seqs == 0 || total_tokens == 0) return rc;
+  return cuda_status(kime::launch_kv_append_varlen(qkv, cu_seqlens, pos, n_seqs, total_tokens, heads, kv_heads, cap,
+                                                   rope_cos, rope_sin, rope_len, k_cache, v_cache, dev_status,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+int kime_attn_chunk(const void* qkv, const int32_t* cu_seqlens, const int32_t* pos, int n_seqs, int total_tokens,
+                    int max_seqlen, int heads, int kv_heads, int head_dim, int cap, float scale,
+                    const float* rope_cos, const float* rope_sin, int rope_len, const void* k_cache,
+                    const void* v_cache, void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                    void* stream) {
+  return chunk_common(qkv, cu_seqlens, pos, n_seqs, total_tokens, max_seqlen, heads, kv_heads, head_dim, cap, scale,
+                      rope_cos, rope_sin, rope_len, k_cache, v_cache, out, workspace, workspace_bytes, dev_status,
+                      stream, false);
+}
+
+int kime_chunk_step(const void* qkv, const int32_t* cu_seqlens, const int32_t* pos, int n_seqs, int total_tokens,
+                    int max_seqlen, int heads, int kv_heads, int head_dim, int cap, float scale,
+                    const float* rope_cos, const float* rope_sin, int rope_len, void* k_cache, void* v_cache,
+                    void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return chunk_common(qkv, cu_seqlens, pos, n_seqs, total_tokens, max_seqlen, heads, kv_heads, head_dim, cap, scale,
+                      rope_cos, rope_sin, rope_len, k_cache, v_cache, out, workspace, workspace_bytes, dev_status,
+                      stream, true);
+}
+
 int kime_rope_tables(double theta, int len, float* cos_out, float* sin_out) {
   if (!(theta > 0.0) || len < 0 || (len > 0 && (!cos_out || !sin_out))) return KIME_EINVAL;
   float inv[kime::kHalf];
@@ -186,16 +278,20 @@ int kime_rope_tables(double theta, int len, float* cos_out, float* sin_out) {
   return KIME_OK;
 }
 
-int kime_attn_debug_tiles(const int32_t* cu_seqlens, int n_seqs, int total_tokens, int max_seqlen, int window,
-                          int causal, void* workspace, size_t workspace_bytes, int32_t* tiles_out, int max_pairs,
-                          int32_t* n_pairs_out, int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int debug_tiles_common(const int32_t* cu_seqlens, const int32_t* pos, int n_seqs, int total_tokens, int max_seqlen,
+                       int window, int causal, int cap, int rope_len, void* workspace, size_t workspace_bytes,
+                       int32_t* tiles_out, int max_pairs, int32_t* n_pairs_out, int32_t* dev_status, void* stream) {
   if (n_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || window < -1) return KIME_EINVAL;
   if (!cu_seqlens || !workspace || !tiles_out || !n_pairs_out) return KIME_EINVAL;
   const int need = kime::max_pairs_for(n_seqs, total_tokens);
   if (max_pairs < need || workspace_bytes < varlen_ws_bytes(n_seqs, total_tokens)) return KIME_ERANGE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int rc = cuda_status(kime::launch_schedule(cu_seqlens, n_seqs, total_tokens, max_seqlen, causal ? 1 : 0, window,
-                                             workspace, need, dev_status, st));
+  int rc = cuda_status(kime::launch_schedule(cu_seqlens, pos, n_seqs, total_tokens, max_seqlen, causal ? 1 : 0,
+                                             window, cap, rope_len, workspace, need, dev_status, st));
   if (rc) return rc;
   const char* ws = static_cast<const char*>(workspace);
   rc = cuda_status(cudaMemcpyAsync(n_pairs_out, ws + offsetof(kime::WsHeader, n_pairs), 4,
@@ -203,6 +299,26 @@ int kime_attn_debug_tiles(const int32_t* cu_seqlens, int n_seqs, int total_token
   if (rc) return rc;
   return cuda_status(cudaMemcpyAsync(tiles_out, ws + sizeof(kime::WsHeader), static_cast<size_t>(need) * 32,
                                      cudaMemcpyDeviceToDevice, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int kime_attn_debug_tiles(const int32_t* cu_seqlens, int n_seqs, int total_tokens, int max_seqlen, int window,
+                          int causal, void* workspace, size_t workspace_bytes, int32_t* tiles_out, int max_pairs,
+                          int32_t* n_pairs_out, int32_t* dev_status, void* stream) {
+  return debug_tiles_common(cu_seqlens, nullptr, n_seqs, total_tokens, max_seqlen, window, causal, 0, 0, workspace,
+                            workspace_bytes, tiles_out, max_pairs, n_pairs_out, dev_status, stream);
+}
+
+int kime_attn_debug_tiles_chunk(const int32_t* cu_seqlens, const int32_t* pos, int n_seqs, int total_tokens,
+                                int max_seqlen, int cap, int rope_len, void* workspace, size_t workspace_bytes,
+                                int32_t* tiles_out, int max_pairs, int32_t* n_pairs_out, int32_t* dev_status,
+                                void* stream) {
+  if (!pos || cap <= 0 || rope_len < 0) return KIME_EINVAL;
+  return debug_tiles_common(cu_seqlens, pos, n_seqs, total_tokens, max_seqlen, -1, 1, cap, rope_len, workspace,
+                            workspace_bytes, tiles_out, max_pairs, n_pairs_out, dev_status, stream);
 }
 
 int kime_attn_last_cuda_error(void) { return g_last_cuda_error; }

@@ -5,6 +5,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,23 +34,26 @@ __device__ __forceinline__ int ceil_pos(int a, int b) { return a <= 0 ? 0 : (a +
 // Number of key tiles kt >= 0 whose last key kt*128 + 127 is <= x.
 __device__ __forceinline__ int tiles_ending_by(int x) { return x < kBN - 1 ? 0 : (x - (kBN - 1)) / kBN + 1; }
 
-// Key-tile ranges of query tile qt (rows q0 = 128 qt .. q1-1, q1 = min(q0+128, L))
-// of a length-L sequence.  Tiles [kb, ke) hold at least one visible key:
-//   k0 < L; causal: k0 <= q1-1; window w: k0 <= q1-1+w and k0+127 >= q0-w.
+// Key-tile ranges of query tile qt of a block of Lq query rows whose row i
+// sits at position off + i, over keys [0, Lk): the tile's positions run from
+// q0 = off + 128 qt to q1-1, q1 = off + min(128 qt + 128, Lq).  A packed
+// sequence is off = 0, Lk = Lq = L; a chunk attending a KV cache is
+// off = pos[s], Lk = pos[s] + L.  Tiles [kb, ke) hold at least one visible key:
+//   k0 < Lk; causal: k0 <= q1-1; window w: k0 <= q1-1+w and k0+127 >= q0-w.
 // Tiles [fb, fe) inside them are full -- every row sees every key:
-//   k0+128 <= L; causal: k0+127 <= q0; window: k0 >= q1-1-w and k0+127 <= q0+w.
-__device__ __forceinline__ void tile_ranges(int L, int qt, int causal, int window, int& kb, int& ke, int& fb,
-                                            int& fe) {
-  const int q0 = qt * kBM, q1 = min(q0 + kBM, L);
+//   k0+128 <= Lk; causal: k0+127 <= q0; window: k0 >= q1-1-w and k0+127 <= q0+w.
+__device__ __forceinline__ void tile_ranges(int Lq, int Lk, int off, int qt, int causal, int window, int& kb,
+                                            int& ke, int& fb, int& fe) {
+  const int q0 = off + qt * kBM, q1 = off + min(qt * kBM + kBM, Lq);
   kb = 0;
-  ke = (L + kBN - 1) / kBN;
+  ke = (Lk + kBN - 1) / kBN;
   if (causal) ke = min(ke, (q1 - 1) / kBN + 1);
   if (window >= 0) {
     ke = min(ke, (q1 - 1 + window) / kBN + 1);
     kb = max(kb, ceil_pos(q0 - window - (kBN - 1), kBN));
   }
   fb = 0;
-  fe = L / kBN;
+  fe = Lk / kBN;
   if (causal) fe = min(fe, tiles_ending_by(q0));
   if (window >= 0) {
     fe = min(fe, tiles_ending_by(q0 + window));
@@ -58,6 +62,10 @@ __device__ __forceinline__ void tile_ranges(int L, int qt, int causal, int windo
   fb = max(fb, kb);
   fe = min(fe, ke);
   if (fe <= fb) fb = fe = kb;
+}
+__device__ __forceinline__ void tile_ranges(int L, int qt, int causal, int window, int& kb, int& ke, int& fb,
+                                            int& fe) {
+  tile_ranges(L, L, 0, qt, causal, window, kb, ke, fb, fe);
 }
 
 // ---- small numeric helpers ---------------------------------------------------
@@ -75,6 +83,18 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+// 2^x of a packed f16 pair with one MUFU operation.
+__device__ __forceinline__ uint32_t fast_exp2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ float f16lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+__device__ __forceinline__ float f16hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
 }
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -17,7 +17,8 @@ constexpr int kMaxGroup = 8;    // largest heads/kv_heads the decode path takes
 
 // One (sequence, query tile) of the schedule with its key-tile ranges:
 // tiles [kt_begin, kt_end) are visited; [full_begin, full_end) among them need
-// no per-column test.  row0 = cu_seqlens[s], L = sequence length.
+// no per-column test.  row0 = cu_seqlens[s], L = sequence length.  (For a chunk
+// attending the cache the ranges count cache key tiles from position 0.)
 struct Pair {
   int32_t s, qt, kt_begin, kt_end, full_begin, full_end, row0, L;
 };
@@ -26,9 +27,11 @@ static_assert(sizeof(Pair) == 32, "Pair is 32 bytes");
 // Two consecutive query tiles (2*qp, 2*qp+1) of one sequence: the unit of the
 // tensor-core kernel, whose two softmax warpgroups share each K/V tile.  nt is
 // 1 when the sequence's last tile has no partner; [kb, ke) is the union of the
-// two tiles' visited key-tile ranges.
+// two tiles' visited key-tile ranges.  off = position of the sequence's first
+// query row (0 for a packed sequence, pos[s] for a chunk attending the cache,
+// whose keys are then cache rows [0, off + L)).
 struct Duo {
-  int32_t s, qt0, nt, kb, ke, row0, L, cost;
+  int32_t s, qt0, nt, kb, ke, row0, L, off;
 };
 static_assert(sizeof(Duo) == 32, "Duo is 32 bytes");
 
@@ -61,14 +64,24 @@ inline Duo* ws_duos(void* ws, int max_pairs) {
 size_t decode_workspace_bytes(int n_seqs, int heads, int kv_heads, int cap);
 
 // Launchers (each returns a cudaError_t of the launch).
-cudaError_t launch_schedule(const int32_t* cu, int n_seqs, int total, int max_seqlen, int causal, int window,
-                            void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
+// pos == nullptr: packed sequences.  Otherwise chunks at offsets pos[s] against
+// a cache of cap rows (positions must stay below cap and rope_len).
+cudaError_t launch_schedule(const int32_t* cu, const int32_t* pos, int n_seqs, int total, int max_seqlen,
+                            int causal, int window, int cap, int rope_len, void* ws, int max_pairs,
+                            int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_varlen_f32(const float* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
                               int window, int causal, float scale, const float* cos_t, const float* sin_t,
                               float* out, void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
-cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, int n_seqs, int total, int heads, int kv_heads,
-                              int window, int causal, float scale, const float* cos_t, const float* sin_t, void* out,
-                              void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
+// k_map / v_map == nullptr: keys and values come from the qkv rows (packed
+// sequences).  Otherwise from caches [n_seqs * kv_heads * cap, 64] (chunks).
+cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_map, const CUtensorMap* v_map,
+                              int n_seqs, int total, int heads, int kv_heads, int cap, int window, int causal,
+                              float scale, const float* cos_t, const float* sin_t, void* out, void* ws,
+                              int max_pairs, int32_t* dev_status, cudaStream_t st);
+cudaError_t launch_kv_append_varlen(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total,
+                                    int heads, int kv_heads, int cap, const float* cos_t, const float* sin_t,
+                                    int rope_len, void* k_cache, void* v_cache, int32_t* dev_status,
+                                    cudaStream_t st);
 cudaError_t launch_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int cap,
                              const float* cos_t, const float* sin_t, int rope_len, void* k_cache, void* v_cache,
                              int32_t* dev_status, cudaStream_t st);

@@ -77,12 +77,17 @@ constexpr uint32_t kOffBar = kOffV + kStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPolyOf8 = 0;  // exponentials per 8 keys taken on the FMA pipe
+#ifndef KIME_EXP_F16
+#define KIME_EXP_F16 0
+#endif
+constexpr bool kExpF16 = KIME_EXP_F16;  // two exponentials per MUFU op on f16 arguments
+constexpr float kLazy = kExpF16 ? 1.f : 8.f;  // reference max moves when exceeded by more
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct UnitInfo {
-  int32_t u, s, qt0, nt, kb, ke, row0, L;
+  int32_t u, s, qt0, nt, kb, ke, row0, L, off;
 };
 
 struct Shared {
@@ -132,7 +137,9 @@ __device__ __forceinline__ void load_table_row(TableRow& t, const float* __restr
 // at chunk k ^ (r & 7)), bf16 on entry, converted in place to the f16 operand
 // the MMAs read.  rope_row: rotate-half RoPE with the row's table entries in
 // float32 (one rounding per operation), times `mul`, rounded once to f16.
-// convert_row: the bf16 values widened and rounded to f16.
+// convert_row: the bf16 values widened and rounded to f16.  zero_row: zeros
+// (cache rows past a chunk's keys, whose contents are undefined: a NaN there
+// would reach O through a zero probability).
 __device__ __forceinline__ void rope_row(uint8_t* tile, int r, const TableRow& tb, float mul) {
   uint8_t* row = tile + r * 128;
   const int sw = r & 7;
@@ -170,8 +177,14 @@ __device__ __forceinline__ void convert_row(uint8_t* tile, int r) {
   }
 }
 
+__device__ __forceinline__ void zero_row(uint8_t* tile, int r) {
+  uint4* row = reinterpret_cast<uint4*>(tile + r * 128);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) row[k] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 struct Params {
-  int heads, kv_heads, window, causal;
+  int heads, kv_heads, cap, window, causal;
   float qmul;  // scale * log2(e), folded into q before its f16 rounding
   const float* cos_t;
   const float* sin_t;
@@ -181,16 +194,27 @@ struct Params {
   int32_t* dev_status;
 };
 
+// kCache = false: a packed batch; K and V are heads of the qkv rows, K rotated
+// here.  kCache = true: chunks attending a KV cache that already holds them
+// (rotated keys); K and V tiles come from the cache maps, rows past the
+// sequence's keys are zeroed, q rows sit at positions off + i.
+template <bool kCache>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap qkv_map, const Params p) {
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap qkv_map, const __grid_constant__ CUtensorMap k_map,
+                      const __grid_constant__ CUtensorMap v_map, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Shared* sh = reinterpret_cast<Shared*>(smem + kOffBar);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
   const int G = p.heads / p.kv_heads;
+  const int kCausal = kCache ? 1 : p.causal, kWindow = kCache ? -1 : p.window;  // chunks: causal, no window
 
   if (tid == 0) {
     tma_prefetch_map(&qkv_map);
+    if (kCache) {
+      tma_prefetch_map(&k_map);
+      tma_prefetch_map(&v_map);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh->unit_full[i], 1);
       mbar_init(&sh->unit_empty[i], 5);  // softmax A, softmax B, two MMA issuers, RoPE
@@ -248,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (inf.u >= 0) {
           const Duo d = p.duos[u / p.heads];
           inf.s = d.s; inf.qt0 = d.qt0; inf.nt = d.nt; inf.kb = d.kb; inf.ke = d.ke; inf.row0 = d.row0; inf.L = d.L;
+          inf.off = kCache ? d.off : 0;
         }
         sh->info[slot] = inf;
         mbar_arrive(&sh->unit_full[slot]);
@@ -262,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (inf.nt == 2)
           tma_load_2d(q + kTile, &qkv_map, &sh->q_full[slot], h * kHead, inf.row0 + (inf.qt0 + 1) * kBM);
         const int kx = (p.heads + g) * kHead, vx = (p.heads + p.kv_heads + g) * kHead;
+        const int kvrow = (inf.s * p.kv_heads + g) * p.cap;  // cache row of key 0
         bool ok = true;
         for (int t = inf.kb; t < inf.ke; ++t, ++c) {
           const int st = c % kStages;
@@ -269,8 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait(&sh->kv_empty[st], ((c / kStages) & 1) ^ 1)) { ok = false; break; }
           PHASE(2);
           mbar_arrive_expect_tx(&sh->kv_full[st], 2 * kTile);
-          tma_load_2d(smem + kOffK + st * kTile, &qkv_map, &sh->kv_full[st], kx, inf.row0 + t * kBN);
-          tma_load_2d(smem + kOffV + st * kTile, &qkv_map, &sh->kv_full[st], vx, inf.row0 + t * kBN);
+          if (kCache) {
+            tma_load_2d(smem + kOffK + st * kTile, &k_map, &sh->kv_full[st], 0, kvrow + t * kBN);
+            tma_load_2d(smem + kOffV + st * kTile, &v_map, &sh->kv_full[st], 0, kvrow + t * kBN);
+          } else {
+            tma_load_2d(smem + kOffK + st * kTile, &qkv_map, &sh->kv_full[st], kx, inf.row0 + t * kBN);
+            tma_load_2d(smem + kOffV + st * kTile, &qkv_map, &sh->kv_full[st], vx, inf.row0 + t * kBN);
+          }
         }
         if (!ok) break;
       }
@@ -291,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const UnitInfo inf = sh->info[slot];
         if (inf.u < 0) break;
         int kb = 0, ke = 0, fb, fe;  // this tile's range; empty when the unit has no tile B
-        if (w < inf.nt) tile_ranges(inf.L, inf.qt0 + w, p.causal, p.window, kb, ke, fb, fe);
+        const int off = kCache ? inf.off : 0;  // position of the unit's row 0
+        if (w < inf.nt) tile_ranges(inf.L, off + inf.L, off, inf.qt0 + w, kCausal, kWindow, kb, ke, fb, fe);
         const uint32_t aq = smem_u32(smem + kOffQ + slot * 2 * kTile) + w * kTile;
         PHASE(4);
         bool ok = wait(&sh->qrot[slot], (n >> 1) & 1);
@@ -366,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       TableRow tb;
       for (int w = 0; w < inf.nt; ++w) {
         const int i = (inf.qt0 + w) * kBM + r;
-        if (i < inf.L)
-          load_table_row(tb, p.cos_t + static_cast<size_t>(i) * kHalf, p.sin_t + static_cast<size_t>(i) * kHalf);
+        const size_t ti = static_cast<size_t>((kCache ? inf.off : 0) + i) * kHalf;  // table row of position off + i
+        if (i < inf.L) load_table_row(tb, p.cos_t + ti, p.sin_t + ti);
         if (w == 0) ok = wait(&sh->q_full[slot], (n >> 1) & 1);
         if (ok) {
           if (i < inf.L)
@@ -383,19 +415,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sh->qrot[slot]);
         mbar_arrive(&sh->unit_empty[slot]);  // every thread has its copy of the unit
       }
+      const int Lk = (kCache ? inf.off : 0) + inf.L;  // keys of the unit's sequence
       for (int t = inf.kb; t < inf.ke; ++t, ++c) {
         const int st = c % kStages, j = t * kBN + r;
-        if (j < inf.L)
+        if (!kCache && j < inf.L)
           load_table_row(tb, p.cos_t + static_cast<size_t>(j) * kHalf, p.sin_t + static_cast<size_t>(j) * kHalf);
         PHASE(2);
         ok = wait(&sh->kv_full[st], (c / kStages) & 1);
         PHASE(3);
         if (ok) {
-          if (j < inf.L)
-            rope_row(smem + kOffK + st * kTile, r, tb, 1.f);
-          else
-            convert_row(smem + kOffK + st * kTile, r);
-          convert_row(smem + kOffV + st * kTile, r);
+          if (kCache) {  // cached keys are rotated already
+            if (j < Lk) {
+              convert_row(smem + kOffK + st * kTile, r);
+              convert_row(smem + kOffV + st * kTile, r);
+            } else {
+              zero_row(smem + kOffK + st * kTile, r);
+              zero_row(smem + kOffV + st * kTile, r);
+            }
+          } else {
+            if (j < inf.L)
+              rope_row(smem + kOffK + st * kTile, r, tb, 1.f);
+            else
+              convert_row(smem + kOffK + st * kTile, r);
+            convert_row(smem + kOffV + st * kTile, r);
+          }
           fence_proxy_async_smem();
         }
         PHASE(4);
@@ -429,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qt = inf.qt0 + w, q0 = qt * kBM, i = q0 + r;
       const bool row_ok = i < inf.L;
       int kb, ke, fb, fe;
-      tile_ranges(inf.L, qt, p.causal, p.window, kb, ke, fb, fe);
+      const int off = kCache ? inf.off : 0;  // position of the unit's row 0
+      tile_ranges(inf.L, off + inf.L, off, qt, kCausal, kWindow, kb, ke, fb, fe);
 
       // Online softmax with a lazily moved reference max: P = 2^(S - m_ref) and
       // O (in TMEM, accumulated by the PV MMAs) stay relative to m_ref, which
@@ -449,12 +493,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < kBN; ++j) x[j] = __uint_as_float(v[j]);
         if (!(t >= fb && t < fe)) {
-          // visible keys of this row in this tile form one interval [lo, hi]
-          int lo = 0, hi = min(kBN - 1, inf.L - 1 - k0);
-          if (p.causal) hi = min(hi, i - k0);
-          if (p.window >= 0) {
-            lo = max(lo, i - p.window - k0);
-            hi = min(hi, i + p.window - k0);
+          // visible keys of this row in this tile form one interval [lo, hi];
+          // the row sits at position off + i, the sequence has off + L keys
+          const int qk = off + i - k0;
+          int lo = 0, hi = min(kBN - 1, off + inf.L - 1 - k0);
+          if (kCausal) hi = min(hi, qk);
+          if (kWindow >= 0) {
+            lo = max(lo, qk - kWindow);
+            hi = min(hi, qk + kWindow);
           }
           if (!row_ok) hi = -1;
 #pragma unroll
@@ -470,9 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 16; j < kBN; j += 2) m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], x[j], x[j + 1]);
         const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         // move the reference max on the first visible keys, or when it is
-        // exceeded by more than 8 (a factor 256)
+        // exceeded by more than kLazy (log2 units)
         float alpha = 1.f;
-        if (mx > m_ref + 8.f) {
+        if (mx > m_ref + kLazy) {
           if (m_ref != -INFINITY) alpha = fast_exp2(m_ref - mx);
           m_ref = mx;
         }
@@ -485,30 +531,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         PHASE(3);
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        // kPolyOf8 of every 8 exponentials run on the FMA pipe (exp2_poly), the
-        // rest on the MUFU, so the two pipes share the load.  A masked key
-        // (-inf) gives 0 on the MUFU and 2^-125 from exp2_poly: both round to
-        // an f16 zero in P, and 2^-125 cannot change l (l >= 1: the row max
-        // contributes 2^(max - m_ref) >= 1).
-        // P = 2^(x - m_use), row sums in four chains; kPolyOf8 of every 8
-        // exponentials on the FMA pipe (exp2_poly), the rest
-        // on the MUFU.  A masked key (-inf) gives 0 on the MUFU and 2^-125 from
-        // exp2_poly: both round to an f16 zero in P, and 2^-125 cannot change l
-        // (l >= 1: the row max contributes 2^(max - m_ref) >= 1).
         float rs2f[4] = {0.f, 0.f, 0.f, 0.f};
+        if (kExpF16) {
+          // P = 2^(x - m_use) two keys per MUFU operation: the argument is
+          // rounded to f16 (x - m_use <= kLazy keeps its error below 2^-11
+          // where P is large) and P comes out as the f16 pair the MMA reads;
+          // a masked key saturates to -65504 and gives 0.
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P at a time
-          uint32_t pw[16];
+          for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P at a time
+            uint32_t pw[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int j = q4 * 32 + 2 * e;
-            const float a0 = x[j] - m_use, a1 = x[j + 1] - m_use;
-            const float p0 = (j & 7) < kPolyOf8 ? exp2_poly(a0) : fast_exp2(a0);
-            const float p1 = ((j + 1) & 7) < kPolyOf8 ? exp2_poly(a1) : fast_exp2(a1);
-            rs2f[e & 3] += p0 + p1;
-            pw[e] = pack_f16x2(p0, p1);
+            for (int e = 0; e < 16; ++e) {
+              const int j = q4 * 32 + 2 * e;
+              const uint32_t ph = fast_exp2_f16x2(pack_f16x2(x[j] - m_use, x[j + 1] - m_use));
+              rs2f[e & 3] += f16lo(ph) + f16hi(ph);
+              pw[e] = ph;
+            }
+            tmem_st16(tP + q4 * 16, pw);  // this row's P: keys 2c, 2c+1 in column c
           }
-          tmem_st16(tP + q4 * 16, pw);  // this row's P: keys 2c, 2c+1 in column c
+        } else {
+          // P = 2^(x - m_use), row sums in four chains; kPolyOf8 of every 8
+          // exponentials on the FMA pipe (exp2_poly), the rest on the MUFU.  A
+          // masked key (-inf) gives 0 on the MUFU and 2^-125 from exp2_poly:
+          // both round to an f16 zero in P, and 2^-125 cannot change l (l >= 1:
+          // the row max contributes 2^(max - m_ref) >= 1).
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P at a time
+            uint32_t pw[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int j = q4 * 32 + 2 * e;
+              const float a0 = x[j] - m_use, a1 = x[j + 1] - m_use;
+              const float p0 = (j & 7) < kPolyOf8 ? exp2_poly(a0) : fast_exp2(a0);
+              const float p1 = ((j + 1) & 7) < kPolyOf8 ? exp2_poly(a1) : fast_exp2(a1);
+              rs2f[e & 3] += p0 + p1;
+              pw[e] = pack_f16x2(p0, p1);
+            }
+            tmem_st16(tP + q4 * 16, pw);  // this row's P: keys 2c, 2c+1 in column c
+          }
         }
         const float rowsum = (rs2f[0] + rs2f[1]) + (rs2f[2] + rs2f[3]);
         l = l * alpha + rowsum;
@@ -587,22 +647,26 @@ extern "C" int kime_debug_phase_clear() {
 }
 #endif
 
-cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, int n_seqs, int total, int heads, int kv_heads,
-                              int window, int causal, float scale, const float* cos_t, const float* sin_t, void* out,
-                              void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st) {
+cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_map, const CUtensorMap* v_map,
+                              int n_seqs, int total, int heads, int kv_heads, int cap, int window, int causal,
+                              float scale, const float* cos_t, const float* sin_t, void* out, void* ws,
+                              int max_pairs, int32_t* dev_status, cudaStream_t st) {
   (void)n_seqs; (void)total;
-  static int configured[64] = {0};
+  const bool cache = k_map != nullptr;
+  static int configured[2][64] = {};
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (dev < 64 && !configured[cache][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(cache ? prefill_tc_kernel<true> : prefill_tc_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[dev] = 1;
+    configured[cache][dev] = 1;
   }
   Params prm;
   prm.heads = heads;
   prm.kv_heads = kv_heads;
+  prm.cap = cap;
   prm.window = window;
   prm.causal = causal;
   prm.qmul = scale * 1.4426950408889634f;
@@ -624,7 +688,8 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, int n_seqs, int total,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, *qkv_map, prm);
+  if (cache) return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true>, *qkv_map, *k_map, *v_map, prm);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false>, *qkv_map, *qkv_map, *qkv_map, prm);
 }
 
 }  // namespace kime

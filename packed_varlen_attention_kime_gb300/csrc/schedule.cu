@@ -10,6 +10,12 @@
 // unit of the tensor-core kernel).  Both lists are ordered longest-first
 // (counting sort on the number of key tiles) so the persistent kernels finish
 // the expensive work early.
+//
+// With per-sequence offsets pos (a chunk of new tokens attending the KV cache
+// that already holds them, ffai-argus 0.7.3 src/text.rs, TextTower::block with
+// index_pos > 0) row i of sequence s sits at position pos[s] + i and its keys
+// are cache rows [0, pos[s] + L); a sequence whose positions would leave
+// [0, min(cap, rope_len)) is reported and skipped.
 #include "kime_common.cuh"
 
 namespace kime {
@@ -23,30 +29,47 @@ __device__ __forceinline__ int bucket_of(int kb, int ke) { return kBuckets - 1 -
 
 // The tensor-core kernel's unit: tiles 2qp and 2qp+1 of one sequence; cost =
 // S tiles the two compute.
-__device__ __forceinline__ Duo make_duo(int s, int qp, int a, int L, int causal, int window) {
+__device__ __forceinline__ Duo make_duo(int s, int qp, int a, int L, int off, int causal, int window, int& cost) {
   Duo d;
   d.s = s;
   d.qt0 = 2 * qp;
   d.nt = (2 * qp + 1) * kBM < L ? 2 : 1;
   d.row0 = a;
   d.L = L;
+  d.off = off;
   int kb, ke, fb, fe;
-  tile_ranges(L, d.qt0, causal, window, kb, ke, fb, fe);
+  tile_ranges(L, off + L, off, d.qt0, causal, window, kb, ke, fb, fe);
   d.kb = kb;
   d.ke = ke;
-  d.cost = ke - kb;
+  cost = ke - kb;
   if (d.nt == 2) {
-    tile_ranges(L, d.qt0 + 1, causal, window, kb, ke, fb, fe);
+    tile_ranges(L, off + L, off, d.qt0 + 1, causal, window, kb, ke, fb, fe);
     d.kb = min(d.kb, kb);
     d.ke = max(d.ke, ke);
-    d.cost += ke - kb;
+    cost += ke - kb;
   }
   return d;
 }
 
+// Status of sequence s (0 when it is scheduled) and its offset.
+__device__ __forceinline__ int check_seq(const int32_t* cu, const int32_t* pos, int s, int total, int max_seqlen,
+                                         int cap, int rope_len, int& off) {
+  const int a = cu[s], b = cu[s + 1];
+  off = 0;
+  if (a < 0 || b < a || b > total) return ST_BAD_CU;
+  if (b - a > max_seqlen) return ST_SEQ_TOO_LONG;
+  if (pos) {
+    off = pos[s];
+    const long long end = static_cast<long long>(off) + (b - a);
+    if (off < 0 || end > cap || end > rope_len) return ST_BAD_POS;
+  }
+  return 0;
+}
+
 __global__ void __launch_bounds__(kSchedThreads)
-    schedule_kernel(const int32_t* __restrict__ cu, int n_seqs, int total, int max_seqlen, int causal, int window,
-                    WsHeader* hdr, Pair* __restrict__ pairs, int max_pairs, Duo* __restrict__ duos, int max_duos,
+    schedule_kernel(const int32_t* __restrict__ cu, const int32_t* __restrict__ pos, int n_seqs, int total,
+                    int max_seqlen, int causal, int window, int cap, int rope_len, WsHeader* hdr,
+                    Pair* __restrict__ pairs, int max_pairs, Duo* __restrict__ duos, int max_duos,
                     int32_t* dev_status) {
   __shared__ int hist[2][kBuckets];
   __shared__ int cursor[2][kBuckets];
@@ -62,24 +85,22 @@ __global__ void __launch_bounds__(kSchedThreads)
   __syncthreads();
   // Pass 1: validate each sequence and histogram its tiles and duos by cost.
   for (int s = threadIdx.x; s < n_seqs; s += blockDim.x) {
-    const int a = cu[s], b = cu[s + 1];
-    if (a < 0 || b < a || b > total) {
-      atomicOr(&s_bad, ST_BAD_CU);
+    int off;
+    const int bad = check_seq(cu, pos, s, total, max_seqlen, cap, rope_len, off);
+    if (bad) {
+      atomicOr(&s_bad, bad);
       continue;
     }
-    if (b - a > max_seqlen) {
-      atomicOr(&s_bad, ST_SEQ_TOO_LONG);
-      continue;
-    }
-    const int L = b - a;
+    const int a = cu[s], L = cu[s + 1] - a;
     for (int qt = 0; qt * kBM < L; ++qt) {
       int kb, ke, fb, fe;
-      tile_ranges(L, qt, causal, window, kb, ke, fb, fe);
+      tile_ranges(L, off + L, off, qt, causal, window, kb, ke, fb, fe);
       atomicAdd(&hist[0][bucket_of(kb, ke)], 1);
     }
     for (int qp = 0; 2 * qp * kBM < L; ++qp) {
-      const Duo d = make_duo(s, qp, a, L, causal, window);
-      atomicAdd(&hist[1][bucket_of(0, d.cost)], 1);
+      int cost;
+      make_duo(s, qp, a, L, off, causal, window, cost);
+      atomicAdd(&hist[1][bucket_of(0, cost)], 1);
     }
   }
   __syncthreads();
@@ -102,18 +123,19 @@ __global__ void __launch_bounds__(kSchedThreads)
   __syncthreads();
   // Pass 2: scatter tiles and duos into cost order (longest first).
   for (int s = threadIdx.x; s < n_seqs; s += blockDim.x) {
-    const int a = cu[s], b = cu[s + 1];
-    if (a < 0 || b < a || b > total || b - a > max_seqlen) continue;
-    const int L = b - a;
+    int off;
+    if (check_seq(cu, pos, s, total, max_seqlen, cap, rope_len, off)) continue;
+    const int a = cu[s], L = cu[s + 1] - a;
     for (int qt = 0; qt * kBM < L; ++qt) {
       int kb, ke, fb, fe;
-      tile_ranges(L, qt, causal, window, kb, ke, fb, fe);
+      tile_ranges(L, off + L, off, qt, causal, window, kb, ke, fb, fe);
       const int at = atomicAdd(&cursor[0][bucket_of(kb, ke)], 1);
       if (at < max_pairs) pairs[at] = Pair{s, qt, kb, ke, fb, fe, a, L};
     }
     for (int qp = 0; 2 * qp * kBM < L; ++qp) {
-      const Duo d = make_duo(s, qp, a, L, causal, window);
-      const int at = atomicAdd(&cursor[1][bucket_of(0, d.cost)], 1);
+      int cost;
+      const Duo d = make_duo(s, qp, a, L, off, causal, window, cost);
+      const int at = atomicAdd(&cursor[1][bucket_of(0, cost)], 1);
       if (at < max_duos) duos[at] = d;
     }
   }
@@ -121,13 +143,14 @@ __global__ void __launch_bounds__(kSchedThreads)
 
 }  // namespace
 
-cudaError_t launch_schedule(const int32_t* cu, int n_seqs, int total, int max_seqlen, int causal, int window,
-                            void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st) {
+cudaError_t launch_schedule(const int32_t* cu, const int32_t* pos, int n_seqs, int total, int max_seqlen,
+                            int causal, int window, int cap, int rope_len, void* ws, int max_pairs,
+                            int32_t* dev_status, cudaStream_t st) {
   WsHeader* hdr = static_cast<WsHeader*>(ws);
   Pair* pairs = ws_pairs(ws);
   Duo* duos = ws_duos(ws, max_pairs);
-  schedule_kernel<<<1, kSchedThreads, 0, st>>>(cu, n_seqs, total, max_seqlen, causal, window, hdr, pairs,
-                                               max_pairs, duos, max_duos_for(n_seqs, total), dev_status);
+  schedule_kernel<<<1, kSchedThreads, 0, st>>>(cu, pos, n_seqs, total, max_seqlen, causal, window, cap, rope_len,
+                                               hdr, pairs, max_pairs, duos, max_duos_for(n_seqs, total), dev_status);
   return cudaGetLastError();
 }
 

@@ -14,6 +14,9 @@ Workloads (head_dim 64 throughout):
                     theta 1e5, causal, scale 1
   smollm2_decode    128 seqs, 9 q / 3 kv heads, BF16 caches [128,3,8192,64]
                     N(0,1), used lengths pos~U[1,8191], theta 1e5, scale 1/8
+  smollm2_chunk     chunked prefill: 32 seqs, 9 q / 3 kv heads, caches
+                    [32,3,8192,64] N(0,1), chunks L~U[128,1024] of BF16 N(0,1)
+                    rows at used lengths pos~U[0,8192-L], theta 1e5, scale 1/8
 """
 from __future__ import annotations
 
@@ -62,6 +65,30 @@ class DecodeCase:
     cap: int
     theta: float
     scale: float
+
+
+@dataclass
+class ChunkCase:
+    name: str
+    lengths: list
+    cu_seqlens: torch.Tensor  # int32 [n+1]
+    pos: torch.Tensor         # int32 [n]: cache rows already used
+    qkv: torch.Tensor         # bf16 [T, W]: the chunks' rows
+    k_cache: torch.Tensor     # bf16 [n, Hkv, cap, 64]
+    v_cache: torch.Tensor
+    heads: int
+    kv_heads: int
+    cap: int
+    theta: float
+    scale: float
+
+    @property
+    def total(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def max_seqlen(self) -> int:
+        return max(self.lengths) if self.lengths else 0
 
 
 def cu_from_lengths(lengths) -> torch.Tensor:
@@ -134,3 +161,27 @@ def decode_case(n_seqs: int = 128, cap: int = 8192, heads: int = 9, kv_heads: in
 def bf16_bits(t: torch.Tensor):
     """numpy uint16 view of a bfloat16 tensor (moved to the CPU)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def chunk_case(n_seqs: int = 32, cap: int = 8192, lo: int = 128, hi: int = 1024, heads: int = 9,
+               kv_heads: int = 3, seed: int = 6, device: str = "cpu", lengths=None, pos=None) -> ChunkCase:
+    """The SmolLM2-shaped chunked-prefill step (defaults), a smaller one, or
+    given lengths / positions.  Cache rows are N(0,1) everywhere (rows at and
+    past pos are what the append overwrites or never reads)."""
+    g = torch.Generator().manual_seed(seed)
+    if lengths is None:
+        lengths = _lengths(g, n_seqs, lo, hi)
+    lengths = [int(x) for x in lengths]
+    n = len(lengths)
+    if pos is None:
+        pos = [int(torch.randint(0, cap - L + 1, (1,), generator=g)) for L in lengths]
+    pos = torch.tensor([int(x) for x in pos], dtype=torch.int32)
+    gv = torch.Generator(device=device).manual_seed(seed * 1000 + 7)
+    qkv = random_qkv(lengths, heads, kv_heads, torch.bfloat16, 1.0, seed * 1000 + 11, device=device)
+    k = torch.empty((n, kv_heads, cap, 64), dtype=torch.bfloat16, device=device)
+    v = torch.empty_like(k)
+    for s in range(n):
+        k[s] = torch.randn((kv_heads, cap, 64), generator=gv, dtype=torch.float32, device=device)
+        v[s] = torch.randn((kv_heads, cap, 64), generator=gv, dtype=torch.float32, device=device)
+    return ChunkCase("smollm2_chunk", lengths, cu_from_lengths(lengths), pos, qkv, k, v, heads, kv_heads, cap,
+                     1e5, 0.125)
