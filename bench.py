@@ -132,6 +132,25 @@ def l2_flush_buffer(dev):
 
 # ---- workloads on the GPU ------------------------------------------------------------
 
+_STATUS = {}
+
+
+def dev_status(dev):
+    """The device status word every library call of this process reports into."""
+    key = str(dev)
+    if key not in _STATUS:
+        _STATUS[key] = torch.zeros(1, dtype=torch.int32, device=dev)
+    return _STATUS[key]
+
+
+def check_status(dev):
+    """Fails the run if any kernel flagged bad input or a timed-out wait."""
+    torch.cuda.synchronize(dev)
+    v = int(dev_status(dev).item())
+    if v != 0:
+        raise RuntimeError(f"device status {v:#x} after the timed work (a kernel flagged an error)")
+
+
 class VarlenRun:
     """Device-resident inputs, tables, outputs and workspace for one varlen workload."""
 
@@ -160,7 +179,8 @@ class VarlenRun:
         cs, sn = self.tables[lay.theta]
         self.kime.kime_attn_varlen(self.case.qkv if qkv is None else qkv, self.cu, c.max_seqlen, c.heads,
                                    c.kv_heads, lay.window, lay.causal, lay.scale, cs, sn,
-                                   out=self.outs[k] if out is None else out, workspace=self.ws)
+                                   out=self.outs[k] if out is None else out, workspace=self.ws,
+                                   dev_status=dev_status(self.dev))
 
 
 class DecodeRun:
@@ -186,7 +206,7 @@ class DecodeRun:
     def step(self):
         c = self.case
         self.kime.kime_decode_step(c.qkv_new, self.pos, c.heads, c.kv_heads, c.k_cache, c.v_cache, c.scale,
-                                   self.cs, self.sn, out=self.out, workspace=self.ws)
+                                   self.cs, self.sn, out=self.out, workspace=self.ws, dev_status=dev_status(self.dev))
 
 
 class ChunkRun:
@@ -198,6 +218,7 @@ class ChunkRun:
         from packed_varlen_attention_kime_gb300.inputs import chunk_case
         self.kime = kime
         c = self.case = chunk_case(device=str(dev))
+        self.dev = dev
         self.cu, self.pos = c.cu_seqlens.to(dev), c.pos.to(dev)
         cs, sn = kime.kime_rope_tables(c.theta, c.cap)
         self.cs, self.sn = cs.to(dev), sn.to(dev)
@@ -217,7 +238,8 @@ class ChunkRun:
     def step(self):
         c = self.case
         self.kime.kime_chunk_step(c.qkv, self.cu, self.pos, c.max_seqlen, c.heads, c.kv_heads, c.k_cache,
-                                  c.v_cache, c.scale, self.cs, self.sn, out=self.out, workspace=self.ws)
+                                  c.v_cache, c.scale, self.cs, self.sn, out=self.out, workspace=self.ws,
+                                  dev_status=dev_status(self.dev))
 
 
 def time_fn(fn, n, warmup, flush, stream, events=1):
@@ -415,6 +437,8 @@ def main():
         del h_qkv, h_out, d_qkv
         extra = extra_measurements(dev, flush, stream, pk)
 
+    check_status(dev)  # any flagged input error or timed-out wait voids the numbers
+
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         rate, cores, sample = oracle_sample_rate(VarlenRunCPU(c), args.cpu_budget)
@@ -451,6 +475,7 @@ def only_arm(args, local):
     if name in ("smollm2_decode", "smollm2_chunk"):
         d = DecodeRun(dev) if name == "smollm2_decode" else ChunkRun(dev)
         per, _ = time_fn(lambda ev: d.step(), args.steps, args.warmup, flush, stream)
+        check_status(dev)
         print(json.dumps({"only": name, "ms": [round(x, 4) for x in per]}))
         return
     r = VarlenRun(name, dev)
@@ -460,6 +485,7 @@ def only_arm(args, local):
         for k in ks:
             r.layer(k)
     per, _ = time_fn(f, args.steps, args.warmup, flush, stream)
+    check_status(dev)
     print(json.dumps({"only": args.only, "layers": [r.case.layers[k].name for k in ks],
                       "ms": [round(x, 4) for x in per]}))
 

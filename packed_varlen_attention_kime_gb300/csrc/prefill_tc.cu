@@ -95,6 +95,7 @@ struct Shared {
   uint64_t q_full[2], q_empty[2], qrot[2];
   uint64_t kv_full[kStages], krot[kStages], kv_empty[kStages];
   uint64_t s_full[2], p_full[2], pv_full[2];
+  uint64_t drain[2];  // wind-down after an abort: each MMA issuer's last commit
   UnitInfo info[2];
   uint32_t tmem_base;
   int32_t abort;
@@ -224,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh->s_full[i], 1);
       mbar_init(&sh->p_full[i], 1);
       mbar_init(&sh->pv_full[i], 1);
+      mbar_init(&sh->drain[i], 1);
     }
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sh->kv_full[i], 1);
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- TMA producer
       griddep_wait();  // the schedule written by the kernel before this one
       const int n_units = p.hdr->n_duos * p.heads;
-      uint32_t n = 0, c = 0;
+      uint32_t n = 0, c = 0, nq = 0;  // units taken, K/V tiles and Q pairs issued
       PHASE_DECL;
       for (;; ++n) {
         const int slot = n & 1;
@@ -286,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(q, &qkv_map, &sh->q_full[slot], h * kHead, inf.row0 + inf.qt0 * kBM);
         if (inf.nt == 2)
           tma_load_2d(q + kTile, &qkv_map, &sh->q_full[slot], h * kHead, inf.row0 + (inf.qt0 + 1) * kBM);
+        ++nq;
         const int kx = (p.heads + g) * kHead, vx = (p.heads + p.kv_heads + g) * kHead;
         const int kvrow = (inf.s * p.kv_heads + g) * p.cap;  // cache row of key 0
         bool ok = true;
@@ -304,6 +307,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
+      }
+      if (*abort_flag) {
+        // every copy this thread issued lands before the CTA releases its
+        // shared memory: the last fill of each stage / Q slot (earlier fills
+        // of a stage completed before the stage was refilled)
+        for (uint32_t st = 0; st < kStages; ++st)
+          if (c > st) mbar_wait(&sh->kv_full[st], (((c - 1 - (c - 1 - st) % kStages)) / kStages) & 1);
+        for (uint32_t sl = 0; sl < 2; ++sl)
+          if (nq > sl) mbar_wait(&sh->q_full[sl], ((nq - 1 - (nq - 1 - sl) % 2) >> 1) & 1);
       }
       PHASE_FLUSH(48, true);
     } else if ((warp == 13 || warp == 14) && lane == 0) {
@@ -369,6 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               issue_s((c + 1) % kStages);
               PHASE(6);
             }
+          } else if (!(ok = wait_k(c))) {
+            // a key tile this query tile does not see: its release must still
+            // follow the fill (and the RoPE pass), or this issuer's arrival
+            // could complete the stage's previous phase
+            break;
           }
           tc_commit(&sh->kv_empty[st]);  // this issuer's MMAs reading stage st are issued
           if (t + 1 == inf.ke) tc_commit(&sh->q_empty[slot]);  // and its last S of the unit
@@ -376,6 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mbar_arrive(&sh->unit_empty[slot]);
+      }
+      if (*abort_flag) {  // every MMA this thread issued completes before TMEM is freed
+        tc_commit(&sh->drain[w]);
+        mbar_wait(&sh->drain[w], 0);
       }
       PHASE_FLUSH(w == 0 ? 40 : 56, true);
     }
@@ -474,6 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kb, ke, fb, fe;
       const int off = kCache ? inf.off : 0;  // position of the unit's row 0
       tile_ranges(inf.L, off + inf.L, off, qt, kCausal, kWindow, kb, ke, fb, fe);
+      // chunk rows: the last visible key (this row's position), or none for a padding row
+      const int chunk_hi = row_ok ? off + i : -1;
 
       // Online softmax with a lazily moved reference max: P = 2^(S - m_ref) and
       // O (in TMEM, accumulated by the PV MMAs) stay relative to m_ref, which
@@ -493,16 +516,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < kBN; ++j) x[j] = __uint_as_float(v[j]);
         if (!(t >= fb && t < fe)) {
-          // visible keys of this row in this tile form one interval [lo, hi];
-          // the row sits at position off + i, the sequence has off + L keys
-          const int qk = off + i - k0;
-          int lo = 0, hi = min(kBN - 1, off + inf.L - 1 - k0);
-          if (kCausal) hi = min(hi, qk);
-          if (kWindow >= 0) {
-            lo = max(lo, qk - kWindow);
-            hi = min(hi, qk + kWindow);
+          // visible keys of this row in this tile form one interval [lo, hi]
+          int lo = 0, hi;
+          if (kCache) {
+            hi = min(kBN - 1, chunk_hi - k0);  // causal at position off + i <= off + L - 1
+          } else {
+            hi = min(kBN - 1, inf.L - 1 - k0);
+            if (kCausal) hi = min(hi, i - k0);
+            if (kWindow >= 0) {
+              lo = max(lo, i - kWindow - k0);
+              hi = min(hi, i + kWindow - k0);
+            }
+            if (!row_ok) hi = -1;
           }
-          if (!row_ok) hi = -1;
 #pragma unroll
           for (int j = 0; j < kBN; ++j)
             if (j < lo || j > hi) x[j] = -INFINITY;
@@ -612,21 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     PHASE_FLUSH(16 * w, r == 0);
   }
 
-  // Wind down: after an abort, give copies and MMAs still in flight a bounded
-  // chance to land before shared memory and TMEM are released.
-  __syncthreads();
-  if (*abort_flag && tid == 0) {
-    auto settle = [&](uint64_t* bar) {  // whichever phase is pending, let it finish
-      mbar_wait(bar, 0);
-      mbar_wait(bar, 1);
-    };
-    for (int i = 0; i < kStages; ++i) settle(&sh->kv_full[i]);
-    for (int i = 0; i < 2; ++i) {
-      settle(&sh->q_full[i]);
-      settle(&sh->s_full[i]);
-      settle(&sh->pv_full[i]);
-    }
-  }
+  // Wind down: after an abort the producer and the MMA issuers have waited
+  // (bounded) for their own copies and MMAs in flight; then TMEM is freed.
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
