@@ -11,6 +11,29 @@
 
 #include "kime_internal.h"
 
+// Phase profiler, compiled in only with -DKIME_PHASE_PROFILE: a role's
+// first thread charges clock() time (32-bit: a launch is far below 2^32
+// cycles) to numbered phases and adds its totals to a __device__ array of
+// the translation unit at the end.  Normal builds expand every PHASE_* to
+// nothing.
+#ifdef KIME_PHASE_PROFILE
+#define PHASE_DECL(n) unsigned ph_t0 = static_cast<unsigned>(clock()), ph_acc[n] = {0}
+#define PHASE(k)                                          \
+  {                                                       \
+    const unsigned now_ = static_cast<unsigned>(clock()); \
+    ph_acc[k] += now_ - ph_t0;                            \
+    ph_t0 = now_;                                         \
+  }
+#define PHASE_FLUSH(arr, base, cond)                                                     \
+  if (cond)                                                                              \
+    for (int q_ = 0; q_ < static_cast<int>(sizeof(ph_acc) / sizeof(ph_acc[0])); ++q_) \
+      atomicAdd(&arr[(base) + q_], static_cast<unsigned long long>(ph_acc[q_]))
+#else
+#define PHASE_DECL(n)
+#define PHASE(k)
+#define PHASE_FLUSH(arr, base, cond)
+#endif
+
 namespace kime {
 
 // ---- device-side status bits (OR-ed into *dev_status) ------------------------
@@ -84,75 +107,18 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// 2^x of a packed f16 pair with one MUFU operation.
-__device__ __forceinline__ uint32_t fast_exp2_f16x2(uint32_t x) {
-  uint32_t y;
-  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
-}
-__device__ __forceinline__ float f16lo(uint32_t w) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
-}
-__device__ __forceinline__ float f16hi(uint32_t w) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
-}
+// 2^x on the MUFU (approximate, subnormal results flushed to zero; 2^-inf = 0).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
-// Pairs of floats in one 64-bit register for the f32x2 instructions (one
-// issue slot for two IEEE round-to-nearest operations).
-__device__ __forceinline__ uint64_t f2(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ float f2_lo(uint64_t v) {
-  float a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-  return a;
-}
-__device__ __forceinline__ float f2_hi(uint64_t v) {
-  float a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-  return b;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 // max of three floats in one instruction
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
-}
-
-// 2^x on the FMA pipe, for x <= 127: x = n + f with n = round(x) (the
-// 1.5*2^23 magic-number rounding) and f in [-0.5, 0.5]; 2^f by the degree-3
-// polynomial with the smallest maximum relative error on that interval
-// (7.5e-5; Remez fit, gen_exp2_poly.py); 2^n added to the exponent field.
-// Arguments below -125 are taken as -125 (result 2^-125, not 0), so callers
-// use it only where no key is masked.
-__device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -125.f);
-  const float t = x + 12582912.f;
-  const float f = x - (t - 12582912.f);
-  const float p = fmaf(fmaf(fmaf(0.0551716685f, f, 0.2426111251f), f, 0.6932609677f), f, 0.9999280572f);
-  return __int_as_float(__float_as_int(p) + ((__float_as_int(t) - 0x4B400000) << 23));
 }
 
 // RoPE (rotate-half) of one pair with one rounding per operation and no

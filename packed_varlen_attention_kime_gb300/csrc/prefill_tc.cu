@@ -42,25 +42,9 @@
 // bounded; on a timeout every role winds down.
 #include "kime_common.cuh"
 
-// Phase profiler, compiled in only with -DKIME_PHASE_PROFILE: each role's
-// first thread charges clock64() time to numbered phases and adds its totals
-// to g_kime_phase at the end.  Normal builds expand every PHASE_* to nothing.
 #ifdef KIME_PHASE_PROFILE
-__device__ unsigned long long g_kime_phase[64];
-#define PHASE_DECL unsigned long long ph_t0 = clock64(), ph_acc[12] = {0}
-#define PHASE(k)                              \
-  {                                           \
-    const unsigned long long now_ = clock64(); \
-    ph_acc[k] += now_ - ph_t0;                 \
-    ph_t0 = now_;                              \
-  }
-#define PHASE_FLUSH(base, cond) \
-  if (cond)                     \
-    for (int q_ = 0; q_ < 12; ++q_) atomicAdd(&g_kime_phase[(base) + q_], ph_acc[q_])
-#else
-#define PHASE_DECL
-#define PHASE(k)
-#define PHASE_FLUSH(base, cond)
+constexpr int kPhaseSlots = 96;  // role bases 0, 16, 32, 40, 48, 56; at most 12 phases each
+__device__ unsigned long long g_kime_phase[kPhaseSlots];
 #endif
 
 namespace kime {
@@ -76,12 +60,7 @@ constexpr uint32_t kOffV = kOffK + kStages * kTile;
 constexpr uint32_t kOffBar = kOffV + kStages * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kPolyOf8 = 0;  // exponentials per 8 keys taken on the FMA pipe
-#ifndef KIME_EXP_F16
-#define KIME_EXP_F16 0
-#endif
-constexpr bool kExpF16 = KIME_EXP_F16;  // two exponentials per MUFU op on f16 arguments
-constexpr float kLazy = kExpF16 ? 1.f : 8.f;  // reference max moves when exceeded by more
+constexpr float kLazy = 8.f;  // the reference max moves when exceeded by more (log2 units)
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -262,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       griddep_wait();  // the schedule written by the kernel before this one
       const int n_units = p.hdr->n_duos * p.heads;
       uint32_t n = 0, c = 0, nq = 0;  // units taken, K/V tiles and Q pairs issued
-      PHASE_DECL;
+      PHASE_DECL(4);
       for (;; ++n) {
         const int slot = n & 1;
         const int u = atomicAdd(&p.hdr->next_duo, 1);
@@ -317,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t sl = 0; sl < 2; ++sl)
           if (nq > sl) mbar_wait(&sh->q_full[sl], ((nq - 1 - (nq - 1 - sl) % 2) >> 1) & 1);
       }
-      PHASE_FLUSH(48, true);
+      PHASE_FLUSH(g_kime_phase, 48, true);
     } else if ((warp == 13 || warp == 14) && lane == 0) {
       // ---------------------------------------------------------- MMA issuers
       // one per query tile (warp 13: tile A, warp 14: tile B), so neither
@@ -325,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w = warp - 13;
       uint32_t n = 0, c = 0, pc = 0;
       const uint32_t tS = tmem + w * 128, tO = tmem + 256 + w * 64, tP = tmem + 384 + w * 64;
-      PHASE_DECL;
+      PHASE_DECL(8);
       for (;; ++n) {
         const int slot = n & 1;
         PHASE(4);
@@ -398,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(&sh->drain[w]);
         mbar_wait(&sh->drain[w], 0);
       }
-      PHASE_FLUSH(w == 0 ? 40 : 56, true);
+      PHASE_FLUSH(g_kime_phase, w == 0 ? 40 : 56, true);
     }
     __syncwarp();
   } else if (wg == 2) {
@@ -406,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ RoPE
     const int r = tid - 256;  // row of every tile this thread converts
     uint32_t n = 0, c = 0;
-    PHASE_DECL;
+    PHASE_DECL(6);
     for (;; ++n) {
       const int slot = n & 1;
       bool ok = wait(&sh->unit_full[slot], (n >> 1) & 1);
@@ -469,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
     }
-    PHASE_FLUSH(32, r == 0);
+    PHASE_FLUSH(g_kime_phase, 32, r == 0);
   } else {
     regs_inc<160>();
     // ------------------------------------------------------------ softmax warpgroups
@@ -479,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + w * 128 + lane_off, tO = tmem + 256 + w * 64 + lane_off;
     const uint32_t tP = tmem + 384 + w * 64 + lane_off;
     uint32_t n = 0, sc = 0, pvc = 0;
-    PHASE_DECL;
+    PHASE_DECL(9);
     for (;; ++n) {
       const int slot = n & 1;
       bool ok = wait(&sh->unit_full[slot], (n >> 1) & 1);
@@ -557,44 +536,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         PHASE(3);
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        // P = 2^(x - m_use) on the MUFU, row sums in four chains.  A masked key
+        // (-inf) gives 0.
         float rs2f[4] = {0.f, 0.f, 0.f, 0.f};
-        if (kExpF16) {
-          // P = 2^(x - m_use) two keys per MUFU operation: the argument is
-          // rounded to f16 (x - m_use <= kLazy keeps its error below 2^-11
-          // where P is large) and P comes out as the f16 pair the MMA reads;
-          // a masked key saturates to -65504 and gives 0.
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P at a time
-            uint32_t pw[16];
+        for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P at a time
+          uint32_t pw[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int j = q4 * 32 + 2 * e;
-              const uint32_t ph = fast_exp2_f16x2(pack_f16x2(x[j] - m_use, x[j + 1] - m_use));
-              rs2f[e & 3] += f16lo(ph) + f16hi(ph);
-              pw[e] = ph;
-            }
-            tmem_st16(tP + q4 * 16, pw);  // this row's P: keys 2c, 2c+1 in column c
+          for (int e = 0; e < 16; ++e) {
+            const int j = q4 * 32 + 2 * e;
+            const float p0 = fast_exp2(x[j] - m_use), p1 = fast_exp2(x[j + 1] - m_use);
+            rs2f[e & 3] += p0 + p1;
+            pw[e] = pack_f16x2(p0, p1);
           }
-        } else {
-          // P = 2^(x - m_use), row sums in four chains; kPolyOf8 of every 8
-          // exponentials on the FMA pipe (exp2_poly), the rest on the MUFU.  A
-          // masked key (-inf) gives 0 on the MUFU and 2^-125 from exp2_poly:
-          // both round to an f16 zero in P, and 2^-125 cannot change l (l >= 1:
-          // the row max contributes 2^(max - m_ref) >= 1).
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P at a time
-            uint32_t pw[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int j = q4 * 32 + 2 * e;
-              const float a0 = x[j] - m_use, a1 = x[j + 1] - m_use;
-              const float p0 = (j & 7) < kPolyOf8 ? exp2_poly(a0) : fast_exp2(a0);
-              const float p1 = ((j + 1) & 7) < kPolyOf8 ? exp2_poly(a1) : fast_exp2(a1);
-              rs2f[e & 3] += p0 + p1;
-              pw[e] = pack_f16x2(p0, p1);
-            }
-            tmem_st16(tP + q4 * 16, pw);  // this row's P: keys 2c, 2c+1 in column c
-          }
+          tmem_st16(tP + q4 * 16, pw);  // this row's P: keys 2c, 2c+1 in column c
         }
         const float rowsum = (rs2f[0] + rs2f[1]) + (rs2f[2] + rs2f[3]);
         l = l * alpha + rowsum;
@@ -635,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       PHASE(8);
     }
-    PHASE_FLUSH(16 * w, r == 0);
+    PHASE_FLUSH(g_kime_phase, 16 * w, r == 0);
   }
 
   // Wind down: after an abort the producer and the MMA issuers have waited
@@ -655,7 +610,7 @@ extern "C" int kime_debug_phase_read(unsigned long long* host) {
   return cudaMemcpyFromSymbol(host, g_kime_phase, sizeof(g_kime_phase));
 }
 extern "C" int kime_debug_phase_clear() {
-  unsigned long long z[64] = {0};
+  unsigned long long z[kPhaseSlots] = {0};
   return cudaMemcpyToSymbol(g_kime_phase, z, sizeof(z));
 }
 #endif
