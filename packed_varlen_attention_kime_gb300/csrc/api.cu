@@ -204,8 +204,15 @@ int decode_common(const void* qkv_new, const int32_t* pos, int n_seqs, int heads
       !aligned16(rope_cos) || !aligned16(rope_sin))
     return KIME_EINVAL;
   if (n_seqs > 65535) return KIME_ERANGE;
+  if (static_cast<long long>(kime::dec_items_for(cap)) * n_seqs * kv_heads >= (1LL << 30)) return KIME_ERANGE;
   if (workspace_bytes < kime::decode_workspace_bytes(n_seqs, heads, kv_heads, cap)) return KIME_ERANGE;
-  return cuda_status(kime::launch_decode(qkv_new, pos, n_seqs, heads, kv_heads, cap, scale, rope_cos, rope_sin,
+  if (static_cast<long long>(n_seqs) * kv_heads * cap >= (1LL << 31)) return KIME_ERANGE;
+  CUtensorMap kmap, vmap;
+  const int rows = n_seqs * kv_heads * cap;
+  int rc = encode_qkv_map(&kmap, k_cache, rows, kime::kHead);
+  if (rc) return rc;
+  if ((rc = encode_qkv_map(&vmap, v_cache, rows, kime::kHead))) return rc;
+  return cuda_status(kime::launch_decode(&kmap, &vmap, qkv_new, pos, n_seqs, heads, kv_heads, cap, scale, rope_cos, rope_sin,
                                          rope_len, k_cache, v_cache, out, workspace, dev_status,
                                          static_cast<cudaStream_t>(stream), append));
 }

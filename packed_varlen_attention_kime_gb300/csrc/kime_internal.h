@@ -50,6 +50,20 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int max_pairs_for(int n_seqs, int total_tokens) { return total_tokens / kBM + n_seqs + 1; }
 inline int max_duos_for(int n_seqs, int total_tokens) { return total_tokens / (2 * kBM) + n_seqs + 1; }
 inline int dec_chunks_for(int cap) { return (cap + kDecChunk - 1) / kDecChunk; }
+constexpr int kDecItemChunks = 16;  // chunks per decode work item
+// consumer groups of the decode kernel for G = heads / kv_heads (parts per item)
+inline int dec_groups_for(int G) { (void)G; return 1; }
+inline int dec_items_for(int cap) { return (dec_chunks_for(cap) + kDecItemChunks - 1) / kDecItemChunks; }
+// Decode workspace: a 16-byte plan header (work counter, item count), tickets
+// [n_seqs * kv_heads] int32, the work list int4 [n_seqs * kv_heads * items],
+// then (256-byte aligned) partials [n_seqs][kv_heads][items][G][68] f32.
+inline size_t dec_ws_items_offset(int n_seqs, int kv_heads) {
+  return align_up(16 + static_cast<size_t>(n_seqs) * kv_heads * 4, 16);
+}
+inline size_t dec_ws_head_bytes(int n_seqs, int kv_heads, int cap) {
+  return align_up(dec_ws_items_offset(n_seqs, kv_heads) +
+                      static_cast<size_t>(n_seqs) * kv_heads * dec_items_for(cap) * 16, 256);
+}
 
 // Prefill workspace: header | pairs[max_pairs] | duos[max_duos].
 inline size_t varlen_workspace_bytes(int n_seqs, int total_tokens) {
@@ -85,7 +99,10 @@ cudaError_t launch_kv_append_varlen(const void* qkv, const int32_t* cu, const in
 cudaError_t launch_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int cap,
                              const float* cos_t, const float* sin_t, int rope_len, void* k_cache, void* v_cache,
                              int32_t* dev_status, cudaStream_t st);
-cudaError_t launch_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int cap,
+// k_map / v_map: the caches as [n_seqs * kv_heads * cap, 64] bf16 rows (boxes
+// of 128 rows, 128-byte swizzle).
+cudaError_t launch_decode(const CUtensorMap* k_map, const CUtensorMap* v_map, const void* qkv_new, const int32_t* pos,
+                          int n_seqs, int heads, int kv_heads, int cap,
                           float scale, const float* cos_t, const float* sin_t, int rope_len, const void* k_cache,
                           const void* v_cache, void* out, void* ws, int32_t* dev_status, cudaStream_t st,
                           bool append);
