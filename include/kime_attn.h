@@ -48,7 +48,11 @@ typedef enum {
   KIME_ETIMEOUT = -4 /* reserved for callers mapping KIME_DEV_TIMEOUT to a status */
 } kime_status;
 
-typedef enum { KIME_F32 = 0, KIME_BF16 = 1 } kime_dtype;
+/* Element types of qkv and out.  KIME_F32_F16OUT / KIME_F32_BF16OUT: FP32 qkv
+ * and a 16-bit output, the mixed precision of kime-cuda 0.0.3 src/plan.rs
+ * (fn types: with Precision::F16 attention's qkv stays FP32 -- FP16 rounding of
+ * q and k would move ModernBERT's softmax -- while its output is FP16). */
+typedef enum { KIME_F32 = 0, KIME_BF16 = 1, KIME_F32_F16OUT = 2, KIME_F32_BF16OUT = 3 } kime_dtype;
 
 /* Bits OR-ed into *dev_status by the kernels. */
 #define KIME_DEV_BAD_CU 1       /* cu_seqlens not monotone, outside [0,total], cu[0]!=0 or cu[n]!=total */
@@ -68,18 +72,22 @@ typedef enum { KIME_F32 = 0, KIME_BF16 = 1 } kime_dtype;
  * offset 0 is ffai-argus CausalSoftmax.  Masked keys are skipped, never
  * materialised.
  *
- *  qkv          device, [total_tokens, W], dtype (KIME_F32 or KIME_BF16)
+ *  qkv          device, [total_tokens, W]: FP32 (KIME_F32, KIME_F32_F16OUT,
+ *               KIME_F32_BF16OUT) or BF16 (KIME_BF16)
  *  cu_seqlens   device int32 [n_seqs+1], cu[0]=0, non-decreasing, cu[n]=total_tokens
  *  max_seqlen   host upper bound on every sequence length; must be <= rope_len
  *  window       -1 or >= 0; causal 0/1; scale > 0 (0.125, or 1 if q is pre-scaled)
  *  rope_cos/sin device float32 [rope_len, 32]
- *  out          device, [total_tokens, heads*64], same dtype as qkv; rows of
- *               skipped sequences are left untouched
+ *  out          device, [total_tokens, heads*64]: FP32 (KIME_F32), BF16
+ *               (KIME_BF16, KIME_F32_BF16OUT) or FP16 (KIME_F32_F16OUT),
+ *               rounded to nearest even from FP32; rows of skipped sequences
+ *               are left untouched
  *  workspace    device scratch of kime_attn_workspace_bytes(0, ...) bytes;
  *               contents need no initialisation; calls that share it must be
  *               ordered on one stream
- * BF16 runs on the tensor cores (tcgen05, FP32 accumulate); FP32 runs on FP32
- * FMA.  Two launches: the device scheduler, then the attention kernel. */
+ * BF16 runs on the tensor cores (tcgen05, FP32 accumulate); FP32 qkv (all
+ * three FP32 codes) runs on FP32 FMA.  Two launches: the device scheduler,
+ * then the attention kernel. */
 int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int n_seqs, int total_tokens,
                      int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal, float scale,
                      const float* rope_cos, const float* rope_sin, int rope_len, void* out, void* workspace,

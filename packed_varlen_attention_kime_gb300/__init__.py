@@ -25,7 +25,7 @@ __all__ = [
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkime_attn.so")
 
-KIME_F32, KIME_BF16 = 0, 1
+KIME_F32, KIME_BF16, KIME_F32_F16OUT, KIME_F32_BF16OUT = 0, 1, 2, 3
 DEV_BAD_CU, DEV_SEQ_TOO_LONG, DEV_BAD_POS, DEV_TIMEOUT = 1, 2, 4, 8
 
 EXPORTED_SYMBOLS = (
@@ -104,12 +104,15 @@ def _stream(stream, device):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _dtype_code(t: torch.Tensor) -> int:
-    if t.dtype == torch.float32:
-        return KIME_F32
-    if t.dtype == torch.bfloat16:
+def _dtype_code(qkv: torch.Tensor, out_dtype) -> int:
+    """kime_dtype of (qkv, out): same type, or FP32 qkv with a 16-bit output."""
+    if qkv.dtype == torch.bfloat16 and out_dtype == torch.bfloat16:
         return KIME_BF16
-    raise TypeError(f"qkv must be float32 or bfloat16, got {t.dtype}")
+    if qkv.dtype == torch.float32:
+        codes = {torch.float32: KIME_F32, torch.float16: KIME_F32_F16OUT, torch.bfloat16: KIME_F32_BF16OUT}
+        if out_dtype in codes:
+            return codes[out_dtype]
+    raise TypeError(f"unsupported qkv/out dtypes {qkv.dtype} -> {out_dtype}")
 
 
 def kime_attn_workspace_bytes(op: int, n_seqs: int, total_tokens: int = 0, heads: int = 1,
@@ -127,17 +130,19 @@ def kime_rope_tables(theta: float, length: int):
 
 
 def kime_attn_varlen(qkv, cu_seqlens, max_seqlen, heads, kv_heads, window, causal, scale,
-                     rope_cos, rope_sin, out=None, workspace=None, dev_status=None, stream=None):
-    """Attention over the packed batch; returns ``out`` [T, heads*64] (qkv's dtype)."""
+                     rope_cos, rope_sin, out=None, workspace=None, dev_status=None, stream=None, out_dtype=None):
+    """Attention over the packed batch; returns ``out`` [T, heads*64].  Its
+    dtype is qkv's, or (FP32 qkv) float16 / bfloat16 when ``out`` or
+    ``out_dtype`` says so."""
     lib = load_library()
     T = qkv.shape[0]
     n_seqs = cu_seqlens.numel() - 1
     if out is None:
-        out = torch.empty((T, heads * 64), dtype=qkv.dtype, device=qkv.device)
+        out = torch.empty((T, heads * 64), dtype=out_dtype or qkv.dtype, device=qkv.device)
     need = kime_attn_workspace_bytes(0, n_seqs, T)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=qkv.device)
-    rc = lib.kime_attn_varlen(_p(qkv), _dtype_code(qkv), _p(cu_seqlens), n_seqs, T, int(max_seqlen), heads,
+    rc = lib.kime_attn_varlen(_p(qkv), _dtype_code(qkv, out.dtype), _p(cu_seqlens), n_seqs, T, int(max_seqlen), heads,
                               kv_heads, 64, int(window), int(bool(causal)), float(scale), _p(rope_cos),
                               _p(rope_sin), rope_cos.shape[0], _p(out), _p(workspace),
                               workspace.numel() * workspace.element_size(), _p(dev_status),
@@ -158,7 +163,7 @@ def kime_attn_varlen_noalloc(qkv, cu_seqlens, max_seqlen, heads, kv_heads, windo
     n_seqs = cu_seqlens.numel() - 1
     if out is None:
         out = torch.empty((T, heads * 64), dtype=qkv.dtype, device=qkv.device)
-    rc = lib.kime_attn_varlen_noalloc(_p(qkv), _dtype_code(qkv), _p(cu_seqlens), n_seqs, T, int(max_seqlen),
+    rc = lib.kime_attn_varlen_noalloc(_p(qkv), _dtype_code(qkv, out.dtype), _p(cu_seqlens), n_seqs, T, int(max_seqlen),
                                       heads, kv_heads, 64, int(window), int(bool(causal)), float(scale),
                                       _p(rope_cos), _p(rope_sin), rope_cos.shape[0], _p(out), _p(dev_status),
                                       _stream(stream, qkv.device))

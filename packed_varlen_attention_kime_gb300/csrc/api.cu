@@ -87,7 +87,8 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
                      int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal, float scale,
                      const float* rope_cos, const float* rope_sin, int rope_len, void* out, void* workspace,
                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  if (dtype != KIME_F32 && dtype != KIME_BF16) return KIME_EINVAL;
+  if (dtype != KIME_F32 && dtype != KIME_BF16 && dtype != KIME_F32_F16OUT && dtype != KIME_F32_BF16OUT)
+    return KIME_EINVAL;
   if (!heads_ok(heads, kv_heads, head_dim)) return KIME_EINVAL;
   if (n_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || rope_len < 0 || window < -1) return KIME_EINVAL;
   if (!(scale > 0.f) || !isfinite(scale)) return KIME_EINVAL;
@@ -106,10 +107,11 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
   int rc = cuda_status(kime::launch_schedule(cu_seqlens, nullptr, n_seqs, total_tokens, max_seqlen, causal, window,
                                              0, 0, workspace, max_pairs, dev_status, st));
   if (rc) return rc;
-  if (dtype == KIME_F32) {
+  if (dtype != KIME_BF16) {
+    const int out_kind = dtype == KIME_F32 ? 0 : (dtype == KIME_F32_F16OUT ? 1 : 2);
     return cuda_status(kime::launch_varlen_f32(static_cast<const float*>(qkv), cu_seqlens, n_seqs, total_tokens,
-                                               heads, kv_heads, window, causal, scale, rope_cos, rope_sin,
-                                               static_cast<float*>(out), workspace, max_pairs, dev_status, st));
+                                               heads, kv_heads, window, causal, scale, rope_cos, rope_sin, out,
+                                               out_kind, workspace, max_pairs, dev_status, st));
   }
   CUtensorMap map;
   rc = encode_qkv_map(&map, qkv, total_tokens, static_cast<int>(W));

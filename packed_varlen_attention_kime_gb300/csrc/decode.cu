@@ -578,27 +578,25 @@ __global__ void __launch_bounds__(DecCfg<G>::threads, DecCfg<G>::ctas_per_sm)
         }
         bar_group(cg);
         if (*g_last) {
-          // per-head max of m over the parts (strided, then reduced), then
-          // blocks of part weights 2^(m_c - M) in shared memory; every output
-          // sums its column over the parts with independent loads
+          // per-head max M of m over the parts, then blocks of part weights
+          // 2^(m_c - M) in shared memory (with L = sum l_c 2^(m_c - M)); every
+          // output sums its column over the parts with independent loads
           const float* all = partials + (static_cast<size_t>(s) * kv_heads + g) * max_items * kGrp * G * kPartialFloats;
-          float* red = red_o;                      // [G][128], reusing this group's buffers
-          float* hdr = red + G * kGroupThreads;    // [G] M, [G] L
-          float* wts = hdr + 2 * G;                // [block][G]
+          float* hdr = red_o;                      // [G] M, [G] L (this group's buffers)
+          float* wts = hdr + 2 * G;                // [block][G] m_c, then weights
           constexpr int kBlock = kMergeBlock;
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            float M = -INFINITY;
-            for (int cc = gtid; cc < n_parts; cc += kGroupThreads)
-              M = fmaxf(M, __ldcg(all + (cc * G + hh) * kPartialFloats));
-            red[hh * kGroupThreads + gtid] = M;
-          }
-          bar_group(cg);
-          if (gtid < G) {
-            float M = -INFINITY;
-            for (int k = 0; k < kGroupThreads; ++k) M = fmaxf(M, red[gtid * kGroupThreads + k]);
-            hdr[gtid] = M;
-            hdr[G + gtid] = 0.f;
+          if (gtid < G) hdr[gtid] = -INFINITY;
+          for (int c0 = 0; c0 < n_parts; c0 += kBlock) {
+            const int nb = min(kBlock, n_parts - c0);
+            bar_group(cg);
+            for (int e = gtid; e < nb * G; e += kGroupThreads) wts[e] = __ldcg(all + (c0 * G + e) * kPartialFloats);
+            bar_group(cg);
+            if (gtid < G) {
+              float M = hdr[gtid];
+              for (int cc = 0; cc < nb; ++cc) M = fmaxf(M, wts[cc * G + gtid]);
+              hdr[gtid] = M;
+              hdr[G + gtid] = 0.f;
+            }
           }
           constexpr int kPer = (G * kHead + kGroupThreads - 1) / kGroupThreads;
           float O[kPer];

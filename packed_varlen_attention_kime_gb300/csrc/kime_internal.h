@@ -83,9 +83,11 @@ size_t decode_workspace_bytes(int n_seqs, int heads, int kv_heads, int cap);
 cudaError_t launch_schedule(const int32_t* cu, const int32_t* pos, int n_seqs, int total, int max_seqlen,
                             int causal, int window, int cap, int rope_len, void* ws, int max_pairs,
                             int32_t* dev_status, cudaStream_t st);
+// out_kind: 0 FP32 out, 1 FP16 out, 2 BF16 out (round to nearest even).
 cudaError_t launch_varlen_f32(const float* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
                               int window, int causal, float scale, const float* cos_t, const float* sin_t,
-                              float* out, void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
+                              void* out, int out_kind, void* ws, int max_pairs, int32_t* dev_status,
+                              cudaStream_t st);
 // k_map / v_map == nullptr: keys and values come from the qkv rows (packed
 // sequences).  Otherwise from caches [n_seqs * kv_heads * cap, 64] (chunks).
 cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_map, const CUtensorMap* v_map,

@@ -42,9 +42,22 @@ __device__ __forceinline__ void load_rotated(const float* __restrict__ qkv, size
   }
 }
 
+// Output element stores: FP32, or FP32 rounded once to FP16 / BF16 (nearest
+// even) for the mixed-precision variant (FP32 qkv, 16-bit out).
+__device__ __forceinline__ void store4(float* dst, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(dst) = make_float4(a, b, c, d);
+}
+__device__ __forceinline__ void store4(__half* dst, float a, float b, float c, float d) {
+  *reinterpret_cast<uint2*>(dst) = make_uint2(pack_f16x2(a, b), pack_f16x2(c, d));
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* dst, float a, float b, float c, float d) {
+  *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(a, b), pack_bf16x2(c, d));
+}
+
+template <typename OutT>
 __global__ void __launch_bounds__(kThreads)
     varlen_f32_kernel(const float* __restrict__ qkv, int heads, int kv_heads, int window, int causal, float scale,
-                      const float* __restrict__ cos_t, const float* __restrict__ sin_t, float* __restrict__ out,
+                      const float* __restrict__ cos_t, const float* __restrict__ sin_t, OutT* __restrict__ out,
                       WsHeader* hdr, const Pair* __restrict__ pairs) {
   extern __shared__ float4 smem_f4[];
   float(*Ks)[kHead] = reinterpret_cast<float(*)[kHead]>(smem_f4);
@@ -129,29 +142,25 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     if (valid) {
-      float* dst = out + static_cast<size_t>(pr.row0 + i) * heads * kHead + h * kHead;
+      OutT* dst = out + static_cast<size_t>(pr.row0 + i) * heads * kHead + h * kHead;
       const float inv = 1.f / l;
 #pragma unroll
-      for (int d = 0; d < kHead; d += 4)
-        *reinterpret_cast<float4*>(dst + d) = make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+      for (int d = 0; d < kHead; d += 4) store4(dst + d, o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
     }
     __syncthreads();  // s_unit is rewritten at the top
   }
 }
 
-}  // namespace
-
-cudaError_t launch_varlen_f32(const float* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
-                              int window, int causal, float scale, const float* cos_t, const float* sin_t,
-                              float* out, void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st) {
-  (void)cu; (void)n_seqs; (void)total; (void)max_pairs; (void)dev_status;
+template <typename OutT>
+cudaError_t launch_f32_as(const float* qkv, int heads, int kv_heads, int window, int causal, float scale,
+                          const float* cos_t, const float* sin_t, OutT* out, void* ws, cudaStream_t st) {
   static int configured[64] = {0};
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int smem = 2 * kBN * kHead * static_cast<int>(sizeof(float));
   if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(varlen_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(varlen_f32_kernel<OutT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
@@ -167,8 +176,23 @@ cudaError_t launch_varlen_f32(const float* qkv, const int32_t* cu, int n_seqs, i
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, varlen_f32_kernel, qkv, heads, kv_heads, window, causal, scale, cos_t, sin_t, out,
-                            hdr, pairs);
+  return cudaLaunchKernelEx(&cfg, varlen_f32_kernel<OutT>, qkv, heads, kv_heads, window, causal, scale, cos_t, sin_t,
+                            out, hdr, pairs);
+}
+
+}  // namespace
+
+cudaError_t launch_varlen_f32(const float* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
+                              int window, int causal, float scale, const float* cos_t, const float* sin_t,
+                              void* out, int out_kind, void* ws, int max_pairs, int32_t* dev_status,
+                              cudaStream_t st) {
+  (void)cu; (void)n_seqs; (void)total; (void)max_pairs; (void)dev_status;
+  if (out_kind == 1)
+    return launch_f32_as(qkv, heads, kv_heads, window, causal, scale, cos_t, sin_t, static_cast<__half*>(out), ws, st);
+  if (out_kind == 2)
+    return launch_f32_as(qkv, heads, kv_heads, window, causal, scale, cos_t, sin_t, static_cast<__nv_bfloat16*>(out),
+                         ws, st);
+  return launch_f32_as(qkv, heads, kv_heads, window, causal, scale, cos_t, sin_t, static_cast<float*>(out), ws, st);
 }
 
 }  // namespace kime

@@ -96,6 +96,27 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("out_dtype,u", [(torch.float16, 2.0 ** -11), (torch.bfloat16, 2.0 ** -8)])
+def test_varlen_f32_qkv_16bit_out(cuda_lib, out_dtype, u):
+    # kime-cuda's mixed precision (FP32 qkv, 16-bit attention output): the
+    # output is the FP32 path's result rounded once to nearest even, bit for
+    # bit, so against the oracle it is within 1e-5 plus half an ulp
+    lengths, H, Hkv, window, causal = [300, 129, 5, 1], 3, 1, 64, True
+    cu = cu_from_lengths(lengths)
+    qkv = random_qkv(lengths, H, Hkv, torch.float32, 1.0, seed=41)
+    dev = torch.device("cuda")
+    c, s = gpu_tables(1e4, max(lengths))
+    f32 = kime.kime_attn_varlen(qkv.to(dev), cu.to(dev), max(lengths), H, Hkv, window, causal, 0.125, c, s)
+    o16 = kime.kime_attn_varlen(qkv.to(dev), cu.to(dev), max(lengths), H, Hkv, window, causal, 0.125, c, s,
+                                out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert o16.dtype == out_dtype
+    assert torch.equal(o16.view(torch.int16), f32.to(out_dtype).view(torch.int16))
+    ref = run_oracle_varlen(qkv, cu, H, Hkv, window, causal, 0.125, 1e4, max(lengths))
+    got = o16.float().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= 1e-5 * (1 + u) + u * np.abs(ref))
+
+
 @pytest.mark.parametrize("lengths,H,Hkv,window,causal,scale", SMALL)
 def test_varlen_f32_small_all_elements(cuda_lib, lengths, H, Hkv, window, causal, scale):
     cu = cu_from_lengths(lengths)
