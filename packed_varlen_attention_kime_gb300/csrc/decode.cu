@@ -178,11 +178,14 @@ struct DecPlan {
 // items come first, then
 // the shorter last items by decreasing size (a counting sort on the chunk
 // count), so the CTAs that take the last items finish soon after the others.
-// Also zeroes the tickets and reports positions outside [0, min(cap,
-// rope_len)) (those sequences get no items).
+// Item 0 of (s, g) number b < n_static is not listed: CTA b of the decode
+// kernel takes it at once, before this list is ready.  Also zeroes the
+// tickets and reports positions outside [0, min(cap, rope_len)) (those
+// sequences get no items).
 __global__ void __launch_bounds__(1024)
     decode_plan_kernel(const int32_t* __restrict__ pos, int n_seqs, int kv_heads, int cap, int rope_len,
-                       DecPlan* plan, int32_t* __restrict__ tickets, int4* __restrict__ items, int32_t* dev_status) {
+                       int n_static, DecPlan* plan, int32_t* __restrict__ tickets, int4* __restrict__ items,
+                       int32_t* dev_status) {
   __shared__ int hist[kItemChunks + 1], cursor[kItemChunks + 1];
   __shared__ int s_bad;
   griddep_launch_dependents();  // the decode kernel sets itself up meanwhile
@@ -201,8 +204,9 @@ __global__ void __launch_bounds__(1024)
       s_bad = 1;
       continue;
     }
-    if (n_c / kItemChunks) atomicAdd(&hist[kItemChunks], (n_c / kItemChunks) * kv_heads);
-    if (n_c % kItemChunks) atomicAdd(&hist[n_c % kItemChunks], kv_heads);
+    for (int g = 0; g < kv_heads; ++g)  // item 0 of the first n_static (s, g) is not listed
+      for (int k = s * kv_heads + g < n_static ? 1 : 0; k * kItemChunks < n_c; ++k)
+        atomicAdd(&hist[min(kItemChunks, n_c - k * kItemChunks)], 1);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -220,11 +224,9 @@ __global__ void __launch_bounds__(1024)
     const int n_c = chunks_of(s);
     if (n_c < 0) continue;
     const int P = pos[s];
-    for (int k = 0; k * kItemChunks < n_c; ++k) {
-      const int sz = min(kItemChunks, n_c - k * kItemChunks);
-      const int at = atomicAdd(&cursor[sz], kv_heads);
-      for (int g = 0; g < kv_heads; ++g) items[at + g] = make_int4(s, g, k, P);
-    }
+    for (int g = 0; g < kv_heads; ++g)
+      for (int k = s * kv_heads + g < n_static ? 1 : 0; k * kItemChunks < n_c; ++k)
+        items[atomicAdd(&cursor[min(kItemChunks, n_c - k * kItemChunks)], 1)] = make_int4(s, g, k, P);
   }
 }
 
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(DecCfg<G>::threads, DecCfg<G>::ctas_per_sm)
                   const float* __restrict__ sin_t, int rope_len, uint16_t* __restrict__ k_cache,
                   uint16_t* __restrict__ v_cache, __nv_bfloat16* __restrict__ out,
                   float* __restrict__ partials, int32_t* __restrict__ tickets, DecPlan* plan,
-                  const int4* __restrict__ items, int max_items, int32_t* dev_status) {
+                  const int4* __restrict__ items, int max_items, int n_static, int32_t* dev_status) {
   using Lay = DecLayout<G>;
   using Cfg = DecCfg<G>;
   constexpr int kRing = Cfg::ring, kDecWarps = Cfg::warps;
@@ -292,15 +294,29 @@ __global__ void __launch_bounds__(DecCfg<G>::threads, DecCfg<G>::ctas_per_sm)
     uint32_t it = 0, cs = 0;  // items published, chunks issued
     bool ok = true;
     PHASE_DECL(5);
-    griddep_wait();  // the work list of the plan kernel before this one
-    const int n_items = plan->n_items;
+    // The first item of CTA b < n_static is item 0 of (s, g) number b, taken
+    // at once; the rest come one at a time from the plan kernel's list.
+    bool first = blockIdx.x < n_static, listed = false;
+    int n_items = 0;
     for (;;) {
-      // one item at a time from the list
-      int idx = 0;
-      if (lane == 0) idx = atomicAdd(&plan->next, 1);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
-      if (idx >= n_items) break;
-      const int4 rec = items[idx];
+      int4 rec;
+      if (first) {
+        first = false;
+        const int sg = blockIdx.x, s0 = sg / kv_heads, P0 = __ldg(pos + s0);
+        if (P0 < 0 || P0 >= cap || P0 >= rope_len) continue;  // reported by the plan kernel
+        rec = make_int4(s0, sg - s0 * kv_heads, 0, P0);
+      } else {
+        if (!listed) {
+          griddep_wait();  // the work list of the plan kernel before this one
+          n_items = plan->n_items;
+          listed = true;
+        }
+        int idx = 0;
+        if (lane == 0) idx = atomicAdd(&plan->next, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx >= n_items) break;
+        rec = items[idx];
+      }
       PHASE(0);
       {
         const int is = rec.x, ig = rec.y, ik = rec.z, iP = rec.w;
@@ -572,6 +588,7 @@ __global__ void __launch_bounds__(DecCfg<G>::threads, DecCfg<G>::ctas_per_sm)
         // arrive merges all of them
         bar_group(cg);
         if (gtid == 0) {
+          griddep_wait();  // the tickets were zeroed by the plan kernel
           __threadfence();
           *g_last = atomicAdd(&tickets[s * kv_heads + g], 1) == n_parts - 1;
           __threadfence();
@@ -673,14 +690,17 @@ cudaError_t launch_decode_g(const CUtensorMap* k_map, const CUtensorMap* v_map, 
   int32_t* tickets = reinterpret_cast<int32_t*>(w + sizeof(DecPlan));
   int4* items = reinterpret_cast<int4*>(w + dec_ws_items_offset(n_seqs, kv_heads));
   float* partials = reinterpret_cast<float*>(w + dec_ws_head_bytes(n_seqs, kv_heads, cap));
-  decode_plan_kernel<<<1, 1024, 0, st>>>(pos, n_seqs, kv_heads, cap, rope_len, plan, tickets, items, dev_status);
+  const long long n_max = static_cast<long long>(max_items) * n_seqs * kv_heads;
+  const int grid = static_cast<int>(std::min<long long>(static_cast<long long>(DecCfg<G>::ctas_per_sm) * sms, n_max));
+  const int n_static = std::min(grid, n_seqs * kv_heads);
+  decode_plan_kernel<<<1, 1024, 0, st>>>(pos, n_seqs, kv_heads, cap, rope_len, n_static, plan, tickets, items,
+                                         dev_status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long long n_max = static_cast<long long>(max_items) * n_seqs * kv_heads;
   // launched with programmatic stream serialization: its prologue overlaps
   // the plan kernel, whose list it waits for (griddep_wait) before reading it
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(std::min<long long>(static_cast<long long>(DecCfg<G>::ctas_per_sm) * sms, n_max)));
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(DecCfg<G>::threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -693,7 +713,7 @@ cudaError_t launch_decode_g(const CUtensorMap* k_map, const CUtensorMap* v_map, 
                             pos, n_seqs, heads, kv_heads, cap, scale * 1.4426950408889634f, cos_t, sin_t, rope_len,
                             static_cast<uint16_t*>(k_cache), static_cast<uint16_t*>(v_cache),
                             static_cast<__nv_bfloat16*>(out), partials, tickets, plan,
-                            static_cast<const int4*>(items), max_items, dev_status);
+                            static_cast<const int4*>(items), max_items, n_static, dev_status);
   return cudaGetLastError();
 }
 
