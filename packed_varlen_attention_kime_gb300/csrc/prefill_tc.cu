@@ -244,10 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       PHASE_DECL(4);
       for (;; ++n) {
         const int slot = n & 1;
-        const int u = atomicAdd(&p.hdr->next_duo, 1);
         PHASE(3);
         if (!wait(&sh->unit_empty[slot], ((n >> 1) & 1) ^ 1)) break;
         PHASE(0);
+        // claimed only once its slot is free, so no unit waits behind a busy CTA
+        const int u = atomicAdd(&p.hdr->next_duo, 1);
         UnitInfo inf;
         inf.u = u < n_units ? u : -1;
         if (inf.u >= 0) {
