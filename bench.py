@@ -43,7 +43,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # global layer, from one ncu capture (profiles/prefill_tc_modernbert_base_global.md),
 # keyed by the SHA-1 of the kernel source it was taken on: any change to the
 # kernel makes the figure stale, and the bench then reports null.
-MEASURED_TRAFFIC = {"e4aefcd97dc62cd205b4dea1e0062470ed162928": 107149312}
+MEASURED_TRAFFIC = {"0b79eefb679d749be95d267968ad3ff384c288d8": 107548160}
 
 
 def measured_traffic():

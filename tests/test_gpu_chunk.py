@@ -200,3 +200,13 @@ def test_chunk_host_errors(cuda_lib):
     mis = flat[2:2 + qkv.numel() * 2].view(torch.bfloat16).view(qkv.shape)
     with pytest.raises(kime.KimeError):  # misaligned qkv
         kime.kime_kv_append_varlen(mis, cu, pos, 9, 3, kc, vc, c, s)
+
+
+def test_chunk_of_empty_blocks_launches_nothing(cuda_lib):
+    # every sequence has an empty block: no rows, nothing written, no error
+    case = chunk_case(lengths=[0, 0, 0], pos=[5, 0, 63], cap=64, seed=38)
+    dev = torch.device("cuda")
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, kc, vc = gpu_chunk(case, "step", dev_status=st)
+    assert out.shape[0] == 0 and int(st.item()) == 0
+    assert torch.equal(kc.view(torch.int16), case.k_cache.to(dev).view(torch.int16))

@@ -113,3 +113,16 @@ def test_decode_host_argument_errors(cuda_lib):
     with pytest.raises(kime.KimeError):  # heads/kv_heads = 9 > 8
         kime.kime_attn_decode(case.qkv_new.to(dev), case.pos.to(dev), 9, 1, case.k_cache.to(dev),
                               case.v_cache.to(dev), 0.125, c, s)
+
+
+def test_decode_empty_batch_launches_nothing(cuda_lib):
+    dev = torch.device("cuda")
+    case = decode_case(n_seqs=1, cap=64, seed=25, max_pos=10)
+    c, s = gpu_tables(case.theta, case.cap)
+    kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
+    empty_pos = torch.zeros(0, dtype=torch.int32, device=dev)
+    out = kime.kime_decode_step(case.qkv_new.to(dev)[:0], empty_pos, case.heads, case.kv_heads, kc, vc,
+                                case.scale, c, s)
+    torch.cuda.synchronize()
+    assert out.shape[0] == 0
+    assert torch.equal(kc.view(torch.int16), case.k_cache.to(dev).view(torch.int16))
