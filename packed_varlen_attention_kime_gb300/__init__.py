@@ -139,8 +139,10 @@ def kime_attn_varlen(qkv, cu_seqlens, max_seqlen, heads, kv_heads, window, causa
     n_seqs = cu_seqlens.numel() - 1
     if out is None:
         out = torch.empty((T, heads * 64), dtype=out_dtype or qkv.dtype, device=qkv.device)
-    need = kime_attn_workspace_bytes(0, n_seqs, T)
     if workspace is None:
+        # BF16 qkv: room for the prepared key/value rows, which long sequences use
+        op = 3 if qkv.dtype == torch.bfloat16 else 0
+        need = kime_attn_workspace_bytes(op, n_seqs, T, heads, kv_heads)
         workspace = torch.empty(need, dtype=torch.uint8, device=qkv.device)
     rc = lib.kime_attn_varlen(_p(qkv), _dtype_code(qkv, out.dtype), _p(cu_seqlens), n_seqs, T, int(max_seqlen), heads,
                               kv_heads, 64, int(window), int(bool(causal)), float(scale), _p(rope_cos),

@@ -56,7 +56,41 @@ int encode_qkv_map(CUtensorMap* map, const void* qkv, int total, int W) {
   return KIME_OK;
 }
 
+// 2-D map over a RoPE table [rope_len, 32] f32: boxes of 128 rows (the
+// positions of one key tile), 128-byte swizzle, rows past rope_len read as zero.
+int encode_table_map(CUtensorMap* map, const float* table, int rope_len) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return KIME_ECUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kime::kHalf), static_cast<cuuint64_t>(rope_len > 0 ? rope_len : 1)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kime::kHalf) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kime::kHalf), static_cast<cuuint32_t>(kime::kBN)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(table), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_cuda_error = static_cast<int>(r);
+    return KIME_ECUDA;
+  }
+  return KIME_OK;
+}
+
 size_t varlen_ws_bytes(int n_seqs, int total) { return kime::varlen_workspace_bytes(n_seqs, total); }
+
+// Workspace with room for the prepared key/value rows of a packed batch
+// (launch_kv_prep), placed after the scheduler's lists at a 1 KB boundary.
+size_t prep_offset(int n_seqs, int total) { return (varlen_ws_bytes(n_seqs, total) + 1023) & ~static_cast<size_t>(1023); }
+size_t prep_ws_bytes(int n_seqs, int total, int kv_heads) {
+  return prep_offset(n_seqs, total) + static_cast<size_t>(total) * kv_heads * 2 * kime::kHead * 2;
+}
+// Keys are prepared once per call when each key tile would otherwise be
+// rotated by several query units: sequences longer than four query tiles,
+// and a window (if any) wide enough for a key tile to be seen by more than
+// one unit of two query tiles.
+constexpr int kPrepMinSeqlen = 512;
+bool prep_pays(int max_seqlen, int window) {
+  return max_seqlen > kPrepMinSeqlen && (window < 0 || window >= 2 * kime::kBM);
+}
 
 bool heads_ok(int heads, int kv_heads, int head_dim) {
   return head_dim == kime::kHead && heads > 0 && kv_heads > 0 && heads % kv_heads == 0;
@@ -79,6 +113,10 @@ size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads
   if (op == 2) {
     if (total_tokens < 0) return 0;
     return varlen_ws_bytes(n_seqs, total_tokens);
+  }
+  if (op == 3) {
+    if (total_tokens < 0 || !heads_ok(heads, kv_heads, kime::kHead)) return 0;
+    return prep_ws_bytes(n_seqs, total_tokens, kv_heads);
   }
   return 0;
 }
@@ -113,10 +151,21 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
                                                heads, kv_heads, window, causal, scale, rope_cos, rope_sin, out,
                                                out_kind, workspace, max_pairs, dev_status, st));
   }
-  CUtensorMap map;
-  rc = encode_qkv_map(&map, qkv, total_tokens, static_cast<int>(W));
-  if (rc) return rc;
-  return cuda_status(kime::launch_prefill_tc(&map, nullptr, nullptr, n_seqs, total_tokens, heads, kv_heads, 0, window,
+  CUtensorMap map, cmap, smap, pmap;
+  if ((rc = encode_qkv_map(&map, qkv, total_tokens, static_cast<int>(W)))) return rc;
+  const bool prep = prep_pays(max_seqlen, window) && workspace_bytes >= prep_ws_bytes(n_seqs, total_tokens, kv_heads);
+  if (prep) {
+    void* kv = static_cast<char*>(workspace) + prep_offset(n_seqs, total_tokens);
+    if ((rc = encode_qkv_map(&pmap, kv, total_tokens, 2 * kv_heads * kime::kHead))) return rc;
+    if ((rc = cuda_status(kime::launch_kv_prep(qkv, cu_seqlens, n_seqs, total_tokens, heads, kv_heads, rope_cos,
+                                               rope_sin, rope_len, kv, st))))
+      return rc;
+  } else {
+    if ((rc = encode_table_map(&cmap, rope_cos, rope_len))) return rc;
+    if ((rc = encode_table_map(&smap, rope_sin, rope_len))) return rc;
+  }
+  return cuda_status(kime::launch_prefill_tc(&map, nullptr, nullptr, prep ? nullptr : &cmap, prep ? nullptr : &smap,
+                                             prep ? &pmap : nullptr, n_seqs, total_tokens, heads, kv_heads, 0, window,
                                              causal, scale, rope_cos, rope_sin, out, workspace, max_pairs,
                                              dev_status, st));
 }
@@ -167,7 +216,8 @@ int chunk_attend(const void* qkv, const int32_t* cu, const int32_t* pos, int n_s
   if ((rc = encode_qkv_map(&qmap, qkv, total, W))) return rc;
   if ((rc = encode_qkv_map(&kmap, k_cache, rows, kime::kHead))) return rc;
   if ((rc = encode_qkv_map(&vmap, v_cache, rows, kime::kHead))) return rc;
-  return cuda_status(kime::launch_prefill_tc(&qmap, &kmap, &vmap, n_seqs, total, heads, kv_heads, cap, -1, 1, scale,
+  return cuda_status(kime::launch_prefill_tc(&qmap, &kmap, &vmap, nullptr, nullptr, nullptr, n_seqs, total, heads, kv_heads,
+                                             cap, -1, 1, scale,
                                              rope_cos, rope_sin, out, workspace, max_pairs, dev_status, st));
 }
 

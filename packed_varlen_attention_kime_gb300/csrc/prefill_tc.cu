@@ -22,24 +22,30 @@
 //                thread r owns row r of a tile
 //   warpgroup 3  warp 12: TMA producer (Q tiles, 4-stage K/V ring);
 //                warps 13, 14: MMA issuers (one thread each, tcgen05.mma), one
-//                per query tile, so the two tiles' MMAs never wait on each other
-// Registers are rebalanced with setmaxnreg: 160 for the softmax warpgroups,
-// 136 for RoPE, 56 for the producer / MMA warpgroup (sum 512 x 128).
+//                per query tile: S MMAs go out in the ring order (a shared
+//                turn counter), each tile's PV as soon as its P is stored
+// Registers are rebalanced with setmaxnreg: 168 for the softmax warpgroups,
+// 120 for RoPE and 56 for the producer / MMA warpgroup when the kernel
+// rotates the keys, else 112 and 64 (sum 512 x 128 either way).
 // MMA operands are f16 (11-bit significand): q and k are rotated in float32
 // and rounded once to f16 (q times scale*log2(e) first, so S arrives in log2
 // units), V is widened from bf16 exactly, P is rounded to f16.  Inputs must
 // stay inside the f16 range (|value| < 65504; conversions saturate).
-// TMEM (512 columns): S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383,
-// P_A 384..447, P_B 448..511 (f16 P, two per 32-bit column).
-// Per key tile t each tile's issuer issues PV(t) then S(t+1) as soon as its
-// softmax warpgroup has stored P(t), so one warpgroup's softmax overlaps the
-// other's MMAs.  The PV MMAs take P
-// from TMEM (A operand) and V from shared memory, and accumulate O in TMEM.  A
-// softmax warpgroup reads S(t) once, takes P(t) = 2^(S - m_ref) against a
-// reference max that moves only when exceeded by more than 2^8 (then O is
-// rescaled in TMEM), and stores P(t) into TMEM.  Keeping P out of shared
-// memory leaves its bandwidth to the MMA operands Q, K, V.  Every wait is
-// bounded; on a timeout every role winds down.
+// TMEM (512 columns): a ring of three S buffers, 0..127, 128..255, 256..383,
+// shared by both query tiles, then O_A 384..447 and O_B 448..511.  P(t) (f16,
+// two per 32-bit column) overwrites the first 64 columns of the buffer that
+// held S(t).  The S MMAs of a unit take ring buffers in a fixed order, key
+// tile by key tile, tile A before tile B; a buffer is refilled once the PV
+// MMA that read its P has completed.  With three buffers each issuer issues
+// S(t+1) while its softmax warpgroup still works on S(t), so a warpgroup goes
+// from one key tile to the next without waiting for the tensor pipe, and one
+// warpgroup's softmax overlaps the other's MMAs.  The PV MMAs take P from TMEM
+// (A operand) and V from shared memory, and accumulate O in TMEM.  A softmax
+// warpgroup reads S(t) once, takes P(t) = 2^(S - m_ref) against a reference
+// max that moves only when exceeded by more than 2^8 (then O is rescaled in
+// TMEM), and stores P(t) into TMEM.  Keeping P out of shared memory leaves its
+// bandwidth to the MMA operands Q, K, V.  Every wait is bounded; on a timeout
+// every role winds down.
 #include "kime_common.cuh"
 
 #ifdef KIME_PHASE_PROFILE
@@ -52,32 +58,48 @@ namespace kime {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kStages = 4;
+constexpr int kMaxStages = 4;
 constexpr uint32_t kTile = kBM * kHead * 2;  // 16 KB: 128 rows x 128 B
-constexpr uint32_t kOffQ = 0;                // 2 unit slots x 2 tiles
-constexpr uint32_t kOffK = kOffQ + 4 * kTile;
-constexpr uint32_t kOffV = kOffK + kStages * kTile;
-constexpr uint32_t kOffBar = kOffV + kStages * kTile;
-constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
+// Shared memory: Q (2 unit slots x 2 tiles), the K/V ring, and when the
+// kernel rotates the keys itself a ring of RoPE table tiles (cos and sin rows
+// of the 128 key positions of a K tile, 2 x 16 KB): 3 K/V stages + 2 table
+// stages then, else 4 K/V stages.
+template <bool kTab>
+struct Layout {
+  static constexpr int stages = kTab ? 3 : 4;
+  static constexpr int tab_stages = kTab ? 2 : 0;
+  static constexpr uint32_t q = 0;
+  static constexpr uint32_t k = q + 4 * kTile;
+  static constexpr uint32_t v = k + stages * kTile;
+  static constexpr uint32_t tab = v + stages * kTile;
+  static constexpr uint32_t bar = tab + tab_stages * 2 * kTile;
+  static constexpr uint32_t bytes = bar + 512 + 1024;
+  static_assert(bytes <= 232448, "shared memory per CTA");
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLazy = 8.f;  // the reference max moves when exceeded by more (log2 units)
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 struct UnitInfo {
   int32_t u, s, qt0, nt, kb, ke, row0, L, off;
 };
 
+constexpr int kSBufs = 3;  // S buffers in TMEM
+
 struct Shared {
   uint64_t unit_full[2], unit_empty[2];
   uint64_t q_full[2], q_empty[2], qrot[2];
-  uint64_t kv_full[kStages], krot[kStages], kv_empty[kStages];
-  uint64_t s_full[2], p_full[2], pv_full[2];
+  uint64_t kv_full[kMaxStages], krot[kMaxStages], kv_empty[kMaxStages];
+  uint64_t tab_empty[2];  // a table tile has been read (RoPE done with its K tile)
+  uint64_t s_full[2][2];    // per query tile, alternating: S(t) and S(t+1) may both be done
+  uint64_t s_free[kSBufs];  // the PV that read the buffer's P has completed
+  uint64_t p_full[2], pv_full[2];
   uint64_t drain[2];  // wind-down after an abort: each MMA issuer's last commit
   UnitInfo info[2];
   uint32_t tmem_base;
   int32_t abort;
+  int32_t s_turn;  // S MMAs issued so far; the next one in ring order has this index
 };
 static_assert(sizeof(Shared) <= 512, "barrier block");
 
@@ -90,6 +112,35 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
       : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
       : "memory");
   return r != 0;
+}
+
+// Order of a unit's S MMAs in the ring: key tile by key tile, tile A before
+// tile B.  kb[w], n[w]: first visible key tile and count of query tile w.
+struct SOrder {
+  int kb[2], n[2];
+};
+__device__ __forceinline__ SOrder s_order(int L, int qt0, int nt, int off, int causal, int window) {
+  SOrder o;
+  int fb, fe, ke;
+  tile_ranges(L, off + L, off, qt0, causal, window, o.kb[0], ke, fb, fe);
+  o.n[0] = ke - o.kb[0];
+  o.kb[1] = 0;
+  o.n[1] = 0;
+  if (nt > 1) {
+    tile_ranges(L, off + L, off, qt0 + 1, causal, window, o.kb[1], ke, fb, fe);
+    o.n[1] = ke - o.kb[1];
+  }
+  return o;
+}
+// Position within the unit's S order of query tile w's S for key tile t.
+__device__ __forceinline__ int s_rank(const SOrder& o, int w, int t) {
+  return min(max(t + w - o.kb[0], 0), o.n[0]) + min(max(t - o.kb[1], 0), o.n[1]);
+}
+// From tile w's S for key tile t to its S for key tile t + 1: one step, plus
+// one when the other tile's S for key tile t + w (the other tile's key tiles
+// are [okb, oke)) comes between them.
+__device__ __forceinline__ int s_step(int k, int w, int t, int okb, int oke) {
+  return k + 1 + (t + w >= okb && t + w < oke ? 1 : 0);
 }
 
 template <uint32_t N>
@@ -113,10 +164,22 @@ __device__ __forceinline__ void load_table_row(TableRow& t, const float* __restr
   }
 }
 
+// Row r's entries from a table tile in shared memory: the cos (or sin) rows of
+// 128 positions, 128 bytes each, 128-byte swizzled like the operand tiles.
+__device__ __forceinline__ void load_table_row_smem(TableRow& t, const uint8_t* ctile, const uint8_t* stile, int r) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int o = r * 128 + ((k ^ (r & 7)) << 4);
+    t.c[k] = *reinterpret_cast<const float4*>(ctile + o);
+    t.s[k] = *reinterpret_cast<const float4*>(stile + o);
+  }
+}
+
 // Row r of a 128-byte-swizzled [128 x 64] tile (16-byte chunk k of row r sits
 // at chunk k ^ (r & 7)), bf16 on entry, converted in place to the f16 operand
 // the MMAs read.  rope_row: rotate-half RoPE with the row's table entries in
-// float32 (one rounding per operation), times `mul`, rounded once to f16.
+// float32 (y_t = fma(x_t, c, -(x_{t+32} s)), y_{t+32} = fma(x_{t+32}, c,
+// x_t s)), times `mul`, rounded once to f16.
 // convert_row: the bf16 values widened and rounded to f16.  zero_row: zeros
 // (cache rows past a chunk's keys, whose contents are undefined: a NaN there
 // would reach O through a zero probability).
@@ -136,8 +199,16 @@ __device__ __forceinline__ void rope_row(uint8_t* tile, int r, const TableRow& t
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       float a0, a1, b0, b1;
-      rope_pair(bf16lo(aw[e]), bf16lo(bw[e]), cc[2 * e], ss[2 * e], a0, b0);
-      rope_pair(bf16hi(aw[e]), bf16hi(bw[e]), cc[2 * e + 1], ss[2 * e + 1], a1, b1);
+      {
+        const float xa = bf16lo(aw[e]), xb = bf16lo(bw[e]);
+        a0 = __fmaf_rn(xa, cc[2 * e], -__fmul_rn(xb, ss[2 * e]));
+        b0 = __fmaf_rn(xb, cc[2 * e], __fmul_rn(xa, ss[2 * e]));
+      }
+      {
+        const float xa = bf16hi(aw[e]), xb = bf16hi(bw[e]);
+        a1 = __fmaf_rn(xa, cc[2 * e + 1], -__fmul_rn(xb, ss[2 * e + 1]));
+        b1 = __fmaf_rn(xb, cc[2 * e + 1], __fmul_rn(xa, ss[2 * e + 1]));
+      }
       ya[e] = pack_f16x2(a0 * mul, a1 * mul);
       yb[e] = pack_f16x2(b0 * mul, b1 * mul);
     }
@@ -175,13 +246,20 @@ struct Params {
 };
 
 // kCache = false: a packed batch; K and V are heads of the qkv rows, K rotated
-// here.  kCache = true: chunks attending a KV cache that already holds them
+// here, or (kPrep) read from the prepared rows of kv_prep_kernel (keys
+// rotated, keys and values in f16), passed as k_map.  kCache = true: chunks
+// attending a KV cache that already holds them
 // (rotated keys); K and V tiles come from the cache maps, rows past the
 // sequence's keys are zeroed, q rows sit at positions off + i.
-template <bool kCache>
+template <bool kCache, bool kPrep>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qkv_map, const __grid_constant__ CUtensorMap k_map,
-                      const __grid_constant__ CUtensorMap v_map, const Params p) {
+                      const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap cos_map,
+                      const __grid_constant__ CUtensorMap sin_map, const Params p) {
+  constexpr bool kTab = !kCache && !kPrep;  // keys rotated here, tables staged with each K tile
+  using Lay = Layout<kTab>;
+  constexpr int kStages = Lay::stages;
+  constexpr uint32_t kOffQ = Lay::q, kOffK = Lay::k, kOffV = Lay::v, kOffTab = Lay::tab, kOffBar = Lay::bar;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Shared* sh = reinterpret_cast<Shared*>(smem + kOffBar);
@@ -194,6 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kCache) {
       tma_prefetch_map(&k_map);
       tma_prefetch_map(&v_map);
+    } else if (kPrep) {
+      tma_prefetch_map(&k_map);
+    } else {
+      tma_prefetch_map(&cos_map);
+      tma_prefetch_map(&sin_map);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh->unit_full[i], 1);
@@ -201,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh->q_full[i], 1);
       mbar_init(&sh->q_empty[i], 2);     // both MMA issuers
       mbar_init(&sh->qrot[i], 1);
-      mbar_init(&sh->s_full[i], 1);
+      mbar_init(&sh->s_full[i][0], 1);
+      mbar_init(&sh->s_full[i][1], 1);
       mbar_init(&sh->p_full[i], 1);
       mbar_init(&sh->pv_full[i], 1);
       mbar_init(&sh->drain[i], 1);
@@ -211,7 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh->krot[i], 1);
       mbar_init(&sh->kv_empty[i], 2);  // both MMA issuers
     }
+    for (int i = 0; i < kSBufs; ++i) mbar_init(&sh->s_free[i], 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&sh->tab_empty[i], 1);
     sh->abort = 0;
+    sh->s_turn = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -235,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (wg == 3) {
-    regs_dec<56>();
+    regs_dec<kTab ? 56 : 64>();
     if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       griddep_wait();  // the schedule written by the kernel before this one
@@ -276,14 +363,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = c % kStages;
           PHASE(3);
           if (!wait(&sh->kv_empty[st], ((c / kStages) & 1) ^ 1)) { ok = false; break; }
+          if (kTab && !wait(&sh->tab_empty[c & 1], ((c >> 1) & 1) ^ 1)) { ok = false; break; }
           PHASE(2);
-          mbar_arrive_expect_tx(&sh->kv_full[st], 2 * kTile);
-          if (kCache) {
+          mbar_arrive_expect_tx(&sh->kv_full[st], (kTab ? 4 : 2) * kTile);
+          if (kPrep) {  // prepared rows [total, 2 * kv_heads * 64]: keys, then values
+            tma_load_2d(smem + kOffK + st * kTile, &k_map, &sh->kv_full[st], g * kHead, inf.row0 + t * kBN);
+            tma_load_2d(smem + kOffV + st * kTile, &k_map, &sh->kv_full[st], (p.kv_heads + g) * kHead,
+                        inf.row0 + t * kBN);
+          } else if (kCache) {
             tma_load_2d(smem + kOffK + st * kTile, &k_map, &sh->kv_full[st], 0, kvrow + t * kBN);
             tma_load_2d(smem + kOffV + st * kTile, &v_map, &sh->kv_full[st], 0, kvrow + t * kBN);
           } else {
             tma_load_2d(smem + kOffK + st * kTile, &qkv_map, &sh->kv_full[st], kx, inf.row0 + t * kBN);
             tma_load_2d(smem + kOffV + st * kTile, &qkv_map, &sh->kv_full[st], vx, inf.row0 + t * kBN);
+            // the RoPE table rows of key positions t*128 .. t*128 + 127
+            uint8_t* tb = smem + kOffTab + (c & 1) * 2 * kTile;
+            tma_load_2d(tb, &cos_map, &sh->kv_full[st], 0, t * kBN);
+            tma_load_2d(tb + kTile, &sin_map, &sh->kv_full[st], 0, t * kBN);
           }
         }
         if (!ok) break;
@@ -301,10 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if ((warp == 13 || warp == 14) && lane == 0) {
       // ---------------------------------------------------------- MMA issuers
       // one per query tile (warp 13: tile A, warp 14: tile B), so neither
-      // softmax warpgroup's MMAs queue behind the other's
+      // tile's PV MMAs queue behind the other tile's softmax
       const int w = warp - 13;
-      uint32_t n = 0, c = 0, pc = 0;
-      const uint32_t tS = tmem + w * 128, tO = tmem + 256 + w * 64, tP = tmem + 384 + w * 64;
+      uint32_t n = 0, c = 0, pc = 0, sc = 0;  // units, key tiles, P tiles, S MMAs of this tile
+      int sbase = 0;                          // S MMAs of both tiles in earlier units
+      volatile int32_t* turn = &sh->s_turn;
+      const uint32_t tO = tmem + kSBufs * 128 + w * 64;
       PHASE_DECL(8);
       for (;; ++n) {
         const int slot = n & 1;
@@ -313,59 +411,116 @@ __global__ void __launch_bounds__(kThreads, 1)
         PHASE(0);
         const UnitInfo inf = sh->info[slot];
         if (inf.u < 0) break;
-        int kb = 0, ke = 0, fb, fe;  // this tile's range; empty when the unit has no tile B
         const int off = kCache ? inf.off : 0;  // position of the unit's row 0
-        if (w < inf.nt) tile_ranges(inf.L, off + inf.L, off, inf.qt0 + w, kCausal, kWindow, kb, ke, fb, fe);
+        const SOrder o = s_order(inf.L, inf.qt0, inf.nt, off, kCausal, kWindow);
+        // this tile's key tiles (none when the unit has no tile B), and the other tile's
+        // (selected, not indexed: w is not a compile-time constant)
+        const int kb = w ? o.kb[1] : o.kb[0], ke = kb + (w ? o.n[1] : o.n[0]);
+        const int okb = w ? o.kb[0] : o.kb[1], oke = okb + (w ? o.n[0] : o.n[1]);
+        int kS = sbase + s_rank(o, w, kb), kP = kS;  // ring-order indices of the next S and of the next PV's S
+        sbase += o.n[0] + o.n[1];
         const uint32_t aq = smem_u32(smem + kOffQ + slot * 2 * kTile) + w * kTile;
         PHASE(4);
         bool ok = wait(&sh->qrot[slot], (n >> 1) & 1);
         PHASE(1);
-        auto issue_s = [&](int stage) {
+        // S for key tile t, whose K tile is number cc of the ring, may be
+        // issued once its turn in the ring order has come, its K tile is in
+        // and rotated, and the PV that read its buffer's previous P is done.
+        auto s_ready = [&](uint32_t cc) -> bool {
+          const int k = kS;
+          if (*turn != k) return false;
+          __threadfence_block();  // the buffer's earlier uses are seen through the turn
+          const uint32_t ph = (cc / kStages) & 1;
+          if (!mbar_test(&sh->kv_full[cc % kStages], ph) || (!kPrep && !mbar_test(&sh->krot[cc % kStages], ph)))
+            return false;
+          return k < kSBufs || mbar_test(&sh->s_free[k % kSBufs], ((k / kSBufs) - 1) & 1);
+        };
+        auto issue_s = [&](int t, uint32_t cc) {
+          const int k = kS;
+          kS = s_step(kS, w, t, okb, oke);
           tc_fence_after();
-          const uint32_t bk = smem_u32(smem + kOffK + stage * kTile);
+          const uint32_t bk = smem_u32(smem + kOffK + (cc % kStages) * kTile), tS = tmem + (k % kSBufs) * 128;
 #pragma unroll
           for (int ks = 0; ks < kHead / 16; ++ks)
             tc_mma_ss(tS, sdesc_sw128(aq + ks * 32, 16, 1024), sdesc_sw128(bk + ks * 32, 16, 1024), kIdescS, ks > 0);
-          tc_commit(&sh->s_full[w]);
+          tc_commit(&sh->s_full[w][sc & 1]);
+          ++sc;
+          __threadfence_block();
+          *turn = k + 1;
         };
-        auto wait_k = [&](uint32_t cc) {  // K tile number cc of the ring landed and rotated
-          const uint32_t ph = (cc / kStages) & 1;
-          return wait(&sh->kv_full[cc % kStages], ph) && wait(&sh->krot[cc % kStages], ph);
+        auto issue_pv = [&](int t, int st) {
+          const int k = kP;
+          kP = s_step(kP, w, t, okb, oke);
+          tc_fence_after();
+          const uint32_t bv = smem_u32(smem + kOffV + st * kTile), tP = tmem + (k % kSBufs) * 128;
+          const uint32_t acc0 = t > kb ? 1u : 0u;
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks)
+            tc_mma_ts(tO, tP + ks * 8, sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, ks > 0 ? 1u : acc0);
+          tc_commit(&sh->s_free[k % kSBufs]);
+          tc_commit(&sh->pv_full[w]);
+        };
+        // Bounded poll: every condition is tested without blocking, so one
+        // thread can wait for whichever of two events comes first.
+        uint64_t t0 = 0;
+        uint32_t spins = 0;
+        auto timed_out = [&]() -> bool {
+          if (*abort_flag) return true;
+          if ((++spins & 15) != 0) return false;
+          const uint64_t now = globaltimer();
+          if (t0 == 0) t0 = now;
+          if (now - t0 <= kWaitLimitNs) return false;
+          *abort_flag = 1;
+          report(p.dev_status, ST_TIMEOUT);
+          return true;
         };
         // the first S of this tile's range (it may start after the unit's first key tile)
         if (ok && ke > kb) {
+          const uint32_t c0 = c + (kb - inf.kb);
           PHASE(4);
-          ok = wait_k(c + (kb - inf.kb));
+          t0 = 0;
+          while (ok && !s_ready(c0)) {
+            ok = !timed_out();
+            __nanosleep(32);
+          }
           PHASE(2);
-          if (ok) issue_s((c + (kb - inf.kb)) % kStages);
+          if (ok) issue_s(kb, c0);
           PHASE(6);
         }
         for (int t = inf.kb; ok && t < inf.ke; ++t, ++c) {
           const int st = c % kStages;
           if (t >= kb && t < ke) {
-            PHASE(4);
-            if (!(ok = wait(&sh->p_full[w], (pc++) & 1))) break;
-            PHASE(3);
-            tc_fence_after();
-            const uint32_t bv = smem_u32(smem + kOffV + st * kTile);
-            const uint32_t acc0 = t > kb ? 1u : 0u;
-#pragma unroll
-            for (int ks = 0; ks < kBN / 16; ++ks)
-              tc_mma_ts(tO, tP + ks * 8, sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, ks > 0 ? 1u : acc0);
-            tc_commit(&sh->pv_full[w]);
-            PHASE(5);
-            if (t + 1 < ke) {
-              PHASE(4);
-              if (!(ok = wait_k(c + 1))) break;
-              PHASE(2);
-              issue_s((c + 1) % kStages);
-              PHASE(6);
+            // S(t+1) and PV(t), whichever can go first (S first when both can)
+            bool la = t + 1 < ke, pv = true;
+            t0 = 0;
+            while (la || pv) {
+              if (la && s_ready(c + 1)) {
+                PHASE(2);
+                issue_s(t + 1, c + 1);
+                la = false;
+                PHASE(6);
+              } else if (pv && mbar_try_wait_ns(&sh->p_full[w], pc & 1, la ? 64u : 1000u)) {
+                // (suspended while P is pending, briefly when S(t+1) is too,
+                // so the poll takes few issue slots from the other warps)
+                PHASE(3);
+                ++pc;
+                issue_pv(t, st);
+                pv = false;
+                PHASE(5);
+              } else if (timed_out()) {
+                ok = false;
+                break;
+              } else if (!pv) {
+                __nanosleep(32);
+              }
             }
-          } else if (!(ok = wait_k(c))) {
+            if (!ok) break;
+          } else {
             // a key tile this query tile does not see: its release must still
             // follow the fill (and the RoPE pass), or this issuer's arrival
             // could complete the stage's previous phase
-            break;
+            const uint32_t ph = (c / kStages) & 1;
+            if (!(ok = wait(&sh->kv_full[st], ph) && (kPrep || wait(&sh->krot[st], ph)))) break;
           }
           tc_commit(&sh->kv_empty[st]);  // this issuer's MMAs reading stage st are issued
           if (t + 1 == inf.ke) tc_commit(&sh->q_empty[slot]);  // and its last S of the unit
@@ -382,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (wg == 2) {
-    regs_inc<136>();
+    regs_inc<kTab ? 120 : 112>();
     // ------------------------------------------------------------ RoPE
     const int r = tid - 256;  // row of every tile this thread converts
     uint32_t n = 0, c = 0;
@@ -417,10 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sh->unit_empty[slot]);  // every thread has its copy of the unit
       }
       const int Lk = (kCache ? inf.off : 0) + inf.L;  // keys of the unit's sequence
-      for (int t = inf.kb; t < inf.ke; ++t, ++c) {
+      for (int t = inf.kb; !kPrep && t < inf.ke; ++t, ++c) {  // (prepared keys need nothing here)
         const int st = c % kStages, j = t * kBN + r;
-        if (!kCache && j < inf.L)
-          load_table_row(tb, p.cos_t + static_cast<size_t>(j) * kHalf, p.sin_t + static_cast<size_t>(j) * kHalf);
         PHASE(2);
         ok = wait(&sh->kv_full[st], (c / kStages) & 1);
         PHASE(3);
@@ -434,31 +587,37 @@ __global__ void __launch_bounds__(kThreads, 1)
               zero_row(smem + kOffV + st * kTile, r);
             }
           } else {
-            if (j < inf.L)
+            if (j < inf.L) {
+              const uint8_t* tab = smem + kOffTab + (c & 1) * 2 * kTile;  // loaded with this K tile
+              load_table_row_smem(tb, tab, tab + kTile, r);
               rope_row(smem + kOffK + st * kTile, r, tb, 1.f);
-            else
+            } else {
               convert_row(smem + kOffK + st * kTile, r);
+            }
             convert_row(smem + kOffV + st * kTile, r);
           }
           fence_proxy_async_smem();
         }
         PHASE(4);
         if (named_bar_or(3, 128, !ok)) { ok = false; break; }
-        if (r == 0) mbar_arrive(&sh->krot[st]);
+        if (r == 0) {
+          mbar_arrive(&sh->krot[st]);
+          if (kTab) mbar_arrive(&sh->tab_empty[c & 1]);
+        }
         PHASE(5);
       }
       if (!ok) break;
     }
     PHASE_FLUSH(g_kime_phase, 32, r == 0);
   } else {
-    regs_inc<160>();
+    regs_inc<168>();
     // ------------------------------------------------------------ softmax warpgroups
     const int w = wg;                  // 0: tile A, 1: tile B
     const int r = tid & 127;           // row in the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + w * 128 + lane_off, tO = tmem + 256 + w * 64 + lane_off;
-    const uint32_t tP = tmem + 384 + w * 64 + lane_off;
+    const uint32_t tO = tmem + kSBufs * 128 + w * 64 + lane_off;
     uint32_t n = 0, sc = 0, pvc = 0;
+    int sbase = 0;  // S MMAs of both tiles in earlier units, modulo the ring size
     PHASE_DECL(9);
     for (;; ++n) {
       const int slot = n & 1;
@@ -468,12 +627,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_or(1 + w, 128, false);  // every thread has its copy of the unit
       if (r == 0 && inf.u >= 0) mbar_arrive(&sh->unit_empty[slot]);
       if (inf.u < 0) break;
+      const int off = kCache ? inf.off : 0;  // position of the unit's row 0
+      const SOrder o = s_order(inf.L, inf.qt0, inf.nt, off, kCausal, kWindow);
+      // ring buffer of this tile's first S, and the other tile's key tiles
+      int buf = (sbase + s_rank(o, w, w ? o.kb[1] : o.kb[0])) % kSBufs;
+      const int okb = w ? o.kb[0] : o.kb[1], oke = okb + (w ? o.n[0] : o.n[1]);
+      sbase = (sbase + o.n[0] + o.n[1]) % kSBufs;
       if (w >= inf.nt) continue;  // no partner tile in this unit
       const int h = inf.u % p.heads;
       const int qt = inf.qt0 + w, q0 = qt * kBM, i = q0 + r;
       const bool row_ok = i < inf.L;
       int kb, ke, fb, fe;
-      const int off = kCache ? inf.off : 0;  // position of the unit's row 0
       tile_ranges(inf.L, off + inf.L, off, qt, kCausal, kWindow, kb, ke, fb, fe);
       // chunk rows: the last visible key (this row's position), or none for a padding row
       const int chunk_hi = row_ok ? off + i : -1;
@@ -486,9 +650,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = kb; t < ke; ++t) {
         const int k0 = t * kBN;
         PHASE(7);
-        ok = wait(&sh->s_full[w], (sc++) & 1);
+        ok = wait(&sh->s_full[w][sc & 1], (sc >> 1) & 1);
+        ++sc;
         tc_fence_after();
         PHASE(0);
+        // S(t) and then P(t) live in ring buffer buf
+        const uint32_t tS = tmem + buf * 128 + lane_off;
+        buf = s_step(buf, w, t, okb, oke);
+        buf -= buf >= kSBufs ? kSBufs : 0;
         uint32_t v[128];
         tmem_ld128_wait(tS, v);
         PHASE(1);
@@ -529,32 +698,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = mx;
         }
         PHASE(2);
-        // PV of the previous tile must be done before P is overwritten (it read
-        // P) and before O is rescaled (it accumulated into O).
-        if (t > kb) {
-          ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
-          tc_fence_after();
-        }
-        PHASE(3);
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
         // P = 2^(x - m_use) on the MUFU, row sums in four chains.  A masked key
         // (-inf) gives 0.
         float rs2f[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {  // 32 keys -> 16 columns of P at a time
-          uint32_t pw[16];
+        for (int q8 = 0; q8 < 8; ++q8) {  // 16 keys -> 8 columns of P at a time
+          uint32_t pw[8];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int j = q4 * 32 + 2 * e;
+          for (int e = 0; e < 8; ++e) {
+            const int j = q8 * 16 + 2 * e;
             const float p0 = fast_exp2(x[j] - m_use), p1 = fast_exp2(x[j + 1] - m_use);
             rs2f[e & 3] += p0 + p1;
             pw[e] = pack_f16x2(p0, p1);
           }
-          tmem_st16(tP + q4 * 16, pw);  // this row's P: keys 2c, 2c+1 in column c
+          tmem_st8(tS + q8 * 8, pw);  // this row's P: keys 2c, 2c+1 in column c
         }
         const float rowsum = (rs2f[0] + rs2f[1]) + (rs2f[2] + rs2f[3]);
         l = l * alpha + rowsum;
         PHASE(4);
+        // PV of the previous tile must be done before O is rescaled (it
+        // accumulated into O); it read P(t-1) from another buffer.
+        if (t > kb) {
+          ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
+          tc_fence_after();
+        }
+        PHASE(3);
         if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {
           uint32_t ov[64];
           tmem_ld64_wait(tO, ov);
@@ -617,20 +786,25 @@ extern "C" int kime_debug_phase_clear() {
 #endif
 
 cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_map, const CUtensorMap* v_map,
+                              const CUtensorMap* cos_map, const CUtensorMap* sin_map, const CUtensorMap* prep_map,
                               int n_seqs, int total, int heads, int kv_heads, int cap, int window, int causal,
                               float scale, const float* cos_t, const float* sin_t, void* out, void* ws,
                               int max_pairs, int32_t* dev_status, cudaStream_t st) {
   (void)n_seqs; (void)total;
-  const bool cache = k_map != nullptr;
-  static int configured[2][64] = {};
+  // kernel variant: 0 packed (keys rotated here), 1 packed with prepared rows, 2 chunks against the caches
+  const int mode = k_map != nullptr ? 2 : (prep_map != nullptr ? 1 : 0);
+  static int configured[3][64] = {};
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (dev < 64 && !configured[cache][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(cache ? prefill_tc_kernel<true> : prefill_tc_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const uint32_t smem_bytes = mode == 0 ? Layout<true>::bytes : Layout<false>::bytes;
+  const void* fn = mode == 0   ? reinterpret_cast<const void*>(prefill_tc_kernel<false, false>)
+                   : mode == 1 ? reinterpret_cast<const void*>(prefill_tc_kernel<false, true>)
+                               : reinterpret_cast<const void*>(prefill_tc_kernel<true, false>);
+  if (dev < 64 && !configured[mode][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    configured[cache][dev] = 1;
+    configured[mode][dev] = 1;
   }
   Params prm;
   prm.heads = heads;
@@ -646,19 +820,24 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
   prm.duos = ws_duos(ws, max_pairs);
   prm.dev_status = dev_status;
   // launched with programmatic stream serialization: its prologue overlaps the
-  // scheduler, whose lists it waits for (griddep_wait) before reading them
+  // kernel before it (the scheduler), whose lists it waits for (griddep_wait)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cache) return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true>, *qkv_map, *k_map, *v_map, prm);
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false>, *qkv_map, *qkv_map, *qkv_map, prm);
+  if (mode == 2)
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, false>, *qkv_map, *k_map, *v_map, *qkv_map, *qkv_map, prm);
+  if (mode == 1)
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, true>, *qkv_map, *prep_map, *qkv_map, *qkv_map, *qkv_map,
+                              prm);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, false>, *qkv_map, *qkv_map, *qkv_map, *cos_map, *sin_map,
+                            prm);
 }
 
 }  // namespace kime

@@ -1,0 +1,114 @@
+// prep.cu -- keys and values of a packed batch prepared once per call for the
+// tensor-core attention kernel.
+//
+// The attention kernel works on units of two 128-row query tiles of one head;
+// every unit of a sequence reads all of the sequence's key tiles it can see,
+// so inside the kernel each key tile of a long sequence would be rotated
+// again for every unit (ceil(L / 256) times under full attention).  This pass
+// rotates every key once, at its position within its own sequence (rotate-half
+// RoPE with the float32 tables; positions restart at each sequence, kime-cpu
+// 0.0.17 src/kime_cpu/plan.rs, Step::Rope), and rounds it to f16, and widens
+// every value to f16; the attention kernel then loads the prepared rows as
+// they are.  Its arithmetic is the attention kernel's own for a key row: for
+// the pair (t, t + 32), y_t = fma(x_t, c, -(x_{t+32} s)) and
+// y_{t+32} = fma(x_{t+32}, c, x_t s) in float32, each rounded once to f16, so
+// the attention results are the same bits with or without this pass.
+//
+// Output: kv [total, 2 * kv_heads * 64] f16, row j = the keys of kv heads
+// 0 .. kv_heads-1 of qkv row j, then its values.  One warp per row; lane q of
+// the row's key (or value) 16-byte chunks holds 8 elements of head q / 8, and
+// swaps them with lane q ^ 4, which holds the other half of the rotation pairs.
+#include "kime_common.cuh"
+
+namespace kime {
+
+namespace {
+
+constexpr int kPrepWarps = 8;
+
+__global__ void __launch_bounds__(32 * kPrepWarps)
+    kv_prep_kernel(const uint16_t* __restrict__ qkv, const int32_t* __restrict__ cu, int n_seqs, int total,
+                   int heads, int kv_heads, const float* __restrict__ cos_t, const float* __restrict__ sin_t,
+                   int rope_len, uint16_t* __restrict__ kv) {
+  const int j = blockIdx.x * kPrepWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (j >= total) return;
+  // the sequence owning row j: the largest s with cu[s] <= j; its position there
+  int lo = 0, hi = n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu + mid) <= j) lo = mid;
+    else hi = mid - 1;
+  }
+  const int pos = j - __ldg(cu + lo);
+  // a row outside [0, rope_len) belongs to no valid sequence (the scheduler
+  // reports the bad cu_seqlens and skips it): converted without rotation
+  const bool rot = pos >= 0 && pos < rope_len;
+  const size_t W = static_cast<size_t>(kHead) * (heads + 2 * kv_heads);
+  const uint4* src = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(j) * W + static_cast<size_t>(heads) * kHead);
+  uint4* dst = reinterpret_cast<uint4*>(kv + static_cast<size_t>(j) * 2 * kv_heads * kHead);
+  const int nch = kv_heads * (kHead / 8);  // 16-byte chunks of the row's keys (and of its values)
+  const float* crow = cos_t + static_cast<size_t>(rot ? pos : 0) * kHalf;
+  const float* srow = sin_t + static_cast<size_t>(rot ? pos : 0) * kHalf;
+  // keys: every lane takes part in each round (the partner exchange needs the
+  // whole warp); chunks q and q ^ 4 are both in range or both out of it
+  for (int q0 = 0; q0 < nch; q0 += 32) {
+    const int q = q0 + lane;
+    const bool in = q < nch;
+    const uint4 x = in ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+    uint4 y;
+    y.x = __shfl_xor_sync(0xffffffffu, x.x, 4);
+    y.y = __shfl_xor_sync(0xffffffffu, x.y, 4);
+    y.z = __shfl_xor_sync(0xffffffffu, x.z, 4);
+    y.w = __shfl_xor_sync(0xffffffffu, x.w, 4);
+    if (!in) continue;
+    const int a = q & 7;  // chunk within the head: 0..3 low half, 4..7 high half
+    uint4 o;
+    if (rot) {
+      const int t0 = (a & 3) * 8;  // pair index of the chunk's first element
+      const float4 c0 = __ldg(reinterpret_cast<const float4*>(crow + t0));
+      const float4 c1 = __ldg(reinterpret_cast<const float4*>(crow + t0 + 4));
+      const float4 s0 = __ldg(reinterpret_cast<const float4*>(srow + t0));
+      const float4 s1 = __ldg(reinterpret_cast<const float4*>(srow + t0 + 4));
+      const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+      const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+      uint32_t ow[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float x0 = bf16lo(xw[e]), x1 = bf16hi(xw[e]), p0 = bf16lo(yw[e]), p1 = bf16hi(yw[e]);
+        float r0, r1;
+        if (a < 4) {  // y_t = x_t c - x_{t+32} s
+          r0 = __fmaf_rn(x0, cc[2 * e], -__fmul_rn(p0, ss[2 * e]));
+          r1 = __fmaf_rn(x1, cc[2 * e + 1], -__fmul_rn(p1, ss[2 * e + 1]));
+        } else {      // y_{t+32} = x_{t+32} c + x_t s
+          r0 = __fmaf_rn(x0, cc[2 * e], __fmul_rn(p0, ss[2 * e]));
+          r1 = __fmaf_rn(x1, cc[2 * e + 1], __fmul_rn(p1, ss[2 * e + 1]));
+        }
+        ow[e] = pack_f16x2(r0, r1);
+      }
+      o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    } else {
+      o = make_uint4(pack_f16x2(bf16lo(x.x), bf16hi(x.x)), pack_f16x2(bf16lo(x.y), bf16hi(x.y)),
+                     pack_f16x2(bf16lo(x.z), bf16hi(x.z)), pack_f16x2(bf16lo(x.w), bf16hi(x.w)));
+    }
+    dst[q] = o;
+  }
+  // values: widened to f16
+  for (int q = lane; q < nch; q += 32) {
+    const uint4 x = __ldg(src + nch + q);
+    dst[nch + q] = make_uint4(pack_f16x2(bf16lo(x.x), bf16hi(x.x)), pack_f16x2(bf16lo(x.y), bf16hi(x.y)),
+                              pack_f16x2(bf16lo(x.z), bf16hi(x.z)), pack_f16x2(bf16lo(x.w), bf16hi(x.w)));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_prep(const void* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
+                           const float* cos_t, const float* sin_t, int rope_len, void* kv, cudaStream_t st) {
+  const int grid = (total + kPrepWarps - 1) / kPrepWarps;
+  kv_prep_kernel<<<grid, 32 * kPrepWarps, 0, st>>>(static_cast<const uint16_t*>(qkv), cu, n_seqs, total, heads,
+                                                   kv_heads, cos_t, sin_t, rope_len, static_cast<uint16_t*>(kv));
+  return cudaGetLastError();
+}
+
+}  // namespace kime

@@ -203,6 +203,31 @@ def test_workloads_full_size_sampled(cuda_lib, name):
         check_bf16(g.numpy(), ref, f"{name}/{lay.name}")
 
 
+@pytest.mark.parametrize("window,causal", [(-1, False), (-1, True), (600, False)])
+def test_prepared_keys_path_is_bitwise_the_fused_path(cuda_lib, window, causal):
+    # Long sequences take the key-preparation pass when the workspace has room
+    # for its rows (op 3); with the minimal workspace (op 0) the attention
+    # kernel rotates every key tile itself.  Same arithmetic: same bits.
+    lengths, H, Hkv = [1500, 700, 1, 129, 2100], 4, 2
+    dev = torch.device("cuda")
+    qkv_cpu = random_qkv(lengths, H, Hkv, torch.bfloat16, 1.5, seed=31)
+    qkv = qkv_cpu.to(dev)
+    cu = cu_from_lengths(lengths)
+    T, n, mx = qkv.shape[0], len(lengths), max(lengths)
+    assert kime.kime_attn_workspace_bytes(3, n, T, H, Hkv) > kime.kime_attn_workspace_bytes(0, n, T)
+    c, s = gpu_tables(1e4, mx)
+    outs = []
+    for op in (0, 3):
+        ws = torch.empty(kime.kime_attn_workspace_bytes(op, n, T, H, Hkv), dtype=torch.uint8, device=dev)
+        outs.append(kime.kime_attn_varlen(qkv, cu.to(dev), mx, H, Hkv, window, causal, 0.125, c, s, workspace=ws))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    rows, hs = sample_items(cu.numpy(), H, 300, seed=5)
+    ref = run_oracle_varlen(qkv_cpu, cu, H, Hkv, window, causal, 0.125, 1e4, mx, rows=rows, heads=hs)
+    g = outs[1].float().cpu().reshape(T, H, 64)[torch.from_numpy(rows).long(), torch.from_numpy(hs).long()]
+    check_bf16(g.numpy(), ref, f"prepared keys w{window} c{causal}")
+
+
 def test_device_status_flags_bad_cu_and_skips(cuda_lib):
     dev = torch.device("cuda")
     lengths, H = [100, 50, 30], 2
