@@ -25,21 +25,21 @@
 //                per query tile: S MMAs go out in the ring order (a shared
 //                turn counter), each tile's PV as soon as its P is stored
 // Registers are rebalanced with setmaxnreg: 168 for the softmax warpgroups,
-// 120 for RoPE and 56 for the producer / MMA warpgroup when the kernel
-// rotates the keys, else 112 and 64 (sum 512 x 128 either way).
+// 112 for RoPE, 64 for the producer / MMA warpgroup (sum 512 x 128).
 // MMA operands are f16 (11-bit significand): q and k are rotated in float32
 // and rounded once to f16 (q times scale*log2(e) first, so S arrives in log2
 // units), V is widened from bf16 exactly, P is rounded to f16.  Inputs must
 // stay inside the f16 range (|value| < 65504; conversions saturate).
-// TMEM (512 columns): a ring of three S buffers, 0..127, 128..255, 256..383,
-// shared by both query tiles, then O_A 384..447 and O_B 448..511.  P(t) (f16,
-// two per 32-bit column) overwrites the first 64 columns of the buffer that
-// held S(t).  The S MMAs of a unit take ring buffers in a fixed order, key
-// tile by key tile, tile A before tile B; a buffer is refilled once the PV
-// MMA that read its P has completed.  With three buffers each issuer issues
-// S(t+1) while its softmax warpgroup still works on S(t), so a warpgroup goes
-// from one key tile to the next without waiting for the tensor pipe, and one
-// warpgroup's softmax overlaps the other's MMAs.  The PV MMAs take P from TMEM
+// TMEM (512 columns): a ring of two S buffers 0..127 and 128..255 shared by
+// both query tiles, O_A 256..319, O_B 320..383, P_A 384..447, P_B 448..511
+// (f16 P, two per 32-bit column).  The S MMAs of a unit take ring buffers in
+// a fixed order, key tile by key tile, tile A before tile B; a buffer is
+// refilled as soon as the softmax warpgroup has loaded the S it held into
+// registers.  So each issuer issues S(t+1) while its softmax warpgroup still
+// works on S(t), a warpgroup goes from one key tile to the next without
+// waiting for the tensor pipe, and one warpgroup's softmax overlaps the
+// other's MMAs.  P(t) goes to the tile's own P columns once PV(t-1), which
+// read P(t-1), has completed.  The PV MMAs take P from TMEM
 // (A operand) and V from shared memory, and accumulate O in TMEM.  A softmax
 // warpgroup reads S(t) once, takes P(t) = 2^(S - m_ref) against a reference
 // max that moves only when exceeded by more than 2^8 (then O is rescaled in
@@ -85,7 +85,7 @@ struct UnitInfo {
   int32_t u, s, qt0, nt, kb, ke, row0, L, off;
 };
 
-constexpr int kSBufs = 3;  // S buffers in TMEM
+constexpr int kSBufs = 2;  // S buffers in TMEM
 
 struct Shared {
   uint64_t unit_full[2], unit_empty[2];
@@ -93,7 +93,7 @@ struct Shared {
   uint64_t kv_full[kMaxStages], krot[kMaxStages], kv_empty[kMaxStages];
   uint64_t tab_empty[2];  // a table tile has been read (RoPE done with its K tile)
   uint64_t s_full[2][2];    // per query tile, alternating: S(t) and S(t+1) may both be done
-  uint64_t s_free[kSBufs];  // the PV that read the buffer's P has completed
+  uint64_t s_read[kSBufs];  // the softmax warpgroup has loaded the buffer's S (one arrival per warp)
   uint64_t p_full[2], pv_full[2];
   uint64_t drain[2];  // wind-down after an abort: each MMA issuer's last commit
   UnitInfo info[2];
@@ -143,14 +143,23 @@ __device__ __forceinline__ int s_step(int k, int w, int t, int okb, int oke) {
   return k + 1 + (t + w >= okb && t + w < oke ? 1 : 0);
 }
 
+// Per-warpgroup register counts (setmaxnreg).  Every warp starts with the
+// launch count, 65536 / kThreads = 128 (__launch_bounds__(kThreads, 1)); a
+// .dec must not raise it and an .inc must not lower it (either is an illegal
+// instruction), and the counts of the four warpgroups must sum to 4 x 128.
+constexpr uint32_t kLaunchRegs = 65536 / kThreads;
 template <uint32_t N>
 __device__ __forceinline__ void regs_dec() {
+  static_assert(N <= kLaunchRegs && N % 8 == 0 && N >= 24, "setmaxnreg.dec lowers the count");
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() {
+  static_assert(N >= kLaunchRegs && N % 8 == 0 && N <= 256, "setmaxnreg.inc raises the count");
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
+constexpr uint32_t kRegsSoftmax = 168, kRegsRope = 112, kRegsIssue = 64;
+static_assert(2 * kRegsSoftmax + kRegsRope + kRegsIssue == 4 * kLaunchRegs, "register split");
 
 // One row's cos/sin table entries (32 + 32 floats), loaded ahead of use.
 struct TableRow {
@@ -295,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh->krot[i], 1);
       mbar_init(&sh->kv_empty[i], 2);  // both MMA issuers
     }
-    for (int i = 0; i < kSBufs; ++i) mbar_init(&sh->s_free[i], 1);
+    for (int i = 0; i < kSBufs; ++i) mbar_init(&sh->s_read[i], 4);
     for (int i = 0; i < 2; ++i) mbar_init(&sh->tab_empty[i], 1);
     sh->abort = 0;
     sh->s_turn = 0;
@@ -322,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (wg == 3) {
-    regs_dec<kTab ? 56 : 64>();
+    regs_dec<kRegsIssue>();
     if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       griddep_wait();  // the schedule written by the kernel before this one
@@ -402,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t n = 0, c = 0, pc = 0, sc = 0;  // units, key tiles, P tiles, S MMAs of this tile
       int sbase = 0;                          // S MMAs of both tiles in earlier units
       volatile int32_t* turn = &sh->s_turn;
-      const uint32_t tO = tmem + kSBufs * 128 + w * 64;
+      const uint32_t tO = tmem + 256 + w * 64, tP = tmem + 384 + w * 64;
       PHASE_DECL(8);
       for (;; ++n) {
         const int slot = n & 1;
@@ -417,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (selected, not indexed: w is not a compile-time constant)
         const int kb = w ? o.kb[1] : o.kb[0], ke = kb + (w ? o.n[1] : o.n[0]);
         const int okb = w ? o.kb[0] : o.kb[1], oke = okb + (w ? o.n[0] : o.n[1]);
-        int kS = sbase + s_rank(o, w, kb), kP = kS;  // ring-order indices of the next S and of the next PV's S
+        int kS = sbase + s_rank(o, w, kb);  // ring-order index of this tile's next S
         sbase += o.n[0] + o.n[1];
         const uint32_t aq = smem_u32(smem + kOffQ + slot * 2 * kTile) + w * kTile;
         PHASE(4);
@@ -425,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         PHASE(1);
         // S for key tile t, whose K tile is number cc of the ring, may be
         // issued once its turn in the ring order has come, its K tile is in
-        // and rotated, and the PV that read its buffer's previous P is done.
+        // and rotated, and the S its buffer held before has been loaded.
         auto s_ready = [&](uint32_t cc) -> bool {
           const int k = kS;
           if (*turn != k) return false;
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ph = (cc / kStages) & 1;
           if (!mbar_test(&sh->kv_full[cc % kStages], ph) || (!kPrep && !mbar_test(&sh->krot[cc % kStages], ph)))
             return false;
-          return k < kSBufs || mbar_test(&sh->s_free[k % kSBufs], ((k / kSBufs) - 1) & 1);
+          return k < kSBufs || mbar_test(&sh->s_read[k % kSBufs], ((k / kSBufs) - 1) & 1);
         };
         auto issue_s = [&](int t, uint32_t cc) {
           const int k = kS;
@@ -449,15 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           *turn = k + 1;
         };
         auto issue_pv = [&](int t, int st) {
-          const int k = kP;
-          kP = s_step(kP, w, t, okb, oke);
           tc_fence_after();
-          const uint32_t bv = smem_u32(smem + kOffV + st * kTile), tP = tmem + (k % kSBufs) * 128;
+          const uint32_t bv = smem_u32(smem + kOffV + st * kTile);
           const uint32_t acc0 = t > kb ? 1u : 0u;
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks)
             tc_mma_ts(tO, tP + ks * 8, sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, ks > 0 ? 1u : acc0);
-          tc_commit(&sh->s_free[k % kSBufs]);
           tc_commit(&sh->pv_full[w]);
         };
         // Bounded poll: every condition is tested without blocking, so one
@@ -537,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (wg == 2) {
-    regs_inc<kTab ? 120 : 112>();
+    regs_dec<kRegsRope>();
     // ------------------------------------------------------------ RoPE
     const int r = tid - 256;  // row of every tile this thread converts
     uint32_t n = 0, c = 0;
@@ -610,12 +616,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     PHASE_FLUSH(g_kime_phase, 32, r == 0);
   } else {
-    regs_inc<168>();
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax warpgroups
     const int w = wg;                  // 0: tile A, 1: tile B
     const int r = tid & 127;           // row in the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tO = tmem + kSBufs * 128 + w * 64 + lane_off;
+    const uint32_t tO = tmem + 256 + w * 64 + lane_off, tP = tmem + 384 + w * 64 + lane_off;
     uint32_t n = 0, sc = 0, pvc = 0;
     int sbase = 0;  // S MMAs of both tiles in earlier units, modulo the ring size
     PHASE_DECL(9);
@@ -654,12 +660,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++sc;
         tc_fence_after();
         PHASE(0);
-        // S(t) and then P(t) live in ring buffer buf
-        const uint32_t tS = tmem + buf * 128 + lane_off;
+        // S(t) is in ring buffer buf, free again once every warp has loaded it
+        const int bcur = buf;
         buf = s_step(buf, w, t, okb, oke);
         buf -= buf >= kSBufs ? kSBufs : 0;
         uint32_t v[128];
-        tmem_ld128_wait(tS, v);
+        tmem_ld128_wait(tmem + bcur * 128 + lane_off, v);
+        tc_fence_before();
+        if (lane == 0) mbar_arrive(&sh->s_read[bcur]);
         PHASE(1);
         float x[128];
 #pragma unroll
@@ -699,6 +707,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         PHASE(2);
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        // PV(t-1) read P(t-1) from this tile's P columns and accumulated into
+        // O: it completes before P(t) is stored and O is rescaled.
+        if (t > kb) {
+          ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
+          tc_fence_after();
+        }
+        PHASE(3);
         // P = 2^(x - m_use) on the MUFU, row sums in four chains.  A masked key
         // (-inf) gives 0.
         float rs2f[4] = {0.f, 0.f, 0.f, 0.f};
@@ -712,18 +727,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             rs2f[e & 3] += p0 + p1;
             pw[e] = pack_f16x2(p0, p1);
           }
-          tmem_st8(tS + q8 * 8, pw);  // this row's P: keys 2c, 2c+1 in column c
+          tmem_st8(tP + q8 * 8, pw);  // this row's P: keys 2c, 2c+1 in column c
         }
         const float rowsum = (rs2f[0] + rs2f[1]) + (rs2f[2] + rs2f[3]);
         l = l * alpha + rowsum;
         PHASE(4);
-        // PV of the previous tile must be done before O is rescaled (it
-        // accumulated into O); it read P(t-1) from another buffer.
-        if (t > kb) {
-          ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
-          tc_fence_after();
-        }
-        PHASE(3);
         if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {
           uint32_t ov[64];
           tmem_ld64_wait(tO, ov);
