@@ -85,14 +85,14 @@ typedef enum { KIME_F32 = 0, KIME_BF16 = 1, KIME_F32_F16OUT = 2, KIME_F32_BF16OU
  *  workspace    device scratch of at least kime_attn_workspace_bytes(0, ...)
  *               bytes; contents need no initialisation; calls that share it
  *               must be ordered on one stream.  With BF16 qkv and at least
- *               kime_attn_workspace_bytes(3, ...) bytes, batches whose key
- *               tiles are read by several query units (max_seqlen > 512 and
- *               window -1 or >= 256) first rotate every key once into the
- *               workspace (a third launch) instead of once per query unit:
- *               faster, and the same result bits
+ *               kime_attn_workspace_bytes(3, ...) bytes, the qkv rows are
+ *               first prepared into the workspace (a third launch: queries
+ *               and keys rotated once each, queries scaled, all in FP16) and
+ *               the attention kernel does no RoPE work: faster, and the same
+ *               result bits
  * BF16 runs on the tensor cores (tcgen05, FP32 accumulate); FP32 qkv (all
- * three FP32 codes) runs on FP32 FMA.  Launches: the device scheduler, the key
- * preparation when it applies, then the attention kernel. */
+ * three FP32 codes) runs on FP32 FMA.  Launches: the device scheduler, the row
+ * preparation when the workspace has room for it, then the attention kernel. */
 int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int n_seqs, int total_tokens,
                      int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal, float scale,
                      const float* rope_cos, const float* rope_sin, int rope_len, void* out, void* workspace,
@@ -195,9 +195,9 @@ int kime_chunk_step(const void* qkv, const int32_t* cu_seqlens, const int32_t* p
 
 /* Scratch bytes for op 0 (varlen, the minimum: uses n_seqs, total_tokens),
  * op 1 (decode: uses n_seqs, heads, kv_heads, cap), op 2 (chunked prefill:
- * uses n_seqs, total_tokens) or op 3 (varlen with room for the prepared keys
- * and values, total_tokens * kv_heads * 256 bytes more: uses n_seqs,
- * total_tokens, heads, kv_heads).  Returns 0 for an unknown op or malformed
+ * uses n_seqs, total_tokens) or op 3 (varlen with room for the prepared qkv
+ * rows, about total_tokens * 128 * (heads + 2 * kv_heads) bytes more: uses
+ * n_seqs, total_tokens, heads, kv_heads).  Returns 0 for an unknown op or malformed
  * sizes. */
 size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads, int kv_heads, int cap);
 

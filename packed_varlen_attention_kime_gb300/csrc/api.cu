@@ -77,19 +77,12 @@ int encode_table_map(CUtensorMap* map, const float* table, int rope_len) {
 
 size_t varlen_ws_bytes(int n_seqs, int total) { return kime::varlen_workspace_bytes(n_seqs, total); }
 
-// Workspace with room for the prepared key/value rows of a packed batch
-// (launch_kv_prep), placed after the scheduler's lists at a 1 KB boundary.
+// Workspace with room for the prepared qkv rows of a packed batch
+// (launch_qkv_prep, [total, W] f16), placed after the scheduler's lists at a
+// 1 KB boundary.
 size_t prep_offset(int n_seqs, int total) { return (varlen_ws_bytes(n_seqs, total) + 1023) & ~static_cast<size_t>(1023); }
-size_t prep_ws_bytes(int n_seqs, int total, int kv_heads) {
-  return prep_offset(n_seqs, total) + static_cast<size_t>(total) * kv_heads * 2 * kime::kHead * 2;
-}
-// Keys are prepared once per call when each key tile would otherwise be
-// rotated by several query units: sequences longer than four query tiles,
-// and a window (if any) wide enough for a key tile to be seen by more than
-// one unit of two query tiles.
-constexpr int kPrepMinSeqlen = 512;
-bool prep_pays(int max_seqlen, int window) {
-  return max_seqlen > kPrepMinSeqlen && (window < 0 || window >= 2 * kime::kBM);
+size_t prep_ws_bytes(int n_seqs, int total, int heads, int kv_heads) {
+  return prep_offset(n_seqs, total) + static_cast<size_t>(total) * kime::kHead * (heads + 2 * kv_heads) * 2;
 }
 
 bool heads_ok(int heads, int kv_heads, int head_dim) {
@@ -116,7 +109,7 @@ size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads
   }
   if (op == 3) {
     if (total_tokens < 0 || !heads_ok(heads, kv_heads, kime::kHead)) return 0;
-    return prep_ws_bytes(n_seqs, total_tokens, kv_heads);
+    return prep_ws_bytes(n_seqs, total_tokens, heads, kv_heads);
   }
   return 0;
 }
@@ -153,12 +146,14 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
   }
   CUtensorMap map, cmap, smap, pmap;
   if ((rc = encode_qkv_map(&map, qkv, total_tokens, static_cast<int>(W)))) return rc;
-  const bool prep = prep_pays(max_seqlen, window) && workspace_bytes >= prep_ws_bytes(n_seqs, total_tokens, kv_heads);
+  // with room in the workspace, the rows are prepared once (RoPE and f16) and
+  // the attention kernel does no RoPE work
+  const bool prep = workspace_bytes >= prep_ws_bytes(n_seqs, total_tokens, heads, kv_heads);
   if (prep) {
-    void* kv = static_cast<char*>(workspace) + prep_offset(n_seqs, total_tokens);
-    if ((rc = encode_qkv_map(&pmap, kv, total_tokens, 2 * kv_heads * kime::kHead))) return rc;
-    if ((rc = cuda_status(kime::launch_kv_prep(qkv, cu_seqlens, n_seqs, total_tokens, heads, kv_heads, rope_cos,
-                                               rope_sin, rope_len, kv, st))))
+    void* rows = static_cast<char*>(workspace) + prep_offset(n_seqs, total_tokens);
+    if ((rc = encode_qkv_map(&pmap, rows, total_tokens, static_cast<int>(W)))) return rc;
+    if ((rc = cuda_status(kime::launch_qkv_prep(qkv, cu_seqlens, n_seqs, total_tokens, heads, kv_heads, scale,
+                                                rope_cos, rope_sin, rope_len, rows, st))))
       return rc;
   } else {
     if ((rc = encode_table_map(&cmap, rope_cos, rope_len))) return rc;

@@ -89,21 +89,24 @@ cudaError_t launch_varlen_f32(const float* qkv, const int32_t* cu, int n_seqs, i
                               void* out, int out_kind, void* ws, int max_pairs, int32_t* dev_status,
                               cudaStream_t st);
 // k_map / v_map == nullptr: packed sequences.  Then with prep_map (the rows
-// written by launch_kv_prep, [total, 2 * kv_heads * 64] f16) keys and values
-// come from there; without it from the qkv rows, rotated in the kernel with
-// the RoPE tables cos_map / sin_map ([rope_len, 32] f32, boxes of 128 rows).
-// Otherwise keys and values come from caches [n_seqs * kv_heads * cap, 64]
-// (chunks) and the table and prep maps are unused.
+// written by launch_qkv_prep, [total, W] f16 in the qkv layout) everything
+// comes from there and no RoPE is left to do; without it from the qkv rows,
+// with Q and K rotated in the kernel (K with the RoPE tables cos_map /
+// sin_map, [rope_len, 32] f32, boxes of 128 rows).  Otherwise K and V come
+// from caches [n_seqs * kv_heads * cap, 64] (chunks) and the table and prep
+// maps are unused.
 cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_map, const CUtensorMap* v_map,
                               const CUtensorMap* cos_map, const CUtensorMap* sin_map, const CUtensorMap* prep_map,
                               int n_seqs, int total,
                               int heads, int kv_heads, int cap, int window, int causal,
                               float scale, const float* cos_t, const float* sin_t, void* out, void* ws,
                               int max_pairs, int32_t* dev_status, cudaStream_t st);
-// Keys of a packed batch rotated at their positions and rounded to f16,
-// values widened to f16: kv [total, 2 * kv_heads * 64] (prep.cu).
-cudaError_t launch_kv_prep(const void* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
-                           const float* cos_t, const float* sin_t, int rope_len, void* kv, cudaStream_t st);
+// A packed batch's qkv rows prepared for the attention kernel (prep.cu):
+// queries rotated at their positions and scaled by scale * log2(e), keys
+// rotated, all rounded to f16, values widened to f16; out [total, W] f16.
+cudaError_t launch_qkv_prep(const void* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
+                            float scale, const float* cos_t, const float* sin_t, int rope_len, void* out,
+                            cudaStream_t st);
 cudaError_t launch_kv_append_varlen(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total,
                                     int heads, int kv_heads, int cap, const float* cos_t, const float* sin_t,
                                     int rope_len, void* k_cache, void* v_cache, int32_t* dev_status,

@@ -254,10 +254,11 @@ struct Params {
   int32_t* dev_status;
 };
 
-// kCache = false: a packed batch; K and V are heads of the qkv rows, K rotated
-// here, or (kPrep) read from the prepared rows of kv_prep_kernel (keys
-// rotated, keys and values in f16), passed as k_map.  kCache = true: chunks
-// attending a KV cache that already holds them
+// kCache = false: a packed batch; Q, K and V are heads of the qkv rows, Q and
+// K rotated here, or (kPrep) qkv_map holds the rows prepared by
+// qkv_prep_kernel (queries rotated and scaled, keys rotated, all in f16) and
+// no RoPE is left to do.  kCache = true: chunks attending a KV cache that
+// already holds them
 // (rotated keys); K and V tiles come from the cache maps, rows past the
 // sequence's keys are zeroed, q rows sit at positions off + i.
 template <bool kCache, bool kPrep>
@@ -281,9 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kCache) {
       tma_prefetch_map(&k_map);
       tma_prefetch_map(&v_map);
-    } else if (kPrep) {
-      tma_prefetch_map(&k_map);
-    } else {
+    } else if (!kPrep) {
       tma_prefetch_map(&cos_map);
       tma_prefetch_map(&sin_map);
     }
@@ -375,20 +374,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kTab && !wait(&sh->tab_empty[c & 1], ((c >> 1) & 1) ^ 1)) { ok = false; break; }
           PHASE(2);
           mbar_arrive_expect_tx(&sh->kv_full[st], (kTab ? 4 : 2) * kTile);
-          if (kPrep) {  // prepared rows [total, 2 * kv_heads * 64]: keys, then values
-            tma_load_2d(smem + kOffK + st * kTile, &k_map, &sh->kv_full[st], g * kHead, inf.row0 + t * kBN);
-            tma_load_2d(smem + kOffV + st * kTile, &k_map, &sh->kv_full[st], (p.kv_heads + g) * kHead,
-                        inf.row0 + t * kBN);
-          } else if (kCache) {
+          if (kCache) {
             tma_load_2d(smem + kOffK + st * kTile, &k_map, &sh->kv_full[st], 0, kvrow + t * kBN);
             tma_load_2d(smem + kOffV + st * kTile, &v_map, &sh->kv_full[st], 0, kvrow + t * kBN);
           } else {
             tma_load_2d(smem + kOffK + st * kTile, &qkv_map, &sh->kv_full[st], kx, inf.row0 + t * kBN);
             tma_load_2d(smem + kOffV + st * kTile, &qkv_map, &sh->kv_full[st], vx, inf.row0 + t * kBN);
-            // the RoPE table rows of key positions t*128 .. t*128 + 127
-            uint8_t* tb = smem + kOffTab + (c & 1) * 2 * kTile;
-            tma_load_2d(tb, &cos_map, &sh->kv_full[st], 0, t * kBN);
-            tma_load_2d(tb + kTile, &sin_map, &sh->kv_full[st], 0, t * kBN);
+            if (kTab) {  // the RoPE table rows of key positions t*128 .. t*128 + 127
+              uint8_t* tb = smem + kOffTab + (c & 1) * 2 * kTile;
+              tma_load_2d(tb, &cos_map, &sh->kv_full[st], 0, t * kBN);
+              tma_load_2d(tb + kTile, &sin_map, &sh->kv_full[st], 0, t * kBN);
+            }
           }
         }
         if (!ok) break;
@@ -555,10 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       PHASE(0);
       const UnitInfo inf = sh->info[slot];
       if (inf.u < 0) break;
-      // the unit's query tiles: row r of each, at positions q0 + r
+      // the unit's query tiles: row r of each, at positions q0 + r (prepared
+      // rows are rotated and scaled already: only their arrival is waited for)
       uint8_t* q = smem + kOffQ + slot * 2 * kTile;
       TableRow tb;
-      for (int w = 0; w < inf.nt; ++w) {
+      if (kPrep) ok = wait(&sh->q_full[slot], (n >> 1) & 1);
+      for (int w = 0; !kPrep && w < inf.nt; ++w) {
         const int i = (inf.qt0 + w) * kBM + r;
         const size_t ti = static_cast<size_t>((kCache ? inf.off : 0) + i) * kHalf;  // table row of position off + i
         if (i < inf.L) load_table_row(tb, p.cos_t + ti, p.sin_t + ti);
@@ -714,19 +712,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
         }
         PHASE(3);
-        // P = 2^(x - m_use) on the MUFU, row sums in four chains.  A masked key
-        // (-inf) gives 0.
+        // P = 2^(x - m_use): the differences in float32 pairs, rounded to f16
+        // pairs, two exponentials per MUFU operation (P in f16, as the MMA
+        // takes it); row sums in f16 over 16 keys, then float32.  A masked
+        // key (-inf) gives 0.
         float rs2f[4] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t mm;
+        asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(m_use));
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) {  // 16 keys -> 8 columns of P at a time
           uint32_t pw[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int j = q8 * 16 + 2 * e;
-            const float p0 = fast_exp2(x[j] - m_use), p1 = fast_exp2(x[j + 1] - m_use);
-            rs2f[e & 3] += p0 + p1;
-            pw[e] = pack_f16x2(p0, p1);
+            uint64_t xx, d;
+            asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "f"(x[j]), "f"(x[j + 1]));
+            asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(xx), "l"(mm));
+            uint32_t h;
+            asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.f16x2.f32 %0, hi, lo;\n\t}" : "=r"(h) : "l"(d));
+            asm("ex2.approx.f16x2 %0, %1;" : "=r"(pw[e]) : "r"(h));
           }
+          uint32_t a0, a1, a2, a3, b0, b1, c0;
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a0) : "r"(pw[0]), "r"(pw[1]));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a1) : "r"(pw[2]), "r"(pw[3]));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a2) : "r"(pw[4]), "r"(pw[5]));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a3) : "r"(pw[6]), "r"(pw[7]));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(b0) : "r"(a0), "r"(a1));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(b1) : "r"(a2), "r"(a3));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(c0) : "r"(b0), "r"(b1));
+          float lo, hi;
+          asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}" : "=f"(lo), "=f"(hi) : "r"(c0));
+          rs2f[q8 & 3] += lo + hi;
           tmem_st8(tP + q8 * 8, pw);  // this row's P: keys 2c, 2c+1 in column c
         }
         const float rowsum = (rs2f[0] + rs2f[1]) + (rs2f[2] + rs2f[3]);
@@ -842,8 +858,8 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
   if (mode == 2)
     return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, false>, *qkv_map, *k_map, *v_map, *qkv_map, *qkv_map, prm);
   if (mode == 1)
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, true>, *qkv_map, *prep_map, *qkv_map, *qkv_map, *qkv_map,
-                              prm);
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, true>, *prep_map, *prep_map, *prep_map, *prep_map,
+                              *prep_map, prm);
   return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, false>, *qkv_map, *qkv_map, *qkv_map, *cos_map, *sin_map,
                             prm);
 }

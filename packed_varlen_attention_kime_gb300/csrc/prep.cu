@@ -1,35 +1,37 @@
-// prep.cu -- keys and values of a packed batch prepared once per call for the
+// prep.cu -- a packed batch's qkv rows prepared once per call for the
 // tensor-core attention kernel.
 //
 // The attention kernel works on units of two 128-row query tiles of one head;
 // every unit of a sequence reads all of the sequence's key tiles it can see,
 // so inside the kernel each key tile of a long sequence would be rotated
-// again for every unit (ceil(L / 256) times under full attention).  This pass
-// rotates every key once, at its position within its own sequence (rotate-half
-// RoPE with the float32 tables; positions restart at each sequence, kime-cpu
-// 0.0.17 src/kime_cpu/plan.rs, Step::Rope), and rounds it to f16, and widens
-// every value to f16; the attention kernel then loads the prepared rows as
-// they are.  Its arithmetic is the attention kernel's own for a key row: for
-// the pair (t, t + 32), y_t = fma(x_t, c, -(x_{t+32} s)) and
-// y_{t+32} = fma(x_{t+32}, c, x_t s) in float32, each rounded once to f16, so
-// the attention results are the same bits with or without this pass.
+// again for every unit (ceil(L / 256) times under full attention), and the
+// RoPE work on the kernel's own warps is what limits short sequences.  This
+// pass rotates every query and key once, at its position within its own
+// sequence (rotate-half RoPE with the float32 tables; positions restart at
+// each sequence, kime-cpu 0.0.17 src/kime_cpu/plan.rs, Step::Rope), scales
+// the queries by scale * log2(e), rounds both to f16, and widens every value
+// to f16; the attention kernel then loads the prepared rows as they are.  Its
+// arithmetic is the attention kernel's own: for the pair (t, t + 32),
+// y_t = fma(x_t, c, -(x_{t+32} s)) and y_{t+32} = fma(x_{t+32}, c, x_t s) in
+// float32, times the query multiplier for query heads, each rounded once to
+// f16, so the attention results are the same bits with or without this pass.
 //
-// Output: kv [total, 2 * kv_heads * 64] f16, row j = the keys of kv heads
-// 0 .. kv_heads-1 of qkv row j, then its values.  One warp per row; lane q of
-// the row's key (or value) 16-byte chunks holds 8 elements of head q / 8, and
-// swaps them with lane q ^ 4, which holds the other half of the rotation pairs.
+// Output: rows [total, W] f16 in the qkv layout (W = 64 * (heads + 2 *
+// kv_heads)).  One warp per row; lane q of a round holds the 16-byte chunk q
+// of the row (8 elements of head q / 8) and swaps it with lane q ^ 4, which
+// holds the other half of the rotation pairs.
 #include "kime_common.cuh"
 
 namespace kime {
 
 namespace {
 
-constexpr int kPrepWarps = 8;
+constexpr int kPrepWarps = 8;  // rows per CTA
 
 __global__ void __launch_bounds__(32 * kPrepWarps)
-    kv_prep_kernel(const uint16_t* __restrict__ qkv, const int32_t* __restrict__ cu, int n_seqs, int total,
-                   int heads, int kv_heads, const float* __restrict__ cos_t, const float* __restrict__ sin_t,
-                   int rope_len, uint16_t* __restrict__ kv) {
+    qkv_prep_kernel(const uint16_t* __restrict__ qkv, const int32_t* __restrict__ cu, int n_seqs, int total,
+                    int heads, int kv_heads, float qmul, const float* __restrict__ cos_t,
+                    const float* __restrict__ sin_t, int rope_len, uint16_t* __restrict__ out) {
   const int j = blockIdx.x * kPrepWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (j >= total) return;
   // the sequence owning row j: the largest s with cu[s] <= j; its position there
@@ -44,16 +46,18 @@ __global__ void __launch_bounds__(32 * kPrepWarps)
   // reports the bad cu_seqlens and skips it): converted without rotation
   const bool rot = pos >= 0 && pos < rope_len;
   const size_t W = static_cast<size_t>(kHead) * (heads + 2 * kv_heads);
-  const uint4* src = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(j) * W + static_cast<size_t>(heads) * kHead);
-  uint4* dst = reinterpret_cast<uint4*>(kv + static_cast<size_t>(j) * 2 * kv_heads * kHead);
-  const int nch = kv_heads * (kHead / 8);  // 16-byte chunks of the row's keys (and of its values)
+  const uint4* src = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(j) * W);
+  uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(j) * W);
+  const int nrot = (heads + kv_heads) * (kHead / 8);  // 16-byte chunks of the row's queries and keys
+  const int nall = (heads + 2 * kv_heads) * (kHead / 8);
   const float* crow = cos_t + static_cast<size_t>(rot ? pos : 0) * kHalf;
   const float* srow = sin_t + static_cast<size_t>(rot ? pos : 0) * kHalf;
-  // keys: every lane takes part in each round (the partner exchange needs the
-  // whole warp); chunks q and q ^ 4 are both in range or both out of it
-  for (int q0 = 0; q0 < nch; q0 += 32) {
+  // queries and keys: every lane takes part in each round (the partner
+  // exchange needs the whole warp); chunks q and q ^ 4 are both in range or
+  // both out of it
+  for (int q0 = 0; q0 < nrot; q0 += 32) {
     const int q = q0 + lane;
-    const bool in = q < nch;
+    const bool in = q < nrot;
     const uint4 x = in ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
     uint4 y;
     y.x = __shfl_xor_sync(0xffffffffu, x.x, 4);
@@ -61,7 +65,8 @@ __global__ void __launch_bounds__(32 * kPrepWarps)
     y.z = __shfl_xor_sync(0xffffffffu, x.z, 4);
     y.w = __shfl_xor_sync(0xffffffffu, x.w, 4);
     if (!in) continue;
-    const int a = q & 7;  // chunk within the head: 0..3 low half, 4..7 high half
+    const int a = q & 7;                                 // chunk within the head: 0..3 low half, 4..7 high half
+    const float mul = (q >> 3) < heads ? qmul : 1.f;     // query heads carry scale * log2(e)
     uint4 o;
     if (rot) {
       const int t0 = (a & 3) * 8;  // pair index of the chunk's first element
@@ -84,30 +89,32 @@ __global__ void __launch_bounds__(32 * kPrepWarps)
           r0 = __fmaf_rn(x0, cc[2 * e], __fmul_rn(p0, ss[2 * e]));
           r1 = __fmaf_rn(x1, cc[2 * e + 1], __fmul_rn(p1, ss[2 * e + 1]));
         }
-        ow[e] = pack_f16x2(r0, r1);
+        ow[e] = pack_f16x2(r0 * mul, r1 * mul);
       }
       o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-    } else {
+    } else {  // a row of no valid sequence: converted only
       o = make_uint4(pack_f16x2(bf16lo(x.x), bf16hi(x.x)), pack_f16x2(bf16lo(x.y), bf16hi(x.y)),
                      pack_f16x2(bf16lo(x.z), bf16hi(x.z)), pack_f16x2(bf16lo(x.w), bf16hi(x.w)));
     }
     dst[q] = o;
   }
   // values: widened to f16
-  for (int q = lane; q < nch; q += 32) {
-    const uint4 x = __ldg(src + nch + q);
-    dst[nch + q] = make_uint4(pack_f16x2(bf16lo(x.x), bf16hi(x.x)), pack_f16x2(bf16lo(x.y), bf16hi(x.y)),
-                              pack_f16x2(bf16lo(x.z), bf16hi(x.z)), pack_f16x2(bf16lo(x.w), bf16hi(x.w)));
+  for (int q = nrot + lane; q < nall; q += 32) {
+    const uint4 x = __ldg(src + q);
+    dst[q] = make_uint4(pack_f16x2(bf16lo(x.x), bf16hi(x.x)), pack_f16x2(bf16lo(x.y), bf16hi(x.y)),
+                        pack_f16x2(bf16lo(x.z), bf16hi(x.z)), pack_f16x2(bf16lo(x.w), bf16hi(x.w)));
   }
 }
 
 }  // namespace
 
-cudaError_t launch_kv_prep(const void* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
-                           const float* cos_t, const float* sin_t, int rope_len, void* kv, cudaStream_t st) {
+cudaError_t launch_qkv_prep(const void* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
+                            float scale, const float* cos_t, const float* sin_t, int rope_len, void* out,
+                            cudaStream_t st) {
   const int grid = (total + kPrepWarps - 1) / kPrepWarps;
-  kv_prep_kernel<<<grid, 32 * kPrepWarps, 0, st>>>(static_cast<const uint16_t*>(qkv), cu, n_seqs, total, heads,
-                                                   kv_heads, cos_t, sin_t, rope_len, static_cast<uint16_t*>(kv));
+  qkv_prep_kernel<<<grid, 32 * kPrepWarps, 0, st>>>(static_cast<const uint16_t*>(qkv), cu, n_seqs, total, heads,
+                                                    kv_heads, scale * 1.4426950408889634f, cos_t, sin_t, rope_len,
+                                                    static_cast<uint16_t*>(out));
   return cudaGetLastError();
 }
 

@@ -203,12 +203,22 @@ def test_workloads_full_size_sampled(cuda_lib, name):
         check_bf16(g.numpy(), ref, f"{name}/{lay.name}")
 
 
-@pytest.mark.parametrize("window,causal", [(-1, False), (-1, True), (600, False)])
-def test_prepared_keys_path_is_bitwise_the_fused_path(cuda_lib, window, causal):
-    # Long sequences take the key-preparation pass when the workspace has room
-    # for its rows (op 3); with the minimal workspace (op 0) the attention
-    # kernel rotates every key tile itself.  Same arithmetic: same bits.
-    lengths, H, Hkv = [1500, 700, 1, 129, 2100], 4, 2
+PREP_CASES = [
+    ([1500, 700, 1, 129, 2100], 4, 2, -1, False),
+    ([1500, 700, 1, 129, 2100], 4, 2, -1, True),
+    ([1500, 700, 1, 129, 2100], 4, 2, 600, False),
+    ([1, 2, 63, 64, 65, 127, 128, 129, 255, 300, 0, 513], 3, 1, 64, False),
+    ([1, 2, 63, 64, 65, 127, 128, 129, 255, 300, 0, 513], 3, 3, 0, False),
+    ([1, 2, 63, 64, 65, 127, 128, 129, 255, 300, 0, 513], 6, 2, -1, True),
+]
+
+
+@pytest.mark.parametrize("lengths,H,Hkv,window,causal", PREP_CASES)
+def test_prepared_rows_path_is_bitwise_the_fused_path(cuda_lib, lengths, H, Hkv, window, causal):
+    # With a workspace of op 3 size the qkv rows are prepared once (RoPE, the
+    # query scale, f16) and the attention kernel does no RoPE; with the minimal
+    # workspace (op 0) the kernel rotates queries and key tiles itself.  Same
+    # arithmetic: same bits.
     dev = torch.device("cuda")
     qkv_cpu = random_qkv(lengths, H, Hkv, torch.bfloat16, 1.5, seed=31)
     qkv = qkv_cpu.to(dev)
@@ -225,7 +235,7 @@ def test_prepared_keys_path_is_bitwise_the_fused_path(cuda_lib, window, causal):
     rows, hs = sample_items(cu.numpy(), H, 300, seed=5)
     ref = run_oracle_varlen(qkv_cpu, cu, H, Hkv, window, causal, 0.125, 1e4, mx, rows=rows, heads=hs)
     g = outs[1].float().cpu().reshape(T, H, 64)[torch.from_numpy(rows).long(), torch.from_numpy(hs).long()]
-    check_bf16(g.numpy(), ref, f"prepared keys w{window} c{causal}")
+    check_bf16(g.numpy(), ref, f"prepared rows {lengths} w{window} c{causal}")
 
 
 def test_device_status_flags_bad_cu_and_skips(cuda_lib):
