@@ -25,7 +25,8 @@
 //                per query tile: S MMAs go out in the ring order (a shared
 //                turn counter), each tile's PV as soon as its P is stored
 // Registers are rebalanced with setmaxnreg: 168 for the softmax warpgroups,
-// 112 for RoPE, 64 for the producer / MMA warpgroup (sum 512 x 128).
+// 112 for RoPE, 64 for the producer / MMA warpgroup (96 and 80 with prepared
+// rows; sum 512 x 128).
 // MMA operands are f16 (11-bit significand): q and k are rotated in float32
 // and rounded once to f16 (q times scale*log2(e) first, so S arrives in log2
 // units), V is widened from bf16 exactly, P is rounded to f16.  Inputs must
@@ -51,6 +52,12 @@
 #ifdef KIME_PHASE_PROFILE
 constexpr int kPhaseSlots = 96;  // role bases 0, 16, 32, 40, 48, 56; at most 12 phases each
 __device__ unsigned long long g_kime_phase[kPhaseSlots];
+// per CTA (globaltimer): entry, first unit claimed, last claim (none left), exit; units taken
+__device__ unsigned long long g_kime_span[5 * 256];
+#define SPAN(k, v) \
+  if (blockIdx.x < 256) g_kime_span[5 * blockIdx.x + (k)] = (v)
+#else
+#define SPAN(k, v)
 #endif
 
 namespace kime {
@@ -73,7 +80,8 @@ struct Layout {
   static constexpr uint32_t v = k + stages * kTile;
   static constexpr uint32_t tab = v + stages * kTile;
   static constexpr uint32_t bar = tab + tab_stages * 2 * kTile;
-  static constexpr uint32_t bytes = bar + 512 + 1024;
+  static constexpr uint32_t lrow = bar + 512;  // [2][128] f32: each tile's row sums for the epilogue warpgroup
+  static constexpr uint32_t bytes = lrow + 1024 + 1024;
   static_assert(bytes <= 232448, "shared memory per CTA");
 };
 constexpr uint32_t kTmemCols = 512;
@@ -95,6 +103,7 @@ struct Shared {
   uint64_t s_full[2][2];    // per query tile, alternating: S(t) and S(t+1) may both be done
   uint64_t s_read[kSBufs];  // the softmax warpgroup has loaded the buffer's S (one arrival per warp)
   uint64_t p_full[2], pv_full[2];
+  uint64_t epi_full[2], o_free[2];  // prepared rows: the tile's O is final / has been read out
   uint64_t drain[2];  // wind-down after an abort: each MMA issuer's last commit
   UnitInfo info[2];
   uint32_t tmem_base;
@@ -158,8 +167,15 @@ __device__ __forceinline__ void regs_inc() {
   static_assert(N >= kLaunchRegs && N % 8 == 0 && N <= 256, "setmaxnreg.inc raises the count");
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
-constexpr uint32_t kRegsSoftmax = 168, kRegsRope = 112, kRegsIssue = 64;
-static_assert(2 * kRegsSoftmax + kRegsRope + kRegsIssue == 4 * kLaunchRegs, "register split");
+// softmax warpgroups 168; RoPE / epilogue warpgroup and producer / MMA
+// warpgroup 112 and 64, or with prepared rows (no RoPE, more bookkeeping in
+// the MMA issuers) 96 and 80
+constexpr uint32_t kRegsSoftmax = 168;
+template <bool kPrep>
+struct RegSplit {
+  static constexpr uint32_t rope = kPrep ? 96 : 112, issue = kPrep ? 80 : 64;
+  static_assert(2 * kRegsSoftmax + rope + issue == 4 * kLaunchRegs, "register split");
+};
 
 // One row's cos/sin table entries (32 + 32 floats), loaded ahead of use.
 struct TableRow {
@@ -275,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Shared* sh = reinterpret_cast<Shared*>(smem + kOffBar);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
   const int G = p.heads / p.kv_heads;
+  if (tid == 0) SPAN(0, globaltimer());
   const int kCausal = kCache ? 1 : p.causal, kWindow = kCache ? -1 : p.window;  // chunks: causal, no window
 
   if (tid == 0) {
@@ -295,6 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh->s_full[i][0], 1);
       mbar_init(&sh->s_full[i][1], 1);
       mbar_init(&sh->p_full[i], 1);
+      mbar_init(&sh->epi_full[i], 4);  // one arrival per warp
+      mbar_init(&sh->o_free[i], 4);
       mbar_init(&sh->pv_full[i], 1);
       mbar_init(&sh->drain[i], 1);
     }
@@ -330,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (wg == 3) {
-    regs_dec<kRegsIssue>();
+    regs_dec<RegSplit<kPrep>::issue>();
     if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       griddep_wait();  // the schedule written by the kernel before this one
@@ -344,6 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         PHASE(0);
         // claimed only once its slot is free, so no unit waits behind a busy CTA
         const int u = atomicAdd(&p.hdr->next_duo, 1);
+        if (n == 0) SPAN(1, globaltimer());
+        if (u >= n_units) {
+          SPAN(2, globaltimer());
+          SPAN(4, n);
+        }
         UnitInfo inf;
         inf.u = u < n_units ? u : -1;
         if (inf.u >= 0) {
@@ -405,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile's PV MMAs queue behind the other tile's softmax
       const int w = warp - 13;
       uint32_t n = 0, c = 0, pc = 0, sc = 0;  // units, key tiles, P tiles, S MMAs of this tile
+      uint32_t ou = 0;  // units in which this tile's O was accumulated (read out by the epilogue warpgroup)
       int sbase = 0;                          // S MMAs of both tiles in earlier units
       volatile int32_t* turn = &sh->s_turn;
       const uint32_t tO = tmem + 256 + w * 64, tP = tmem + 384 + w * 64;
@@ -504,6 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else if (pv && mbar_try_wait_ns(&sh->p_full[w], pc & 1, la ? 64u : 1000u)) {
                 // (suspended while P is pending, briefly when S(t+1) is too,
                 // so the poll takes few issue slots from the other warps)
+                // prepared rows: the unit's first PV overwrites O, which the
+                // epilogue warpgroup must have read out for the unit before
+                if (kPrep && t == kb && ou > 0 && !wait(&sh->o_free[w], (ou - 1) & 1)) {
+                  ok = false;
+                  break;
+                }
                 PHASE(3);
                 ++pc;
                 issue_pv(t, st);
@@ -529,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           PHASE(7);
         }
         if (!ok) break;
+        if (ke > kb) ++ou;
         mbar_arrive(&sh->unit_empty[slot]);
       }
       if (*abort_flag) {  // every MMA this thread issued completes before TMEM is freed
@@ -539,10 +571,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (wg == 2) {
-    regs_dec<kRegsRope>();
+    regs_dec<RegSplit<kPrep>::rope>();
     // ------------------------------------------------------------ RoPE
     const int r = tid - 256;  // row of every tile this thread converts
     uint32_t n = 0, c = 0;
+    // prepared rows: this warpgroup has no RoPE work and writes the output
+    // rows instead, one unit behind the softmax warpgroups
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t ne0 = 0, ne1 = 0;  // epilogues done for tile A / tile B
+    UnitInfo prev;
+    prev.u = -1;
+    auto epilogue = [&](const UnitInfo& e) -> bool {
+      bool eok = true;
+      if (e.u < 0) return eok;
+      const int h = e.u % p.heads;
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        if (w >= e.nt) break;
+        const uint32_t cnt = w ? ne1 : ne0;
+        eok = eok && wait(&sh->epi_full[w], cnt & 1);
+        if (w) ++ne1;
+        else ++ne0;
+        tc_fence_after();
+        uint32_t ov[64];
+        tmem_ld64_wait(tmem + 256 + w * 64 + lane_off, ov);
+        const float lv = reinterpret_cast<const float*>(smem + Lay::lrow)[w * kBM + r];
+        tc_fence_before();
+        __syncwarp();
+        if (eok && lane == 0) mbar_arrive(&sh->o_free[w]);
+        const int i = (e.qt0 + w) * kBM + r;
+        if (eok && i < e.L) {
+          const float inv = 1.f / lv;
+          __nv_bfloat16* dst = p.out + static_cast<size_t>(e.row0 + i) * p.heads * kHead + h * kHead;
+#pragma unroll
+          for (int d = 0; d < kHead; d += 8) {
+            uint4 wv;
+            wv.x = pack_bf16x2(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv);
+            wv.y = pack_bf16x2(__uint_as_float(ov[d + 2]) * inv, __uint_as_float(ov[d + 3]) * inv);
+            wv.z = pack_bf16x2(__uint_as_float(ov[d + 4]) * inv, __uint_as_float(ov[d + 5]) * inv);
+            wv.w = pack_bf16x2(__uint_as_float(ov[d + 6]) * inv, __uint_as_float(ov[d + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + d) = wv;
+          }
+        }
+      }
+      return eok;
+    };
     PHASE_DECL(6);
     for (;; ++n) {
       const int slot = n & 1;
@@ -550,7 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (named_bar_or(3, 128, !ok)) break;
       PHASE(0);
       const UnitInfo inf = sh->info[slot];
-      if (inf.u < 0) break;
+      if (inf.u < 0) {
+        if (kPrep) epilogue(prev);
+        break;
+      }
       // the unit's query tiles: row r of each, at positions q0 + r (prepared
       // rows are rotated and scaled already: only their arrival is waited for)
       uint8_t* q = smem + kOffQ + slot * 2 * kTile;
@@ -576,6 +652,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sh->unit_empty[slot]);  // every thread has its copy of the unit
       }
       const int Lk = (kCache ? inf.off : 0) + inf.L;  // keys of the unit's sequence
+      if (kPrep) {
+        ok = epilogue(prev);
+        prev = inf;
+        if (named_bar_or(3, 128, !ok)) break;
+      }
       for (int t = inf.kb; !kPrep && t < inf.ke; ++t, ++c) {  // (prepared keys need nothing here)
         const int st = c % kStages, j = t * kBN + r;
         PHASE(2);
@@ -764,6 +845,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       ok = wait(&sh->pv_full[w], (pvc++) & 1);
+      if (kPrep) {
+        // prepared rows: the epilogue warpgroup reads O out and writes the
+        // rows; this warpgroup goes on to the next unit
+        reinterpret_cast<float*>(smem + Lay::lrow)[w * kBM + r] = l;
+        tc_fence_before();
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(&sh->epi_full[w]);
+        if (named_bar_or(1 + w, 128, !ok)) break;
+        PHASE(8);
+        continue;
+      }
       tc_fence_after();
       uint32_t ov[64];
       tmem_ld64_wait(tO, ov);
@@ -795,6 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (tid == 0) SPAN(3, globaltimer());
 }
 
 }  // namespace
@@ -802,6 +895,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #ifdef KIME_PHASE_PROFILE
 extern "C" int kime_debug_phase_read(unsigned long long* host) {
   return cudaMemcpyFromSymbol(host, g_kime_phase, sizeof(g_kime_phase));
+}
+extern "C" int kime_debug_span_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_kime_span, sizeof(g_kime_span));
 }
 extern "C" int kime_debug_phase_clear() {
   unsigned long long z[kPhaseSlots] = {0};

@@ -33,7 +33,10 @@ __global__ void __launch_bounds__(32 * kPrepWarps)
                     int heads, int kv_heads, float qmul, const float* __restrict__ cos_t,
                     const float* __restrict__ sin_t, int rope_len, uint16_t* __restrict__ out) {
   const int j = blockIdx.x * kPrepWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (j >= total) return;
+  if (j >= total) {
+    griddep_wait();
+    return;
+  }
   // the sequence owning row j: the largest s with cu[s] <= j; its position there
   int lo = 0, hi = n_seqs - 1;
   while (lo < hi) {
@@ -104,6 +107,10 @@ __global__ void __launch_bounds__(32 * kPrepWarps)
     dst[q] = make_uint4(pack_f16x2(bf16lo(x.x), bf16hi(x.x)), pack_f16x2(bf16lo(x.y), bf16hi(x.y)),
                         pack_f16x2(bf16lo(x.z), bf16hi(x.z)), pack_f16x2(bf16lo(x.w), bf16hi(x.w)));
   }
+  // this pass runs beside the scheduler (it reads none of its output); it
+  // ends only after the scheduler has, so the attention kernel, which waits
+  // for this pass, also finds the scheduler's lists complete
+  griddep_wait();
 }
 
 }  // namespace
@@ -111,11 +118,20 @@ __global__ void __launch_bounds__(32 * kPrepWarps)
 cudaError_t launch_qkv_prep(const void* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
                             float scale, const float* cos_t, const float* sin_t, int rope_len, void* out,
                             cudaStream_t st) {
-  const int grid = (total + kPrepWarps - 1) / kPrepWarps;
-  qkv_prep_kernel<<<grid, 32 * kPrepWarps, 0, st>>>(static_cast<const uint16_t*>(qkv), cu, n_seqs, total, heads,
-                                                    kv_heads, scale * 1.4426950408889634f, cos_t, sin_t, rope_len,
-                                                    static_cast<uint16_t*>(out));
-  return cudaGetLastError();
+  // launched with programmatic stream serialization: it starts while the
+  // scheduler (which lets dependents start at once) still runs
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((total + kPrepWarps - 1) / kPrepWarps);
+  cfg.blockDim = dim3(32 * kPrepWarps);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, qkv_prep_kernel, static_cast<const uint16_t*>(qkv), cu, n_seqs, total, heads,
+                            kv_heads, scale * 1.4426950408889634f, cos_t, sin_t, rope_len,
+                            static_cast<uint16_t*>(out));
 }
 
 }  // namespace kime
