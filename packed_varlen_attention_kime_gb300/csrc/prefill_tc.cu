@@ -22,8 +22,7 @@
 //                thread r owns row r of a tile
 //   warpgroup 3  warp 12: TMA producer (Q tiles, 4-stage K/V ring);
 //                warps 13, 14: MMA issuers (one thread each, tcgen05.mma), one
-//                per query tile: S MMAs go out in the ring order (a shared
-//                turn counter), each tile's PV as soon as its P is stored
+//                per query tile, so neither tile's MMAs wait on the other's
 // Registers are rebalanced with setmaxnreg: 168 for the softmax warpgroups,
 // 112 for RoPE, 64 for the producer / MMA warpgroup (96 and 80 with prepared
 // rows; sum 512 x 128).
@@ -31,16 +30,14 @@
 // and rounded once to f16 (q times scale*log2(e) first, so S arrives in log2
 // units), V is widened from bf16 exactly, P is rounded to f16.  Inputs must
 // stay inside the f16 range (|value| < 65504; conversions saturate).
-// TMEM (512 columns): a ring of two S buffers 0..127 and 128..255 shared by
-// both query tiles, O_A 256..319, O_B 320..383, P_A 384..447, P_B 448..511
-// (f16 P, two per 32-bit column).  The S MMAs of a unit take ring buffers in
-// a fixed order, key tile by key tile, tile A before tile B; a buffer is
-// refilled as soon as the softmax warpgroup has loaded the S it held into
-// registers.  So each issuer issues S(t+1) while its softmax warpgroup still
-// works on S(t), a warpgroup goes from one key tile to the next without
-// waiting for the tensor pipe, and one warpgroup's softmax overlaps the
-// other's MMAs.  P(t) goes to the tile's own P columns once PV(t-1), which
-// read P(t-1), has completed.  The PV MMAs take P from TMEM
+// TMEM (512 columns): S_A 0..127, S_B 128..255, O_A 256..319, O_B 320..383,
+// P_A 384..447, P_B 448..511 (f16 P, two per 32-bit column).  A tile's S
+// buffer is refilled as soon as its softmax warpgroup has loaded S(t) into
+// registers, so the issuer issues S(t+1) while the warpgroup still works on
+// S(t): a warpgroup goes from one key tile to the next without waiting for
+// the tensor pipe, and one warpgroup's softmax overlaps the other's MMAs.
+// P(t) goes to the tile's own P columns once PV(t-1), which read P(t-1), has
+// completed.  The PV MMAs take P from TMEM
 // (A operand) and V from shared memory, and accumulate O in TMEM.  A softmax
 // warpgroup reads S(t) once, takes P(t) = 2^(S - m_ref) against a reference
 // max that moves only when exceeded by more than 2^8 (then O is rescaled in
@@ -56,8 +53,22 @@ __device__ unsigned long long g_kime_phase[kPhaseSlots];
 __device__ unsigned long long g_kime_span[5 * 256];
 #define SPAN(k, v) \
   if (blockIdx.x < 256) g_kime_span[5 * blockIdx.x + (k)] = (v)
+// event timeline of the first CTAs: globaltimer and tag (role << 24 | code << 16 | argument)
+constexpr int kEvCtas = 4, kEvMax = 1024;
+__device__ unsigned long long g_kime_ev_t[kEvCtas * kEvMax];
+__device__ unsigned int g_kime_ev_tag[kEvCtas * kEvMax];
+__device__ int g_kime_ev_n[kEvCtas];
+#define EV(role, code, arg)                                                          \
+  if (blockIdx.x < kEvCtas) {                                                        \
+    const int i_ = atomicAdd(&g_kime_ev_n[blockIdx.x], 1);                           \
+    if (i_ < kEvMax) {                                                               \
+      g_kime_ev_t[blockIdx.x * kEvMax + i_] = globaltimer();                         \
+      g_kime_ev_tag[blockIdx.x * kEvMax + i_] = ((role) << 24) | ((code) << 16) | ((arg) & 0xffff); \
+    }                                                                                \
+  }
 #else
 #define SPAN(k, v)
+#define EV(role, code, arg)
 #endif
 
 namespace kime {
@@ -93,7 +104,6 @@ struct UnitInfo {
   int32_t u, s, qt0, nt, kb, ke, row0, L, off;
 };
 
-constexpr int kSBufs = 2;  // S buffers in TMEM
 
 struct Shared {
   uint64_t unit_full[2], unit_empty[2];
@@ -101,14 +111,13 @@ struct Shared {
   uint64_t kv_full[kMaxStages], krot[kMaxStages], kv_empty[kMaxStages];
   uint64_t tab_empty[2];  // a table tile has been read (RoPE done with its K tile)
   uint64_t s_full[2][2];    // per query tile, alternating: S(t) and S(t+1) may both be done
-  uint64_t s_read[kSBufs];  // the softmax warpgroup has loaded the buffer's S (one arrival per warp)
+  uint64_t s_read[2];  // the softmax warpgroup has loaded its tile's S (one arrival per warp)
   uint64_t p_full[2], pv_full[2];
   uint64_t epi_full[2], o_free[2];  // prepared rows: the tile's O is final / has been read out
   uint64_t drain[2];  // wind-down after an abort: each MMA issuer's last commit
   UnitInfo info[2];
   uint32_t tmem_base;
   int32_t abort;
-  int32_t s_turn;  // S MMAs issued so far; the next one in ring order has this index
 };
 static_assert(sizeof(Shared) <= 512, "barrier block");
 
@@ -121,35 +130,6 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
       : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
       : "memory");
   return r != 0;
-}
-
-// Order of a unit's S MMAs in the ring: key tile by key tile, tile A before
-// tile B.  kb[w], n[w]: first visible key tile and count of query tile w.
-struct SOrder {
-  int kb[2], n[2];
-};
-__device__ __forceinline__ SOrder s_order(int L, int qt0, int nt, int off, int causal, int window) {
-  SOrder o;
-  int fb, fe, ke;
-  tile_ranges(L, off + L, off, qt0, causal, window, o.kb[0], ke, fb, fe);
-  o.n[0] = ke - o.kb[0];
-  o.kb[1] = 0;
-  o.n[1] = 0;
-  if (nt > 1) {
-    tile_ranges(L, off + L, off, qt0 + 1, causal, window, o.kb[1], ke, fb, fe);
-    o.n[1] = ke - o.kb[1];
-  }
-  return o;
-}
-// Position within the unit's S order of query tile w's S for key tile t.
-__device__ __forceinline__ int s_rank(const SOrder& o, int w, int t) {
-  return min(max(t + w - o.kb[0], 0), o.n[0]) + min(max(t - o.kb[1], 0), o.n[1]);
-}
-// From tile w's S for key tile t to its S for key tile t + 1: one step, plus
-// one when the other tile's S for key tile t + w (the other tile's key tiles
-// are [okb, oke)) comes between them.
-__device__ __forceinline__ int s_step(int k, int w, int t, int okb, int oke) {
-  return k + 1 + (t + w >= okb && t + w < oke ? 1 : 0);
 }
 
 // Per-warpgroup register counts (setmaxnreg).  Every warp starts with the
@@ -322,10 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh->krot[i], 1);
       mbar_init(&sh->kv_empty[i], 2);  // both MMA issuers
     }
-    for (int i = 0; i < kSBufs; ++i) mbar_init(&sh->s_read[i], 4);
+    for (int i = 0; i < 2; ++i) mbar_init(&sh->s_read[i], 4);
     for (int i = 0; i < 2; ++i) mbar_init(&sh->tab_empty[i], 1);
     sh->abort = 0;
-    sh->s_turn = 0;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -363,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         PHASE(0);
         // claimed only once its slot is free, so no unit waits behind a busy CTA
         const int u = atomicAdd(&p.hdr->next_duo, 1);
+        EV(0, 0, n);
         if (n == 0) SPAN(1, globaltimer());
         if (u >= n_units) {
           SPAN(2, globaltimer());
@@ -387,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(q, &qkv_map, &sh->q_full[slot], h * kHead, inf.row0 + inf.qt0 * kBM);
         if (inf.nt == 2)
           tma_load_2d(q + kTile, &qkv_map, &sh->q_full[slot], h * kHead, inf.row0 + (inf.qt0 + 1) * kBM);
+        EV(0, 1, n);
         ++nq;
         const int kx = (p.heads + g) * kHead, vx = (p.heads + p.kv_heads + g) * kHead;
         const int kvrow = (inf.s * p.kv_heads + g) * p.cap;  // cache row of key 0
@@ -397,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait(&sh->kv_empty[st], ((c / kStages) & 1) ^ 1)) { ok = false; break; }
           if (kTab && !wait(&sh->tab_empty[c & 1], ((c >> 1) & 1) ^ 1)) { ok = false; break; }
           PHASE(2);
+          EV(0, 2, c);
           mbar_arrive_expect_tx(&sh->kv_full[st], (kTab ? 4 : 2) * kTile);
           if (kCache) {
             tma_load_2d(smem + kOffK + st * kTile, &k_map, &sh->kv_full[st], 0, kvrow + t * kBN);
@@ -430,9 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w = warp - 13;
       uint32_t n = 0, c = 0, pc = 0, sc = 0;  // units, key tiles, P tiles, S MMAs of this tile
       uint32_t ou = 0;  // units in which this tile's O was accumulated (read out by the epilogue warpgroup)
-      int sbase = 0;                          // S MMAs of both tiles in earlier units
-      volatile int32_t* turn = &sh->s_turn;
-      const uint32_t tO = tmem + 256 + w * 64, tP = tmem + 384 + w * 64;
+      const uint32_t tS = tmem + w * 128, tO = tmem + 256 + w * 64, tP = tmem + 384 + w * 64;
       PHASE_DECL(8);
       for (;; ++n) {
         const int slot = n & 1;
@@ -442,41 +422,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const UnitInfo inf = sh->info[slot];
         if (inf.u < 0) break;
         const int off = kCache ? inf.off : 0;  // position of the unit's row 0
-        const SOrder o = s_order(inf.L, inf.qt0, inf.nt, off, kCausal, kWindow);
-        // this tile's key tiles (none when the unit has no tile B), and the other tile's
-        // (selected, not indexed: w is not a compile-time constant)
-        const int kb = w ? o.kb[1] : o.kb[0], ke = kb + (w ? o.n[1] : o.n[0]);
-        const int okb = w ? o.kb[0] : o.kb[1], oke = okb + (w ? o.n[0] : o.n[1]);
-        int kS = sbase + s_rank(o, w, kb);  // ring-order index of this tile's next S
-        sbase += o.n[0] + o.n[1];
+        int kb = 0, ke = 0, fb, fe;  // this tile's key tiles; none when the unit has no tile B
+        if (w < inf.nt) tile_ranges(inf.L, off + inf.L, off, inf.qt0 + w, kCausal, kWindow, kb, ke, fb, fe);
         const uint32_t aq = smem_u32(smem + kOffQ + slot * 2 * kTile) + w * kTile;
         PHASE(4);
         bool ok = wait(&sh->qrot[slot], (n >> 1) & 1);
         PHASE(1);
-        // S for key tile t, whose K tile is number cc of the ring, may be
-        // issued once its turn in the ring order has come, its K tile is in
-        // and rotated, and the S its buffer held before has been loaded.
+        // S for the key tile that is number cc of the K/V ring may be issued
+        // once that tile is in (and rotated) and the softmax warpgroup has
+        // loaded the S before it out of the tile's S buffer
         auto s_ready = [&](uint32_t cc) -> bool {
-          const int k = kS;
-          if (*turn != k) return false;
-          __threadfence_block();  // the buffer's earlier uses are seen through the turn
           const uint32_t ph = (cc / kStages) & 1;
           if (!mbar_test(&sh->kv_full[cc % kStages], ph) || (!kPrep && !mbar_test(&sh->krot[cc % kStages], ph)))
             return false;
-          return k < kSBufs || mbar_test(&sh->s_read[k % kSBufs], ((k / kSBufs) - 1) & 1);
+          return sc == 0 || mbar_test(&sh->s_read[w], (sc - 1) & 1);
         };
         auto issue_s = [&](int t, uint32_t cc) {
-          const int k = kS;
-          kS = s_step(kS, w, t, okb, oke);
           tc_fence_after();
-          const uint32_t bk = smem_u32(smem + kOffK + (cc % kStages) * kTile), tS = tmem + (k % kSBufs) * 128;
+          const uint32_t bk = smem_u32(smem + kOffK + (cc % kStages) * kTile);
 #pragma unroll
           for (int ks = 0; ks < kHead / 16; ++ks)
             tc_mma_ss(tS, sdesc_sw128(aq + ks * 32, 16, 1024), sdesc_sw128(bk + ks * 32, 16, 1024), kIdescS, ks > 0);
           tc_commit(&sh->s_full[w][sc & 1]);
+          EV(1 + w, 0, t);
           ++sc;
-          __threadfence_block();
-          *turn = k + 1;
         };
         auto issue_pv = [&](int t, int st) {
           tc_fence_after();
@@ -486,8 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < kBN / 16; ++ks)
             tc_mma_ts(tO, tP + ks * 8, sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, ks > 0 ? 1u : acc0);
           tc_commit(&sh->pv_full[w]);
+          EV(1 + w, 1, t);
         };
-        // Bounded poll: every condition is tested without blocking, so one
+        // Bounded poll: the conditions are tested without blocking, so one
         // thread can wait for whichever of two events comes first.
         uint64_t t0 = 0;
         uint32_t spins = 0;
@@ -506,10 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t c0 = c + (kb - inf.kb);
           PHASE(4);
           t0 = 0;
-          while (ok && !s_ready(c0)) {
-            ok = !timed_out();
-            __nanosleep(32);
-          }
+          while (ok && !s_ready(c0)) ok = !timed_out();
           PHASE(2);
           if (ok) issue_s(kb, c0);
           PHASE(6);
@@ -526,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issue_s(t + 1, c + 1);
                 la = false;
                 PHASE(6);
-              } else if (pv && mbar_try_wait_ns(&sh->p_full[w], pc & 1, la ? 64u : 1000u)) {
+              } else if (pv && mbar_try_wait_ns(&sh->p_full[w], pc & 1, la ? 32u : 1000u)) {
                 // (suspended while P is pending, briefly when S(t+1) is too,
                 // so the poll takes few issue slots from the other warps)
                 // prepared rows: the unit's first PV overwrites O, which the
@@ -543,8 +510,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else if (timed_out()) {
                 ok = false;
                 break;
-              } else if (!pv) {
-                __nanosleep(32);
               }
             }
             if (!ok) break;
@@ -590,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w >= e.nt) break;
         const uint32_t cnt = w ? ne1 : ne0;
         eok = eok && wait(&sh->epi_full[w], cnt & 1);
+        if (r == 0) EV(5, 0, w);
         if (w) ++ne1;
         else ++ne0;
         tc_fence_after();
@@ -599,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (eok && lane == 0) mbar_arrive(&sh->o_free[w]);
+        if (r == 0) EV(5, 1, w);
         const int i = (e.qt0 + w) * kBM + r;
         if (eok && i < e.L) {
           const float inv = 1.f / lv;
@@ -702,7 +669,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tO = tmem + 256 + w * 64 + lane_off, tP = tmem + 384 + w * 64 + lane_off;
     uint32_t n = 0, sc = 0, pvc = 0;
-    int sbase = 0;  // S MMAs of both tiles in earlier units, modulo the ring size
     PHASE_DECL(9);
     for (;; ++n) {
       const int slot = n & 1;
@@ -713,11 +679,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (r == 0 && inf.u >= 0) mbar_arrive(&sh->unit_empty[slot]);
       if (inf.u < 0) break;
       const int off = kCache ? inf.off : 0;  // position of the unit's row 0
-      const SOrder o = s_order(inf.L, inf.qt0, inf.nt, off, kCausal, kWindow);
-      // ring buffer of this tile's first S, and the other tile's key tiles
-      int buf = (sbase + s_rank(o, w, w ? o.kb[1] : o.kb[0])) % kSBufs;
-      const int okb = w ? o.kb[0] : o.kb[1], oke = okb + (w ? o.n[0] : o.n[1]);
-      sbase = (sbase + o.n[0] + o.n[1]) % kSBufs;
       if (w >= inf.nt) continue;  // no partner tile in this unit
       const int h = inf.u % p.heads;
       const int qt = inf.qt0 + w, q0 = qt * kBM, i = q0 + r;
@@ -736,17 +697,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int k0 = t * kBN;
         PHASE(7);
         ok = wait(&sh->s_full[w][sc & 1], (sc >> 1) & 1);
+        if (r == 0) EV(3 + w, 0, t);
         ++sc;
         tc_fence_after();
         PHASE(0);
-        // S(t) is in ring buffer buf, free again once every warp has loaded it
-        const int bcur = buf;
-        buf = s_step(buf, w, t, okb, oke);
-        buf -= buf >= kSBufs ? kSBufs : 0;
+        // the tile's S buffer is free again once every warp has loaded S(t)
         uint32_t v[128];
-        tmem_ld128_wait(tmem + bcur * 128 + lane_off, v);
+        tmem_ld128_wait(tmem + w * 128 + lane_off, v);
         tc_fence_before();
-        if (lane == 0) mbar_arrive(&sh->s_read[bcur]);
+        if (lane == 0) mbar_arrive(&sh->s_read[w]);
         PHASE(1);
         float x[128];
 #pragma unroll
@@ -841,6 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         if (named_bar_or(1 + w, 128, !ok)) { ok = false; break; }
         if (r == 0) mbar_arrive(&sh->p_full[w]);
+        if (r == 0) EV(3 + w, 1, t);
         PHASE(6);
       }
       if (!ok) break;
@@ -852,6 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (ok && lane == 0) mbar_arrive(&sh->epi_full[w]);
+        if (r == 0) EV(3 + w, 2, n);
         if (named_bar_or(1 + w, 128, !ok)) break;
         PHASE(8);
         continue;
@@ -895,6 +856,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #ifdef KIME_PHASE_PROFILE
 extern "C" int kime_debug_phase_read(unsigned long long* host) {
   return cudaMemcpyFromSymbol(host, g_kime_phase, sizeof(g_kime_phase));
+}
+extern "C" int kime_debug_ev_read(unsigned long long* t, unsigned int* tag, int* n) {
+  int rc = cudaMemcpyFromSymbol(t, g_kime_ev_t, sizeof(g_kime_ev_t));
+  if (!rc) rc = cudaMemcpyFromSymbol(tag, g_kime_ev_tag, sizeof(g_kime_ev_tag));
+  if (!rc) rc = cudaMemcpyFromSymbol(n, g_kime_ev_n, sizeof(g_kime_ev_n));
+  return rc;
+}
+extern "C" int kime_debug_ev_clear() {
+  int z[kEvCtas] = {0};
+  return cudaMemcpyToSymbol(g_kime_ev_n, z, sizeof(z));
 }
 extern "C" int kime_debug_span_read(unsigned long long* host) {
   return cudaMemcpyFromSymbol(host, g_kime_span, sizeof(g_kime_span));
