@@ -19,7 +19,9 @@
 //   warpgroup 1  softmax for query tile B
 //   warpgroup 2  RoPE: rotates the unit's Q tiles (double-buffered per unit)
 //                and every K tile in shared memory, converts each V tile;
-//                thread r owns row r of a tile
+//                thread r owns row r of a tile.  On prepared rows there is no
+//                RoPE work and it writes the output rows instead, one unit
+//                behind the softmax warpgroups
 //   warpgroup 3  warp 12: TMA producer (Q tiles, 4-stage K/V ring);
 //                warps 13, 14: MMA issuers (one thread each, tcgen05.mma), one
 //                per query tile, so neither tile's MMAs wait on the other's

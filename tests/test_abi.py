@@ -51,3 +51,17 @@ def test_package_does_not_import_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
                 assert "kime_oracle" not in src, f
+
+
+def test_workspace_sizes_are_host_arithmetic(lib):
+    # host-only entry point (no GPU): op 3 is op 0 at a 1 KB boundary plus the
+    # prepared rows [total, 64 * (heads + 2 * kv_heads)] f16; malformed sizes give 0
+    for n, T, H, Hkv in [(1, 1, 1, 1), (64, 20249, 12, 12), (16, 18272, 9, 3), (8, 38690, 16, 16)]:
+        op0 = kime.kime_attn_workspace_bytes(0, n, T)
+        op3 = kime.kime_attn_workspace_bytes(3, n, T, H, Hkv)
+        assert op0 > 0 and op3 == ((op0 + 1023) // 1024) * 1024 + T * 64 * (H + 2 * Hkv) * 2
+        assert kime.kime_attn_workspace_bytes(2, n, T) == op0
+    assert kime.kime_attn_workspace_bytes(3, 4, 100, 6, 4) == 0  # heads not a multiple of kv_heads
+    assert kime.kime_attn_workspace_bytes(0, -1, 10) == 0
+    assert kime.kime_attn_workspace_bytes(9, 4, 100) == 0
+    assert kime.kime_attn_workspace_bytes(1, 128, 0, 9, 3, 8192) > 0
