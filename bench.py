@@ -39,11 +39,12 @@ sys.path.insert(0, ROOT)
 METRIC = ("packed-varlen attention tokens/s & TFLOP/s (% BF16 peak); decode GB/s (% HBM) at 1 GB300")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) of one attention launch of the ModernBERT-base
-# global layer, from one ncu capture (profiles/prefill_tc_modernbert_base_global.md),
-# keyed by the SHA-1 of the kernel source it was taken on: any change to the
-# kernel makes the figure stale, and the bench then reports null.
-MEASURED_TRAFFIC = {"0b79eefb679d749be95d267968ad3ff384c288d8": 107548160}
+# DRAM bytes (read + write) of one attention-kernel launch (prefill_tc_kernel
+# on prepared rows) of the ModernBERT-base global layer, from one ncu capture
+# (profiles/prefill_tc_modernbert_base_global.md), keyed by the SHA-1 of the
+# kernel source it was taken on: any change to the kernel makes the figure
+# stale, and the bench then reports null.
+MEASURED_TRAFFIC = {"9d91c9ade721c75e644c37a78ca9f81a36c588eb": 105965056}
 
 
 def measured_traffic():
@@ -424,7 +425,7 @@ def main():
             "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": measured_traffic(),
             "kernel": "kime_attn_varlen, ModernBERT-base global layer: schedule_kernel + qkv_prep_kernel + "
                       "prefill_tc_kernel (shares in profiles/launches_modernbert_base_layer_pair.md); avg_ms is "
-                      "the whole call",
+                      "the whole call, traffic the attention kernel's DRAM bytes",
             "algorithmic_bytes": g_bytes, "avg_ms": round(g_ms, 5), "peak_source": pk_src}
     flops_step = sum(run.flops)
     tflops = flops_step / (ms_step * 1e-3) / 1e12
