@@ -197,8 +197,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(a, parity)) return true;
+    // suspended for up to ~1 us per try (woken as soon as the phase completes),
+    // so a waiting warp takes almost no issue slots from the warps at work
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait_ns(bar, parity, 1000)) return true;
     if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
 }
