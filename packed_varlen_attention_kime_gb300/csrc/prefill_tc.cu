@@ -55,22 +55,27 @@ __device__ unsigned long long g_kime_phase[kPhaseSlots];
 __device__ unsigned long long g_kime_span[5 * 256];
 #define SPAN(k, v) \
   if (blockIdx.x < 256) g_kime_span[5 * blockIdx.x + (k)] = (v)
-// event timeline of the first CTAs: globaltimer and tag (role << 24 | code << 16 | argument)
-constexpr int kEvCtas = 4, kEvMax = 1024;
-__device__ unsigned long long g_kime_ev_t[kEvCtas * kEvMax];
-__device__ unsigned int g_kime_ev_tag[kEvCtas * kEvMax];
-__device__ int g_kime_ev_n[kEvCtas];
-#define EV(role, code, arg)                                                          \
-  if (blockIdx.x < kEvCtas) {                                                        \
-    const int i_ = atomicAdd(&g_kime_ev_n[blockIdx.x], 1);                           \
-    if (i_ < kEvMax) {                                                               \
-      g_kime_ev_t[blockIdx.x * kEvMax + i_] = globaltimer();                         \
-      g_kime_ev_tag[blockIdx.x * kEvMax + i_] = ((role) << 24) | ((code) << 16) | ((arg) & 0xffff); \
-    }                                                                                \
+// event timeline of the first CTAs: per logging thread (one per role) its own
+// slice of globaltimer stamps and tags (code << 16 | argument), plain stores
+constexpr int kEvCtas = 4, kEvRoles = 6, kEvMax = 512;
+__device__ unsigned long long g_kime_ev_t[kEvCtas * kEvRoles * kEvMax];
+__device__ unsigned int g_kime_ev_tag[kEvCtas * kEvRoles * kEvMax];
+__device__ int g_kime_ev_n[kEvCtas * kEvRoles];
+#define EV(role, code, arg)                                                                   \
+  if (blockIdx.x < kEvCtas) {                                                                 \
+    const int base_ = (blockIdx.x * kEvRoles + (role)) * kEvMax;                              \
+    if (ev_n < kEvMax) {                                                                      \
+      g_kime_ev_t[base_ + ev_n] = globaltimer();                                              \
+      g_kime_ev_tag[base_ + ev_n] = ((code) << 16) | ((arg) & 0xffff);                        \
+    }                                                                                         \
+    ++ev_n;                                                                                   \
+    g_kime_ev_n[blockIdx.x * kEvRoles + (role)] = ev_n;                                       \
   }
+#define EV_DECL int ev_n = 0
 #else
 #define SPAN(k, v)
 #define EV(role, code, arg)
+#define EV_DECL
 #endif
 
 namespace kime {
@@ -336,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       griddep_wait();  // the schedule written by the kernel before this one
       const int n_units = p.hdr->n_duos * p.heads;
       uint32_t n = 0, c = 0, nq = 0;  // units taken, K/V tiles and Q pairs issued
+      EV_DECL;
       PHASE_DECL(4);
       for (;; ++n) {
         const int slot = n & 1;
@@ -413,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile's PV MMAs queue behind the other tile's softmax
       const int w = warp - 13;
       uint32_t n = 0, c = 0, pc = 0, sc = 0;  // units, key tiles, P tiles, S MMAs of this tile
+      EV_DECL;
       uint32_t ou = 0;  // units in which this tile's O was accumulated (read out by the epilogue warpgroup)
       const uint32_t tS = tmem + w * 128, tO = tmem + 256 + w * 64, tP = tmem + 384 + w * 64;
       PHASE_DECL(8);
@@ -546,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows instead, one unit behind the softmax warpgroups
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t ne0 = 0, ne1 = 0;  // epilogues done for tile A / tile B
+    EV_DECL;
     UnitInfo prev;
     prev.u = -1;
     auto epilogue = [&](const UnitInfo& e) -> bool {
@@ -671,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tO = tmem + 256 + w * 64 + lane_off, tP = tmem + 384 + w * 64 + lane_off;
     uint32_t n = 0, sc = 0, pvc = 0;
+    EV_DECL;
     PHASE_DECL(9);
     for (;; ++n) {
       const int slot = n & 1;
@@ -859,14 +868,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 extern "C" int kime_debug_phase_read(unsigned long long* host) {
   return cudaMemcpyFromSymbol(host, g_kime_phase, sizeof(g_kime_phase));
 }
-extern "C" int kime_debug_ev_read(unsigned long long* t, unsigned int* tag, int* n) {
+extern "C" int kime_debug_ev_read(unsigned long long* t, unsigned int* tag, int* n) {  // kEvCtas x kEvRoles slices
   int rc = cudaMemcpyFromSymbol(t, g_kime_ev_t, sizeof(g_kime_ev_t));
   if (!rc) rc = cudaMemcpyFromSymbol(tag, g_kime_ev_tag, sizeof(g_kime_ev_tag));
   if (!rc) rc = cudaMemcpyFromSymbol(n, g_kime_ev_n, sizeof(g_kime_ev_n));
   return rc;
 }
 extern "C" int kime_debug_ev_clear() {
-  int z[kEvCtas] = {0};
+  int z[kEvCtas * kEvRoles] = {0};
   return cudaMemcpyToSymbol(g_kime_ev_n, z, sizeof(z));
 }
 extern "C" int kime_debug_span_read(unsigned long long* host) {
