@@ -209,6 +209,37 @@ class VarlenRun:
                                    dev_status=dev_status(self.dev))
 
 
+class Fp32Run:
+    """ModernBERT-base shapes with FP32 qkv: the CUDA-core FP32 path and the
+    tensor-core 3xTF32 path (each layer's QK^T and PV as three TF32 products)."""
+
+    def __init__(self, dev):
+        import packed_varlen_attention_kime_gb300 as kime
+        from packed_varlen_attention_kime_gb300.inputs import varlen_case
+        self.kime = kime
+        c = self.case = varlen_case("modernbert_base", device=str(dev))
+        self.qkv = c.qkv.float()
+        self.dev = dev
+        self.cu = c.cu_seqlens.to(dev)
+        self.tables = {}
+        for lay in c.layers:
+            if lay.theta not in self.tables:
+                cs, sn = kime.kime_rope_tables(lay.theta, c.max_seqlen)
+                self.tables[lay.theta] = (cs.to(dev), sn.to(dev))
+        self.out = torch.empty((c.total, c.heads * 64), dtype=torch.float32, device=dev)
+        n = len(c.lengths)
+        self.ws = {p: torch.empty(kime.kime_attn_workspace_bytes(op, n, c.total, c.heads, c.kv_heads),
+                                  dtype=torch.uint8, device=dev) for p, op in ((None, 0), ("3xtf32", 4))}
+        self.flops = [4 * 64 * c.heads * visible_pairs(c.lengths, l.window, l.causal) for l in c.layers]
+
+    def layer(self, k, precision):
+        c, lay = self.case, self.case.layers[k]
+        cs, sn = self.tables[lay.theta]
+        self.kime.kime_attn_varlen(self.qkv, self.cu, c.max_seqlen, c.heads, c.kv_heads, lay.window, lay.causal,
+                                   lay.scale, cs, sn, out=self.out, workspace=self.ws[precision],
+                                   dev_status=dev_status(self.dev), precision=precision)
+
+
 class DecodeRun:
     def __init__(self, dev):
         import packed_varlen_attention_kime_gb300 as kime
@@ -330,6 +361,25 @@ def extra_measurements(dev, flush, stream, pk, reps=10):
                             "tokens_per_s": round(ch.case.total / (ms * 1e-3)), "flops": ch.flops,
                             "bytes": ch.bytes}
     del ch
+    torch.cuda.empty_cache()
+    # FP32 qkv: CUDA-core path vs 3xTF32 on the tensor cores.  The tensor work
+    # is three TF32 products per useful product; its peak is the measured BF16
+    # peak times the nominal TF32 / BF16 ratio (1.1 / 2.25 PFLOP/s dense)
+    fr = Fp32Run(dev)
+    tf32_peak = pk["bf16_tflops"] * 1.1 / 2.25
+    layers = {}
+    for k, lay in enumerate(fr.case.layers):
+        row = {}
+        for prec, key in ((None, "simt"), ("3xtf32", "3xtf32")):
+            per, _ = time_fn(lambda ev, k=k, prec=prec: fr.layer(k, prec), reps, 3, flush, stream)
+            ms = statistics.median(per)
+            row[key + "_ms"] = round(ms, 4)
+            row[key + "_tflops"] = round(fr.flops[k] / (ms * 1e-3) / 1e12, 2)
+        row["3xtf32_tc_frac"] = round(3 * row["3xtf32_tflops"] / tf32_peak, 4)
+        layers[lay.name] = row
+    out["modernbert_base_fp32"] = {"tokens": fr.case.total, "layers": layers,
+                                   "tf32_peak_tflops": round(tf32_peak, 1)}
+    del fr
     torch.cuda.empty_cache()
     return out
 
@@ -506,6 +556,18 @@ def only_arm(args, local):
         per, _ = time_fn(lambda ev: d.step(), args.steps, args.warmup, flush, stream)
         check_status(dev)
         print(json.dumps({"only": name, "ms": [round(x, 4) for x in per]}))
+        return
+    if name == "modernbert_base_fp32":  # the 3xTF32 path
+        fr = Fp32Run(dev)
+        ks = [k for k, l in enumerate(fr.case.layers) if not layer or l.name == layer]
+
+        def g(ev):
+            for k in ks:
+                fr.layer(k, "3xtf32")
+        per, _ = time_fn(g, args.steps, args.warmup, flush, stream)
+        check_status(dev)
+        print(json.dumps({"only": args.only, "layers": [fr.case.layers[k].name for k in ks],
+                          "ms": [round(x, 4) for x in per]}))
         return
     r = VarlenRun(name, dev)
     ks = [k for k, l in enumerate(r.case.layers) if not layer or l.name == layer]

@@ -51,8 +51,19 @@ typedef enum {
 /* Element types of qkv and out.  KIME_F32_F16OUT / KIME_F32_BF16OUT: FP32 qkv
  * and a 16-bit output, the mixed precision of kime-cuda 0.0.3 src/plan.rs
  * (fn types: with Precision::F16 attention's qkv stays FP32 -- FP16 rounding of
- * q and k would move ModernBERT's softmax -- while its output is FP16). */
-typedef enum { KIME_F32 = 0, KIME_BF16 = 1, KIME_F32_F16OUT = 2, KIME_F32_BF16OUT = 3 } kime_dtype;
+ * q and k would move ModernBERT's softmax -- while its output is FP16).
+ * KIME_F32_3XTF32: FP32 qkv and FP32 out, with QK^T and PV on the tensor cores
+ * as three TF32 products each (x = hi + lo, hi = x rounded to TF32; a b taken
+ * as a_lo b_hi + a_hi b_lo + a_hi b_hi, FP32 accumulate): the FP32 accuracy
+ * contract at TF32 tensor rates (kime-cuda's FP32 attention on tensor cores);
+ * needs kime_attn_workspace_bytes(4, ...) bytes of workspace. */
+typedef enum {
+  KIME_F32 = 0,
+  KIME_BF16 = 1,
+  KIME_F32_F16OUT = 2,
+  KIME_F32_BF16OUT = 3,
+  KIME_F32_3XTF32 = 4
+} kime_dtype;
 
 /* Bits OR-ed into *dev_status by the kernels. */
 #define KIME_DEV_BAD_CU 1       /* cu_seqlens not monotone, outside [0,total], cu[0]!=0 or cu[n]!=total */
@@ -73,12 +84,13 @@ typedef enum { KIME_F32 = 0, KIME_BF16 = 1, KIME_F32_F16OUT = 2, KIME_F32_BF16OU
  * materialised.
  *
  *  qkv          device, [total_tokens, W]: FP32 (KIME_F32, KIME_F32_F16OUT,
- *               KIME_F32_BF16OUT) or BF16 (KIME_BF16)
+ *               KIME_F32_BF16OUT, KIME_F32_3XTF32) or BF16 (KIME_BF16)
  *  cu_seqlens   device int32 [n_seqs+1], cu[0]=0, non-decreasing, cu[n]=total_tokens
  *  max_seqlen   host upper bound on every sequence length; must be <= rope_len
  *  window       -1 or >= 0; causal 0/1; scale > 0 (0.125, or 1 if q is pre-scaled)
  *  rope_cos/sin device float32 [rope_len, 32]
- *  out          device, [total_tokens, heads*64]: FP32 (KIME_F32), BF16
+ *  out          device, [total_tokens, heads*64]: FP32 (KIME_F32,
+ *               KIME_F32_3XTF32), BF16
  *               (KIME_BF16, KIME_F32_BF16OUT) or FP16 (KIME_F32_F16OUT),
  *               rounded to nearest even from FP32; rows of skipped sequences
  *               are left untouched
@@ -89,10 +101,15 @@ typedef enum { KIME_F32 = 0, KIME_BF16 = 1, KIME_F32_F16OUT = 2, KIME_F32_BF16OU
  *               first prepared into the workspace (a third launch: queries
  *               and keys rotated once each, queries scaled, all in FP16) and
  *               the attention kernel does no RoPE work: faster, and the same
- *               result bits
- * BF16 runs on the tensor cores (tcgen05, FP32 accumulate); FP32 qkv (all
- * three FP32 codes) runs on FP32 FMA.  Launches: the device scheduler, the row
- * preparation when the workspace has room for it, then the attention kernel. */
+ *               result bits.  KIME_F32_3XTF32 needs
+ *               kime_attn_workspace_bytes(4, ...) bytes (KIME_ERANGE if less)
+ * BF16 runs on the tensor cores (tcgen05, FP32 accumulate); FP32 qkv with
+ * KIME_F32 / KIME_F32_F16OUT / KIME_F32_BF16OUT runs on FP32 FMA.  Launches:
+ * the device scheduler, the row preparation when the workspace has room for
+ * it, then the attention kernel.  KIME_F32_3XTF32 enqueues a memset of part of
+ * the workspace, the scheduler, the split pass (queries and keys rotated, all
+ * values split into TF32 high and low parts, values transposed) and the
+ * tensor-core attention kernel. */
 int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int n_seqs, int total_tokens,
                      int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal, float scale,
                      const float* rope_cos, const float* rope_sin, int rope_len, void* out, void* workspace,
@@ -197,8 +214,12 @@ int kime_chunk_step(const void* qkv, const int32_t* cu_seqlens, const int32_t* p
  * op 1 (decode: uses n_seqs, heads, kv_heads, cap), op 2 (chunked prefill:
  * uses n_seqs, total_tokens) or op 3 (varlen with room for the prepared qkv
  * rows, about total_tokens * 128 * (heads + 2 * kv_heads) bytes more: uses
- * n_seqs, total_tokens, heads, kv_heads).  Returns 0 for an unknown op or malformed
- * sizes. */
+ * n_seqs, total_tokens, heads, kv_heads) or op 4 (varlen with KIME_F32_3XTF32:
+ * op 0 at a 1 KB boundary, then the split planes, each 1 KB aligned: queries
+ * [total_tokens, 64 * heads] f32 twice, keys [total_tokens, 64 * kv_heads] f32
+ * twice, transposed values [64 * kv_heads, tp] f32 twice, with tp =
+ * total_tokens + 4 * n_seqs + 4 rounded up to a multiple of 4).  Returns 0 for
+ * an unknown op or malformed sizes. */
 size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads, int kv_heads, int cap);
 
 /* Host helper: float32 cos/sin tables [len, 32] for heads of 64 by kime-cuda's

@@ -19,13 +19,14 @@ __all__ = [
     "KimeError", "load_library", "kime_attn_varlen", "kime_kv_append", "kime_attn_decode",
     "kime_attn_workspace_bytes", "kime_rope_tables", "kime_attn_debug_tiles", "kime_attn_varlen_noalloc",
     "kime_decode_step", "kime_kv_append_varlen", "kime_attn_chunk", "kime_chunk_step",
-    "kime_attn_debug_tiles_chunk", "KIME_F32", "KIME_BF16", "EXPORTED_SYMBOLS", "NOALLOC_SCRATCH_BYTES",
+    "kime_attn_debug_tiles_chunk", "KIME_F32", "KIME_BF16", "KIME_F32_3XTF32", "EXPORTED_SYMBOLS",
+    "NOALLOC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkime_attn.so")
 
-KIME_F32, KIME_BF16, KIME_F32_F16OUT, KIME_F32_BF16OUT = 0, 1, 2, 3
+KIME_F32, KIME_BF16, KIME_F32_F16OUT, KIME_F32_BF16OUT, KIME_F32_3XTF32 = 0, 1, 2, 3, 4
 DEV_BAD_CU, DEV_SEQ_TOO_LONG, DEV_BAD_POS, DEV_TIMEOUT = 1, 2, 4, 8
 
 EXPORTED_SYMBOLS = (
@@ -104,8 +105,15 @@ def _stream(stream, device):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _dtype_code(qkv: torch.Tensor, out_dtype) -> int:
-    """kime_dtype of (qkv, out): same type, or FP32 qkv with a 16-bit output."""
+def _dtype_code(qkv: torch.Tensor, out_dtype, precision=None) -> int:
+    """kime_dtype of (qkv, out): same type, or FP32 qkv with a 16-bit output;
+    precision="3xtf32" selects FP32 on the tensor cores (FP32 qkv and out)."""
+    if precision == "3xtf32":
+        if qkv.dtype == torch.float32 and out_dtype == torch.float32:
+            return KIME_F32_3XTF32
+        raise TypeError(f"3xTF32 needs float32 qkv and out, got {qkv.dtype} -> {out_dtype}")
+    if precision is not None:
+        raise ValueError(f"unknown precision {precision!r}")
     if qkv.dtype == torch.bfloat16 and out_dtype == torch.bfloat16:
         return KIME_BF16
     if qkv.dtype == torch.float32:
@@ -130,21 +138,25 @@ def kime_rope_tables(theta: float, length: int):
 
 
 def kime_attn_varlen(qkv, cu_seqlens, max_seqlen, heads, kv_heads, window, causal, scale,
-                     rope_cos, rope_sin, out=None, workspace=None, dev_status=None, stream=None, out_dtype=None):
+                     rope_cos, rope_sin, out=None, workspace=None, dev_status=None, stream=None, out_dtype=None,
+                     precision=None):
     """Attention over the packed batch; returns ``out`` [T, heads*64].  Its
     dtype is qkv's, or (FP32 qkv) float16 / bfloat16 when ``out`` or
-    ``out_dtype`` says so."""
+    ``out_dtype`` says so.  ``precision="3xtf32"`` (FP32 qkv and out) runs the
+    FP32 attention on the tensor cores as three TF32 products."""
     lib = load_library()
     T = qkv.shape[0]
     n_seqs = cu_seqlens.numel() - 1
     if out is None:
         out = torch.empty((T, heads * 64), dtype=out_dtype or qkv.dtype, device=qkv.device)
+    code = _dtype_code(qkv, out.dtype, precision)
     if workspace is None:
-        # BF16 qkv: room for the prepared key/value rows, which long sequences use
-        op = 3 if qkv.dtype == torch.bfloat16 else 0
+        # BF16 qkv: room for the prepared key/value rows, which long sequences
+        # use; 3xTF32: room for the split planes
+        op = 3 if qkv.dtype == torch.bfloat16 else (4 if code == KIME_F32_3XTF32 else 0)
         need = kime_attn_workspace_bytes(op, n_seqs, T, heads, kv_heads)
-        workspace = torch.empty(need, dtype=torch.uint8, device=qkv.device)
-    rc = lib.kime_attn_varlen(_p(qkv), _dtype_code(qkv, out.dtype), _p(cu_seqlens), n_seqs, T, int(max_seqlen), heads,
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=qkv.device)
+    rc = lib.kime_attn_varlen(_p(qkv), code, _p(cu_seqlens), n_seqs, T, int(max_seqlen), heads,
                               kv_heads, 64, int(window), int(bool(causal)), float(scale), _p(rope_cos),
                               _p(rope_sin), rope_cos.shape[0], _p(out), _p(workspace),
                               workspace.numel() * workspace.element_size(), _p(dev_status),

@@ -75,6 +75,26 @@ int encode_table_map(CUtensorMap* map, const float* table, int rope_len) {
   return KIME_OK;
 }
 
+// 2-D map over an f32 plane [rows, cols] (a split qkv plane of the 3xTF32
+// path): boxes of box_rows rows x 32 columns (128 bytes), 128-byte swizzle,
+// elements past either end read as zero.
+int encode_f32_plane_map(CUtensorMap* map, const void* plane, long long cols, long long rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return KIME_ECUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  cuuint32_t box[2] = {32, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(plane), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_cuda_error = static_cast<int>(r);
+    return KIME_ECUDA;
+  }
+  return KIME_OK;
+}
+
 size_t varlen_ws_bytes(int n_seqs, int total) { return kime::varlen_workspace_bytes(n_seqs, total); }
 
 // Workspace with room for the prepared qkv rows of a packed batch
@@ -111,6 +131,10 @@ size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads
     if (total_tokens < 0 || !heads_ok(heads, kv_heads, kime::kHead)) return 0;
     return prep_ws_bytes(n_seqs, total_tokens, heads, kv_heads);
   }
+  if (op == 4) {
+    if (total_tokens < 0 || !heads_ok(heads, kv_heads, kime::kHead)) return 0;
+    return kime::tf32_planes(n_seqs, total_tokens, heads, kv_heads).end;
+  }
   return 0;
 }
 
@@ -118,7 +142,8 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
                      int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal, float scale,
                      const float* rope_cos, const float* rope_sin, int rope_len, void* out, void* workspace,
                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  if (dtype != KIME_F32 && dtype != KIME_BF16 && dtype != KIME_F32_F16OUT && dtype != KIME_F32_BF16OUT)
+  if (dtype != KIME_F32 && dtype != KIME_BF16 && dtype != KIME_F32_F16OUT && dtype != KIME_F32_BF16OUT &&
+      dtype != KIME_F32_3XTF32)
     return KIME_EINVAL;
   if (!heads_ok(heads, kv_heads, head_dim)) return KIME_EINVAL;
   if (n_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || rope_len < 0 || window < -1) return KIME_EINVAL;
@@ -135,8 +160,34 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int max_pairs = kime::max_pairs_for(n_seqs, total_tokens);
-  int rc = cuda_status(kime::launch_schedule(cu_seqlens, nullptr, n_seqs, total_tokens, max_seqlen, causal, window,
-                                             0, 0, workspace, max_pairs, dev_status, st));
+  int rc;
+  if (dtype == KIME_F32_3XTF32) {
+    // FP32 on the tensor cores: planes cleared, scheduler, split pass, attention
+    if (workspace_bytes < kime::tf32_planes(n_seqs, total_tokens, heads, kv_heads).end) return KIME_ERANGE;
+    const kime::Tf32Planes pl = kime::tf32_planes(n_seqs, total_tokens, heads, kv_heads);
+    char* w = static_cast<char*>(workspace);
+    CUtensorMap qh, ql, kh, kl, vh, vl;
+    const long long hq = 64LL * heads, hk = 64LL * kv_heads;
+    if ((rc = encode_f32_plane_map(&qh, w + pl.qh, hq, total_tokens, kime::kBM)) ||
+        (rc = encode_f32_plane_map(&ql, w + pl.ql, hq, total_tokens, kime::kBM)) ||
+        (rc = encode_f32_plane_map(&kh, w + pl.kh, hk, total_tokens, 64)) ||
+        (rc = encode_f32_plane_map(&kl, w + pl.kl, hk, total_tokens, 64)) ||
+        (rc = encode_f32_plane_map(&vh, w + pl.vh, pl.tp, hk, 64)) ||
+        (rc = encode_f32_plane_map(&vl, w + pl.vl, pl.tp, hk, 64)))
+      return rc;
+    if ((rc = cuda_status(kime::launch_tf32_clear(n_seqs, total_tokens, heads, kv_heads, workspace, st)))) return rc;
+    if ((rc = cuda_status(kime::launch_schedule(cu_seqlens, nullptr, n_seqs, total_tokens, max_seqlen, causal,
+                                                window, 0, 0, workspace, max_pairs, dev_status, st))))
+      return rc;
+    if ((rc = cuda_status(kime::launch_tf32_split(static_cast<const float*>(qkv), cu_seqlens, n_seqs, total_tokens,
+                                                  heads, kv_heads, scale, rope_cos, rope_sin, rope_len, workspace,
+                                                  st))))
+      return rc;
+    return cuda_status(kime::launch_prefill_3xtf32(&qh, &ql, &kh, &kl, &vh, &vl, heads, kv_heads, window, causal,
+                                                   static_cast<float*>(out), workspace, dev_status, st));
+  }
+  rc = cuda_status(kime::launch_schedule(cu_seqlens, nullptr, n_seqs, total_tokens, max_seqlen, causal, window,
+                                         0, 0, workspace, max_pairs, dev_status, st));
   if (rc) return rc;
   if (dtype != KIME_BF16) {
     const int out_kind = dtype == KIME_F32 ? 0 : (dtype == KIME_F32_F16OUT ? 1 : 2);

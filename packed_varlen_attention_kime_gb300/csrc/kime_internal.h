@@ -70,6 +70,35 @@ inline size_t varlen_workspace_bytes(int n_seqs, int total_tokens) {
   return sizeof(WsHeader) + static_cast<size_t>(max_pairs_for(n_seqs, total_tokens)) * sizeof(Pair) +
          static_cast<size_t>(max_duos_for(n_seqs, total_tokens)) * sizeof(Duo);
 }
+// FP32 attention on the tensor cores (3xTF32): after the scheduler's lists
+// (at a 1 KB boundary) the split qkv planes, each 1 KB aligned -- rotated and
+// scaled queries (high and low TF32 parts) [total, heads*64] f32, rotated keys
+// [total, kv_heads*64] f32, and the values transposed, [kv_heads*64, tp] f32,
+// token j of sequence s in column tf32_vt_col(cu[s], s) + (j - cu[s]), every
+// sequence starting at a multiple of 4 columns (16 bytes: a TMA x coordinate
+// rule) and the gaps zero.
+struct Tf32Planes {
+  size_t qh, ql, kh, kl, vh, vl, end;
+  int tp;  // columns of a transposed value plane
+};
+inline int tf32_vt_cols(int n_seqs, int total_tokens) {
+  return static_cast<int>(align_up(static_cast<size_t>(total_tokens) + 4 * static_cast<size_t>(n_seqs) + 4, 4));
+}
+inline Tf32Planes tf32_planes(int n_seqs, int total_tokens, int heads, int kv_heads) {
+  Tf32Planes p;
+  p.tp = tf32_vt_cols(n_seqs, total_tokens);
+  const size_t q = align_up(static_cast<size_t>(total_tokens) * heads * kHead * 4, 1024);
+  const size_t k = align_up(static_cast<size_t>(total_tokens) * kv_heads * kHead * 4, 1024);
+  const size_t v = align_up(static_cast<size_t>(kv_heads) * kHead * p.tp * 4, 1024);
+  p.qh = align_up(varlen_workspace_bytes(n_seqs, total_tokens), 1024);
+  p.ql = p.qh + q;
+  p.kh = p.ql + q;
+  p.kl = p.kh + k;
+  p.vh = p.kl + k;
+  p.vl = p.vh + v;
+  p.end = p.vl + v;
+  return p;
+}
 inline Pair* ws_pairs(void* ws) { return reinterpret_cast<Pair*>(static_cast<char*>(ws) + sizeof(WsHeader)); }
 inline Duo* ws_duos(void* ws, int max_pairs) {
   return reinterpret_cast<Duo*>(static_cast<char*>(ws) + sizeof(WsHeader) + static_cast<size_t>(max_pairs) * sizeof(Pair));
@@ -104,6 +133,21 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
 // A packed batch's qkv rows prepared for the attention kernel (prep.cu):
 // queries rotated at their positions and scaled by scale * log2(e), keys
 // rotated, all rounded to f16, values widened to f16; out [total, W] f16.
+// 3xTF32 FP32 path: the value planes cleared (before the scheduler), the
+// split pass (queries and keys rotated, queries scaled by scale * log2(e),
+// values transposed; every value split into high and low TF32 parts) into the
+// planes of tf32_planes(), then the attention kernel.
+// The planes are 2-D maps of 32-column (128-byte) boxes: q_h / q_l over
+// [total, heads*64] (128-row boxes), k_h / k_l over [total, kv_heads*64] and
+// v_h / v_l over [kv_heads*64, tp] (64-row boxes).
+cudaError_t launch_tf32_clear(int n_seqs, int total, int heads, int kv_heads, void* ws, cudaStream_t st);
+cudaError_t launch_tf32_split(const float* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
+                              float scale, const float* cos_t, const float* sin_t, int rope_len, void* ws,
+                              cudaStream_t st);
+cudaError_t launch_prefill_3xtf32(const CUtensorMap* q_h, const CUtensorMap* q_l, const CUtensorMap* k_h,
+                                  const CUtensorMap* k_l, const CUtensorMap* v_h, const CUtensorMap* v_l,
+                                  int heads, int kv_heads, int window, int causal, float* out, void* ws,
+                                  int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_qkv_prep(const void* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
                             float scale, const float* cos_t, const float* sin_t, int rope_len, void* out,
                             cudaStream_t st);

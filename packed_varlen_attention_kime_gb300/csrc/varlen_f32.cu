@@ -3,8 +3,9 @@
 //
 // Same schedule, tile classification and semantics as the tensor-core BF16
 // kernel; it exists because FP32 inputs must keep FP32 accuracy (max abs error
-// 1e-5 against the FP64 oracle), which neither BF16 nor TF32 tensor-core
-// operands can give.  kime-cuda 0.0.3 (src/plan.rs, Step::Attention) likewise
+// 1e-5 against the FP64 oracle), which neither BF16 nor single TF32
+// tensor-core operands can give (the tensor-core alternative, three TF32
+// products per product, is tf32x3.cu).  kime-cuda 0.0.3 (src/plan.rs, Step::Attention) likewise
 // keeps attention's qkv in FP32 (fn types: FP16 rounding of q and k moves
 // ModernBERT's softmax).
 //
