@@ -24,12 +24,15 @@
 //           the scheduler's list.  Thread r owns row r of the 128-row query
 //           tile (TMEM lane r).  Key tiles are visited in 64-key halves:
 //           S = Q K^T (three 128x64x64 TF32 MMA chains into TMEM), online
-//           softmax in FP32 on S loaded from TMEM, P split into high and low
+//           softmax in FP32 on S loaded from TMEM (exponentials on the MUFU,
+//           ex2.approx: relative error about 2^-22, far inside the FP32
+//           contract), P split into high and low
 //           parts stored to TMEM, O += P V (three chains, A = P from TMEM,
 //           B = V^T from shared memory), O rescaled in TMEM when the row max
 //           moves.  Q (high, low: 64 KB) stays in shared memory for the unit;
 //           the K / V^T halves (64 KB each) are double-buffered, the next one
-//           loaded by TMA while the current one is in the softmax.  Thread 0
+//           loaded by TMA (as soon as the PV that read its stage is done)
+//           while the current one is in the softmax.  Thread 0
 //           issues the copies and the MMAs.
 #include "kime_common.cuh"
 #include "kime_internal.h"
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(kT3Threads, 1)
   uint32_t nq = 0, ns = 0, npv = 0;
   uint32_t c = 0;                      // K/V halves consumed (all units): stage c & 1
   uint32_t issued_q = 0, issued_c = 0; // thread 0: copies started (for the wind-down)
-  bool ok = true;
+  bool ok = true, lost = false;  // lost: thread 0's wait for the previous PV ran out
 
   for (;;) {
     if (tid == 0) s_unit = atomicAdd(&p.hdr->next_unit, 1);
@@ -326,8 +329,15 @@ __global__ void __launch_bounds__(kT3Threads, 1)
             mma_tf32_ss(tS, sdesc_sw128(A[q] + (ks >> 2) * kSlabQ + (ks & 3) * 32, 16, 1024),
                         sdesc_sw128(B[q] + (ks >> 2) * kSlabK + (ks & 3) * 32, 16, 1024), (q | ks) != 0);
         tc_commit(&s_done);
+        // the next half's copies go into the stage that the previous half's
+        // PV read: issued as soon as that PV is done, they have the whole
+        // softmax of this half to land
+        if (k > 0 && k + 1 < nsub) {
+          if (mbar_wait(&pv_done, npv & 1)) load_half(k + 1);
+          else lost = true;
+        }
       }
-      ok = mbar_wait(&s_done, ns & 1);
+      ok = mbar_wait(&s_done, ns & 1) && !lost;
       ok = __syncthreads_and(ok);
       if (!ok) break;
       ++ns;
@@ -349,11 +359,11 @@ __global__ void __launch_bounds__(kT3Threads, 1)
 #pragma unroll
         for (int j = 0; j < 64; ++j) x[j] = 0.f;
       } else {
-        alpha = exp2f(m - m_new);
+        alpha = fast_exp2(m - m_new);
         float rs = 0.f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          x[j] = exp2f(x[j] - m_new);
+          x[j] = fast_exp2(x[j] - m_new);
           rs += x[j];
         }
         l = l * alpha + rs;
@@ -367,7 +377,6 @@ __global__ void __launch_bounds__(kT3Threads, 1)
         if (!ok) break;
         ++npv;
         tc_fence_after();
-        if (tid == 0 && k + 1 < nsub) load_half(k + 1);  // into the stage that PV read
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
