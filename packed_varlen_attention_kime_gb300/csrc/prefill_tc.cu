@@ -756,48 +756,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         PHASE(2);
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        // PV(t-1) read P(t-1) from this tile's P columns and accumulated into
-        // O: it completes before P(t) is stored and O is rescaled.
-        if (t > kb) {
-          ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
-          tc_fence_after();
-        }
-        PHASE(3);
         // P = 2^(x - m_use): the differences in float32 pairs, rounded to f16
         // pairs, two exponentials per MUFU operation (P in f16, as the MMA
         // takes it); row sums in f16 over 16 keys, then float32.  A masked
-        // key (-inf) gives 0.
-        float rs2f[4] = {0.f, 0.f, 0.f, 0.f};
+        // key (-inf) gives 0.  All 64 exponent pairs first (independent
+        // chains the schedulers can interleave), then the sums.
         uint64_t mm;
         asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(m_use));
+        uint32_t pw[64];
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {  // 16 keys -> 8 columns of P at a time
-          uint32_t pw[8];
+        for (int e = 0; e < 64; ++e) {
+          uint64_t xx, d;
+          asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "f"(x[2 * e]), "f"(x[2 * e + 1]));
+          asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(xx), "l"(mm));
+          uint32_t h;
+          asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.f16x2.f32 %0, hi, lo;\n\t}" : "=r"(h) : "l"(d));
+          asm("ex2.approx.f16x2 %0, %1;" : "=r"(pw[e]) : "r"(h));
+        }
+        float rs2f[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int j = q8 * 16 + 2 * e;
-            uint64_t xx, d;
-            asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "f"(x[j]), "f"(x[j + 1]));
-            asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(xx), "l"(mm));
-            uint32_t h;
-            asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.f16x2.f32 %0, hi, lo;\n\t}" : "=r"(h) : "l"(d));
-            asm("ex2.approx.f16x2 %0, %1;" : "=r"(pw[e]) : "r"(h));
-          }
+        for (int q8 = 0; q8 < 8; ++q8) {  // 16 keys
+          const uint32_t* g = pw + 8 * q8;
           uint32_t a0, a1, a2, a3, b0, b1, c0;
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a0) : "r"(pw[0]), "r"(pw[1]));
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a1) : "r"(pw[2]), "r"(pw[3]));
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a2) : "r"(pw[4]), "r"(pw[5]));
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a3) : "r"(pw[6]), "r"(pw[7]));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a0) : "r"(g[0]), "r"(g[1]));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a1) : "r"(g[2]), "r"(g[3]));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a2) : "r"(g[4]), "r"(g[5]));
+          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a3) : "r"(g[6]), "r"(g[7]));
           asm("add.rn.f16x2 %0, %1, %2;" : "=r"(b0) : "r"(a0), "r"(a1));
           asm("add.rn.f16x2 %0, %1, %2;" : "=r"(b1) : "r"(a2), "r"(a3));
           asm("add.rn.f16x2 %0, %1, %2;" : "=r"(c0) : "r"(b0), "r"(b1));
           float lo, hi;
           asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}" : "=f"(lo), "=f"(hi) : "r"(c0));
           rs2f[q8 & 3] += lo + hi;
-          tmem_st8(tP + q8 * 8, pw);  // this row's P: keys 2c, 2c+1 in column c
         }
         const float rowsum = (rs2f[0] + rs2f[1]) + (rs2f[2] + rs2f[3]);
         l = l * alpha + rowsum;
+        // PV(t-1) read P(t-1) from this tile's P columns and accumulated into
+        // O: it completes before P(t) is stored and O is rescaled (the
+        // exponentials above overlap it)
+        if (t > kb) {
+          ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
+          tc_fence_after();
+        }
+        PHASE(3);
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) {  // this row's P: keys 2c, 2c+1 in column c
+          const uint32_t p8[8] = {pw[8 * q8], pw[8 * q8 + 1], pw[8 * q8 + 2], pw[8 * q8 + 3],
+                                  pw[8 * q8 + 4], pw[8 * q8 + 5], pw[8 * q8 + 6], pw[8 * q8 + 7]};
+          tmem_st8(tP + q8 * 8, p8);
+        }
         PHASE(4);
         if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {
           uint32_t ov[64];
