@@ -107,8 +107,12 @@ constexpr float kLazy = 8.f;  // the reference max moves when exceeded by more (
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
 
+// kbase: the unit's key tiles are keys kbase + 128 t .. kbase + 128 t + 127
+// for t in [kb, ke).  With a window (packed sequences) the grid starts at the
+// unit's first visible key, max(0, q0 - window): a 128-row query tile with
+// window 64 then sees 2 key tiles, not the 3 of the 128-aligned grid.
 struct UnitInfo {
-  int32_t u, s, qt0, nt, kb, ke, row0, L, off;
+  int32_t u, s, qt0, nt, kb, ke, row0, L, off, kbase;
 };
 
 
@@ -362,6 +366,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const Duo d = p.duos[u / p.heads];
           inf.s = d.s; inf.qt0 = d.qt0; inf.nt = d.nt; inf.kb = d.kb; inf.ke = d.ke; inf.row0 = d.row0; inf.L = d.L;
           inf.off = kCache ? d.off : 0;
+          inf.kbase = 0;
+          if (!kCache && kWindow >= 0 && d.qt0 * kBM > kWindow) {
+            // the unit's key tiles on the grid from its first visible key: the
+            // union of its query tiles' ranges there
+            inf.kbase = d.qt0 * kBM - kWindow;
+            int kb, ke, fb, fe;
+            tile_ranges(d.L, d.L - inf.kbase, -inf.kbase, d.qt0, kCausal, kWindow, kb, ke, fb, fe);
+            inf.kb = kb;
+            inf.ke = ke;
+            if (d.nt == 2) {
+              tile_ranges(d.L, d.L - inf.kbase, -inf.kbase, d.qt0 + 1, kCausal, kWindow, kb, ke, fb, fe);
+              inf.kb = min(inf.kb, kb);
+              inf.ke = max(inf.ke, ke);
+            }
+          }
         }
         sh->info[slot] = inf;
         mbar_arrive(&sh->unit_full[slot]);
@@ -392,12 +411,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(smem + kOffK + st * kTile, &k_map, &sh->kv_full[st], 0, kvrow + t * kBN);
             tma_load_2d(smem + kOffV + st * kTile, &v_map, &sh->kv_full[st], 0, kvrow + t * kBN);
           } else {
-            tma_load_2d(smem + kOffK + st * kTile, &qkv_map, &sh->kv_full[st], kx, inf.row0 + t * kBN);
-            tma_load_2d(smem + kOffV + st * kTile, &qkv_map, &sh->kv_full[st], vx, inf.row0 + t * kBN);
-            if (kTab) {  // the RoPE table rows of key positions t*128 .. t*128 + 127
+            const int k0 = inf.kbase + t * kBN;  // the tile's first key
+            tma_load_2d(smem + kOffK + st * kTile, &qkv_map, &sh->kv_full[st], kx, inf.row0 + k0);
+            tma_load_2d(smem + kOffV + st * kTile, &qkv_map, &sh->kv_full[st], vx, inf.row0 + k0);
+            if (kTab) {  // the RoPE table rows of key positions k0 .. k0 + 127
               uint8_t* tb = smem + kOffTab + (c & 1) * 2 * kTile;
-              tma_load_2d(tb, &cos_map, &sh->kv_full[st], 0, t * kBN);
-              tma_load_2d(tb + kTile, &sin_map, &sh->kv_full[st], 0, t * kBN);
+              tma_load_2d(tb, &cos_map, &sh->kv_full[st], 0, k0);
+              tma_load_2d(tb + kTile, &sin_map, &sh->kv_full[st], 0, k0);
             }
           }
         }
@@ -432,7 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (inf.u < 0) break;
         const int off = kCache ? inf.off : 0;  // position of the unit's row 0
         int kb = 0, ke = 0, fb, fe;  // this tile's key tiles; none when the unit has no tile B
-        if (w < inf.nt) tile_ranges(inf.L, off + inf.L, off, inf.qt0 + w, kCausal, kWindow, kb, ke, fb, fe);
+        if (w < inf.nt)
+          tile_ranges(inf.L, off + inf.L - inf.kbase, off - inf.kbase, inf.qt0 + w, kCausal, kWindow, kb, ke, fb, fe);
         const uint32_t aq = smem_u32(smem + kOffQ + slot * 2 * kTile) + w * kTile;
         PHASE(4);
         bool ok = wait(&sh->qrot[slot], (n >> 1) & 1);
@@ -635,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (named_bar_or(3, 128, !ok)) break;
       }
       for (int t = inf.kb; !kPrep && t < inf.ke; ++t, ++c) {  // (prepared keys need nothing here)
-        const int st = c % kStages, j = t * kBN + r;
+        const int st = c % kStages, j = inf.kbase + t * kBN + r;
         PHASE(2);
         ok = wait(&sh->kv_full[st], (c / kStages) & 1);
         PHASE(3);
@@ -695,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qt = inf.qt0 + w, q0 = qt * kBM, i = q0 + r;
       const bool row_ok = i < inf.L;
       int kb, ke, fb, fe;
-      tile_ranges(inf.L, off + inf.L, off, qt, kCausal, kWindow, kb, ke, fb, fe);
+      tile_ranges(inf.L, off + inf.L - inf.kbase, off - inf.kbase, qt, kCausal, kWindow, kb, ke, fb, fe);
       // chunk rows: the last visible key (this row's position), or none for a padding row
       const int chunk_hi = row_ok ? off + i : -1;
 
@@ -705,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // than 2^8.  Logits arrive in log2 units (scale*log2(e) is folded into q).
       float m_ref = -INFINITY, l = 0.f;
       for (int t = kb; t < ke; ++t) {
-        const int k0 = t * kBN;
+        const int k0 = inf.kbase + t * kBN;
         PHASE(7);
         ok = wait(&sh->s_full[w][sc & 1], (sc >> 1) & 1);
         if (r == 0) EV(3 + w, 0, t);
