@@ -423,6 +423,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--e2e-graph", type=int, default=1, help="replay the end-to-end step from a CUDA graph")
     ap.add_argument("--e2e-groups", type=int, default=8,
                     help="sequence groups the end-to-end step pipelines its copies and calls over")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -505,7 +506,7 @@ def main():
     bounds = [0]
     for g in range(1, n_groups):  # split at the sequence boundary nearest g/n of the tokens
         tgt = c.total * g / n_groups
-        bounds.append(min(range(bounds[-1] + 1, len(c.lengths)), key=lambda s: abs(cu_h[s] - tgt)))
+        bounds.append(min(range(bounds[-1] + 1, len(c.lengths) - (n_groups - g) + 1), key=lambda s: abs(cu_h[s] - tgt)))
     bounds.append(len(c.lengths))
     groups = []
     for a, b in zip(bounds[:-1], bounds[1:]):
@@ -514,9 +515,9 @@ def main():
         groups.append((r0, r1, h_cu_g, torch.empty_like(h_cu_g, device=dev), max(c.lengths[a:b])))
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
 
-    def e2e_step(ev):
+    def enqueue(origin):  # the pipelined step, forked from and joined back to stream `origin`
         start = torch.cuda.Event()
-        start.record(stream)
+        start.record(origin)
         for st in (s_in, s_cmp, s_out):
             st.wait_event(start)
         for r0, r1, h_cu_g, d_cu_g, mx in groups:
@@ -540,7 +541,23 @@ def main():
                     h[r0:r1].copy_(o[r0:r1], non_blocking=True)
         done = torch.cuda.Event()
         done.record(s_out)
-        stream.wait_event(done)
+        origin.wait_event(done)
+
+    if args.e2e_graph:
+        # captured once (after a direct run for the first-call set-up) and
+        # replayed each step: the host enqueues one graph, not every group's
+        # calls and copies
+        enqueue(stream)
+        torch.cuda.synchronize()
+        graph, cap = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
+        with torch.cuda.graph(graph, stream=cap):
+            enqueue(cap)
+
+        def e2e_step(ev):
+            graph.replay()
+    else:
+        def e2e_step(ev):
+            enqueue(stream)
     e_per, _ = time_fn(e2e_step, max(5, args.steps // 5), 3, flush, stream)
     e_ms = statistics.mean(e_per)
     ref_out = [o.clone() for o in run.outs]
@@ -553,7 +570,8 @@ def main():
     e2e = {"value": round(world * c.total / (e_ms * 1e-3)), "unit": "tokens/s",
            "h2d_bytes_per_step": h_qkv.numel() * 2 + sum(g[2].numel() * 4 for g in groups),
            "d2h_bytes_per_step": sum(o.numel() * 2 for o in run.outs), "ms_per_step": round(e_ms, 4),
-           "pipeline": f"{n_groups} sequence groups; copy in, both layers and copy out on three streams"}
+           "pipeline": f"{n_groups} sequence groups; copy in, both layers and copy out on three streams"
+                       + ("; captured once as a CUDA graph, replayed each step" if args.e2e_graph else "")}
 
     extra = {}
     if not args.no_extra and rank == 0:
