@@ -109,8 +109,11 @@ constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
 
 // kbase: the unit's key tiles are keys kbase + 128 t .. kbase + 128 t + 127
 // for t in [kb, ke).  With a window (packed sequences) the grid starts at the
-// unit's first visible key, max(0, q0 - window): a 128-row query tile with
-// window 64 then sees 2 key tiles, not the 3 of the 128-aligned grid.
+// unit's first visible key, q0 - window, when that means fewer tile visits: a
+// 128-row query tile with window 64 then sees 2 key tiles, not the 3 of the
+// 128-aligned grid.  For q0 < window the grid starts below key 0; those keys
+// are masked, and their rows (another sequence's, or the TMA fill before row
+// 0) never reach the output.
 struct UnitInfo {
   int32_t u, s, qt0, nt, kb, ke, row0, L, off, kbase;
 };
@@ -367,18 +370,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           inf.s = d.s; inf.qt0 = d.qt0; inf.nt = d.nt; inf.kb = d.kb; inf.ke = d.ke; inf.row0 = d.row0; inf.L = d.L;
           inf.off = kCache ? d.off : 0;
           inf.kbase = 0;
-          if (!kCache && kWindow >= 0 && d.qt0 * kBM > kWindow) {
-            // the unit's key tiles on the grid from its first visible key: the
-            // union of its query tiles' ranges there
-            inf.kbase = d.qt0 * kBM - kWindow;
-            int kb, ke, fb, fe;
-            tile_ranges(d.L, d.L - inf.kbase, -inf.kbase, d.qt0, kCausal, kWindow, kb, ke, fb, fe);
-            inf.kb = kb;
-            inf.ke = ke;
+          if (!kCache && kWindow >= 0) {
+            // the unit's key tiles on the grid from its first visible key,
+            // q0 - window (the union of its query tiles' ranges there), when
+            // its query tiles then visit fewer tiles than on the 128-aligned
+            // grid -- never more for q0 > window; for q0 < window the grid
+            // starts below key 0 (those keys are masked) and is taken only
+            // when it visits strictly fewer
+            const int kbase = d.qt0 * kBM - kWindow;
+            int kb, ke, fb, fe, kb2 = 0, ke2 = 0, akb, ake, akb2 = 0, ake2 = 0;
+            tile_ranges(d.L, d.L - kbase, -kbase, d.qt0, kCausal, kWindow, kb, ke, fb, fe);
+            tile_ranges(d.L, d.qt0, kCausal, kWindow, akb, ake, fb, fe);
             if (d.nt == 2) {
-              tile_ranges(d.L, d.L - inf.kbase, -inf.kbase, d.qt0 + 1, kCausal, kWindow, kb, ke, fb, fe);
-              inf.kb = min(inf.kb, kb);
-              inf.ke = max(inf.ke, ke);
+              tile_ranges(d.L, d.L - kbase, -kbase, d.qt0 + 1, kCausal, kWindow, kb2, ke2, fb, fe);
+              tile_ranges(d.L, d.qt0 + 1, kCausal, kWindow, akb2, ake2, fb, fe);
+            }
+            const int visits = (ke - kb) + (ke2 - kb2), aligned = (ake - akb) + (ake2 - akb2);
+            if (kbase > 0 || visits < aligned) {
+              inf.kbase = kbase;
+              inf.kb = d.nt == 2 ? min(kb, kb2) : kb;
+              inf.ke = d.nt == 2 ? max(ke, ke2) : ke;
             }
           }
         }
@@ -751,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             hi = min(kBN - 1, inf.L - 1 - k0);
             if (kCausal) hi = min(hi, i - k0);
             if (kWindow >= 0) {
-              lo = max(lo, i - kWindow - k0);
+              lo = max(lo, max(i - kWindow, 0) - k0);  // (a grid may start below key 0)
               hi = min(hi, i + kWindow - k0);
             }
             if (!row_ok) hi = -1;

@@ -93,6 +93,9 @@ SMALL = [
     ([400, 1, 257], 9, 3, 65, True, 0.125),
     ([513, 200], 2, 1, 0, False, 0.125),
     ([250, 260], 4, 4, 300, False, 0.125),
+    # long sequences with window 64: units past the first take their key tiles
+    # on a grid starting at their first visible key (not 128-aligned)
+    ([1100, 700], 4, 2, 64, False, 0.125),
 ]
 
 
