@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (profiles/prefill_tc_modernbert_base_global.md), keyed by the SHA-1 of the
 # kernel source it was taken on: any change to the kernel makes the figure
 # stale, and the bench then reports null.
-MEASURED_TRAFFIC = {"7a1ff03600dfc9e02c7d41b836255a5e2dd17147": 106665472}
+MEASURED_TRAFFIC = {"3b3fa32d18768b584cc0ddb23f4853bcbe91e413": 105834752}
 
 
 def measured_traffic():
@@ -443,6 +443,91 @@ def oracle_single_core():
             "decode_sample": f"sequences 0-{n - 1} of {len(d.pos)} (keys 0..pos, all {d.heads} q heads)"}
 
 
+def end_to_end(args, dev, stream, flush, run, world):
+    """The headline step end to end through the public API: pinned host qkv ->
+    device, both layers, both outputs -> pinned host, every step.  The batch is
+    cut into contiguous groups of sequences, each a packed batch of its own:
+    copies in, the two layers, and copies out run on three streams, so group
+    g's layers overlap group g+1's copy in and group g-1's copy out (the link is
+    full duplex)."""
+    c = run.case
+    h_qkv = c.qkv.cpu().pin_memory()
+    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in run.outs]
+    d_qkv = torch.empty_like(c.qkv)
+    cu_h = c.cu_seqlens.tolist()
+    n_groups = max(1, min(args.e2e_groups, len(c.lengths)))
+    bounds = [0]
+    for g in range(1, n_groups):  # split at the sequence boundary nearest g/n of the tokens
+        tgt = c.total * g / n_groups
+        bounds.append(min(range(bounds[-1] + 1, len(c.lengths) - (n_groups - g) + 1),
+                          key=lambda s: abs(cu_h[s] - tgt)))
+    bounds.append(len(c.lengths))
+    groups = []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        r0, r1 = cu_h[a], cu_h[b]
+        h_cu_g = torch.tensor([x - r0 for x in cu_h[a:b + 1]], dtype=torch.int32).pin_memory()
+        groups.append((r0, r1, h_cu_g, torch.empty_like(h_cu_g, device=dev), max(c.lengths[a:b])))
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+
+    def enqueue(origin):  # the pipelined step, forked from and joined back to stream `origin`
+        start = torch.cuda.Event()
+        start.record(origin)
+        for st in (s_in, s_cmp, s_out):
+            st.wait_event(start)
+        for r0, r1, h_cu_g, d_cu_g, mx in groups:
+            with torch.cuda.stream(s_in):
+                d_qkv[r0:r1].copy_(h_qkv[r0:r1], non_blocking=True)
+                d_cu_g.copy_(h_cu_g, non_blocking=True)
+            e_in = torch.cuda.Event()
+            e_in.record(s_in)
+            s_cmp.wait_event(e_in)
+            with torch.cuda.stream(s_cmp):
+                for k, lay in enumerate(c.layers):
+                    cs, sn = run.tables[lay.theta]
+                    run.kime.kime_attn_varlen(d_qkv[r0:r1], d_cu_g, mx, c.heads, c.kv_heads, lay.window,
+                                              lay.causal, lay.scale, cs, sn, out=run.outs[k][r0:r1],
+                                              workspace=run.ws, dev_status=dev_status(dev), stream=s_cmp)
+            e_cmp = torch.cuda.Event()
+            e_cmp.record(s_cmp)
+            s_out.wait_event(e_cmp)
+            with torch.cuda.stream(s_out):
+                for h, o in zip(h_out, run.outs):
+                    h[r0:r1].copy_(o[r0:r1], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(s_out)
+        origin.wait_event(done)
+
+    if args.e2e_graph:
+        # captured once (after a direct run for the first-call set-up) and
+        # replayed each step: the host enqueues one graph, not every group's
+        # calls and copies
+        enqueue(stream)
+        torch.cuda.synchronize()
+        graph, cap = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
+        with torch.cuda.graph(graph, stream=cap):
+            enqueue(cap)
+
+        def e2e_step(ev):
+            graph.replay()
+    else:
+        def e2e_step(ev):
+            enqueue(stream)
+    e_per, _ = time_fn(e2e_step, max(5, args.steps // 5), 3, flush, stream)
+    e_ms = statistics.mean(e_per)
+    ref_out = [o.clone() for o in run.outs]
+    for k in range(len(c.layers)):  # the pipelined groups give the whole batch's bits
+        run.layer(k)
+    torch.cuda.synchronize()
+    if not all(torch.equal(a, b) for a, b in zip(ref_out, run.outs)) or \
+            not all(torch.equal(h, o.cpu()) for h, o in zip(h_out, run.outs)):
+        raise RuntimeError("pipelined end-to-end outputs differ from the whole-batch calls")
+    return {"value": round(world * c.total / (e_ms * 1e-3)), "unit": "tokens/s",
+            "h2d_bytes_per_step": h_qkv.numel() * 2 + sum(g[2].numel() * 4 for g in groups),
+            "d2h_bytes_per_step": sum(o.numel() * 2 for o in run.outs), "ms_per_step": round(e_ms, 4),
+            "pipeline": f"{n_groups} sequence groups; copy in, both layers and copy out on three streams"
+                        + ("; captured once as a CUDA graph, replayed each step" if args.e2e_graph else "")}
+
+
 # ---- main ----------------------------------------------------------------------------
 
 def main():
@@ -453,6 +538,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--e2e-graph", type=int, default=1, help="replay the end-to-end step from a CUDA graph")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (e2e null): profiling runs")
     ap.add_argument("--e2e-groups", type=int, default=8,
                     help="sequence groups the end-to-end step pipelines its copies and calls over")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -522,85 +608,10 @@ def main():
     flops_step = sum(run.flops)
     tflops = flops_step / (ms_step * 1e-3) / 1e12
 
-    # end to end through the public API: pinned host qkv -> device, both layers,
-    # both outputs -> pinned host, every step.  The batch is cut into contiguous
-    # groups of sequences, each a packed batch of its own: copies in, the two
-    # layers, and copies out run on three streams, so group g's layers overlap
-    # group g+1's copy in and group g-1's copy out (the link is full duplex).
-    h_qkv = c.qkv.cpu().pin_memory()
-    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in run.outs]
-    d_qkv = torch.empty_like(c.qkv)
-    cu_h = c.cu_seqlens.tolist()
-    n_groups = max(1, min(args.e2e_groups, len(c.lengths)))
-    bounds = [0]
-    for g in range(1, n_groups):  # split at the sequence boundary nearest g/n of the tokens
-        tgt = c.total * g / n_groups
-        bounds.append(min(range(bounds[-1] + 1, len(c.lengths) - (n_groups - g) + 1), key=lambda s: abs(cu_h[s] - tgt)))
-    bounds.append(len(c.lengths))
-    groups = []
-    for a, b in zip(bounds[:-1], bounds[1:]):
-        r0, r1 = cu_h[a], cu_h[b]
-        h_cu_g = torch.tensor([x - r0 for x in cu_h[a:b + 1]], dtype=torch.int32).pin_memory()
-        groups.append((r0, r1, h_cu_g, torch.empty_like(h_cu_g, device=dev), max(c.lengths[a:b])))
-    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-
-    def enqueue(origin):  # the pipelined step, forked from and joined back to stream `origin`
-        start = torch.cuda.Event()
-        start.record(origin)
-        for st in (s_in, s_cmp, s_out):
-            st.wait_event(start)
-        for r0, r1, h_cu_g, d_cu_g, mx in groups:
-            with torch.cuda.stream(s_in):
-                d_qkv[r0:r1].copy_(h_qkv[r0:r1], non_blocking=True)
-                d_cu_g.copy_(h_cu_g, non_blocking=True)
-            e_in = torch.cuda.Event()
-            e_in.record(s_in)
-            s_cmp.wait_event(e_in)
-            with torch.cuda.stream(s_cmp):
-                for k, lay in enumerate(c.layers):
-                    cs, sn = run.tables[lay.theta]
-                    run.kime.kime_attn_varlen(d_qkv[r0:r1], d_cu_g, mx, c.heads, c.kv_heads, lay.window,
-                                              lay.causal, lay.scale, cs, sn, out=run.outs[k][r0:r1],
-                                              workspace=run.ws, dev_status=dev_status(dev), stream=s_cmp)
-            e_cmp = torch.cuda.Event()
-            e_cmp.record(s_cmp)
-            s_out.wait_event(e_cmp)
-            with torch.cuda.stream(s_out):
-                for h, o in zip(h_out, run.outs):
-                    h[r0:r1].copy_(o[r0:r1], non_blocking=True)
-        done = torch.cuda.Event()
-        done.record(s_out)
-        origin.wait_event(done)
-
-    if args.e2e_graph:
-        # captured once (after a direct run for the first-call set-up) and
-        # replayed each step: the host enqueues one graph, not every group's
-        # calls and copies
-        enqueue(stream)
-        torch.cuda.synchronize()
-        graph, cap = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
-        with torch.cuda.graph(graph, stream=cap):
-            enqueue(cap)
-
-        def e2e_step(ev):
-            graph.replay()
-    else:
-        def e2e_step(ev):
-            enqueue(stream)
-    e_per, _ = time_fn(e2e_step, max(5, args.steps // 5), 3, flush, stream)
-    e_ms = statistics.mean(e_per)
-    ref_out = [o.clone() for o in run.outs]
-    for k in range(len(c.layers)):  # the pipelined groups give the whole batch's bits
-        run.layer(k)
-    torch.cuda.synchronize()
-    if not all(torch.equal(a, b) for a, b in zip(ref_out, run.outs)) or \
-            not all(torch.equal(h, o.cpu()) for h, o in zip(h_out, run.outs)):
-        raise RuntimeError("pipelined end-to-end outputs differ from the whole-batch calls")
-    e2e = {"value": round(world * c.total / (e_ms * 1e-3)), "unit": "tokens/s",
-           "h2d_bytes_per_step": h_qkv.numel() * 2 + sum(g[2].numel() * 4 for g in groups),
-           "d2h_bytes_per_step": sum(o.numel() * 2 for o in run.outs), "ms_per_step": round(e_ms, 4),
-           "pipeline": f"{n_groups} sequence groups; copy in, both layers and copy out on three streams"
-                       + ("; captured once as a CUDA graph, replayed each step" if args.e2e_graph else "")}
+    # end to end through the public API, with host buffers (end_to_end)
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(args, dev, stream, flush, run, world)
 
     # the same step with a warm L2 (no flush between steps, back to back),
     # labelled: reported beside the cold-L2 value, never as it
@@ -619,7 +630,6 @@ def main():
 
     extra = {}
     if not args.no_extra and rank == 0:
-        del h_qkv, h_out, d_qkv
         extra = extra_measurements(dev, flush, stream, pk)
 
     check_status(dev)  # any flagged input error or timed-out wait voids the numbers
