@@ -467,7 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tile_ranges(inf.L, off + inf.L - inf.kbase, off - inf.kbase, inf.qt0 + w, kCausal, kWindow, kb, ke, fb, fe);
         const uint32_t aq = smem_u32(smem + kOffQ + slot * 2 * kTile) + w * kTile;
         PHASE(4);
-        bool ok = wait(&sh->qrot[slot], (n >> 1) & 1);
+        // the unit's Q: rotated by the RoPE warpgroup, or (prepared rows)
+        // ready as soon as its copy has landed -- then the issuer does not wait
+        // for the epilogue warpgroup, which writes the previous unit's rows
+        // before it gets to this unit
+        bool ok = wait(kPrep ? &sh->q_full[slot] : &sh->qrot[slot], (n >> 1) & 1);
         PHASE(1);
         // S for the key tile that is number cc of the K/V ring may be issued
         // once that tile is in (and rotated) and the softmax warpgroup has
