@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (profiles/prefill_tc_modernbert_base_global.md), keyed by the SHA-1 of the
 # kernel source it was taken on: any change to the kernel makes the figure
 # stale, and the bench then reports null.
-MEASURED_TRAFFIC = {"3b3fa32d18768b584cc0ddb23f4853bcbe91e413": 105834752}
+MEASURED_TRAFFIC = {"7796c0db5bf582c4cbe5ba9e78afeade88a082c6": 106347776}
 
 
 def measured_traffic():
