@@ -43,6 +43,18 @@ def test_binding_exposes_the_same_names():
     assert set(kime.EXPORTED_SYMBOLS) == set(declared_functions())
 
 
+def test_binding_constants_match_the_header():
+    # the dtype codes and status bits the binding passes and reads are the
+    # header's own values
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    enum = dict((k, int(v)) for k, v in re.findall(r"\b(KIME_[A-Z0-9_]+)\s*=\s*(-?\d+)", text))
+    for name in ("KIME_F32", "KIME_BF16", "KIME_F32_F16OUT", "KIME_F32_BF16OUT", "KIME_F32_3XTF32"):
+        assert getattr(kime, name) == enum[name], name
+    defines = dict((k, int(v)) for k, v in re.findall(r"#define\s+(KIME_DEV_[A-Z_]+)\s+(\d+)", text))
+    for name, value in defines.items():
+        assert getattr(kime, name[len("KIME_"):]) == value, name
+
+
 def test_package_does_not_import_the_oracle():
     pkg = os.path.join(ROOT, "packed_varlen_attention_kime_gb300")
     for dirpath, _, files in os.walk(pkg):
