@@ -264,9 +264,8 @@ int kime_attn_debug_tiles_chunk(const int32_t* cu_seqlens, const int32_t* pos, i
  * about 48 bytes per 128 tokens plus 64 per sequence; with KIME_F32_3XTF32 it
  * is kime_attn_workspace_bytes(4, ...), which only small batches fit; a BF16
  * batch has its rows prepared only when they fit in the array too).  The first
- * call on a
- * device looks up the array's device address with that device current; make
- * it before any stream capture.  All calls share the array, so calls that
+ * call on a device looks up the array's device address with that device
+ * current; make it before any stream capture.  All calls share the array, so calls that
  * overlap on the GPU race; order them on one stream.  Allocates nothing. */
 int kime_attn_varlen_noalloc(const void* qkv, int dtype, const int32_t* cu_seqlens, int n_seqs, int total_tokens,
                              int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal,
