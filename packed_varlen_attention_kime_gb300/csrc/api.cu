@@ -111,6 +111,8 @@ bool heads_ok(int heads, int kv_heads, int head_dim) {
 
 }  // namespace
 
+void kime::set_last_cuda_error(int e) { g_last_cuda_error = e; }
+
 extern "C" {
 
 size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads, int kv_heads, int cap) {
@@ -210,10 +212,12 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
     if ((rc = encode_table_map(&cmap, rope_cos, rope_len))) return rc;
     if ((rc = encode_table_map(&smap, rope_sin, rope_len))) return rc;
   }
-  return cuda_status(kime::launch_prefill_tc(&map, nullptr, nullptr, prep ? nullptr : &cmap, prep ? nullptr : &smap,
-                                             prep ? &pmap : nullptr, n_seqs, total_tokens, heads, kv_heads, 0, window,
-                                             causal, scale, rope_cos, rope_sin, out, workspace, max_pairs,
-                                             dev_status, st));
+  if (prep)
+    return cuda_status(kime::launch_prefill_rows(&pmap, heads, kv_heads, window, causal, out, workspace, max_pairs,
+                                                 dev_status, st));
+  return cuda_status(kime::launch_prefill_tc(&map, nullptr, nullptr, &cmap, &smap, nullptr, n_seqs, total_tokens,
+                                             heads, kv_heads, 0, window, causal, scale, rope_cos, rope_sin, out,
+                                             workspace, max_pairs, dev_status, st));
 }
 
 int kime_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,

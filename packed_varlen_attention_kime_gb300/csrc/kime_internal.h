@@ -105,6 +105,9 @@ inline Duo* ws_duos(void* ws, int max_pairs) {
 }
 
 size_t decode_workspace_bytes(int n_seqs, int heads, int kv_heads, int cap);
+// Records a failing CUDA call's error as the calling thread's
+// kime_attn_last_cuda_error() (entry points outside api.cu report through it).
+void set_last_cuda_error(int e);
 
 // Launchers (each returns a cudaError_t of the launch).
 // pos == nullptr: packed sequences.  Otherwise chunks at offsets pos[s] against
@@ -130,6 +133,11 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
                               int heads, int kv_heads, int cap, int window, int causal,
                               float scale, const float* cos_t, const float* sin_t, void* out, void* ws,
                               int max_pairs, int32_t* dev_status, cudaStream_t st);
+// Attention over prepared rows (prefill_rows.cu): rows_map addresses the
+// rows written by launch_qkv_prep ([total, W] f16, boxes of 128 rows x 64
+// columns, 128-byte swizzle); the work list is the scheduler's in ws.
+cudaError_t launch_prefill_rows(const CUtensorMap* rows_map, int heads, int kv_heads, int window, int causal,
+                                void* out, void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
 // A packed batch's qkv rows prepared for the attention kernel (prep.cu):
 // queries rotated at their positions and scaled by scale * log2(e), keys
 // rotated, all rounded to f16, values widened to f16; out [total, W] f16.

@@ -43,10 +43,19 @@ extern "C" int kime_attn_varlen_noalloc(const void* qkv, int dtype, const int32_
   const size_t need = kime_attn_workspace_bytes(0, n_seqs, total_tokens, heads, kv_heads, 1);
   if (need > kNoAllocScratchBytes) return KIME_ERANGE;  // batch too large for the built-in scratch
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KIME_ECUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    kime::set_last_cuda_error(static_cast<int>(e));
+    return KIME_ECUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return KIME_ERANGE;  // more devices than the address table holds
   void* scratch = g_scratch_addr[dev].load(std::memory_order_acquire);
   if (!scratch) {
-    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || !scratch) return KIME_ECUDA;
+    e = cudaGetSymbolAddress(&scratch, g_noalloc_scratch);
+    if (e != cudaSuccess || !scratch) {
+      kime::set_last_cuda_error(static_cast<int>(e));
+      return KIME_ECUDA;
+    }
     g_scratch_addr[dev].store(scratch, std::memory_order_release);
   }
   return kime_attn_varlen(qkv, dtype, cu_seqlens, n_seqs, total_tokens, max_seqlen, heads, kv_heads, head_dim,
