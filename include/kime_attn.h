@@ -70,6 +70,9 @@ typedef enum {
 #define KIME_DEV_SEQ_TOO_LONG 2 /* a sequence longer than max_seqlen: it is skipped */
 #define KIME_DEV_BAD_POS 4      /* a decode/append position outside [0, min(cap, rope_len)): skipped */
 #define KIME_DEV_TIMEOUT 8      /* a pipeline wait ran past its time limit; the work item is abandoned */
+#define KIME_DEV_RANGE 16       /* BF16 path: a rotated (and scaled) q or k, or a v, beyond the f16 range (|x| > 65504)
+                                   was rounded to f16 for the tensor cores and saturated; the results are computed
+                                   from the saturated values */
 
 /* kime_attn_varlen -- attention over a packed batch of variable-length
  * sequences (kime-cuda Op::Attention / kime-cpu Step::Attention, with the RoPE
@@ -103,7 +106,10 @@ typedef enum {
  *               the attention kernel does no RoPE work: faster, and the same
  *               result bits.  KIME_F32_3XTF32 needs
  *               kime_attn_workspace_bytes(4, ...) bytes (KIME_ERANGE if less)
- * BF16 runs on the tensor cores (tcgen05, FP32 accumulate); FP32 qkv with
+ * BF16 runs on the tensor cores (tcgen05, FP32 accumulate) with f16 operands:
+ * rotated keys, scaled rotated queries and values are rounded to f16, so they
+ * must lie within its range (|x| <= 65504; beyond, they saturate and
+ * KIME_DEV_RANGE is set).  FP32 qkv with
  * KIME_F32 / KIME_F32_F16OUT / KIME_F32_BF16OUT runs on FP32 FMA.  Launches:
  * the device scheduler, the row preparation when the workspace has room for
  * it, then the attention kernel.  KIME_F32_3XTF32 enqueues a memset of part of
@@ -138,19 +144,24 @@ int kime_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int head
  *  qkv_new, pos, caches as for kime_kv_append (caches are read only)
  *  out          device bf16 [n_seqs, heads*64]
  *  workspace    device scratch of kime_attn_workspace_bytes(1, ...) bytes
- * Split-KV, 256 keys per CTA, with a merge by the last CTA to finish;
- * heads/kv_heads must be 1..8.  One memset of the per-(sequence, kv head)
- * tickets and one kernel launch. */
+ * Split-KV on the tensor cores: the keys 0..=pos[s] of each (sequence, kv
+ * head) are cut into chunks of 128 keys and the chunks into work items of up
+ * to 16; a one-CTA plan kernel lists the items (longest first) and zeroes the
+ * per-(sequence, kv head) merge tickets, and a persistent decode kernel
+ * (three CTAs per SM) streams each item's K/V tiles and reduces all q heads of
+ * the kv group together; the last item of a (sequence, kv head) to finish
+ * merges the partial results.  heads/kv_heads must be 1..8.  Two launches,
+ * no memset. */
 int kime_attn_decode(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
                      int cap, float scale, const float* rope_cos, const float* rope_sin, int rope_len,
                      const void* k_cache, const void* v_cache, void* out, void* workspace, size_t workspace_bytes,
                      int32_t* dev_status, void* stream);
 
 /* kime_decode_step -- kime_kv_append followed by kime_attn_decode in one
- * launch (plus the ticket memset): the CTA whose 128-key chunk holds row pos[s]
- * of a kv head writes the appended row (same rotation and rounding as
- * kime_kv_append) to the caches and uses it directly; no other CTA reads that
- * row.  Arguments as kime_attn_decode, with writable caches; workspace from
+ * decode launch (after the plan kernel): the work item whose chunks hold row
+ * pos[s] of a kv head writes the appended row (same rotation and rounding as
+ * kime_kv_append) to the caches and uses it directly; no other item reads
+ * that row.  Arguments as kime_attn_decode, with writable caches; workspace from
  * kime_attn_workspace_bytes(1, ...). */
 int kime_decode_step(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,
                      int cap, float scale, const float* rope_cos, const float* rope_sin, int rope_len, void* k_cache,

@@ -27,7 +27,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkime_attn.so")
 
 KIME_F32, KIME_BF16, KIME_F32_F16OUT, KIME_F32_BF16OUT, KIME_F32_3XTF32 = 0, 1, 2, 3, 4
-DEV_BAD_CU, DEV_SEQ_TOO_LONG, DEV_BAD_POS, DEV_TIMEOUT = 1, 2, 4, 8
+DEV_BAD_CU, DEV_SEQ_TOO_LONG, DEV_BAD_POS, DEV_TIMEOUT, DEV_RANGE = 1, 2, 4, 8, 16
 
 EXPORTED_SYMBOLS = (
     "kime_attn_varlen", "kime_kv_append", "kime_attn_decode", "kime_attn_workspace_bytes",

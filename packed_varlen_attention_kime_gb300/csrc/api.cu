@@ -206,7 +206,7 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
     void* rows = static_cast<char*>(workspace) + prep_offset(n_seqs, total_tokens);
     if ((rc = encode_qkv_map(&pmap, rows, total_tokens, static_cast<int>(W)))) return rc;
     if ((rc = cuda_status(kime::launch_qkv_prep(qkv, cu_seqlens, n_seqs, total_tokens, heads, kv_heads, scale,
-                                                rope_cos, rope_sin, rope_len, rows, st))))
+                                                rope_cos, rope_sin, rope_len, rows, dev_status, st))))
       return rc;
   } else {
     if ((rc = encode_table_map(&cmap, rope_cos, rope_len))) return rc;

@@ -42,7 +42,11 @@ enum : int32_t {
   ST_SEQ_TOO_LONG = 2,  // a sequence longer than max_seqlen (or the RoPE table)
   ST_BAD_POS = 4,       // decode / append position outside [0, min(cap, rope_len))
   ST_TIMEOUT = 8,       // an mbarrier wait ran past its time limit
+  ST_RANGE = 16,        // an f16 tensor-core operand beyond the f16 range (saturated)
 };
+
+// Largest finite f16; conversions with satfinite clamp beyond it.
+constexpr float kF16Max = 65504.f;
 
 // Time limit of one bounded mbarrier wait (ns of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

@@ -141,6 +141,7 @@ cudaError_t launch_prefill_rows(const CUtensorMap* rows_map, int heads, int kv_h
 // A packed batch's qkv rows prepared for the attention kernel (prep.cu):
 // queries rotated at their positions and scaled by scale * log2(e), keys
 // rotated, all rounded to f16, values widened to f16; out [total, W] f16.
+// Any of them beyond the f16 range (saturated) sets ST_RANGE in dev_status.
 // 3xTF32 FP32 path: the value planes cleared (before the scheduler), the
 // split pass (queries and keys rotated, queries scaled by scale * log2(e),
 // values transposed; every value split into high and low TF32 parts) into the
@@ -158,7 +159,7 @@ cudaError_t launch_prefill_3xtf32(const CUtensorMap* q_h, const CUtensorMap* q_l
                                   int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_qkv_prep(const void* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
                             float scale, const float* cos_t, const float* sin_t, int rope_len, void* out,
-                            cudaStream_t st);
+                            int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_kv_append_varlen(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total,
                                     int heads, int kv_heads, int cap, const float* cos_t, const float* sin_t,
                                     int rope_len, void* k_cache, void* v_cache, int32_t* dev_status,

@@ -199,10 +199,11 @@ __device__ __forceinline__ void load_table_row_smem(TableRow& t, const uint8_t* 
 // the MMAs read.  rope_row: rotate-half RoPE with the row's table entries in
 // float32 (y_t = fma(x_t, c, -(x_{t+32} s)), y_{t+32} = fma(x_{t+32}, c,
 // x_t s)), times `mul`, rounded once to f16.
-// convert_row: the bf16 values widened and rounded to f16.  zero_row: zeros
+// convert_row: the bf16 values widened and rounded to f16.  Both keep in `big`
+// the largest magnitude they round (beyond kF16Max it saturates).  zero_row: zeros
 // (cache rows past a chunk's keys, whose contents are undefined: a NaN there
 // would reach O through a zero probability).
-__device__ __forceinline__ void rope_row(uint8_t* tile, int r, const TableRow& tb, float mul) {
+__device__ __forceinline__ void rope_row(uint8_t* tile, int r, const TableRow& tb, float mul, float& big) {
   uint8_t* row = tile + r * 128;
   const int sw = r & 7;
 #pragma unroll
@@ -228,6 +229,7 @@ __device__ __forceinline__ void rope_row(uint8_t* tile, int r, const TableRow& t
         a1 = __fmaf_rn(xa, cc[2 * e + 1], -__fmul_rn(xb, ss[2 * e + 1]));
         b1 = __fmaf_rn(xb, cc[2 * e + 1], __fmul_rn(xa, ss[2 * e + 1]));
       }
+      big = fmax3(big, fmax3(fabsf(a0 * mul), fabsf(a1 * mul), fabsf(b0 * mul)), fabsf(b1 * mul));
       ya[e] = pack_f16x2(a0 * mul, a1 * mul);
       yb[e] = pack_f16x2(b0 * mul, b1 * mul);
     }
@@ -236,12 +238,15 @@ __device__ __forceinline__ void rope_row(uint8_t* tile, int r, const TableRow& t
   }
 }
 
-__device__ __forceinline__ void convert_row(uint8_t* tile, int r) {
+__device__ __forceinline__ void convert_row(uint8_t* tile, int r, float& big) {
   uint4* row = reinterpret_cast<uint4*>(tile + r * 128);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const int k = kk ^ (r & 7);  // neighbouring rows touch different banks
     const uint4 a = row[k];
+    big = fmax3(big, fmax3(fabsf(bf16lo(a.x)), fabsf(bf16hi(a.x)), fabsf(bf16lo(a.y))),
+                fmax3(fabsf(bf16hi(a.y)), fmax3(fabsf(bf16lo(a.z)), fabsf(bf16hi(a.z)), fabsf(bf16lo(a.w))),
+                      fabsf(bf16hi(a.w))));
     row[k] = make_uint4(pack_f16x2(bf16lo(a.x), bf16hi(a.x)), pack_f16x2(bf16lo(a.y), bf16hi(a.y)),
                         pack_f16x2(bf16lo(a.z), bf16hi(a.z)), pack_f16x2(bf16lo(a.w), bf16hi(a.w)));
   }
@@ -585,6 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ RoPE
     const int r = tid - 256;  // row of every tile this thread converts
     uint32_t n = 0, c = 0;
+    float big = 0.f;  // largest magnitude this thread rounded to f16
     // prepared rows: this warpgroup has no RoPE work and writes the output
     // rows instead, one unit behind the softmax warpgroups
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -652,9 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w == 0) ok = wait(&sh->q_full[slot], (n >> 1) & 1);
         if (ok) {
           if (i < inf.L)
-            rope_row(q + w * kTile, r, tb, p.qmul);
+            rope_row(q + w * kTile, r, tb, p.qmul, big);
           else
-            convert_row(q + w * kTile, r);
+            convert_row(q + w * kTile, r, big);
         }
       }
       fence_proxy_async_smem();
@@ -678,8 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           if (kCache) {  // cached keys are rotated already
             if (j < Lk) {
-              convert_row(smem + kOffK + st * kTile, r);
-              convert_row(smem + kOffV + st * kTile, r);
+              convert_row(smem + kOffK + st * kTile, r, big);
+              convert_row(smem + kOffV + st * kTile, r, big);
             } else {
               zero_row(smem + kOffK + st * kTile, r);
               zero_row(smem + kOffV + st * kTile, r);
@@ -688,11 +694,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j < inf.L) {
               const uint8_t* tab = smem + kOffTab + (c & 1) * 2 * kTile;  // loaded with this K tile
               load_table_row_smem(tb, tab, tab + kTile, r);
-              rope_row(smem + kOffK + st * kTile, r, tb, 1.f);
+              rope_row(smem + kOffK + st * kTile, r, tb, 1.f, big);
             } else {
-              convert_row(smem + kOffK + st * kTile, r);
+              convert_row(smem + kOffK + st * kTile, r, big);
             }
-            convert_row(smem + kOffV + st * kTile, r);
+            convert_row(smem + kOffV + st * kTile, r, big);
           }
           fence_proxy_async_smem();
         }
@@ -706,6 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
     }
+    // an operand beyond the f16 range was saturated: reported once per warp
+    if (__any_sync(0xffffffffu, big > kF16Max) && lane == 0) report(p.dev_status, ST_RANGE);
     PHASE_FLUSH(g_kime_phase, 32, r == 0);
   } else {
     regs_inc<kRegsSoftmax>();

@@ -31,7 +31,8 @@ constexpr int kPrepWarps = 8;  // rows per CTA
 __global__ void __launch_bounds__(32 * kPrepWarps)
     qkv_prep_kernel(const uint16_t* __restrict__ qkv, const int32_t* __restrict__ cu, int n_seqs, int total,
                     int heads, int kv_heads, float qmul, const float* __restrict__ cos_t,
-                    const float* __restrict__ sin_t, int rope_len, uint16_t* __restrict__ out) {
+                    const float* __restrict__ sin_t, int rope_len, uint16_t* __restrict__ out,
+                    int32_t* dev_status) {
   const int j = blockIdx.x * kPrepWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (j >= total) {
     griddep_wait();
@@ -53,6 +54,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps)
   uint4* dst = reinterpret_cast<uint4*>(out + static_cast<size_t>(j) * W);
   const int nrot = (heads + kv_heads) * (kHead / 8);  // 16-byte chunks of the row's queries and keys
   const int nall = (heads + 2 * kv_heads) * (kHead / 8);
+  float big = 0.f;  // largest magnitude rounded to f16 in this row (an operand beyond kF16Max saturates)
   const float* crow = cos_t + static_cast<size_t>(rot ? pos : 0) * kHalf;
   const float* srow = sin_t + static_cast<size_t>(rot ? pos : 0) * kHalf;
   // queries and keys: every lane takes part in each round (the partner
@@ -92,10 +94,11 @@ __global__ void __launch_bounds__(32 * kPrepWarps)
           r0 = __fmaf_rn(x0, cc[2 * e], __fmul_rn(p0, ss[2 * e]));
           r1 = __fmaf_rn(x1, cc[2 * e + 1], __fmul_rn(p1, ss[2 * e + 1]));
         }
+        big = fmax3(big, fabsf(r0 * mul), fabsf(r1 * mul));
         ow[e] = pack_f16x2(r0 * mul, r1 * mul);
       }
       o = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-    } else {  // a row of no valid sequence: converted only
+    } else {  // a row of no valid sequence: converted only (its range is not checked)
       o = make_uint4(pack_f16x2(bf16lo(x.x), bf16hi(x.x)), pack_f16x2(bf16lo(x.y), bf16hi(x.y)),
                      pack_f16x2(bf16lo(x.z), bf16hi(x.z)), pack_f16x2(bf16lo(x.w), bf16hi(x.w)));
     }
@@ -104,9 +107,13 @@ __global__ void __launch_bounds__(32 * kPrepWarps)
   // values: widened to f16
   for (int q = nrot + lane; q < nall; q += 32) {
     const uint4 x = __ldg(src + q);
+    big = fmax3(big, fmax3(fabsf(bf16lo(x.x)), fabsf(bf16hi(x.x)), fabsf(bf16lo(x.y))),
+                fmax3(fabsf(bf16hi(x.y)), fmax3(fabsf(bf16lo(x.z)), fabsf(bf16hi(x.z)), fabsf(bf16lo(x.w))),
+                      fabsf(bf16hi(x.w))));
     dst[q] = make_uint4(pack_f16x2(bf16lo(x.x), bf16hi(x.x)), pack_f16x2(bf16lo(x.y), bf16hi(x.y)),
                         pack_f16x2(bf16lo(x.z), bf16hi(x.z)), pack_f16x2(bf16lo(x.w), bf16hi(x.w)));
   }
+  if (__any_sync(0xffffffffu, rot && big > kF16Max) && lane == 0) report(dev_status, ST_RANGE);
   // this pass runs beside the scheduler (it reads none of its output); it
   // ends only after the scheduler has, so the attention kernel, which waits
   // for this pass, also finds the scheduler's lists complete
@@ -117,7 +124,7 @@ __global__ void __launch_bounds__(32 * kPrepWarps)
 
 cudaError_t launch_qkv_prep(const void* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
                             float scale, const float* cos_t, const float* sin_t, int rope_len, void* out,
-                            cudaStream_t st) {
+                            int32_t* dev_status, cudaStream_t st) {
   // launched with programmatic stream serialization: it starts while the
   // scheduler (which lets dependents start at once) still runs
   cudaLaunchConfig_t cfg = {};
@@ -131,7 +138,7 @@ cudaError_t launch_qkv_prep(const void* qkv, const int32_t* cu, int n_seqs, int 
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, qkv_prep_kernel, static_cast<const uint16_t*>(qkv), cu, n_seqs, total, heads,
                             kv_heads, scale * 1.4426950408889634f, cos_t, sin_t, rope_len,
-                            static_cast<uint16_t*>(out));
+                            static_cast<uint16_t*>(out), dev_status);
 }
 
 }  // namespace kime

@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kSchedThreads = 1024;
 constexpr int kBuckets = 256;
+static_assert(kBuckets % 32 == 0, "buckets per lane");
 
 __device__ __forceinline__ int bucket_of(int kb, int ke) { return kBuckets - 1 - min(ke - kb, kBuckets - 1); }
 
@@ -104,20 +105,35 @@ __global__ void __launch_bounds__(kSchedThreads)
     }
   }
   __syncthreads();
-  if (threadIdx.x < 2) {
-    const int k = threadIdx.x;
-    int acc = 0;
-    for (int i = 0; i < kBuckets; ++i) {
-      cursor[k][i] = acc;
-      acc += hist[k][i];
+  if (threadIdx.x < 64) {
+    // exclusive prefix sums of the two histograms, one warp each: lane j
+    // holds buckets 8j .. 8j+7, a warp scan adds the lanes' totals
+    const int k = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kPer = kBuckets / 32;
+    int local[kPer], sum = 0;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      local[q] = sum;
+      sum += hist[k][lane * kPer + q];
     }
-    if (k == 0) {
-      hdr->n_pairs = min(acc, max_pairs);
-      hdr->next_unit = 0;
-      if (s_bad) report(dev_status, s_bad);
-    } else {
-      hdr->n_duos = min(acc, max_duos);
-      hdr->next_duo = 0;
+    int incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    const int before = incl - sum;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) cursor[k][lane * kPer + q] = before + local[q];
+    if (lane == 31) {
+      if (k == 0) {
+        hdr->n_pairs = min(incl, max_pairs);
+        hdr->next_unit = 0;
+        if (s_bad) report(dev_status, s_bad);
+      } else {
+        hdr->n_duos = min(incl, max_duos);
+        hdr->next_duo = 0;
+      }
     }
   }
   __syncthreads();
