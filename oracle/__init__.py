@@ -60,6 +60,8 @@ def _load():
         lib.kime_oracle_kv_append_varlen.restype = I
         lib.kime_oracle_attn_chunk.argtypes = [P, P, P, I, I, I, I, D, P, P, I, P, P, P, P, L, P, I]
         lib.kime_oracle_attn_chunk.restype = I
+        lib.kime_oracle_qkv_proj.argtypes = [P, P, I, I, I, P, I]
+        lib.kime_oracle_qkv_proj.restype = I
         _lib = lib
     return _lib
 
@@ -263,3 +265,27 @@ def attn_chunk(qkv_bits, cu, pos, heads, kv_heads, cap, scale, cos, sin, k_cache
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return out
+
+
+def qkv_proj(x_bits, w_bits, nthreads=None):
+    """The QKV projection in float64: qkv [T, O] = x [T, K] . w [O, K]^T, with
+    x and w given as bfloat16 bits (uint16); the weight is [out width, in width]."""
+    lib = _load()
+    x = np.ascontiguousarray(x_bits, np.uint16)
+    w = np.ascontiguousarray(w_bits, np.uint16)
+    assert x.ndim == 2 and w.ndim == 2 and x.shape[1] == w.shape[1]
+    out = np.zeros((x.shape[0], w.shape[0]), np.float64)
+    rc = lib.kime_oracle_qkv_proj(_ptr(x), _ptr(w), x.shape[0], x.shape[1], w.shape[0], _ptr(out),
+                                  _threads(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (code {rc})")
+    return out
+
+
+def attn_varlen_proj(x_bits, w_bits, cu, heads, kv_heads, window, causal, scale, cos, sin, rows=None,
+                     row_heads=None, nthreads=None):
+    """Attention of a packed batch whose qkv rows are the projection of x:
+    qkv_proj, then attn_varlen on the float64 rows (nothing rounded between)."""
+    qkv = qkv_proj(x_bits, w_bits, nthreads)
+    return attn_varlen(qkv, cu, heads, kv_heads, window, causal, scale, cos, sin, rows=rows,
+                       row_heads=row_heads, nthreads=nthreads)

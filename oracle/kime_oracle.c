@@ -562,3 +562,54 @@ int kime_oracle_attn_chunk(const uint16_t *qkv, const int32_t *cu, const int32_t
         for (int t = 0; t < nthreads; t++) pthread_join(th[t], NULL);
     return 0;
 }
+
+/* ---- QKV projection (the step before attention) ------------------------
+ *
+ * qkv[t, o] = sum_k x[t, k] * w[o, k] for every token row t of the packed
+ * batch and every output column o (o in [0, 64*(heads + 2*kv_heads))): the
+ * weight is stored [out width, in width], as kime-cuda 0.0.3 src/plan.rs lays
+ * out the weight of Op::Gemm (shape [out.width, a.width]), and q, k and v are
+ * the one fused [960, 576] weight ffai-argus 0.7.3 src/text.rs describes
+ * under Block::q (q rows first, then k, then v; argus keeps them as three
+ * matrices, which is the same product column block by column block).  x and w
+ * are bfloat16 bit patterns, widened exactly; every product and sum is in
+ * double, k in increasing order.  No bias, no activation (the attention
+ * projection of both towers has neither). */
+typedef struct {
+    const uint16_t *x, *w;
+    int rows, in_w, out_w;
+    double *out;
+    int t0, t1;
+} proj_job;
+
+static void *proj_worker(void *p) {
+    const proj_job *j = (const proj_job *)p;
+    for (int t = j->t0; t < j->t1; ++t)
+        for (int o = 0; o < j->out_w; ++o) {
+            double acc = 0.0;
+            for (int k = 0; k < j->in_w; ++k)
+                acc += bf16_bits_to_double(j->x[(size_t)t * j->in_w + k]) *
+                       bf16_bits_to_double(j->w[(size_t)o * j->in_w + k]);
+            j->out[(size_t)t * j->out_w + o] = acc;
+        }
+    return NULL;
+}
+
+int kime_oracle_qkv_proj(const uint16_t *x, const uint16_t *w, int rows, int in_w, int out_w, double *out,
+                         int nthreads) {
+    if (rows < 0 || in_w <= 0 || out_w <= 0) return -1;
+    if (rows == 0) return 0;
+    if (!x || !w || !out) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (nthreads > rows) nthreads = rows;
+    proj_job jobs[256];
+    pthread_t th[256];
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i] = (proj_job){x, w, rows, in_w, out_w, out, (int)((long)rows * i / nthreads),
+                             (int)((long)rows * (i + 1) / nthreads)};
+        pthread_create(&th[i], NULL, proj_worker, &jobs[i]);
+    }
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    return 0;
+}

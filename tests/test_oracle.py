@@ -12,6 +12,9 @@ bfloat16 rounding), a closed form, or an invariant stated on the source pages:
       of new tokens at index_pos is appended to the cache, then attends it
       with CausalSoftmax offset index_pos.
   kime-cuda 0.0.3 src/plan.rs, fn rope_tables: the table recipe.
+  ffai-argus Block::q and kime-cuda Op::Gemm: the QKV projection out = x W^T
+      with one [out, in] weight, q rows then k then v; the q rows pre-scaled
+      by 1/8, exactly.
 """
 import json
 import os
@@ -560,3 +563,86 @@ def test_chunk_sampled_rows_equal_full_computation():
         assert np.array_equal(part[k], full[r, h * 64:(h + 1) * 64])
     with pytest.raises(ValueError):
         oracle.attn_chunk(bits, cu, np.array([2, 14], np.int32), H, Hkv, cap, 0.125, c, s, kb, vb)
+
+
+# ---- QKV projection (the step before attention) ----------------------------------
+
+def bf16_of(a):
+    """float array -> bfloat16 bits (values chosen exactly representable, or rounded)."""
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def widen(bits):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy().astype(np.float64)
+
+
+def test_qkv_proj_golden():
+    # hand-derived: out[t][o] = sum_k x[t][k] w[o][k] with w stored [out, in]
+    with open(os.path.join(GOLDEN, "qkv_proj_small.json")) as f:
+        g = json.load(f)
+    got = oracle.qkv_proj(bf16_of(g["x"]), bf16_of(g["w"]))
+    assert np.array_equal(got, np.array(g["out"]))
+
+
+def test_qkv_proj_selection_weights_pick_columns_exactly():
+    # w[o] = unit row e_{perm[o]}: output column o is input column perm[o],
+    # exactly -- a transposed weight or a swapped index would pick others
+    rng = np.random.default_rng(7)
+    x = bf16_of(rng.normal(size=(37, 128)))
+    perm = rng.permutation(128)[:96]
+    w = np.zeros((96, 128), np.float32)
+    w[np.arange(96), perm] = 1.0
+    got = oracle.qkv_proj(x, bf16_of(w))
+    assert np.array_equal(got, widen(x)[:, perm])
+
+
+def test_qkv_proj_matches_dense_numpy():
+    # an independent formulation: numpy's dense product of the widened operands
+    rng = np.random.default_rng(8)
+    x = bf16_of(rng.normal(size=(53, 192)))
+    w = bf16_of(rng.normal(scale=0.07, size=(320, 192)))
+    ref = widen(x) @ widen(w).T
+    got = oracle.qkv_proj(x, w)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+    assert oracle.qkv_proj(x[:0], w).shape == (0, 320)
+
+
+def test_projection_scale_fold_is_bitwise():
+    # argus Block::q: the q weight pre-scaled by 1/8 at load, with scale 1,
+    # equals the unscaled weight with scale 1/8 bit for bit (a power of two)
+    rng = np.random.default_rng(9)
+    lengths, H, Hkv, hidden = [19, 7, 33], 3, 1, 64
+    T = sum(lengths)
+    x = bf16_of(rng.normal(size=(T, hidden)))
+    wf = rng.normal(scale=0.125, size=(64 * (H + 2 * Hkv), hidden)).astype(np.float32)
+    w = bf16_of(wf)
+    w_fold = widen(w).astype(np.float32)
+    w_fold[: 64 * H] *= 0.125
+    w_fold = bf16_of(w_fold)
+    c, s = tables64(1e5, 64)
+    a = oracle.attn_varlen_proj(x, w, cu_of(lengths), H, Hkv, -1, True, 0.125, c, s)
+    b = oracle.attn_varlen_proj(x, w_fold, cu_of(lengths), H, Hkv, -1, True, 1.0, c, s)
+    assert np.array_equal(a, b)
+
+
+def test_projection_gqa_blocks():
+    # the weight's rows are q heads, then k heads, then v heads: zeroing the
+    # v rows of kv head 1 zeroes exactly the outputs of the q heads of group 1
+    rng = np.random.default_rng(10)
+    lengths, H, Hkv, hidden = [12, 9], 4, 2, 64
+    T = sum(lengths)
+    x = bf16_of(rng.normal(size=(T, hidden)))
+    w = widen(bf16_of(rng.normal(scale=0.125, size=(64 * (H + 2 * Hkv), hidden)))).astype(np.float32)
+    c, s = tables64(1e4, 16)
+    base = oracle.attn_varlen_proj(x, bf16_of(w), cu_of(lengths), H, Hkv, -1, False, 0.125, c, s)
+    w2 = w.copy()
+    v1 = 64 * (H + Hkv + 1)
+    w2[v1:v1 + 64] = 0.0
+    out = oracle.attn_varlen_proj(x, bf16_of(w2), cu_of(lengths), H, Hkv, -1, False, 0.125, c, s)
+    G = H // Hkv
+    for h in range(H):
+        blk = slice(h * 64, (h + 1) * 64)
+        if h // G == 1:
+            assert np.all(out[:, blk] == 0.0)
+        else:
+            assert np.array_equal(out[:, blk], base[:, blk])
