@@ -233,6 +233,39 @@ int kime_chunk_step(const void* qkv, const int32_t* cu_seqlens, const int32_t* p
  * an unknown op or malformed sizes. */
 size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads, int kv_heads, int cap);
 
+/* kime_qkv_proj -- the QKV projection of a packed batch, the step before
+ * attention: qkv = x W^T with one fused weight stored [out width, in width],
+ * q rows, then k, then v (kime-cuda 0.0.3 src/plan.rs, Op::Gemm: weight shape
+ * [out.width, a.width]; ffai-argus 0.7.3 src/text.rs, Block::q: the fused
+ * [960, 576] weight of q, k and v).  No bias, no activation.
+ *
+ *  x            device bf16 [total_tokens, hidden], row-major, 16-byte aligned
+ *  w            device bf16 [64*(heads + 2*kv_heads), hidden]
+ *  hidden       a positive multiple of 64
+ *  qkv          device bf16 [total_tokens, 64*(heads + 2*kv_heads)]: each value
+ *               a sum of bf16 products accumulated in FP32 on the tensor cores,
+ *               rounded to bf16 (nearest even)
+ * One launch.  Returns KIME_EINVAL for bad shapes or pointers, KIME_ERANGE for
+ * sizes beyond the library's index range. */
+int kime_qkv_proj(const void* x, const void* w, int total_tokens, int hidden, int heads, int kv_heads,
+                  int head_dim, void* qkv, int32_t* dev_status, void* stream);
+
+/* kime_attn_varlen_proj -- kime_attn_varlen on BF16 qkv rows given by their
+ * projection, qkv = x W^T (as kime_qkv_proj), with the projection fused into
+ * the attention's producer: the projection's epilogue applies RoPE at each
+ * token's position within its sequence, multiplies queries by
+ * scale * log2(e) and rounds q, k and v once to f16 -- the prepared rows the
+ * attention kernel loads -- from the FP32 accumulators, so no bf16 qkv is
+ * written or read.  Arguments as kime_attn_varlen (dtype BF16 implied) plus
+ * x, w and hidden as kime_qkv_proj; the workspace must hold
+ * kime_attn_workspace_bytes(3, ...) bytes (KIME_ERANGE if less).  Launches:
+ * the scheduler, the projection (beside it), the attention kernel.  An f16
+ * operand beyond 65504 sets KIME_DEV_RANGE. */
+int kime_attn_varlen_proj(const void* x, const void* w, const int32_t* cu_seqlens, int n_seqs, int total_tokens,
+                          int hidden, int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal,
+                          float scale, const float* rope_cos, const float* rope_sin, int rope_len, void* out,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
 /* Host helper: float32 cos/sin tables [len, 32] for heads of 64 by kime-cuda's
  * fn rope_tables: inv_i = 1/(float)(theta^(float)(2i/64)) in float32, angle =
  * (float)p * inv_i in float32, cos and sin taken in double and narrowed.

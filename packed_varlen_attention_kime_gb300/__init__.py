@@ -21,6 +21,7 @@ __all__ = [
     "kime_decode_step", "kime_kv_append_varlen", "kime_attn_chunk", "kime_chunk_step",
     "kime_attn_debug_tiles_chunk", "KIME_F32", "KIME_BF16", "KIME_F32_3XTF32", "EXPORTED_SYMBOLS",
     "NOALLOC_SCRATCH_BYTES",
+    "kime_qkv_proj", "kime_attn_varlen_proj",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "kime_attn_varlen", "kime_kv_append", "kime_attn_decode", "kime_attn_workspace_bytes",
     "kime_rope_tables", "kime_attn_debug_tiles", "kime_attn_last_cuda_error", "kime_attn_status_string",
     "kime_attn_varlen_noalloc", "kime_decode_step", "kime_kv_append_varlen", "kime_attn_chunk",
-    "kime_chunk_step", "kime_attn_debug_tiles_chunk",
+    "kime_chunk_step", "kime_attn_debug_tiles_chunk", "kime_qkv_proj", "kime_attn_varlen_proj",
 )
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -81,6 +82,10 @@ def load_library(path: str = LIB_PATH):
     lib.kime_chunk_step.restype = I
     lib.kime_attn_debug_tiles_chunk.argtypes = [P, P, I, I, I, I, I, P, S, P, I, P, P, P]
     lib.kime_attn_debug_tiles_chunk.restype = I
+    lib.kime_qkv_proj.argtypes = [P, P, I, I, I, I, I, P, P, P]
+    lib.kime_qkv_proj.restype = I
+    lib.kime_attn_varlen_proj.argtypes = [P, P, P, I, I, I, I, I, I, I, I, I, F, P, P, I, P, P, S, P, P]
+    lib.kime_attn_varlen_proj.restype = I
     lib.kime_attn_last_cuda_error.argtypes = []
     lib.kime_attn_last_cuda_error.restype = I
     lib.kime_attn_status_string.argtypes = [I]
@@ -162,6 +167,40 @@ def kime_attn_varlen(qkv, cu_seqlens, max_seqlen, heads, kv_heads, window, causa
                               workspace.numel() * workspace.element_size(), _p(dev_status),
                               _stream(stream, qkv.device))
     _check("kime_attn_varlen", rc)
+    return out
+
+
+def kime_qkv_proj(x, w, heads, kv_heads, out=None, dev_status=None, stream=None):
+    """qkv = x w^T (bf16 x [T, hidden], bf16 w [64*(heads+2*kv_heads), hidden]);
+    returns bf16 qkv [T, 64*(heads+2*kv_heads)]."""
+    lib = load_library()
+    T, hidden = x.shape
+    if out is None:
+        out = torch.empty((T, w.shape[0]), dtype=torch.bfloat16, device=x.device)
+    rc = lib.kime_qkv_proj(_p(x), _p(w), T, hidden, heads, kv_heads, 64, _p(out), _p(dev_status),
+                           _stream(stream, x.device))
+    _check("kime_qkv_proj", rc)
+    return out
+
+
+def kime_attn_varlen_proj(x, w, cu_seqlens, max_seqlen, heads, kv_heads, window, causal, scale, rope_cos,
+                          rope_sin, out=None, workspace=None, dev_status=None, stream=None):
+    """Attention over the packed batch whose qkv rows are x w^T, the projection
+    fused into the attention's producer; returns bf16 out [T, heads*64]."""
+    lib = load_library()
+    T, hidden = x.shape
+    n_seqs = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty((T, heads * 64), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        need = kime_attn_workspace_bytes(3, n_seqs, T, heads, kv_heads)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    rc = lib.kime_attn_varlen_proj(_p(x), _p(w), _p(cu_seqlens), n_seqs, T, hidden, int(max_seqlen), heads,
+                                   kv_heads, 64, int(window), int(bool(causal)), float(scale), _p(rope_cos),
+                                   _p(rope_sin), rope_cos.shape[0], _p(out), _p(workspace),
+                                   workspace.numel() * workspace.element_size(), _p(dev_status),
+                                   _stream(stream, x.device))
+    _check("kime_attn_varlen_proj", rc)
     return out
 
 

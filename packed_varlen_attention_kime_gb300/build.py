@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkime_attn.so")
-SOURCES = ["api.cu", "schedule.cu", "varlen_f32.cu", "prefill_tc.cu", "prefill_rows.cu", "prep.cu", "decode.cu", "chunk.cu", "noalloc.cu", "tf32x3.cu"]
+SOURCES = ["api.cu", "schedule.cu", "varlen_f32.cu", "prefill_tc.cu", "prefill_rows.cu", "prep.cu", "proj.cu", "decode.cu", "chunk.cu", "noalloc.cu", "tf32x3.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

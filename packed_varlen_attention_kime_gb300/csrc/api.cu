@@ -56,6 +56,26 @@ int encode_qkv_map(CUtensorMap* map, const void* qkv, int total, int W) {
   return KIME_OK;
 }
 
+// 2-D map over a bf16 row-major matrix [rows, cols]: boxes of 64 columns
+// (128 bytes) x box_rows rows, 128-byte swizzle, elements past the ends read
+// as zero.
+int encode_bf16_map(CUtensorMap* map, const void* base, long long rows, long long cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return KIME_ECUDA;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_cuda_error = static_cast<int>(r);
+    return KIME_ECUDA;
+  }
+  return KIME_OK;
+}
+
 // 2-D map over a RoPE table [rope_len, 32] f32: boxes of 128 rows (the
 // positions of one key tile), 128-byte swizzle, rows past rope_len read as zero.
 int encode_table_map(CUtensorMap* map, const float* table, int rope_len) {
@@ -218,6 +238,62 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
   return cuda_status(kime::launch_prefill_tc(&map, nullptr, nullptr, &cmap, &smap, nullptr, n_seqs, total_tokens,
                                              heads, kv_heads, 0, window, causal, scale, rope_cos, rope_sin, out,
                                              workspace, max_pairs, dev_status, st));
+}
+
+int kime_qkv_proj(const void* x, const void* w, int total_tokens, int hidden, int heads, int kv_heads,
+                  int head_dim, void* qkv, int32_t* dev_status, void* stream) {
+  if (!heads_ok(heads, kv_heads, head_dim) || total_tokens < 0 || hidden <= 0 || hidden % 64 != 0)
+    return KIME_EINVAL;
+  if (total_tokens == 0) return KIME_OK;
+  if (!x || !w || !qkv || !aligned16(x) || !aligned16(w) || !aligned16(qkv)) return KIME_EINVAL;
+  const long long W = 64LL * (heads + 2LL * kv_heads);
+  if (W > (1LL << 30) || static_cast<long long>(total_tokens) * (W > hidden ? W : hidden) > (1LL << 46))
+    return KIME_ERANGE;
+  CUtensorMap xm, wm;
+  int rc;
+  if ((rc = encode_bf16_map(&xm, x, total_tokens, hidden, kime::kBM))) return rc;
+  if ((rc = encode_bf16_map(&wm, w, W, hidden, 192))) return rc;
+  return cuda_status(kime::launch_qkv_proj(&xm, &wm, total_tokens, hidden, heads, kv_heads, nullptr, 0, 1.f,
+                                           nullptr, nullptr, 0, qkv, 1, dev_status,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+int kime_attn_varlen_proj(const void* x, const void* w, const int32_t* cu_seqlens, int n_seqs, int total_tokens,
+                          int hidden, int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal,
+                          float scale, const float* rope_cos, const float* rope_sin, int rope_len, void* out,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (!heads_ok(heads, kv_heads, head_dim) || hidden <= 0 || hidden % 64 != 0) return KIME_EINVAL;
+  if (n_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || rope_len < 0 || window < -1) return KIME_EINVAL;
+  if (!(scale > 0.f) || !isfinite(scale)) return KIME_EINVAL;
+  if (causal != 0 && causal != 1) return KIME_EINVAL;
+  if (n_seqs == 0 || total_tokens == 0) return KIME_OK;
+  if (!x || !w || !cu_seqlens || !rope_cos || !rope_sin || !out || !workspace) return KIME_EINVAL;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(out) || !aligned16(rope_cos) || !aligned16(rope_sin) ||
+      !aligned16(workspace))
+    return KIME_EINVAL;
+  if (max_seqlen > rope_len) return KIME_ERANGE;
+  const long long W = 64LL * (heads + 2LL * kv_heads);
+  if (W > (1LL << 30) || static_cast<long long>(total_tokens) * (W > hidden ? W : hidden) > (1LL << 46))
+    return KIME_ERANGE;
+  if (workspace_bytes < prep_ws_bytes(n_seqs, total_tokens, heads, kv_heads)) return KIME_ERANGE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int max_pairs = kime::max_pairs_for(n_seqs, total_tokens);
+  void* rows = static_cast<char*>(workspace) + prep_offset(n_seqs, total_tokens);
+  CUtensorMap xm, wm, pmap;
+  int rc;
+  if ((rc = encode_bf16_map(&xm, x, total_tokens, hidden, kime::kBM))) return rc;
+  if ((rc = encode_bf16_map(&wm, w, W, hidden, 192))) return rc;
+  if ((rc = encode_qkv_map(&pmap, rows, total_tokens, static_cast<int>(W)))) return rc;
+  // scheduler, then the projection writing the prepared rows beside it, then
+  // the attention kernel over them
+  if ((rc = cuda_status(kime::launch_schedule(cu_seqlens, nullptr, n_seqs, total_tokens, max_seqlen, causal,
+                                              window, 0, 0, workspace, max_pairs, dev_status, st))))
+    return rc;
+  if ((rc = cuda_status(kime::launch_qkv_proj(&xm, &wm, total_tokens, hidden, heads, kv_heads, cu_seqlens, n_seqs,
+                                              scale, rope_cos, rope_sin, rope_len, rows, 0, dev_status, st))))
+    return rc;
+  return cuda_status(kime::launch_prefill_rows(&pmap, heads, kv_heads, window, causal, out, workspace, max_pairs,
+                                               dev_status, st));
 }
 
 int kime_kv_append(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim,

@@ -138,6 +138,16 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
 // columns, 128-byte swizzle); the work list is the scheduler's in ws.
 cudaError_t launch_prefill_rows(const CUtensorMap* rows_map, int heads, int kv_heads, int window, int causal,
                                 void* out, void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
+// The QKV projection qkv = x W^T (proj.cu): x_map over x [T, hidden] bf16
+// (boxes of 64 columns x 128 rows), w_map over W [64 (heads + 2 kv_heads),
+// hidden] bf16 (boxes of 64 columns x 192 rows), both with 128-byte swizzle;
+// hidden a multiple of 64.  mode 0 writes the prepared rows (as
+// launch_qkv_prep does from bf16 qkv: RoPE at the positions cu gives, q times
+// scale * log2(e), f16), mode 1 the bf16 qkv rows (cu, tables unused).
+cudaError_t launch_qkv_proj(const CUtensorMap* x_map, const CUtensorMap* w_map, int T, int hidden, int heads,
+                            int kv_heads, const int32_t* cu, int n_seqs, float scale, const float* cos_t,
+                            const float* sin_t, int rope_len, void* out, int mode, int32_t* dev_status,
+                            cudaStream_t st);
 // A packed batch's qkv rows prepared for the attention kernel (prep.cu):
 // queries rotated at their positions and scaled by scale * log2(e), keys
 // rotated, all rounded to f16, values widened to f16; out [total, W] f16.

@@ -17,6 +17,10 @@ Workloads (head_dim 64 throughout):
   smollm2_chunk     chunked prefill: 32 seqs, 9 q / 3 kv heads, caches
                     [32,3,8192,64] N(0,1), chunks L~U[128,1024] of BF16 N(0,1)
                     rows at used lengths pos~U[0,8192-L], theta 1e5, scale 1/8
+  smollm2_proj      the SmolLM2 prefill from the layer's input: 16 x 1142 token
+                    rows x of hidden 576, BF16 N(0,1); one fused q/k/v weight
+                    [960, 576] BF16 N(0, 1/576), its q rows x 1/8 (pre-scaled at
+                    load); 9 q / 3 kv heads, theta 1e5, causal, scale 1
 """
 from __future__ import annotations
 
@@ -156,6 +160,51 @@ def decode_case(n_seqs: int = 128, cap: int = 8192, heads: int = 9, kv_heads: in
         k[s] = torch.randn((kv_heads, cap, 64), generator=gv, dtype=torch.float32, device=device)
         v[s] = torch.randn((kv_heads, cap, 64), generator=gv, dtype=torch.float32, device=device)
     return DecodeCase("smollm2_decode", pos, qkv_new, k, v, heads, kv_heads, cap, 1e5, 0.125)
+
+
+@dataclass
+class ProjCase:
+    name: str
+    lengths: list
+    cu_seqlens: torch.Tensor  # int32 [n+1]
+    x: torch.Tensor           # bf16 [T, hidden]
+    w: torch.Tensor           # bf16 [64*(H+2Hkv), hidden]: q rows, k rows, v rows
+    heads: int
+    kv_heads: int
+    theta: float
+    window: int
+    causal: bool
+    scale: float
+
+    @property
+    def total(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def max_seqlen(self) -> int:
+        return max(self.lengths) if self.lengths else 0
+
+
+def random_proj(lengths, hidden, heads, kv_heads, seed, device="cpu", q_scale=None):
+    """x [T, hidden] bf16 N(0,1) and a weight [64*(H+2Hkv), hidden] bf16
+    N(0, 1/hidden) (projections of unit variance), q rows optionally scaled."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    T = sum(int(v) for v in lengths)
+    x = torch.randn((T, hidden), generator=g, dtype=torch.float32, device=device).to(torch.bfloat16)
+    w = torch.randn((64 * (heads + 2 * kv_heads), hidden), generator=g, dtype=torch.float32, device=device)
+    w = w * (1.0 / hidden) ** 0.5
+    if q_scale is not None:
+        w[: heads * 64] *= q_scale
+    return x, w.to(torch.bfloat16)
+
+
+def proj_case(name: str = "smollm2_proj", device: str = "cpu") -> ProjCase:
+    """The projection-fed SmolLM2 prefill workload."""
+    if name != "smollm2_proj":
+        raise KeyError(name)
+    lengths = [1142] * 16
+    x, w = random_proj(lengths, 576, 9, 3, 8 * 1000 + 7, device=device, q_scale=0.125)
+    return ProjCase(name, lengths, cu_from_lengths(lengths), x, w, 9, 3, 1e5, -1, True, 1.0)
 
 
 def bf16_bits(t: torch.Tensor):
