@@ -1,18 +1,22 @@
 """Benchmark of the packed-varlen attention hot path on GB300.
 
-One step = the attention of one ModernBERT-base-shaped encoder layer pair over
-one packed batch (64 sequences, lengths U[32,512], 12 heads x 64, BF16 qkv
-N(0, 1.5^2)): the local layer (window 64, RoPE theta 1e4) then the global
-layer (full, theta 1.6e5), each one kime_attn_varlen call (device scheduler +
-tcgen05 attention kernel).  Inputs are resident in HBM before the timed region
-and L2 is flushed before every timed step (a 512 MB write, then a 256 MB read
-that leaves only clean lines in L2).
+One step = the attention of one ModernBERT-large-shaped encoder layer pair
+over one packed batch (8 sequences, lengths U[1024,8192], ~38.7k tokens, 16
+heads x 64, BF16 qkv N(0, 1.5^2)): the local layer (window 64, RoPE theta
+1e4) then the global layer (full, theta 1.6e5), each one kime_attn_varlen
+call (device scheduler, row preparation, tcgen05 attention kernel).  Inputs
+are resident in HBM before the timed region and L2 is flushed before every
+timed step (a 512 MB write, then a 256 MB read that leaves only clean lines in
+L2).
 
-The same run also times, outside the headline number: ModernBERT-large-shaped
-layers (8 x U[1024,8192]), SmolLM2-shaped causal GQA prefill (16 x 1142) and
-the SmolLM2-shaped decode step (KV append + split-KV decode, 128 sequences,
-cache 8192) -- the "extra" object -- and the FP64 CPU oracle on a bounded
-sample of the headline workload (cpu_baseline).
+The same run also times, outside the headline number, each as the median of
+200 flushed repetitions after 20 warm-ups: ModernBERT-base-shaped layers (64 x
+U[32,512], the HBM-bound workload), SmolLM2-shaped causal GQA prefill (16 x
+1142), the same prefill fed by its QKV projection (fused into the attention
+producer, and projection-then-attend), the SmolLM2-shaped decode step (KV
+append + split-KV decode, 128 sequences, cache 8192), chunked prefill, and
+the FP32-qkv paths -- the "extra" object -- and the FP64 CPU oracle on a
+bounded sample of the headline workload (cpu_baseline).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extra]
 
@@ -38,21 +42,29 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = ("packed-varlen attention tokens/s & TFLOP/s (% BF16 peak); decode GB/s (% HBM) at 1 GB300")
+HEADLINE = "modernbert_large"  # the largest single-GPU configuration: 8 x U[1024,8192] tokens, 16 heads
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) of one attention-kernel launch (prefill_tc_kernel
-# on prepared rows) of the ModernBERT-base global layer, from one ncu capture
-# (profiles/prefill_tc_modernbert_base_global.md), keyed by the SHA-1 of the
-# kernel source it was taken on: any change to the kernel makes the figure
-# stale, and the bench then reports null.
-MEASURED_TRAFFIC = {"7796c0db5bf582c4cbe5ba9e78afeade88a082c6": 106347776}
+# DRAM bytes (read + write) of one kime_attn_varlen call -- the sum over its
+# kernels (scheduler, row preparation, attention kernel over prepared rows),
+# from one ncu capture of each workload's layer (profiles/), keyed by the
+# SHA-1 of those kernels' sources together: any change to them makes the
+# figure stale, and the bench then reports null.
+MEASURED_TRAFFIC = {}
+TRAFFIC_SOURCES = ("schedule.cu", "prep.cu", "prefill_rows.cu")
 
 
-def measured_traffic():
+def traffic_key():
     import hashlib
-    src = os.path.join(ROOT, "packed_varlen_attention_kime_gb300", "csrc", "prefill_tc.cu")
-    with open(src, "rb") as f:
-        return MEASURED_TRAFFIC.get(hashlib.sha1(f.read()).hexdigest())
+    h = hashlib.sha1()
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "packed_varlen_attention_kime_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload):
+    return MEASURED_TRAFFIC.get((traffic_key(), workload))
 
 
 # ---- helpers ---------------------------------------------------------------------
@@ -299,6 +311,47 @@ class ChunkRun:
                                   dev_status=dev_status(self.dev))
 
 
+class ProjRun:
+    """The SmolLM2 prefill fed by its QKV projection (x [T, 576], fused weight
+    [960, 576]): fused (kime_attn_varlen_proj: the projection writes the
+    prepared rows), projection then attend (kime_qkv_proj writing bf16 qkv,
+    then kime_attn_varlen), and the projection alone."""
+
+    def __init__(self, dev):
+        import packed_varlen_attention_kime_gb300 as kime
+        from packed_varlen_attention_kime_gb300.inputs import proj_case
+        self.kime = kime
+        c = self.case = proj_case(device=str(dev))
+        self.dev = dev
+        self.cu = c.cu_seqlens.to(dev)
+        cs, sn = kime.kime_rope_tables(c.theta, c.max_seqlen)
+        self.cs, self.sn = cs.to(dev), sn.to(dev)
+        W = c.w.shape[0]
+        self.qkv = torch.empty((c.total, W), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((c.total, c.heads * 64), dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(kime.kime_attn_workspace_bytes(3, len(c.lengths), c.total, c.heads, c.kv_heads),
+                              dtype=torch.uint8, device=dev)
+        self.gemm_flops = 2 * c.total * c.x.shape[1] * W
+        self.attn_flops = 4 * 64 * c.heads * visible_pairs(c.lengths, c.window, c.causal)
+
+    def fused(self):
+        c = self.case
+        self.kime.kime_attn_varlen_proj(c.x, c.w, self.cu, c.max_seqlen, c.heads, c.kv_heads, c.window, c.causal,
+                                        c.scale, self.cs, self.sn, out=self.out, workspace=self.ws,
+                                        dev_status=dev_status(self.dev))
+
+    def proj(self):
+        c = self.case
+        self.kime.kime_qkv_proj(c.x, c.w, c.heads, c.kv_heads, out=self.qkv, dev_status=dev_status(self.dev))
+
+    def unfused(self):
+        c = self.case
+        self.proj()
+        self.kime.kime_attn_varlen(self.qkv, self.cu, c.max_seqlen, c.heads, c.kv_heads, c.window, c.causal,
+                                   c.scale, self.cs, self.sn, out=self.out, workspace=self.ws,
+                                   dev_status=dev_status(self.dev))
+
+
 def time_fn(fn, n, warmup, flush, stream, events=1):
     """Median and mean ms of fn over n calls, L2 flushed before each; fn gets
     the list of events to record its sub-steps (len events+1)."""
@@ -319,9 +372,20 @@ def time_fn(fn, n, warmup, flush, stream, events=1):
     return per, subs
 
 
-def extra_measurements(dev, flush, stream, pk, reps=10):
+def layer_figures(r, k, ms, pk):
+    """Throughput and roofline fractions of layer k of a VarlenRun taking ms."""
+    tf = r.flops[k] / (ms * 1e-3) / 1e12
+    gbs = r.bytes_per_layer / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 4), "tflops": round(tf, 2), "gbs": round(gbs, 1),
+            "tc_frac": round(tf / pk["bf16_tflops"], 4), "hbm_frac": round(gbs / pk["hbm_gbs"], 4),
+            "roof_frac": round(max(r.flops[k] / (pk["bf16_tflops"] * 1e12),
+                                   r.bytes_per_layer / (pk["hbm_gbs"] * 1e9)) / (ms * 1e-3), 4)}
+
+
+def extra_measurements(dev, flush, stream, pk, reps=200, warmup=20):
+    """The other workloads: medians of `reps` flushed repetitions."""
     out = {}
-    for name in ("modernbert_large", "smollm2_prefill"):
+    for name in ("modernbert_base", "smollm2_prefill"):
         r = VarlenRun(name, dev)
         nl = len(r.case.layers)
 
@@ -330,22 +394,38 @@ def extra_measurements(dev, flush, stream, pk, reps=10):
                 r.layer(k)
                 if ev is not None and k + 1 < nl:
                     ev[k + 1].record(stream)
-        per, subs = time_fn(f, reps, 3, flush, stream, events=nl)
-        layers = {}
-        for k, lay in enumerate(r.case.layers):
-            ms = statistics.median([s[k] for s in subs])
-            tf = r.flops[k] / (ms * 1e-3) / 1e12
-            gbs = r.bytes_per_layer / (ms * 1e-3) / 1e9
-            layers[lay.name] = {"ms": round(ms, 4), "tflops": round(tf, 2), "gbs": round(gbs, 1),
-                                "tc_frac": round(tf / pk["bf16_tflops"], 4), "hbm_frac": round(gbs / pk["hbm_gbs"], 4),
-                                "roof_frac": round(max(r.flops[k] / (pk["bf16_tflops"] * 1e12),
-                                                       r.bytes_per_layer / (pk["hbm_gbs"] * 1e9)) / (ms * 1e-3), 4)}
+        per, subs = time_fn(f, reps, warmup, flush, stream, events=nl)
+        layers = {lay.name: layer_figures(r, k, statistics.median([s[k] for s in subs]), pk)
+                  for k, lay in enumerate(r.case.layers)}
         out[name] = {"tokens": r.case.total, "tokens_per_s": round(r.case.total / (statistics.median(per) * 1e-3)),
                      "layers": layers}
+        if name == "modernbert_base":
+            k = [lay.name for lay in r.case.layers].index("global")
+            ms = layers["global"]["ms"]
+            ach = r.bytes_per_layer / (ms * 1e-3) / 1e9
+            out[name]["roofline"] = {
+                "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": measured_traffic("modernbert_base:global"),
+                "kernel": "kime_attn_varlen call, global layer: schedule_kernel + qkv_prep_kernel + "
+                          "prefill_rows_kernel; traffic summed over the three",
+                "algorithmic_bytes": r.bytes_per_layer, "avg_ms": ms}
         del r
         torch.cuda.empty_cache()
+    pr = ProjRun(dev)
+    row = {}
+    for key, fn in (("fused", pr.fused), ("unfused", pr.unfused), ("proj", pr.proj)):
+        per, _ = time_fn(lambda ev, fn=fn: fn(), reps, warmup, flush, stream)
+        row[key + "_ms"] = round(statistics.median(per), 4)
+    row["proj_tflops"] = round(pr.gemm_flops / (row["proj_ms"] * 1e-3) / 1e12, 1)
+    row["fused_tokens_per_s"] = round(pr.case.total / (row["fused_ms"] * 1e-3))
+    row["unfused_tokens_per_s"] = round(pr.case.total / (row["unfused_ms"] * 1e-3))
+    row["gemm_flops"] = pr.gemm_flops
+    row["attn_flops"] = pr.attn_flops
+    out["smollm2_proj"] = row
+    del pr
+    torch.cuda.empty_cache()
     d = DecodeRun(dev)
-    per, _ = time_fn(lambda ev: d.step(), reps, 3, flush, stream)
+    per, _ = time_fn(lambda ev: d.step(), reps, warmup, flush, stream)
     ms = statistics.median(per)
     gbs = d.bytes / (ms * 1e-3) / 1e9
     out["smollm2_decode"] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "hbm_frac": round(gbs / pk["hbm_gbs"], 4),
@@ -353,7 +433,7 @@ def extra_measurements(dev, flush, stream, pk, reps=10):
     del d
     torch.cuda.empty_cache()
     ch = ChunkRun(dev)
-    per, _ = time_fn(lambda ev: ch.step(), reps, 3, flush, stream)
+    per, _ = time_fn(lambda ev: ch.step(), reps, warmup, flush, stream)
     ms = statistics.median(per)
     tf = ch.flops / (ms * 1e-3) / 1e12
     out["smollm2_chunk"] = {"ms": round(ms, 4), "tflops": round(tf, 2), "tc_frac": round(tf / pk["bf16_tflops"], 4),
@@ -371,7 +451,8 @@ def extra_measurements(dev, flush, stream, pk, reps=10):
     for k, lay in enumerate(fr.case.layers):
         row = {}
         for prec, key in ((None, "simt"), ("3xtf32", "3xtf32")):
-            per, _ = time_fn(lambda ev, k=k, prec=prec: fr.layer(k, prec), reps, 3, flush, stream)
+            n = reps if prec else max(reps // 4, 20)  # the CUDA-core path takes ~2 ms a call
+            per, _ = time_fn(lambda ev, k=k, prec=prec: fr.layer(k, prec), n, warmup, flush, stream)
             ms = statistics.median(per)
             row[key + "_ms"] = round(ms, 4)
             row[key + "_tflops"] = round(fr.flops[k] / (ms * 1e-3) / 1e12, 2)
@@ -386,9 +467,10 @@ def extra_measurements(dev, flush, stream, pk, reps=10):
 
 # ---- CPU oracle leg ----------------------------------------------------------------
 
-def oracle_sample_rate(case, budget_s=15.0):
-    """Oracle throughput (tokens/s over the layer pair) on whole sequences of the
-    workload, taken in order until about budget_s of CPU work is done."""
+def oracle_sample_rate(case, budget_s=15.0, prefix=1024):
+    """Oracle throughput (tokens/s over the layer pair) on the first `prefix`
+    tokens of the workload's sequences (each a sequence of its own), taken in
+    order until about budget_s of CPU work is done."""
     import oracle
     from packed_varlen_attention_kime_gb300.inputs import bf16_bits, cu_from_lengths
     oracle.build()
@@ -401,7 +483,8 @@ def oracle_sample_rate(case, budget_s=15.0):
     tokens, spent, nseq = 0, 0.0, 0
     cu = case.cu_seqlens.numpy()
     while nseq < len(case.lengths) and spent < budget_s:
-        a, b = int(cu[nseq]), int(cu[nseq + 1])
+        a = int(cu[nseq])
+        b = min(int(cu[nseq + 1]), a + prefix)
         sub_cu = cu_from_lengths([b - a]).numpy()
         t0 = time.perf_counter()
         for lay in case.layers:
@@ -411,7 +494,8 @@ def oracle_sample_rate(case, budget_s=15.0):
         spent += time.perf_counter() - t0
         tokens += b - a
         nseq += 1
-    return tokens / spent, cores, f"first {nseq} of {len(case.lengths)} sequences ({tokens} tokens), both layers"
+    return tokens / spent, cores, (f"the first {prefix} tokens of each of the first {nseq} of {len(case.lengths)} "
+                                    f"sequences ({tokens} tokens), both layers")
 
 
 def oracle_single_core():
@@ -545,6 +629,7 @@ def main():
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s load before the timed steps")
     ap.add_argument("--only", default=None,
                     help="profiling aid: run only WORKLOAD[:LAYER] (modernbert_base, modernbert_large, "
+                         "smollm2_proj[:fused|unfused|proj], "
                          "smollm2_prefill, smollm2_decode, smollm2_chunk) for --steps steps and print its timings")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -568,7 +653,7 @@ def main():
     pk, pk_src = peaks()
     stream = torch.cuda.current_stream(dev)
     flush = l2_flush_buffer(dev)
-    run = VarlenRun("modernbert_base", dev)
+    run = VarlenRun(HEADLINE, dev)
     c = run.case
 
     def step(ev):
@@ -594,17 +679,23 @@ def main():
     ms_step = total_ms / args.steps
     value = world * c.total * args.steps / (total_ms * 1e-3)
 
-    # roofline of the dominant call (the global layer: scheduler, row preparation, attention kernel)
-    g_ms = statistics.mean(s[1] for s in subs)
-    l_ms = statistics.mean(s[0] for s in subs)
-    g_bytes = run.bytes_per_layer
-    achieved = g_bytes / (g_ms * 1e-3) / 1e9
-    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-            "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": measured_traffic(),
-            "kernel": "kime_attn_varlen, ModernBERT-base global layer: schedule_kernel + qkv_prep_kernel + "
-                      "prefill_tc_kernel (shares in profiles/launches_modernbert_base_layer_pair.md); avg_ms is "
-                      "the whole call, traffic the attention kernel's DRAM bytes",
-            "algorithmic_bytes": g_bytes, "avg_ms": round(g_ms, 5), "peak_source": pk_src}
+    # roofline of the dominant call, the global layer (tensor-bound): its
+    # useful FLOPs over the whole call's time (scheduler, row preparation and
+    # attention kernel; the attention kernel is most of it, see the launch
+    # list in profiles/), against the burst BF16 peak (the call is timed alone
+    # between L2 flushes)
+    gk = [lay.name for lay in c.layers].index("global")
+    lk = [lay.name for lay in c.layers].index("local")
+    g_ms = statistics.mean(s[gk] for s in subs)
+    l_ms = statistics.mean(s[lk] for s in subs)
+    achieved = run.flops[gk] / (g_ms * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(achieved / pk["bf16_tflops"], 4),
+            "traffic": measured_traffic(f"{HEADLINE}:global"),
+            "kernel": "kime_attn_varlen call, ModernBERT-large global layer: schedule_kernel + qkv_prep_kernel + "
+                      "prefill_rows_kernel; avg_ms is the whole call, traffic the DRAM bytes of all three",
+            "algorithmic_flops": run.flops[gk], "algorithmic_bytes": run.bytes_per_layer,
+            "avg_ms": round(g_ms, 5), "peak_source": f"{pk_src} (burst)"}
     flops_step = sum(run.flops)
     tflops = flops_step / (ms_step * 1e-3) / 1e12
 
@@ -645,7 +736,7 @@ def main():
             "metric": METRIC, "value": round(value), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "modernbert_base local+global layer pair", "seqs": len(c.lengths),
+            "config": {"workload": "modernbert_large local+global layer pair", "seqs": len(c.lengths),
                        "tokens": c.total, "heads": c.heads, "head_dim": 64,
                        "layers": ["local window 64 theta 1e4", "global full theta 1.6e5"],
                        "l2": "flushed before every timed step: 512 MB write, then a 256 MB read so the lines "
@@ -674,6 +765,13 @@ def only_arm(args, local):
         per, _ = time_fn(lambda ev: d.step(), args.steps, args.warmup, flush, stream)
         check_status(dev)
         print(json.dumps({"only": name, "ms": [round(x, 4) for x in per]}))
+        return
+    if name == "smollm2_proj":  # fused (default), unfused, or the projection alone
+        pr = ProjRun(dev)
+        fn = {"": pr.fused, "fused": pr.fused, "unfused": pr.unfused, "proj": pr.proj}[layer]
+        per, _ = time_fn(lambda ev: fn(), args.steps, args.warmup, flush, stream)
+        check_status(dev)
+        print(json.dumps({"only": args.only, "ms": [round(x, 4) for x in per]}))
         return
     if name == "modernbert_base_fp32":  # the 3xTF32 path
         fr = Fp32Run(dev)
@@ -719,7 +817,7 @@ def reference_arm(args, rank, world):
     import oracle
     from packed_varlen_attention_kime_gb300.inputs import bf16_bits, cu_from_lengths, varlen_case
     oracle.build()
-    case = varlen_case("modernbert_base")
+    case = varlen_case(HEADLINE)
     x = bf16_bits(case.qkv)
     cores = os.cpu_count() or 1
     tabs = {}
@@ -727,9 +825,9 @@ def reference_arm(args, rank, world):
         cs, sn = oracle.rope_tables_f32(lay.theta, case.max_seqlen)
         tabs[lay.theta] = (cs.astype(np.float64), sn.astype(np.float64))
     cu = case.cu_seqlens.numpy()
-    # one step: the two shortest-index sequences' worth of rows, both layers
-    a, b = int(cu[0]), int(cu[2])
-    sub_cu = cu_from_lengths(case.lengths[:2]).numpy()
+    # one step: the first 512 tokens of sequence 0 as a sequence of their own, both layers
+    a, b = int(cu[0]), int(cu[0]) + 512
+    sub_cu = cu_from_lengths([512]).numpy()
 
     def step():
         for lay in case.layers:
@@ -747,10 +845,11 @@ def reference_arm(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": "modernbert_base local+global layer pair",
-                       "sample": f"sequences 0-1 ({b - a} tokens) of 64, both layers, per step"},
+            "config": {"workload": "modernbert_large local+global layer pair",
+                       "sample": f"the first {b - a} tokens of sequence 0 of {len(case.lengths)}, both layers, "
+                                 "per step"},
             "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"sequences 0-1 ({b - a} tokens), both layers, per step"},
+                             "sample": f"the first {b - a} tokens of sequence 0, both layers, per step"},
             "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     if world > 1:
