@@ -24,7 +24,7 @@
 // CTA = 192 threads, persistent over output tiles of 128 token rows x 3 heads
 // (the last column tile of a row may hold fewer heads):
 //   warps 0..3  epilogue: thread r owns row r of the tile (TMEM lane r)
-//   warp 4      TMA producer: x and W slabs of 64 hidden columns, 4 stages
+//   warp 4      TMA producer: x and W slabs of 64 hidden columns, 5 stages
 //   warp 5      MMA issuer (one thread)
 // TMEM holds two accumulators of 192 columns, so the epilogue of one tile
 // runs while the MMAs of the next accumulate.  Every wait is bounded in time.
@@ -35,13 +35,15 @@ namespace kime {
 namespace {
 
 constexpr int kPThreads = 192;
-constexpr int kPStages = 4;
+constexpr int kPStages = 5;
 constexpr int kNH = 3;                          // heads per column tile
 constexpr uint32_t kATile = kBM * 64 * 2;       // 16 KB: 128 token rows x 64 hidden (bf16)
 constexpr uint32_t kBTile = kNH * 64 * 64 * 2;  // 24 KB: 192 weight rows x 64 hidden
 constexpr uint32_t kStageBytes = kATile + kBTile;
 constexpr uint32_t kPBar = kPStages * kStageBytes;
-constexpr uint32_t kPSmem = kPBar + 256 + 1024;  // + barriers, alignment slack
+constexpr int kCuSmem = 4096;                     // cu_seqlens entries kept in shared memory
+constexpr uint32_t kPCu = kPBar + 256;
+constexpr uint32_t kPSmem = kPCu + kCuSmem * 4 + 1024;  // + barriers, cu_seqlens, alignment slack
 static_assert(kPSmem <= 232448, "shared memory per CTA");
 constexpr uint32_t kAccCols = kNH * 64;          // one accumulator
 constexpr uint32_t kPTmemCols = 512;             // two accumulators (384) rounded to a power of two
@@ -76,6 +78,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
   const int n_rt = (p.T + kBM - 1) / kBM, n_ct = (n_heads + kNH - 1) / kNH;
   const int n_tiles = n_rt * n_ct, ksl = p.hidden / 64;
 
+  // the epilogue's binary searches for token positions read cu_seqlens from
+  // shared memory when it fits (a global-memory search costs a dependent
+  // L2 round trip per step, per row, per tile)
+  int32_t* cu_s = reinterpret_cast<int32_t*>(smem + kPCu);
+  const bool cu_in_smem = p.mode == 0 && p.n_seqs + 1 <= kCuSmem;
+  if (cu_in_smem)
+    for (int k = tid; k <= p.n_seqs; k += kPThreads) cu_s[k] = __ldg(p.cu + k);
   if (tid == 0) {
     tma_prefetch_map(&x_map);
     tma_prefetch_map(&w_map);
@@ -177,14 +186,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
       // the token's position within its own sequence: the largest s with cu[s] <= row
       int pos = -1;
       if (p.mode == 0 && row < p.T) {
+        const int32_t* cu = cu_in_smem ? cu_s : p.cu;
         int lo = 0, hi = p.n_seqs - 1;
         while (lo < hi) {
           const int mid = (lo + hi + 1) >> 1;
-          if (__ldg(p.cu + mid) <= row) lo = mid;
+          if (cu[mid] <= row) lo = mid;
           else hi = mid - 1;
         }
-        pos = row - __ldg(p.cu + lo);
+        pos = row - cu[lo];
         if (pos >= p.rope_len) pos = -1;  // a row of no valid sequence: converted without rotation
+      }
+      // the row's table entries, loaded once for the tile's rotated heads and
+      // before the wait, so the loads overlap the tile's MMAs
+      float4 ct4[8], st4[8];
+      const bool any_rot = p.mode == 0 && pos >= 0 && ct * kNH < p.heads + p.kv_heads;
+      if (any_rot) {
+        const float4* cr = reinterpret_cast<const float4*>(p.cos_t + static_cast<size_t>(pos) * kHalf);
+        const float4* sr = reinterpret_cast<const float4*>(p.sin_t + static_cast<size_t>(pos) * kHalf);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          ct4[q] = __ldg(cr + q);
+          st4[q] = __ldg(sr + q);
+        }
       }
       const uint32_t acc = i & 1;
       bool ok = wait(&sh->acc_full[acc], (i >> 1) & 1);
@@ -209,11 +232,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const bool rotate = gh < p.heads + p.kv_heads && pos >= 0;
         if (rotate) {
           const float mul = gh < p.heads ? p.qmul : 1.f;
-          const float4* cr = reinterpret_cast<const float4*>(p.cos_t + static_cast<size_t>(pos) * kHalf);
-          const float4* sr = reinterpret_cast<const float4*>(p.sin_t + static_cast<size_t>(pos) * kHalf);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const float4 c4 = __ldg(cr + q), s4 = __ldg(sr + q);
+            const float4 c4 = ct4[q], s4 = st4[q];
             const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ss[4] = {s4.x, s4.y, s4.z, s4.w};
             float lo2[4], hi2[4];
 #pragma unroll

@@ -84,21 +84,29 @@ __global__ void __launch_bounds__(kSchedThreads)
     if (n_seqs > 0 && (cu[0] != 0 || cu[n_seqs] != total)) s_bad = ST_BAD_CU;
   }
   __syncthreads();
+  // Work split: one thread per sequence, or -- when sequences are long on
+  // average (few sequences of many tiles) -- one warp per sequence with its
+  // lanes taking the tiles.
+  const bool by_warp = n_seqs > 0 && total / n_seqs > 8 * kBM;
+  const int lane = threadIdx.x & 31;
+  const int s0 = by_warp ? static_cast<int>(threadIdx.x >> 5) : static_cast<int>(threadIdx.x);
+  const int ds = by_warp ? static_cast<int>(blockDim.x >> 5) : static_cast<int>(blockDim.x);
+  const int t0 = by_warp ? lane : 0, dt = by_warp ? 32 : 1;
   // Pass 1: validate each sequence and histogram its tiles and duos by cost.
-  for (int s = threadIdx.x; s < n_seqs; s += blockDim.x) {
+  for (int s = s0; s < n_seqs; s += ds) {
     int off;
     const int bad = check_seq(cu, pos, s, total, max_seqlen, cap, rope_len, off);
     if (bad) {
-      atomicOr(&s_bad, bad);
+      if (t0 == 0) atomicOr(&s_bad, bad);
       continue;
     }
     const int a = cu[s], L = cu[s + 1] - a;
-    for (int qt = 0; qt * kBM < L; ++qt) {
+    for (int qt = t0; qt * kBM < L; qt += dt) {
       int kb, ke, fb, fe;
       tile_ranges(L, off + L, off, qt, causal, window, kb, ke, fb, fe);
       atomicAdd(&hist[0][bucket_of(kb, ke)], 1);
     }
-    for (int qp = 0; 2 * qp * kBM < L; ++qp) {
+    for (int qp = t0; 2 * qp * kBM < L; qp += dt) {
       int cost;
       make_duo(s, qp, a, L, off, causal, window, cost);
       atomicAdd(&hist[1][bucket_of(0, cost)], 1);
@@ -108,7 +116,7 @@ __global__ void __launch_bounds__(kSchedThreads)
   if (threadIdx.x < 64) {
     // exclusive prefix sums of the two histograms, one warp each: lane j
     // holds buckets 8j .. 8j+7, a warp scan adds the lanes' totals
-    const int k = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k = threadIdx.x >> 5;
     constexpr int kPer = kBuckets / 32;
     int local[kPer], sum = 0;
 #pragma unroll
@@ -138,17 +146,17 @@ __global__ void __launch_bounds__(kSchedThreads)
   }
   __syncthreads();
   // Pass 2: scatter tiles and duos into cost order (longest first).
-  for (int s = threadIdx.x; s < n_seqs; s += blockDim.x) {
+  for (int s = s0; s < n_seqs; s += ds) {
     int off;
     if (check_seq(cu, pos, s, total, max_seqlen, cap, rope_len, off)) continue;
     const int a = cu[s], L = cu[s + 1] - a;
-    for (int qt = 0; qt * kBM < L; ++qt) {
+    for (int qt = t0; qt * kBM < L; qt += dt) {
       int kb, ke, fb, fe;
       tile_ranges(L, off + L, off, qt, causal, window, kb, ke, fb, fe);
       const int at = atomicAdd(&cursor[0][bucket_of(kb, ke)], 1);
       if (at < max_pairs) pairs[at] = Pair{s, qt, kb, ke, fb, fe, a, L};
     }
-    for (int qp = 0; 2 * qp * kBM < L; ++qp) {
+    for (int qp = t0; 2 * qp * kBM < L; qp += dt) {
       int cost;
       const Duo d = make_duo(s, qp, a, L, off, causal, window, cost);
       const int at = atomicAdd(&cursor[1][bucket_of(0, cost)], 1);

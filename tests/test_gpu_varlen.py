@@ -56,6 +56,10 @@ def test_schedule_small_shapes_bit_exact(cuda_lib, causal):
     total = int(cu[-1])
     for w in WINDOWS + [127, 128, 2000]:
         assert_tiles_equal(cu, total, 1000, causal, w)
+    # few long sequences (the scheduler then gives each sequence a warp)
+    cu = cu_from_lengths([3000, 1, 5000, 4097, 0])
+    for w in WINDOWS + [2000, 6000]:
+        assert_tiles_equal(cu, int(cu[-1]), 5000, causal, w)
 
 
 @pytest.mark.parametrize("name", ["modernbert_base", "modernbert_large", "smollm2_prefill"])
