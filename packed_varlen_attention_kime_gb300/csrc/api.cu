@@ -235,9 +235,9 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
   if (prep)
     return cuda_status(kime::launch_prefill_rows(&pmap, heads, kv_heads, window, causal, out, workspace, max_pairs,
                                                  dev_status, st));
-  return cuda_status(kime::launch_prefill_tc(&map, nullptr, nullptr, &cmap, &smap, nullptr, n_seqs, total_tokens,
-                                             heads, kv_heads, 0, window, causal, scale, rope_cos, rope_sin, out,
-                                             workspace, max_pairs, dev_status, st));
+  return cuda_status(kime::launch_prefill_tc(&map, nullptr, nullptr, &cmap, &smap, heads, kv_heads, 0, window,
+                                             causal, scale, rope_cos, rope_sin, out, workspace, max_pairs,
+                                             dev_status, st));
 }
 
 int kime_qkv_proj(const void* x, const void* w, int total_tokens, int hidden, int heads, int kv_heads,
@@ -342,8 +342,7 @@ int chunk_attend(const void* qkv, const int32_t* cu, const int32_t* pos, int n_s
   if ((rc = encode_qkv_map(&qmap, qkv, total, W))) return rc;
   if ((rc = encode_qkv_map(&kmap, k_cache, rows, kime::kHead))) return rc;
   if ((rc = encode_qkv_map(&vmap, v_cache, rows, kime::kHead))) return rc;
-  return cuda_status(kime::launch_prefill_tc(&qmap, &kmap, &vmap, nullptr, nullptr, nullptr, n_seqs, total, heads, kv_heads,
-                                             cap, -1, 1, scale,
+  return cuda_status(kime::launch_prefill_tc(&qmap, &kmap, &vmap, nullptr, nullptr, heads, kv_heads, cap, -1, 1, scale,
                                              rope_cos, rope_sin, out, workspace, max_pairs, dev_status, st));
 }
 

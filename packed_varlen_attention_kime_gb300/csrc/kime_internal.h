@@ -120,19 +120,15 @@ cudaError_t launch_varlen_f32(const float* qkv, const int32_t* cu, int n_seqs, i
                               int window, int causal, float scale, const float* cos_t, const float* sin_t,
                               void* out, int out_kind, void* ws, int max_pairs, int32_t* dev_status,
                               cudaStream_t st);
-// k_map / v_map == nullptr: packed sequences.  Then with prep_map (the rows
-// written by launch_qkv_prep, [total, W] f16 in the qkv layout) everything
-// comes from there and no RoPE is left to do; without it from the qkv rows,
-// with Q and K rotated in the kernel (K with the RoPE tables cos_map /
-// sin_map, [rope_len, 32] f32, boxes of 128 rows).  Otherwise K and V come
-// from caches [n_seqs * kv_heads * cap, 64] (chunks) and the table and prep
-// maps are unused.
+// The kernel that applies RoPE in shared memory (prefill_tc.cu).  k_map /
+// v_map == nullptr: packed sequences, Q and K rotated in the kernel (K with the
+// RoPE tables cos_map / sin_map, [rope_len, 32] f32, boxes of 128 rows).
+// Otherwise K and V come from caches [n_seqs * kv_heads * cap, 64] (chunks)
+// and the table maps are unused.
 cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_map, const CUtensorMap* v_map,
-                              const CUtensorMap* cos_map, const CUtensorMap* sin_map, const CUtensorMap* prep_map,
-                              int n_seqs, int total,
-                              int heads, int kv_heads, int cap, int window, int causal,
-                              float scale, const float* cos_t, const float* sin_t, void* out, void* ws,
-                              int max_pairs, int32_t* dev_status, cudaStream_t st);
+                              const CUtensorMap* cos_map, const CUtensorMap* sin_map, int heads, int kv_heads, int cap,
+                              int window, int causal, float scale, const float* cos_t, const float* sin_t, void* out,
+                              void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
 // Attention over prepared rows (prefill_rows.cu): rows_map addresses the
 // rows written by launch_qkv_prep ([total, W] f16, boxes of 128 rows x 64
 // columns, 128-byte swizzle); the work list is the scheduler's in ws.

@@ -1,6 +1,9 @@
 // prefill_tc.cu -- packed variable-length attention over a BF16 fused qkv
-// buffer on the sm_103a tensor cores: warp-specialised, two query tiles per
-// CTA sharing every K/V tile, ping-pong between two softmax warpgroups.
+// buffer on the sm_103a tensor cores, with RoPE applied in shared memory:
+// the kernel of kime_attn_varlen when the workspace has no room for prepared
+// rows (see prefill_rows.cu for the kernel over prepared rows), and of chunked
+// prefill against the KV cache.  Warp-specialised, two query tiles per CTA
+// sharing every K/V tile, ping-pong between two softmax warpgroups.
 //
 // Semantics (per sequence s, head h, local query i of a length-L sequence):
 // out = softmax over visible keys j of scale * <rope(q_i, i), rope(k_j, j)>,
@@ -19,15 +22,12 @@
 //   warpgroup 1  softmax for query tile B
 //   warpgroup 2  RoPE: rotates the unit's Q tiles (double-buffered per unit)
 //                and every K tile in shared memory, converts each V tile;
-//                thread r owns row r of a tile.  On prepared rows there is no
-//                RoPE work and it writes the output rows instead, one unit
-//                behind the softmax warpgroups
+//                thread r owns row r of a tile
 //   warpgroup 3  warp 12: TMA producer (Q tiles, 4-stage K/V ring);
 //                warps 13, 14: MMA issuers (one thread each, tcgen05.mma), one
 //                per query tile, so neither tile's MMAs wait on the other's
 // Registers are rebalanced with setmaxnreg: 168 for the softmax warpgroups,
-// 112 for RoPE, 64 for the producer / MMA warpgroup (96 and 80 with prepared
-// rows; sum 512 x 128).
+// 112 for RoPE, 64 for the producer / MMA warpgroup (sum 512 x 128).
 // MMA operands are f16 (11-bit significand): q and k are rotated in float32
 // and rounded once to f16 (q times scale*log2(e) first, so S arrives in log2
 // units), V is widened from bf16 exactly, P is rounded to f16.  Inputs must
@@ -98,8 +98,7 @@ struct Layout {
   static constexpr uint32_t v = k + stages * kTile;
   static constexpr uint32_t tab = v + stages * kTile;
   static constexpr uint32_t bar = tab + tab_stages * 2 * kTile;
-  static constexpr uint32_t lrow = bar + 512;  // [2][128] f32: each tile's row sums for the epilogue warpgroup
-  static constexpr uint32_t bytes = lrow + 1024 + 1024;
+  static constexpr uint32_t bytes = bar + 512 + 1024;  // + alignment slack
   static_assert(bytes <= 232448, "shared memory per CTA");
 };
 constexpr uint32_t kTmemCols = 512;
@@ -127,7 +126,6 @@ struct Shared {
   uint64_t s_full[2][2];    // per query tile, alternating: S(t) and S(t+1) may both be done
   uint64_t s_read[2];  // the softmax warpgroup has loaded its tile's S (one arrival per warp)
   uint64_t p_full[2], pv_full[2];
-  uint64_t epi_full[2], o_free[2];  // prepared rows: the tile's O is final / has been read out
   uint64_t drain[2];  // wind-down after an abort: each MMA issuer's last commit
   UnitInfo info[2];
   uint32_t tmem_base;
@@ -161,15 +159,9 @@ __device__ __forceinline__ void regs_inc() {
   static_assert(N >= kLaunchRegs && N % 8 == 0 && N <= 256, "setmaxnreg.inc raises the count");
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
-// softmax warpgroups 168; RoPE / epilogue warpgroup and producer / MMA
-// warpgroup 112 and 64, or with prepared rows (no RoPE, more bookkeeping in
-// the MMA issuers) 96 and 80
-constexpr uint32_t kRegsSoftmax = 168;
-template <bool kPrep>
-struct RegSplit {
-  static constexpr uint32_t rope = kPrep ? 96 : 112, issue = kPrep ? 80 : 64;
-  static_assert(2 * kRegsSoftmax + rope + issue == 4 * kLaunchRegs, "register split");
-};
+// softmax warpgroups 168, RoPE warpgroup 112, producer / MMA warpgroup 64
+constexpr uint32_t kRegsSoftmax = 168, kRegsRope = 112, kRegsIssue = 64;
+static_assert(2 * kRegsSoftmax + kRegsRope + kRegsIssue == 4 * kLaunchRegs, "register split");
 
 // One row's cos/sin table entries (32 + 32 floats), loaded ahead of use.
 struct TableRow {
@@ -270,18 +262,15 @@ struct Params {
 };
 
 // kCache = false: a packed batch; Q, K and V are heads of the qkv rows, Q and
-// K rotated here, or (kPrep) qkv_map holds the rows prepared by
-// qkv_prep_kernel (queries rotated and scaled, keys rotated, all in f16) and
-// no RoPE is left to do.  kCache = true: chunks attending a KV cache that
-// already holds them
-// (rotated keys); K and V tiles come from the cache maps, rows past the
-// sequence's keys are zeroed, q rows sit at positions off + i.
-template <bool kCache, bool kPrep>
+// K rotated here.  kCache = true: chunks attending a KV cache that already
+// holds them (rotated keys); K and V tiles come from the cache maps, rows past
+// the sequence's keys are zeroed, q rows sit at positions off + i.
+template <bool kCache>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qkv_map, const __grid_constant__ CUtensorMap k_map,
                       const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap cos_map,
                       const __grid_constant__ CUtensorMap sin_map, const Params p) {
-  constexpr bool kTab = !kCache && !kPrep;  // keys rotated here, tables staged with each K tile
+  constexpr bool kTab = !kCache;  // keys rotated here, tables staged with each K tile
   using Lay = Layout<kTab>;
   constexpr int kStages = Lay::stages;
   constexpr uint32_t kOffQ = Lay::q, kOffK = Lay::k, kOffV = Lay::v, kOffTab = Lay::tab, kOffBar = Lay::bar;
@@ -298,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kCache) {
       tma_prefetch_map(&k_map);
       tma_prefetch_map(&v_map);
-    } else if (!kPrep) {
+    } else {
       tma_prefetch_map(&cos_map);
       tma_prefetch_map(&sin_map);
     }
@@ -311,8 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh->s_full[i][0], 1);
       mbar_init(&sh->s_full[i][1], 1);
       mbar_init(&sh->p_full[i], 1);
-      mbar_init(&sh->epi_full[i], 4);  // one arrival per warp
-      mbar_init(&sh->o_free[i], 4);
       mbar_init(&sh->pv_full[i], 1);
       mbar_init(&sh->drain[i], 1);
     }
@@ -347,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (wg == 3) {
-    regs_dec<RegSplit<kPrep>::issue>();
+    regs_dec<kRegsIssue>();
     if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- TMA producer
       griddep_wait();  // the schedule written by the kernel before this one
@@ -456,7 +443,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w = warp - 13;
       uint32_t n = 0, c = 0, pc = 0, sc = 0;  // units, key tiles, P tiles, S MMAs of this tile
       EV_DECL;
-      uint32_t ou = 0;  // units in which this tile's O was accumulated (read out by the epilogue warpgroup)
       const uint32_t tS = tmem + w * 128, tO = tmem + 256 + w * 64, tP = tmem + 384 + w * 64;
       PHASE_DECL(8);
       for (;; ++n) {
@@ -472,18 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tile_ranges(inf.L, off + inf.L - inf.kbase, off - inf.kbase, inf.qt0 + w, kCausal, kWindow, kb, ke, fb, fe);
         const uint32_t aq = smem_u32(smem + kOffQ + slot * 2 * kTile) + w * kTile;
         PHASE(4);
-        // the unit's Q: rotated by the RoPE warpgroup, or (prepared rows)
-        // ready as soon as its copy has landed -- then the issuer does not wait
-        // for the epilogue warpgroup, which writes the previous unit's rows
-        // before it gets to this unit
-        bool ok = wait(kPrep ? &sh->q_full[slot] : &sh->qrot[slot], (n >> 1) & 1);
+        // the unit's Q, rotated by the RoPE warpgroup
+        bool ok = wait(&sh->qrot[slot], (n >> 1) & 1);
         PHASE(1);
         // S for the key tile that is number cc of the K/V ring may be issued
         // once that tile is in (and rotated) and the softmax warpgroup has
         // loaded the S before it out of the tile's S buffer
         auto s_ready = [&](uint32_t cc) -> bool {
           const uint32_t ph = (cc / kStages) & 1;
-          if (!mbar_test(&sh->kv_full[cc % kStages], ph) || (!kPrep && !mbar_test(&sh->krot[cc % kStages], ph)))
+          if (!mbar_test(&sh->kv_full[cc % kStages], ph) || !mbar_test(&sh->krot[cc % kStages], ph))
             return false;
           return sc == 0 || mbar_test(&sh->s_read[w], (sc - 1) & 1);
         };
@@ -546,12 +529,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else if (pv && mbar_try_wait_ns(&sh->p_full[w], pc & 1, la ? 32u : 1000u)) {
                 // (suspended while P is pending, briefly when S(t+1) is too,
                 // so the poll takes few issue slots from the other warps)
-                // prepared rows: the unit's first PV overwrites O, which the
-                // epilogue warpgroup must have read out for the unit before
-                if (kPrep && t == kb && ou > 0 && !wait(&sh->o_free[w], (ou - 1) & 1)) {
-                  ok = false;
-                  break;
-                }
                 PHASE(3);
                 ++pc;
                 issue_pv(t, st);
@@ -568,14 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // follow the fill (and the RoPE pass), or this issuer's arrival
             // could complete the stage's previous phase
             const uint32_t ph = (c / kStages) & 1;
-            if (!(ok = wait(&sh->kv_full[st], ph) && (kPrep || wait(&sh->krot[st], ph)))) break;
+            if (!(ok = wait(&sh->kv_full[st], ph) && wait(&sh->krot[st], ph))) break;
           }
           tc_commit(&sh->kv_empty[st]);  // this issuer's MMAs reading stage st are issued
           if (t + 1 == inf.ke) tc_commit(&sh->q_empty[slot]);  // and its last S of the unit
           PHASE(7);
         }
         if (!ok) break;
-        if (ke > kb) ++ou;
         mbar_arrive(&sh->unit_empty[slot]);
       }
       if (*abort_flag) {  // every MMA this thread issued completes before TMEM is freed
@@ -586,55 +562,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (wg == 2) {
-    regs_dec<RegSplit<kPrep>::rope>();
+    regs_dec<kRegsRope>();
     // ------------------------------------------------------------ RoPE
     const int r = tid - 256;  // row of every tile this thread converts
     uint32_t n = 0, c = 0;
     float big = 0.f;  // largest magnitude this thread rounded to f16
-    // prepared rows: this warpgroup has no RoPE work and writes the output
-    // rows instead, one unit behind the softmax warpgroups
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t ne0 = 0, ne1 = 0;  // epilogues done for tile A / tile B
-    EV_DECL;
-    UnitInfo prev;
-    prev.u = -1;
-    auto epilogue = [&](const UnitInfo& e) -> bool {
-      bool eok = true;
-      if (e.u < 0) return eok;
-      const int h = e.u % p.heads;
-#pragma unroll
-      for (int w = 0; w < 2; ++w) {
-        if (w >= e.nt) break;
-        const uint32_t cnt = w ? ne1 : ne0;
-        eok = eok && wait(&sh->epi_full[w], cnt & 1);
-        if (r == 0) EV(5, 0, w);
-        if (w) ++ne1;
-        else ++ne0;
-        tc_fence_after();
-        uint32_t ov[64];
-        tmem_ld64_wait(tmem + 256 + w * 64 + lane_off, ov);
-        const float lv = reinterpret_cast<const float*>(smem + Lay::lrow)[w * kBM + r];
-        tc_fence_before();
-        __syncwarp();
-        if (eok && lane == 0) mbar_arrive(&sh->o_free[w]);
-        if (r == 0) EV(5, 1, w);
-        const int i = (e.qt0 + w) * kBM + r;
-        if (eok && i < e.L) {
-          const float inv = 1.f / lv;
-          __nv_bfloat16* dst = p.out + static_cast<size_t>(e.row0 + i) * p.heads * kHead + h * kHead;
-#pragma unroll
-          for (int d = 0; d < kHead; d += 8) {
-            uint4 wv;
-            wv.x = pack_bf16x2(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv);
-            wv.y = pack_bf16x2(__uint_as_float(ov[d + 2]) * inv, __uint_as_float(ov[d + 3]) * inv);
-            wv.z = pack_bf16x2(__uint_as_float(ov[d + 4]) * inv, __uint_as_float(ov[d + 5]) * inv);
-            wv.w = pack_bf16x2(__uint_as_float(ov[d + 6]) * inv, __uint_as_float(ov[d + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + d) = wv;
-          }
-        }
-      }
-      return eok;
-    };
     PHASE_DECL(6);
     for (;; ++n) {
       const int slot = n & 1;
@@ -642,16 +574,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (named_bar_or(3, 128, !ok)) break;
       PHASE(0);
       const UnitInfo inf = sh->info[slot];
-      if (inf.u < 0) {
-        if (kPrep) epilogue(prev);
-        break;
-      }
-      // the unit's query tiles: row r of each, at positions q0 + r (prepared
-      // rows are rotated and scaled already: only their arrival is waited for)
+      if (inf.u < 0) break;
+      // the unit's query tiles: row r of each, at positions q0 + r
       uint8_t* q = smem + kOffQ + slot * 2 * kTile;
       TableRow tb;
-      if (kPrep) ok = wait(&sh->q_full[slot], (n >> 1) & 1);
-      for (int w = 0; !kPrep && w < inf.nt; ++w) {
+      for (int w = 0; w < inf.nt; ++w) {
         const int i = (inf.qt0 + w) * kBM + r;
         const size_t ti = static_cast<size_t>((kCache ? inf.off : 0) + i) * kHalf;  // table row of position off + i
         if (i < inf.L) load_table_row(tb, p.cos_t + ti, p.sin_t + ti);
@@ -671,12 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&sh->unit_empty[slot]);  // every thread has its copy of the unit
       }
       const int Lk = (kCache ? inf.off : 0) + inf.L;  // keys of the unit's sequence
-      if (kPrep) {
-        ok = epilogue(prev);
-        prev = inf;
-        if (named_bar_or(3, 128, !ok)) break;
-      }
-      for (int t = inf.kb; !kPrep && t < inf.ke; ++t, ++c) {  // (prepared keys need nothing here)
+      for (int t = inf.kb; t < inf.ke; ++t, ++c) {
         const int st = c % kStages, j = inf.kbase + t * kBN + r;
         PHASE(2);
         ok = wait(&sh->kv_full[st], (c / kStages) & 1);
@@ -867,18 +789,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       ok = wait(&sh->pv_full[w], (pvc++) & 1);
-      if (kPrep) {
-        // prepared rows: the epilogue warpgroup reads O out and writes the
-        // rows; this warpgroup goes on to the next unit
-        reinterpret_cast<float*>(smem + Lay::lrow)[w * kBM + r] = l;
-        tc_fence_before();
-        __syncwarp();
-        if (ok && lane == 0) mbar_arrive(&sh->epi_full[w]);
-        if (r == 0) EV(3 + w, 2, n);
-        if (named_bar_or(1 + w, 128, !ok)) break;
-        PHASE(8);
-        continue;
-      }
       tc_fence_after();
       uint32_t ov[64];
       tmem_ld64_wait(tO, ov);
@@ -939,25 +849,23 @@ extern "C" int kime_debug_phase_clear() {
 #endif
 
 cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_map, const CUtensorMap* v_map,
-                              const CUtensorMap* cos_map, const CUtensorMap* sin_map, const CUtensorMap* prep_map,
-                              int n_seqs, int total, int heads, int kv_heads, int cap, int window, int causal,
-                              float scale, const float* cos_t, const float* sin_t, void* out, void* ws,
-                              int max_pairs, int32_t* dev_status, cudaStream_t st) {
-  (void)n_seqs; (void)total;
-  // kernel variant: 0 packed (keys rotated here), 1 packed with prepared rows, 2 chunks against the caches
-  const int mode = k_map != nullptr ? 2 : (prep_map != nullptr ? 1 : 0);
-  static int configured[3][64] = {};
+                              const CUtensorMap* cos_map, const CUtensorMap* sin_map, int heads, int kv_heads, int cap,
+                              int window, int causal, float scale, const float* cos_t, const float* sin_t, void* out,
+                              void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st) {
+  // kernel variant: packed sequences (keys rotated here), or chunks against the caches
+  const bool chunks = k_map != nullptr;
+  static int configured[2][64] = {};
   int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const uint32_t smem_bytes = mode == 0 ? Layout<true>::bytes : Layout<false>::bytes;
-  const void* fn = mode == 0   ? reinterpret_cast<const void*>(prefill_tc_kernel<false, false>)
-                   : mode == 1 ? reinterpret_cast<const void*>(prefill_tc_kernel<false, true>)
-                               : reinterpret_cast<const void*>(prefill_tc_kernel<true, false>);
-  if (dev < 64 && !configured[mode][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-    if (e != cudaSuccess) return e;
-    configured[mode][dev] = 1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const uint32_t smem_bytes = chunks ? Layout<false>::bytes : Layout<true>::bytes;
+  const void* fn = chunks ? reinterpret_cast<const void*>(prefill_tc_kernel<true>)
+                          : reinterpret_cast<const void*>(prefill_tc_kernel<false>);
+  if (dev >= 64 || !configured[chunks][dev]) {
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) != cudaSuccess)
+      return e;
+    if (dev < 64) configured[chunks][dev] = 1;
   }
   Params prm;
   prm.heads = heads;
@@ -984,13 +892,9 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (mode == 2)
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, false>, *qkv_map, *k_map, *v_map, *qkv_map, *qkv_map, prm);
-  if (mode == 1)
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, true>, *prep_map, *prep_map, *prep_map, *prep_map,
-                              *prep_map, prm);
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, false>, *qkv_map, *qkv_map, *qkv_map, *cos_map, *sin_map,
-                            prm);
+  if (chunks)
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true>, *qkv_map, *k_map, *v_map, *qkv_map, *qkv_map, prm);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false>, *qkv_map, *qkv_map, *qkv_map, *cos_map, *sin_map, prm);
 }
 
 }  // namespace kime
