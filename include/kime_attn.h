@@ -112,10 +112,11 @@ typedef enum {
  * KIME_DEV_RANGE is set).  FP32 qkv with
  * KIME_F32 / KIME_F32_F16OUT / KIME_F32_BF16OUT runs on FP32 FMA.  Launches:
  * the device scheduler, the row preparation when the workspace has room for
- * it, then the attention kernel.  KIME_F32_3XTF32 enqueues a memset of part of
- * the workspace, the scheduler, the split pass (queries and keys rotated, all
- * values split into TF32 high and low parts, values transposed) and the
- * tensor-core attention kernel. */
+ * it, then the attention kernel.  KIME_F32_3XTF32 enqueues the scheduler, a
+ * preparation pass (keys rotated, values transposed, FP32, into the
+ * workspace) and the tensor-core attention kernel, which splits every operand
+ * into TF32 high and low parts itself and reads, rotates and scales the
+ * queries from qkv. */
 int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int n_seqs, int total_tokens,
                      int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal, float scale,
                      const float* rope_cos, const float* rope_sin, int rope_len, void* out, void* workspace,
@@ -226,11 +227,10 @@ int kime_chunk_step(const void* qkv, const int32_t* cu_seqlens, const int32_t* p
  * uses n_seqs, total_tokens) or op 3 (varlen with room for the prepared qkv
  * rows, about total_tokens * 128 * (heads + 2 * kv_heads) bytes more: uses
  * n_seqs, total_tokens, heads, kv_heads) or op 4 (varlen with KIME_F32_3XTF32:
- * op 0 at a 1 KB boundary, then the split planes, each 1 KB aligned: queries
- * [total_tokens, 64 * heads] f32 twice, keys [total_tokens, 64 * kv_heads] f32
- * twice, transposed values [64 * kv_heads, tp] f32 twice, with tp =
- * total_tokens + 4 * n_seqs + 4 rounded up to a multiple of 4).  Returns 0 for
- * an unknown op or malformed sizes. */
+ * op 0 at a 1 KB boundary, then two planes, each 1 KB aligned: rotated keys
+ * [total_tokens, 64 * kv_heads] f32 and transposed values [64 * kv_heads, tp]
+ * f32, with tp = 4 * ceil(total_tokens / 4) + 68 * n_seqs).  Returns 0 for an
+ * unknown op or malformed sizes. */
 size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads, int kv_heads, int cap);
 
 /* kime_qkv_proj -- the QKV projection of a packed batch, the step before

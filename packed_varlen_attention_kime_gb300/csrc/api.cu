@@ -95,7 +95,7 @@ int encode_table_map(CUtensorMap* map, const float* table, int rope_len) {
   return KIME_OK;
 }
 
-// 2-D map over an f32 plane [rows, cols] (a split qkv plane of the 3xTF32
+// 2-D map over an f32 matrix [rows, cols] (FP32 qkv rows for the 3xTF32
 // path): boxes of box_rows rows x 32 columns (128 bytes), 128-byte swizzle,
 // elements past either end read as zero.
 int encode_f32_plane_map(CUtensorMap* map, const void* plane, long long cols, long long rows, int box_rows) {
@@ -155,7 +155,7 @@ size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads
   }
   if (op == 4) {
     if (total_tokens < 0 || !heads_ok(heads, kv_heads, kime::kHead)) return 0;
-    return kime::tf32_planes(n_seqs, total_tokens, heads, kv_heads).end;
+    return kime::tf32_planes(n_seqs, total_tokens, kv_heads).end;
   }
   return 0;
 }
@@ -184,29 +184,25 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
   const int max_pairs = kime::max_pairs_for(n_seqs, total_tokens);
   int rc;
   if (dtype == KIME_F32_3XTF32) {
-    // FP32 on the tensor cores: planes cleared, scheduler, split pass, attention
-    if (workspace_bytes < kime::tf32_planes(n_seqs, total_tokens, heads, kv_heads).end) return KIME_ERANGE;
-    const kime::Tf32Planes pl = kime::tf32_planes(n_seqs, total_tokens, heads, kv_heads);
+    // FP32 on the tensor cores: scheduler, preparation pass (beside it), attention
+    const kime::Tf32Planes pl = kime::tf32_planes(n_seqs, total_tokens, kv_heads);
+    if (workspace_bytes < pl.end) return KIME_ERANGE;
     char* w = static_cast<char*>(workspace);
-    CUtensorMap qh, ql, kh, kl, vh, vl;
-    const long long hq = 64LL * heads, hk = 64LL * kv_heads;
-    if ((rc = encode_f32_plane_map(&qh, w + pl.qh, hq, total_tokens, kime::kBM)) ||
-        (rc = encode_f32_plane_map(&ql, w + pl.ql, hq, total_tokens, kime::kBM)) ||
-        (rc = encode_f32_plane_map(&kh, w + pl.kh, hk, total_tokens, 64)) ||
-        (rc = encode_f32_plane_map(&kl, w + pl.kl, hk, total_tokens, 64)) ||
-        (rc = encode_f32_plane_map(&vh, w + pl.vh, pl.tp, hk, 64)) ||
-        (rc = encode_f32_plane_map(&vl, w + pl.vl, pl.tp, hk, 64)))
+    const long long hk = 64LL * kv_heads;
+    CUtensorMap qmap, kmap, vmap;
+    if ((rc = encode_f32_plane_map(&qmap, qkv, W, total_tokens, 64)) ||
+        (rc = encode_f32_plane_map(&kmap, w + pl.kr, hk, total_tokens, 64)) ||
+        (rc = encode_f32_plane_map(&vmap, w + pl.vt, pl.tp, hk, 64)))
       return rc;
-    if ((rc = cuda_status(kime::launch_tf32_clear(n_seqs, total_tokens, heads, kv_heads, workspace, st)))) return rc;
     if ((rc = cuda_status(kime::launch_schedule(cu_seqlens, nullptr, n_seqs, total_tokens, max_seqlen, causal,
                                                 window, 0, 0, workspace, max_pairs, dev_status, st))))
       return rc;
-    if ((rc = cuda_status(kime::launch_tf32_split(static_cast<const float*>(qkv), cu_seqlens, n_seqs, total_tokens,
-                                                  heads, kv_heads, scale, rope_cos, rope_sin, rope_len, workspace,
-                                                  st))))
+    if ((rc = cuda_status(kime::launch_tf32_kv_prep(static_cast<const float*>(qkv), cu_seqlens, n_seqs, total_tokens,
+                                                    heads, kv_heads, rope_cos, rope_sin, rope_len, workspace, st))))
       return rc;
-    return cuda_status(kime::launch_prefill_3xtf32(&qh, &ql, &kh, &kl, &vh, &vl, heads, kv_heads, window, causal,
-                                                   static_cast<float*>(out), workspace, dev_status, st));
+    return cuda_status(kime::launch_prefill_3xtf32(&qmap, &kmap, &vmap, heads, kv_heads, window, causal, scale,
+                                                   rope_cos, rope_sin, static_cast<float*>(out), workspace,
+                                                   dev_status, st));
   }
   rc = cuda_status(kime::launch_schedule(cu_seqlens, nullptr, n_seqs, total_tokens, max_seqlen, causal, window,
                                          0, 0, workspace, max_pairs, dev_status, st));

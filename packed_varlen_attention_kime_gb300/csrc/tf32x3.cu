@@ -13,27 +13,50 @@
 // lo to TF32 (<= 2^-21 |a b|): FP32-level accuracy at TF32 tensor rates.
 //
 // Two kernels:
-//   split   one pass over the qkv rows: queries and keys rotated (the same
-//           float32 evaluation as the CUDA-core FP32 kernel), queries scaled by
-//           scale * log2(e) (the softmax then works in log2 units), values
-//           transposed, everything split into TF32 high and low planes.  The
-//           transposed values put each sequence at a column that is a multiple
-//           of 4 (16 bytes), so a TMA box of a sequence's keys always starts on
-//           a 16-byte boundary.
-//   attend  persistent CTAs of 128 threads take (query tile, head) units from
-//           the scheduler's list.  Thread r owns row r of the 128-row query
-//           tile (TMEM lane r).  Key tiles are visited in 64-key halves:
-//           S = Q K^T (three 128x64x64 TF32 MMA chains into TMEM), online
-//           softmax in FP32 on S loaded from TMEM (exponentials on the MUFU,
-//           ex2.approx: relative error about 2^-22, far inside the FP32
-//           contract), P split into high and low
-//           parts stored to TMEM, O += P V (three chains, A = P from TMEM,
-//           B = V^T from shared memory), O rescaled in TMEM when the row max
-//           moves.  Q (high, low: 64 KB) stays in shared memory for the unit;
-//           the K / V^T halves (64 KB each) are double-buffered, the next one
-//           loaded by TMA (as soon as the PV that read its stage is done)
-//           while the current one is in the softmax.  Thread 0
-//           issues the copies and the MMAs.
+//   prep    beside the scheduler, one pass over the qkv rows: keys rotated
+//           (the float32 evaluation of every kernel here) into a key plane;
+//           values transposed into a value plane (V^T is the K-major B
+//           operand of O += P V; the TF32 MMA takes its operands K-major
+//           here), each sequence's columns followed by zeros up to its next
+//           multiple of 64 keys.  Both FP32, the size of the raw rows.
+//   attend  persistent CTAs of 512 threads over (128-row query tile, head)
+//           units of the scheduler's list, the unit's keys visited in 64-key
+//           halves:
+//     warps 0-7   softmax: warps w and w + 4 share TMEM lanes 32 (w mod 4) ..
+//                 +31 (rows of the tile) and take key columns 0-31 and 32-63
+//                 of each half; they exchange their partial row maxima
+//                 through shared memory.  FP32 online softmax (exponentials on
+//                 the MUFU, ex2.approx: relative error about 2^-22), P split
+//                 into TF32 high and low parts stored to TMEM, O / l at the
+//                 end.  At the start of a unit the same warps read its raw
+//                 query tile from shared memory, rotate it, multiply it by
+//                 scale * log2(e) (the softmax then works in base 2) and store
+//                 its high and low parts in TMEM: the A operand of S = Q K^T.
+//     warps 8-11  operand split: each half's keys and V^T, as loaded, split
+//                 in place into high parts, low parts beside them
+//     warp 12     TMA producer of the raw query tiles and the key halves (a
+//                 3-stage ring); it also claims the units
+//     warp 13     TMA producer of the V^T halves (a 2-stage ring)
+//     warps 14-15 MMA issuers (one thread each; one thread issuing alone
+//                 cannot keep up with these small MMAs): warp 14 issues S(h) =
+//                 Q K^T as three 128x64x64 TF32 chains, A from TMEM; warp 15
+//                 O += P(h) V(h) as three chains, A = P from TMEM.  With two S
+//                 buffers S(h+1) runs while the softmax works on S(h) and
+//                 PV(h) while it works on S(h+1).  The next unit's queries
+//                 are stored to TMEM before the epilogue of the current one,
+//                 so S of its first half runs while the current unit's last
+//                 PV does.
+// The softmax moves its reference maximum lazily (only when a row's maximum
+// exceeds it by more than 2^8; P then stays below 2^8 and O is rescaled in
+// TMEM), so it almost never touches O before the epilogue.
+//
+// TMEM (512 columns): S 0..191 (three buffers of 64; the softmax writes P's
+// high parts over the S it has read), P low 192..319 (two buffers), O
+// 320..383, Q high 384..447, Q low 448..511.  Per S buffer a barrier says
+// when the PV that read its P has completed: the S issuer waits for it
+// before reusing the buffer (so it can run two halves ahead of the PVs), and
+// the softmax waits for it only to reuse a P-low buffer or to rescale O.
+// Every wait is bounded in time; on a timeout every role winds down.
 #include "kime_common.cuh"
 #include "kime_internal.h"
 
@@ -41,17 +64,25 @@ namespace kime {
 
 namespace {
 
-constexpr int kT3Threads = 128;
-constexpr int kSub = 64;                  // keys per visited half tile
-constexpr uint32_t kSlabQ = kBM * 128;    // one 32-column (128-byte) slab of a 128-row tile: 16 KB
-constexpr uint32_t kSlabK = kSub * 128;   // one slab of a 64-row tile: 8 KB
-constexpr uint32_t kOffQh = 0, kOffQl = 2 * kSlabQ, kOffStage = 4 * kSlabQ;
-constexpr uint32_t kKh = 0, kKl = 2 * kSlabK, kVh = 4 * kSlabK, kVl = 6 * kSlabK, kStageBytes = 8 * kSlabK;
-constexpr uint32_t kT3Smem = kOffStage + 2 * kStageBytes + 1024;  // + slack to align the base to 1 KB
-static_assert(kT3Smem <= 232448, "shared memory");
-constexpr uint32_t kQBytes = 4 * kSlabQ, kKVBytes = kStageBytes;  // transaction bytes per load group
-// TMEM columns: S 0..63, P high 64..127, P low 128..191, O 192..255
-constexpr uint32_t kT3Cols = 256, kColPh = 64, kColPl = 128, kColO = 192;
+constexpr int kT3Threads = 512;
+constexpr int kSub = 64;                 // keys per visited half tile
+constexpr int kKStages = 3, kVStages = 2;
+constexpr uint32_t kSlabQ = kBM * 128;   // one 32-column (128-byte) slab of a 128-row tile: 16 KB
+constexpr uint32_t kSlabK = kSub * 128;  // one slab of a 64-row tile: 8 KB
+// shared memory, offsets from a 1 KB aligned base: the raw query tile, the
+// key stages and the V^T stages (high parts, where the loads land, then low
+// parts; two slabs each)
+constexpr uint32_t kHalfBytes = 2 * kSlabK;  // one operand of one half: 16 KB
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = 2 * kSlabQ;
+constexpr uint32_t kOffV = kOffK + kKStages * 2 * kHalfBytes;
+constexpr uint32_t kT3Smem = kOffV + kVStages * 2 * kHalfBytes + 1024;  // + slack to align the base to 1 KB
+static_assert(kT3Smem + 4096 <= 232448, "shared memory (dynamic + the barrier block)");
+constexpr uint32_t kColS = 0, kColPl = 192, kColO = 320, kColQh = 384, kColQl = 448;
+constexpr int kSBufs = 3;  // S / P-high buffers
+constexpr uint32_t kT3Cols = 512;
+constexpr float kLazy = 8.f;       // the reference max moves when exceeded by more (log2 units)
+constexpr float kNone = -3.0e38f;  // "no visible key yet": below every logit, finite
 
 // Instruction descriptor, kind::tf32: TF32 A and B (format 2), FP32 D, both
 // K-major.
@@ -61,13 +92,7 @@ __host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
 }
 constexpr uint32_t kIdesc = idesc_tf32_f32(kBM, 64);  // S: 128 x 64 keys; O: 128 x 64 dims
 
-__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(acc)
-      : "memory");
-}
+// D[tmem] (+)= A[tmem] B[smem], kind::tf32
 __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -83,34 +108,32 @@ __device__ __forceinline__ float tf32_hi(float x) {
   return __uint_as_float(r);
 }
 
-// First column of sequence s in a transposed value plane (a multiple of 4;
-// sequence s + 1 starts at least L_s + 1 columns later).
-__host__ __device__ __forceinline__ int vt_col(int cu_s, int s) { return 4 * ((cu_s + 3) >> 2) + 4 * s; }
-
-__device__ __forceinline__ bool visible(int i, int j, int L, int causal, int window) {
-  if (j >= L) return false;
-  if (causal && j > i) return false;
-  if (window >= 0 && abs(i - j) > window) return false;
-  return true;
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
-// ------------------------------------------------------------------ split
-constexpr int kSplitRows = 32;  // tokens per CTA
+// ------------------------------------------------------------------- prep
+constexpr int kPrepRows = 32;  // tokens per CTA
 
 __global__ void __launch_bounds__(256)
-    tf32_split_kernel(const float* __restrict__ qkv, const int32_t* __restrict__ cu, int n_seqs, int total,
-                      int heads, int kv_heads, float qmul, const float* __restrict__ cos_t,
-                      const float* __restrict__ sin_t, int rope_len, int tp, float* __restrict__ qh,
-                      float* __restrict__ ql, float* __restrict__ kh, float* __restrict__ kl,
-                      float* __restrict__ vh, float* __restrict__ vl) {
-  __shared__ float vs[kSplitRows][kHead + 1];
-  __shared__ int s_col[kSplitRows], s_pos[kSplitRows];
+    tf32_kv_prep_kernel(const float* __restrict__ qkv, const int32_t* __restrict__ cu, int n_seqs, int total,
+                        int heads, int kv_heads, const float* __restrict__ cos_t, const float* __restrict__ sin_t,
+                        int rope_len, int tp, float* __restrict__ kr, float* __restrict__ vt) {
+  __shared__ float vs[kPrepRows][kHead + 1];
+  __shared__ int s_col[kPrepRows], s_pos[kPrepRows], s_pad[kPrepRows];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j0 = blockIdx.x * kSplitRows;
+  const int j0 = blockIdx.x * kPrepRows;
   const size_t W = static_cast<size_t>(kHead) * (heads + 2 * kv_heads);
-  if (tid < kSplitRows) {
+  if (tid < kPrepRows) {
     const int j = j0 + tid;
-    int col = -1, pos = -1;
+    int col = -1, pos = -1, pad = 0;
     if (j < total) {
       // the sequence owning row j: the largest s with cu[s] <= j
       int lo = 0, hi = n_seqs - 1;
@@ -119,69 +142,66 @@ __global__ void __launch_bounds__(256)
         if (__ldg(cu + mid) <= j) lo = mid;
         else hi = mid - 1;
       }
-      const int c0 = __ldg(cu + lo);
+      const int c0 = __ldg(cu + lo), c1 = __ldg(cu + lo + 1);
       pos = j - c0;
       // (with a malformed cu the scheduler reports it and skips the sequence;
       // here only the plane's bounds matter)
       if (pos >= 0 && c0 >= 0 && c0 <= total) {
-        const long long c = static_cast<long long>(vt_col(c0, lo)) + pos;
+        const long long c = static_cast<long long>(tf32_vt_col(c0, lo)) + pos;
         col = c < tp ? static_cast<int>(c) : -1;
+        // the sequence's last token also zeroes the columns up to its next
+        // multiple of 64 keys
+        if (col >= 0 && j + 1 == c1) {
+          const int L = c1 - c0;
+          pad = min((L + kSub - 1) / kSub * kSub - L, tp - 1 - col);
+        }
       }
     }
     s_col[tid] = col;
     s_pos[tid] = pos;
+    s_pad[tid] = pad;
   }
   __syncthreads();
-  // queries and keys: warp w rotates tokens w, w + 8, ...; lane l takes the
-  // pair (l, l + 32) of every head
-  const int hq = heads * kHead, hk = kv_heads * kHead;
-  for (int t = warp; t < kSplitRows; t += 8) {
+  // keys: warp w rotates tokens w, w + 8, ...; lane l takes the pair (l, l + 32)
+  const int hk = kv_heads * kHead;
+  for (int t = warp; t < kPrepRows; t += 8) {
     const int j = j0 + t;
     if (j >= total) break;
     const int pos = s_pos[t];
     const bool rot = pos >= 0 && pos < rope_len;  // a row of no valid sequence: not rotated
     const float c = rot ? __ldg(cos_t + static_cast<size_t>(pos) * kHalf + lane) : 1.f;
     const float s = rot ? __ldg(sin_t + static_cast<size_t>(pos) * kHalf + lane) : 0.f;
-    const float* x = qkv + static_cast<size_t>(j) * W;
-    for (int hd = 0; hd < heads + kv_heads; ++hd) {
-      const float a = __ldg(x + hd * kHead + lane), b = __ldg(x + hd * kHead + lane + kHalf);
+    const float* x = qkv + static_cast<size_t>(j) * W + heads * kHead;
+    float* d = kr + static_cast<size_t>(j) * hk;
+    for (int g = 0; g < kv_heads; ++g) {
+      const float a = __ldg(x + g * kHead + lane), b = __ldg(x + g * kHead + lane + kHalf);
       float ya = a, yb = b;
       if (rot) rope_pair(a, b, c, s, ya, yb);
-      float *dh, *dl;
-      if (hd < heads) {
-        ya *= qmul;
-        yb *= qmul;
-        dh = qh + static_cast<size_t>(j) * hq + hd * kHead;
-        dl = ql + static_cast<size_t>(j) * hq + hd * kHead;
-      } else {
-        dh = kh + static_cast<size_t>(j) * hk + (hd - heads) * kHead;
-        dl = kl + static_cast<size_t>(j) * hk + (hd - heads) * kHead;
-      }
-      const float ha = tf32_hi(ya), hb = tf32_hi(yb);
-      dh[lane] = ha;
-      dh[lane + kHalf] = hb;
-      dl[lane] = ya - ha;
-      dl[lane + kHalf] = yb - hb;
+      d[g * kHead + lane] = ya;
+      d[g * kHead + lane + kHalf] = yb;
     }
   }
   // values: one kv head at a time through shared memory, written transposed
   // (consecutive threads: consecutive tokens of one dimension)
   for (int g = 0; g < kv_heads; ++g) {
     __syncthreads();
-    for (int e = tid; e < kSplitRows * kHead; e += 256) {
+    for (int e = tid; e < kPrepRows * kHead; e += 256) {
       const int t = e / kHead, d = e % kHead, j = j0 + t;
       vs[t][d] = j < total ? __ldg(qkv + static_cast<size_t>(j) * W + (heads + kv_heads + g) * kHead + d) : 0.f;
     }
     __syncthreads();
-    for (int e = tid; e < kSplitRows * kHead; e += 256) {
-      const int d = e / kSplitRows, t = e % kSplitRows;
+    for (int e = tid; e < kPrepRows * kHead; e += 256) {
+      const int d = e / kPrepRows, t = e % kPrepRows;
       const int col = s_col[t];
-      if (col < 0) continue;
-      const float v = vs[t][d], h = tf32_hi(v);
-      const size_t at = static_cast<size_t>(g * kHead + d) * tp + col;
-      vh[at] = h;
-      vl[at] = v - h;
+      if (col >= 0) vt[static_cast<size_t>(g * kHead + d) * tp + col] = vs[t][d];
     }
+  }
+  // the zero columns after each sequence that ends in this CTA's tokens
+  for (int t = 0; t < kPrepRows; ++t) {
+    const int pad = s_pad[t];  // (uniform across the CTA)
+    if (pad <= 0) continue;
+    const int col = s_col[t] + 1;
+    for (int e = tid; e < pad * hk; e += 256) vt[static_cast<size_t>(e / pad) * tp + col + e % pad] = 0.f;
   }
   // runs beside the scheduler (it reads none of its output) and ends only
   // after it, so the attention kernel, which waits for this pass, also finds
@@ -189,9 +209,57 @@ __global__ void __launch_bounds__(256)
   griddep_wait();
 }
 
+// A half's operand in shared memory, split in place: the FP32 values (two
+// slabs of 64 rows x 32 columns as the TMA wrote them) become their TF32
+// high parts, and the low parts go to the same offsets of lo.  The 128
+// threads of the split warps take consecutive 16-byte chunks.
+__device__ __forceinline__ void split_half(uint8_t* hi, uint8_t* lo, int ct) {
+  float4 x[8];
+#pragma unroll
+  for (int it = 0; it < 8; ++it) x[it] = *reinterpret_cast<const float4*>(hi + (ct + 128 * it) * 16);
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const float4 v = x[it];
+    const float4 h = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+    *reinterpret_cast<float4*>(hi + (ct + 128 * it) * 16) = h;
+    *reinterpret_cast<float4*>(lo + (ct + 128 * it) * 16) = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+  }
+}
+
 // ----------------------------------------------------------------- attend
+// A unit as the producer publishes it: query tile q0 .. q0 + 127 of sequence
+// s (rows row0 .. row0 + L - 1), head h (kv head g); halves [hb, hb + nsub)
+// of 64 keys, of which [ffb, ffe) are seen whole by every row of the tile.
+// u < 0 ends the list.
+struct UnitInfo {
+  int32_t u, s, h, g, row0, L, q0, hb, nsub, ffb, ffe;
+};
+
+struct Shared {
+  uint64_t unit_full[2], unit_empty[2];
+  uint64_t q_raw_full, q_raw_empty;  // the raw query tile in shared memory
+  uint64_t q_ready;                  // Q high / low stored in TMEM (one arrival per softmax warp)
+  uint64_t q_free;                   // every S of a unit has completed (its Q columns may be rewritten)
+  uint64_t k_raw_full[kKStages], k_ready[kKStages], k_empty[kKStages];  // loaded, split (one arrival per key split warp), read by S
+  uint64_t v_raw_full[kVStages], v_ready[kVStages], v_empty[kVStages];  // the same for V^T, read by PV
+  uint64_t s_full[kSBufs];  // S(h) computed, by S buffer h mod 3
+  uint64_t p_full[kSBufs];  // P(h) stored, O rescaled (one arrival per softmax warp)
+  uint64_t pv_buf[kSBufs];  // PV(h) has completed
+  uint64_t o_free;     // the epilogue has read O (one arrival per softmax warp)
+  uint64_t drain[2];  // wind-down after an abort: each issuer's last commit
+  UnitInfo info[2];
+  float xch[2][2][kBM];  // partial row maxima: [buffer][column half][row]
+  float xl[2][kBM];      // partial row sums at the epilogue: [column half][row]
+  uint32_t tmem_base;
+  int32_t abort;
+};
+static_assert(sizeof(Shared) <= 4096, "barrier block");
+
 struct T3Params {
   int heads, kv_heads, window, causal;
+  float qmul;  // scale * log2(e)
+  const float* cos_t;
+  const float* sin_t;
   float* out;
   WsHeader* hdr;
   const Pair* pairs;
@@ -199,256 +267,513 @@ struct T3Params {
 };
 
 __global__ void __launch_bounds__(kT3Threads, 1)
-    prefill_3xtf32_kernel(const __grid_constant__ CUtensorMap q_h, const __grid_constant__ CUtensorMap q_l,
-                          const __grid_constant__ CUtensorMap k_h, const __grid_constant__ CUtensorMap k_l,
-                          const __grid_constant__ CUtensorMap v_h, const __grid_constant__ CUtensorMap v_l,
-                          const T3Params p) {
+    prefill_3xtf32_kernel(const __grid_constant__ CUtensorMap qkv_map, const __grid_constant__ CUtensorMap k_map,
+                          const __grid_constant__ CUtensorMap v_map, const T3Params p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t q_full, kv_full[2], s_done, pv_done, drain;
-  __shared__ uint32_t tmem_slot;
-  __shared__ int s_unit;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t sb = (raw + 1023u) & ~1023u;  // 1 KB aligned (128-byte swizzle atoms)
-  uint8_t* const sp = smem_raw + (sb - raw);
+  __shared__ Shared shs;
+  Shared* sh = &shs;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    mbar_init(&q_full, 1);
-    mbar_init(&kv_full[0], 1);
-    mbar_init(&kv_full[1], 1);
-    mbar_init(&s_done, 1);
-    mbar_init(&pv_done, 1);
-    mbar_init(&drain, 1);
+    tma_prefetch_map(&qkv_map);
+    tma_prefetch_map(&k_map);
+    tma_prefetch_map(&v_map);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh->unit_full[i], 1);
+      mbar_init(&sh->unit_empty[i], 8);  // softmax, 4 split warps, V producer, both issuers
+    }
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(&sh->s_full[i], 1);
+      mbar_init(&sh->p_full[i], 8);
+      mbar_init(&sh->pv_buf[i], 1);
+    }
+    mbar_init(&sh->q_raw_full, 1);
+    mbar_init(&sh->q_raw_empty, 8);
+    mbar_init(&sh->q_ready, 8);
+    mbar_init(&sh->q_free, 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&sh->k_raw_full[i], 1);
+      mbar_init(&sh->k_ready[i], 4);
+      mbar_init(&sh->k_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&sh->v_raw_full[i], 1);
+      mbar_init(&sh->v_ready[i], 4);
+      mbar_init(&sh->v_empty[i], 1);
+    }
+
+    mbar_init(&sh->o_free, 8);
+    mbar_init(&sh->drain[0], 1);
+    mbar_init(&sh->drain[1], 1);
+    sh->abort = 0;
     fence_mbar_init();
-    tma_prefetch_map(&q_h);
-    tma_prefetch_map(&q_l);
-    tma_prefetch_map(&k_h);
-    tma_prefetch_map(&k_l);
-    tma_prefetch_map(&v_h);
-    tma_prefetch_map(&v_l);
   }
   if (warp == 0) {
-    tmem_alloc(&tmem_slot, kT3Cols);
+    tmem_alloc(&sh->tmem_base, kT3Cols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_slot;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tS = tmem, tPh = tmem + kColPh, tPl = tmem + kColPl, tO = tmem + kColO;
+  const uint32_t tmem = sh->tmem_base;
+  volatile int32_t* abort_flag = &sh->abort;
 
-  griddep_wait();  // the scheduler's list and the split planes
-  const int n_units = p.hdr->n_pairs * p.heads;
-  const int G = p.heads / p.kv_heads;
+  // Bounded wait; a timeout anywhere raises the CTA's abort flag, after which
+  // every wait that would block returns false at once and every role leaves
+  // its loop.
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_test(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity)) return true;
+    *abort_flag = 1;
+    report(p.dev_status, ST_TIMEOUT);
+    return false;
+  };
 
-  // barrier phases (every thread passes the same waits, so the counts agree)
-  uint32_t nq = 0, ns = 0, npv = 0;
-  uint32_t c = 0;                      // K/V halves consumed (all units): stage c & 1
-  uint32_t issued_q = 0, issued_c = 0; // thread 0: copies started (for the wind-down)
-  bool ok = true, lost = false;  // lost: thread 0's wait for the previous PV ran out
-
-  for (;;) {
-    if (tid == 0) s_unit = atomicAdd(&p.hdr->next_unit, 1);
-    __syncthreads();
-    const int u = s_unit;
-    __syncthreads();  // every thread has read s_unit before it is rewritten
-    if (u >= n_units) break;
-    const Pair pr = p.pairs[u / p.heads];
-    const int h = u % p.heads, g = h / G;
-    const int q0 = pr.qt * kBM, q1 = min(q0 + kBM, pr.L);
-    const int i = q0 + tid;
-    const bool row_ok = i < pr.L;
-    // the visited halves [hb, he) of the unit's key tiles
-    auto half_visited = [&](int hf) {
-      const int k0 = hf * kSub;
-      if (k0 >= pr.L) return false;
-      if (p.causal && k0 > q1 - 1) return false;
-      if (p.window >= 0 && (k0 > q1 - 1 + p.window || k0 + kSub - 1 < q0 - p.window)) return false;
-      return true;
-    };
-    int hb = 2 * pr.kt_begin, he = 2 * pr.kt_end;
-    while (hb < he && !half_visited(hb)) ++hb;
-    while (he > hb && !half_visited(he - 1)) --he;
-    const int nsub = he - hb;
-    if (nsub == 0) continue;  // (every valid row sees at least its own key)
-    const int vcol = vt_col(pr.row0, pr.s);
-
-    // copies of half number k of this unit into stage (c0 + k) & 1
-    const uint32_t c0 = c;
-    auto load_half = [&](int k) {
-      const uint32_t cc = c0 + k, st = cc & 1;
-      const int k0 = (hb + k) * kSub;
-      uint8_t* base = sp + kOffStage + st * kStageBytes;
-      mbar_arrive_expect_tx(&kv_full[st], kKVBytes);
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        tma_load_2d(base + kKh + a * kSlabK, &k_h, &kv_full[st], g * kHead + 32 * a, pr.row0 + k0);
-        tma_load_2d(base + kKl + a * kSlabK, &k_l, &kv_full[st], g * kHead + 32 * a, pr.row0 + k0);
-        tma_load_2d(base + kVh + a * kSlabK, &v_h, &kv_full[st], vcol + k0 + 32 * a, g * kHead);
-        tma_load_2d(base + kVl + a * kSlabK, &v_l, &kv_full[st], vcol + k0 + 32 * a, g * kHead);
-      }
-      issued_c = cc + 1;
-    };
-    if (tid == 0) {
-      // every MMA of the previous unit has completed (its last PV was waited
-      // for), so Q and both stages are free
-      mbar_arrive_expect_tx(&q_full, kQBytes);
-#pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        tma_load_2d(sp + kOffQh + a * kSlabQ, &q_h, &q_full, h * kHead + 32 * a, pr.row0 + q0);
-        tma_load_2d(sp + kOffQl + a * kSlabQ, &q_l, &q_full, h * kHead + 32 * a, pr.row0 + q0);
-      }
-      issued_q = nq + 1;
-      load_half(0);
-      if (nsub > 1) load_half(1);
-    }
-    ok = mbar_wait(&q_full, nq & 1);
-    ok = __syncthreads_and(ok);
-    if (!ok) break;
-    ++nq;
-
-    float m = -INFINITY, l = 0.f;
-    for (int k = 0; k < nsub; ++k, ++c) {
-      const uint32_t st = c & 1;
-      const int hf = hb + k, k0 = hf * kSub, kt = hf >> 1;
-      const bool full = kt >= pr.full_begin && kt < pr.full_end;
-      ok = mbar_wait(&kv_full[st], (c >> 1) & 1);
-      ok = __syncthreads_and(ok);
-      if (!ok) break;
-      if (tid == 0) {
-        // S = Q K^T: the two small products first, then the high one
-        tc_fence_after();
-        const uint32_t kb = sb + kOffStage + st * kStageBytes;
-        const uint32_t A[3] = {sb + kOffQl, sb + kOffQh, sb + kOffQh};
-        const uint32_t B[3] = {kb + kKh, kb + kKl, kb + kKh};
-#pragma unroll
-        for (int q = 0; q < 3; ++q)
-#pragma unroll
-          for (int ks = 0; ks < kHead / 8; ++ks)
-            mma_tf32_ss(tS, sdesc_sw128(A[q] + (ks >> 2) * kSlabQ + (ks & 3) * 32, 16, 1024),
-                        sdesc_sw128(B[q] + (ks >> 2) * kSlabK + (ks & 3) * 32, 16, 1024), (q | ks) != 0);
-        tc_commit(&s_done);
-        // the next half's copies go into the stage that the previous half's
-        // PV read: issued as soon as that PV is done, they have the whole
-        // softmax of this half to land
-        if (k > 0 && k + 1 < nsub) {
-          if (mbar_wait(&pv_done, npv & 1)) load_half(k + 1);
-          else lost = true;
+  if (warp == 12) {
+    if (lane == 0) {
+      // ------------------------------------------- TMA producer: units, Q, keys
+      griddep_wait();  // the scheduler's list and the key / value planes
+      const int n_units = p.hdr->n_pairs * p.heads;
+      const int G = p.heads / p.kv_heads;
+      uint32_t n = 0, nq = 0, c = 0;  // units published, query tiles and key halves loaded
+      bool ok = true;
+      for (;; ++n) {
+        const int slot = n & 1;
+        if (!(ok = wait(&sh->unit_empty[slot], ((n >> 1) & 1) ^ 1))) break;
+        UnitInfo inf;
+        inf.u = -1;
+        for (;;) {
+          const int u = atomicAdd(&p.hdr->next_unit, 1);
+          if (u >= n_units) break;
+          const Pair pr = p.pairs[u / p.heads];
+          const int q0 = pr.qt * kBM, q1 = min(q0 + kBM, pr.L);
+          // the halves of the pair's key tiles that hold a visible key
+          auto visited = [&](int hf) {
+            const int k0 = hf * kSub;
+            if (k0 >= pr.L) return false;
+            if (p.causal && k0 > q1 - 1) return false;
+            if (p.window >= 0 && (k0 > q1 - 1 + p.window || k0 + kSub - 1 < q0 - p.window)) return false;
+            return true;
+          };
+          int hb = 2 * pr.kt_begin, he = 2 * pr.kt_end;
+          while (hb < he && !visited(hb)) ++hb;
+          while (he > hb && !visited(he - 1)) --he;
+          if (he == hb) continue;  // (every valid row sees at least its own key)
+          inf.u = u;
+          inf.s = pr.s;
+          inf.h = u % p.heads;
+          inf.g = inf.h / G;
+          inf.row0 = pr.row0;
+          inf.L = pr.L;
+          inf.q0 = q0;
+          inf.hb = hb;
+          inf.nsub = he - hb;
+          inf.ffb = 2 * pr.full_begin;
+          inf.ffe = 2 * pr.full_end;
+          break;
         }
-      }
-      ok = mbar_wait(&s_done, ns & 1) && !lost;
-      ok = __syncthreads_and(ok);
-      if (!ok) break;
-      ++ns;
-      tc_fence_after();
-      uint32_t sv[64];
-      tmem_ld64_wait(tS + lane_off, sv);
-      // online softmax in log2 units (q carries scale * log2(e))
-      float x[64];
-      float mx = -INFINITY;
+        sh->info[slot] = inf;
+        mbar_arrive(&sh->unit_full[slot]);
+        if (inf.u < 0) break;
+        // the raw query tile: two slabs of 32 dims, each as two 64-row boxes
+        if (!(ok = wait(&sh->q_raw_empty, (nq & 1) ^ 1))) break;
+        mbar_arrive_expect_tx(&sh->q_raw_full, 2 * kSlabQ);
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const bool vis = row_ok && (full || visible(i, k0 + j, pr.L, p.causal, p.window));
-        x[j] = vis ? __uint_as_float(sv[j]) : -INFINITY;
-        mx = fmaxf(mx, x[j]);
-      }
-      const float m_new = fmaxf(m, mx);
-      float alpha = 1.f;
-      if (m_new == -INFINITY) {
+        for (int a = 0; a < 2; ++a)
 #pragma unroll
-        for (int j = 0; j < 64; ++j) x[j] = 0.f;
-      } else {
-        alpha = fast_exp2(m - m_new);
-        float rs = 0.f;
+          for (int b = 0; b < 2; ++b)
+            tma_load_2d(smem + kOffQ + a * kSlabQ + b * kSlabK, &qkv_map, &sh->q_raw_full, inf.h * kHead + 32 * a,
+                        inf.row0 + inf.q0 + 64 * b);
+        ++nq;
+        for (int k = 0; k < inf.nsub; ++k, ++c) {
+          const uint32_t st = c % kKStages;
+          if (!(ok = wait(&sh->k_empty[st], ((c / kKStages) & 1) ^ 1))) break;
+          uint8_t* kb = smem + kOffK + st * 2 * kHalfBytes;
+          mbar_arrive_expect_tx(&sh->k_raw_full[st], kHalfBytes);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          x[j] = fast_exp2(x[j] - m_new);
-          rs += x[j];
+          for (int a = 0; a < 2; ++a)
+            tma_load_2d(kb + a * kSlabK, &k_map, &sh->k_raw_full[st], inf.g * kHead + 32 * a,
+                        inf.row0 + (inf.hb + k) * kSub);
         }
-        l = l * alpha + rs;
-        m = m_new;
-      }
-      // PV of the previous half read P from TMEM and accumulated into O: it
-      // completes before P is stored again and O is rescaled
-      if (k > 0) {
-        ok = mbar_wait(&pv_done, npv & 1);
-        ok = __syncthreads_and(ok);
         if (!ok) break;
-        ++npv;
-        tc_fence_after();
       }
+      if (*abort_flag) {
+        // every copy this thread issued lands before the CTA releases its
+        // shared memory: the last fill of each stage, the last query tile
+        for (uint32_t st = 0; st < kKStages; ++st)
+          if (c > st) mbar_wait(&sh->k_raw_full[st], (((c - 1) - ((c - 1 - st) % kKStages)) / kKStages) & 1);
+        if (nq > 0) mbar_wait(&sh->q_raw_full, (nq - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 13) {
+    if (lane == 0) {
+      // -------------------------------------------------- TMA producer: V^T
+      uint32_t n = 0, c = 0;
+      bool ok = true;
+      for (;; ++n) {
+        const int slot = n & 1;
+        if (!(ok = wait(&sh->unit_full[slot], (n >> 1) & 1))) break;
+        const UnitInfo inf = sh->info[slot];
+        mbar_arrive(&sh->unit_empty[slot]);
+        if (inf.u < 0) break;
+        const int vcol = tf32_vt_col(inf.row0, inf.s);
+        for (int k = 0; k < inf.nsub; ++k, ++c) {
+          const uint32_t st = c % kVStages;
+          if (!(ok = wait(&sh->v_empty[st], ((c / kVStages) & 1) ^ 1))) break;
+          uint8_t* vb = smem + kOffV + st * 2 * kHalfBytes;
+          mbar_arrive_expect_tx(&sh->v_raw_full[st], kHalfBytes);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t ph[16], pl[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float v = x[16 * q + e], hi = tf32_hi(v);
-          ph[e] = __float_as_uint(hi);
-          pl[e] = __float_as_uint(v - hi);
+          for (int a = 0; a < 2; ++a)
+            tma_load_2d(vb + a * kSlabK, &v_map, &sh->v_raw_full[st], vcol + (inf.hb + k) * kSub + 32 * a,
+                        inf.g * kHead);
         }
-        tmem_st16(tPh + lane_off + 16 * q, ph);
-        tmem_st16(tPl + lane_off + 16 * q, pl);
+        if (!ok) break;
       }
-      if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        uint32_t ov[64];
-        tmem_ld64_wait(tO + lane_off, ov);
+      if (*abort_flag)
+        for (uint32_t st = 0; st < kVStages; ++st)
+          if (c > st) mbar_wait(&sh->v_raw_full[st], (((c - 1) - ((c - 1 - st) % kVStages)) / kVStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp >= 8 && warp < 12) {
+    // ----------------------------------------------------------- operand split
+    const int ct = tid - 256;  // 0 .. 127
+    uint32_t n = 0, h = 0;
+    bool ok = true;
+    for (;; ++n) {
+      const int slot = n & 1;
+      ok = __all_sync(0xffffffffu, ok && wait(&sh->unit_full[slot], (n >> 1) & 1));
+      if (!ok) break;
+      const UnitInfo inf = sh->info[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->unit_empty[slot]);
+      if (inf.u < 0) break;
+      for (int k = 0; ok && k < inf.nsub; ++k, ++h) {
+        const uint32_t ks = h % kKStages, vs = h % kVStages;
+        ok = __all_sync(0xffffffffu, wait(&sh->k_raw_full[ks], (h / kKStages) & 1));
+        if (!ok) break;
+        uint8_t* kb = smem + kOffK + ks * 2 * kHalfBytes;
+        split_half(kb, kb + kHalfBytes, ct);
+        fence_proxy_async_smem();  // visible to the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->k_ready[ks]);
+        ok = __all_sync(0xffffffffu, wait(&sh->v_raw_full[vs], (h / kVStages) & 1));
+        if (!ok) break;
+        uint8_t* vb = smem + kOffV + vs * 2 * kHalfBytes;
+        split_half(vb, vb + kHalfBytes, ct);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->v_ready[vs]);
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 14) {
+    if (lane == 0) {
+      // ------------------------------------------------------ MMA issuer: S
+      // S(h) = Q K^T, the two small products first, then the high one.  Its
+      // buffer last held S(h-3) and then P(h-3)'s high parts, read by PV(h-3)
+      // from the other issuer: that PV has completed before S(h) is issued.
+      const uint64_t kd0 = sdesc_sw128(smem_u32(smem) + kOffK, 16, 1024);  // descriptor of key stage 0
+      uint32_t n = 0, h = 0;  // units, halves
+      bool ok = true;
+      for (;; ++n) {
+        const int slot = n & 1;
+        if (!(ok = wait(&sh->unit_full[slot], (n >> 1) & 1))) break;
+        const UnitInfo inf = sh->info[slot];
+        mbar_arrive(&sh->unit_empty[slot]);
+        if (inf.u < 0) break;
+        for (int k = 0; k < inf.nsub; ++k, ++h) {
+          const uint32_t st = h % kKStages;
+          if (!(ok = wait(&sh->k_ready[st], (h / kKStages) & 1))) break;
+          if (k == 0 && !(ok = wait(&sh->q_ready, n & 1))) break;
+          if (h >= kSBufs && !(ok = wait(&sh->pv_buf[h % kSBufs], ((h - kSBufs) / kSBufs) & 1))) break;
+          tc_fence_after();
+          // descriptors advance by (byte offset >> 4) in their address field
+          const uint64_t kd = kd0 + ((st * 2 * kHalfBytes) >> 4);
+          const uint32_t tS = tmem + kColS + 64 * (h % kSBufs);
+#pragma unroll 1
+          for (int q = 0; q < 3; ++q) {
+            const uint32_t a = q == 0 ? tmem + kColQl : tmem + kColQh;
+            const uint64_t b = kd + ((q == 1 ? kHalfBytes : 0u) >> 4);
 #pragma unroll
-        for (int d = 0; d < kHead; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
-        tmem_st64(tO + lane_off, ov);
+            for (int ks = 0; ks < kHead / 8; ++ks)
+              mma_tf32_ts(tS, a + ks * 8, b + (((ks >> 2) * kSlabK + (ks & 3) * 32) >> 4), (q | ks) != 0 ? 1u : 0u);
+          }
+          tc_commit(&sh->s_full[h % kSBufs]);
+          tc_commit(&sh->k_empty[st]);
+          if (k + 1 == inf.nsub) tc_commit(&sh->q_free);
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) {  // every MMA this thread issued completes before TMEM is freed
+        tc_commit(&sh->drain[0]);
+        mbar_wait(&sh->drain[0], 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 15) {
+    if (lane == 0) {
+      // ----------------------------------------------------- MMA issuer: PV
+      // O += P(h) V(h), the two small products first, then the high one; a
+      // unit's first half overwrites O once the epilogue of the unit before
+      // it has read O
+      const uint64_t vd0 = sdesc_sw128(smem_u32(smem) + kOffV, 16, 1024);  // descriptor of V^T stage 0
+      uint32_t n = 0, h = 0;
+      bool ok = true;
+      for (;; ++n) {
+        const int slot = n & 1;
+        if (!(ok = wait(&sh->unit_full[slot], (n >> 1) & 1))) break;
+        const UnitInfo inf = sh->info[slot];
+        mbar_arrive(&sh->unit_empty[slot]);
+        if (inf.u < 0) break;
+        for (int k = 0; k < inf.nsub; ++k, ++h) {
+          const uint32_t st = h % kVStages;
+          if (!(ok = wait(&sh->p_full[h % kSBufs], (h / kSBufs) & 1))) break;
+          if (!(ok = wait(&sh->v_ready[st], (h / kVStages) & 1))) break;
+          if (k == 0 && n > 0 && !(ok = wait(&sh->o_free, (n - 1) & 1))) break;
+          tc_fence_after();
+          const uint64_t vd = vd0 + ((st * 2 * kHalfBytes) >> 4);
+          const uint32_t ph = tmem + kColS + 64 * (h % kSBufs), pl = tmem + kColPl + 64 * (h & 1);
+#pragma unroll 1
+          for (int q = 0; q < 3; ++q) {
+            const uint32_t a = q == 0 ? pl : ph;
+            const uint64_t b = vd + ((q == 1 ? kHalfBytes : 0u) >> 4);
+#pragma unroll
+            for (int ks = 0; ks < kSub / 8; ++ks)
+              mma_tf32_ts(tmem + kColO, a + ks * 8, b + (((ks >> 2) * kSlabK + (ks & 3) * 32) >> 4),
+                          (k > 0 || (q | ks) != 0) ? 1u : 0u);
+          }
+          tc_commit(&sh->pv_buf[h % kSBufs]);
+          tc_commit(&sh->v_empty[st]);
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) {
+        tc_commit(&sh->drain[1]);
+        mbar_wait(&sh->drain[1], 0);
+      }
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int c = warp >> 2;                    // key columns 32c .. 32c + 31 of each half; O columns likewise
+    const int r = (warp & 3) * 32 + lane;       // row in the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t h = 0, xc = 0;
+    bool ok = true;
+    UnitInfo inf;
+    // The unit's queries, rotated and scaled, split into TMEM: this thread
+    // takes rotation pairs (t, t + 32) for t in 16c .. 16c + 15 of row r.
+    // Every softmax warp passes the same named barriers in the same order: per
+    // unit two over all eight warps (in load_unit), per half and at the
+    // epilogue one over the two warps of the same rows.  A failed wait is
+    // carried to the next eight-warp barrier, where all leave together.
+    auto load_unit = [&](uint32_t m, bool good) -> bool {
+      const int slot = m & 1;
+      good = __all_sync(0xffffffffu, good && wait(&sh->unit_full[slot], (m >> 1) & 1));
+      if (named_bar_or(1, 256, !good)) {
+        inf.u = -1;
+        return false;
+      }
+      inf = sh->info[slot];
+      named_bar_or(1, 256, false);  // every thread has its copy of the unit
+      if (tid == 0) mbar_arrive(&sh->unit_empty[slot]);
+      if (inf.u < 0) return true;
+      const int pos = inf.q0 + r;
+      const bool rot = pos < inf.L;  // (a row past the sequence's end is never written out)
+      const float* crow = p.cos_t + static_cast<size_t>(rot ? pos : 0) * kHalf + 16 * c;
+      const float* srow = p.sin_t + static_cast<size_t>(rot ? pos : 0) * kHalf + 16 * c;
+      float4 cs[4], sn[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        cs[e] = __ldg(reinterpret_cast<const float4*>(crow) + e);
+        sn[e] = __ldg(reinterpret_cast<const float4*>(srow) + e);
+      }
+      good = __all_sync(0xffffffffu, wait(&sh->q_raw_full, m & 1));
+      // the previous unit's S MMAs have read its Q columns
+      if (m > 0) good = __all_sync(0xffffffffu, good && wait(&sh->q_free, (m - 1) & 1));
+      if (!good) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // pairs 16c + 8 half .. + 7
+        uint32_t hlo[8], hhi[8], llo[8], lhi[8];
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int e = 2 * half + e2;
+          // 16-byte chunk 4c + e of the row in each slab (128-byte swizzle)
+          const uint32_t off = r * 128 + (((4 * c + e) ^ (r & 7)) << 4);
+          const float4 a4 = *reinterpret_cast<const float4*>(smem + kOffQ + off);
+          const float4 b4 = *reinterpret_cast<const float4*>(smem + kOffQ + kSlabQ + off);
+          const float xa[4] = {a4.x, a4.y, a4.z, a4.w}, xb[4] = {b4.x, b4.y, b4.z, b4.w};
+          const float cc[4] = {cs[e].x, cs[e].y, cs[e].z, cs[e].w}, ss[4] = {sn[e].x, sn[e].y, sn[e].z, sn[e].w};
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            float ya = xa[f], yb = xb[f];
+            if (rot) rope_pair(xa[f], xb[f], cc[f], ss[f], ya, yb);
+            ya *= p.qmul;
+            yb *= p.qmul;
+            const float ha = tf32_hi(ya), hb = tf32_hi(yb);
+            hlo[4 * e2 + f] = __float_as_uint(ha);
+            llo[4 * e2 + f] = __float_as_uint(ya - ha);
+            hhi[4 * e2 + f] = __float_as_uint(hb);
+            lhi[4 * e2 + f] = __float_as_uint(yb - hb);
+          }
+        }
+        const uint32_t col = 16 * c + 8 * half;
+        tmem_st8(tmem + kColQh + col + lane_off, hlo);
+        tmem_st8(tmem + kColQh + 32 + col + lane_off, hhi);
+        tmem_st8(tmem + kColQl + col + lane_off, llo);
+        tmem_st8(tmem + kColQl + 32 + col + lane_off, lhi);
       }
       tmem_wait_st();
       tc_fence_before();
-      __syncthreads();
-      if (tid == 0) {
-        // O += P V: the two small products first, then the high one; the
-        // unit's first half overwrites O
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sh->q_raw_empty);  // the raw tile may take the next unit's queries
+        mbar_arrive(&sh->q_ready);
+      }
+      return true;
+    };
+    // One pass per unit: its queries into TMEM (unit m), the previous unit's
+    // epilogue, then this unit's halves.  The queries of unit m go into TMEM
+    // once every S of unit m-1 is done, so its first S overlaps unit m-1's
+    // last PV.
+    UnitInfo cur;
+    cur.u = -1;
+    int i = 0;
+    bool row_ok = false;
+    float l = 0.f;
+    for (uint32_t m = 0;; ++m) {
+      ok = load_unit(m, ok);
+      if (cur.u >= 0) {
+        // epilogue: the row sums of both warps, then the unit's last PV, then O
+        // / l in this warp's 32 output columns
+        sh->xl[c][r] = l;
+        if (named_bar_or(2 + (warp & 3), 64, !ok)) ok = false;  // (the next load_unit barrier ends the loop)
+        const float inv = 1.f / (l + sh->xl[1 - c][r]);
+        // (the partner reads xl[c] before its next barrier with this thread,
+        // which comes before xl is written again)
+        ok = __all_sync(0xffffffffu, ok && wait(&sh->pv_buf[(h - 1) % kSBufs], ((h - 1) / kSBufs) & 1));
         tc_fence_after();
-        const uint32_t vb = sb + kOffStage + st * kStageBytes;
-        const uint32_t A[3] = {tPl, tPh, tPh};
-        const uint32_t B[3] = {vb + kVh, vb + kVl, vb + kVh};
+        if (ok) {
+          uint32_t ov[32];
+          tmem_ld32_wait(tmem + kColO + 32 * c + lane_off, ov);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->o_free);
+          if (row_ok) {
+            float* dst = p.out + static_cast<size_t>(cur.row0 + i) * p.heads * kHead + cur.h * kHead + 32 * c;
 #pragma unroll
-        for (int q = 0; q < 3; ++q)
+            for (int d = 0; d < 32; d += 4)
+              *reinterpret_cast<float4*>(dst + d) =
+                  make_float4(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv,
+                              __uint_as_float(ov[d + 2]) * inv, __uint_as_float(ov[d + 3]) * inv);
+          }
+        }
+      }
+      if (inf.u < 0) break;
+      cur = inf;
+      i = cur.q0 + r;
+      row_ok = i < cur.L;
+      // Online softmax with a lazily moved reference max m_ref: P = 2^(S -
+      // m_ref); O and the row sum l stay relative to m_ref, which moves --
+      // rescaling both -- only when a row's max exceeds it by more than 2^8.
+      // Both warps of a row hold the same m_ref; each sums its own columns.
+      float m_ref = kNone;
+      l = 0.f;
+      for (int k = 0; k < cur.nsub; ++k, ++h) {
+        ok = __all_sync(0xffffffffu, ok && wait(&sh->s_full[h % kSBufs], (h / kSBufs) & 1));
+        tc_fence_after();
+        const uint32_t tS = tmem + kColS + 64 * (h % kSBufs) + 32 * c + lane_off;
+        const uint32_t tPl = tmem + kColPl + 64 * (h & 1) + 32 * c + lane_off;
+        uint32_t sv[32];
+        if (ok) tmem_ld32_wait(tS, sv);
+        const int hf = cur.hb + k, k0 = hf * kSub + 32 * c;  // this warp's first key
+        const bool full = hf >= cur.ffb && hf < cur.ffe;
+        // visible keys of this row among this warp's 32: columns [lo, hi]
+        int lo = 0, hi = 31;
+        if (!full) {
+          hi = min(31, cur.L - 1 - k0);
+          if (p.causal) hi = min(hi, i - k0);
+          if (p.window >= 0) {
+            lo = max(0, i - p.window - k0);
+            hi = min(hi, i + p.window - k0);
+          }
+          if (!row_ok) hi = -1;
+        }
+        // masked columns count as kNone (below every logit)
 #pragma unroll
-          for (int ks = 0; ks < kSub / 8; ++ks)
-            mma_tf32_ts(tO, A[q] + ks * 8, sdesc_sw128(B[q] + (ks >> 2) * kSlabK + (ks & 3) * 32, 16, 1024),
-                        (k | q | ks) != 0);
-        tc_commit(&pv_done);
+        for (int j = 0; j < 32; ++j)
+          if (!(j >= lo && j <= hi)) sv[j] = __float_as_uint(kNone);
+        float m8[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m8[q] = fmaxf(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m8[q] = fmax3(m8[q], __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
+        float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        // the row's maximum over both warps' columns
+        float* xb = &sh->xch[xc & 1][0][0];
+        ++xc;
+        xb[c * kBM + r] = mx;
+        // the two warps of these rows only (barrier 2 + lane quarter, 64 threads)
+        if (named_bar_or(2 + (warp & 3), 64, !ok)) {
+          ok = false;  // (all eight warps learn of it at load_unit's barrier)
+          break;
+        }
+        mx = fmaxf(mx, xb[(1 - c) * kBM + r]);
+        float alpha = 1.f;
+        if (mx > m_ref + kLazy) {
+          if (m_ref != kNone) alpha = fast_exp2(m_ref - mx);
+          m_ref = mx;
+        }
+        // P = 2^(S - m_ref); a masked column (kNone) gives 0, also while the
+        // row has no visible key yet (m_ref = kNone: its reference is taken as 0)
+        const float mr = m_ref == kNone ? 0.f : m_ref;
+        // P-low buffer h mod 2 was last read by PV(h-2)
+        if (h >= 2) {
+          ok = __all_sync(0xffffffffu, wait(&sh->pv_buf[(h - 2) % kSBufs], ((h - 2) / kSBufs) & 1));
+          tc_fence_after();
+        }
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {  // 16 columns at a time: P high over S, P low beside
+          uint32_t ph[16], pl[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float pe = fast_exp2(__uint_as_float(sv[16 * q + e]) - mr), hv = tf32_hi(pe);
+            s4[e & 3] += pe;
+            ph[e] = __float_as_uint(hv);
+            pl[e] = __float_as_uint(pe - hv);
+          }
+          tmem_st16(tS + 16 * q, ph);
+          tmem_st16(tPl + 16 * q, pl);
+        }
+        l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+        // O is rescaled once PV(h-1) has accumulated into it (and before
+        // PV(h), which waits for this half's P)
+        if (k > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          ok = __all_sync(0xffffffffu, ok && wait(&sh->pv_buf[(h - 1) % kSBufs], ((h - 1) / kSBufs) & 1));
+          tc_fence_after();
+          if (ok) {
+            uint32_t ov[32];
+            tmem_ld32_wait(tmem + kColO + 32 * c + lane_off, ov);
+#pragma unroll
+            for (int d = 0; d < 32; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
+            tmem_st32(tmem + kColO + 32 * c + lane_off, ov);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(&sh->p_full[h % kSBufs]);
       }
     }
-    if (!ok) break;
-    // epilogue: the last PV, then O / l
-    ok = mbar_wait(&pv_done, npv & 1);
-    ok = __syncthreads_and(ok);
-    if (!ok) break;
-    ++npv;
-    tc_fence_after();
-    uint32_t ov[64];
-    tmem_ld64_wait(tO + lane_off, ov);
-    tc_fence_before();
-    if (row_ok) {
-      const float inv = 1.f / l;
-      float* dst = p.out + static_cast<size_t>(pr.row0 + i) * p.heads * kHead + h * kHead;
-#pragma unroll
-      for (int d = 0; d < kHead; d += 4)
-        *reinterpret_cast<float4*>(dst + d) =
-            make_float4(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv,
-                        __uint_as_float(ov[d + 2]) * inv, __uint_as_float(ov[d + 3]) * inv);
-    }
-    __syncthreads();  // every O load is done before the next unit's first PV
   }
 
-  if (!ok) {
-    // a wait ran past its limit: report, then let the copies and MMAs this
-    // CTA started finish (bounded) before TMEM is freed
-    if (tid == 0) {
-      report(p.dev_status, ST_TIMEOUT);
-      if (issued_q > nq) mbar_wait(&q_full, nq & 1);
-      for (uint32_t cc = c; cc < issued_c; ++cc) mbar_wait(&kv_full[cc & 1], (cc >> 1) & 1);
-      tc_commit(&drain);
-      mbar_wait(&drain, 0);
-    }
-  }
+  // Wind down: after an abort the producer and the issuer have waited
+  // (bounded) for their own copies and MMAs in flight; then TMEM is freed.
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -459,22 +784,14 @@ __global__ void __launch_bounds__(kT3Threads, 1)
 
 }  // namespace
 
-cudaError_t launch_tf32_clear(int n_seqs, int total, int heads, int kv_heads, void* ws, cudaStream_t st) {
-  // the gaps between the sequences' value columns read as zeros (a key tile
-  // of a sequence may reach into them; its P there is 0, and 0 * 0 = 0)
-  const Tf32Planes pl = tf32_planes(n_seqs, total, heads, kv_heads);
-  return cudaMemsetAsync(static_cast<char*>(ws) + pl.vh, 0, pl.end - pl.vh, st);
-}
-
-cudaError_t launch_tf32_split(const float* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
-                              float scale, const float* cos_t, const float* sin_t, int rope_len, void* ws,
-                              cudaStream_t st) {
-  const Tf32Planes pl = tf32_planes(n_seqs, total, heads, kv_heads);
+cudaError_t launch_tf32_kv_prep(const float* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
+                                const float* cos_t, const float* sin_t, int rope_len, void* ws, cudaStream_t st) {
+  const Tf32Planes pl = tf32_planes(n_seqs, total, kv_heads);
   char* w = static_cast<char*>(ws);
   // launched with programmatic stream serialization: it starts while the
   // scheduler (which lets dependents start at once) still runs
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((total + kSplitRows - 1) / kSplitRows);
+  cfg.gridDim = dim3((total + kPrepRows - 1) / kPrepRows);
   cfg.blockDim = dim3(256);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -482,35 +799,38 @@ cudaError_t launch_tf32_split(const float* qkv, const int32_t* cu, int n_seqs, i
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tf32_split_kernel, qkv, cu, n_seqs, total, heads, kv_heads,
-                            scale * 1.4426950408889634f, cos_t, sin_t, rope_len, pl.tp,
-                            reinterpret_cast<float*>(w + pl.qh), reinterpret_cast<float*>(w + pl.ql),
-                            reinterpret_cast<float*>(w + pl.kh), reinterpret_cast<float*>(w + pl.kl),
-                            reinterpret_cast<float*>(w + pl.vh), reinterpret_cast<float*>(w + pl.vl));
+  return cudaLaunchKernelEx(&cfg, tf32_kv_prep_kernel, qkv, cu, n_seqs, total, heads, kv_heads, cos_t, sin_t,
+                            rope_len, pl.tp, reinterpret_cast<float*>(w + pl.kr), reinterpret_cast<float*>(w + pl.vt));
 }
 
-cudaError_t launch_prefill_3xtf32(const CUtensorMap* q_h, const CUtensorMap* q_l, const CUtensorMap* k_h,
-                                  const CUtensorMap* k_l, const CUtensorMap* v_h, const CUtensorMap* v_l,
-                                  int heads, int kv_heads, int window, int causal, float* out, void* ws,
-                                  int32_t* dev_status, cudaStream_t st) {
-  static int configured[64] = {0};
+cudaError_t launch_prefill_3xtf32(const CUtensorMap* qkv_map, const CUtensorMap* k_map, const CUtensorMap* v_map,
+                                  int heads, int kv_heads, int window, int causal, float scale, const float* cos_t,
+                                  const float* sin_t, float* out, void* ws, int32_t* dev_status, cudaStream_t st) {
+  static int configured[64] = {};
   int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_3xtf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kT3Smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = 1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if (dev >= 64 || !configured[dev]) {
+    if ((e = cudaFuncSetAttribute(prefill_3xtf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kT3Smem)) !=
+        cudaSuccess)
+      return e;
+    if (dev < 64) configured[dev] = 1;
   }
   T3Params prm;
   prm.heads = heads;
   prm.kv_heads = kv_heads;
   prm.window = window;
   prm.causal = causal;
+  prm.qmul = scale * 1.4426950408889634f;
+  prm.cos_t = cos_t;
+  prm.sin_t = sin_t;
   prm.out = out;
   prm.hdr = static_cast<WsHeader*>(ws);
   prm.pairs = ws_pairs(ws);
   prm.dev_status = dev_status;
+  // launched with programmatic stream serialization: its prologue overlaps
+  // the kernels before it, whose results the producer waits for (griddep_wait)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms);
   cfg.blockDim = dim3(kT3Threads);
@@ -521,7 +841,7 @@ cudaError_t launch_prefill_3xtf32(const CUtensorMap* q_h, const CUtensorMap* q_l
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_3xtf32_kernel, *q_h, *q_l, *k_h, *k_l, *v_h, *v_l, prm);
+  return cudaLaunchKernelEx(&cfg, prefill_3xtf32_kernel, *qkv_map, *k_map, *v_map, prm);
 }
 
 }  // namespace kime

@@ -116,8 +116,9 @@ def test_window_at_least_length_is_bitwise_full(cuda_lib):
 
 
 def test_packing_order_does_not_change_a_sequence_bitwise(cuda_lib):
-    # the transposed values sit at other columns in another packing; the
-    # results of a sequence do not move
+    # a sequence's rows and transposed value columns sit elsewhere in another
+    # packing (and its last key half reaches into other neighbours); its
+    # results do not move
     lengths, H, Hkv = [333, 10, 129, 512], 6, 3
     qkv = random_qkv(lengths, H, Hkv, torch.float32, 1.0, seed=66)
     cu = cu_from_lengths(lengths)
@@ -169,7 +170,7 @@ def test_workspace_too_small_and_dtype_errors_raise(cuda_lib):
     qkv = random_qkv(lengths, H, H, torch.float32, 1.0, seed=69).to(dev)
     cu = cu_from_lengths(lengths).to(dev)
     c, s = gpu_tables(1e4, 64)
-    small = torch.empty(kime.kime_attn_workspace_bytes(0, 2, 49), dtype=torch.uint8, device=dev)
+    small = torch.empty(kime.kime_attn_workspace_bytes(4, 2, 49, H, H) - 8, dtype=torch.uint8, device=dev)
     with pytest.raises(kime.KimeError):
         kime.kime_attn_varlen(qkv, cu, 40, H, H, -1, False, 0.125, c, s, workspace=small, precision="3xtf32")
     with pytest.raises(TypeError):
@@ -177,8 +178,8 @@ def test_workspace_too_small_and_dtype_errors_raise(cuda_lib):
 
 
 def test_replays_from_a_cuda_graph(cuda_lib):
-    # the memset, scheduler, split pass and attention kernel are all on the
-    # given stream and allocate nothing: one capture, replayed on new inputs
+    # the scheduler, preparation pass and attention kernel are all on the given
+    # stream and allocate nothing: one capture, replayed on new inputs
     dev = torch.device("cuda")
     lengths, H, Hkv = [700, 1, 129, 300], 4, 2
     cu = cu_from_lengths(lengths).to(dev)
