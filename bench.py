@@ -542,6 +542,10 @@ def end_to_end(args, dev, stream, flush, run, world):
     h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in run.outs]
     d_qkv = torch.empty_like(c.qkv)
     cu_h = c.cu_seqlens.tolist()
+    # n groups of whole sequences, about equal in tokens: fewer groups cost
+    # fewer calls (each with its own scheduler, preparation and tail), more
+    # groups a shorter first copy in and last copy out; on the ModernBERT-large
+    # pair 4 groups measured 1.93 ms per step, 8 groups 2.01, 2 groups 2.32
     n_groups = max(1, min(args.e2e_groups, len(c.lengths)))
     bounds = [0]
     for g in range(1, n_groups):  # split at the sequence boundary nearest g/n of the tokens
@@ -626,7 +630,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--e2e-graph", type=int, default=1, help="replay the end-to-end step from a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (e2e null): profiling runs")
-    ap.add_argument("--e2e-groups", type=int, default=8,
+    ap.add_argument("--e2e-groups", type=int, default=4,
                     help="sequence groups the end-to-end step pipelines its copies and calls over")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s load before the timed steps")
