@@ -293,3 +293,26 @@ def test_host_argument_errors_raise(cuda_lib):
     e = kime.kime_attn_varlen(qkv[:0], torch.zeros(1, dtype=torch.int32, device=dev), 0, 2, 2, -1, False,
                               0.125, c, s)
     assert e.shape[0] == 0
+
+
+def test_narrow_window_over_long_sequences_rotates_in_the_attention_kernel(cuda_lib):
+    # A window of at most 128 over sequences of mean length >= 1024 runs the
+    # kernel that rotates its own tiles whatever the workspace: the minimal
+    # and the row-preparing workspaces give the same bits there, and the
+    # result meets the BF16 contract against the oracle (sampled rows).
+    dev = torch.device("cuda")
+    lengths, H, Hkv = [1500, 1100, 1300], 4, 2
+    cu = cu_from_lengths(lengths)
+    qkv = random_qkv(lengths, H, Hkv, torch.bfloat16, 1.5, seed=14).to(dev)
+    T, n, mx = sum(lengths), len(lengths), max(lengths)
+    c, s = gpu_tables(1e4, mx)
+    outs = {}
+    for op in (0, 3):
+        ws = torch.empty(kime.kime_attn_workspace_bytes(op, n, T, H, Hkv), dtype=torch.uint8, device=dev)
+        outs[op] = kime.kime_attn_varlen(qkv, cu.to(dev), mx, H, Hkv, 64, False, 0.125, c, s, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[3])
+    rows, hs = sample_items(cu.numpy(), H, 200, seed=15)
+    ref = run_oracle_varlen(qkv.cpu(), cu, H, Hkv, 64, False, 0.125, 1e4, mx, rows=rows, heads=hs)
+    g = outs[3].float().cpu().reshape(T, H, 64)[torch.from_numpy(rows).long(), torch.from_numpy(hs).long()]
+    check_bf16(g.numpy(), ref, "window 64, long sequences")
