@@ -56,7 +56,7 @@ typedef enum {
  * as three TF32 products each (x = hi + lo, hi = x rounded to TF32; a b taken
  * as a_lo b_hi + a_hi b_lo + a_hi b_hi, FP32 accumulate): the FP32 accuracy
  * contract at TF32 tensor rates (kime-cuda's FP32 attention on tensor cores);
- * needs kime_attn_workspace_bytes(4, ...) bytes of workspace. */
+ * the workspace of op 0 suffices (op 4 gives the same size). */
 typedef enum {
   KIME_F32 = 0,
   KIME_BF16 = 1,
@@ -108,19 +108,17 @@ typedef enum {
  *               order, so the last bits of the output may differ).  Not for
  *               a window of at most 128 over sequences of mean length 1024
  *               or more: there the kernel that rotates its own tiles is the
- *               faster one and runs whatever the workspace.  KIME_F32_3XTF32 needs
- *               kime_attn_workspace_bytes(4, ...) bytes (KIME_ERANGE if less)
+ *               faster one and runs whatever the workspace.
  * BF16 runs on the tensor cores (tcgen05, FP32 accumulate) with f16 operands:
  * rotated keys, scaled rotated queries and values are rounded to f16, so they
  * must lie within its range (|x| <= 65504; beyond, they saturate and
  * KIME_DEV_RANGE is set).  FP32 qkv with
  * KIME_F32 / KIME_F32_F16OUT / KIME_F32_BF16OUT runs on FP32 FMA.  Launches:
  * the device scheduler, the row preparation when the workspace has room for
- * it, then the attention kernel.  KIME_F32_3XTF32 enqueues the scheduler, a
- * preparation pass (keys rotated, values transposed, FP32, into the
- * workspace) and the tensor-core attention kernel, which splits every operand
- * into TF32 high and low parts itself and reads, rotates and scales the
- * queries from qkv. */
+ * it, then the attention kernel.  KIME_F32_3XTF32 enqueues the scheduler and
+ * one tensor-core kernel that reads the FP32 qkv rows itself (queries and keys
+ * rotated, queries scaled, every operand split into TF32 high and low parts,
+ * values transposed, all in shared memory and tensor memory). */
 int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int n_seqs, int total_tokens,
                      int max_seqlen, int heads, int kv_heads, int head_dim, int window, int causal, float scale,
                      const float* rope_cos, const float* rope_sin, int rope_len, void* out, void* workspace,
@@ -231,10 +229,8 @@ int kime_chunk_step(const void* qkv, const int32_t* cu_seqlens, const int32_t* p
  * uses n_seqs, total_tokens) or op 3 (varlen with room for the prepared qkv
  * rows, about total_tokens * 128 * (heads + 2 * kv_heads) bytes more: uses
  * n_seqs, total_tokens, heads, kv_heads) or op 4 (varlen with KIME_F32_3XTF32:
- * op 0 at a 1 KB boundary, then two planes, each 1 KB aligned: rotated keys
- * [total_tokens, 64 * kv_heads] f32 and transposed values [64 * kv_heads, tp]
- * f32, with tp = 4 * ceil(total_tokens / 4) + 68 * n_seqs).  Returns 0 for an
- * unknown op or malformed sizes. */
+ * the size of op 0; heads and kv_heads are checked).  Returns 0 for an unknown
+ * op or malformed sizes. */
 size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads, int kv_heads, int cap);
 
 /* kime_qkv_proj -- the QKV projection of a packed batch, the step before
@@ -309,9 +305,9 @@ int kime_attn_debug_tiles_chunk(const int32_t* cu_seqlens, const int32_t* pos, i
  * library, held by every GPU that loads the library until the process exits.
  * Returns KIME_ERANGE, launching nothing, when the batch needs more scratch than
  * that (kime_attn_workspace_bytes(0, n_seqs, total_tokens, ...) is the need:
- * about 48 bytes per 128 tokens plus 64 per sequence; with KIME_F32_3XTF32 it
- * is kime_attn_workspace_bytes(4, ...), which only small batches fit; a BF16
- * batch has its rows prepared only when they fit in the array too).  The first
+ * about 48 bytes per 128 tokens plus 64 per sequence, KIME_F32_3XTF32
+ * included; a BF16 batch has its rows prepared only when they fit in the
+ * array too).  The first
  * call on a device looks up the array's device address with that device
  * current; make it before any stream capture.  All calls share the array, so calls that
  * overlap on the GPU race; order them on one stream.  Allocates nothing. */

@@ -156,8 +156,7 @@ def kime_attn_varlen(qkv, cu_seqlens, max_seqlen, heads, kv_heads, window, causa
         out = torch.empty((T, heads * 64), dtype=out_dtype or qkv.dtype, device=qkv.device)
     code = _dtype_code(qkv, out.dtype, precision)
     if workspace is None:
-        # BF16 qkv: room for the prepared rows, which the faster kernel reads;
-        # 3xTF32: room for the rotated-key and transposed-value planes
+        # BF16 qkv: room for the prepared rows, which the faster kernel reads
         op = 3 if qkv.dtype == torch.bfloat16 else (4 if code == KIME_F32_3XTF32 else 0)
         need = kime_attn_workspace_bytes(op, n_seqs, T, heads, kv_heads)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=qkv.device)

@@ -153,9 +153,9 @@ size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads
     if (total_tokens < 0 || !heads_ok(heads, kv_heads, kime::kHead)) return 0;
     return prep_ws_bytes(n_seqs, total_tokens, heads, kv_heads);
   }
-  if (op == 4) {
+  if (op == 4) {  // the 3xTF32 path needs no more scratch than op 0
     if (total_tokens < 0 || !heads_ok(heads, kv_heads, kime::kHead)) return 0;
-    return kime::tf32_planes(n_seqs, total_tokens, kv_heads).end;
+    return varlen_ws_bytes(n_seqs, total_tokens);
   }
   return 0;
 }
@@ -184,25 +184,14 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
   const int max_pairs = kime::max_pairs_for(n_seqs, total_tokens);
   int rc;
   if (dtype == KIME_F32_3XTF32) {
-    // FP32 on the tensor cores: scheduler, preparation pass (beside it), attention
-    const kime::Tf32Planes pl = kime::tf32_planes(n_seqs, total_tokens, kv_heads);
-    if (workspace_bytes < pl.end) return KIME_ERANGE;
-    char* w = static_cast<char*>(workspace);
-    const long long hk = 64LL * kv_heads;
-    CUtensorMap qmap, kmap, vmap;
-    if ((rc = encode_f32_plane_map(&qmap, qkv, W, total_tokens, 64)) ||
-        (rc = encode_f32_plane_map(&kmap, w + pl.kr, hk, total_tokens, 64)) ||
-        (rc = encode_f32_plane_map(&vmap, w + pl.vt, pl.tp, hk, 64)))
-      return rc;
+    // FP32 on the tensor cores: the scheduler, then the attention kernel on the raw qkv rows
+    CUtensorMap qmap;
+    if ((rc = encode_f32_plane_map(&qmap, qkv, W, total_tokens, 64))) return rc;
     if ((rc = cuda_status(kime::launch_schedule(cu_seqlens, nullptr, n_seqs, total_tokens, max_seqlen, causal,
                                                 window, 0, 0, workspace, max_pairs, dev_status, st))))
       return rc;
-    if ((rc = cuda_status(kime::launch_tf32_kv_prep(static_cast<const float*>(qkv), cu_seqlens, n_seqs, total_tokens,
-                                                    heads, kv_heads, rope_cos, rope_sin, rope_len, workspace, st))))
-      return rc;
-    return cuda_status(kime::launch_prefill_3xtf32(&qmap, &kmap, &vmap, heads, kv_heads, window, causal, scale,
-                                                   rope_cos, rope_sin, static_cast<float*>(out), workspace,
-                                                   dev_status, st));
+    return cuda_status(kime::launch_prefill_3xtf32(&qmap, heads, kv_heads, window, causal, scale, rope_cos, rope_sin,
+                                                   static_cast<float*>(out), workspace, dev_status, st));
   }
   rc = cuda_status(kime::launch_schedule(cu_seqlens, nullptr, n_seqs, total_tokens, max_seqlen, causal, window,
                                          0, 0, workspace, max_pairs, dev_status, st));

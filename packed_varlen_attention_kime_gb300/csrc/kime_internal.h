@@ -70,28 +70,6 @@ inline size_t varlen_workspace_bytes(int n_seqs, int total_tokens) {
   return sizeof(WsHeader) + static_cast<size_t>(max_pairs_for(n_seqs, total_tokens)) * sizeof(Pair) +
          static_cast<size_t>(max_duos_for(n_seqs, total_tokens)) * sizeof(Duo);
 }
-// FP32 attention on the tensor cores (3xTF32): after the scheduler's lists (at
-// a 1 KB boundary) two FP32 planes, each 1 KB aligned: rotated keys
-// [total, kv_heads*64], and values transposed, [kv_heads*64, tp], token j of
-// sequence s in column tf32_vt_col(cu[s], s) + (j - cu[s]).  Each sequence
-// starts at a multiple of 4 columns (16 bytes: a TMA x coordinate rule) and is
-// followed by at least 65 columns before the next one starts, of which the
-// preparation pass zeroes those up to the sequence's next multiple of 64
-// keys: every 64-key half the attention kernel reads then lies in its own
-// sequence's columns, with zeros (never uninitialised bits) past its end.
-struct Tf32Planes {
-  size_t kr, vt, end;
-  int tp;  // columns of the transposed value plane
-};
-__host__ __device__ inline int tf32_vt_col(int cu_s, int s) { return 4 * ((cu_s + 3) >> 2) + 68 * s; }
-inline Tf32Planes tf32_planes(int n_seqs, int total_tokens, int kv_heads) {
-  Tf32Planes p;
-  p.tp = tf32_vt_col(total_tokens, n_seqs);
-  p.kr = align_up(varlen_workspace_bytes(n_seqs, total_tokens), 1024);
-  p.vt = p.kr + align_up(static_cast<size_t>(total_tokens) * kv_heads * kHead * 4, 1024);
-  p.end = p.vt + align_up(static_cast<size_t>(kv_heads) * kHead * p.tp * 4, 1024);
-  return p;
-}
 inline Pair* ws_pairs(void* ws) { return reinterpret_cast<Pair*>(static_cast<char*>(ws) + sizeof(WsHeader)); }
 inline Duo* ws_duos(void* ws, int max_pairs) {
   return reinterpret_cast<Duo*>(static_cast<char*>(ws) + sizeof(WsHeader) + static_cast<size_t>(max_pairs) * sizeof(Pair));
@@ -141,17 +119,13 @@ cudaError_t launch_qkv_proj(const CUtensorMap* x_map, const CUtensorMap* w_map, 
 // queries rotated at their positions and scaled by scale * log2(e), keys
 // rotated, all rounded to f16, values widened to f16; out [total, W] f16.
 // Any of them beyond the f16 range (saturated) sets ST_RANGE in dev_status.
-// 3xTF32 FP32 path: the scheduler, beside it the preparation pass (keys
-// rotated, values transposed, both FP32, into the planes of tf32_planes()),
-// then the attention kernel, which reads the queries from the FP32 qkv rows
-// through qkv_map (f32 [total, W]) and the planes through k_map / v_map, all
-// with 32-column x 64-row boxes and 128-byte swizzle, and writes out [total,
-// heads*64] f32.
-cudaError_t launch_tf32_kv_prep(const float* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
-                                const float* cos_t, const float* sin_t, int rope_len, void* ws, cudaStream_t st);
-cudaError_t launch_prefill_3xtf32(const CUtensorMap* qkv_map, const CUtensorMap* k_map, const CUtensorMap* v_map,
-                                  int heads, int kv_heads, int window, int causal, float scale, const float* cos_t,
-                                  const float* sin_t, float* out, void* ws, int32_t* dev_status, cudaStream_t st);
+// 3xTF32 FP32 path: after the scheduler, one kernel that reads the FP32 qkv
+// rows through qkv_map (f32 [total, W], 32-column x 64-row boxes, 128-byte
+// swizzle), rotates, scales, splits and transposes its operands itself and
+// writes out [total, heads*64] f32.
+cudaError_t launch_prefill_3xtf32(const CUtensorMap* qkv_map, int heads, int kv_heads, int window, int causal,
+                                  float scale, const float* cos_t, const float* sin_t, float* out, void* ws,
+                                  int32_t* dev_status, cudaStream_t st);
 cudaError_t launch_qkv_prep(const void* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
                             float scale, const float* cos_t, const float* sin_t, int rope_len, void* out,
                             int32_t* dev_status, cudaStream_t st);

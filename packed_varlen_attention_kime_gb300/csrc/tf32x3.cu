@@ -12,16 +12,9 @@
 // accumulation, leaving out a_lo b_lo (<= 2^-22 |a b|) and the truncation of
 // lo to TF32 (<= 2^-21 |a b|): FP32-level accuracy at TF32 tensor rates.
 //
-// Two kernels:
-//   prep    beside the scheduler, one pass over the qkv rows: keys rotated
-//           (the float32 evaluation of every kernel here) into a key plane;
-//           values transposed into a value plane (V^T is the K-major B
-//           operand of O += P V; the TF32 MMA takes its operands K-major
-//           here), each sequence's columns followed by zeros up to its next
-//           multiple of 64 keys.  Both FP32, the size of the raw rows.
-//   attend  persistent CTAs of 512 threads over (128-row query tile, head)
-//           units of the scheduler's list, the unit's keys visited in 64-key
-//           halves:
+// One kernel, after the scheduler: persistent CTAs of 512 threads over
+// (128-row query tile, head) units of the scheduler's list, reading the FP32
+// qkv rows as they are and visiting the unit's keys in 64-key halves:
 //     warps 0-7   softmax: warps w and w + 4 share TMEM lanes 32 (w mod 4) ..
 //                 +31 (rows of the tile) and take key columns 0-31 and 32-63
 //                 of each half; they exchange their partial row maxima
@@ -32,16 +25,20 @@
 //                 query tile from shared memory, rotate it, multiply it by
 //                 scale * log2(e) (the softmax then works in base 2) and store
 //                 its high and low parts in TMEM: the A operand of S = Q K^T.
-//     warps 8-11  operand split: each half's keys and V^T, as loaded, split
-//                 in place into high parts, low parts beside them
+//     warps 8-11  operand preparation: each half's keys, as loaded, rotated
+//                 at their positions (the float32 evaluation of every kernel
+//                 here) and split in place (high parts over the raw values,
+//                 low parts beside them); its values split and transposed
+//                 (V^T is the K-major B operand of O += P V; the TF32 MMA
+//                 takes its operands K-major here)
 //     warp 12     TMA producer of the raw query tiles and the key halves (a
 //                 3-stage ring); it also claims the units
-//     warp 13     TMA producer of the V^T halves (a 2-stage ring)
+//     warp 13     TMA producer of the value halves (a 2-stage ring)
 //     warps 14-15 MMA issuers (one thread each; one thread issuing alone
 //                 cannot keep up with these small MMAs): warp 14 issues S(h) =
 //                 Q K^T as three 128x64x64 TF32 chains, A from TMEM; warp 15
-//                 O += P(h) V(h) as three chains, A = P from TMEM.  With two S
-//                 buffers S(h+1) runs while the softmax works on S(h) and
+//                 O += P(h) V(h) as three chains, A = P from TMEM.  With three
+//                 S buffers S(h+1) runs while the softmax works on S(h) and
 //                 PV(h) while it works on S(h+1).  The next unit's queries
 //                 are stored to TMEM before the epilogue of the current one,
 //                 so S of its first half runs while the current unit's last
@@ -119,110 +116,44 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
-// ------------------------------------------------------------------- prep
-constexpr int kPrepRows = 32;  // tokens per CTA
-
-__global__ void __launch_bounds__(256)
-    tf32_kv_prep_kernel(const float* __restrict__ qkv, const int32_t* __restrict__ cu, int n_seqs, int total,
-                        int heads, int kv_heads, const float* __restrict__ cos_t, const float* __restrict__ sin_t,
-                        int rope_len, int tp, float* __restrict__ kr, float* __restrict__ vt) {
-  __shared__ float vs[kPrepRows][kHead + 1];
-  __shared__ int s_col[kPrepRows], s_pos[kPrepRows], s_pad[kPrepRows];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int j0 = blockIdx.x * kPrepRows;
-  const size_t W = static_cast<size_t>(kHead) * (heads + 2 * kv_heads);
-  if (tid < kPrepRows) {
-    const int j = j0 + tid;
-    int col = -1, pos = -1, pad = 0;
-    if (j < total) {
-      // the sequence owning row j: the largest s with cu[s] <= j
-      int lo = 0, hi = n_seqs - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(cu + mid) <= j) lo = mid;
-        else hi = mid - 1;
-      }
-      const int c0 = __ldg(cu + lo), c1 = __ldg(cu + lo + 1);
-      pos = j - c0;
-      // (with a malformed cu the scheduler reports it and skips the sequence;
-      // here only the plane's bounds matter)
-      if (pos >= 0 && c0 >= 0 && c0 <= total) {
-        const long long c = static_cast<long long>(tf32_vt_col(c0, lo)) + pos;
-        col = c < tp ? static_cast<int>(c) : -1;
-        // the sequence's last token also zeroes the columns up to its next
-        // multiple of 64 keys
-        if (col >= 0 && j + 1 == c1) {
-          const int L = c1 - c0;
-          pad = min((L + kSub - 1) / kSub * kSub - L, tp - 1 - col);
-        }
-      }
-    }
-    s_col[tid] = col;
-    s_pos[tid] = pos;
-    s_pad[tid] = pad;
-  }
-  __syncthreads();
-  // keys: warp w rotates tokens w, w + 8, ...; lane l takes the pair (l, l + 32)
-  const int hk = kv_heads * kHead;
-  for (int t = warp; t < kPrepRows; t += 8) {
-    const int j = j0 + t;
-    if (j >= total) break;
-    const int pos = s_pos[t];
-    const bool rot = pos >= 0 && pos < rope_len;  // a row of no valid sequence: not rotated
-    const float c = rot ? __ldg(cos_t + static_cast<size_t>(pos) * kHalf + lane) : 1.f;
-    const float s = rot ? __ldg(sin_t + static_cast<size_t>(pos) * kHalf + lane) : 0.f;
-    const float* x = qkv + static_cast<size_t>(j) * W + heads * kHead;
-    float* d = kr + static_cast<size_t>(j) * hk;
-    for (int g = 0; g < kv_heads; ++g) {
-      const float a = __ldg(x + g * kHead + lane), b = __ldg(x + g * kHead + lane + kHalf);
-      float ya = a, yb = b;
-      if (rot) rope_pair(a, b, c, s, ya, yb);
-      d[g * kHead + lane] = ya;
-      d[g * kHead + lane + kHalf] = yb;
-    }
-  }
-  // values: one kv head at a time through shared memory, written transposed
-  // (consecutive threads: consecutive tokens of one dimension)
-  for (int g = 0; g < kv_heads; ++g) {
-    __syncthreads();
-    for (int e = tid; e < kPrepRows * kHead; e += 256) {
-      const int t = e / kHead, d = e % kHead, j = j0 + t;
-      vs[t][d] = j < total ? __ldg(qkv + static_cast<size_t>(j) * W + (heads + kv_heads + g) * kHead + d) : 0.f;
-    }
-    __syncthreads();
-    for (int e = tid; e < kPrepRows * kHead; e += 256) {
-      const int d = e / kPrepRows, t = e % kPrepRows;
-      const int col = s_col[t];
-      if (col >= 0) vt[static_cast<size_t>(g * kHead + d) * tp + col] = vs[t][d];
-    }
-  }
-  // the zero columns after each sequence that ends in this CTA's tokens
-  for (int t = 0; t < kPrepRows; ++t) {
-    const int pad = s_pad[t];  // (uniform across the CTA)
-    if (pad <= 0) continue;
-    const int col = s_col[t] + 1;
-    for (int e = tid; e < pad * hk; e += 256) vt[static_cast<size_t>(e / pad) * tp + col + e % pad] = 0.f;
-  }
-  // runs beside the scheduler (it reads none of its output) and ends only
-  // after it, so the attention kernel, which waits for this pass, also finds
-  // the scheduler's lists complete
-  griddep_wait();
-}
-
-// A half's operand in shared memory, split in place: the FP32 values (two
-// slabs of 64 rows x 32 columns as the TMA wrote them) become their TF32
-// high parts, and the low parts go to the same offsets of lo.  The 128
-// threads of the split warps take consecutive 16-byte chunks.
-__device__ __forceinline__ void split_half(uint8_t* hi, uint8_t* lo, int ct) {
-  float4 x[8];
+// Keys of one half, in place: the raw tile (two slabs: dims 0-31 and 32-63,
+// 64 rows, 128-byte swizzle) rotated at positions k0 + j (rows at or past L
+// are masked keys: left unrotated, their table rows may not exist) and split,
+// high parts over the raw values, low parts into kl at the same offsets.
+// Element (j, d) and its rotation partner (j, d + 32) sit at the same offset
+// of the two slabs; the 16-byte chunk at offset o of a slab holds row o / 128,
+// dims 4c .. 4c + 3 with c = (o / 16 mod 8) xor (row mod 8).  The 128
+// threads of the split warps take consecutive chunks.
+__device__ __forceinline__ void prep_keys(uint8_t* kh, uint8_t* kl, int k0, int L, const float* __restrict__ cos_t,
+                                          const float* __restrict__ sin_t, int ct) {
+  // every load first (the table rows come from L2), then the arithmetic and the stores
+  float4 a[4], b[4], cs[4], sn[4];
 #pragma unroll
-  for (int it = 0; it < 8; ++it) x[it] = *reinterpret_cast<const float4*>(hi + (ct + 128 * it) * 16);
+  for (int it = 0; it < 4; ++it) {
+    const int cp = ct + 128 * it;
+    const int j = cp >> 3, c = (cp & 7) ^ (j & 7);
+    a[it] = *reinterpret_cast<const float4*>(kh + cp * 16);
+    b[it] = *reinterpret_cast<const float4*>(kh + kSlabK + cp * 16);
+    const int pos = min(k0 + j, L - 1);  // (rows at or past L are not rotated below)
+    cs[it] = __ldg(reinterpret_cast<const float4*>(cos_t + static_cast<size_t>(pos) * kHalf + 4 * c));
+    sn[it] = __ldg(reinterpret_cast<const float4*>(sin_t + static_cast<size_t>(pos) * kHalf + 4 * c));
+  }
 #pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const float4 v = x[it];
-    const float4 h = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
-    *reinterpret_cast<float4*>(hi + (ct + 128 * it) * 16) = h;
-    *reinterpret_cast<float4*>(lo + (ct + 128 * it) * 16) = make_float4(v.x - h.x, v.y - h.y, v.z - h.z, v.w - h.w);
+  for (int it = 0; it < 4; ++it) {
+    const int cp = ct + 128 * it;
+    float4 x = a[it], y = b[it];
+    if (k0 + (cp >> 3) < L) {
+      rope_pair(a[it].x, b[it].x, cs[it].x, sn[it].x, x.x, y.x);
+      rope_pair(a[it].y, b[it].y, cs[it].y, sn[it].y, x.y, y.y);
+      rope_pair(a[it].z, b[it].z, cs[it].z, sn[it].z, x.z, y.z);
+      rope_pair(a[it].w, b[it].w, cs[it].w, sn[it].w, x.w, y.w);
+    }
+    const float4 hx = make_float4(tf32_hi(x.x), tf32_hi(x.y), tf32_hi(x.z), tf32_hi(x.w));
+    const float4 hy = make_float4(tf32_hi(y.x), tf32_hi(y.y), tf32_hi(y.z), tf32_hi(y.w));
+    *reinterpret_cast<float4*>(kh + cp * 16) = hx;
+    *reinterpret_cast<float4*>(kh + kSlabK + cp * 16) = hy;
+    *reinterpret_cast<float4*>(kl + cp * 16) = make_float4(x.x - hx.x, x.y - hx.y, x.z - hx.z, x.w - hx.w);
+    *reinterpret_cast<float4*>(kl + kSlabK + cp * 16) = make_float4(y.x - hy.x, y.y - hy.y, y.z - hy.z, y.w - hy.w);
   }
 }
 
@@ -267,8 +198,7 @@ struct T3Params {
 };
 
 __global__ void __launch_bounds__(kT3Threads, 1)
-    prefill_3xtf32_kernel(const __grid_constant__ CUtensorMap qkv_map, const __grid_constant__ CUtensorMap k_map,
-                          const __grid_constant__ CUtensorMap v_map, const T3Params p) {
+    prefill_3xtf32_kernel(const __grid_constant__ CUtensorMap qkv_map, const T3Params p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared shs;
   Shared* sh = &shs;
@@ -277,8 +207,6 @@ __global__ void __launch_bounds__(kT3Threads, 1)
 
   if (tid == 0) {
     tma_prefetch_map(&qkv_map);
-    tma_prefetch_map(&k_map);
-    tma_prefetch_map(&v_map);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh->unit_full[i], 1);
       mbar_init(&sh->unit_empty[i], 8);  // softmax, 4 split warps, V producer, both issuers
@@ -334,7 +262,7 @@ __global__ void __launch_bounds__(kT3Threads, 1)
   if (warp == 12) {
     if (lane == 0) {
       // ------------------------------------------- TMA producer: units, Q, keys
-      griddep_wait();  // the scheduler's list and the key / value planes
+      griddep_wait();  // the scheduler's list
       const int n_units = p.hdr->n_pairs * p.heads;
       const int G = p.heads / p.kv_heads;
       uint32_t n = 0, nq = 0, c = 0;  // units published, query tiles and key halves loaded
@@ -390,11 +318,11 @@ __global__ void __launch_bounds__(kT3Threads, 1)
         for (int k = 0; k < inf.nsub; ++k, ++c) {
           const uint32_t st = c % kKStages;
           if (!(ok = wait(&sh->k_empty[st], ((c / kKStages) & 1) ^ 1))) break;
-          uint8_t* kb = smem + kOffK + st * 2 * kHalfBytes;
+          uint8_t* kb = smem + kOffK + st * 2 * kHalfBytes;  // the raw keys land in the high part
           mbar_arrive_expect_tx(&sh->k_raw_full[st], kHalfBytes);
 #pragma unroll
           for (int a = 0; a < 2; ++a)
-            tma_load_2d(kb + a * kSlabK, &k_map, &sh->k_raw_full[st], inf.g * kHead + 32 * a,
+            tma_load_2d(kb + a * kSlabK, &qkv_map, &sh->k_raw_full[st], (p.heads + inf.g) * kHead + 32 * a,
                         inf.row0 + (inf.hb + k) * kSub);
         }
         if (!ok) break;
@@ -419,16 +347,15 @@ __global__ void __launch_bounds__(kT3Threads, 1)
         const UnitInfo inf = sh->info[slot];
         mbar_arrive(&sh->unit_empty[slot]);
         if (inf.u < 0) break;
-        const int vcol = tf32_vt_col(inf.row0, inf.s);
+        const int vx = (p.heads + p.kv_heads + inf.g) * kHead;
         for (int k = 0; k < inf.nsub; ++k, ++c) {
           const uint32_t st = c % kVStages;
           if (!(ok = wait(&sh->v_empty[st], ((c / kVStages) & 1) ^ 1))) break;
-          uint8_t* vb = smem + kOffV + st * 2 * kHalfBytes;
+          uint8_t* vl = smem + kOffV + st * 2 * kHalfBytes + kHalfBytes;  // the raw values land in the low part
           mbar_arrive_expect_tx(&sh->v_raw_full[st], kHalfBytes);
 #pragma unroll
           for (int a = 0; a < 2; ++a)
-            tma_load_2d(vb + a * kSlabK, &v_map, &sh->v_raw_full[st], vcol + (inf.hb + k) * kSub + 32 * a,
-                        inf.g * kHead);
+            tma_load_2d(vl + a * kSlabK, &qkv_map, &sh->v_raw_full[st], vx + 32 * a, inf.row0 + (inf.hb + k) * kSub);
         }
         if (!ok) break;
       }
@@ -438,31 +365,74 @@ __global__ void __launch_bounds__(kT3Threads, 1)
     }
     __syncwarp();
   } else if (warp >= 8 && warp < 12) {
-    // ----------------------------------------------------------- operand split
-    const int ct = tid - 256;  // 0 .. 127
+    // ------------------------------------------------------ operand preparation
+    // The four warps pass the same named barriers (id 6, 128 threads): one
+    // per unit, one per half; a failed wait is carried to the next of them.
+    const int ct = tid - 256, cw = warp - 8;  // 0 .. 127, 0 .. 3
     uint32_t n = 0, h = 0;
     bool ok = true;
     for (;; ++n) {
       const int slot = n & 1;
       ok = __all_sync(0xffffffffu, ok && wait(&sh->unit_full[slot], (n >> 1) & 1));
-      if (!ok) break;
+      if (named_bar_or(6, 128, !ok)) break;
       const UnitInfo inf = sh->info[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->unit_empty[slot]);
       if (inf.u < 0) break;
-      for (int k = 0; ok && k < inf.nsub; ++k, ++h) {
+      for (int k = 0; k < inf.nsub; ++k, ++h) {
         const uint32_t ks = h % kKStages, vs = h % kVStages;
-        ok = __all_sync(0xffffffffu, wait(&sh->k_raw_full[ks], (h / kKStages) & 1));
-        if (!ok) break;
-        uint8_t* kb = smem + kOffK + ks * 2 * kHalfBytes;
-        split_half(kb, kb + kHalfBytes, ct);
-        fence_proxy_async_smem();  // visible to the tensor core
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->k_ready[ks]);
-        ok = __all_sync(0xffffffffu, wait(&sh->v_raw_full[vs], (h / kVStages) & 1));
-        if (!ok) break;
-        uint8_t* vb = smem + kOffV + vs * 2 * kHalfBytes;
-        split_half(vb, vb + kHalfBytes, ct);
+        // keys: rotated at their positions and split in place
+        ok = __all_sync(0xffffffffu, ok && wait(&sh->k_raw_full[ks], (h / kKStages) & 1));
+        if (ok) {
+          uint8_t* kb = smem + kOffK + ks * 2 * kHalfBytes;
+          prep_keys(kb, kb + kHalfBytes, (inf.hb + k) * kSub, inf.L, p.cos_t, p.sin_t, ct);
+          fence_proxy_async_smem();  // visible to the tensor core
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->k_ready[ks]);
+        }
+        // values: the raw tile (slabs of 32 dims, 64 key rows, in the low
+        // part) read as 4x4 blocks, then written transposed (slabs of 32
+        // keys, 64 dim rows): high parts into the high part, low parts over
+        // the raw tile.  Lane (kg_lo, dg_lo) = (lane & 7, lane >> 3) takes
+        // blocks of keys 4 kg .. 4 kg + 3 and dims 4 dg .. 4 dg + 3; every
+        // 16-byte access of a warp spreads over all eight chunk positions.
+        ok = __all_sync(0xffffffffu, ok && wait(&sh->v_raw_full[vs], (h / kVStages) & 1));
+        uint8_t* vh = smem + kOffV + vs * 2 * kHalfBytes;
+        uint8_t* vl = vh + kHalfBytes;
+        float4 blk[2][4];
+        if (ok) {
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = 2 * cw + i, kg = (lane & 7) + 8 * (c & 1), dg = (lane >> 3) + 4 * (c >> 1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 4 * kg + e;
+              blk[i][e] = *reinterpret_cast<const float4*>(vl + (dg >> 3) * kSlabK + j * 128 +
+                                                           (((dg & 7) ^ (j & 7)) << 4));
+            }
+          }
+        }
+        // every raw value has been read before any low part overwrites it
+        if (named_bar_or(6, 128, !ok)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int c = 2 * cw + i, kg = (lane & 7) + 8 * (c & 1), dg = (lane >> 3) + 4 * (c >> 1);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int d = 4 * dg + e;
+            const float4 v = e == 0 ? make_float4(blk[i][0].x, blk[i][1].x, blk[i][2].x, blk[i][3].x)
+                           : e == 1 ? make_float4(blk[i][0].y, blk[i][1].y, blk[i][2].y, blk[i][3].y)
+                           : e == 2 ? make_float4(blk[i][0].z, blk[i][1].z, blk[i][2].z, blk[i][3].z)
+                                    : make_float4(blk[i][0].w, blk[i][1].w, blk[i][2].w, blk[i][3].w);
+            const float4 hv = make_float4(tf32_hi(v.x), tf32_hi(v.y), tf32_hi(v.z), tf32_hi(v.w));
+            const uint32_t off = (kg >> 3) * kSlabK + d * 128 + (((kg & 7) ^ (d & 7)) << 4);
+            *reinterpret_cast<float4*>(vh + off) = hv;
+            *reinterpret_cast<float4*>(vl + off) = make_float4(v.x - hv.x, v.y - hv.y, v.z - hv.z, v.w - hv.w);
+          }
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->v_ready[vs]);
@@ -784,28 +754,9 @@ __global__ void __launch_bounds__(kT3Threads, 1)
 
 }  // namespace
 
-cudaError_t launch_tf32_kv_prep(const float* qkv, const int32_t* cu, int n_seqs, int total, int heads, int kv_heads,
-                                const float* cos_t, const float* sin_t, int rope_len, void* ws, cudaStream_t st) {
-  const Tf32Planes pl = tf32_planes(n_seqs, total, kv_heads);
-  char* w = static_cast<char*>(ws);
-  // launched with programmatic stream serialization: it starts while the
-  // scheduler (which lets dependents start at once) still runs
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((total + kPrepRows - 1) / kPrepRows);
-  cfg.blockDim = dim3(256);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tf32_kv_prep_kernel, qkv, cu, n_seqs, total, heads, kv_heads, cos_t, sin_t,
-                            rope_len, pl.tp, reinterpret_cast<float*>(w + pl.kr), reinterpret_cast<float*>(w + pl.vt));
-}
-
-cudaError_t launch_prefill_3xtf32(const CUtensorMap* qkv_map, const CUtensorMap* k_map, const CUtensorMap* v_map,
-                                  int heads, int kv_heads, int window, int causal, float scale, const float* cos_t,
-                                  const float* sin_t, float* out, void* ws, int32_t* dev_status, cudaStream_t st) {
+cudaError_t launch_prefill_3xtf32(const CUtensorMap* qkv_map, int heads, int kv_heads, int window, int causal,
+                                  float scale, const float* cos_t, const float* sin_t, float* out, void* ws,
+                                  int32_t* dev_status, cudaStream_t st) {
   static int configured[64] = {};
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -841,7 +792,7 @@ cudaError_t launch_prefill_3xtf32(const CUtensorMap* qkv_map, const CUtensorMap*
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_3xtf32_kernel, *qkv_map, *k_map, *v_map, prm);
+  return cudaLaunchKernelEx(&cfg, prefill_3xtf32_kernel, *qkv_map, prm);
 }
 
 }  // namespace kime

@@ -116,9 +116,8 @@ def test_window_at_least_length_is_bitwise_full(cuda_lib):
 
 
 def test_packing_order_does_not_change_a_sequence_bitwise(cuda_lib):
-    # a sequence's rows and transposed value columns sit elsewhere in another
-    # packing (and its last key half reaches into other neighbours); its
-    # results do not move
+    # a sequence's rows sit elsewhere in another packing (and its last key
+    # half reaches into other neighbours); its results do not move
     lengths, H, Hkv = [333, 10, 129, 512], 6, 3
     qkv = random_qkv(lengths, H, Hkv, torch.float32, 1.0, seed=66)
     cu = cu_from_lengths(lengths)
@@ -178,8 +177,8 @@ def test_workspace_too_small_and_dtype_errors_raise(cuda_lib):
 
 
 def test_replays_from_a_cuda_graph(cuda_lib):
-    # the scheduler, preparation pass and attention kernel are all on the given
-    # stream and allocate nothing: one capture, replayed on new inputs
+    # the scheduler and the attention kernel are both on the given stream and
+    # allocate nothing: one capture, replayed on new inputs
     dev = torch.device("cuda")
     lengths, H, Hkv = [700, 1, 129, 300], 4, 2
     cu = cu_from_lengths(lengths).to(dev)

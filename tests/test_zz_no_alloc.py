@@ -68,7 +68,7 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(cuda_lib):
 
 def test_noalloc_3xtf32_through_the_c_abi(cuda_lib):
     # the Python wrapper passes only qkv's own dtype; the C entry also takes
-    # KIME_F32_3XTF32 when its key and value planes fit in the array
+    # KIME_F32_3XTF32 (whose scratch is the scheduler's alone)
     dev = torch.device("cuda")
     lib = kime.load_library()
     for lengths, H, Hkv, window, causal, seed in [([7, 13], 2, 2, -1, False, 36), ([40, 9], 3, 1, 4, True, 37)]:
