@@ -125,6 +125,18 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// "no visible key yet" for a running row maximum: below every logit, finite,
+// so no -inf is ever formed
+constexpr float kNone = -3.0e38f;
+
+// acc += the two f16 halves of a packed pair, each added in float32 (one
+// rounding per addition, no f16 arithmetic)
+__device__ __forceinline__ void add_f16x2_f32(float& a0, float& a1, uint32_t pair) {
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(pair));
+}
+
 // RoPE (rotate-half) of one pair with one rounding per operation and no
 // contraction: the float32 evaluation every kernel here uses.
 __device__ __forceinline__ void rope_pair(float a, float b, float c, float s, float& ya, float& yb) {

@@ -67,7 +67,6 @@ struct Layout {
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLazy = 8.f;       // the reference max moves when exceeded by more (log2 units)
-constexpr float kNone = -3.0e38f;  // "no visible key yet": below every logit, finite
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
 
@@ -139,14 +138,6 @@ __device__ __forceinline__ void unit_ranges(const UnitInfo& inf, int w, int caus
                                             int& fb, int& fe) {
   kb = ke = fb = fe = 0;
   if (w < inf.nt) tile_ranges(inf.L, inf.L - inf.kbase, -inf.kbase, inf.qt0 + w, causal, window, kb, ke, fb, fe);
-}
-
-// acc += the two f16 halves of a packed pair, each added in float32 (one
-// rounding per addition, no f16 arithmetic)
-__device__ __forceinline__ void add_f16x2_f32(float& a0, float& a1, uint32_t pair) {
-  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
-      : "+f"(a0), "+f"(a1)
-      : "r"(pair));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)

@@ -103,6 +103,22 @@ struct Layout {
 };
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLazy = 8.f;  // the reference max moves when exceeded by more (log2 units)
+
+// f16 bit pattern of an integer 0..2047 (exact), at compile time
+__host__ __device__ constexpr uint32_t f16_bits_small(int n) {
+  int e = 0;
+  while ((n >> (e + 1)) != 0) ++e;
+  return n == 0 ? 0u : (static_cast<uint32_t>(e + 15) << 10) | ((static_cast<uint32_t>(n) << (10 - e)) & 0x3FFu);
+}
+static_assert(f16_bits_small(1) == 0x3C00u && f16_bits_small(127) == 0x57F0u && f16_bits_small(128) == 0x5800u,
+              "f16 encoding of small integers");
+
+// an integer of magnitude at most 2048 in both halves of an f16 pair (exact)
+__device__ __forceinline__ uint32_t f16x2_splat(int n) {
+  uint32_t r;
+  asm("{\n\t.reg .f16 h;\n\tcvt.rn.f16.s32 h, %1;\n\tmov.b32 %0, {h, h};\n\t}" : "=r"(r) : "r"(n));
+  return r;
+}
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
 
@@ -669,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O (in TMEM, accumulated by the PV MMAs) stay relative to m_ref, which
       // only moves -- rescaling O and l -- when a row's max exceeds it by more
       // than 2^8.  Logits arrive in log2 units (scale*log2(e) is folded into q).
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = kNone, l = 0.f;
       for (int t = kb; t < ke; ++t) {
         const int k0 = inf.kbase + t * kBN;
         PHASE(7);
@@ -684,12 +700,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         if (lane == 0) mbar_arrive(&sh->s_read[w]);
         PHASE(1);
-        float x[128];
-#pragma unroll
-        for (int j = 0; j < kBN; ++j) x[j] = __uint_as_float(v[j]);
-        if (!(t >= fb && t < fe)) {
-          // visible keys of this row in this tile form one interval [lo, hi]
-          int lo = 0, hi;
+        // visible keys of this row in this tile form one interval [lo, hi]
+        // of column indices (only partial tiles test columns)
+        const bool full = t >= fb && t < fe;
+        int lo = 0, hi = kBN - 1;
+        if (!full) {
           if (kCache) {
             hi = min(kBN - 1, chunk_hi - k0);  // causal at position off + i <= off + L - 1
           } else {
@@ -701,62 +716,91 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!row_ok) hi = -1;
           }
-#pragma unroll
-          for (int j = 0; j < kBN; ++j)
-            if (j < lo || j > hi) x[j] = -INFINITY;
+          lo = min(lo, kBN);
+          hi = max(hi, -1);
         }
         // row max: eight running maxima, each taking two keys per three-input
         // max (64 instructions for 128 keys, short dependency chains)
         float m8[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(x[2 * k], x[2 * k + 1]);
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
 #pragma unroll
-        for (int j = 16; j < kBN; j += 2) m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], x[j], x[j + 1]);
-        const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        for (int j = 16; j < kBN; j += 2)
+          m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+        float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        // On a partial tile that maximum also covers masked columns, so it only
+        // bounds the visible one from above: when it cannot move the reference
+        // (the usual case after a row's first tile) the visible maximum cannot
+        // either; otherwise the maximum is taken again over the visible
+        // columns alone (kNone when there are none), tested against a bit word
+        // per 32 columns.
+        if (!full && __any_sync(0xffffffffu, mx > m_ref + kLazy)) {
+          uint32_t vis[kBN / 32];
+#pragma unroll
+          for (int k = 0; k < kBN / 32; ++k) {
+            const int a = lo - 32 * k, b = hi - 32 * k;  // the interval in this word's bit positions
+            const uint32_t upto_b = b < 0 ? 0u : (2u << min(b, 31)) - 1u;
+            const uint32_t below_a = a <= 0 ? 0u : (a >= 32 ? ~0u : (1u << a) - 1u);
+            vis[k] = upto_b & ~below_a;
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = kNone;
+#pragma unroll
+          for (int j = 0; j < kBN; ++j)
+            if ((vis[j >> 5] >> (j & 31)) & 1u) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(v[j]));
+          mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        }
         // move the reference max on the first visible keys, or when it is
         // exceeded by more than kLazy (log2 units)
         float alpha = 1.f;
         if (mx > m_ref + kLazy) {
-          if (m_ref != -INFINITY) alpha = fast_exp2(m_ref - mx);
+          if (m_ref != kNone) alpha = fast_exp2(m_ref - mx);
           m_ref = mx;
         }
         PHASE(2);
-        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        // P = 2^(x - m_use): the differences in float32 pairs, rounded to f16
-        // pairs, two exponentials per MUFU operation (P in f16, as the MMA
-        // takes it); row sums in f16 over 16 keys, then float32.  A masked
-        // key (-inf) gives 0.  All 64 exponent pairs first (independent
-        // chains the schedulers can interleave), then the sums.
+        // P = 2^(x - m_ref): the differences in float32 pairs, rounded to f16
+        // pairs (saturating, so no difference becomes infinite), two
+        // exponentials per MUFU operation (P in f16, as the MMA takes it).
+        // All 64 exponent pairs first (independent chains the schedulers can
+        // interleave), then the masked columns set to probability zero.
         uint64_t mm;
-        asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(m_use));
+        asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(m_ref));
         uint32_t pw[64];
 #pragma unroll
         for (int e = 0; e < 64; ++e) {
           uint64_t xx, d;
-          asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "f"(x[2 * e]), "f"(x[2 * e + 1]));
+          asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "r"(v[2 * e]), "r"(v[2 * e + 1]));
           asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(xx), "l"(mm));
           uint32_t h;
-          asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.f16x2.f32 %0, hi, lo;\n\t}" : "=r"(h) : "l"(d));
+          asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.satfinite.f16x2.f32 %0, hi, lo;\n\t}"
+              : "=r"(h)
+              : "l"(d));
           asm("ex2.approx.f16x2 %0, %1;" : "=r"(pw[e]) : "r"(h));
         }
-        float rs2f[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!full) {
+          // column indices against [lo, hi] as f16 pairs (exact for 0..128):
+          // each half of a comparison is 0xFFFF when true
+          const uint32_t lo2 = f16x2_splat(lo), hi2 = f16x2_splat(hi);
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {  // 16 keys
-          const uint32_t* g = pw + 8 * q8;
-          uint32_t a0, a1, a2, a3, b0, b1, c0;
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a0) : "r"(g[0]), "r"(g[1]));
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a1) : "r"(g[2]), "r"(g[3]));
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a2) : "r"(g[4]), "r"(g[5]));
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(a3) : "r"(g[6]), "r"(g[7]));
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(b0) : "r"(a0), "r"(a1));
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(b1) : "r"(a2), "r"(a3));
-          asm("add.rn.f16x2 %0, %1, %2;" : "=r"(c0) : "r"(b0), "r"(b1));
-          float lo, hi;
-          asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}" : "=f"(lo), "=f"(hi) : "r"(c0));
-          rs2f[q8 & 3] += lo + hi;
+          for (int e = 0; e < 64; ++e) {
+            const uint32_t cols = f16_bits_small(2 * e) | (f16_bits_small(2 * e + 1) << 16);
+            uint32_t ge, le;
+            asm("set.ge.u32.f16x2 %0, %1, %2;" : "=r"(ge) : "r"(cols), "r"(lo2));
+            asm("set.le.u32.f16x2 %0, %1, %2;" : "=r"(le) : "r"(cols), "r"(hi2));
+            pw[e] &= ge & le;
+          }
         }
-        const float rowsum = (rs2f[0] + rs2f[1]) + (rs2f[2] + rs2f[3]);
-        l = l * alpha + rowsum;
+        // the row sum: the f16 probabilities the PV MMA takes, each added in
+        // float32
+        float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 64; e += 4) {
+          add_f16x2_f32(s8[0], s8[1], pw[e]);
+          add_f16x2_f32(s8[2], s8[3], pw[e + 1]);
+          add_f16x2_f32(s8[4], s8[5], pw[e + 2]);
+          add_f16x2_f32(s8[6], s8[7], pw[e + 3]);
+        }
+        l = l * alpha + (((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7])));
         // PV(t-1) read P(t-1) from this tile's P columns and accumulated into
         // O: it completes before P(t) is stored and O is rescaled (the
         // exponentials above overlap it)

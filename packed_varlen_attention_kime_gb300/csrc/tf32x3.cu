@@ -79,7 +79,6 @@ constexpr uint32_t kColS = 0, kColPl = 192, kColO = 320, kColQh = 384, kColQl = 
 constexpr int kSBufs = 3;  // S / P-high buffers
 constexpr uint32_t kT3Cols = 512;
 constexpr float kLazy = 8.f;       // the reference max moves when exceeded by more (log2 units)
-constexpr float kNone = -3.0e38f;  // "no visible key yet": below every logit, finite
 
 // Instruction descriptor, kind::tf32: TF32 A and B (format 2), FP32 D, both
 // K-major.
