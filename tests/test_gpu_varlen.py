@@ -223,8 +223,8 @@ PREP_CASES = [
 @pytest.mark.parametrize("lengths,H,Hkv,window,causal", PREP_CASES)
 def test_prepared_rows_and_fused_paths_match_the_oracle(cuda_lib, lengths, H, Hkv, window, causal):
     # With a workspace of op 3 size the qkv rows are prepared once (RoPE, the
-    # query scale, f16) and the attention kernel over prepared rows runs (row
-    # sums on the tensor core); with the minimal workspace (op 0) the kernel
+    # query scale, f16) and the attention kernel over prepared rows runs; with
+    # the minimal workspace (op 0) the kernel
     # that rotates queries and key tiles itself runs.  Both are checked
     # against the oracle on the same sampled rows.
     dev = torch.device("cuda")
@@ -244,6 +244,31 @@ def test_prepared_rows_and_fused_paths_match_the_oracle(cuda_lib, lengths, H, Hk
     for op, o in zip((0, 3), outs):
         g = o.float().cpu().reshape(T, H, 64)[torch.from_numpy(rows).long(), torch.from_numpy(hs).long()]
         check_bf16(g.numpy(), ref, f"op {op} {lengths} w{window} c{causal}")
+
+
+# Sequences with an odd number of query tiles end in a unit of one tile (1-,
+# 3- and 9-tile sequences here, of several costs), next to units of two.
+ODD_TILES = [300, 290, 260, 1100, 1150, 100, 120, 128, 50]
+ODD_CASES = [
+    (ODD_TILES, 4, 2, -1, False),
+    (ODD_TILES, 4, 2, -1, True),
+    (ODD_TILES, 4, 4, 64, False),
+    (ODD_TILES, 6, 2, 200, True),
+]
+
+
+@pytest.mark.parametrize("lengths,H,Hkv,window,causal", ODD_CASES)
+def test_odd_tile_counts_match_the_oracle_everywhere(cuda_lib, lengths, H, Hkv, window, causal):
+    dev = torch.device("cuda")
+    qkv_cpu = random_qkv(lengths, H, Hkv, torch.bfloat16, 1.5, seed=41)
+    cu = cu_from_lengths(lengths)
+    T, n, mx = qkv_cpu.shape[0], len(lengths), max(lengths)
+    c, s = gpu_tables(1e4, mx)
+    ws = torch.empty(kime.kime_attn_workspace_bytes(3, n, T, H, Hkv), dtype=torch.uint8, device=dev)
+    out = kime.kime_attn_varlen(qkv_cpu.to(dev), cu.to(dev), mx, H, Hkv, window, causal, 0.125, c, s, workspace=ws)
+    torch.cuda.synchronize()
+    ref = run_oracle_varlen(qkv_cpu, cu, H, Hkv, window, causal, 0.125, 1e4, mx)
+    check_bf16(out.float().cpu().numpy().reshape(ref.shape), ref, f"odd tile counts w{window} c{causal}")
 
 
 def test_device_status_flags_bad_cu_and_skips(cuda_lib):
