@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t n = 0, c = 0, pc = 0, sc = 0;  // units, key tiles, P tiles, S MMAs of this tile
       const uint32_t tS = tmem + kColS + w * 128, tO = tmem + kColO + w * 64, tP = tmem + kColP + w * 64;
       const uint32_t sbase = smem_u32(smem);
+      const uint64_t dk0 = sdesc_sw128(sbase + Layout::k, 16, 1024), dv0 = sdesc_sw128(sbase + Layout::v, 0, 1024);
       for (;; ++n) {
         const int slot = n & 1;
         if (!wait(&sh->unit_full[slot], (n >> 1) & 1)) break;
@@ -279,14 +280,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P(t), so waiting for that load, then for P(t), in this order loses
         // nothing, and every wait suspends this thread instead of polling
         // (the softmax warps of its scheduler keep the issue slots).
+        // descriptors advance by 32 bytes (2 in the address field) per
+        // 16-wide k step; the K stages' differ by their offset
+        const uint64_t dq = sdesc_sw128(aq, 16, 1024);
         auto issue_s = [&](uint32_t cc) -> bool {
           if (!wait(&sh->kv_full[cc % kStages], (cc / kStages) & 1)) return false;
           if (sc > 0 && !wait(&sh->s_read[w], (sc - 1) & 1)) return false;
           tc_fence_after();
-          const uint32_t bk = sbase + Layout::k + (cc % kStages) * kTile;
+          const uint64_t dk = dk0 + ((cc % kStages) * kTile >> 4);
 #pragma unroll
-          for (int ks = 0; ks < kHead / 16; ++ks)
-            tc_mma_ss(tS, sdesc_sw128(aq + ks * 32, 16, 1024), sdesc_sw128(bk + ks * 32, 16, 1024), kIdescS, ks > 0);
+          for (int ks = 0; ks < kHead / 16; ++ks) tc_mma_ss(tS, dq + 2 * ks, dk + 2 * ks, kIdescS, ks > 0);
           tc_commit(&sh->s_full[w]);
           ++sc;
           return true;
@@ -295,11 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait(&sh->p_full[w], pc & 1)) return false;
           ++pc;
           tc_fence_after();
-          const uint32_t bv = sbase + Layout::v + st * kTile;
+          const uint64_t dv = dv0 + (st * kTile >> 4);  // 2048 bytes (128) per 16 keys
           const uint32_t acc0 = t > kb ? 1u : 0u;
 #pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks)
-            tc_mma_ts(tO, tP + ks * 8, sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, ks > 0 ? 1u : acc0);
+          for (int ks = 0; ks < kBN / 16; ++ks) tc_mma_ts(tO, tP + ks * 8, dv + 128 * ks, kIdescPV, ks > 0 ? 1u : acc0);
           tc_commit(&sh->pv_full[w]);
           return true;
         };
