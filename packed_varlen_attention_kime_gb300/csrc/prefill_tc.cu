@@ -480,6 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S for the key tile that is number cc of the K/V ring may be issued
         // once that tile is in (and rotated) and the softmax warpgroup has
         // loaded the S before it out of the tile's S buffer
+        // descriptors advance by 32 bytes (2 in the address field) per
+        // 16-wide k step; the stages' differ by their offset
         auto s_ready = [&](uint32_t cc) -> bool {
           const uint32_t ph = (cc / kStages) & 1;
           if (!mbar_test(&sh->kv_full[cc % kStages], ph) || !mbar_test(&sh->krot[cc % kStages], ph))
@@ -488,21 +490,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto issue_s = [&](int t, uint32_t cc) {
           tc_fence_after();
-          const uint32_t bk = smem_u32(smem + kOffK + (cc % kStages) * kTile);
+          const uint64_t dq = sdesc_sw128(aq, 16, 1024);
+          const uint64_t dk = sdesc_sw128(smem_u32(smem + kOffK + (cc % kStages) * kTile), 16, 1024);
 #pragma unroll
-          for (int ks = 0; ks < kHead / 16; ++ks)
-            tc_mma_ss(tS, sdesc_sw128(aq + ks * 32, 16, 1024), sdesc_sw128(bk + ks * 32, 16, 1024), kIdescS, ks > 0);
+          for (int ks = 0; ks < kHead / 16; ++ks) tc_mma_ss(tS, dq + 2 * ks, dk + 2 * ks, kIdescS, ks > 0);
           tc_commit(&sh->s_full[w][sc & 1]);
           EV(1 + w, 0, t);
           ++sc;
         };
         auto issue_pv = [&](int t, int st) {
           tc_fence_after();
-          const uint32_t bv = smem_u32(smem + kOffV + st * kTile);
+          const uint64_t dv = sdesc_sw128(smem_u32(smem + kOffV + st * kTile), 0, 1024);  // + 128 per 16 keys
           const uint32_t acc0 = t > kb ? 1u : 0u;
 #pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks)
-            tc_mma_ts(tO, tP + ks * 8, sdesc_sw128(bv + ks * 2048, 0, 1024), kIdescPV, ks > 0 ? 1u : acc0);
+          for (int ks = 0; ks < kBN / 16; ++ks) tc_mma_ts(tO, tP + ks * 8, dv + 128 * ks, kIdescPV, ks > 0 ? 1u : acc0);
           tc_commit(&sh->pv_full[w]);
           EV(1 + w, 1, t);
         };
