@@ -532,91 +532,83 @@ def oracle_single_core():
 
 def end_to_end(args, dev, stream, flush, run, world):
     """The headline step end to end through the public API: pinned host qkv ->
-    device, both layers, both outputs -> pinned host, every step.  The batch is
-    cut into contiguous groups of sequences, each a packed batch of its own:
-    copies in, the two layers, and copies out run on three streams, so group
-    g's layers overlap group g+1's copy in and group g-1's copy out (the link is
-    full duplex)."""
+    device, both layers, both outputs -> pinned host, every step.  Steps are
+    pipelined as a server would run them, with two sets of device and pinned
+    host buffers: step k+1's copy in overlaps step k's layers and step k-1's
+    copy out (the link is full duplex), on three streams ordered by events; a
+    buffer set is refilled only after the step two back has finished with it.
+    Each step still copies its own inputs in and its results out.  Timed over
+    K consecutive steps, the first copy in and the last copy out included."""
     c = run.case
     h_qkv = c.qkv.cpu().pin_memory()
-    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in run.outs]
-    d_qkv = torch.empty_like(c.qkv)
-    cu_h = c.cu_seqlens.tolist()
-    # n groups of whole sequences, about equal in tokens: fewer groups cost
-    # fewer calls (each with its own scheduler, preparation and tail), more
-    # groups a shorter first copy in and last copy out; on the ModernBERT-large
-    # pair 4 groups measured 1.93 ms per step, 8 groups 2.01, 2 groups 2.32
-    n_groups = max(1, min(args.e2e_groups, len(c.lengths)))
-    bounds = [0]
-    for g in range(1, n_groups):  # split at the sequence boundary nearest g/n of the tokens
-        tgt = c.total * g / n_groups
-        bounds.append(min(range(bounds[-1] + 1, len(c.lengths) - (n_groups - g) + 1),
-                          key=lambda s: abs(cu_h[s] - tgt)))
-    bounds.append(len(c.lengths))
-    groups = []
-    for a, b in zip(bounds[:-1], bounds[1:]):
-        r0, r1 = cu_h[a], cu_h[b]
-        h_cu_g = torch.tensor([x - r0 for x in cu_h[a:b + 1]], dtype=torch.int32).pin_memory()
-        groups.append((r0, r1, h_cu_g, torch.empty_like(h_cu_g, device=dev), max(c.lengths[a:b])))
+    h_cu = c.cu_seqlens.cpu().to(torch.int32).pin_memory()
+    mx = max(c.lengths)
+    d_qkv = [torch.empty_like(c.qkv) for _ in range(2)]
+    d_cu = [torch.empty_like(h_cu, device=dev) for _ in range(2)]
+    d_out = [[torch.empty_like(o) for o in run.outs] for _ in range(2)]
+    h_out = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in run.outs] for _ in range(2)]
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    status = dev_status(dev)
 
-    def enqueue(origin):  # the pipelined step, forked from and joined back to stream `origin`
-        start = torch.cuda.Event()
-        start.record(origin)
-        for st in (s_in, s_cmp, s_out):
-            st.wait_event(start)
-        for r0, r1, h_cu_g, d_cu_g, mx in groups:
-            with torch.cuda.stream(s_in):
-                d_qkv[r0:r1].copy_(h_qkv[r0:r1], non_blocking=True)
-                d_cu_g.copy_(h_cu_g, non_blocking=True)
-            e_in = torch.cuda.Event()
-            e_in.record(s_in)
-            s_cmp.wait_event(e_in)
-            with torch.cuda.stream(s_cmp):
-                for k, lay in enumerate(c.layers):
-                    cs, sn = run.tables[lay.theta]
-                    run.kime.kime_attn_varlen(d_qkv[r0:r1], d_cu_g, mx, c.heads, c.kv_heads, lay.window,
-                                              lay.causal, lay.scale, cs, sn, out=run.outs[k][r0:r1],
-                                              workspace=run.ws, dev_status=dev_status(dev), stream=s_cmp)
-            e_cmp = torch.cuda.Event()
-            e_cmp.record(s_cmp)
-            s_out.wait_event(e_cmp)
-            with torch.cuda.stream(s_out):
-                for h, o in zip(h_out, run.outs):
-                    h[r0:r1].copy_(o[r0:r1], non_blocking=True)
-        done = torch.cuda.Event()
-        done.record(s_out)
-        origin.wait_event(done)
+    def enqueue(k):
+        b = k & 1
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(ev_cmp[b])  # step k-2's layers have read this input buffer
+            d_qkv[b].copy_(h_qkv, non_blocking=True)
+            d_cu[b].copy_(h_cu, non_blocking=True)
+            ev_in[b].record(s_in)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(ev_in[b])
+            if k >= 2:
+                s_cmp.wait_event(ev_out[b])  # step k-2's outputs have left this buffer
+            for li, lay in enumerate(c.layers):
+                cs, sn = run.tables[lay.theta]
+                run.kime.kime_attn_varlen(d_qkv[b], d_cu[b], mx, c.heads, c.kv_heads, lay.window, lay.causal,
+                                          lay.scale, cs, sn, out=d_out[b][li], workspace=run.ws,
+                                          dev_status=status, stream=s_cmp)
+            ev_cmp[b].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_cmp[b])
+            for h, o in zip(h_out[b], d_out[b]):
+                h.copy_(o, non_blocking=True)
+            ev_out[b].record(s_out)
 
-    if args.e2e_graph:
-        # captured once (after a direct run for the first-call set-up) and
-        # replayed each step: the host enqueues one graph, not every group's
-        # calls and copies
-        enqueue(stream)
+    def run_steps(n):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
-        graph, cap = torch.cuda.CUDAGraph(), torch.cuda.Stream(dev)
-        with torch.cuda.graph(graph, stream=cap):
-            enqueue(cap)
+        start.record(stream)
+        for st in (s_in, s_cmp, s_out):
+            st.wait_stream(stream)
+        for k in range(n):
+            enqueue(k)
+        for st in (s_in, s_cmp, s_out):
+            stream.wait_stream(st)
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
 
-        def e2e_step(ev):
-            graph.replay()
-    else:
-        def e2e_step(ev):
-            enqueue(stream)
-    e_per, _ = time_fn(e2e_step, max(5, args.steps // 5), 3, flush, stream)
-    e_ms = statistics.mean(e_per)
-    ref_out = [o.clone() for o in run.outs]
-    for k in range(len(c.layers)):  # the pipelined groups give the whole batch's bits
+    run_steps(4)  # warm-up (first-call set-up, pinned pages touched)
+    n = max(10, args.steps)
+    e_ms = max_over_ranks(run_steps(n), dev if world > 1 else None) / n
+    # the pipelined steps give the whole batch's bits (both buffer sets)
+    for k in range(len(c.layers)):
         run.layer(k)
     torch.cuda.synchronize()
-    if not all(torch.equal(a, b) for a, b in zip(ref_out, run.outs)) or \
-            not all(torch.equal(h, o.cpu()) for h, o in zip(h_out, run.outs)):
-        raise RuntimeError("pipelined end-to-end outputs differ from the whole-batch calls")
+    for b in range(2):
+        if not all(torch.equal(x, y) for x, y in zip(d_out[b], run.outs)) or \
+                not all(torch.equal(h, o.cpu()) for h, o in zip(h_out[b], run.outs)):
+            raise RuntimeError("pipelined end-to-end outputs differ from the whole-batch calls")
     return {"value": round(world * c.total / (e_ms * 1e-3)), "unit": "tokens/s",
-            "h2d_bytes_per_step": h_qkv.numel() * 2 + sum(g[2].numel() * 4 for g in groups),
+            "h2d_bytes_per_step": h_qkv.numel() * 2 + h_cu.numel() * 4,
             "d2h_bytes_per_step": sum(o.numel() * 2 for o in run.outs), "ms_per_step": round(e_ms, 4),
-            "pipeline": f"{n_groups} sequence groups; copy in, both layers and copy out on three streams"
-                        + ("; captured once as a CUDA graph, replayed each step" if args.e2e_graph else "")}
+            "pipeline": f"{n} consecutive steps timed together; step k+1's copy in overlaps step k's two layer "
+                        "calls and step k-1's copy out (two buffer sets, three streams); first copy in and last "
+                        f"copy out included; no L2 flush between steps: each step's input "
+                        f"({h_qkv.numel() * 2 / 1e6:.0f} MB) is larger than L2"}
 
 
 # ---- main ----------------------------------------------------------------------------
@@ -628,10 +620,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true")
-    ap.add_argument("--e2e-graph", type=int, default=1, help="replay the end-to-end step from a CUDA graph")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (e2e null): profiling runs")
-    ap.add_argument("--e2e-groups", type=int, default=4,
-                    help="sequence groups the end-to-end step pipelines its copies and calls over")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s load before the timed steps")
     ap.add_argument("--only", default=None,
