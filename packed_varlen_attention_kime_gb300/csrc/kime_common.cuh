@@ -137,6 +137,22 @@ __device__ __forceinline__ void add_f16x2_f32(float& a0, float& a1, uint32_t pai
       : "r"(pair));
 }
 
+// f16 bit pattern of an integer 0..2047 (exact), at compile time
+__host__ __device__ constexpr uint32_t f16_bits_small(int n) {
+  int e = 0;
+  while ((n >> (e + 1)) != 0) ++e;
+  return n == 0 ? 0u : (static_cast<uint32_t>(e + 15) << 10) | ((static_cast<uint32_t>(n) << (10 - e)) & 0x3FFu);
+}
+static_assert(f16_bits_small(1) == 0x3C00u && f16_bits_small(127) == 0x57F0u && f16_bits_small(128) == 0x5800u,
+              "f16 encoding of small integers");
+
+// an integer of magnitude at most 2048 in both halves of an f16 pair (exact)
+__device__ __forceinline__ uint32_t f16x2_splat(int n) {
+  uint32_t r;
+  asm("{\n\t.reg .f16 h;\n\tcvt.rn.f16.s32 h, %1;\n\tmov.b32 %0, {h, h};\n\t}" : "=r"(r) : "r"(n));
+  return r;
+}
+
 // RoPE (rotate-half) of one pair with one rounding per operation and no
 // contraction: the float32 evaluation every kernel here uses.
 __device__ __forceinline__ void rope_pair(float a, float b, float c, float s, float& ya, float& yb) {

@@ -386,24 +386,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             hi = min(hi, i + window - k0);
           }
           if (!row_ok) hi = -1;
+          lo = min(lo, 64);
+          hi = max(hi, -1);
         }
-        float mx;
-        if (full) {
-          float m8[8];
+        // this half's maximum: eight running maxima, two keys per three-input
+        // max.  On a partial tile that maximum also covers masked columns, so
+        // it only bounds the visible one from above: when it cannot move the
+        // reference (the usual case after a row's first tile) neither can the
+        // visible one, and either gives the same reference below; otherwise
+        // the warp takes the maximum again over the visible columns alone
+        // (kNone when there are none), tested against a bit word per 32
+        // columns.
+        float m8[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
 #pragma unroll
-          for (int j = 16; j < 64; j += 2)
-            m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-          mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-        } else {
-          // the maximum over the visible columns only (kNone when there are none)
-          float m8[8];
+        for (int j = 16; j < 64; j += 2)
+          m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+        float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+        if (!full && __any_sync(0xffffffffu, mx > m_ref + kLazy)) {
+          uint32_t vis[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int a = lo - 32 * k, b = hi - 32 * k;  // the interval in this word's bit positions
+            const uint32_t upto_b = b < 0 ? 0u : (2u << min(b, 31)) - 1u;
+            const uint32_t below_a = a <= 0 ? 0u : (a >= 32 ? ~0u : (1u << a) - 1u);
+            vis[k] = upto_b & ~below_a;
+          }
 #pragma unroll
           for (int k = 0; k < 8; ++k) m8[k] = kNone;
 #pragma unroll
           for (int j = 0; j < 64; ++j)
-            if (j >= lo && j <= hi) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(v[j]));
+            if ((vis[j >> 5] >> (j & 31)) & 1u) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(v[j]));
           mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         }
         // the row's maximum over both halves
@@ -434,16 +448,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "r"(v[2 * e]), "r"(v[2 * e + 1]));
           asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(xx), "l"(mm));
           uint32_t hh;
-          asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.f16x2.f32 %0, hi, lo;\n\t}" : "=r"(hh) : "l"(d));
+          asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.satfinite.f16x2.f32 %0, hi, lo;\n\t}"
+              : "=r"(hh)
+              : "l"(d));
           asm("ex2.approx.f16x2 %0, %1;" : "=r"(pw[e]) : "r"(hh));
         }
         if (!full) {
-          // masked columns: probability zero
+          // masked columns: probability zero, from the column indices compared
+          // with [lo, hi] as f16 pairs (exact for -1..64; each half of a
+          // comparison is 0xFFFF when true)
+          const uint32_t lo2 = f16x2_splat(lo), hi2 = f16x2_splat(hi);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const uint32_t m0 = (2 * e >= lo && 2 * e <= hi) ? 0x0000FFFFu : 0u;
-            const uint32_t m1 = (2 * e + 1 >= lo && 2 * e + 1 <= hi) ? 0xFFFF0000u : 0u;
-            pw[e] &= m0 | m1;
+            const uint32_t cols = f16_bits_small(2 * e) | (f16_bits_small(2 * e + 1) << 16);
+            uint32_t ge, le;
+            asm("set.ge.u32.f16x2 %0, %1, %2;" : "=r"(ge) : "r"(cols), "r"(lo2));
+            asm("set.le.u32.f16x2 %0, %1, %2;" : "=r"(le) : "r"(cols), "r"(hi2));
+            pw[e] &= ge & le;
           }
         }
         // the row sum of this half: the f16 probabilities the PV MMA takes,

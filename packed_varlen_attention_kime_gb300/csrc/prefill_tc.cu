@@ -104,21 +104,6 @@ struct Layout {
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLazy = 8.f;  // the reference max moves when exceeded by more (log2 units)
 
-// f16 bit pattern of an integer 0..2047 (exact), at compile time
-__host__ __device__ constexpr uint32_t f16_bits_small(int n) {
-  int e = 0;
-  while ((n >> (e + 1)) != 0) ++e;
-  return n == 0 ? 0u : (static_cast<uint32_t>(e + 15) << 10) | ((static_cast<uint32_t>(n) << (10 - e)) & 0x3FFu);
-}
-static_assert(f16_bits_small(1) == 0x3C00u && f16_bits_small(127) == 0x57F0u && f16_bits_small(128) == 0x5800u,
-              "f16 encoding of small integers");
-
-// an integer of magnitude at most 2048 in both halves of an f16 pair (exact)
-__device__ __forceinline__ uint32_t f16x2_splat(int n) {
-  uint32_t r;
-  asm("{\n\t.reg .f16 h;\n\tcvt.rn.f16.s32 h, %1;\n\tmov.b32 %0, {h, h};\n\t}" : "=r"(r) : "r"(n));
-  return r;
-}
 constexpr uint32_t kIdescS = idesc_f16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
 
@@ -132,7 +117,6 @@ constexpr uint32_t kIdescPV = idesc_f16_f32(128, 64, 0, 1);
 struct UnitInfo {
   int32_t u, s, qt0, nt, kb, ke, row0, L, off, kbase;
 };
-
 
 struct Shared {
   uint64_t unit_full[2], unit_empty[2];
