@@ -103,8 +103,11 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
 // Attention over prepared rows (prefill_rows.cu): rows_map addresses the
 // rows written by launch_qkv_prep ([total, W] f16, boxes of 128 rows x 64
 // columns, 128-byte swizzle); the work list is the scheduler's in ws.
+// short_seqs: the sequences are short on average (units end every few key
+// tiles), which selects the kernel whose epilogue coalesces its stores.
 cudaError_t launch_prefill_rows(const CUtensorMap* rows_map, int heads, int kv_heads, int window, int causal,
-                                void* out, void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st);
+                                void* out, void* ws, int max_pairs, int short_seqs, int32_t* dev_status,
+                                cudaStream_t st);
 // The QKV projection qkv = x W^T (proj.cu): x_map over x [T, hidden] bf16
 // (boxes of 64 columns x 128 rows), w_map over W [64 (heads + 2 kv_heads),
 // hidden] bf16 (boxes of 64 columns x 192 rows), both with 128-byte swizzle;

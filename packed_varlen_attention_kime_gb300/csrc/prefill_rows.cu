@@ -140,6 +140,12 @@ __device__ __forceinline__ void unit_ranges(const UnitInfo& inf, int w, int caus
   if (w < inf.nt) tile_ranges(inf.L, inf.L - inf.kbase, -inf.kbase, inf.qt0 + w, causal, window, kb, ke, fb, fe);
 }
 
+// kCoalesce: the epilogue transposes each warp's output chunks among groups
+// of four lanes so that every store writes 64 contiguous bytes of eight rows
+// (for short sequences, where units end every few key tiles and their stores
+// meet in the store queue); otherwise each thread stores its own row (for
+// long sequences the extra code costs more than it saves).  Same bits.
+template <bool kCoalesce>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_rows_kernel(const __grid_constant__ CUtensorMap rows_map, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -512,18 +518,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         if (named_bar_or(bar_id, 256, !ok)) break;
         const float lsum = l + xl[(1 - c) * 128 + r];
-        if (row_ok) {
-          const float inv = 1.f / lsum;
+        // this half's 32 output columns of the row, O / l, as four 16-byte
+        // chunks (a row without visible keys computes garbage and is not
+        // stored)
+        const float inv = 1.f / lsum;
+        uint32_t wv[16];
+#pragma unroll
+        for (int d = 0; d < 32; d += 2) wv[d >> 1] = pack_bf16x2(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv);
+        if constexpr (kCoalesce) {
+          // Transposed among each group of four lanes (two butterfly steps),
+          // so that lane 4g + j holds chunk j of rows 4g .. 4g + 3: each store
+          // below then writes 64 contiguous bytes of eight rows rather than
+          // 16 bytes of 32 rows.
+          const int j4 = lane & 3;
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {  // the off-diagonal 2x2 blocks trade places
+            const int out_at = (j4 & 2) ? m : m + 2;
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+              const uint32_t x = (j4 & 2) ? wv[4 * m + w4] : wv[4 * (m + 2) + w4];
+              const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 2);
+              if (out_at == m) wv[4 * m + w4] = y; else wv[4 * (m + 2) + w4] = y;
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {  // each 2x2 block is transposed
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+              const uint32_t x = (j4 & 1) ? wv[4 * (2 * b) + w4] : wv[4 * (2 * b + 1) + w4];
+              const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 1);
+              if (j4 & 1) wv[4 * (2 * b) + w4] = y; else wv[4 * (2 * b + 1) + w4] = y;
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int ik = i - lane + (lane & ~3) + k;  // the row whose chunk j4 this lane holds in slot k
+            if (ik < inf.L) {
+              __nv_bfloat16* dst = p.out + static_cast<size_t>(inf.row0 + ik) * p.heads * kHead + h * kHead + 32 * c;
+              *reinterpret_cast<uint4*>(dst + 8 * j4) = make_uint4(wv[4 * k], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
+            }
+          }
+        } else if (row_ok) {
           __nv_bfloat16* dst = p.out + static_cast<size_t>(inf.row0 + i) * p.heads * kHead + h * kHead + 32 * c;
 #pragma unroll
-          for (int d = 0; d < 32; d += 8) {
-            uint4 wv;
-            wv.x = pack_bf16x2(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv);
-            wv.y = pack_bf16x2(__uint_as_float(ov[d + 2]) * inv, __uint_as_float(ov[d + 3]) * inv);
-            wv.z = pack_bf16x2(__uint_as_float(ov[d + 4]) * inv, __uint_as_float(ov[d + 5]) * inv);
-            wv.w = pack_bf16x2(__uint_as_float(ov[d + 6]) * inv, __uint_as_float(ov[d + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + d) = wv;
-          }
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
         }
         // (the partner reads xl[c] before its next barrier with this thread,
         // the first of the next unit, so xl is free to be written again then)
@@ -543,8 +582,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_prefill_rows(const CUtensorMap* rows_map, int heads, int kv_heads, int window, int causal,
-                                void* out, void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st) {
+namespace {
+template <bool kCoalesce>
+cudaError_t launch_rows(const CUtensorMap* rows_map, const Params& prm, cudaStream_t st) {
   static int configured[64] = {};
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -553,22 +593,13 @@ cudaError_t launch_prefill_rows(const CUtensorMap* rows_map, int heads, int kv_h
   if (dev >= 64 || !configured[dev]) {
     // the register split above assumes the launch count ptxas gave the kernel
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, prefill_rows_kernel)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, prefill_rows_kernel<kCoalesce>)) != cudaSuccess) return e;
     if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidKernelImage;
-    if ((e = cudaFuncSetAttribute(prefill_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(prefill_rows_kernel<kCoalesce>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   Layout::bytes)) != cudaSuccess)
       return e;
     if (dev < 64) configured[dev] = 1;
   }
-  Params prm;
-  prm.heads = heads;
-  prm.kv_heads = kv_heads;
-  prm.window = window;
-  prm.causal = causal;
-  prm.out = static_cast<__nv_bfloat16*>(out);
-  prm.hdr = static_cast<WsHeader*>(ws);
-  prm.duos = ws_duos(ws, max_pairs);
-  prm.dev_status = dev_status;
   // launched with programmatic stream serialization: its prologue overlaps
   // the kernels before it, whose results it waits for (griddep_wait)
   cudaLaunchConfig_t cfg = {};
@@ -581,7 +612,23 @@ cudaError_t launch_prefill_rows(const CUtensorMap* rows_map, int heads, int kv_h
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_rows_kernel, *rows_map, prm);
+  return cudaLaunchKernelEx(&cfg, prefill_rows_kernel<kCoalesce>, *rows_map, prm);
+}
+}  // namespace
+
+cudaError_t launch_prefill_rows(const CUtensorMap* rows_map, int heads, int kv_heads, int window, int causal,
+                                void* out, void* ws, int max_pairs, int short_seqs, int32_t* dev_status,
+                                cudaStream_t st) {
+  Params prm;
+  prm.heads = heads;
+  prm.kv_heads = kv_heads;
+  prm.window = window;
+  prm.causal = causal;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.hdr = static_cast<WsHeader*>(ws);
+  prm.duos = ws_duos(ws, max_pairs);
+  prm.dev_status = dev_status;
+  return short_seqs ? launch_rows<true>(rows_map, prm, st) : launch_rows<false>(rows_map, prm, st);
 }
 
 }  // namespace kime

@@ -271,6 +271,27 @@ def test_odd_tile_counts_match_the_oracle_everywhere(cuda_lib, lengths, H, Hkv, 
     check_bf16(out.float().cpu().numpy().reshape(ref.shape), ref, f"odd tile counts w{window} c{causal}")
 
 
+@pytest.mark.parametrize("causal,window", [(False, -1), (True, -1), (False, 200)])
+def test_both_epilogue_stores_give_the_same_bits(cuda_lib, causal, window):
+    # The kernel over prepared rows has two epilogues: stores coalesced
+    # through a four-lane transpose (batches of short sequences) or one row
+    # per thread (long ones).  A 300-token sequence alone takes the first,
+    # packed with a 7,000-token one the second; its rows match bit for bit.
+    dev = torch.device("cuda")
+    H, Hkv = 4, 2
+    both = random_qkv([300, 7000], H, Hkv, torch.bfloat16, 1.5, seed=45)
+    outs = []
+    for lengths, qkv in (([300], both[:300]), ([300, 7000], both)):
+        cu = cu_from_lengths(lengths)
+        T, n, mx = qkv.shape[0], len(lengths), max(lengths)
+        c, s = gpu_tables(1e4, mx)
+        ws = torch.empty(kime.kime_attn_workspace_bytes(3, n, T, H, Hkv), dtype=torch.uint8, device=dev)
+        outs.append(kime.kime_attn_varlen(qkv.contiguous().to(dev), cu.to(dev), mx, H, Hkv, window, causal, 0.125,
+                                          c, s, workspace=ws))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1][:300])
+
+
 def test_device_status_flags_bad_cu_and_skips(cuda_lib):
     dev = torch.device("cuda")
     lengths, H = [100, 50, 30], 2
