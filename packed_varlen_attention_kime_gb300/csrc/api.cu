@@ -235,6 +235,7 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
                                                  short_seqs(n_seqs, total_tokens), dev_status, st));
   return cuda_status(kime::launch_prefill_tc(&map, nullptr, nullptr, &cmap, &smap, heads, kv_heads, 0, window,
                                              causal, scale, rope_cos, rope_sin, out, workspace, max_pairs,
+                                             short_seqs(n_seqs, total_tokens) || (window >= 0 && window <= 128),
                                              dev_status, st));
 }
 
@@ -341,7 +342,7 @@ int chunk_attend(const void* qkv, const int32_t* cu, const int32_t* pos, int n_s
   if ((rc = encode_qkv_map(&kmap, k_cache, rows, kime::kHead))) return rc;
   if ((rc = encode_qkv_map(&vmap, v_cache, rows, kime::kHead))) return rc;
   return cuda_status(kime::launch_prefill_tc(&qmap, &kmap, &vmap, nullptr, nullptr, heads, kv_heads, cap, -1, 1, scale,
-                                             rope_cos, rope_sin, out, workspace, max_pairs, dev_status, st));
+                                             rope_cos, rope_sin, out, workspace, max_pairs, 0, dev_status, st));
 }
 
 int chunk_common(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total, int max_seqlen,

@@ -265,7 +265,12 @@ struct Params {
 // K rotated here.  kCache = true: chunks attending a KV cache that already
 // holds them (rotated keys); K and V tiles come from the cache maps, rows past
 // the sequence's keys are zeroed, q rows sit at positions off + i.
-template <bool kCache>
+// kCoalesce: the epilogue transposes each warp's output chunks among groups
+// of four lanes (per 64-byte half row) so that every store writes 64
+// contiguous bytes of eight rows -- for units that end every few key tiles
+// (a narrow window, short sequences), whose stores otherwise crowd the store
+// queue; long units keep one row per thread (less code).  Same bits.
+template <bool kCache, bool kCoalesce>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qkv_map, const __grid_constant__ CUtensorMap k_map,
                       const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap cos_map,
@@ -823,7 +828,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64_wait(tO, ov);
       tc_fence_before();
       if (named_bar_or(1 + w, 128, !ok)) break;
-      if (row_ok) {
+      if constexpr (kCoalesce) {
+        // the row's 64 output columns, O / l, as eight 16-byte chunks (a row
+        // without visible keys computes garbage and is not stored), then per
+        // half row transposed among each group of four lanes (two butterfly
+        // steps): lane 4g + j then holds chunk j of the half for rows 4g ..
+        // 4g + 3, and each store writes 64 contiguous bytes of eight rows
+        const float inv = 1.f / l;
+        uint32_t wv[32];
+#pragma unroll
+        for (int d = 0; d < kHead; d += 2) wv[d >> 1] = pack_bf16x2(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv);
+        const int j4 = lane & 3;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t* hv = wv + 16 * hf;
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {  // the off-diagonal 2x2 blocks trade places
+            const int out_at = (j4 & 2) ? m : m + 2;
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+              const uint32_t x = (j4 & 2) ? hv[4 * m + w4] : hv[4 * (m + 2) + w4];
+              const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 2);
+              if (out_at == m) hv[4 * m + w4] = y; else hv[4 * (m + 2) + w4] = y;
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {  // each 2x2 block is transposed
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+              const uint32_t x = (j4 & 1) ? hv[4 * (2 * b) + w4] : hv[4 * (2 * b + 1) + w4];
+              const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 1);
+              if (j4 & 1) hv[4 * (2 * b) + w4] = y; else hv[4 * (2 * b + 1) + w4] = y;
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int ik = i - lane + (lane & ~3) + k;  // the row whose chunks j4 this lane holds in slot k
+          if (ik < inf.L) {
+            __nv_bfloat16* dst = p.out + static_cast<size_t>(inf.row0 + ik) * p.heads * kHead + h * kHead + 8 * j4;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(wv[4 * k], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
+            *reinterpret_cast<uint4*>(dst + 32) =
+                make_uint4(wv[16 + 4 * k], wv[16 + 4 * k + 1], wv[16 + 4 * k + 2], wv[16 + 4 * k + 3]);
+          }
+        }
+      } else if (row_ok) {
         const float inv = 1.f / l;
         __nv_bfloat16* dst = p.out + static_cast<size_t>(inf.row0 + i) * p.heads * kHead + h * kHead;
 #pragma unroll
@@ -880,21 +929,25 @@ extern "C" int kime_debug_phase_clear() {
 cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_map, const CUtensorMap* v_map,
                               const CUtensorMap* cos_map, const CUtensorMap* sin_map, int heads, int kv_heads, int cap,
                               int window, int causal, float scale, const float* cos_t, const float* sin_t, void* out,
-                              void* ws, int max_pairs, int32_t* dev_status, cudaStream_t st) {
-  // kernel variant: packed sequences (keys rotated here), or chunks against the caches
-  const bool chunks = k_map != nullptr;
-  static int configured[2][64] = {};
+                              void* ws, int max_pairs, int short_units, int32_t* dev_status, cudaStream_t st) {
+  // kernel variant: packed sequences (keys rotated here), or chunks against
+  // the caches; the epilogue's stores coalesced or one row per thread
+  const bool chunks = k_map != nullptr, co = short_units != 0;
+  static int configured[4][64] = {};
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const uint32_t smem_bytes = chunks ? Layout<false>::bytes : Layout<true>::bytes;
-  const void* fn = chunks ? reinterpret_cast<const void*>(prefill_tc_kernel<true>)
-                          : reinterpret_cast<const void*>(prefill_tc_kernel<false>);
-  if (dev >= 64 || !configured[chunks][dev]) {
+  const void* fn = chunks ? (co ? reinterpret_cast<const void*>(prefill_tc_kernel<true, true>)
+                                : reinterpret_cast<const void*>(prefill_tc_kernel<true, false>))
+                          : (co ? reinterpret_cast<const void*>(prefill_tc_kernel<false, true>)
+                                : reinterpret_cast<const void*>(prefill_tc_kernel<false, false>));
+  const int vi = 2 * chunks + co;
+  if (dev >= 64 || !configured[vi][dev]) {
     if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) != cudaSuccess)
       return e;
-    if (dev < 64) configured[chunks][dev] = 1;
+    if (dev < 64) configured[vi][dev] = 1;
   }
   Params prm;
   prm.heads = heads;
@@ -922,8 +975,14 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (chunks)
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true>, *qkv_map, *k_map, *v_map, *qkv_map, *qkv_map, prm);
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false>, *qkv_map, *qkv_map, *qkv_map, *cos_map, *sin_map, prm);
+    return co ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, true>, *qkv_map, *k_map, *v_map, *qkv_map,
+                                   *qkv_map, prm)
+              : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, false>, *qkv_map, *k_map, *v_map, *qkv_map,
+                                   *qkv_map, prm);
+  return co ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, true>, *qkv_map, *qkv_map, *qkv_map, *cos_map,
+                                 *sin_map, prm)
+            : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, false>, *qkv_map, *qkv_map, *qkv_map, *cos_map,
+                                 *sin_map, prm);
 }
 
 }  // namespace kime
