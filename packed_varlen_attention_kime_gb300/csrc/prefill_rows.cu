@@ -42,6 +42,8 @@
 // unit the two warpgroups of a tile add their row sums and each writes its 32
 // output columns of the row, O / l.  Every wait is bounded in time; on a
 // timeout every role winds down.
+#include <type_traits>
+
 #include "kime_common.cuh"
 
 namespace kime {
@@ -370,138 +372,157 @@ __global__ void __launch_bounds__(kThreads, 1)
       // to m_ref, which moves -- rescaling O and l -- only when a row's max
       // exceeds it by more than 2^8.  Logits arrive in log2 units.
       float m_ref = kNone, l = 0.f;
-      for (int t = kb; t < ke; ++t) {
-        ok = wait(&sh->s_full[w], sc & 1) && ok;
-        ++sc;
-        tc_fence_after();
-        uint32_t v[64];
-        tmem_ld64_wait(tS, v);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->s_read[w]);  // the S buffer may take S(t+1)
-        // visible keys of this row in this half form one interval [lo, hi]
-        // of column indices 0..63 (only partial tiles test columns)
-        const bool full = t >= fb && t < fe;
-        int lo = 0, hi = 63;
-        if (!full) {
-          const int k0 = inf.kbase + t * kBN + 64 * c;  // this half's first key
-          hi = min(63, inf.L - 1 - k0);
-          if (causal) hi = min(hi, i - k0);
-          if (window >= 0) {
-            lo = max(0, max(i - window, 0) - k0);  // (a grid may start below key 0)
-            hi = min(hi, i + window - k0);
-          }
-          if (!row_ok) hi = -1;
-          lo = min(lo, 64);
-          hi = max(hi, -1);
-        }
-        // this half's maximum: eight running maxima, two keys per three-input
-        // max.  On a partial tile that maximum also covers masked columns, so
-        // it only bounds the visible one from above: when it cannot move the
-        // reference (the usual case after a row's first tile) neither can the
-        // visible one, and either gives the same reference below; otherwise
-        // the warp takes the maximum again over the visible columns alone
-        // (kNone when there are none), tested against a bit word per 32
-        // columns.
-        float m8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
-#pragma unroll
-        for (int j = 16; j < 64; j += 2)
-          m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-        float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-        if (!full && __any_sync(0xffffffffu, mx > m_ref + kLazy)) {
-          uint32_t vis[2];
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int a = lo - 32 * k, b = hi - 32 * k;  // the interval in this word's bit positions
-            const uint32_t upto_b = b < 0 ? 0u : (2u << min(b, 31)) - 1u;
-            const uint32_t below_a = a <= 0 ? 0u : (a >= 32 ? ~0u : (1u << a) - 1u);
-            vis[k] = upto_b & ~below_a;
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = kNone;
-#pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if ((vis[j >> 5] >> (j & 31)) & 1u) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(v[j]));
-          mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-        }
-        // the row's maximum over both halves
-        float* xb = xch + (xc & 1) * 256;
-        ++xc;
-        xb[c * 128 + r] = mx;
-        if (named_bar_or(bar_id, 256, !ok)) {
-          ok = false;
-          break;
-        }
-        mx = fmaxf(mx, xb[(1 - c) * 128 + r]);
-        // move the reference max on the first visible keys, or when it is
-        // exceeded by more than kLazy
-        float alpha = 1.f;
-        if (mx > m_ref + kLazy) {
-          if (m_ref != kNone) alpha = fast_exp2(m_ref - mx);
-          m_ref = mx;
-        }
-        // P = 2^(x - m_ref): the differences in float32 pairs, rounded to f16
-        // pairs, two exponentials per MUFU operation (P in f16, as the MMA
-        // takes it)
-        uint64_t mm;
-        asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(m_ref));
-        uint32_t pw[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          uint64_t xx, d;
-          asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "r"(v[2 * e]), "r"(v[2 * e + 1]));
-          asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(xx), "l"(mm));
-          uint32_t hh;
-          asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.satfinite.f16x2.f32 %0, hi, lo;\n\t}"
-              : "=r"(hh)
-              : "l"(d));
-          asm("ex2.approx.f16x2 %0, %1;" : "=r"(pw[e]) : "r"(hh));
-        }
-        if (!full) {
-          // masked columns: probability zero, from the column indices compared
-          // with [lo, hi] as f16 pairs (exact for -1..64; each half of a
-          // comparison is 0xFFFF when true)
-          const uint32_t lo2 = f16x2_splat(lo), hi2 = f16x2_splat(hi);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const uint32_t cols = f16_bits_small(2 * e) | (f16_bits_small(2 * e + 1) << 16);
-            uint32_t ge, le;
-            asm("set.ge.u32.f16x2 %0, %1, %2;" : "=r"(ge) : "r"(cols), "r"(lo2));
-            asm("set.le.u32.f16x2 %0, %1, %2;" : "=r"(le) : "r"(cols), "r"(hi2));
-            pw[e] &= ge & le;
-          }
-        }
-        // the row sum of this half: the f16 probabilities the PV MMA takes,
-        // each added in float32
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          add_f16x2_f32(s4[0], s4[1], pw[e]);
-          add_f16x2_f32(s4[2], s4[3], pw[e + 1]);
-        }
-        l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
-        // PV(t-1) read P(t-1) and accumulated into O: it completes before
-        // P(t) is stored and O is rescaled
-        if (t > kb) {
-          ok = wait(&sh->pv_full[w], pvc & 1) && ok;
-          ++pvc;
+      // One key tile of the unit.  For long units full_tag says at compile
+      // time whether every row sees all of the tile's keys, so the full tiles
+      // [fb, fe) -- the run in the middle of the range, nearly all of them on
+      // long full-attention layers -- loop over code without the partial
+      // tiles' column tests; short units, which alternate between the two
+      // kinds, keep one loop that tests each tile (less code).
+      auto tile = [&](const int t, auto full_tag) -> bool {
+          ok = wait(&sh->s_full[w], sc & 1) && ok;
+          ++sc;
           tc_fence_after();
-        }
-        tmem_st32(tP, pw);
-        if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {  // this half's 32 output columns
-          uint32_t ov[32];
-          tmem_ld32(tO, ov);
-          tmem_wait_ld();
-#pragma unroll
-          for (int d = 0; d < 32; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
-          tmem_st32(tO, ov);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->p_full[w]);
+          uint32_t v[64];
+          tmem_ld64_wait(tS, v);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->s_read[w]);  // the S buffer may take S(t+1)
+          // visible keys of this row in this half form one interval [lo, hi]
+          // of column indices 0..63 (only partial tiles test columns)
+          bool full;
+          if constexpr (std::is_same_v<decltype(full_tag), bool>)
+            full = t >= fb && t < fe;
+          else
+            full = decltype(full_tag)::value;
+          int lo = 0, hi = 63;
+          if (!full) {
+            const int k0 = inf.kbase + t * kBN + 64 * c;  // this half's first key
+            hi = min(63, inf.L - 1 - k0);
+            if (causal) hi = min(hi, i - k0);
+            if (window >= 0) {
+              lo = max(0, max(i - window, 0) - k0);  // (a grid may start below key 0)
+              hi = min(hi, i + window - k0);
+            }
+            if (!row_ok) hi = -1;
+            lo = min(lo, 64);
+            hi = max(hi, -1);
+          }
+          // this half's maximum: eight running maxima, two keys per three-input
+          // max.  On a partial tile that maximum also covers masked columns, so
+          // it only bounds the visible one from above: when it cannot move the
+          // reference (the usual case after a row's first tile) neither can the
+          // visible one, and either gives the same reference below; otherwise
+          // the warp takes the maximum again over the visible columns alone
+          // (kNone when there are none), tested against a bit word per 32
+          // columns.
+          float m8[8];
+  #pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+  #pragma unroll
+          for (int j = 16; j < 64; j += 2)
+            m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+          float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+          if (!full && __any_sync(0xffffffffu, mx > m_ref + kLazy)) {
+            uint32_t vis[2];
+  #pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int a = lo - 32 * k, b = hi - 32 * k;  // the interval in this word's bit positions
+              const uint32_t upto_b = b < 0 ? 0u : (2u << min(b, 31)) - 1u;
+              const uint32_t below_a = a <= 0 ? 0u : (a >= 32 ? ~0u : (1u << a) - 1u);
+              vis[k] = upto_b & ~below_a;
+            }
+  #pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = kNone;
+  #pragma unroll
+            for (int j = 0; j < 64; ++j)
+              if ((vis[j >> 5] >> (j & 31)) & 1u) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(v[j]));
+            mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+          }
+          // the row's maximum over both halves
+          float* xb = xch + (xc & 1) * 256;
+          ++xc;
+          xb[c * 128 + r] = mx;
+          if (named_bar_or(bar_id, 256, !ok)) {
+            ok = false;
+            return false;
+          }
+          mx = fmaxf(mx, xb[(1 - c) * 128 + r]);
+          // move the reference max on the first visible keys, or when it is
+          // exceeded by more than kLazy
+          float alpha = 1.f;
+          if (mx > m_ref + kLazy) {
+            if (m_ref != kNone) alpha = fast_exp2(m_ref - mx);
+            m_ref = mx;
+          }
+          // P = 2^(x - m_ref): the differences in float32 pairs, rounded to f16
+          // pairs, two exponentials per MUFU operation (P in f16, as the MMA
+          // takes it)
+          uint64_t mm;
+          asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(m_ref));
+          uint32_t pw[32];
+  #pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            uint64_t xx, d;
+            asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "r"(v[2 * e]), "r"(v[2 * e + 1]));
+            asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(xx), "l"(mm));
+            uint32_t hh;
+            asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.satfinite.f16x2.f32 %0, hi, lo;\n\t}"
+                : "=r"(hh)
+                : "l"(d));
+            asm("ex2.approx.f16x2 %0, %1;" : "=r"(pw[e]) : "r"(hh));
+          }
+          if (!full) {
+            // masked columns: probability zero, from the column indices compared
+            // with [lo, hi] as f16 pairs (exact for -1..64; each half of a
+            // comparison is 0xFFFF when true)
+            const uint32_t lo2 = f16x2_splat(lo), hi2 = f16x2_splat(hi);
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const uint32_t cols = f16_bits_small(2 * e) | (f16_bits_small(2 * e + 1) << 16);
+              uint32_t ge, le;
+              asm("set.ge.u32.f16x2 %0, %1, %2;" : "=r"(ge) : "r"(cols), "r"(lo2));
+              asm("set.le.u32.f16x2 %0, %1, %2;" : "=r"(le) : "r"(cols), "r"(hi2));
+              pw[e] &= ge & le;
+            }
+          }
+          // the row sum of this half: the f16 probabilities the PV MMA takes,
+          // each added in float32
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            add_f16x2_f32(s4[0], s4[1], pw[e]);
+            add_f16x2_f32(s4[2], s4[3], pw[e + 1]);
+          }
+          l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+          // PV(t-1) read P(t-1) and accumulated into O: it completes before
+          // P(t) is stored and O is rescaled
+          if (t > kb) {
+            ok = wait(&sh->pv_full[w], pvc & 1) && ok;
+            ++pvc;
+            tc_fence_after();
+          }
+          tmem_st32(tP, pw);
+          if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {  // this half's 32 output columns
+            uint32_t ov[32];
+            tmem_ld32(tO, ov);
+            tmem_wait_ld();
+  #pragma unroll
+            for (int d = 0; d < 32; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
+            tmem_st32(tO, ov);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->p_full[w]);
+        return true;
+      };
+      bool more = true;
+      if constexpr (kCoalesce) {
+        for (int t = kb; more && t < ke; ++t) more = tile(t, true);
+      } else {
+        for (int t = kb; more && t < fb; ++t) more = tile(t, std::false_type{});
+        for (int t = fb; more && t < fe; ++t) more = tile(t, std::true_type{});
+        for (int t = fe; more && t < ke; ++t) more = tile(t, std::false_type{});
       }
       // the tile's 256 threads leave together after a failed wait
       if (named_bar_or(bar_id, 256, !ok)) break;
