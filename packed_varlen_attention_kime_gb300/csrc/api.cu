@@ -235,8 +235,7 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
                                                  short_seqs(n_seqs, total_tokens), dev_status, st));
   return cuda_status(kime::launch_prefill_tc(&map, nullptr, nullptr, &cmap, &smap, heads, kv_heads, 0, window,
                                              causal, scale, rope_cos, rope_sin, out, workspace, max_pairs,
-                                             short_seqs(n_seqs, total_tokens) || (window >= 0 && window <= 128),
-                                             dev_status, st));
+                                             short_seqs(n_seqs, total_tokens), dev_status, st));
 }
 
 int kime_qkv_proj(const void* x, const void* w, int total_tokens, int hidden, int heads, int kv_heads,

@@ -100,8 +100,9 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
                               const CUtensorMap* cos_map, const CUtensorMap* sin_map, int heads, int kv_heads, int cap,
                               int window, int causal, float scale, const float* cos_t, const float* sin_t, void* out,
                               void* ws, int max_pairs, int short_units, int32_t* dev_status, cudaStream_t st);
-// (short_units: units end every few key tiles -- a narrow window or short
-// sequences -- which selects the kernel whose epilogue coalesces its stores.)
+// (short_units: the sequences are short on average; with a window of at most
+// 128 the units are short anyway.  Either selects a kernel whose epilogue
+// coalesces its stores.)
 // Attention over prepared rows (prefill_rows.cu): rows_map addresses the
 // rows written by launch_qkv_prep ([total, W] f16, boxes of 128 rows x 64
 // columns, 128-byte swizzle); the work list is the scheduler's in ws.

@@ -265,12 +265,17 @@ struct Params {
 // K rotated here.  kCache = true: chunks attending a KV cache that already
 // holds them (rotated keys); K and V tiles come from the cache maps, rows past
 // the sequence's keys are zeroed, q rows sit at positions off + i.
-// kCoalesce: the epilogue transposes each warp's output chunks among groups
-// of four lanes (per 64-byte half row) so that every store writes 64
-// contiguous bytes of eight rows -- for units that end every few key tiles
-// (a narrow window, short sequences), whose stores otherwise crowd the store
-// queue; long units keep one row per thread (less code).  Same bits.
-template <bool kCache, bool kCoalesce>
+// kMode (same bits in every mode):
+//   0  long units: each key tile tested for being full (every row sees all
+//      its keys), one output row per thread in the epilogue (least code);
+//   1  short sequences: units end every few key tiles and their stores crowd
+//      the store queue, so the epilogue transposes each warp's output chunks
+//      among groups of four lanes (per 64-byte half row) and every store
+//      writes 64 contiguous bytes of eight rows;
+//   2  a window of at most 128: as 1, and every key tile takes the partial
+//      path (a query tile's keys then span tiles no row sees whole, so the
+//      full-tile code would only take room in the loop).
+template <bool kCache, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qkv_map, const __grid_constant__ CUtensorMap k_map,
                       const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap cos_map,
@@ -692,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         PHASE(1);
         // visible keys of this row in this tile form one interval [lo, hi]
         // of column indices (only partial tiles test columns)
-        const bool full = t >= fb && t < fe;
+        const bool full = kMode != 2 && t >= fb && t < fe;
         int lo = 0, hi = kBN - 1;
         if (!full) {
           if (kCache) {
@@ -828,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64_wait(tO, ov);
       tc_fence_before();
       if (named_bar_or(1 + w, 128, !ok)) break;
-      if constexpr (kCoalesce) {
+      if constexpr (kMode >= 1) {
         // the row's 64 output columns, O / l, as eight 16-byte chunks (a row
         // without visible keys computes garbage and is not stored), then per
         // half row transposed among each group of four lanes (two butterfly
@@ -930,20 +935,21 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
                               const CUtensorMap* cos_map, const CUtensorMap* sin_map, int heads, int kv_heads, int cap,
                               int window, int causal, float scale, const float* cos_t, const float* sin_t, void* out,
                               void* ws, int max_pairs, int short_units, int32_t* dev_status, cudaStream_t st) {
-  // kernel variant: packed sequences (keys rotated here), or chunks against
-  // the caches; the epilogue's stores coalesced or one row per thread
-  const bool chunks = k_map != nullptr, co = short_units != 0;
+  // kernel variant: packed sequences (keys rotated here) in one of three
+  // modes, or chunks against the caches (long units)
+  const bool chunks = k_map != nullptr;
+  const int mode = chunks ? 0 : (window >= 0 && window <= 128 ? 2 : (short_units ? 1 : 0));
   static int configured[4][64] = {};
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const uint32_t smem_bytes = chunks ? Layout<false>::bytes : Layout<true>::bytes;
-  const void* fn = chunks ? (co ? reinterpret_cast<const void*>(prefill_tc_kernel<true, true>)
-                                : reinterpret_cast<const void*>(prefill_tc_kernel<true, false>))
-                          : (co ? reinterpret_cast<const void*>(prefill_tc_kernel<false, true>)
-                                : reinterpret_cast<const void*>(prefill_tc_kernel<false, false>));
-  const int vi = 2 * chunks + co;
+  const void* fn = chunks      ? reinterpret_cast<const void*>(prefill_tc_kernel<true, 0>)
+                   : mode == 2 ? reinterpret_cast<const void*>(prefill_tc_kernel<false, 2>)
+                   : mode == 1 ? reinterpret_cast<const void*>(prefill_tc_kernel<false, 1>)
+                               : reinterpret_cast<const void*>(prefill_tc_kernel<false, 0>);
+  const int vi = chunks ? 3 : mode;
   if (dev >= 64 || !configured[vi][dev]) {
     if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) != cudaSuccess)
       return e;
@@ -975,14 +981,15 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (chunks)
-    return co ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, true>, *qkv_map, *k_map, *v_map, *qkv_map,
-                                   *qkv_map, prm)
-              : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, false>, *qkv_map, *k_map, *v_map, *qkv_map,
-                                   *qkv_map, prm);
-  return co ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, true>, *qkv_map, *qkv_map, *qkv_map, *cos_map,
-                                 *sin_map, prm)
-            : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, false>, *qkv_map, *qkv_map, *qkv_map, *cos_map,
-                                 *sin_map, prm);
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true, 0>, *qkv_map, *k_map, *v_map, *qkv_map, *qkv_map, prm);
+  if (mode == 2)
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, 2>, *qkv_map, *qkv_map, *qkv_map, *cos_map, *sin_map,
+                              prm);
+  if (mode == 1)
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, 1>, *qkv_map, *qkv_map, *qkv_map, *cos_map, *sin_map,
+                              prm);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false, 0>, *qkv_map, *qkv_map, *qkv_map, *cos_map, *sin_map,
+                            prm);
 }
 
 }  // namespace kime
