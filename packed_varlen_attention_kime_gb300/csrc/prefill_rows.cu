@@ -142,12 +142,17 @@ __device__ __forceinline__ void unit_ranges(const UnitInfo& inf, int w, int caus
   if (w < inf.nt) tile_ranges(inf.L, inf.L - inf.kbase, -inf.kbase, inf.qt0 + w, causal, window, kb, ke, fb, fe);
 }
 
-// kCoalesce: the epilogue transposes each warp's output chunks among groups
-// of four lanes so that every store writes 64 contiguous bytes of eight rows
-// (for short sequences, where units end every few key tiles and their stores
-// meet in the store queue); otherwise each thread stores its own row (for
-// long sequences the extra code costs more than it saves).  Same bits.
-template <bool kCoalesce>
+// kMode (same bits in every mode):
+//   0  long units: the full key tiles (every row sees all their keys) loop
+//      over code without column tests, and each thread stores its own output
+//      row (extra code costs more than it saves here);
+//   1  short sequences: units end every few key tiles and their stores meet
+//      in the store queue, so the epilogue transposes each warp's output
+//      chunks among groups of four lanes and every store writes 64
+//      contiguous bytes of eight rows; one loop tests each tile;
+//   2  a window of at most 128: as 1, with every key tile on the partial path
+//      (no 128-key tile is then seen whole by every row).
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_rows_kernel(const __grid_constant__ CUtensorMap rows_map, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -517,7 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       bool more = true;
-      if constexpr (kCoalesce) {
+      if constexpr (kMode == 2) {
+        for (int t = kb; more && t < ke; ++t) more = tile(t, std::false_type{});
+      } else if constexpr (kMode == 1) {
         for (int t = kb; more && t < ke; ++t) more = tile(t, true);
       } else {
         for (int t = kb; more && t < fb; ++t) more = tile(t, std::false_type{});
@@ -546,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t wv[16];
 #pragma unroll
         for (int d = 0; d < 32; d += 2) wv[d >> 1] = pack_bf16x2(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv);
-        if constexpr (kCoalesce) {
+        if constexpr (kMode >= 1) {
           // Transposed among each group of four lanes (two butterfly steps),
           // so that lane 4g + j holds chunk j of rows 4g .. 4g + 3: each store
           // below then writes 64 contiguous bytes of eight rows rather than
@@ -604,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 namespace {
-template <bool kCoalesce>
+template <int kMode>
 cudaError_t launch_rows(const CUtensorMap* rows_map, const Params& prm, cudaStream_t st) {
   static int configured[64] = {};
   int dev = 0, sms = 0;
@@ -614,9 +621,9 @@ cudaError_t launch_rows(const CUtensorMap* rows_map, const Params& prm, cudaStre
   if (dev >= 64 || !configured[dev]) {
     // the register split above assumes the launch count ptxas gave the kernel
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, prefill_rows_kernel<kCoalesce>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, prefill_rows_kernel<kMode>)) != cudaSuccess) return e;
     if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidKernelImage;
-    if ((e = cudaFuncSetAttribute(prefill_rows_kernel<kCoalesce>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(prefill_rows_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   Layout::bytes)) != cudaSuccess)
       return e;
     if (dev < 64) configured[dev] = 1;
@@ -633,7 +640,7 @@ cudaError_t launch_rows(const CUtensorMap* rows_map, const Params& prm, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_rows_kernel<kCoalesce>, *rows_map, prm);
+  return cudaLaunchKernelEx(&cfg, prefill_rows_kernel<kMode>, *rows_map, prm);
 }
 }  // namespace
 
@@ -649,7 +656,8 @@ cudaError_t launch_prefill_rows(const CUtensorMap* rows_map, int heads, int kv_h
   prm.hdr = static_cast<WsHeader*>(ws);
   prm.duos = ws_duos(ws, max_pairs);
   prm.dev_status = dev_status;
-  return short_seqs ? launch_rows<true>(rows_map, prm, st) : launch_rows<false>(rows_map, prm, st);
+  if (window >= 0 && window <= 128) return launch_rows<2>(rows_map, prm, st);
+  return short_seqs ? launch_rows<1>(rows_map, prm, st) : launch_rows<0>(rows_map, prm, st);
 }
 
 }  // namespace kime
