@@ -46,6 +46,8 @@
 // TMEM), and stores P(t) into TMEM.  Keeping P out of shared memory leaves its
 // bandwidth to the MMA operands Q, K, V.  Every wait is bounded; on a timeout
 // every role winds down.
+#include <type_traits>
+
 #include "kime_common.cuh"
 
 #ifdef KIME_PHASE_PROFILE
@@ -681,150 +683,167 @@ __global__ void __launch_bounds__(kThreads, 1)
       // only moves -- rescaling O and l -- when a row's max exceeds it by more
       // than 2^8.  Logits arrive in log2 units (scale*log2(e) is folded into q).
       float m_ref = kNone, l = 0.f;
-      for (int t = kb; t < ke; ++t) {
-        const int k0 = inf.kbase + t * kBN;
-        PHASE(7);
-        ok = wait(&sh->s_full[w][sc & 1], (sc >> 1) & 1);
-        if (r == 0) EV(3 + w, 0, t);
-        ++sc;
-        tc_fence_after();
-        PHASE(0);
-        // the tile's S buffer is free again once every warp has loaded S(t)
-        uint32_t v[128];
-        tmem_ld128_wait(tmem + w * 128 + lane_off, v);
-        tc_fence_before();
-        if (lane == 0) mbar_arrive(&sh->s_read[w]);
-        PHASE(1);
-        // visible keys of this row in this tile form one interval [lo, hi]
-        // of column indices (only partial tiles test columns)
-        const bool full = kMode != 2 && t >= fb && t < fe;
-        int lo = 0, hi = kBN - 1;
-        if (!full) {
-          if (kCache) {
-            hi = min(kBN - 1, chunk_hi - k0);  // causal at position off + i <= off + L - 1
-          } else {
-            hi = min(kBN - 1, inf.L - 1 - k0);
-            if (kCausal) hi = min(hi, i - k0);
-            if (kWindow >= 0) {
-              lo = max(lo, max(i - kWindow, 0) - k0);  // (a grid may start below key 0)
-              hi = min(hi, i + kWindow - k0);
-            }
-            if (!row_ok) hi = -1;
-          }
-          lo = min(lo, kBN);
-          hi = max(hi, -1);
-        }
-        // row max: eight running maxima, each taking two keys per three-input
-        // max (64 instructions for 128 keys, short dependency chains)
-        float m8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
-#pragma unroll
-        for (int j = 16; j < kBN; j += 2)
-          m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-        float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-        // On a partial tile that maximum also covers masked columns, so it only
-        // bounds the visible one from above: when it cannot move the reference
-        // (the usual case after a row's first tile) the visible maximum cannot
-        // either; otherwise the maximum is taken again over the visible
-        // columns alone (kNone when there are none), tested against a bit word
-        // per 32 columns.
-        if (!full && __any_sync(0xffffffffu, mx > m_ref + kLazy)) {
-          uint32_t vis[kBN / 32];
-#pragma unroll
-          for (int k = 0; k < kBN / 32; ++k) {
-            const int a = lo - 32 * k, b = hi - 32 * k;  // the interval in this word's bit positions
-            const uint32_t upto_b = b < 0 ? 0u : (2u << min(b, 31)) - 1u;
-            const uint32_t below_a = a <= 0 ? 0u : (a >= 32 ? ~0u : (1u << a) - 1u);
-            vis[k] = upto_b & ~below_a;
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) m8[k] = kNone;
-#pragma unroll
-          for (int j = 0; j < kBN; ++j)
-            if ((vis[j >> 5] >> (j & 31)) & 1u) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(v[j]));
-          mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-        }
-        // move the reference max on the first visible keys, or when it is
-        // exceeded by more than kLazy (log2 units)
-        float alpha = 1.f;
-        if (mx > m_ref + kLazy) {
-          if (m_ref != kNone) alpha = fast_exp2(m_ref - mx);
-          m_ref = mx;
-        }
-        PHASE(2);
-        // P = 2^(x - m_ref): the differences in float32 pairs, rounded to f16
-        // pairs (saturating, so no difference becomes infinite), two
-        // exponentials per MUFU operation (P in f16, as the MMA takes it).
-        // All 64 exponent pairs first (independent chains the schedulers can
-        // interleave), then the masked columns set to probability zero.
-        uint64_t mm;
-        asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(m_ref));
-        uint32_t pw[64];
-#pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          uint64_t xx, d;
-          asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "r"(v[2 * e]), "r"(v[2 * e + 1]));
-          asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(xx), "l"(mm));
-          uint32_t h;
-          asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.satfinite.f16x2.f32 %0, hi, lo;\n\t}"
-              : "=r"(h)
-              : "l"(d));
-          asm("ex2.approx.f16x2 %0, %1;" : "=r"(pw[e]) : "r"(h));
-        }
-        if (!full) {
-          // column indices against [lo, hi] as f16 pairs (exact for 0..128):
-          // each half of a comparison is 0xFFFF when true
-          const uint32_t lo2 = f16x2_splat(lo), hi2 = f16x2_splat(hi);
-#pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            const uint32_t cols = f16_bits_small(2 * e) | (f16_bits_small(2 * e + 1) << 16);
-            uint32_t ge, le;
-            asm("set.ge.u32.f16x2 %0, %1, %2;" : "=r"(ge) : "r"(cols), "r"(lo2));
-            asm("set.le.u32.f16x2 %0, %1, %2;" : "=r"(le) : "r"(cols), "r"(hi2));
-            pw[e] &= ge & le;
-          }
-        }
-        // the row sum: the f16 probabilities the PV MMA takes, each added in
-        // float32
-        float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 64; e += 4) {
-          add_f16x2_f32(s8[0], s8[1], pw[e]);
-          add_f16x2_f32(s8[2], s8[3], pw[e + 1]);
-          add_f16x2_f32(s8[4], s8[5], pw[e + 2]);
-          add_f16x2_f32(s8[6], s8[7], pw[e + 3]);
-        }
-        l = l * alpha + (((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7])));
-        // PV(t-1) read P(t-1) from this tile's P columns and accumulated into
-        // O: it completes before P(t) is stored and O is rescaled (the
-        // exponentials above overlap it)
-        if (t > kb) {
-          ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
+      // One key tile; in long units (mode 0) full_tag says at compile time
+      // whether every row sees all of the tile's keys, so the full tiles
+      // [fb, fe) -- the run in the middle of the range -- loop over code
+      // without the partial tiles' column tests.
+      auto tile = [&](const int t, auto full_tag) -> bool {
+          const int k0 = inf.kbase + t * kBN;
+          PHASE(7);
+          ok = wait(&sh->s_full[w][sc & 1], (sc >> 1) & 1);
+          if (r == 0) EV(3 + w, 0, t);
+          ++sc;
           tc_fence_after();
-        }
-        PHASE(3);
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) {  // this row's P: keys 2c, 2c+1 in column c
-          const uint32_t p8[8] = {pw[8 * q8], pw[8 * q8 + 1], pw[8 * q8 + 2], pw[8 * q8 + 3],
-                                  pw[8 * q8 + 4], pw[8 * q8 + 5], pw[8 * q8 + 6], pw[8 * q8 + 7]};
-          tmem_st8(tP + q8 * 8, p8);
-        }
-        PHASE(4);
-        if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {
-          uint32_t ov[64];
-          tmem_ld64_wait(tO, ov);
-#pragma unroll
-          for (int d = 0; d < kHead; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
-          tmem_st64(tO, ov);
-        }
-        tmem_wait_st();
-        PHASE(5);
-        tc_fence_before();
-        if (named_bar_or(1 + w, 128, !ok)) { ok = false; break; }
-        if (r == 0) mbar_arrive(&sh->p_full[w]);
-        if (r == 0) EV(3 + w, 1, t);
-        PHASE(6);
+          PHASE(0);
+          // the tile's S buffer is free again once every warp has loaded S(t)
+          uint32_t v[128];
+          tmem_ld128_wait(tmem + w * 128 + lane_off, v);
+          tc_fence_before();
+          if (lane == 0) mbar_arrive(&sh->s_read[w]);
+          PHASE(1);
+          // visible keys of this row in this tile form one interval [lo, hi]
+          // of column indices (only partial tiles test columns)
+          bool full;
+          if constexpr (std::is_same_v<decltype(full_tag), bool>)
+            full = kMode != 2 && t >= fb && t < fe;
+          else
+            full = decltype(full_tag)::value;
+          int lo = 0, hi = kBN - 1;
+          if (!full) {
+            if (kCache) {
+              hi = min(kBN - 1, chunk_hi - k0);  // causal at position off + i <= off + L - 1
+            } else {
+              hi = min(kBN - 1, inf.L - 1 - k0);
+              if (kCausal) hi = min(hi, i - k0);
+              if (kWindow >= 0) {
+                lo = max(lo, max(i - kWindow, 0) - k0);  // (a grid may start below key 0)
+                hi = min(hi, i + kWindow - k0);
+              }
+              if (!row_ok) hi = -1;
+            }
+            lo = min(lo, kBN);
+            hi = max(hi, -1);
+          }
+          // row max: eight running maxima, each taking two keys per three-input
+          // max (64 instructions for 128 keys, short dependency chains)
+          float m8[8];
+  #pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = fmaxf(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+  #pragma unroll
+          for (int j = 16; j < kBN; j += 2)
+            m8[(j >> 1) & 7] = fmax3(m8[(j >> 1) & 7], __uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+          float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+          // On a partial tile that maximum also covers masked columns, so it only
+          // bounds the visible one from above: when it cannot move the reference
+          // (the usual case after a row's first tile) the visible maximum cannot
+          // either; otherwise the maximum is taken again over the visible
+          // columns alone (kNone when there are none), tested against a bit word
+          // per 32 columns.
+          if (!full && __any_sync(0xffffffffu, mx > m_ref + kLazy)) {
+            uint32_t vis[kBN / 32];
+  #pragma unroll
+            for (int k = 0; k < kBN / 32; ++k) {
+              const int a = lo - 32 * k, b = hi - 32 * k;  // the interval in this word's bit positions
+              const uint32_t upto_b = b < 0 ? 0u : (2u << min(b, 31)) - 1u;
+              const uint32_t below_a = a <= 0 ? 0u : (a >= 32 ? ~0u : (1u << a) - 1u);
+              vis[k] = upto_b & ~below_a;
+            }
+  #pragma unroll
+            for (int k = 0; k < 8; ++k) m8[k] = kNone;
+  #pragma unroll
+            for (int j = 0; j < kBN; ++j)
+              if ((vis[j >> 5] >> (j & 31)) & 1u) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(v[j]));
+            mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+          }
+          // move the reference max on the first visible keys, or when it is
+          // exceeded by more than kLazy (log2 units)
+          float alpha = 1.f;
+          if (mx > m_ref + kLazy) {
+            if (m_ref != kNone) alpha = fast_exp2(m_ref - mx);
+            m_ref = mx;
+          }
+          PHASE(2);
+          // P = 2^(x - m_ref): the differences in float32 pairs, rounded to f16
+          // pairs (saturating, so no difference becomes infinite), two
+          // exponentials per MUFU operation (P in f16, as the MMA takes it).
+          // All 64 exponent pairs first (independent chains the schedulers can
+          // interleave), then the masked columns set to probability zero.
+          uint64_t mm;
+          asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(m_ref));
+          uint32_t pw[64];
+  #pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            uint64_t xx, d;
+            asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "r"(v[2 * e]), "r"(v[2 * e + 1]));
+            asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(xx), "l"(mm));
+            uint32_t h;
+            asm("{\n\t.reg .f32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tcvt.rn.satfinite.f16x2.f32 %0, hi, lo;\n\t}"
+                : "=r"(h)
+                : "l"(d));
+            asm("ex2.approx.f16x2 %0, %1;" : "=r"(pw[e]) : "r"(h));
+          }
+          if (!full) {
+            // column indices against [lo, hi] as f16 pairs (exact for 0..128):
+            // each half of a comparison is 0xFFFF when true
+            const uint32_t lo2 = f16x2_splat(lo), hi2 = f16x2_splat(hi);
+  #pragma unroll
+            for (int e = 0; e < 64; ++e) {
+              const uint32_t cols = f16_bits_small(2 * e) | (f16_bits_small(2 * e + 1) << 16);
+              uint32_t ge, le;
+              asm("set.ge.u32.f16x2 %0, %1, %2;" : "=r"(ge) : "r"(cols), "r"(lo2));
+              asm("set.le.u32.f16x2 %0, %1, %2;" : "=r"(le) : "r"(cols), "r"(hi2));
+              pw[e] &= ge & le;
+            }
+          }
+          // the row sum: the f16 probabilities the PV MMA takes, each added in
+          // float32
+          float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+          for (int e = 0; e < 64; e += 4) {
+            add_f16x2_f32(s8[0], s8[1], pw[e]);
+            add_f16x2_f32(s8[2], s8[3], pw[e + 1]);
+            add_f16x2_f32(s8[4], s8[5], pw[e + 2]);
+            add_f16x2_f32(s8[6], s8[7], pw[e + 3]);
+          }
+          l = l * alpha + (((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7])));
+          // PV(t-1) read P(t-1) from this tile's P columns and accumulated into
+          // O: it completes before P(t) is stored and O is rescaled (the
+          // exponentials above overlap it)
+          if (t > kb) {
+            ok = ok && wait(&sh->pv_full[w], (pvc++) & 1);
+            tc_fence_after();
+          }
+          PHASE(3);
+  #pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8) {  // this row's P: keys 2c, 2c+1 in column c
+            const uint32_t p8[8] = {pw[8 * q8], pw[8 * q8 + 1], pw[8 * q8 + 2], pw[8 * q8 + 3],
+                                    pw[8 * q8 + 4], pw[8 * q8 + 5], pw[8 * q8 + 6], pw[8 * q8 + 7]};
+            tmem_st8(tP + q8 * 8, p8);
+          }
+          PHASE(4);
+          if (t > kb && __any_sync(0xffffffffu, alpha != 1.f)) {
+            uint32_t ov[64];
+            tmem_ld64_wait(tO, ov);
+  #pragma unroll
+            for (int d = 0; d < kHead; ++d) ov[d] = __float_as_uint(__uint_as_float(ov[d]) * alpha);
+            tmem_st64(tO, ov);
+          }
+          tmem_wait_st();
+          PHASE(5);
+          tc_fence_before();
+          if (named_bar_or(1 + w, 128, !ok)) { ok = false; return false; }
+          if (r == 0) mbar_arrive(&sh->p_full[w]);
+          if (r == 0) EV(3 + w, 1, t);
+          PHASE(6);
+        return true;
+      };
+      bool more = true;
+      if constexpr (kMode == 0) {
+        for (int t = kb; more && t < fb; ++t) more = tile(t, std::false_type{});
+        for (int t = fb; more && t < fe; ++t) more = tile(t, std::true_type{});
+        for (int t = fe; more && t < ke; ++t) more = tile(t, std::false_type{});
+      } else {
+        for (int t = kb; more && t < ke; ++t) more = tile(t, true);
       }
       if (!ok) break;
       ok = wait(&sh->pv_full[w], (pvc++) & 1);
