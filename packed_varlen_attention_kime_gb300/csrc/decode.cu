@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(DecCfg<G>::threads, DecCfg<G>::ctas_per_sm)
       const int s = item.s, g = item.g, P = item.P;
       // this warp: keys 32 gw .. 32 gw + 31 of every chunk of the group; its
       // running (m, l) for row gq and O (rows gq, gq + 8) as 8 n-tiles of dims
-      float m_run = -INFINITY, l_run = 0.f;
+      float m_run = kNone, l_run = 0.f;  // kNone: no key yet (finite, below every logit)
       float oacc[8][4];
 #pragma unroll
       for (int nd = 0; nd < 8; ++nd) oacc[nd][0] = oacc[nd][1] = oacc[nd][2] = oacc[nd][3] = 0.f;
@@ -488,19 +488,19 @@ __global__ void __launch_bounds__(DecCfg<G>::threads, DecCfg<G>::ctas_per_sm)
           mma_bf16(sacc[nt], qa[2], b1[0], b1[1]);
           mma_bf16(sacc[nt], qa[3], b1[2], b1[3]);
         }
-        // row gq: keys kbase + 8 nt + 2 tq (+1); keys past pos[s] are masked
-        float mloc = -INFINITY;
+        // row gq: keys kbase + 8 nt + 2 tq (+1); keys past pos[s] are left
+        // out of the maximum and get probability 0 below (no -inf is formed)
+        float mloc = kNone;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
           const int k0 = kbase + nt * 8 + 2 * tq;
-          if (k0 >= nk) sacc[nt][0] = -INFINITY;
-          if (k0 + 1 >= nk) sacc[nt][1] = -INFINITY;
-          mloc = fmax3(mloc, sacc[nt][0], sacc[nt][1]);
+          if (k0 < nk) mloc = fmaxf(mloc, sacc[nt][0]);
+          if (k0 + 1 < nk) mloc = fmaxf(mloc, sacc[nt][1]);
         }
         mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
         mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
         if (mloc > m_run) {  // the running max grows: rescale l and O
-          const float alpha = fast_exp2(m_run - mloc);  // 0 while m_run is still -inf
+          const float alpha = fast_exp2(m_run - mloc);  // 0 while m_run is still kNone
           l_run *= alpha;
 #pragma unroll
           for (int nd = 0; nd < 8; ++nd) {
@@ -509,14 +509,16 @@ __global__ void __launch_bounds__(DecCfg<G>::threads, DecCfg<G>::ctas_per_sm)
           }
           m_run = mloc;
         }
-        const float m_use = m_run == -INFINITY ? 0.f : m_run;
+        const float m_use = m_run == kNone ? 0.f : m_run;
         // P = 2^(S - m) rounded to bf16 (the row sum takes the rounded values,
         // so the weights and their normalisation agree), as the A operand of
         // P V: k-step kk = n-tiles 2kk (pieces 0) and 2kk + 1 (pieces 2)
         uint32_t pa[2][4];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-          const uint32_t pw = pack_bf16x2(fast_exp2(sacc[nt][0] - m_use), fast_exp2(sacc[nt][1] - m_use));
+          const int k0 = kbase + nt * 8 + 2 * tq;
+          const uint32_t pw = pack_bf16x2(k0 < nk ? fast_exp2(sacc[nt][0] - m_use) : 0.f,
+                                          k0 + 1 < nk ? fast_exp2(sacc[nt][1] - m_use) : 0.f);
           l_run += bf16lo(pw) + bf16hi(pw);
           pa[nt >> 1][(nt & 1) * 2] = pw;
           pa[nt >> 1][(nt & 1) * 2 + 1] = 0u;
@@ -562,13 +564,13 @@ __global__ void __launch_bounds__(DecCfg<G>::threads, DecCfg<G>::ctas_per_sm)
       float* part = partials + ((static_cast<size_t>(s) * kv_heads + g) * max_items * kGrp + pc) * G * kPartialFloats;
       for (int e = gtid; e < G * kHead; e += kGroupThreads) {
         const int hh = e / kHead, d = e % kHead;
-        float M = -INFINITY;
+        float M = kNone;
 #pragma unroll
         for (int wv = 0; wv < 4; ++wv) M = fmaxf(M, red_m[wv * G + hh]);
         float Lsum = 0.f, O = 0.f;
 #pragma unroll
         for (int wv = 0; wv < 4; ++wv) {
-          const float wgt = red_m[wv * G + hh] == -INFINITY ? 0.f : fast_exp2(red_m[wv * G + hh] - M);
+          const float wgt = red_m[wv * G + hh] == kNone ? 0.f : fast_exp2(red_m[wv * G + hh] - M);
           Lsum = fmaf(red_l[wv * G + hh], wgt, Lsum);
           O = fmaf(red_o[(wv * G + hh) * kHead + d], wgt, O);
         }
@@ -602,7 +604,7 @@ __global__ void __launch_bounds__(DecCfg<G>::threads, DecCfg<G>::ctas_per_sm)
           float* hdr = red_o;                      // [G] M, [G] L (this group's buffers)
           float* wts = hdr + 2 * G;                // [block][G] m_c, then weights
           constexpr int kBlock = kMergeBlock;
-          if (gtid < G) hdr[gtid] = -INFINITY;
+          if (gtid < G) hdr[gtid] = kNone;
           for (int c0 = 0; c0 < n_parts; c0 += kBlock) {
             const int nb = min(kBlock, n_parts - c0);
             bar_group(cg);
@@ -624,7 +626,7 @@ __global__ void __launch_bounds__(DecCfg<G>::threads, DecCfg<G>::ctas_per_sm)
             bar_group(cg);
             for (int e = gtid; e < nb * G; e += kGroupThreads) {
               const float mc = __ldcg(all + (c0 * G + e) * kPartialFloats);
-              wts[e] = mc == -INFINITY ? 0.f : fast_exp2(mc - hdr[e % G]);
+              wts[e] = mc == kNone ? 0.f : fast_exp2(mc - hdr[e % G]);
             }
             bar_group(cg);
             if (gtid < G) {

@@ -661,26 +661,37 @@ __global__ void __launch_bounds__(kT3Threads, 1)
         if (ok) tmem_ld32_wait(tS, sv);
         const int hf = cur.hb + k, k0 = hf * kSub + 32 * c;  // this warp's first key
         const bool full = hf >= cur.ffb && hf < cur.ffe;
-        // visible keys of this row among this warp's 32: columns [lo, hi]
-        int lo = 0, hi = 31;
+        // visible keys of this row among this warp's 32: columns [lo, hi],
+        // one bit each in vis
+        uint32_t vis = ~0u;
         if (!full) {
-          hi = min(31, cur.L - 1 - k0);
+          int lo = 0, hi = min(31, cur.L - 1 - k0);
           if (p.causal) hi = min(hi, i - k0);
           if (p.window >= 0) {
             lo = max(0, i - p.window - k0);
             hi = min(hi, i + p.window - k0);
           }
           if (!row_ok) hi = -1;
+          const uint32_t upto_hi = hi < 0 ? 0u : (2u << min(hi, 31)) - 1u;
+          const uint32_t below_lo = lo <= 0 ? 0u : (lo >= 32 ? ~0u : (1u << lo) - 1u);
+          vis = upto_hi & ~below_lo;
         }
-        // masked columns count as kNone (below every logit)
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (!(j >= lo && j <= hi)) sv[j] = __float_as_uint(kNone);
+        // the maximum over the visible columns (kNone when there are none);
+        // masked columns are left out, and get probability 0 below
         float m8[8];
+        if (full) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) m8[q] = fmaxf(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]));
+          for (int q = 0; q < 8; ++q) m8[q] = fmaxf(__uint_as_float(sv[4 * q]), __uint_as_float(sv[4 * q + 1]));
 #pragma unroll
-        for (int q = 0; q < 8; ++q) m8[q] = fmax3(m8[q], __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
+          for (int q = 0; q < 8; ++q)
+            m8[q] = fmax3(m8[q], __uint_as_float(sv[4 * q + 2]), __uint_as_float(sv[4 * q + 3]));
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) m8[q] = kNone;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if ((vis >> j) & 1u) m8[j >> 2] = fmaxf(m8[j >> 2], __uint_as_float(sv[j]));
+        }
         float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         // the row's maximum over both warps' columns
         float* xb = &sh->xch[xc & 1][0][0];
@@ -697,8 +708,9 @@ __global__ void __launch_bounds__(kT3Threads, 1)
           if (m_ref != kNone) alpha = fast_exp2(m_ref - mx);
           m_ref = mx;
         }
-        // P = 2^(S - m_ref); a masked column (kNone) gives 0, also while the
-        // row has no visible key yet (m_ref = kNone: its reference is taken as 0)
+        // P = 2^(S - m_ref) for the visible columns, 0 for the masked ones
+        // (while the row has no visible key yet, m_ref = kNone, its reference
+        // is taken as 0)
         const float mr = m_ref == kNone ? 0.f : m_ref;
         // P-low buffer h mod 2 was last read by PV(h-2)
         if (h >= 2) {
@@ -711,7 +723,8 @@ __global__ void __launch_bounds__(kT3Threads, 1)
           uint32_t ph[16], pl[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float pe = fast_exp2(__uint_as_float(sv[16 * q + e]) - mr), hv = tf32_hi(pe);
+            const float pe = (vis >> (16 * q + e)) & 1u ? fast_exp2(__uint_as_float(sv[16 * q + e]) - mr) : 0.f;
+            const float hv = tf32_hi(pe);
             s4[e & 3] += pe;
             ph[e] = __float_as_uint(hv);
             pl[e] = __float_as_uint(pe - hv);

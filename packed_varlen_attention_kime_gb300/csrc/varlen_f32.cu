@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kChunk = 16;
+static_assert(kChunk <= 32, "one visibility bit per key of a chunk");
 
 __device__ __forceinline__ bool visible(int i, int j, int L, int causal, int window) {
   if (j >= L) return false;
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(kThreads)
     const int kcol = (heads + g) * kHead, vcol = (heads + kv_heads + g) * kHead;
 
     float q[kHead], o[kHead];
-    float m = -INFINITY, l = 0.f;
+    float m = kNone, l = 0.f;  // kNone: no visible key yet (finite, below every logit)
 #pragma unroll
     for (int d = 0; d < kHead; ++d) o[d] = 0.f;
     if (valid) load_rotated(qkv, W, pr.row0 + i, h * kHead, i, cos_t, sin_t, q);
@@ -111,30 +112,34 @@ __global__ void __launch_bounds__(kThreads)
       if (!valid) continue;
       const bool full = kt >= pr.full_begin && kt < pr.full_end;
       for (int c = 0; c < kBN; c += kChunk) {
+        // scores of the visible keys only; masked keys are skipped in the
+        // maximum and get probability 0 (no -inf is formed)
         float sc[kChunk];
-        float cmax = -INFINITY;
+        uint32_t vis = 0;
+        float cmax = kNone;
 #pragma unroll
         for (int jj = 0; jj < kChunk; ++jj) {
           const int j = k0 + c + jj;
+          sc[jj] = 0.f;
           if (full || visible(i, j, pr.L, causal, window)) {
             float acc = 0.f;
 #pragma unroll
             for (int d = 0; d < kHead; ++d) acc = fmaf(q[d], Ks[c + jj][d], acc);
             sc[jj] = acc * scale;
-          } else {
-            sc[jj] = -INFINITY;
+            vis |= 1u << jj;
+            cmax = fmaxf(cmax, sc[jj]);
           }
-          cmax = fmaxf(cmax, sc[jj]);
         }
-        if (cmax == -INFINITY) continue;
+        if (vis == 0) continue;
         const float m_new = fmaxf(m, cmax);
-        const float alpha = expf(m - m_new);
+        const float alpha = expf(m - m_new);  // 0 while m is kNone (l and o are 0 then)
         l *= alpha;
 #pragma unroll
         for (int d = 0; d < kHead; ++d) o[d] *= alpha;
 #pragma unroll
         for (int jj = 0; jj < kChunk; ++jj) {
-          const float p = expf(sc[jj] - m_new);
+          float p = expf(sc[jj] - m_new);
+          if (!((vis >> jj) & 1u)) p = 0.f;
           l += p;
 #pragma unroll
           for (int d = 0; d < kHead; ++d) o[d] = fmaf(p, Vs[c + jj][d], o[d]);
