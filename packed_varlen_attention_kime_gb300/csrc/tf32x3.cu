@@ -196,6 +196,10 @@ struct T3Params {
   int32_t* dev_status;
 };
 
+// kNarrow: a window of at most 64; every 64-key half is then partial for some
+// row of the tile, so every half takes the partial path (the full-half code
+// would only take room).  Same bits.
+template <bool kNarrow>
 __global__ void __launch_bounds__(kT3Threads, 1)
     prefill_3xtf32_kernel(const __grid_constant__ CUtensorMap qkv_map, const T3Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -660,7 +664,7 @@ __global__ void __launch_bounds__(kT3Threads, 1)
         uint32_t sv[32];
         if (ok) tmem_ld32_wait(tS, sv);
         const int hf = cur.hb + k, k0 = hf * kSub + 32 * c;  // this warp's first key
-        const bool full = hf >= cur.ffb && hf < cur.ffe;
+        const bool full = !kNarrow && hf >= cur.ffb && hf < cur.ffe;
         // visible keys of this row among this warp's 32: columns [lo, hi],
         // one bit each in vis
         uint32_t vis = ~0u;
@@ -769,16 +773,18 @@ __global__ void __launch_bounds__(kT3Threads, 1)
 cudaError_t launch_prefill_3xtf32(const CUtensorMap* qkv_map, int heads, int kv_heads, int window, int causal,
                                   float scale, const float* cos_t, const float* sin_t, float* out, void* ws,
                                   int32_t* dev_status, cudaStream_t st) {
-  static int configured[64] = {};
+  static int configured[2][64] = {};
+  const bool narrow = window >= 0 && window <= 64;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if (dev >= 64 || !configured[dev]) {
-    if ((e = cudaFuncSetAttribute(prefill_3xtf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kT3Smem)) !=
-        cudaSuccess)
+  if (dev >= 64 || !configured[narrow][dev]) {
+    const void* fn = narrow ? reinterpret_cast<const void*>(prefill_3xtf32_kernel<true>)
+                            : reinterpret_cast<const void*>(prefill_3xtf32_kernel<false>);
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kT3Smem)) != cudaSuccess)
       return e;
-    if (dev < 64) configured[dev] = 1;
+    if (dev < 64) configured[narrow][dev] = 1;
   }
   T3Params prm;
   prm.heads = heads;
@@ -804,7 +810,8 @@ cudaError_t launch_prefill_3xtf32(const CUtensorMap* qkv_map, int heads, int kv_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_3xtf32_kernel, *qkv_map, prm);
+  return narrow ? cudaLaunchKernelEx(&cfg, prefill_3xtf32_kernel<true>, *qkv_map, prm)
+                : cudaLaunchKernelEx(&cfg, prefill_3xtf32_kernel<false>, *qkv_map, prm);
 }
 
 }  // namespace kime
