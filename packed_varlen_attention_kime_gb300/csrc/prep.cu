@@ -39,6 +39,10 @@ __global__ void __launch_bounds__(32 * kPrepWarps)
                     int heads, int kv_heads, float qmul, const float* __restrict__ cos_t,
                     const float* __restrict__ sin_t, int rope_len, uint16_t* __restrict__ out,
                     int32_t* dev_status) {
+  // The attention kernel after this one may launch as soon as every CTA of
+  // this grid has started: it sets itself up while the last CTAs run and
+  // waits for this grid's results before reading them.
+  griddep_launch_dependents();
   const int j = blockIdx.x * kPrepWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (j >= total) {
     griddep_wait();
