@@ -105,10 +105,7 @@ typedef enum {
  *               and keys rotated once each, queries scaled, all in FP16) and
  *               the attention kernel does no RoPE work: faster, with the same
  *               f16 operands and contract (its row sums add in another
- *               order, so the last bits of the output may differ).  Not for
- *               a window of at most 128 over sequences of mean length 1024
- *               or more: there the kernel that rotates its own tiles is the
- *               faster one and runs whatever the workspace.
+ *               order, so the last bits of the output may differ).
  * BF16 runs on the tensor cores (tcgen05, FP32 accumulate) with f16 operands:
  * rotated keys, scaled rotated queries and values are rounded to f16, so they
  * must lie within its range (|x| <= 65504; beyond, they saturate and

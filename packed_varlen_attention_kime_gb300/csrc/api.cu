@@ -213,13 +213,11 @@ int kime_attn_varlen(const void* qkv, int dtype, const int32_t* cu_seqlens, int 
   CUtensorMap map, cmap, smap, pmap;
   if ((rc = encode_qkv_map(&map, qkv, total_tokens, static_cast<int>(W)))) return rc;
   // With room in the workspace, the rows are prepared once (RoPE and f16) and
-  // the attention kernel does no RoPE work -- except for a narrow window over
-  // long sequences: there each key tile is visited by only a few query tiles,
-  // and rotating it in the attention kernel costs less than the extra pass
-  // over every row (ModernBERT-large local layer, window 64, mean length
-  // 4,836: 0.197 ms against 0.228 ms; at mean length 316 the two tie).
-  const bool narrow_long = window >= 0 && window <= 128 && total_tokens >= 1024LL * n_seqs;
-  const bool prep = !narrow_long && workspace_bytes >= prep_ws_bytes(n_seqs, total_tokens, heads, kv_heads);
+  // the attention kernel does no RoPE work: the faster way for every layer
+  // measured (ModernBERT-large local layer, window 64: 0.169 ms against 0.184
+  // for the kernel that rotates its own tiles; the global layers and short
+  // sequences by more).
+  const bool prep = workspace_bytes >= prep_ws_bytes(n_seqs, total_tokens, heads, kv_heads);
   if (prep) {
     void* rows = static_cast<char*>(workspace) + prep_offset(n_seqs, total_tokens);
     if ((rc = encode_qkv_map(&pmap, rows, total_tokens, static_cast<int>(W)))) return rc;

@@ -341,11 +341,11 @@ def test_host_argument_errors_raise(cuda_lib):
     assert e.shape[0] == 0
 
 
-def test_narrow_window_over_long_sequences_rotates_in_the_attention_kernel(cuda_lib):
-    # A window of at most 128 over sequences of mean length >= 1024 runs the
-    # kernel that rotates its own tiles whatever the workspace: the minimal
-    # and the row-preparing workspaces give the same bits there, and the
-    # result meets the BF16 contract against the oracle (sampled rows).
+def test_narrow_window_over_long_sequences_meets_the_contract_with_either_workspace(cuda_lib):
+    # A window of 64 over long sequences, through the minimal workspace (the
+    # kernel that rotates its own tiles, every tile on its partial path) and
+    # the row-preparing one (prepared rows, every tile on the partial path):
+    # both meet the BF16 contract against the oracle on sampled rows.
     dev = torch.device("cuda")
     lengths, H, Hkv = [1500, 1100, 1300], 4, 2
     cu = cu_from_lengths(lengths)
@@ -357,8 +357,8 @@ def test_narrow_window_over_long_sequences_rotates_in_the_attention_kernel(cuda_
         ws = torch.empty(kime.kime_attn_workspace_bytes(op, n, T, H, Hkv), dtype=torch.uint8, device=dev)
         outs[op] = kime.kime_attn_varlen(qkv, cu.to(dev), mx, H, Hkv, 64, False, 0.125, c, s, workspace=ws)
     torch.cuda.synchronize()
-    assert torch.equal(outs[0], outs[3])
     rows, hs = sample_items(cu.numpy(), H, 200, seed=15)
     ref = run_oracle_varlen(qkv.cpu(), cu, H, Hkv, 64, False, 0.125, 1e4, mx, rows=rows, heads=hs)
-    g = outs[3].float().cpu().reshape(T, H, 64)[torch.from_numpy(rows).long(), torch.from_numpy(hs).long()]
-    check_bf16(g.numpy(), ref, "window 64, long sequences")
+    for op in (0, 3):
+        g = outs[op].float().cpu().reshape(T, H, 64)[torch.from_numpy(rows).long(), torch.from_numpy(hs).long()]
+        check_bf16(g.numpy(), ref, f"window 64, long sequences, op {op}")
