@@ -533,38 +533,39 @@ def oracle_single_core():
 def end_to_end(args, dev, stream, flush, run, world):
     """The headline step end to end through the public API: pinned host qkv ->
     device, both layers, both outputs -> pinned host, every step.  Steps are
-    pipelined as a server would run them, with two sets of device and pinned
+    pipelined as a server would run them, with NB sets of device and pinned
     host buffers: step k+1's copy in overlaps step k's layers and step k-1's
     copy out (the link is full duplex), on three streams ordered by events; a
-    buffer set is refilled only after the step two back has finished with it.
+    buffer set is refilled only after the step NB back has finished with it.
     Each step still copies its own inputs in and its results out.  Timed over
     K consecutive steps, the first copy in and the last copy out included."""
     c = run.case
     h_qkv = c.qkv.cpu().pin_memory()
     h_cu = c.cu_seqlens.cpu().to(torch.int32).pin_memory()
     mx = max(c.lengths)
-    d_qkv = [torch.empty_like(c.qkv) for _ in range(2)]
-    d_cu = [torch.empty_like(h_cu, device=dev) for _ in range(2)]
-    d_out = [[torch.empty_like(o) for o in run.outs] for _ in range(2)]
-    h_out = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in run.outs] for _ in range(2)]
+    NB = args.e2e_buffers
+    d_qkv = [torch.empty_like(c.qkv) for _ in range(NB)]
+    d_cu = [torch.empty_like(h_cu, device=dev) for _ in range(NB)]
+    d_out = [[torch.empty_like(o) for o in run.outs] for _ in range(NB)]
+    h_out = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in run.outs] for _ in range(NB)]
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_cmp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(NB)]
+    ev_cmp = [torch.cuda.Event() for _ in range(NB)]
+    ev_out = [torch.cuda.Event() for _ in range(NB)]
     status = dev_status(dev)
 
     def enqueue(k):
-        b = k & 1
+        b = k % NB
         with torch.cuda.stream(s_in):
-            if k >= 2:
-                s_in.wait_event(ev_cmp[b])  # step k-2's layers have read this input buffer
+            if k >= NB:
+                s_in.wait_event(ev_cmp[b])  # step k-NB's layers have read this input buffer
             d_qkv[b].copy_(h_qkv, non_blocking=True)
             d_cu[b].copy_(h_cu, non_blocking=True)
             ev_in[b].record(s_in)
         with torch.cuda.stream(s_cmp):
             s_cmp.wait_event(ev_in[b])
-            if k >= 2:
-                s_cmp.wait_event(ev_out[b])  # step k-2's outputs have left this buffer
+            if k >= NB:
+                s_cmp.wait_event(ev_out[b])  # step k-NB's outputs have left this buffer
             for li, lay in enumerate(c.layers):
                 cs, sn = run.tables[lay.theta]
                 run.kime.kime_attn_varlen(d_qkv[b], d_cu[b], mx, c.heads, c.kv_heads, lay.window, lay.causal,
@@ -594,11 +595,11 @@ def end_to_end(args, dev, stream, flush, run, world):
     run_steps(4)  # warm-up (first-call set-up, pinned pages touched)
     n = max(10, args.steps)
     e_ms = max_over_ranks(run_steps(n), dev if world > 1 else None) / n
-    # the pipelined steps give the whole batch's bits (both buffer sets)
+    # the pipelined steps give the whole batch's bits (every buffer set)
     for k in range(len(c.layers)):
         run.layer(k)
     torch.cuda.synchronize()
-    for b in range(2):
+    for b in range(NB):
         if not all(torch.equal(x, y) for x, y in zip(d_out[b], run.outs)) or \
                 not all(torch.equal(h, o.cpu()) for h, o in zip(h_out[b], run.outs)):
             raise RuntimeError("pipelined end-to-end outputs differ from the whole-batch calls")
@@ -606,7 +607,7 @@ def end_to_end(args, dev, stream, flush, run, world):
             "h2d_bytes_per_step": h_qkv.numel() * 2 + h_cu.numel() * 4,
             "d2h_bytes_per_step": sum(o.numel() * 2 for o in run.outs), "ms_per_step": round(e_ms, 4),
             "pipeline": f"{n} consecutive steps timed together; step k+1's copy in overlaps step k's two layer "
-                        "calls and step k-1's copy out (two buffer sets, three streams); first copy in and last "
+                        f"calls and step k-1's copy out ({NB} buffer sets, three streams); first copy in and last "
                         f"copy out included; no L2 flush between steps: each step's input "
                         f"({h_qkv.numel() * 2 / 1e6:.0f} MB) is larger than L2"}
 
@@ -621,6 +622,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (e2e null): profiling runs")
+    ap.add_argument("--e2e-buffers", type=int, default=2,
+                    help="device and pinned host buffer sets the end-to-end steps rotate through")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-soak", action="store_true", help="skip the 1 s load before the timed steps")
     ap.add_argument("--only", default=None,
