@@ -137,6 +137,16 @@ __device__ __forceinline__ void add_f16x2_f32(float& a0, float& a1, uint32_t pai
       : "r"(pair));
 }
 
+// the same sums as add_f16x2_f32 (bit for bit): both halves widened, then one
+// packed float32 pair addition
+__device__ __forceinline__ void add_f16x2_f32x2(float& a0, float& a1, uint32_t pair) {
+  asm("{\n\t.reg .f16 l, h;\n\t.reg .f32 fl, fh;\n\t.reg .b64 x, acc;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.f32.f16 fl, l;\n\tcvt.f32.f16 fh, h;\n\tmov.b64 x, {fl, fh};\n\tmov.b64 acc, {%0, %1};\n\t"
+      "add.rn.f32x2 acc, acc, x;\n\tmov.b64 {%0, %1}, acc;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(pair));
+}
+
 // f16 bit pattern of an integer 0..2047 (exact), at compile time
 __host__ __device__ constexpr uint32_t f16_bits_small(int n) {
   int e = 0;

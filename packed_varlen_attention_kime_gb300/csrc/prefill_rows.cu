@@ -491,12 +491,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // the row sum of this half: the f16 probabilities the PV MMA takes,
-          // each added in float32
+          // each added in float32.  Long units add each widened pair with one
+          // packed float32 addition (the same sums, one instruction fewer per
+          // pair; faster there, slower on the short-unit instantiations)
           float s4[4] = {0.f, 0.f, 0.f, 0.f};
   #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            add_f16x2_f32(s4[0], s4[1], pw[e]);
-            add_f16x2_f32(s4[2], s4[3], pw[e + 1]);
+            if constexpr (kMode == 0) {
+              add_f16x2_f32x2(s4[0], s4[1], pw[e]);
+              add_f16x2_f32x2(s4[2], s4[3], pw[e + 1]);
+            } else {
+              add_f16x2_f32(s4[0], s4[1], pw[e]);
+              add_f16x2_f32(s4[2], s4[3], pw[e + 1]);
+            }
           }
           l = l * alpha + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
           // PV(t-1) read P(t-1) and accumulated into O: it completes before
