@@ -295,8 +295,8 @@ class ChunkRun:
         cs, sn = kime.kime_rope_tables(c.theta, c.cap)
         self.cs, self.sn = cs.to(dev), sn.to(dev)
         self.out = torch.empty((c.total, c.heads * 64), dtype=torch.bfloat16, device=dev)
-        self.ws = torch.empty(kime.kime_attn_workspace_bytes(2, len(c.lengths), c.total), dtype=torch.uint8,
-                              device=dev)
+        self.ws = torch.empty(kime.kime_attn_workspace_bytes(5, len(c.lengths), c.total, c.heads, c.kv_heads, c.cap),
+                              dtype=torch.uint8, device=dev)
         L = np.array(c.lengths, np.int64)
         P = c.pos.numpy().astype(np.int64)
         keys = int((P + L).sum())                       # cache rows each kv head's prefix spans

@@ -311,7 +311,9 @@ def _chunk(fn, qkv, cu_seqlens, pos, max_seqlen, heads, kv_heads, k_cache, v_cac
     cap = k_cache.shape[2]
     if out is None:
         out = torch.empty((T, heads * 64), dtype=torch.bfloat16, device=qkv.device)
-    need = kime_attn_workspace_bytes(2, n, T)
+    # room for the prepared rows (op 5): the faster path; any workspace of at
+    # least kime_attn_workspace_bytes(2, ...) bytes is accepted
+    need = kime_attn_workspace_bytes(5, n, T, heads, kv_heads, cap)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=qkv.device)
     rc = getattr(lib, fn)(_p(qkv), _p(cu_seqlens), _p(pos), n, T, int(max_seqlen), heads, kv_heads, 64, cap,

@@ -133,6 +133,21 @@ size_t prep_ws_bytes(int n_seqs, int total, int heads, int kv_heads) {
   return prep_offset(n_seqs, total) + static_cast<size_t>(total) * kime::kHead * (heads + 2 * kv_heads) * 2;
 }
 
+// Workspace of the chunked prefill over prepared rows (launch_chunk_prep):
+// the scheduler's lists, then at 1 KB boundaries the chunk's prepared query
+// rows [total, heads*64] f16 and the widened cache rows [n_seqs * kv_heads *
+// cap_pad, 128] f16, cap_pad = cap rounded up to whole 128-key tiles (so no
+// key tile of one kv head reaches into the next).
+int cap_pad_for(int cap) { return (cap + kime::kBN - 1) / kime::kBN * kime::kBN; }
+size_t chunk_kv16_offset(int n_seqs, int total, int heads) {
+  return (prep_offset(n_seqs, total) + static_cast<size_t>(total) * kime::kHead * heads * 2 + 1023) &
+         ~static_cast<size_t>(1023);
+}
+size_t chunk_prep_ws_bytes(int n_seqs, int total, int heads, int kv_heads, int cap) {
+  return chunk_kv16_offset(n_seqs, total, heads) +
+         static_cast<size_t>(n_seqs) * kv_heads * cap_pad_for(cap) * 2 * kime::kHead * 2;
+}
+
 bool heads_ok(int heads, int kv_heads, int head_dim) {
   return head_dim == kime::kHead && heads > 0 && kv_heads > 0 && heads % kv_heads == 0;
 }
@@ -164,6 +179,10 @@ size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads
   if (op == 4) {  // the 3xTF32 path needs no more scratch than op 0
     if (total_tokens < 0 || !heads_ok(heads, kv_heads, kime::kHead)) return 0;
     return varlen_ws_bytes(n_seqs, total_tokens);
+  }
+  if (op == 5) {  // chunked prefill over prepared rows
+    if (total_tokens < 0 || !heads_ok(heads, kv_heads, kime::kHead) || cap <= 0 || cap > (1 << 30)) return 0;
+    return chunk_prep_ws_bytes(n_seqs, total_tokens, heads, kv_heads, cap);
   }
   return 0;
 }
@@ -328,11 +347,30 @@ int chunk_args_ok(const void* qkv, const int32_t* cu, const int32_t* pos, int n_
 int chunk_attend(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total, int max_seqlen,
                  int heads, int kv_heads, int cap, float scale, const float* rope_cos, const float* rope_sin,
                  int rope_len, const void* k_cache, const void* v_cache, void* out, void* workspace,
-                 int32_t* dev_status, cudaStream_t st) {
+                 size_t workspace_bytes, int32_t* dev_status, cudaStream_t st) {
   const int max_pairs = kime::max_pairs_for(n_seqs, total);
   int rc = cuda_status(kime::launch_schedule(cu, pos, n_seqs, total, max_seqlen, 1, -1, cap, rope_len, workspace,
                                              max_pairs, dev_status, st));
   if (rc) return rc;
+  // With room in the workspace the chunk's queries are prepared and the
+  // visible cache rows widened to f16 once, and the attention kernel over
+  // prepared rows takes them (SmolLM2 chunked prefill: see the measurements
+  // of the chunk step); else the kernel that converts its own tiles.
+  const int cap_pad = cap_pad_for(cap);
+  if (workspace_bytes >= chunk_prep_ws_bytes(n_seqs, total, heads, kv_heads, cap) &&
+      static_cast<long long>(n_seqs) * kv_heads * cap_pad < (1LL << 31)) {
+    void* q16 = static_cast<char*>(workspace) + prep_offset(n_seqs, total);
+    void* kv16 = static_cast<char*>(workspace) + chunk_kv16_offset(n_seqs, total, heads);
+    CUtensorMap qmap, kvmap;
+    if ((rc = encode_qkv_map(&qmap, q16, total, 64 * heads))) return rc;
+    if ((rc = encode_qkv_map(&kvmap, kv16, n_seqs * kv_heads * cap_pad, 2 * kime::kHead))) return rc;
+    if ((rc = cuda_status(kime::launch_chunk_prep(qkv, cu, pos, n_seqs, total, heads, kv_heads, cap, cap_pad, scale,
+                                                  rope_cos, rope_sin, rope_len, k_cache, v_cache, q16, kv16,
+                                                  dev_status, st))))
+      return rc;
+    return cuda_status(kime::launch_prefill_rows_chunk(&qmap, &kvmap, heads, kv_heads, cap_pad, out, workspace,
+                                                       max_pairs, dev_status, st));
+  }
   const int W = 64 * (heads + 2 * kv_heads), rows = n_seqs * kv_heads * cap;
   CUtensorMap qmap, kmap, vmap;
   if ((rc = encode_qkv_map(&qmap, qkv, total, W))) return rc;
@@ -361,7 +399,7 @@ int chunk_common(const void* qkv, const int32_t* cu, const int32_t* pos, int n_s
     if (rc) return rc;
   }
   return chunk_attend(qkv, cu, pos, n_seqs, total, max_seqlen, heads, kv_heads, cap, scale, rope_cos, rope_sin,
-                      rope_len, k_cache, v_cache, out, workspace, dev_status, st);
+                      rope_len, k_cache, v_cache, out, workspace, workspace_bytes, dev_status, st);
 }
 
 int decode_common(const void* qkv_new, const int32_t* pos, int n_seqs, int heads, int kv_heads, int head_dim, int cap,

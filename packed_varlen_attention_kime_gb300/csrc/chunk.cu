@@ -8,8 +8,10 @@
 // token at position pos[s] + i: its k heads, rotated there (float32, one
 // rounding per operation, then bf16 round-to-nearest-even), and its v heads go
 // to cache row pos[s] + i of caches [n_seqs, kv_heads, cap, 64].  The
-// attention half is the tensor-core prefill kernel reading its keys and values
-// from the cache (prefill_tc.cu, kCache).
+// attention half is a tensor-core prefill kernel: with room in the workspace
+// it runs over rows prepared once by chunk_prep_kernel below
+// (prefill_rows.cu, chunk mode), else it reads its keys and values from the
+// cache itself (prefill_tc.cu, kCache).
 //
 // One warp per token row; lanes stride over the row's kv heads (rotation
 // pairs, then v elements).  A sequence whose block would leave
@@ -80,7 +82,170 @@ __global__ void __launch_bounds__(32 * kRowsPerCta)
   }
 }
 
+// The rows of the chunk attention over prepared rows.  Blocks [0, q_blocks)
+// take the chunk rows, one warp per row: its query heads rotated at position
+// pos[s] + i with the float32 tables, y_t = fma(x_t, c, -(x_{t+32} s)) and
+// y_{t+32} = fma(x_{t+32}, c, x_t s), times scale * log2(e), each rounded once
+// to f16 (the arithmetic of the attention kernels that rotate their own
+// tiles); lane q of a round holds 16-byte chunk q of the row's queries and
+// swaps it with lane q ^ 4, which holds the other halves of its pairs.  Every
+// other block takes one 128-key tile of one (sequence, kv head): cache rows
+// below pos[s] + L widened to f16 (K in columns 0..63, V in 64..127; cached
+// keys are rotated already), the rest of the tile zero, so the masked keys
+// the attention kernel visits are finite; tiles wholly past pos[s] + L are
+// never read and are skipped.  Sequences with positions outside [0, min(cap,
+// rope_len)) are skipped (the scheduler reports them and lists none of their
+// tiles).  An operand beyond the f16 range saturates and sets KIME_DEV_RANGE.
+constexpr int kChunkPrepWarps = 4;
+
+__device__ __forceinline__ float absmax_bf16x8(const uint4& x) {
+  return fmax3(fmax3(fabsf(bf16lo(x.x)), fabsf(bf16hi(x.x)), fabsf(bf16lo(x.y))),
+               fmax3(fabsf(bf16hi(x.y)), fabsf(bf16lo(x.z)), fabsf(bf16hi(x.z))),
+               fmaxf(fabsf(bf16lo(x.w)), fabsf(bf16hi(x.w))));
+}
+
+__device__ __forceinline__ uint4 widen_bf16x8(const uint4& x) {
+  return make_uint4(pack_f16x2(bf16lo(x.x), bf16hi(x.x)), pack_f16x2(bf16lo(x.y), bf16hi(x.y)),
+                    pack_f16x2(bf16lo(x.z), bf16hi(x.z)), pack_f16x2(bf16lo(x.w), bf16hi(x.w)));
+}
+
+__global__ void __launch_bounds__(32 * kChunkPrepWarps)
+    chunk_prep_kernel(const uint16_t* __restrict__ qkv, const int32_t* __restrict__ cu,
+                      const int32_t* __restrict__ pos, int n_seqs, int total, int heads, int kv_heads, int cap,
+                      int cap_pad, float qmul, const float* __restrict__ cos_t, const float* __restrict__ sin_t,
+                      int rope_len, const uint16_t* __restrict__ k_cache, const uint16_t* __restrict__ v_cache,
+                      uint16_t* __restrict__ q16, uint16_t* __restrict__ kv16, int q_blocks, int32_t* dev_status) {
+  // the attention kernel may launch once every CTA of this grid has started;
+  // it waits for this grid's results before reading them
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float big = 0.f;  // largest magnitude rounded to f16 by this lane
+  if (static_cast<int>(blockIdx.x) < q_blocks) {
+    const int j = blockIdx.x * kChunkPrepWarps + warp;
+    if (j < total) {
+      int lo = 0, hi = n_seqs - 1;  // the sequence owning row j: the largest s with cu[s] <= j
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(cu + mid) <= j) lo = mid;
+        else hi = mid - 1;
+      }
+      const int a0 = __ldg(cu + lo), L = __ldg(cu + lo + 1) - a0, i = j - a0, off = __ldg(pos + lo);
+      const long long end = static_cast<long long>(off) + L;
+      if (i >= 0 && i < L && off >= 0 && end <= cap && end <= rope_len) {
+        const int P = off + i;
+        const size_t W = static_cast<size_t>(kHead) * (heads + 2 * kv_heads);
+        const uint4* src = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(j) * W);
+        uint4* dst = reinterpret_cast<uint4*>(q16 + static_cast<size_t>(j) * heads * kHead);
+        const float* crow = cos_t + static_cast<size_t>(P) * kHalf;
+        const float* srow = sin_t + static_cast<size_t>(P) * kHalf;
+        const int nq = heads * (kHead / 8);  // 16-byte chunks of the row's queries (a multiple of 8)
+        for (int q0 = 0; q0 < nq; q0 += 32) {
+          const int q = q0 + lane;
+          const bool in = q < nq;  // chunks q and q ^ 4 are both in range or both out of it
+          const uint4 x = in ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+          uint4 y;
+          y.x = __shfl_xor_sync(0xffffffffu, x.x, 4);
+          y.y = __shfl_xor_sync(0xffffffffu, x.y, 4);
+          y.z = __shfl_xor_sync(0xffffffffu, x.z, 4);
+          y.w = __shfl_xor_sync(0xffffffffu, x.w, 4);
+          if (!in) continue;
+          const int a = q & 7;         // chunk within the head: 0..3 low half, 4..7 high half
+          const int t0 = (a & 3) * 8;  // pair index of the chunk's first element
+          const float4 c0 = __ldg(reinterpret_cast<const float4*>(crow + t0));
+          const float4 c1 = __ldg(reinterpret_cast<const float4*>(crow + t0 + 4));
+          const float4 s0 = __ldg(reinterpret_cast<const float4*>(srow + t0));
+          const float4 s1 = __ldg(reinterpret_cast<const float4*>(srow + t0 + 4));
+          const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+          const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+          uint32_t ow[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = bf16lo(xw[e]), x1 = bf16hi(xw[e]), p0 = bf16lo(yw[e]), p1 = bf16hi(yw[e]);
+            float r0, r1;
+            if (a < 4) {  // y_t = x_t c - x_{t+32} s
+              r0 = __fmaf_rn(x0, cc[2 * e], -__fmul_rn(p0, ss[2 * e]));
+              r1 = __fmaf_rn(x1, cc[2 * e + 1], -__fmul_rn(p1, ss[2 * e + 1]));
+            } else {      // y_{t+32} = x_{t+32} c + x_t s
+              r0 = __fmaf_rn(x0, cc[2 * e], __fmul_rn(p0, ss[2 * e]));
+              r1 = __fmaf_rn(x1, cc[2 * e + 1], __fmul_rn(p1, ss[2 * e + 1]));
+            }
+            big = fmax3(big, fabsf(r0 * qmul), fabsf(r1 * qmul));
+            ow[e] = pack_f16x2(r0 * qmul, r1 * qmul);
+          }
+          dst[q] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+      }
+    }
+  } else {
+    const int tiles = cap_pad / kBN;
+    const int b = static_cast<int>(blockIdx.x) - q_blocks, sg = b / tiles, key0 = (b - sg * tiles) * kBN;
+    const int s = sg / kv_heads;
+    const int off = __ldg(pos + s), L = __ldg(cu + s + 1) - __ldg(cu + s);
+    const long long end = static_cast<long long>(off) + L;
+    if (off >= 0 && L >= 0 && end <= cap && end <= rope_len && key0 < end) {
+      const int Lk = static_cast<int>(end);
+      const size_t crow0 = static_cast<size_t>(sg) * cap;      // cache row of key 0
+      const size_t wrow0 = static_cast<size_t>(sg) * cap_pad;  // widened row of key 0
+      // warp w takes keys key0 + 32 w .. + 31, four keys a round, eight lanes
+      // a key (16 bytes of K and of V each); every load before any store
+      const int kr = lane >> 3, ch = lane & 7;
+      uint4 kx[8], vx[8];
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int key = key0 + warp * 32 + it * 4 + kr;
+        kx[it] = vx[it] = make_uint4(0u, 0u, 0u, 0u);
+        if (key < Lk) {
+          kx[it] = __ldg(reinterpret_cast<const uint4*>(k_cache + (crow0 + key) * kHead) + ch);
+          vx[it] = __ldg(reinterpret_cast<const uint4*>(v_cache + (crow0 + key) * kHead) + ch);
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int key = key0 + warp * 32 + it * 4 + kr;
+        uint4* d = reinterpret_cast<uint4*>(kv16 + (wrow0 + key) * (2 * kHead));
+        if (key < Lk) {
+          big = fmax3(big, absmax_bf16x8(kx[it]), absmax_bf16x8(vx[it]));
+          d[ch] = widen_bf16x8(kx[it]);
+          d[8 + ch] = widen_bf16x8(vx[it]);
+        } else {
+          d[ch] = make_uint4(0u, 0u, 0u, 0u);
+          d[8 + ch] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
+  }
+  if (__any_sync(0xffffffffu, big > kF16Max) && lane == 0) report(dev_status, ST_RANGE);
+  // this pass runs beside the scheduler (it reads none of its output); it
+  // ends only after the scheduler has, so the attention kernel, which waits
+  // for this pass, also finds the scheduler's lists complete
+  griddep_wait();
+}
+
 }  // namespace
+
+cudaError_t launch_chunk_prep(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total, int heads,
+                              int kv_heads, int cap, int cap_pad, float scale, const float* cos_t, const float* sin_t,
+                              int rope_len, const void* k_cache, const void* v_cache, void* q16, void* kv16,
+                              int32_t* dev_status, cudaStream_t st) {
+  const int q_blocks = (total + kChunkPrepWarps - 1) / kChunkPrepWarps;
+  const long long kv_blocks = static_cast<long long>(n_seqs) * kv_heads * (cap_pad / kBN);
+  if (q_blocks + kv_blocks >= (1LL << 31)) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(q_blocks + kv_blocks));
+  cfg.blockDim = dim3(32 * kChunkPrepWarps);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float qmul = scale * 1.4426950408889634f;
+  return cudaLaunchKernelEx(&cfg, chunk_prep_kernel, static_cast<const uint16_t*>(qkv), cu, pos, n_seqs, total,
+                            heads, kv_heads, cap, cap_pad, qmul, cos_t, sin_t, rope_len,
+                            static_cast<const uint16_t*>(k_cache), static_cast<const uint16_t*>(v_cache),
+                            static_cast<uint16_t*>(q16), static_cast<uint16_t*>(kv16), q_blocks, dev_status);
+}
 
 cudaError_t launch_kv_append_varlen(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total,
                                     int heads, int kv_heads, int cap, const float* cos_t, const float* sin_t,

@@ -111,6 +111,24 @@ cudaError_t launch_prefill_tc(const CUtensorMap* qkv_map, const CUtensorMap* k_m
 cudaError_t launch_prefill_rows(const CUtensorMap* rows_map, int heads, int kv_heads, int window, int causal,
                                 void* out, void* ws, int max_pairs, int short_seqs, int32_t* dev_status,
                                 cudaStream_t st);
+// Chunks attending the cache over prepared rows (prefill_rows.cu, the same
+// kernel): q_map addresses the chunk's prepared query rows ([total, heads*64]
+// f16), kv_map the widened cache rows ([n_seqs * kv_heads * cap_pad, 128]
+// f16: K in columns 0..63, V in 64..127), both with boxes of 128 rows x 64
+// columns and 128-byte swizzle; the work list is the chunk scheduler's in ws.
+cudaError_t launch_prefill_rows_chunk(const CUtensorMap* q_map, const CUtensorMap* kv_map, int heads, int kv_heads,
+                                      int cap_pad, void* out, void* ws, int max_pairs, int32_t* dev_status,
+                                      cudaStream_t st);
+// The rows launch_prefill_rows_chunk reads (chunk.cu): the chunk's query heads
+// rotated at positions pos[s] + i, times scale * log2(e), rounded once to f16
+// (q16 [total, heads*64]), and cache rows 0..pos[s] + L_s - 1 of every kv head
+// widened to f16 (kv16 as above), zero rows after them to the end of their
+// 128-row tile.  Launched with programmatic stream serialization after the
+// scheduler, whose lists it does not read; it ends after the scheduler has.
+cudaError_t launch_chunk_prep(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total, int heads,
+                              int kv_heads, int cap, int cap_pad, float scale, const float* cos_t, const float* sin_t,
+                              int rope_len, const void* k_cache, const void* v_cache, void* q16, void* kv16,
+                              int32_t* dev_status, cudaStream_t st);
 // The QKV projection qkv = x W^T (proj.cu): x_map over x [T, hidden] bf16
 // (boxes of 64 columns x 128 rows), w_map over W [64 (heads + 2 kv_heads),
 // hidden] bf16 (boxes of 64 columns x 192 rows), both with 128-byte swizzle;

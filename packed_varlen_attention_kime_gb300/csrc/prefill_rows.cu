@@ -2,14 +2,19 @@
 // cores over prepared qkv rows (prep.cu: queries rotated and multiplied by
 // scale * log2(e), keys rotated, both rounded once to f16, values widened to
 // f16, all in the qkv layout).  This is the kernel of kime_attn_varlen for
-// BF16 qkv when the workspace holds the prepared rows.
+// BF16 qkv when the workspace holds the prepared rows, and of the chunked
+// prefill (kime_attn_chunk) when it holds the chunk's prepared query rows and
+// the cache rows widened to f16 (chunk.cu: chunk_prep_kernel).
 //
 // Semantics (per sequence s, head h, local query i of a length-L sequence):
 // out = softmax over visible keys j of scale * <rope(q_i, i), rope(k_j, j)>,
 // times v_j.  q is head h of the row; k, v are kv head h / (heads/kv_heads)
 // (ffai-argus 0.7.3 src/text.rs, TextTower::block GQA fold).  Key j is
 // visible when j < L, j <= i if causal, |i - j| <= window if window >= 0
-// (kime-cuda 0.0.3 src/plan.rs, Op::Attention: window None = -1).  Masked keys
+// (kime-cuda 0.0.3 src/plan.rs, Op::Attention: window None = -1).  For a
+// chunk the query row i of sequence s sits at position pos[s] + i and sees
+// cache keys 0..pos[s] + i (ffai-argus src/text.rs, CausalSoftmax with offset
+// index_pos).  Masked keys
 // are left out of the row maximum and get probability zero; no -inf is
 // formed (ffai-argus src/text.rs, module doc and CausalSoftmax: deleting the
 // mask is bit-identical to adding -inf).
@@ -97,8 +102,9 @@ __device__ __forceinline__ void regs_inc() {
 // 128-aligned grid (a 128-row query tile with window 64 then sees 2 key
 // tiles, not 3); keys below 0 on such a grid are masked, and their rows
 // (another sequence's, or the TMA fill before row 0) never reach the output.
+// off: the position of the unit's query row 0 (pos[s] for a chunk, else 0).
 struct UnitInfo {
-  int32_t u, s, qt0, nt, kb, ke, row0, L, kbase;
+  int32_t u, s, qt0, nt, kb, ke, row0, L, kbase, off;
 };
 
 struct Shared {
@@ -118,6 +124,7 @@ static_assert(sizeof(Shared) <= 1024, "barrier block");
 
 struct Params {
   int heads, kv_heads, window, causal;
+  int cap_pad;  // chunks: rows per (sequence, kv head) of the widened cache rows
   __nv_bfloat16* out;
   WsHeader* hdr;
   const Duo* duos;
@@ -135,11 +142,18 @@ __device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
-// Query tile w's key-tile ranges in a unit, on the unit's (possibly shifted) grid.
+// Query tile w's key-tile ranges in a unit, on the unit's (possibly shifted)
+// grid; a chunk's queries sit at positions off + row and see keys 0..off + L - 1.
+template <int kMode>
 __device__ __forceinline__ void unit_ranges(const UnitInfo& inf, int w, int causal, int window, int& kb, int& ke,
                                             int& fb, int& fe) {
   kb = ke = fb = fe = 0;
-  if (w < inf.nt) tile_ranges(inf.L, inf.L - inf.kbase, -inf.kbase, inf.qt0 + w, causal, window, kb, ke, fb, fe);
+  if (w < inf.nt) {
+    if constexpr (kMode == 3)
+      tile_ranges(inf.L, inf.off + inf.L, inf.off, inf.qt0 + w, 1, -1, kb, ke, fb, fe);
+    else
+      tile_ranges(inf.L, inf.L - inf.kbase, -inf.kbase, inf.qt0 + w, causal, window, kb, ke, fb, fe);
+  }
 }
 
 // kMode (same bits in every mode):
@@ -151,10 +165,15 @@ __device__ __forceinline__ void unit_ranges(const UnitInfo& inf, int w, int caus
 //      chunks among groups of four lanes and every store writes 64
 //      contiguous bytes of eight rows; one loop tests each tile;
 //   2  a window of at most 128: as 1, with every key tile on the partial path
-//      (no 128-key tile is then seen whole by every row).
+//      (no 128-key tile is then seen whole by every row);
+//   3  chunks against the cache: as 0, with the query tiles from rows_map (the
+//      chunk's prepared query rows, [total, heads * 64]) and the K/V tiles from
+//      kv_map (the widened cache rows: row (s * kv_heads + g) * cap_pad + key,
+//      K in columns 0..63, V in 64..127); causal at positions off + row.
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_rows_kernel(const __grid_constant__ CUtensorMap rows_map, const Params p) {
+    prefill_rows_kernel(const __grid_constant__ CUtensorMap rows_map, const __grid_constant__ CUtensorMap kv_map,
+                        const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Shared* sh = reinterpret_cast<Shared*>(smem + Layout::bar);
@@ -163,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     tma_prefetch_map(&rows_map);
+    if constexpr (kMode == 3) tma_prefetch_map(&kv_map);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh->unit_full[i], 1);
       mbar_init(&sh->unit_empty[i], 4);  // tile A, tile B, both issuers
@@ -221,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const Duo d = p.duos[u / p.heads];
           inf.s = d.s; inf.qt0 = d.qt0; inf.nt = d.nt; inf.kb = d.kb; inf.ke = d.ke; inf.row0 = d.row0; inf.L = d.L;
           inf.kbase = 0;
-          if (window >= 0) {
+          inf.off = kMode == 3 ? d.off : 0;
+          if (kMode != 3 && window >= 0) {
             // the grid from the unit's first visible key when that means fewer tile visits
             const int kbase = d.qt0 * kBM - window;
             int kb, ke, fb, fe, kb2 = 0, ke2 = 0, akb, ake, akb2 = 0, ake2 = 0;
@@ -256,8 +277,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait(&sh->kv_empty[st], ((c / kStages) & 1) ^ 1)) { ok = false; break; }
           const int k0 = inf.kbase + t * kBN;  // the tile's first key
           mbar_arrive_expect_tx(&sh->kv_full[st], 2 * kTile);
-          tma_load_2d(smem + Layout::k + st * kTile, &rows_map, &sh->kv_full[st], kx, inf.row0 + k0);
-          tma_load_2d(smem + Layout::v + st * kTile, &rows_map, &sh->kv_full[st], vx, inf.row0 + k0);
+          if constexpr (kMode == 3) {
+            const int kvrow = (inf.s * p.kv_heads + g) * p.cap_pad + k0;  // widened cache row of the tile's key 0
+            tma_load_2d(smem + Layout::k + st * kTile, &kv_map, &sh->kv_full[st], 0, kvrow);
+            tma_load_2d(smem + Layout::v + st * kTile, &kv_map, &sh->kv_full[st], kHead, kvrow);
+          } else {
+            tma_load_2d(smem + Layout::k + st * kTile, &rows_map, &sh->kv_full[st], kx, inf.row0 + k0);
+            tma_load_2d(smem + Layout::v + st * kTile, &rows_map, &sh->kv_full[st], vx, inf.row0 + k0);
+          }
         }
         if (!ok) break;
       }
@@ -284,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const UnitInfo inf = sh->info[slot];
         if (inf.u < 0) break;
         int kb, ke, fb, fe;  // this tile's key tiles; none when the unit has no tile B
-        unit_ranges(inf, w, causal, window, kb, ke, fb, fe);
+        unit_ranges<kMode>(inf, w, causal, window, kb, ke, fb, fe);
         const uint32_t aq = sbase + Layout::q + (slot * 2 + w) * kTile;
         bool ok = wait(&sh->q_full[slot], (n >> 1) & 1);
         // S for the key tile that is number cc of the K/V ring: once that
@@ -370,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = (inf.qt0 + w) * kBM + r;
       const bool row_ok = i < inf.L;
       int kb, ke, fb, fe;
-      unit_ranges(inf, w, causal, window, kb, ke, fb, fe);
+      unit_ranges<kMode>(inf, w, causal, window, kb, ke, fb, fe);
 
       // Online softmax with a lazily moved reference max m_ref: P = 2^(S -
       // m_ref), O (accumulated by the PV MMAs) and the row sum l stay relative
@@ -402,11 +429,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           int lo = 0, hi = 63;
           if (!full) {
             const int k0 = inf.kbase + t * kBN + 64 * c;  // this half's first key
-            hi = min(63, inf.L - 1 - k0);
-            if (causal) hi = min(hi, i - k0);
-            if (window >= 0) {
-              lo = max(0, max(i - window, 0) - k0);  // (a grid may start below key 0)
-              hi = min(hi, i + window - k0);
+            if constexpr (kMode == 3) {
+              hi = min(63, inf.off + i - k0);  // causal at position off + i (below off + L)
+            } else {
+              hi = min(63, inf.L - 1 - k0);
+              if (causal) hi = min(hi, i - k0);
+              if (window >= 0) {
+                lo = max(0, max(i - window, 0) - k0);  // (a grid may start below key 0)
+                hi = min(hi, i + window - k0);
+              }
             }
             if (!row_ok) hi = -1;
             lo = min(lo, 64);
@@ -497,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float s4[4] = {0.f, 0.f, 0.f, 0.f};
   #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            if constexpr (kMode == 0) {
+            if constexpr (kMode == 0 || kMode == 3) {
               add_f16x2_f32x2(s4[0], s4[1], pw[e]);
               add_f16x2_f32x2(s4[2], s4[3], pw[e + 1]);
             } else {
@@ -560,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t wv[16];
 #pragma unroll
         for (int d = 0; d < 32; d += 2) wv[d >> 1] = pack_bf16x2(__uint_as_float(ov[d]) * inv, __uint_as_float(ov[d + 1]) * inv);
-        if constexpr (kMode >= 1) {
+        if constexpr (kMode == 1 || kMode == 2) {
           // Transposed among each group of four lanes (two butterfly steps),
           // so that lane 4g + j holds chunk j of rows 4g .. 4g + 3: each store
           // below then writes 64 contiguous bytes of eight rows rather than
@@ -619,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 template <int kMode>
-cudaError_t launch_rows(const CUtensorMap* rows_map, const Params& prm, cudaStream_t st) {
+cudaError_t launch_rows(const CUtensorMap* rows_map, const CUtensorMap* kv_map, const Params& prm, cudaStream_t st) {
   static int configured[64] = {};
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -647,7 +678,7 @@ cudaError_t launch_rows(const CUtensorMap* rows_map, const Params& prm, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_rows_kernel<kMode>, *rows_map, prm);
+  return cudaLaunchKernelEx(&cfg, prefill_rows_kernel<kMode>, *rows_map, *kv_map, prm);
 }
 }  // namespace
 
@@ -659,12 +690,29 @@ cudaError_t launch_prefill_rows(const CUtensorMap* rows_map, int heads, int kv_h
   prm.kv_heads = kv_heads;
   prm.window = window;
   prm.causal = causal;
+  prm.cap_pad = 0;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.hdr = static_cast<WsHeader*>(ws);
   prm.duos = ws_duos(ws, max_pairs);
   prm.dev_status = dev_status;
-  if (window >= 0 && window <= 128) return launch_rows<2>(rows_map, prm, st);
-  return short_seqs ? launch_rows<1>(rows_map, prm, st) : launch_rows<0>(rows_map, prm, st);
+  if (window >= 0 && window <= 128) return launch_rows<2>(rows_map, rows_map, prm, st);
+  return short_seqs ? launch_rows<1>(rows_map, rows_map, prm, st) : launch_rows<0>(rows_map, rows_map, prm, st);
+}
+
+cudaError_t launch_prefill_rows_chunk(const CUtensorMap* q_map, const CUtensorMap* kv_map, int heads, int kv_heads,
+                                      int cap_pad, void* out, void* ws, int max_pairs, int32_t* dev_status,
+                                      cudaStream_t st) {
+  Params prm;
+  prm.heads = heads;
+  prm.kv_heads = kv_heads;
+  prm.window = -1;
+  prm.causal = 1;
+  prm.cap_pad = cap_pad;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.hdr = static_cast<WsHeader*>(ws);
+  prm.duos = ws_duos(ws, max_pairs);
+  prm.dev_status = dev_status;
+  return launch_rows<3>(q_map, kv_map, prm, st);
 }
 
 }  // namespace kime

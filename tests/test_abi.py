@@ -79,6 +79,17 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     for n, T, H, Hkv in [(1, 1, 1, 1), (2, 20, 2, 2), (64, 20249, 12, 12), (16, 18272, 9, 3)]:
         assert kime.kime_attn_workspace_bytes(4, n, T, H, Hkv) == kime.kime_attn_workspace_bytes(0, n, T)
     assert kime.kime_attn_workspace_bytes(4, 4, 100, 6, 4) == 0
+    # op 5 (chunked prefill over prepared rows): op 2 at a 1 KB boundary, the
+    # chunk's query rows [total, 64 * heads] f16, a 1 KB boundary, then the
+    # widened cache rows [n * kv_heads * cap rounded up to 128, 128] f16
+    for n, T, H, Hkv, cap in [(1, 1, 1, 1, 1), (8, 1000, 9, 3, 1600), (32, 17600, 9, 3, 8192), (3, 5, 8, 1, 1000)]:
+        op2 = kime.kime_attn_workspace_bytes(2, n, T)
+        q_end = ((op2 + 1023) // 1024) * 1024 + T * 64 * H * 2
+        cap_pad = (cap + 127) // 128 * 128
+        want = ((q_end + 1023) // 1024) * 1024 + n * Hkv * cap_pad * 256
+        assert kime.kime_attn_workspace_bytes(5, n, T, H, Hkv, cap) == want
+    assert kime.kime_attn_workspace_bytes(5, 4, 100, 6, 4, 512) == 0  # heads not a multiple of kv_heads
+    assert kime.kime_attn_workspace_bytes(5, 4, 100, 6, 3, 0) == 0    # no cache rows
     assert kime.kime_attn_workspace_bytes(0, -1, 10) == 0
     assert kime.kime_attn_workspace_bytes(9, 4, 100) == 0
     assert kime.kime_attn_workspace_bytes(1, 128, 0, 9, 3, 8192) > 0

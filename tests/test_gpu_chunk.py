@@ -28,18 +28,24 @@ def poison_unused_rows(case):
         case.v_cache[s, :, end:].view(torch.int16).fill_(NAN_BF16)
 
 
-def gpu_chunk(case, mode="step", dev_status=None):
-    """mode: 'step' (kime_chunk_step), 'split' (append then attend)."""
+def gpu_chunk(case, mode="step", dev_status=None, ws_op=None):
+    """mode: 'step' (kime_chunk_step), 'split' (append then attend).  ws_op:
+    the workspace size (2: the kernel that converts its own tiles, 5: the one
+    over prepared rows); None: the binding's default."""
     dev = torch.device("cuda")
     c, s = gpu_tables(case.theta, case.cap)
     qkv, cu, pos = case.qkv.to(dev), case.cu_seqlens.to(dev), case.pos.to(dev)
     kc, vc = case.k_cache.to(dev, copy=True), case.v_cache.to(dev, copy=True)
     args = (qkv, cu, pos, max(case.max_seqlen, 1), case.heads, case.kv_heads, kc, vc, case.scale, c, s)
+    ws = None
+    if ws_op is not None:
+        nb = kime.kime_attn_workspace_bytes(ws_op, len(case.lengths), case.total, case.heads, case.kv_heads, case.cap)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=dev)
     if mode == "step":
-        out = kime.kime_chunk_step(*args, dev_status=dev_status)
+        out = kime.kime_chunk_step(*args, workspace=ws, dev_status=dev_status)
     else:
         kime.kime_kv_append_varlen(qkv, cu, pos, case.heads, case.kv_heads, kc, vc, c, s, dev_status=dev_status)
-        out = kime.kime_attn_chunk(*args, dev_status=dev_status)
+        out = kime.kime_attn_chunk(*args, workspace=ws, dev_status=dev_status)
     torch.cuda.synchronize()
     return out, kc, vc
 
@@ -108,6 +114,32 @@ def test_chunk_group_sizes(cuda_lib, heads, kv_heads):
     out, _, _ = gpu_chunk(case)
     ref, _, _ = oracle_chunk(case)
     check_bf16(out.float().cpu().numpy(), ref, f"chunk H{heads}/{kv_heads}")
+
+
+# (lengths, pos, cap, heads, kv_heads): tile edges in the chunk length and the
+# offset, a chunk ending at the last cache row of a cap that is not a whole
+# number of 128-key tiles (the widened rows are padded to whole tiles), one
+# ending on a tile boundary (no zero rows after it), single-token chunks,
+# position 0, GQA groups of 1, 3 and 8
+BOTH_PATHS = [
+    ([1, 5, 128, 129, 300, 0, 257, 64], [0, 200, 128, 126, 1000, 7, 383, 1536], 1600, 9, 3),
+    ([100, 1, 1, 256], [900, 0, 999, 128], 1000, 8, 1),
+    ([640, 3], [0, 637], 640, 4, 4),
+]
+
+
+@pytest.mark.parametrize("lengths,pos,cap,heads,kv_heads", BOTH_PATHS)
+@pytest.mark.parametrize("mode", ["split", "step"])
+def test_chunk_both_workspaces_match_the_oracle(cuda_lib, lengths, pos, cap, heads, kv_heads, mode):
+    case = chunk_case(lengths=lengths, pos=pos, cap=cap, heads=heads, kv_heads=kv_heads, seed=37)
+    poison_unused_rows(case)
+    ref, kb, vb = oracle_chunk(case)
+    for op in (2, 5):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out, kc, vc = gpu_chunk(case, mode, dev_status=st, ws_op=op)
+        assert int(st.item()) == 0, (op, int(st.item()))
+        assert np.array_equal(bf16_bits(kc), kb) and np.array_equal(bf16_bits(vc), vb)
+        check_bf16(out.float().cpu().numpy(), ref, f"chunk workspace op {op} ({mode})")
 
 
 def test_chunk_at_position_zero_matches_causal_prefill_oracle(cuda_lib):

@@ -75,13 +75,15 @@ def test_varlen_replays_from_a_cuda_graph(cuda_lib, op):
         assert torch.equal(out, want), seed
 
 
-def test_chunk_step_replays_from_a_cuda_graph(cuda_lib):
+@pytest.mark.parametrize("op", [2, 5])  # the kernel that converts its own tiles; the one over prepared rows
+def test_chunk_step_replays_from_a_cuda_graph(cuda_lib, op):
     dev = torch.device("cuda")
     case = chunk_case(n_seqs=6, cap=2048, lo=1, hi=300, seed=47)
     n, H, Hkv = len(case.lengths), case.heads, case.kv_heads
     c, s = gpu_tables(case.theta, case.cap)
     qkv, cu, pos = case.qkv.to(dev), case.cu_seqlens.to(dev), case.pos.to(dev)
-    ws = torch.empty(kime.kime_attn_workspace_bytes(2, n, case.total), dtype=torch.uint8, device=dev)
+    ws = torch.empty(kime.kime_attn_workspace_bytes(op, n, case.total, H, Hkv, case.cap), dtype=torch.uint8,
+                     device=dev)
     out = torch.empty((case.total, H * 64), dtype=torch.bfloat16, device=dev)
     step = lambda kc, vc, o: kime.kime_chunk_step(qkv, cu, pos, case.max_seqlen, H, Hkv, kc, vc, case.scale, c, s,
                                                  out=o, workspace=ws)
