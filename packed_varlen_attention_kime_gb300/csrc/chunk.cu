@@ -97,6 +97,10 @@ __global__ void __launch_bounds__(32 * kRowsPerCta)
 // rope_len)) are skipped (the scheduler reports them and lists none of their
 // tiles).  An operand beyond the f16 range saturates and sets KIME_DEV_RANGE.
 constexpr int kChunkPrepWarps = 4;
+// at most 64 registers a thread, so that eight CTAs (32 warps) share an SM:
+// at 104 registers (four CTAs) the widening waited on its loads most of the
+// time (SmolLM2 chunk step: 49 us, DRAM 45% busy)
+constexpr int kChunkPrepCtasPerSm = 8;
 
 __device__ __forceinline__ float absmax_bf16x8(const uint4& x) {
   return fmax3(fmax3(fabsf(bf16lo(x.x)), fabsf(bf16hi(x.x)), fabsf(bf16lo(x.y))),
@@ -109,7 +113,7 @@ __device__ __forceinline__ uint4 widen_bf16x8(const uint4& x) {
                     pack_f16x2(bf16lo(x.z), bf16hi(x.z)), pack_f16x2(bf16lo(x.w), bf16hi(x.w)));
 }
 
-__global__ void __launch_bounds__(32 * kChunkPrepWarps)
+__global__ void __launch_bounds__(32 * kChunkPrepWarps, kChunkPrepCtasPerSm)
     chunk_prep_kernel(const uint16_t* __restrict__ qkv, const int32_t* __restrict__ cu,
                       const int32_t* __restrict__ pos, int n_seqs, int total, int heads, int kv_heads, int cap,
                       int cap_pad, float qmul, const float* __restrict__ cos_t, const float* __restrict__ sin_t,
@@ -187,30 +191,33 @@ __global__ void __launch_bounds__(32 * kChunkPrepWarps)
       const int Lk = static_cast<int>(end);
       const size_t crow0 = static_cast<size_t>(sg) * cap;      // cache row of key 0
       const size_t wrow0 = static_cast<size_t>(sg) * cap_pad;  // widened row of key 0
-      // warp w takes keys key0 + 32 w .. + 31, four keys a round, eight lanes
-      // a key (16 bytes of K and of V each); every load before any store
+      // warp w takes keys key0 + 32 w .. + 31 in two rounds of 16, four keys
+      // a step, eight lanes a key (16 bytes of K and of V each); a round's
+      // loads all before any of its stores
       const int kr = lane >> 3, ch = lane & 7;
-      uint4 kx[8], vx[8];
+      for (int half = 0; half < 2; ++half) {
+        uint4 kx[4], vx[4];
 #pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int key = key0 + warp * 32 + it * 4 + kr;
-        kx[it] = vx[it] = make_uint4(0u, 0u, 0u, 0u);
-        if (key < Lk) {
-          kx[it] = __ldg(reinterpret_cast<const uint4*>(k_cache + (crow0 + key) * kHead) + ch);
-          vx[it] = __ldg(reinterpret_cast<const uint4*>(v_cache + (crow0 + key) * kHead) + ch);
+        for (int it = 0; it < 4; ++it) {
+          const int key = key0 + warp * 32 + half * 16 + it * 4 + kr;
+          kx[it] = vx[it] = make_uint4(0u, 0u, 0u, 0u);
+          if (key < Lk) {
+            kx[it] = __ldg(reinterpret_cast<const uint4*>(k_cache + (crow0 + key) * kHead) + ch);
+            vx[it] = __ldg(reinterpret_cast<const uint4*>(v_cache + (crow0 + key) * kHead) + ch);
+          }
         }
-      }
 #pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        const int key = key0 + warp * 32 + it * 4 + kr;
-        uint4* d = reinterpret_cast<uint4*>(kv16 + (wrow0 + key) * (2 * kHead));
-        if (key < Lk) {
-          big = fmax3(big, absmax_bf16x8(kx[it]), absmax_bf16x8(vx[it]));
-          d[ch] = widen_bf16x8(kx[it]);
-          d[8 + ch] = widen_bf16x8(vx[it]);
-        } else {
-          d[ch] = make_uint4(0u, 0u, 0u, 0u);
-          d[8 + ch] = make_uint4(0u, 0u, 0u, 0u);
+        for (int it = 0; it < 4; ++it) {
+          const int key = key0 + warp * 32 + half * 16 + it * 4 + kr;
+          uint4* d = reinterpret_cast<uint4*>(kv16 + (wrow0 + key) * (2 * kHead));
+          if (key < Lk) {
+            big = fmax3(big, absmax_bf16x8(kx[it]), absmax_bf16x8(vx[it]));
+            d[ch] = widen_bf16x8(kx[it]);
+            d[8 + ch] = widen_bf16x8(vx[it]);
+          } else {
+            d[ch] = make_uint4(0u, 0u, 0u, 0u);
+            d[8 + ch] = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
       }
     }
