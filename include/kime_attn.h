@@ -201,13 +201,21 @@ int kime_kv_append_varlen(const void* qkv, const int32_t* cu_seqlens, const int3
  *  max_seqlen   host upper bound on any chunk length (longer: KIME_DEV_SEQ_TOO_LONG)
  *  scale        softmax scale (> 0, finite)
  *  out          device bf16 [total_tokens, heads*64]
- *  workspace    device scratch of kime_attn_workspace_bytes(2, n_seqs,
- *               total_tokens, ...) bytes
- * BF16 inputs on the tensor cores, FP32 accumulation: the prefill kernel of
+ *  workspace    device scratch of at least kime_attn_workspace_bytes(2, n_seqs,
+ *               total_tokens, ...) bytes.  With kime_attn_workspace_bytes(5,
+ *               n_seqs, total_tokens, heads, kv_heads, cap) bytes the chunk's
+ *               queries are rotated and rounded to f16 once and cache rows
+ *               0..pos[s]+L-1 widened to f16 once, in the workspace, and the
+ *               attention runs over them (the faster path); with less, the
+ *               attention kernel converts its own tiles.  Either gives
+ *               results within the same bound.
+ * BF16 inputs on the tensor cores, FP32 accumulation: the prefill kernels of
  * kime_attn_varlen with K/V tiles taken from the cache.  A sequence whose
  * positions leave [0, min(cap, rope_len)) sets KIME_DEV_BAD_POS and its rows
- * of out are not written.  n_seqs*kv_heads*cap must stay below 2^31.  Two
- * launches (scheduler, attention). */
+ * of out are not written; an operand beyond the f16 range sets
+ * KIME_DEV_RANGE.  n_seqs*kv_heads*cap must stay below 2^31.  Launches:
+ * scheduler and attention, with the op-5 workspace also the preparation
+ * between them. */
 int kime_attn_chunk(const void* qkv, const int32_t* cu_seqlens, const int32_t* pos, int n_seqs, int total_tokens,
                     int max_seqlen, int heads, int kv_heads, int head_dim, int cap, float scale,
                     const float* rope_cos, const float* rope_sin, int rope_len, const void* k_cache,
@@ -215,7 +223,9 @@ int kime_attn_chunk(const void* qkv, const int32_t* cu_seqlens, const int32_t* p
                     void* stream);
 
 /* kime_chunk_step -- kime_kv_append_varlen then kime_attn_chunk on one stream
- * (three launches).  Arguments as kime_attn_chunk, with writable caches. */
+ * (three launches; with the op-5 workspace the preparation writes the
+ * chunk's rows to the caches itself, the same bits, and no append kernel
+ * runs).  Arguments as kime_attn_chunk, with writable caches. */
 int kime_chunk_step(const void* qkv, const int32_t* cu_seqlens, const int32_t* pos, int n_seqs, int total_tokens,
                     int max_seqlen, int heads, int kv_heads, int head_dim, int cap, float scale,
                     const float* rope_cos, const float* rope_sin, int rope_len, void* k_cache, void* v_cache,
@@ -226,8 +236,11 @@ int kime_chunk_step(const void* qkv, const int32_t* cu_seqlens, const int32_t* p
  * uses n_seqs, total_tokens) or op 3 (varlen with room for the prepared qkv
  * rows, about total_tokens * 128 * (heads + 2 * kv_heads) bytes more: uses
  * n_seqs, total_tokens, heads, kv_heads) or op 4 (varlen with KIME_F32_3XTF32:
- * the size of op 0; heads and kv_heads are checked).  Returns 0 for an unknown
- * op or malformed sizes. */
+ * the size of op 0; heads and kv_heads are checked) or op 5 (chunked prefill
+ * over prepared rows: op 2 plus the chunk's query rows, total_tokens * 128 *
+ * heads bytes, and the widened cache rows, n_seqs * kv_heads * (cap rounded
+ * up to a multiple of 128) * 256 bytes: uses all five sizes).  Returns 0 for
+ * an unknown op or malformed sizes. */
 size_t kime_attn_workspace_bytes(int op, int n_seqs, int total_tokens, int heads, int kv_heads, int cap);
 
 /* kime_qkv_proj -- the QKV projection of a packed batch, the step before

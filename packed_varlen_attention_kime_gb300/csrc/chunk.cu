@@ -93,7 +93,11 @@ __global__ void __launch_bounds__(32 * kRowsPerCta)
 // below pos[s] + L widened to f16 (K in columns 0..63, V in 64..127; cached
 // keys are rotated already), the rest of the tile zero, so the masked keys
 // the attention kernel visits are finite; tiles wholly past pos[s] + L are
-// never read and are skipped.  Sequences with positions outside [0, min(cap,
+// never read and are skipped.  With append set (the chunk step) the rows
+// pos[s] .. pos[s] + L - 1 are the chunk's own: taken from its qkv rows, the
+// key rotated as kv_append_varlen_kernel rotates it (rope_pair, then bf16),
+// written to the cache and widened from there, so the step needs no separate
+// append and its cache rows are the same bits.  Sequences with positions outside [0, min(cap,
 // rope_len)) are skipped (the scheduler reports them and lists none of their
 // tiles).  An operand beyond the f16 range saturates and sets KIME_DEV_RANGE.
 constexpr int kChunkPrepWarps = 4;
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(32 * kChunkPrepWarps, kChunkPrepCtasPerSm)
     chunk_prep_kernel(const uint16_t* __restrict__ qkv, const int32_t* __restrict__ cu,
                       const int32_t* __restrict__ pos, int n_seqs, int total, int heads, int kv_heads, int cap,
                       int cap_pad, float qmul, const float* __restrict__ cos_t, const float* __restrict__ sin_t,
-                      int rope_len, const uint16_t* __restrict__ k_cache, const uint16_t* __restrict__ v_cache,
+                      int rope_len, uint16_t* __restrict__ k_cache, uint16_t* __restrict__ v_cache, int append,
                       uint16_t* __restrict__ q16, uint16_t* __restrict__ kv16, int q_blocks, int32_t* dev_status) {
   // the attention kernel may launch once every CTA of this grid has started;
   // it waits for this grid's results before reading them
@@ -184,8 +188,8 @@ __global__ void __launch_bounds__(32 * kChunkPrepWarps, kChunkPrepCtasPerSm)
   } else {
     const int tiles = cap_pad / kBN;
     const int b = static_cast<int>(blockIdx.x) - q_blocks, sg = b / tiles, key0 = (b - sg * tiles) * kBN;
-    const int s = sg / kv_heads;
-    const int off = __ldg(pos + s), L = __ldg(cu + s + 1) - __ldg(cu + s);
+    const int s = sg / kv_heads, g = sg - s * kv_heads;
+    const int a0 = __ldg(cu + s), off = __ldg(pos + s), L = __ldg(cu + s + 1) - a0;
     const long long end = static_cast<long long>(off) + L;
     if (off >= 0 && L >= 0 && end <= cap && end <= rope_len && key0 < end) {
       const int Lk = static_cast<int>(end);
@@ -195,6 +199,7 @@ __global__ void __launch_bounds__(32 * kChunkPrepWarps, kChunkPrepCtasPerSm)
       // a step, eight lanes a key (16 bytes of K and of V each); a round's
       // loads all before any of its stores
       const int kr = lane >> 3, ch = lane & 7;
+      const size_t W = static_cast<size_t>(kHead) * (heads + 2 * kv_heads);
       for (int half = 0; half < 2; ++half) {
         uint4 kx[4], vx[4];
 #pragma unroll
@@ -202,17 +207,61 @@ __global__ void __launch_bounds__(32 * kChunkPrepWarps, kChunkPrepCtasPerSm)
           const int key = key0 + warp * 32 + half * 16 + it * 4 + kr;
           kx[it] = vx[it] = make_uint4(0u, 0u, 0u, 0u);
           if (key < Lk) {
-            kx[it] = __ldg(reinterpret_cast<const uint4*>(k_cache + (crow0 + key) * kHead) + ch);
-            vx[it] = __ldg(reinterpret_cast<const uint4*>(v_cache + (crow0 + key) * kHead) + ch);
+            if (append && key >= off) {  // the chunk's row key - off, as qkv holds it
+              const uint16_t* row = qkv + static_cast<size_t>(a0 + key - off) * W;
+              kx[it] = __ldg(reinterpret_cast<const uint4*>(row + (heads + g) * kHead) + ch);
+              vx[it] = __ldg(reinterpret_cast<const uint4*>(row + (heads + kv_heads + g) * kHead) + ch);
+            } else {
+              kx[it] = __ldg(reinterpret_cast<const uint4*>(k_cache + (crow0 + key) * kHead) + ch);
+              vx[it] = __ldg(reinterpret_cast<const uint4*>(v_cache + (crow0 + key) * kHead) + ch);
+            }
           }
         }
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
           const int key = key0 + warp * 32 + half * 16 + it * 4 + kr;
+          // the other halves of this lane's rotation pairs: lane ch ^ 4 of its key
+          uint4 ky;
+          ky.x = __shfl_xor_sync(0xffffffffu, kx[it].x, 4);
+          ky.y = __shfl_xor_sync(0xffffffffu, kx[it].y, 4);
+          ky.z = __shfl_xor_sync(0xffffffffu, kx[it].z, 4);
+          ky.w = __shfl_xor_sync(0xffffffffu, kx[it].w, 4);
           uint4* d = reinterpret_cast<uint4*>(kv16 + (wrow0 + key) * (2 * kHead));
           if (key < Lk) {
-            big = fmax3(big, absmax_bf16x8(kx[it]), absmax_bf16x8(vx[it]));
-            d[ch] = widen_bf16x8(kx[it]);
+            uint4 kb = kx[it];
+            if (append && key >= off) {
+              // k rotated at position key: pair (t, t + 32), t = 8 (ch mod 4) + e;
+              // lanes 0-3 of a key hold the t halves, lanes 4-7 the t + 32 halves
+              const int t0 = (ch & 3) * 8;
+              const float* crow = cos_t + static_cast<size_t>(key) * kHalf + t0;
+              const float* srow = sin_t + static_cast<size_t>(key) * kHalf + t0;
+              const uint32_t xw[4] = {kx[it].x, kx[it].y, kx[it].z, kx[it].w};
+              const uint32_t yw[4] = {ky.x, ky.y, ky.z, ky.w};
+              uint32_t ow[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float r[2];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                  const float x = h2 ? bf16hi(xw[e]) : bf16lo(xw[e]), y = h2 ? bf16hi(yw[e]) : bf16lo(yw[e]);
+                  const float c = __ldg(crow + 2 * e + h2), sn = __ldg(srow + 2 * e + h2);
+                  float ya, yb;
+                  if (ch < 4) {
+                    rope_pair(x, y, c, sn, ya, yb);
+                    r[h2] = ya;
+                  } else {
+                    rope_pair(y, x, c, sn, ya, yb);
+                    r[h2] = yb;
+                  }
+                }
+                ow[e] = pack_bf16x2(r[0], r[1]);
+              }
+              kb = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+              reinterpret_cast<uint4*>(k_cache + (crow0 + key) * kHead)[ch] = kb;
+              reinterpret_cast<uint4*>(v_cache + (crow0 + key) * kHead)[ch] = vx[it];
+            }
+            big = fmax3(big, absmax_bf16x8(kb), absmax_bf16x8(vx[it]));
+            d[ch] = widen_bf16x8(kb);
             d[8 + ch] = widen_bf16x8(vx[it]);
           } else {
             d[ch] = make_uint4(0u, 0u, 0u, 0u);
@@ -233,7 +282,7 @@ __global__ void __launch_bounds__(32 * kChunkPrepWarps, kChunkPrepCtasPerSm)
 
 cudaError_t launch_chunk_prep(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total, int heads,
                               int kv_heads, int cap, int cap_pad, float scale, const float* cos_t, const float* sin_t,
-                              int rope_len, const void* k_cache, const void* v_cache, void* q16, void* kv16,
+                              int rope_len, void* k_cache, void* v_cache, int append, void* q16, void* kv16,
                               int32_t* dev_status, cudaStream_t st) {
   const int q_blocks = (total + kChunkPrepWarps - 1) / kChunkPrepWarps;
   const long long kv_blocks = static_cast<long long>(n_seqs) * kv_heads * (cap_pad / kBN);
@@ -250,7 +299,7 @@ cudaError_t launch_chunk_prep(const void* qkv, const int32_t* cu, const int32_t*
   const float qmul = scale * 1.4426950408889634f;
   return cudaLaunchKernelEx(&cfg, chunk_prep_kernel, static_cast<const uint16_t*>(qkv), cu, pos, n_seqs, total,
                             heads, kv_heads, cap, cap_pad, qmul, cos_t, sin_t, rope_len,
-                            static_cast<const uint16_t*>(k_cache), static_cast<const uint16_t*>(v_cache),
+                            static_cast<uint16_t*>(k_cache), static_cast<uint16_t*>(v_cache), append,
                             static_cast<uint16_t*>(q16), static_cast<uint16_t*>(kv16), q_blocks, dev_status);
 }
 

@@ -123,11 +123,15 @@ cudaError_t launch_prefill_rows_chunk(const CUtensorMap* q_map, const CUtensorMa
 // rotated at positions pos[s] + i, times scale * log2(e), rounded once to f16
 // (q16 [total, heads*64]), and cache rows 0..pos[s] + L_s - 1 of every kv head
 // widened to f16 (kv16 as above), zero rows after them to the end of their
-// 128-row tile.  Launched with programmatic stream serialization after the
-// scheduler, whose lists it does not read; it ends after the scheduler has.
+// 128-row tile.  append: rows pos[s] .. pos[s] + L_s - 1 come from the chunk's
+// qkv rows and are written to the caches too (launch_kv_append_varlen's
+// rows, bit for bit), so the chunk step needs no separate append; else the
+// caches are only read.  Launched with programmatic stream serialization
+// after the scheduler, whose lists it does not read; it ends after the
+// scheduler has.
 cudaError_t launch_chunk_prep(const void* qkv, const int32_t* cu, const int32_t* pos, int n_seqs, int total, int heads,
                               int kv_heads, int cap, int cap_pad, float scale, const float* cos_t, const float* sin_t,
-                              int rope_len, const void* k_cache, const void* v_cache, void* q16, void* kv16,
+                              int rope_len, void* k_cache, void* v_cache, int append, void* q16, void* kv16,
                               int32_t* dev_status, cudaStream_t st);
 // The QKV projection qkv = x W^T (proj.cu): x_map over x [T, hidden] bf16
 // (boxes of 64 columns x 128 rows), w_map over W [64 (heads + 2 kv_heads),
