@@ -29,12 +29,12 @@ namespace {
 constexpr int kPrepWarps = 8;  // rows per CTA
 
 // kBatch: rounds of 16-byte chunks per lane loaded before any is used -- 4
-// for rows of at least 256 query and key chunks (ModernBERT-large: 0.1649 /
-// 0.9697 ms per local / global call against 0.169 / 0.9739 with 2; with 8,
-// 94 registers a thread, 0.1833 / 0.9882), 2 for rows of many query and key
-// heads (ModernBERT-base: 0.0829 / 0.0932 ms per local / global call against
-// 0.0850 / 0.0952 with 1), 1 for narrow rows, where the longer code costs more
-// than it saves (SmolLM2: 0.0666 against 0.0645 ms).
+// for rows of at least 128 query and key chunks (per local / global call,
+// ModernBERT-large 0.1649 / 0.9697 ms against 0.169 / 0.9739 with 2, and
+// 0.1833 / 0.9882 with 8 at 94 registers a thread; ModernBERT-base 0.0809 /
+// 0.0911 against 0.0829 / 0.0932 with 2 and 0.0850 / 0.0952 with 1), 1 for
+// narrower rows, where the longer code costs more than it saves (SmolLM2
+// prefill: 0.0645 ms against 0.0666 with 2).
 template <int kBatch>
 __global__ void __launch_bounds__(32 * kPrepWarps)
     qkv_prep_kernel(const uint16_t* __restrict__ qkv, const int32_t* __restrict__ cu, int n_seqs, int total,
@@ -174,11 +174,8 @@ cudaError_t launch_qkv_prep(const void* qkv, const int32_t* cu, int n_seqs, int 
   const float qmul = scale * 1.4426950408889634f;
   const uint16_t* src = static_cast<const uint16_t*>(qkv);
   uint16_t* dst = static_cast<uint16_t*>(out);
-  if ((heads + kv_heads) * (kHead / 8) >= 256)
-    return cudaLaunchKernelEx(&cfg, qkv_prep_kernel<4>, src, cu, n_seqs, total, heads, kv_heads, qmul, cos_t, sin_t,
-                              rope_len, dst, dev_status);
   if ((heads + kv_heads) * (kHead / 8) >= 128)  // chunks of a row's queries and keys
-    return cudaLaunchKernelEx(&cfg, qkv_prep_kernel<2>, src, cu, n_seqs, total, heads, kv_heads, qmul, cos_t, sin_t,
+    return cudaLaunchKernelEx(&cfg, qkv_prep_kernel<4>, src, cu, n_seqs, total, heads, kv_heads, qmul, cos_t, sin_t,
                               rope_len, dst, dev_status);
   return cudaLaunchKernelEx(&cfg, qkv_prep_kernel<1>, src, cu, n_seqs, total, heads, kv_heads, qmul, cos_t, sin_t,
                             rope_len, dst, dev_status);
