@@ -31,10 +31,11 @@ constexpr int kPrepWarps = 8;  // rows per CTA
 // kBatch: rounds of 16-byte chunks per lane loaded before any is used -- 4
 // for rows of at least 128 query and key chunks (per local / global call,
 // ModernBERT-large 0.1649 / 0.9697 ms against 0.169 / 0.9739 with 2, and
-// 0.1833 / 0.9882 with 8 at 94 registers a thread; ModernBERT-base 0.0809 /
-// 0.0911 against 0.0829 / 0.0932 with 2 and 0.0850 / 0.0952 with 1), 1 for
-// narrower rows, where the longer code costs more than it saves (SmolLM2
-// prefill: 0.0645 ms against 0.0666 with 2).
+// 0.1833 / 0.9882 with 8 at 94 registers a thread; ModernBERT-base, means of
+// 400 calls, 0.0824 / 0.0923 against 0.0834 / 0.0938 with 2, and 2 against 1
+// 0.0829 / 0.0932 against 0.0850 / 0.0952 in medians), 1 for narrower rows,
+// where the longer code costs more than it saves (SmolLM2 prefill: 0.0645 ms
+// against 0.0666 with 2 or 4).
 template <int kBatch>
 __global__ void __launch_bounds__(32 * kPrepWarps)
     qkv_prep_kernel(const uint16_t* __restrict__ qkv, const int32_t* __restrict__ cu, int n_seqs, int total,
