@@ -151,24 +151,34 @@ __global__ void __launch_bounds__(32 * kChunkPrepWarps, kChunkPrepCtasPerSm)
         const float* crow = cos_t + static_cast<size_t>(P) * kHalf;
         const float* srow = sin_t + static_cast<size_t>(P) * kHalf;
         const int nq = heads * (kHead / 8);  // 16-byte chunks of the row's queries (a multiple of 8)
-        for (int q0 = 0; q0 < nq; q0 += 32) {
-          const int q = q0 + lane;
+        // every chunk of a lane sits at the same place in its head (lane mod 8):
+        // its rotation pairs' table entries are the same in every round
+        const int a = lane & 7, t0 = (a & 3) * 8;
+        const float4 c0 = __ldg(reinterpret_cast<const float4*>(crow + t0));
+        const float4 c1 = __ldg(reinterpret_cast<const float4*>(crow + t0 + 4));
+        const float4 s0 = __ldg(reinterpret_cast<const float4*>(srow + t0));
+        const float4 s1 = __ldg(reinterpret_cast<const float4*>(srow + t0 + 4));
+        const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        for (int qb = 0; qb < nq; qb += 128) {
+          uint4 xs[4];  // four rounds' loads before any is used
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int q = qb + 32 * k + lane;
+            xs[k] = q < nq ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+          if (qb + 32 * k >= nq) break;  // (uniform over the warp)
+          const int q = qb + 32 * k + lane;
           const bool in = q < nq;  // chunks q and q ^ 4 are both in range or both out of it
-          const uint4 x = in ? __ldg(src + q) : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 x = xs[k];
           uint4 y;
           y.x = __shfl_xor_sync(0xffffffffu, x.x, 4);
           y.y = __shfl_xor_sync(0xffffffffu, x.y, 4);
           y.z = __shfl_xor_sync(0xffffffffu, x.z, 4);
           y.w = __shfl_xor_sync(0xffffffffu, x.w, 4);
           if (!in) continue;
-          const int a = q & 7;         // chunk within the head: 0..3 low half, 4..7 high half
-          const int t0 = (a & 3) * 8;  // pair index of the chunk's first element
-          const float4 c0 = __ldg(reinterpret_cast<const float4*>(crow + t0));
-          const float4 c1 = __ldg(reinterpret_cast<const float4*>(crow + t0 + 4));
-          const float4 s0 = __ldg(reinterpret_cast<const float4*>(srow + t0));
-          const float4 s1 = __ldg(reinterpret_cast<const float4*>(srow + t0 + 4));
-          const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
           const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
           uint32_t ow[4];
 #pragma unroll
@@ -186,6 +196,7 @@ __global__ void __launch_bounds__(32 * kChunkPrepWarps, kChunkPrepCtasPerSm)
             ow[e] = pack_f16x2(r0 * qmul, r1 * qmul);
           }
           dst[q] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+          }
         }
       }
     }
