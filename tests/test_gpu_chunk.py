@@ -142,6 +142,34 @@ def test_chunk_both_workspaces_match_the_oracle(cuda_lib, lengths, pos, cap, hea
         check_bf16(out.float().cpu().numpy(), ref, f"chunk workspace op {op} ({mode})")
 
 
+@pytest.mark.parametrize("ws_op,mode", [(2, "split"), (2, "step"), (5, "split"), (5, "step")])
+def test_chunk_f16_range_flag(cuda_lib, ws_op, mode):
+    # Both chunk paths round cached keys and values (the chunk's own rows
+    # included, once appended) and the scaled rotated queries to f16 for the
+    # tensor cores; beyond 65504 they saturate and KIME_DEV_RANGE is set.
+    # Ordinary inputs leave it clear.
+    case = chunk_case(lengths=[150, 40], pos=[300, 0], cap=512, seed=38)
+    H, Hkv = case.heads, case.kv_heads
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, _, _ = gpu_chunk(case, mode, dev_status=st, ws_op=ws_op)
+    assert int(st.item()) == 0 and torch.isfinite(out.float()).all()
+    for what in ("cached k", "cached v", "appended v", "q"):
+        c2 = dataclasses.replace(case, qkv=case.qkv.clone(), k_cache=case.k_cache.clone(),
+                                 v_cache=case.v_cache.clone())
+        if what == "cached k":
+            c2.k_cache[0, 1, 100, 5] = 1e5     # key 100 of sequence 0, below its pos
+        elif what == "cached v":
+            c2.v_cache[0, 0, 299, 7] = -1e5    # the last cached row before the chunk
+        elif what == "appended v":
+            c2.qkv[10, (H + Hkv) * 64 + 3] = 1e5   # chunk row 10 of sequence 0, value head 0
+        else:
+            c2.qkv[20, 3] = 5e5                # a query: 5e5 * 0.125 * log2(e) > 65504
+        st.zero_()
+        out, _, _ = gpu_chunk(c2, mode, dev_status=st, ws_op=ws_op)
+        assert int(st.item()) == kime.DEV_RANGE, what
+        assert torch.isfinite(out.float()).all(), what
+
+
 def test_chunk_at_position_zero_matches_causal_prefill_oracle(cuda_lib):
     # pos = 0 everywhere: the chunk is a causal prefill whose keys went through
     # the cache (rounded to bf16 after rotation); against the chunk oracle it is
