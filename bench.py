@@ -283,9 +283,11 @@ class DecodeRun:
 
 class ChunkRun:
     """Chunked prefill against the KV cache (SmolLM2 shapes): append the chunks
-    and attend, one kime_chunk_step per step (the same positions every step)."""
+    and attend, one kime_chunk_step per step (the same positions every step),
+    with the workspace of op 5 (prepared rows, the binding's default) or of
+    op 2 (the minimum: the kernel that converts its own tiles)."""
 
-    def __init__(self, dev):
+    def __init__(self, dev, ws_op=5):
         import packed_varlen_attention_kime_gb300 as kime
         from packed_varlen_attention_kime_gb300.inputs import chunk_case
         self.kime = kime
@@ -295,8 +297,8 @@ class ChunkRun:
         cs, sn = kime.kime_rope_tables(c.theta, c.cap)
         self.cs, self.sn = cs.to(dev), sn.to(dev)
         self.out = torch.empty((c.total, c.heads * 64), dtype=torch.bfloat16, device=dev)
-        self.ws = torch.empty(kime.kime_attn_workspace_bytes(5, len(c.lengths), c.total, c.heads, c.kv_heads, c.cap),
-                              dtype=torch.uint8, device=dev)
+        self.ws = torch.empty(kime.kime_attn_workspace_bytes(ws_op, len(c.lengths), c.total, c.heads, c.kv_heads,
+                                                             c.cap), dtype=torch.uint8, device=dev)
         L = np.array(c.lengths, np.int64)
         P = c.pos.numpy().astype(np.int64)
         keys = int((P + L).sum())                       # cache rows each kv head's prefix spans
@@ -629,7 +631,8 @@ def main():
     ap.add_argument("--only", default=None,
                     help="profiling aid: run only WORKLOAD[:LAYER] (modernbert_base, modernbert_large, "
                          "smollm2_proj[:fused|unfused|proj], "
-                         "smollm2_prefill, smollm2_decode, smollm2_chunk) for --steps steps and print its timings")
+                         "smollm2_prefill, smollm2_decode, smollm2_chunk[:minimal]) for --steps steps and print its "
+                         "timings (smollm2_chunk:minimal: the chunk step with the minimal workspace)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -760,7 +763,7 @@ def only_arm(args, local):
     flush = l2_flush_buffer(dev)
     name, _, layer = args.only.partition(":")
     if name in ("smollm2_decode", "smollm2_chunk"):
-        d = DecodeRun(dev) if name == "smollm2_decode" else ChunkRun(dev)
+        d = DecodeRun(dev) if name == "smollm2_decode" else ChunkRun(dev, 2 if layer == "minimal" else 5)
         per, _ = time_fn(lambda ev: d.step(), args.steps, args.warmup, flush, stream)
         check_status(dev)
         print(json.dumps({"only": name, "ms": [round(x, 4) for x in per]}))
