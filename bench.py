@@ -766,7 +766,7 @@ def only_arm(args, local):
         d = DecodeRun(dev) if name == "smollm2_decode" else ChunkRun(dev, 2 if layer == "minimal" else 5)
         per, _ = time_fn(lambda ev: d.step(), args.steps, args.warmup, flush, stream)
         check_status(dev)
-        print(json.dumps({"only": name, "ms": [round(x, 4) for x in per]}))
+        print(json.dumps({"only": args.only, "ms": [round(x, 4) for x in per]}))
         return
     if name == "smollm2_proj":  # fused (default), unfused, or the projection alone
         pr = ProjRun(dev)
