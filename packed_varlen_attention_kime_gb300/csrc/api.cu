@@ -267,7 +267,7 @@ int kime_qkv_proj(const void* x, const void* w, int total_tokens, int hidden, in
   CUtensorMap xm, wm;
   int rc;
   if ((rc = encode_bf16_map(&xm, x, total_tokens, hidden, kime::kBM))) return rc;
-  if ((rc = encode_bf16_map(&wm, w, W, hidden, 192))) return rc;
+  if ((rc = encode_bf16_map(&wm, w, W, hidden, 256))) return rc;
   return cuda_status(kime::launch_qkv_proj(&xm, &wm, total_tokens, hidden, heads, kv_heads, nullptr, 0, 1.f,
                                            nullptr, nullptr, 0, qkv, 1, dev_status,
                                            static_cast<cudaStream_t>(stream)));
@@ -297,7 +297,7 @@ int kime_attn_varlen_proj(const void* x, const void* w, const int32_t* cu_seqlen
   CUtensorMap xm, wm, pmap;
   int rc;
   if ((rc = encode_bf16_map(&xm, x, total_tokens, hidden, kime::kBM))) return rc;
-  if ((rc = encode_bf16_map(&wm, w, W, hidden, 192))) return rc;
+  if ((rc = encode_bf16_map(&wm, w, W, hidden, 256))) return rc;
   if ((rc = encode_qkv_map(&pmap, rows, total_tokens, static_cast<int>(W)))) return rc;
   // scheduler, then the projection writing the prepared rows beside it, then
   // the attention kernel over them

@@ -135,7 +135,7 @@ cudaError_t launch_chunk_prep(const void* qkv, const int32_t* cu, const int32_t*
                               int32_t* dev_status, cudaStream_t st);
 // The QKV projection qkv = x W^T (proj.cu): x_map over x [T, hidden] bf16
 // (boxes of 64 columns x 128 rows), w_map over W [64 (heads + 2 kv_heads),
-// hidden] bf16 (boxes of 64 columns x 192 rows), both with 128-byte swizzle;
+// hidden] bf16 (boxes of 64 columns x 256 rows), both with 128-byte swizzle;
 // hidden a multiple of 64.  mode 0 writes the prepared rows (as
 // launch_qkv_prep does from bf16 qkv: RoPE at the positions cu gives, q times
 // scale * log2(e), f16), mode 1 the bf16 qkv rows (cu, tables unused).

@@ -21,12 +21,14 @@
 //     saturates and sets ST_RANGE.
 //   bf16 qkv: the accumulators rounded to bf16, no RoPE (the projection alone).
 //
-// CTA = 192 threads, persistent over output tiles of 128 token rows x 3 heads
-// (the last column tile of a row may hold fewer heads):
+// CTA = 192 threads, persistent over output tiles of 128 token rows x 4 heads
+// (the last column tile of a row may hold fewer heads; 4 heads a tile rather
+// than 3 load 10% fewer operand bytes per product: the SmolLM2 projection
+// 0.0273 against 0.0287 ms):
 //   warps 0..3  epilogue: thread r owns row r of the tile (TMEM lane r)
-//   warp 4      TMA producer: x and W slabs of 64 hidden columns, 5 stages
+//   warp 4      TMA producer: x and W slabs of 64 hidden columns, 4 stages
 //   warp 5      MMA issuer (one thread)
-// TMEM holds two accumulators of 192 columns, so the epilogue of one tile
+// TMEM holds two accumulators of 256 columns, so the epilogue of one tile
 // runs while the MMAs of the next accumulate.  Every wait is bounded in time.
 #include "kime_common.cuh"
 
@@ -35,10 +37,10 @@ namespace kime {
 namespace {
 
 constexpr int kPThreads = 192;
-constexpr int kPStages = 5;
-constexpr int kNH = 3;                          // heads per column tile
+constexpr int kPStages = 4;
+constexpr int kNH = 4;                          // heads per column tile
 constexpr uint32_t kATile = kBM * 64 * 2;       // 16 KB: 128 token rows x 64 hidden (bf16)
-constexpr uint32_t kBTile = kNH * 64 * 64 * 2;  // 24 KB: 192 weight rows x 64 hidden
+constexpr uint32_t kBTile = kNH * 64 * 64 * 2;  // 32 KB: 256 weight rows x 64 hidden
 constexpr uint32_t kStageBytes = kATile + kBTile;
 constexpr uint32_t kPBar = kPStages * kStageBytes;
 constexpr int kCuSmem = 4096;                     // cu_seqlens entries kept in shared memory
@@ -46,7 +48,7 @@ constexpr uint32_t kPCu = kPBar + 256;
 constexpr uint32_t kPSmem = kPCu + kCuSmem * 4 + 1024;  // + barriers, cu_seqlens, alignment slack
 static_assert(kPSmem <= 232448, "shared memory per CTA");
 constexpr uint32_t kAccCols = kNH * 64;          // one accumulator
-constexpr uint32_t kPTmemCols = 512;             // two accumulators (384) rounded to a power of two
+constexpr uint32_t kPTmemCols = 512;             // two accumulators
 
 struct PShared {
   uint64_t full[kPStages], empty[kPStages];
